@@ -1,0 +1,222 @@
+"""CPU oracle for the MoE token path -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The CUDA library (``combine_moe_route_06_gb300``)
+never imports it and shares no code with it.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, double precision, loops in
+the order the pages state the definitions); this module only compiles it with
+gcc and marshals numpy arrays through ctypes.  Status words use bit 1 for an
+inconsistent index input, bit 2 for capacity overflow and bit 3 for an expert
+id >= E.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BIT_INCONSISTENT = 1 << 1
+BIT_CAPACITY = 1 << 2
+BIT_BAD_ID = 1 << 3
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into a shared library (gcc -O2); returns its path."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+                       check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64 = ctypes.c_int32, ctypes.c_int64
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+            lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+            lib.oracle_expected_copies.argtypes = [i32, i32, i32]
+            lib.oracle_expected_copies.restype = ctypes.c_double
+            lib.oracle_route_topk.argtypes = [P, i64, i32, i32, P, P]
+            lib.oracle_dispatch_layout.argtypes = [P, i32, i64, i32, i32, i32, P, P, P, P, P]
+            lib.oracle_dispatch_pack.argtypes = [P, i32, i64, i32, i32, P, i64, P, P, P]
+            lib.oracle_permute_to_experts.argtypes = [P, P, P, i32, i64, i32, i32, i32, i32,
+                                                      i32, i32, i64, i64, P, P, P, P, P]
+            lib.oracle_expert_scale.argtypes = [P, P, P, i32, i32, i64, P]
+            lib.oracle_combine.argtypes = [P, P, P, i32, i64, i32, i32, P]
+            for f in ("oracle_route_topk", "oracle_dispatch_layout", "oracle_dispatch_pack",
+                      "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise ValueError(f"{name}: invalid arguments (rc={rc})")
+
+
+def bf16_to_double(b: int) -> float:
+    return _load().oracle_bf16_to_double(int(b))
+
+
+def bf16_from_double(v: float) -> int:
+    return int(_load().oracle_bf16_from_double(float(v)))
+
+
+def expected_copies(E: int, G: int, k: int) -> float:
+    """Mean number of destination GPUs per token under uniform top-k routing."""
+    return _load().oracle_expected_copies(E, G, k)
+
+
+def route_topk(logits: np.ndarray, k: int):
+    """logits float32 [..., E] -> (ids int32 [..., k], w float64 [..., k])."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    E = logits.shape[-1]
+    lead = logits.shape[:-1]
+    N = int(np.prod(lead)) if lead else 1
+    ids = np.empty(lead + (k,), dtype=np.int32)
+    w = np.empty(lead + (k,), dtype=np.float64)
+    _check(_load().oracle_route_topk(_p(logits), N, E, k, _p(ids), _p(w)), "route_topk")
+    return ids, w
+
+
+def dispatch_layout(ids: np.ndarray, E: int, P: int) -> dict:
+    """ids int32 [S, T, k] -> expert_counts, part_counts, part_offsets, token_slot, status."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    S, T, k = ids.shape
+    out = {
+        "expert_counts": np.empty((S, E), np.int32),
+        "part_counts": np.empty((S, P), np.int32),
+        "part_offsets": np.empty((S, P + 1), np.int32),
+        "token_slot": np.empty((S, T, P), np.int32),
+    }
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_dispatch_layout(_p(ids), S, T, k, E, P, _p(out["expert_counts"]),
+                                          _p(out["part_counts"]), _p(out["part_offsets"]),
+                                          _p(out["token_slot"]), _p(st)), "dispatch_layout")
+    out["status"] = int(st[0])
+    return out
+
+
+def dispatch_pack(x: np.ndarray, token_slot: np.ndarray, cap_send: int, send: np.ndarray | None = None):
+    """x uint16 [S, T, H] (bf16 bits), token_slot [S, T, P] -> (send [S, cap, H], send_src [S, cap], status).
+
+    Rows of `send` that no slot writes keep the contents of the `send` passed
+    in (zeros if none is given).
+    """
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    S, T, H = x.shape
+    P = token_slot.shape[2]
+    if send is None:
+        send = np.zeros((S, cap_send, H), np.uint16)
+    send_src = np.empty((S, cap_send), np.int32)
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_dispatch_pack(_p(x), S, T, H, P, _p(token_slot), cap_send, _p(send),
+                                        _p(send_src), _p(st)), "dispatch_pack")
+    return send, send_src, int(st[0])
+
+
+def permute_to_experts(send: np.ndarray, token_slot: np.ndarray, ids: np.ndarray, E: int,
+                       recv_part: int = -1, align: int = 1, cap_recv: int | None = None,
+                       recv: np.ndarray | None = None) -> dict:
+    """Receiver permute; returns recv, expert_offsets, pair_row, recv_pair, status.
+
+    Rows of `recv` at or beyond min(expert_offsets[E], cap_recv) keep the
+    contents of the `recv` passed in (zeros if none is given).
+    """
+    send = np.ascontiguousarray(send, dtype=np.uint16)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    S, cap_send, H = send.shape
+    _, T, P = token_slot.shape
+    k = ids.shape[2]
+    if cap_recv is None:
+        cap_recv = S * T * k + E * (align - 1)
+    if recv is None:
+        recv = np.zeros((cap_recv, H), np.uint16)
+    out = {
+        "recv": recv,
+        "expert_offsets": np.empty(E + 1, np.int32),
+        "pair_row": np.empty((S, T, k), np.int32),
+        "recv_pair": np.empty(cap_recv, np.int32),
+    }
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_permute_to_experts(
+        _p(send), _p(token_slot), _p(ids), S, T, k, E, P, H, recv_part, align, cap_send,
+        cap_recv, _p(recv), _p(out["expert_offsets"]), _p(out["pair_row"]),
+        _p(out["recv_pair"]), _p(st)), "permute_to_experts")
+    out["status"] = int(st[0])
+    return out
+
+
+def expert_scale(recv: np.ndarray, expert_offsets: np.ndarray, scale: np.ndarray,
+                 y: np.ndarray | None = None) -> np.ndarray:
+    """Stand-in expert: y[row] = bf16(recv[row] * scale[expert of row])."""
+    recv = np.ascontiguousarray(recv, dtype=np.uint16)
+    expert_offsets = np.ascontiguousarray(expert_offsets, dtype=np.int32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    cap, H = recv.shape
+    E = scale.shape[0]
+    if y is None:
+        y = np.zeros_like(recv)
+    _check(_load().oracle_expert_scale(_p(recv), _p(expert_offsets), _p(scale), E, H, cap, _p(y)),
+           "expert_scale")
+    return y
+
+
+def combine(y: np.ndarray, pair_row: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """out[s, t] = bf16(sum_j w[s,t,j] * y[pair_row[s,t,j]]) with a double sum; uint16 [S, T, H]."""
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    pair_row = np.ascontiguousarray(pair_row, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    S, T, k = pair_row.shape
+    H = y.shape[1]
+    out = np.empty((S, T, H), np.uint16)
+    _check(_load().oracle_combine(_p(y), _p(pair_row), _p(w), S, T, k, H, _p(out)), "combine")
+    return out
+
+
+def run_path(x: np.ndarray, logits: np.ndarray, E: int, k: int, P: int, scales: np.ndarray | None,
+             recv_part: int = -1, align: int = 1) -> dict:
+    """The whole path: route -> layout -> pack -> permute -> stand-in expert -> combine.
+
+    `scales` None means the identity expert (combine reads the permuted rows).
+    """
+    S, T, H = x.shape
+    ids, w64 = route_topk(logits, k)
+    w = w64.astype(np.float32)
+    lay = dispatch_layout(ids, E, P)
+    cap_send = T * min(k, P)
+    send, send_src, st_pack = dispatch_pack(x, lay["token_slot"], cap_send)
+    per = permute_to_experts(send, lay["token_slot"], ids, E, recv_part=recv_part, align=align)
+    y = per["recv"] if scales is None else expert_scale(per["recv"], per["expert_offsets"], scales)
+    out = combine(y, per["pair_row"], w)
+    return {"ids": ids, "w": w64, "layout": lay, "send": send, "send_src": send_src,
+            "permute": per, "y": y, "out": out,
+            "status": lay["status"] | st_pack | per["status"]}

@@ -1,0 +1,423 @@
+/*
+ * moe_oracle.c -- CPU oracle for the MoE token path (route, dispatch layout,
+ * pack, receiver permute, stand-in expert, weighted combine).
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use this file.  The CUDA library never includes, links or
+ * calls it, and it shares no code with the CUDA library: every definition
+ * below is written out again from the pages.
+ *
+ * Style: plain single-threaded loops in the order the definitions are stated,
+ * double precision for every floating-point sum, no blocking and no fusion.
+ *
+ * Sources (cited by page and section):
+ *   [a2a]  "a2a-backends", vincentzed.com/writing/a2a-backends
+ *   [b1g]  "Beyond One GPU: Tensor, Pipeline and Expert Parallelism, and Split
+ *          Prefill and Decode", ishwarj.com/writings/llm-inference-7-beyond-one-gpu
+ *
+ * Parity pins: every function here is checked by the CPU test suite against
+ * values the pages print, closed forms, invariants or brute force (see the
+ * tests named after each function).  No function is unpinned.
+ *
+ * Layout conventions (shared with the C-ABI only through its documentation):
+ *   S sources, T tokens per source, k experts per token, E experts, P
+ *   partitions of L = E/P contiguous experts, H bf16 elements per row.
+ *   ids/weights: [S][T][k]; token_slot: [S][T][P]; send: [S][cap_send][H].
+ *   Status bits: bit 1 = inconsistent index input, bit 2 = capacity
+ *   overflow, bit 3 = expert id >= E.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BIT_INCONSISTENT (1u << 1)
+#define ORC_BIT_CAPACITY     (1u << 2)
+#define ORC_BIT_BAD_ID       (1u << 3)
+
+/* ---------------------------------------------------------------- bf16 -- */
+
+/* A bfloat16 bit pattern is the upper half of the float32 with the same value. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round a double to bfloat16, to nearest with ties to even, in ONE rounding
+ * (no detour through float32, which would round twice).
+ * bfloat16 keeps 8 significant bits and float32's exponent range: a normal
+ * value in [2^(e-1), 2^e) has quantum 2^(e-8); below 2^-126 the quantum is
+ * fixed at 2^-133.  Values that round to 2^128 or beyond become infinity.
+ */
+uint16_t oracle_bf16_from_double(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return 0x7FC0u;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80u;
+    int ex;
+    frexp(a, &ex);               /* a in [2^(ex-1), 2^ex) */
+    int qe = ex - 8;
+    if (qe < -133)
+        qe = -133;
+    double q = ldexp(1.0, qe);
+    double r = nearbyint(a / q) * q; /* a/q is exact; default mode: ties to even */
+    if (r >= ldexp(1.0, 128))
+        return sign | 0x7F80u;
+    float f = (float)r;          /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------- closed form, [a2a] 1.3 */
+
+/* Binomial coefficient C(n, r) as a double (multiplicative formula). */
+static double binom(int n, int r)
+{
+    if (r < 0 || r > n)
+        return 0.0;
+    double c = 1.0;
+    for (int i = 1; i <= r; i++)
+        c = c * (double)(n - r + i) / (double)i;
+    return c;
+}
+
+/*
+ * [a2a] 1.3: a GPU holding E/G of E experts misses all k picks of a uniform
+ * router with probability C(E - E/G, k) / C(E, k); a token therefore needs
+ * G * (1 - C(E - E/G, k) / C(E, k)) GPUs on average.
+ */
+double oracle_expected_copies(int E, int G, int k)
+{
+    return (double)G * (1.0 - binom(E - E / G, k) / binom(E, k));
+}
+
+/* ------------------------------------------------------- route, [a2a] 1.1 */
+
+typedef struct {
+    float v;
+    int32_t id;
+} orc_cand;
+
+/* Larger logit first; equal logits: lower expert id first. */
+static int cand_cmp(const void *pa, const void *pb)
+{
+    const orc_cand *a = (const orc_cand *)pa, *b = (const orc_cand *)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->id > b->id) - (a->id < b->id);
+}
+
+/*
+ * [a2a] 1.1: the router gives every token the ids of its chosen experts and
+ * one weight per expert.  Chosen experts: the k largest logits, by sorting
+ * the whole row (descending, ties to the lower id).  Weights: softmax over
+ * the k chosen logits, w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max), in
+ * double.  logits [N][E] -> ids [N][k], w [N][k]; N = S*T rows.
+ */
+int oracle_route_topk(const float *logits, int64_t N, int E, int k,
+                      int32_t *ids, double *w)
+{
+    if (k < 1 || k > E)
+        return -1;
+    orc_cand *c = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)E);
+    if (!c)
+        return -2;
+    for (int64_t n = 0; n < N; n++) {
+        const float *row = logits + n * (int64_t)E;
+        for (int e = 0; e < E; e++) {
+            c[e].v = row[e];
+            c[e].id = e;
+        }
+        qsort(c, (size_t)E, sizeof(orc_cand), cand_cmp);
+        double lmax = (double)c[0].v, denom = 0.0;
+        for (int j = 0; j < k; j++)
+            denom += exp((double)c[j].v - lmax);
+        for (int j = 0; j < k; j++) {
+            ids[n * k + j] = c[j].id;
+            w[n * k + j] = exp((double)c[j].v - lmax) / denom;
+        }
+    }
+    free(c);
+    return 0;
+}
+
+/* ---------------------------------------------- dispatch layout, [a2a] 1.3 */
+
+/*
+ * Expert e lives on partition e / L with L = E / P: contiguous blocks of
+ * experts per GPU, [a2a] 2.1 (local ids first_local .. first_local+num_local)
+ * and the 48-of-384 split of [a2a] 1.1.
+ *
+ * A token is copied once to every partition holding at least one of its
+ * experts ([a2a] 1.1 Figure 1, 1.3 third answer, 3.2 first step).  Ids < 0
+ * are "not routed" and skipped; ids >= E are skipped and flagged.
+ *
+ *   expert_counts[s][e]  = #{(t, j) : ids[s][t][j] == e}
+ *   part_counts[s][p]    = #{t : token t hits partition p}
+ *   part_offsets[s][0]   = 0, part_offsets[s][p+1] = part_offsets[s][p] + part_counts[s][p]
+ *   token_slot[s][t][p]  = part_offsets[s][p] + #{t' < t : t' hits p}, or -1
+ *
+ * Rows of one partition's region are in ascending token order.
+ */
+int oracle_dispatch_layout(const int32_t *ids, int S, int64_t T, int k, int E, int P,
+                           int32_t *expert_counts, int32_t *part_counts,
+                           int32_t *part_offsets, int32_t *token_slot,
+                           uint32_t *status)
+{
+    if (P < 1 || E % P != 0)
+        return -1;
+    const int L = E / P;
+    char *hit = (char *)malloc((size_t)P);
+    if (!hit)
+        return -2;
+    for (int s = 0; s < S; s++) {
+        for (int e = 0; e < E; e++)
+            expert_counts[s * E + e] = 0;
+        for (int p = 0; p < P; p++)
+            part_counts[s * P + p] = 0;
+        /* pass 1: counts */
+        for (int64_t t = 0; t < T; t++) {
+            memset(hit, 0, (size_t)P);
+            for (int j = 0; j < k; j++) {
+                int32_t e = ids[((int64_t)s * T + t) * k + j];
+                if (e < 0)
+                    continue;
+                if (e >= E) {
+                    *status |= ORC_BIT_BAD_ID;
+                    continue;
+                }
+                expert_counts[s * E + e] += 1;
+                hit[e / L] = 1;
+            }
+            for (int p = 0; p < P; p++)
+                part_counts[s * P + p] += hit[p];
+        }
+        part_offsets[s * (P + 1) + 0] = 0;
+        for (int p = 0; p < P; p++)
+            part_offsets[s * (P + 1) + p + 1] = part_offsets[s * (P + 1) + p] + part_counts[s * P + p];
+        /* pass 2: slots, ascending token order within each partition */
+        for (int p = 0; p < P; p++) {
+            int32_t next = part_offsets[s * (P + 1) + p];
+            for (int64_t t = 0; t < T; t++) {
+                int h = 0;
+                for (int j = 0; j < k; j++) {
+                    int32_t e = ids[((int64_t)s * T + t) * k + j];
+                    if (e >= 0 && e < E && e / L == p)
+                        h = 1;
+                }
+                token_slot[((int64_t)s * T + t) * P + p] = h ? next++ : -1;
+            }
+        }
+    }
+    free(hit);
+    return 0;
+}
+
+/* ------------------------------------------------- pack, [a2a] 3.2, 5.1 */
+
+/*
+ * Sender side of dispatch: each (token, partition) with a slot gets a bit copy
+ * of the token's row in that partition's region of the send buffer
+ * ([a2a] 3.2 fourth step, 5.1 "a region for every sender", 6.1 one copy per
+ * GPU that needs the token).  send_src[s][slot] = t is the source token of
+ * the row; unused entries of send_src are -1.  A slot >= cap_send has no room
+ * ([a2a] 4.1, 9.2 the cap): it is dropped and flagged.
+ */
+int oracle_dispatch_pack(const uint16_t *x, int S, int64_t T, int H, int P,
+                         const int32_t *token_slot, int64_t cap_send,
+                         uint16_t *send, int32_t *send_src, uint32_t *status)
+{
+    for (int s = 0; s < S; s++) {
+        for (int64_t r = 0; r < cap_send; r++)
+            send_src[(int64_t)s * cap_send + r] = -1;
+        for (int64_t t = 0; t < T; t++) {
+            for (int p = 0; p < P; p++) {
+                int32_t slot = token_slot[((int64_t)s * T + t) * P + p];
+                if (slot < 0)
+                    continue;
+                if (slot >= cap_send) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue;
+                }
+                memcpy(send + ((int64_t)s * cap_send + slot) * H,
+                       x + ((int64_t)s * T + t) * H, sizeof(uint16_t) * (size_t)H);
+                send_src[(int64_t)s * cap_send + slot] = (int32_t)t;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------ receiver permute, [a2a] 1.5, 3.3, 5.1 */
+
+/*
+ * Receiver side: one row per (token, local expert), grouped by expert in
+ * runs ([a2a] 1.5 contiguous layout; 3.3 "5 rows become 7"; 5.1 the copy
+ * epilogue with do_expand and device-side offsets).
+ *
+ * The receiving set R is one partition (recv_part >= 0) or all of them (-1).
+ * For each expert e in ascending order, cnt_e counts the pairs (s, t, j) with
+ * ids[s][t][j] == e and part(e) in R; runs are padded to a multiple of
+ * `align` rows ([a2a] 1.5: DeepGEMM pads each run to a multiple of 128):
+ *   expert_offsets[0] = 0
+ *   expert_offsets[e+1] = expert_offsets[e] + (part(e) in R ? ceil(cnt_e/align)*align : 0)
+ * Within a run, pairs are in ascending (s, t, j) order (a stable sort of the
+ * pairs by expert id).  The pair's row is a copy of its token's row in the
+ * send region of partition part(e): send[s][token_slot[s][t][part(e)]].
+ *
+ *   pair_row[s][t][j] = row of the pair, or -1 (not in R, id < 0, or row >= cap_recv)
+ *   recv_pair[row]    = (s*T + t)*k + j for pair rows, -1 for padding rows and
+ *                       for rows >= expert_offsets[E]
+ *   recv[row]         = the copy; padding rows are zero
+ *
+ * Flags: row >= cap_recv (dropped) or source slot >= cap_send -> capacity;
+ * source slot < 0 for a routed pair -> inconsistent input (row is zeroed);
+ * id >= E -> bad id (skipped).
+ */
+int oracle_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
+                              const int32_t *ids, int S, int64_t T, int k, int E, int P,
+                              int H, int recv_part, int align, int64_t cap_send,
+                              int64_t cap_recv, uint16_t *recv, int32_t *expert_offsets,
+                              int32_t *pair_row, int32_t *recv_pair, uint32_t *status)
+{
+    if (P < 1 || E % P != 0 || align < 1 || recv_part < -1 || recv_part >= P)
+        return -1;
+    const int L = E / P;
+    const int64_t npairs = (int64_t)S * T * k;
+    int64_t *cnt = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    int64_t *fill = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    if (!cnt || !fill) {
+        free(cnt);
+        free(fill);
+        return -2;
+    }
+    /* counts per expert over the receiving set */
+    for (int64_t q = 0; q < npairs; q++) {
+        int32_t e = ids[q];
+        if (e >= E)
+            *status |= ORC_BIT_BAD_ID;
+        if (e < 0 || e >= E)
+            continue;
+        if (recv_part >= 0 && e / L != recv_part)
+            continue;
+        cnt[e]++;
+    }
+    /* padded run offsets */
+    int64_t off = 0;
+    for (int e = 0; e < E; e++) {
+        expert_offsets[e] = (int32_t)off;
+        int in_r = (recv_part < 0) || (e / L == recv_part);
+        if (in_r)
+            off += (cnt[e] + align - 1) / align * align;
+    }
+    expert_offsets[E] = (int32_t)off;
+    const int64_t total = off;
+    /* every row starts as padding */
+    for (int64_t r = 0; r < cap_recv; r++)
+        recv_pair[r] = -1;
+    for (int64_t r = 0; r < total && r < cap_recv; r++)
+        memset(recv + r * H, 0, sizeof(uint16_t) * (size_t)H);
+    /* pairs in ascending (s, t, j) order go to the end of their expert's run */
+    for (int s = 0; s < S; s++) {
+        for (int64_t t = 0; t < T; t++) {
+            for (int j = 0; j < k; j++) {
+                int64_t q = ((int64_t)s * T + t) * k + j;
+                int32_t e = ids[q];
+                pair_row[q] = -1;
+                if (e < 0 || e >= E)
+                    continue;
+                int p = e / L;
+                if (recv_part >= 0 && p != recv_part)
+                    continue;
+                int64_t row = expert_offsets[e] + fill[e];
+                fill[e]++;
+                if (row >= cap_recv) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue;
+                }
+                pair_row[q] = (int32_t)row;
+                recv_pair[row] = (int32_t)q;
+                int32_t slot = token_slot[((int64_t)s * T + t) * P + p];
+                if (slot < 0) {
+                    *status |= ORC_BIT_INCONSISTENT;
+                    continue; /* row stays zero */
+                }
+                if (slot >= cap_send) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue; /* row stays zero */
+                }
+                memcpy(recv + row * H, send + ((int64_t)s * cap_send + slot) * H,
+                       sizeof(uint16_t) * (size_t)H);
+            }
+        }
+    }
+    free(cnt);
+    free(fill);
+    return 0;
+}
+
+/* ------------------------------------------------------ stand-in expert -- */
+
+/*
+ * Stand-in for the expert kernel (not part of the method; the pages time
+ * dispatch and combine without it, [a2a] 8.1): every row of expert e's run is
+ * multiplied by the scalar scale[e] and rounded once to bfloat16.  Rows at or
+ * beyond min(expert_offsets[E], cap_recv) are not written.
+ */
+int oracle_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
+                        const float *scale, int E, int H, int64_t cap_recv, uint16_t *y)
+{
+    for (int e = 0; e < E; e++) {
+        for (int64_t r = expert_offsets[e]; r < expert_offsets[e + 1] && r < cap_recv; r++) {
+            for (int h = 0; h < H; h++) {
+                double v = oracle_bf16_to_double(recv[r * H + h]) * (double)scale[e];
+                y[r * H + h] = oracle_bf16_from_double(v);
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------ combine, [a2a] 7.1 */
+
+/*
+ * [a2a] 1.1 / 7.1: the MoE output of a token is the sum of its experts'
+ * outputs, each multiplied by its router weight; the home side adds in (at
+ * least) 32-bit floats ([a2a] 7.1, FlashInfer) and the result travels as
+ * bf16 ([a2a] 7.2).  Here the sum is taken in double and rounded once:
+ *   out[s][t][h] = bf16( sum_{j : pair_row >= 0} w[s][t][j] * y[pair_row[s][t][j]][h] )
+ * A token with no valid pair gets +0.
+ */
+int oracle_combine(const uint16_t *y, const int32_t *pair_row, const float *w,
+                   int S, int64_t T, int k, int H, uint16_t *out)
+{
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    if (!acc)
+        return -2;
+    for (int64_t n = 0; n < (int64_t)S * T; n++) {
+        for (int h = 0; h < H; h++)
+            acc[h] = 0.0;
+        for (int j = 0; j < k; j++) {
+            int32_t r = pair_row[n * k + j];
+            if (r < 0)
+                continue;
+            double wj = (double)w[n * k + j];
+            for (int h = 0; h < H; h++)
+                acc[h] += wj * oracle_bf16_to_double(y[(int64_t)r * H + h]);
+        }
+        for (int h = 0; h < H; h++)
+            out[n * H + h] = oracle_bf16_from_double(acc[h]);
+    }
+    free(acc);
+    return 0;
+}

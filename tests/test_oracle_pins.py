@@ -1,0 +1,477 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each oracle function is checked against something other than itself: values
+the pages print (fixtures under tests/golden/, each citing its passage),
+closed forms, invariants, library routines that compute the same thing, and
+brute force on tiny inputs.  Pages cited:
+  a2a-backends  vincentzed.com/writing/a2a-backends
+  Beyond One GPU  ishwarj.com/writings/llm-inference-7-beyond-one-gpu
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import moe_synth as ms
+import oracle
+
+MiB = 1024 * 1024
+
+
+def _golden(name):
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ bf16 --
+
+def test_bf16_round_trip_and_ties():
+    # exact values survive; halfway cases go to the even neighbour
+    for b in (0x0000, 0x8000, 0x3F80, 0xBF80, 0x7F7F, 0x0001, 0x8001, 0x4049):
+        assert oracle.bf16_from_double(oracle.bf16_to_double(b)) == b
+    one = 1.0
+    ulp = 2.0 ** -7
+    assert oracle.bf16_from_double(one + ulp / 2) == 0x3F80          # tie -> even (1.0)
+    assert oracle.bf16_from_double(one + 3 * ulp / 2) == 0x3F82      # tie -> even (1 + 2ulp)
+    assert oracle.bf16_from_double(one + ulp / 2 + 2 ** -40) == 0x3F81  # just above the tie
+    assert oracle.bf16_from_double(-(one + ulp / 2)) == 0xBF80
+    assert oracle.bf16_from_double(3.0e38 * 2) == 0x7F80             # overflow -> inf
+    assert oracle.bf16_from_double(2.0 ** -134) == 0x0000            # below half the smallest subnormal
+    assert oracle.bf16_from_double(3 * 2.0 ** -134) == 0x0002        # 1.5 quanta -> even (2 quanta)
+
+
+def test_bf16_matches_bit_trick_on_floats():
+    # For float32-representable inputs a single rounding to bf16 equals the
+    # classic add-0x7FFF-plus-lsb bit trick (an independent formulation).
+    rng = np.random.default_rng(1)
+    f = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    want = ms.bf16_bits_from_f32(f)
+    got = np.array([oracle.bf16_from_double(float(v)) for v in f], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_double_rounding_is_avoided():
+    # 1 + 2^-8 + 2^-30 is above the halfway point: one rounding gives 1 + 2^-7,
+    # while rounding to float32 first (1 + 2^-8, a tie) then to bf16 gives 1.0.
+    v = 1.0 + 2.0 ** -8 + 2.0 ** -30
+    assert oracle.bf16_from_double(v) == 0x3F81
+
+
+# ------------------------------------------- copies per token, a2a-backends 1.3 --
+
+def test_expected_copies_printed_values():
+    g = _golden("copies_closed_form.json")
+    for c in g["cases"]:
+        v = oracle.expected_copies(c["E"], c["G"], c["k"])
+        assert round(v, g["printed_decimals"]) == pytest.approx(c["printed"], abs=1e-9), c
+
+
+@pytest.mark.parametrize("E,G,k", [(8, 4, 3), (12, 3, 4), (9, 3, 2), (10, 5, 1), (8, 2, 8)])
+def test_expected_copies_brute_force(E, G, k):
+    # average over every k-subset of the number of blocks it touches
+    L = E // G
+    tot = 0
+    n = 0
+    for sub in itertools.combinations(range(E), k):
+        tot += len({e // L for e in sub})
+        n += 1
+    assert oracle.expected_copies(E, G, k) == pytest.approx(tot / n, rel=1e-12)
+
+
+# -------------------------------------------------------- route (a2a 1.1) --
+
+def _check_topk(logits, ids, w, k):
+    E = logits.shape[-1]
+    for n in range(logits.shape[0]):
+        row = logits[n]
+        sel = ids[n]
+        assert len(set(sel.tolist())) == k
+        unsel = np.setdiff1d(np.arange(E), sel)
+        # every chosen logit >= every other one; equal ones resolved to the lower id
+        if unsel.size:
+            m_un = row[unsel].max()
+            assert row[sel].min() >= m_un
+            for e in sel:
+                for e2 in unsel:
+                    if row[e] == row[e2]:
+                        assert e < e2
+        # descending order, ties by ascending id
+        for a, b in zip(sel[:-1], sel[1:]):
+            assert row[a] > row[b] or (row[a] == row[b] and a < b)
+        # weights: positive, sum to one, ratios are exp of logit differences
+        assert np.all(w[n] > 0)
+        assert w[n].sum() == pytest.approx(1.0, abs=1e-12)
+        for j in range(k):
+            assert w[n, j] / w[n, 0] == pytest.approx(math.exp(float(row[sel[j]]) - float(row[sel[0]])),
+                                                      rel=1e-12)
+
+
+def test_route_topk_properties_random():
+    w_ = ms.workload("tiny")
+    logits = ms.gen_logits(w_)[0]
+    ids, w = oracle.route_topk(logits, w_.k)
+    _check_topk(logits, ids, w, w_.k)
+
+
+def test_route_topk_ties_pick_lower_id():
+    rng = np.random.default_rng(7)
+    logits = rng.integers(-2, 3, size=(64, 10)).astype(np.float32)  # many ties
+    ids, w = oracle.route_topk(logits, 4)
+    _check_topk(logits, ids, w, 4)
+    # all-equal row: the k lowest ids, equal weights
+    ids, w = oracle.route_topk(np.zeros((1, 7), np.float32), 3)
+    assert ids.tolist() == [[0, 1, 2]]
+    assert np.allclose(w, 1 / 3)
+
+
+def test_route_topk_full_softmax_and_k1():
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal((20, 12)).astype(np.float32)
+    ids, w = oracle.route_topk(logits, 12)  # k = E: plain softmax, reordered
+    for n in range(20):
+        ref = scipy_special.softmax(logits[n].astype(np.float64))
+        assert np.allclose(w[n], ref[ids[n]], rtol=1e-12, atol=0)
+        assert np.array_equal(ids[n], np.argsort(-logits[n].astype(np.float64), kind="stable"))
+    ids, w = oracle.route_topk(logits, 1)  # k = 1: argmax with weight 1
+    assert np.array_equal(ids[:, 0], np.argmax(logits, axis=1))
+    assert np.all(w == 1.0)
+
+
+def test_route_topk_brute_force_subsets():
+    # the chosen set maximises the sum of logits over all k-subsets (distinct logits)
+    rng = np.random.default_rng(11)
+    logits = rng.standard_normal((30, 7)).astype(np.float32)
+    k = 3
+    ids, _ = oracle.route_topk(logits, k)
+    for n in range(30):
+        best = max(itertools.combinations(range(7), k), key=lambda s: sum(float(logits[n, e]) for e in s))
+        assert set(ids[n].tolist()) == set(best)
+
+
+# ---------------------------------------------------- layout (a2a 1.1, 1.3, 3.2) --
+
+def test_layout_fig1_two_copies():
+    g = _golden("fig1_two_copies.json")
+    ids = np.array(g["ids"], np.int32)[None]
+    lay = oracle.dispatch_layout(ids, g["E"], g["P"])
+    assert int(lay["part_offsets"][0, -1]) == g["expected_copies"]
+    hit = [p for p in range(g["P"]) if lay["token_slot"][0, 0, p] >= 0]
+    assert hit == g["expected_partitions"]
+    assert int(lay["expert_counts"].sum()) == 3
+
+
+def _brute_layout(ids, E, P):
+    """Independent formulation: list every (partition, token) pair a token needs,
+    sort the list by (partition, token) and number it 0, 1, 2, ..."""
+    S, T, k = ids.shape
+    L = E // P
+    slot = -np.ones((S, T, P), np.int64)
+    counts = np.zeros((S, P), np.int64)
+    ecounts = np.zeros((S, E), np.int64)
+    for s in range(S):
+        need = sorted({(int(e) // L, t) for t in range(T) for e in ids[s, t] if 0 <= e < E})
+        for i, (p, t) in enumerate(need):
+            slot[s, t, p] = i
+            counts[s, p] += 1
+        for e in ids[s].ravel():
+            if 0 <= e < E:
+                ecounts[s, e] += 1
+    return slot, counts, ecounts
+
+
+def test_layout_brute_force_all_tiny_inputs():
+    # every id assignment of T=2 tokens, k=2, E=4 (ids in -1..4, 4 = out of range), P=2
+    E, P, k, T = 4, 2, 2, 2
+    vals = [-1, 0, 1, 2, 3, 4]
+    for combo in itertools.product(vals, repeat=T * k):
+        ids = np.array(combo, np.int32).reshape(1, T, k)
+        lay = oracle.dispatch_layout(ids, E, P)
+        slot, counts, ecounts = _brute_layout(ids, E, P)
+        assert np.array_equal(lay["token_slot"], slot), combo
+        assert np.array_equal(lay["part_counts"], counts), combo
+        assert np.array_equal(lay["expert_counts"], ecounts), combo
+        assert np.array_equal(lay["part_offsets"][:, 1:], np.cumsum(counts, axis=1)), combo
+        assert (lay["status"] == oracle.BIT_BAD_ID) == (4 in combo), combo
+
+
+def test_layout_brute_force_random_small():
+    rng = np.random.default_rng(5)
+    for _ in range(40):
+        S, T, P = int(rng.integers(1, 3)), int(rng.integers(0, 9)), int(rng.integers(1, 5))
+        L = int(rng.integers(1, 3))
+        E = P * L
+        k = int(rng.integers(1, min(E, 3) + 1))
+        ids = rng.integers(-1, E, size=(S, T, k)).astype(np.int32)
+        lay = oracle.dispatch_layout(ids, E, P)
+        slot, counts, ecounts = _brute_layout(ids, E, P)
+        assert np.array_equal(lay["token_slot"], slot)
+        assert np.array_equal(lay["part_counts"], counts)
+        assert np.array_equal(lay["expert_counts"], ecounts)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])
+def test_layout_invariants(name):
+    w_ = ms.workload(name)
+    ids, _ = oracle.route_topk(ms.gen_logits(w_), w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    S, T = w_.S, w_.T
+    assert lay["status"] == 0
+    assert lay["expert_counts"].sum() == S * T * w_.k            # nothing skipped
+    copies = (lay["token_slot"] >= 0).sum(axis=2)
+    assert copies.min() >= 1 and copies.max() <= min(w_.k, w_.P)
+    assert np.array_equal(lay["part_offsets"][:, -1], copies.sum(axis=1))
+    for s in range(S):
+        for p in range(w_.P):
+            sl = lay["token_slot"][s, :, p]
+            v = sl[sl >= 0]
+            lo, hi = lay["part_offsets"][s, p], lay["part_offsets"][s, p + 1]
+            assert np.array_equal(v, np.arange(lo, hi))                 # dense, ascending in t
+
+
+def _mean_copies_sigma(E, P, k, T):
+    """Standard error of the mean copy count under uniform routing (exact variance)."""
+    L = E // P
+    q1 = math.comb(E - L, k) / math.comb(E, k)           # P(partition missed)
+    q2 = math.comb(E - 2 * L, k) / math.comb(E, k)       # P(two given partitions missed)
+    var = P * q1 * (1 - q1) + P * (P - 1) * (q2 - q1 * q1)
+    return math.sqrt(var / T)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])
+def test_mean_copies_matches_closed_form(name):
+    w_ = ms.workload(name)
+    ids, _ = oracle.route_topk(ms.gen_logits(w_), w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    c = lay["part_offsets"][0, -1] / w_.T
+    mu = oracle.expected_copies(w_.E, w_.P, w_.k)
+    sig = _mean_copies_sigma(w_.E, w_.P, w_.k, w_.T)
+    assert abs(c - mu) < 5 * sig, (c, mu, sig)
+
+
+def test_bytes_per_gpu_printed_values():
+    g = _golden("bytes_per_gpu.json")
+    rb = g["row_bytes"]
+    for case in g["cases"]:
+        T = case["rows_per_gpu"]
+        w_ = ms.workload("prefill", T=T) if T == 4096 else ms.workload("decode", T=T)
+        ids, _ = oracle.route_topk(ms.gen_logits(w_), w_.k)
+        lay = oracle.dispatch_layout(ids, g["E"], g["G"])
+        broadcast = g["G"] * T * rb / MiB
+        per_expert = lay["expert_counts"].sum() * rb / MiB
+        dedup = lay["part_offsets"][0, -1] * rb / MiB
+        assert broadcast == pytest.approx(case["broadcast_MiB"], abs=0.05)
+        assert per_expert == pytest.approx(case["per_expert_MiB"], abs=0.05)
+        # sampled copies: 5 standard errors of the mean, plus the page's rounding
+        sig = _mean_copies_sigma(g["E"], g["G"], g["k"], T) * T * rb / MiB
+        half_digit = 0.5 if case["dedup_MiB"] >= 100 else 0.05
+        assert abs(dedup - case["dedup_MiB"]) <= 5 * sig + half_digit, (dedup, sig)
+        # the closed-form expectation itself reproduces the printed figure
+        mu = oracle.expected_copies(g["E"], g["G"], g["k"]) * T * rb / MiB
+        assert abs(mu - case["dedup_MiB"]) <= half_digit
+
+
+def test_byte_model_per_expert_copies():
+    g = _golden("byte_model_b1g.json")
+    assert g["k"] * g["d"] * (g["s_dispatch"] + g["s_combine"]) == g["bytes_per_token"]
+    # the oracle's per-expert count (sum of expert_counts) gives one copy per chosen expert
+    rng = np.random.default_rng(2)
+    logits = rng.standard_normal((1, g["tokens"], g["E"])).astype(np.float32)
+    ids, _ = oracle.route_topk(logits, g["k"])
+    lay = oracle.dispatch_layout(ids, g["E"], 8)
+    mb = lay["expert_counts"].sum() * g["d"] * g["s_dispatch"] / 1e6
+    assert round(mb, 2) == g["dispatch_MB_1e6"]
+
+
+# ------------------------------------------------------------- pack (a2a 3.2) --
+
+def test_pack_rows_are_bit_copies():
+    w_ = ms.workload("tiny")
+    inp = ms.gen_inputs(w_)
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap = w_.T * min(w_.k, w_.P)
+    send, src, st = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap)
+    assert st == 0
+    used = lay["part_offsets"][0, -1]
+    assert np.all(src[0, :used] >= 0) and np.all(src[0, used:] == -1)
+    assert np.array_equal(send[0, :used], inp["x"][0, src[0, :used]])
+    for p in range(w_.P):
+        seg = src[0, lay["part_offsets"][0, p]:lay["part_offsets"][0, p + 1]]
+        assert np.all(np.diff(seg) > 0)                                   # ascending tokens
+        # exactly the tokens that need partition p
+        need = [t for t in range(w_.T) if any(e // (w_.E // w_.P) == p for e in ids[0, t])]
+        assert seg.tolist() == need
+
+
+def test_pack_capacity_drop():
+    w_ = ms.workload("tiny")
+    inp = ms.gen_inputs(w_)
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap = 100
+    send, src, st = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap)
+    assert st == oracle.BIT_CAPACITY
+    assert np.all(src[0] >= 0)
+    assert np.array_equal(send[0], inp["x"][0, src[0]])
+
+
+# --------------------------------------------------- permute (a2a 1.5, 3.3, 5.1) --
+
+def test_permute_regroup_5_to_7():
+    g = _golden("regroup_5_to_7.json")
+    ids = np.array(g["ids"], np.int32)[None]
+    T = ids.shape[1]
+    H = 8
+    x = np.arange(T * H, dtype=np.uint16).reshape(1, T, H) + 1
+    lay = oracle.dispatch_layout(ids, g["E"], g["P"])
+    p = g["recv_part"]
+    assert lay["part_counts"][0, p] == g["expected_arrived_rows"]
+    send, src, _ = oracle.dispatch_pack(x, lay["token_slot"], T * 2)
+    per = oracle.permute_to_experts(send, lay["token_slot"], ids, g["E"], recv_part=p)
+    off = per["expert_offsets"]
+    assert off[-1] == g["expected_permuted_rows"]
+    for e_str, toks in g["expected_expert_runs"].items():
+        e = int(e_str)
+        rows = per["recv"][off[e]:off[e + 1]]
+        assert np.array_equal(rows, x[0, toks])
+    assert np.all(per["pair_row"][0][ids[0] // 4 != p] == -1)
+
+
+def _stable_sort_pin(ids, recv_part, E, P, per):
+    """The permuted order is a stable sort of the receiving pairs by expert id."""
+    flat = ids.reshape(-1)
+    L = E // P
+    q = np.nonzero((flat >= 0) & (flat < E) & ((recv_part < 0) | (flat // L == recv_part)))[0]
+    order = q[np.argsort(flat[q], kind="stable")]
+    rp = per["recv_pair"]
+    got = rp[rp >= 0]
+    assert np.array_equal(got, order)
+
+
+@pytest.mark.parametrize("name,align,recv_part", [("tiny", 1, -1), ("tiny", 128, -1), ("tiny", 8, 2),
+                                                  ("decode", 1, -1), ("decode", 128, 3)])
+def test_permute_stable_sort_and_inverse(name, align, recv_part):
+    w_ = ms.workload(name)
+    inp = ms.gen_inputs(w_)
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap = w_.T * min(w_.k, w_.P)
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap)
+    per = oracle.permute_to_experts(send, lay["token_slot"], ids, w_.E, recv_part=recv_part, align=align)
+    assert per["status"] == 0
+    _stable_sort_pin(ids, recv_part, w_.E, w_.P, per)
+    pr = per["pair_row"].reshape(-1)
+    rp = per["recv_pair"]
+    valid = np.nonzero(pr >= 0)[0]
+    assert np.array_equal(rp[pr[valid]], valid)                  # recv_pair o pair_row = id
+    rows = np.nonzero(rp >= 0)[0]
+    assert np.array_equal(pr[rp[rows]], rows)                    # pair_row o recv_pair = id
+    off = per["expert_offsets"]
+    assert np.all(np.diff(off) % align == 0)
+    L = w_.E // w_.P
+    for e in range(w_.E):
+        rr = np.arange(off[e], off[e + 1])
+        real = rr[rp[rr] >= 0]
+        pad = rr[rp[rr] < 0]
+        assert np.all(ids.reshape(-1)[rp[real]] == e)
+        assert np.all(per["recv"][pad] == 0)
+        if recv_part >= 0 and e // L != recv_part:
+            assert rr.size == 0
+    # each row is the source token's row
+    tok = rows // w_.k
+    assert np.array_equal(per["recv"][rows], inp["x"].reshape(-1, w_.H)[rp[rows] // w_.k])
+    _ = tok
+
+
+def test_permute_capacity_drop_and_bad_id():
+    w_ = ms.workload("tiny")
+    inp = ms.gen_inputs(w_)
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    ids = ids.copy()
+    ids[0, 5, 1] = w_.E + 3      # out of range: skipped and flagged
+    ids[0, 6, 0] = -1            # not routed: skipped silently
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    assert lay["status"] == oracle.BIT_BAD_ID
+    cap = w_.T * min(w_.k, w_.P)
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap)
+    per = oracle.permute_to_experts(send, lay["token_slot"], ids, w_.E, cap_recv=100)
+    assert per["status"] == (oracle.BIT_BAD_ID | oracle.BIT_CAPACITY)
+    pr = per["pair_row"].reshape(-1)
+    assert pr.max() < 100 and (pr >= 0).sum() == 100
+    assert pr[5 * w_.k + 1] == -1 and pr[6 * w_.k + 0] == -1
+
+
+# ------------------------------------------------------------ combine (a2a 7.1) --
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_identity_round_trip(name):
+    # identity experts and weights that sum to one return the input rows
+    w_ = ms.workload(name)
+    inp = ms.gen_inputs(w_)
+    r = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, ms.gen_scales(w_, identity=True))
+    assert np.array_equal(r["out"], inp["x"])
+
+
+def test_identity_round_trip_with_alignment():
+    w_ = ms.workload("tiny")
+    inp = ms.gen_inputs(w_)
+    r = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, None, align=128)
+    assert np.array_equal(r["out"], inp["x"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_combine_closed_form_for_scalar_experts(name):
+    # every pair of a token carries the same row x, so out = x * sum_j w_j s_{e_j}
+    w_ = ms.workload(name)
+    inp = ms.gen_inputs(w_)
+    r = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, inp["scales"])
+    ids = r["ids"]
+    w32 = r["w"].astype(np.float32).astype(np.float64)
+    factor = (w32 * inp["scales"].astype(np.float64)[ids]).sum(axis=2)          # [S, T]
+    ref = ms.f32_from_bf16_bits(inp["x"]).astype(np.float64) * factor[..., None]
+    got = ms.f32_from_bf16_bits(r["out"]).astype(np.float64)
+    # two bf16 roundings (expert output, final sum): 2^-8 relative each
+    assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30)
+
+
+def test_combine_partials_sum_to_full():
+    # stage-1 partial combines over each receiving partition add up to the full combine (a2a 7.1)
+    w_ = ms.workload("tiny")
+    inp = ms.gen_inputs(w_)
+    full = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, inp["scales"])
+    acc = np.zeros(inp["x"].shape, np.float64)
+    for p in range(w_.P):
+        part = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, inp["scales"], recv_part=p)
+        acc += ms.f32_from_bf16_bits(part["out"])
+    ref = ms.f32_from_bf16_bits(full["out"]).astype(np.float64)
+    assert np.all(np.abs(acc - ref) <= 1e-2 * np.maximum(np.abs(ref), 1e-3))
+
+
+def test_combine_skips_invalid_pairs_and_empty_tokens():
+    H = 16
+    y = ms.bf16_bits_from_f32(np.arange(3 * H, dtype=np.float32).reshape(3, H) / 8)
+    pair_row = np.array([[[0, -1], [-1, -1], [2, 1]]], np.int32)
+    w = np.array([[[0.5, 0.25], [0.3, 0.7], [0.25, 0.75]]], np.float32)
+    out = oracle.combine(y, pair_row, w)
+    yf = ms.f32_from_bf16_bits(y).astype(np.float64)
+    assert np.array_equal(out[0, 0], ms.bf16_bits_from_f32((0.5 * yf[0]).astype(np.float32)))
+    assert np.all(out[0, 1] == 0)
+    assert np.array_equal(out[0, 2], ms.bf16_bits_from_f32((0.25 * yf[2] + 0.75 * yf[1]).astype(np.float32)))
+
+
+def test_expert_scale_exact_products():
+    # tiny scales (e+1)/16 times bf16 values are exact in float32, so the
+    # oracle's single rounding must equal float32 multiply + bit-trick rounding
+    w_ = ms.workload("tiny")
+    inp = ms.gen_inputs(w_)
+    r = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, inp["scales"])
+    per = r["permute"]
+    off = per["expert_offsets"]
+    for e in range(w_.E):
+        rows = per["recv"][off[e]:off[e + 1]]
+        want = ms.bf16_bits_from_f32(ms.f32_from_bf16_bits(rows) * np.float32(inp["scales"][e]))
+        assert np.array_equal(r["y"][off[e]:off[e + 1]], want)
