@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Throughput of the MoE token path on one GB300: route -> dispatch (layout,
+pack, receiver permute) -> combine, on the prefill workload of the
+a2a-backends page (4,096 tokens per rank, 5,120-wide bf16 rows, 384 experts
+top-6 over 8 partitions of 48).
+
+Prints ONE JSON line.  `value` is algorithmic GB/s of the whole step (bytes
+each call must move, counted from the measured copies and pairs) divided by
+the device time of the step (CUDA events, L2 flushed before every step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (single thread, this host) on the same
+workload and metric.  Under torchrun each rank runs an independent replica on
+its own batch (weak scaling, no data-path collective); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import moe_synth as ms  # noqa: E402
+
+METRIC = "dispatch+combine HBM GB/s and rows/s at 4096-token prefill; % of HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT = "k_perm_copy"
+
+
+# ------------------------------------------------------------ byte model --
+
+def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv):
+    """Bytes each call must read + write at minimum.
+
+    copies: rows packed (sum of part_offsets[s][P]); copies_recv: packed rows
+    bound for the receiving partition(s); pairs_recv: permuted pair rows.
+    """
+    NT = S * T
+    b = {
+        "route": NT * E * 4 + NT * k * 8,
+        "layout": NT * k * 4 + NT * P * 4 + S * (E + 2 * P + 1) * 4,
+        "pack": NT * H * 2 + copies * H * 2 + copies * 4,
+        "permute": copies_recv * H * 2 + pairs_recv * H * 2 + NT * k * 8,
+        "combine": pairs_recv * H * 2 + NT * k * 8 + NT * H * 2,
+    }
+    b["dispatch_combine"] = b["layout"] + b["pack"] + b["permute"] + b["combine"]
+    b["step"] = b["route"] + b["dispatch_combine"]
+    b["perm_copy"] = copies_recv * H * 2 + pairs_recv * H * 2 + NT * k * 8
+    return b
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+# ------------------------------------------------------ distributed glue --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the job time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_workload(name: str, rank: int) -> ms.Workload:
+    """Each rank gets its own batch of the same shape (distinct seeds)."""
+    w = ms.workload(name)
+    return w if rank == 0 else ms.workload(name, index=w.index + 1000 * rank)
+
+
+# ------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loop runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.cmd = ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", str(interval_ms)]
+        self.lines = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0: float | None = None, t1: float | None = None):
+        """Summary of the samples taken between host times t0 and t1 (the loop)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def physical_gpu_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    if ids and local < len(ids) and ids[local].isdigit():
+        return int(ids[local])
+    return local
+
+
+# ------------------------------------------------------- CPU oracle arm --
+
+def oracle_step(inp, w):
+    """One pass of the whole path through the CPU oracle (identity expert)."""
+    import oracle
+    ids, wt = oracle.route_topk(inp["logits"], w.k)
+    lay = oracle.dispatch_layout(ids, w.E, w.P)
+    cap_send = w.T * min(w.k, w.P)
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap_send)
+    per = oracle.permute_to_experts(send, lay["token_slot"], ids, w.E, recv_part=w.recv_part)
+    oracle.combine(per["recv"], per["pair_row"], wt.astype(np.float32))
+    copies = int(lay["part_offsets"][:, -1].sum())
+    L = w.E // w.P
+    if w.recv_part < 0:
+        copies_recv = copies
+    else:
+        copies_recv = int(lay["part_counts"][:, w.recv_part].sum())
+    pairs_recv = int(per["expert_offsets"][-1])
+    _ = L
+    return copies, copies_recv, pairs_recv
+
+
+def time_oracle(w, seconds: float, max_steps: int, min_steps: int = 1):
+    inp = ms.gen_inputs(w)
+    n = 0
+    t0 = time.perf_counter()
+    stats = None
+    while True:
+        stats = oracle_step(inp, w)
+        n += 1
+        el = time.perf_counter() - t0
+        if n >= min_steps and (el >= seconds or n >= max_steps):
+            break
+    b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, *stats)
+    return n, el, b
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    full = ms.workload(args.workload)
+    # bounded sample: shrink the token count so that W + K steps take ~2 minutes
+    inp_full = ms.gen_inputs(full)
+    t0 = time.perf_counter()
+    oracle_step(inp_full, full)
+    t_full = time.perf_counter() - t0
+    frac = min(1.0, 120.0 / ((args.steps + args.warmup) * t_full))
+    T = max(64, int(full.T * frac))
+    w = ms.workload(args.workload, T=T) if T < full.T else full
+    inp = ms.gen_inputs(w) if T < full.T else inp_full
+    for _ in range(args.warmup):
+        oracle_step(inp, w)
+    times = []
+    stats = None
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        stats = oracle_step(inp, w)
+        times.append(time.perf_counter() - t0)
+    b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, *stats)
+    tot = sum(times)
+    value = b["step"] * args.steps / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, "none (CPU)"),
+        "rows_per_s": round(w.S * w.T * args.steps / tot, 1),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} steps of the {w.name} workload with T={w.T} of "
+                                   f"{full.T} tokens per source, single thread"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, l2):
+    return {"workload": f"{w.name}: S={w.S} T={w.T} H={w.H} bf16, E={w.E} top-{w.k}, "
+                        f"P={w.P} partitions, recv_part={w.recv_part}",
+            "tokens_per_rank": w.S * w.T, "hidden": w.H, "experts": w.E, "topk": w.k,
+            "partitions": w.P, "l2": l2, "value_scope": "route+layout+pack+permute+combine"}
+
+
+# ------------------------------------------------------------ GPU arm --
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import combine_moe_route_06_gb300 as m
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    m.load_library()
+
+    w = rank_workload(args.workload, rank)
+    inp = ms.gen_inputs(w)
+    stream = torch.cuda.Stream(device=dev)
+    path = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)   # 1 GiB > L2 (~126 MiB)
+    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+    h_x = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+    h_out = torch.empty((w.S, w.T, w.H), dtype=torch.int16).pin_memory()
+    launches = path.launches_per_step()
+
+    def step():
+        path.step(logits, x, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            flush.fill_(1)
+            step()
+        torch.cuda.synchronize()
+        path.dev_status.zero_()
+        step()
+        torch.cuda.synchronize()
+        status = int(path.dev_status.item())
+        copies = int(path.part_offsets[:, -1].sum().item())
+        copies_recv = copies if w.recv_part < 0 else int(path.part_counts[:, w.recv_part].sum().item())
+        pairs_recv = int(path.expert_offsets[-1].item())
+        b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv)
+
+        # ---------------- timed region: K steps, L2 flushed before each ------
+        K = args.steps
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+        sampler = ClockSampler(physical_gpu_index(local)) if rank == 0 else None
+        m.trace_enable(DOMINANT, max_records=K + 8)
+        m.trace_reset()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+            time.sleep(0.5)
+        t_loop0 = time.perf_counter()
+        flush2 = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+        flush2.fill_(2)                    # head start so the host enqueues ahead of the GPU
+        t_host0 = time.perf_counter()
+        for i in range(K):
+            flush.fill_(1)
+            e = ev[i]
+            e[0].record(stream)
+            path.route(logits, stream)
+            e[1].record(stream)
+            m.moe_dispatch_layout(path.topk_ids, w.E, w.P, path.expert_counts, path.part_counts,
+                                  path.part_offsets, path.token_slot, path.ws, path.dev_status,
+                                  stream)
+            e[2].record(stream)
+            m.moe_dispatch_pack(x, path.token_slot, path.part_offsets, path.send, path.send_src,
+                                path.dev_status, stream)
+            e[3].record(stream)
+            m.moe_permute_to_experts(path.send, path.token_slot, path.topk_ids, w.E, w.recv_part,
+                                     1, path.recv, path.expert_offsets, path.pair_row,
+                                     path.recv_pair, path.ws, path.dev_status, stream)
+            e[4].record(stream)
+            path.combine(stream=stream)
+            e[5].record(stream)
+        host_enqueue_us = (time.perf_counter() - t_host0) * 1e6 / K
+        torch.cuda.synchronize()
+        t_loop1 = time.perf_counter()
+        if dist is not None:
+            dist.barrier()
+        clocks = sampler.stop(t_loop0, t_loop1) if sampler else None
+        del flush2
+        recs = [ms_ for name, ms_ in m.trace_records() if name == DOMINANT]
+        m.trace_disable()
+
+        step_ms = [e[0].elapsed_time(e[5]) for e in ev]
+        stage_ms = {
+            "route": [e[0].elapsed_time(e[1]) for e in ev],
+            "layout": [e[1].elapsed_time(e[2]) for e in ev],
+            "pack": [e[2].elapsed_time(e[3]) for e in ev],
+            "permute": [e[3].elapsed_time(e[4]) for e in ev],
+            "combine": [e[4].elapsed_time(e[5]) for e in ev],
+        }
+        total_ms = sum(step_ms)
+        job_ms = max_over_ranks(total_ms, dist, dev)
+        bytes_all = sum_over_ranks(float(b["step"]) * K, dist, dev)
+        rows_all = sum_over_ranks(float(w.S * w.T) * K, dist, dev)
+        value = bytes_all / (job_ms * 1e-3) / 1e9
+
+        # ---------------- end to end: pinned host in, pinned host out --------
+        Ke = max(10, min(K, 200))
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(Ke):
+            flush.fill_(1)
+            ee[i][0].record(stream)
+            logits.copy_(h_logits, non_blocking=True)
+            x.view(torch.int16).copy_(h_x, non_blocking=True)
+            path.step(logits, x, stream=stream)
+            h_out.copy_(path.out.view(torch.int16), non_blocking=True)
+            ee[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(sum(p[0].elapsed_time(p[1]) for p in ee), dist, dev)
+        e2e_bytes = sum_over_ranks(float(b["step"]) * Ke, dist, dev)
+        e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
+        out_ok = bool(np.array_equal(h_out.numpy().view(np.uint16)[0, :4], path.out[0, :4].view(
+            torch.int16).cpu().numpy().view(np.uint16)))
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_src = measured_peak()
+    dom_ms = statistics.fmean(recs) if recs else None
+    dom_achieved = (b["perm_copy"] / (dom_ms * 1e-3) / 1e9) if dom_ms else None
+    dc_ms = [s - r for s, r in zip(step_ms, stage_ms["route"])]
+    dc_gbs = b["dispatch_combine"] * K / (sum(dc_ms) * 1e-3) / 1e9
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n, el, bb = time_oracle(ms.workload(args.workload), args.cpu_seconds, max_steps=100)
+        cpu = {"value": round(bb["step"] * n / el / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{n} full steps of the {w.name} workload in {el:.1f} s (single thread)"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(job_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(w, "flushed: 1 GiB write before every timed step"),
+        "rows_per_s": round(rows_all / (job_ms * 1e-3), 1),
+        "frac_of_hbm_peak": round(value / peak, 4),
+        "dispatch_combine": {"gbs": round(dc_gbs, 2), "us_median": round(1e3 * statistics.median(dc_ms), 2),
+                             "frac_of_hbm_peak": round(dc_gbs / peak, 4),
+                             "bytes": b["dispatch_combine"]},
+        "stages_us_median": {k_: round(1e3 * statistics.median(v), 2) for k_, v in stage_ms.items()},
+        "stage_bytes": {k_: b[k_] for k_ in ("route", "layout", "pack", "permute", "combine")},
+        "copies_per_token": round(copies / (w.S * w.T), 4),
+        "pairs_recv": pairs_recv,
+        "dev_status": status,
+        "roofline": {"kernel": DOMINANT, "bound": "hbm",
+                     "achieved": round(dom_achieved, 1) if dom_achieved else None,
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(dom_achieved / peak, 4) if dom_achieved else None,
+                     "traffic": None, "bytes_per_launch": b["perm_copy"],
+                     "us_per_launch": round(1e3 * dom_ms, 2) if dom_ms else None,
+                     "launches_timed": len(recs)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
+                "d2h_bytes_per_step": int(h_out.numel() * 2), "steps": Ke,
+                "ms_per_step": round(e2e_ms / Ke, 4), "readback_ok": out_ok},
+        "gpu_launches": launches * K,
+        "host_enqueue_us_per_step": round(host_enqueue_us, 1),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill", choices=sorted(ms.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

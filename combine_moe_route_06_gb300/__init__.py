@@ -1,0 +1,324 @@
+"""GB300 MoE token path: Python binding of libmoeroute.so.
+
+The five calls of the MoE token path (route, dispatch layout, pack, receiver
+permute, combine) run in hand-written sm_103a kernels behind a C ABI
+(``include/moe_route.h``).  This module only marshals torch tensors (device
+pointers, sizes, the current CUDA stream) through ctypes; PyTorch supplies
+device memory and streams.  There is no fallback: if the library is not
+built, importing works but every call raises ``MoeLibraryMissing``.
+
+Function names and argument order follow the C ABI; sizes are read from the
+tensor shapes.  bf16 arrays may be torch.bfloat16, torch.int16 or
+torch.uint16 tensors (the bits are what matters).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CAPACITY", "MOE_ERR_BAD_EXPERT_ID",
+    "MOE_ERR_TIMEOUT", "MOE_ERR_CUDA", "status_bit", "MoeError", "MoeLibraryMissing",
+    "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
+    "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
+    "moe_combine", "moe_expert_scale", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "trace_records",
+]
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_CAPACITY = 2
+MOE_ERR_BAD_EXPERT_ID = 3
+MOE_ERR_TIMEOUT = 4
+MOE_ERR_CUDA = 5
+
+
+def status_bit(code: int) -> int:
+    """Bit that a data error of kind `code` sets in the device status word."""
+    return 1 << code
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+class MoeLibraryMissing(RuntimeError):
+    pass
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libmoeroute.so for sm_103a (in-tree) and return its path."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libmoeroute.so (raises MoeLibraryMissing if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise MoeLibraryMissing(
+                f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sigs = {
+            "moe_version": ([], ctypes.c_int),
+            "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "moe_last_error_message": ([], ctypes.c_char_p),
+            "moe_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
+            "moe_route_topk": ([P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
+            "moe_dispatch_layout": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, sz, P, P],
+                                    ctypes.c_int),
+            "moe_dispatch_pack": ([P, i32, i32, i32, i32, P, P, i32, P, P, P, P], ctypes.c_int),
+            "moe_permute_to_experts": ([P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, P, P, P, P, P, sz, P, P], ctypes.c_int),
+            "moe_combine": ([P, i32, P, P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
+            "moe_expert_scale": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
+            "moe_trace_enable": ([ctypes.c_char_p, i32], ctypes.c_int),
+            "moe_trace_disable": ([], None),
+            "moe_trace_reset": ([], None),
+            "moe_trace_count": ([], ctypes.c_int),
+            "moe_trace_get": ([i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)],
+                              ctypes.c_int),
+        }
+        for name, (args, res) in sigs.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != MOE_OK:
+        lib = load_library()
+        raise MoeError(rc, lib.moe_last_error_message().decode())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+_BF16_TYPES = (torch.bfloat16, torch.int16) + ((torch.uint16,) if hasattr(torch, "uint16") else ())
+
+
+def _dev(t: torch.Tensor, name: str, dtypes, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got shape {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _status_ptr(dev_status):
+    if dev_status is None:
+        return ctypes.c_void_p(0)
+    return _dev(dev_status, "dev_status", (torch.int32,))
+
+
+def moe_version() -> int:
+    return load_library().moe_version()
+
+
+def moe_workspace_bytes(S: int, T: int, k: int, E: int, P: int) -> int:
+    return int(load_library().moe_workspace_bytes(S, T, k, E, P))
+
+
+def moe_route_topk(logits, topk_ids, topk_w, stream=None):
+    """logits f32 [S,T,E] -> topk_ids i32 [S,T,k], topk_w f32 [S,T,k]."""
+    lib = load_library()
+    S, T, E = logits.shape
+    k = topk_ids.shape[2]
+    _check(lib.moe_route_topk(_dev(logits, "logits", (torch.float32,), 3), S, T, E, k,
+                              _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+                              _dev(topk_w, "topk_w", (torch.float32,), 3), _stream(stream)))
+
+
+def moe_dispatch_layout(topk_ids, E, P, expert_counts, part_counts, part_offsets, token_slot,
+                        ws, dev_status=None, stream=None):
+    """topk_ids i32 [S,T,k] -> expert_counts [S,E], part_counts [S,P], part_offsets [S,P+1],
+    token_slot [S,T,P] (all int32); ws is a uint8 device tensor."""
+    lib = load_library()
+    S, T, k = topk_ids.shape
+    _check(lib.moe_dispatch_layout(
+        _dev(topk_ids, "topk_ids", (torch.int32,), 3), S, T, k, E, P,
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(part_counts, "part_counts", (torch.int32,)),
+        _dev(part_offsets, "part_offsets", (torch.int32,)),
+        _dev(token_slot, "token_slot", (torch.int32,)),
+        _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_pack(x, token_slot, part_offsets, send, send_src, dev_status=None, stream=None):
+    """x bf16 [S,T,H] -> send bf16 [S,cap_send,H], send_src i32 [S,cap_send]."""
+    lib = load_library()
+    S, T, H = x.shape
+    P = token_slot.shape[2]
+    cap_send = send.shape[1]
+    _check(lib.moe_dispatch_pack(
+        _dev(x, "x", _BF16_TYPES, 3), S, T, H, P, _dev(token_slot, "token_slot", (torch.int32,), 3),
+        _dev(part_offsets, "part_offsets", (torch.int32,)), cap_send,
+        _dev(send, "send", _BF16_TYPES, 3), _dev(send_src, "send_src", (torch.int32,)),
+        _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_permute_to_experts(send, token_slot, topk_ids, E, recv_part, align, recv, expert_offsets,
+                           pair_row, recv_pair, ws, dev_status=None, stream=None):
+    """send bf16 [S,cap_send,H] -> recv bf16 [cap_recv,H] in expert runs, expert_offsets [E+1],
+    pair_row [S,T,k], recv_pair [cap_recv]."""
+    lib = load_library()
+    S, cap_send, H = send.shape
+    _, T, P = token_slot.shape
+    k = topk_ids.shape[2]
+    cap_recv = recv.shape[0]
+    _check(lib.moe_permute_to_experts(
+        _dev(send, "send", _BF16_TYPES, 3), _dev(token_slot, "token_slot", (torch.int32,), 3),
+        _dev(topk_ids, "topk_ids", (torch.int32,), 3), S, T, k, E, P, H, recv_part, align,
+        cap_send, cap_recv, _dev(recv, "recv", _BF16_TYPES, 2),
+        _dev(expert_offsets, "expert_offsets", (torch.int32,)),
+        _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
+        _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_combine(y, pair_row, topk_w, out, dev_status=None, stream=None):
+    """out[s,t] = bf16(sum_j topk_w[s,t,j] * y[pair_row[s,t,j]]) with fp32 accumulation."""
+    lib = load_library()
+    S, T, k = pair_row.shape
+    H = out.shape[2]
+    _check(lib.moe_combine(_dev(y, "y", _BF16_TYPES, 2), y.shape[0],
+                           _dev(pair_row, "pair_row", (torch.int32,), 3),
+                           _dev(topk_w, "topk_w", (torch.float32,), 3), S, T, k, H,
+                           _dev(out, "out", _BF16_TYPES, 3), _status_ptr(dev_status),
+                           _stream(stream)))
+
+
+def moe_expert_scale(recv, expert_offsets, scale, y, stream=None):
+    """Stand-in expert (not a step of the method): y[r] = bf16(recv[r] * scale[expert of r])."""
+    lib = load_library()
+    cap_recv, H = recv.shape
+    E = scale.shape[0]
+    _check(lib.moe_expert_scale(_dev(recv, "recv", _BF16_TYPES, 2),
+                                _dev(expert_offsets, "expert_offsets", (torch.int32,)),
+                                _dev(scale, "scale", (torch.float32,)), E, H, cap_recv,
+                                _dev(y, "y", _BF16_TYPES, 2), _stream(stream)))
+
+
+def trace_enable(kernel_filter: str | None = None, max_records: int = 4096):
+    """Bracket this library's kernel launches (names containing kernel_filter) with CUDA events."""
+    lib = load_library()
+    _check(lib.moe_trace_enable(kernel_filter.encode() if kernel_filter else None, max_records))
+
+
+def trace_disable():
+    load_library().moe_trace_disable()
+
+
+def trace_reset():
+    load_library().moe_trace_reset()
+
+
+def trace_records() -> list[tuple[str, float]]:
+    """(kernel name, milliseconds) of every traced launch since enable/reset (waits for them)."""
+    lib = load_library()
+    out = []
+    name = ctypes.c_char_p()
+    ms = ctypes.c_float()
+    for i in range(lib.moe_trace_count()):
+        _check(lib.moe_trace_get(i, ctypes.byref(name), ctypes.byref(ms)))
+        out.append((name.value.decode(), float(ms.value)))
+    return out
+
+
+class MoePath:
+    """Device buffers for one shape plus the five calls in order.
+
+    Buffers are allocated once (worst-case capacities, fixed addresses), so a
+    step enqueues kernels only and can be captured in a CUDA graph.
+    """
+
+    def __init__(self, S, T, H, E, k, P, recv_part=-1, align=1, cap_send=None, cap_recv=None,
+                 device="cuda"):
+        self.S, self.T, self.H, self.E, self.k, self.P = S, T, H, E, k, P
+        self.recv_part, self.align = recv_part, align
+        self.cap_send = T * min(k, P) if cap_send is None else cap_send
+        self.cap_recv = S * T * k + E * (align - 1) if cap_recv is None else cap_recv
+        d = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=d)
+        self.topk_ids = torch.empty((S, T, k), **i32)
+        self.topk_w = torch.empty((S, T, k), dtype=torch.float32, device=d)
+        self.expert_counts = torch.empty((S, E), **i32)
+        self.part_counts = torch.empty((S, P), **i32)
+        self.part_offsets = torch.empty((S, P + 1), **i32)
+        self.token_slot = torch.empty((S, T, P), **i32)
+        self.send = torch.empty((S, self.cap_send, H), dtype=torch.bfloat16, device=d)
+        self.send_src = torch.empty((S, self.cap_send), **i32)
+        self.recv = torch.empty((self.cap_recv, H), dtype=torch.bfloat16, device=d)
+        self.expert_offsets = torch.empty((E + 1,), **i32)
+        self.pair_row = torch.empty((S, T, k), **i32)
+        self.recv_pair = torch.empty((self.cap_recv,), **i32)
+        self.out = torch.empty((S, T, H), dtype=torch.bfloat16, device=d)
+        ws = moe_workspace_bytes(S, T, k, E, P)
+        self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=d)
+        self.dev_status = torch.zeros((1,), **i32)
+        self.y = None
+
+    def route(self, logits, stream=None):
+        moe_route_topk(logits, self.topk_ids, self.topk_w, stream)
+
+    def dispatch(self, x, stream=None):
+        """layout + pack + permute (the receiver's copy epilogue is part of dispatch)."""
+        moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts, self.part_counts,
+                            self.part_offsets, self.token_slot, self.ws, self.dev_status, stream)
+        moe_dispatch_pack(x, self.token_slot, self.part_offsets, self.send, self.send_src,
+                          self.dev_status, stream)
+        moe_permute_to_experts(self.send, self.token_slot, self.topk_ids, self.E, self.recv_part,
+                               self.align, self.recv, self.expert_offsets, self.pair_row,
+                               self.recv_pair, self.ws, self.dev_status, stream)
+
+    def expert(self, scale, stream=None):
+        if self.y is None:
+            self.y = torch.empty_like(self.recv)
+        moe_expert_scale(self.recv, self.expert_offsets, scale, self.y, stream)
+        return self.y
+
+    def combine(self, y=None, stream=None):
+        moe_combine(self.recv if y is None else y, self.pair_row, self.topk_w, self.out,
+                    self.dev_status, stream)
+
+    def step(self, logits, x, scale=None, stream=None):
+        """route -> layout -> pack -> permute -> [stand-in expert] -> combine; returns out."""
+        self.route(logits, stream)
+        self.dispatch(x, stream)
+        y = self.expert(scale, stream) if scale is not None else None
+        self.combine(y, stream)
+        return self.out
+
+    def launches_per_step(self, with_expert=False) -> int:
+        """Kernels one step enqueues (route 1, layout 3 or 1, pack 1, permute 4, combine 1)."""
+        layout = 3 if self.T > 0 else 1
+        n = 1 + layout + 1 + 4 + 1
+        return n + (1 if with_expert else 0)

@@ -1,0 +1,255 @@
+// api.cu -- the extern "C" entry points of libmoeroute.so: argument checks,
+// error reporting, then the launchers of the kernel families.
+//
+// Nothing here allocates, frees or synchronises; a rejected call enqueues
+// nothing on the stream.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+moe_status_t fail(moe_status_t code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+moe_status_t cuda_status(cudaError_t e, const char *where)
+{
+    if (e == cudaSuccess) {
+        g_msg[0] = '\0';
+        return MOE_OK;
+    }
+    return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+#define REQUIRE(cond, ...)                                         \
+    do {                                                           \
+        if (!(cond)) return fail(MOE_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+
+// An array of `count` elements: non-null and aligned unless it is empty.
+#define REQUIRE_ARR(p, count, a)                                                             \
+    do {                                                                                     \
+        if ((int64_t)(count) > 0) {                                                          \
+            REQUIRE((p) != nullptr, "%s: null pointer `%s`", __func__, #p);                  \
+            REQUIRE(aligned((p), (a)), "%s: `%s` is not %d-byte aligned", __func__, #p, (int)(a)); \
+        }                                                                                    \
+    } while (0)
+// The optional device status word.
+#define REQUIRE_STATUS(p) \
+    REQUIRE(aligned((p), 4), "%s: `%s` is not 4-byte aligned", __func__, #p)
+
+moe_status_t check_sizes(const char *fn, int S, int T, int k, int E, int P)
+{
+    REQUIRE(S >= 1, "%s: S=%d must be >= 1", fn, S);
+    REQUIRE(T >= 0, "%s: T=%d must be >= 0", fn, T);
+    REQUIRE(k >= 1 && k <= kMaxK, "%s: k=%d must be in [1, %d]", fn, k, kMaxK);
+    REQUIRE(E >= k && E <= kMaxE, "%s: E=%d must be in [k=%d, %d]", fn, E, k, kMaxE);
+    REQUIRE(P >= 1 && P <= kMaxP, "%s: P=%d must be in [1, %d]", fn, P, kMaxP);
+    REQUIRE(E % P == 0, "%s: E=%d must be a multiple of P=%d", fn, E, P);
+    REQUIRE((int64_t)S * T * k < ((int64_t)1 << 31), "%s: S*T*k must be < 2^31", fn);
+    REQUIRE((int64_t)S * T * P < ((int64_t)1 << 31), "%s: S*T*P must be < 2^31", fn);
+    return MOE_OK;
+}
+
+}  // namespace
+
+cudaError_t device_info(DeviceInfo *out)
+{
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DeviceInfo d{};
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&d.max_smem_optin,
+                                        cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess)
+            return e;
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return 10000; }
+
+const char *moe_status_string(moe_status_t code)
+{
+    switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_CAPACITY: return "capacity exceeded";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id out of range";
+    case MOE_ERR_TIMEOUT: return "timeout";
+    case MOE_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+const char *moe_last_error_message(void) { return g_msg; }
+
+size_t moe_workspace_bytes(int S, int T, int k, int E, int P)
+{
+    if (check_sizes("moe_workspace_bytes", S, T, k, E, P) != MOE_OK) return 0;
+    const size_t a = layout_ws_bytes(S, T, E, P);
+    const size_t b = permute_ws_bytes(S, T, E);
+    return a > b ? a : b;
+}
+
+moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k, int32_t *topk_ids,
+                            float *topk_w, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, k, E, 1);
+    if (st != MOE_OK) return st;
+    REQUIRE((int64_t)S * T * E < ((int64_t)1 << 40), "%s: S*T*E too large", __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(logits, NT * E, 4);
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(topk_w, NT * k, 4);
+    return cuda_status(launch_route_topk(logits, (int64_t)S * T, E, k, topk_ids, topk_w, stream),
+                       __func__);
+}
+
+moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, int E, int P,
+                                 int32_t *expert_counts, int32_t *part_counts,
+                                 int32_t *part_offsets, int32_t *token_slot, void *ws,
+                                 size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(expert_counts, (int64_t)S * E, 4);
+    REQUIRE_ARR(part_counts, (int64_t)S * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_STATUS(dev_status);
+    const size_t need = moe_workspace_bytes(S, T, k, E, P);
+    REQUIRE_ARR(ws, need, 256);
+    REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
+    return cuda_status(launch_dispatch_layout(topk_ids, S, T, k, E, P, expert_counts, part_counts,
+                                              part_offsets, token_slot, ws, dev_status, stream),
+                       __func__);
+}
+
+moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
+                               const int32_t *token_slot, const int32_t *part_offsets,
+                               int cap_send, uint16_t *send, int32_t *send_src,
+                               uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(x, NT * H, 16);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(send, (int64_t)S * cap_send * H, 16);
+    REQUIRE_ARR(send_src, (int64_t)S * cap_send, 4);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(launch_dispatch_pack(x, S, T, H, P, token_slot, part_offsets, cap_send,
+                                            send, send_src, dev_status, stream),
+                       __func__);
+}
+
+moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
+                                    const int32_t *topk_ids, int S, int T, int k, int E, int P,
+                                    int H, int recv_part, int align, int cap_send, int cap_recv,
+                                    uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
+                                    int32_t *recv_pair, void *ws, size_t ws_bytes,
+                                    uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, P)", __func__,
+            recv_part);
+    REQUIRE(align >= 1 && align <= 1024, "%s: align=%d must be in [1, 1024]", __func__, align);
+    REQUIRE(cap_send >= 0 && cap_recv >= 0, "%s: capacities must be >= 0", __func__);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    REQUIRE((int64_t)S * T * k + (int64_t)E * (align - 1) < ((int64_t)1 << 31),
+            "%s: S*T*k + E*(align-1) must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(send, (int64_t)S * cap_send * H, 16);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(recv, (int64_t)cap_recv * H, 16);
+    REQUIRE_ARR(expert_offsets, E + 1, 4);
+    REQUIRE_ARR(pair_row, NT * k, 4);
+    REQUIRE_ARR(recv_pair, cap_recv, 4);
+    REQUIRE_STATUS(dev_status);
+    const size_t need = moe_workspace_bytes(S, T, k, E, P);
+    REQUIRE_ARR(ws, need, 256);
+    REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
+    return cuda_status(launch_permute(send, token_slot, topk_ids, S, T, k, E, P, H, recv_part,
+                                      align, cap_send, cap_recv, recv, expert_offsets, pair_row,
+                                      recv_pair, ws, dev_status, stream),
+                       __func__);
+}
+
+moe_status_t moe_combine(const uint16_t *y, int y_rows, const int32_t *pair_row,
+                         const float *topk_w, int S, int T, int k, int H, uint16_t *out,
+                         uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, k, k, 1);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(y_rows >= 0, "%s: y_rows=%d must be >= 0", __func__, y_rows);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(y, (int64_t)y_rows * H, 16);
+    REQUIRE_ARR(pair_row, NT * k, 4);
+    REQUIRE_ARR(topk_w, NT * k, 4);
+    REQUIRE_ARR(out, NT * H, 16);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(
+        launch_combine(y, y_rows, pair_row, topk_w, NT, k, H, out, dev_status, stream), __func__);
+}
+
+moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
+                              const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                              cudaStream_t stream)
+{
+    REQUIRE(E >= 1 && E <= kMaxE, "%s: E=%d must be in [1, %d]", __func__, E, kMaxE);
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(cap_recv >= 0, "%s: cap_recv=%d must be >= 0", __func__, cap_recv);
+    REQUIRE_ARR(recv, (int64_t)cap_recv * H, 16);
+    REQUIRE_ARR(expert_offsets, E + 1, 4);
+    REQUIRE_ARR(scale, E, 4);
+    REQUIRE_ARR(y, (int64_t)cap_recv * H, 16);
+    return cuda_status(
+        launch_expert_scale(recv, expert_offsets, scale, E, H, cap_recv, y, stream), __func__);
+}
+
+}  // extern "C"

@@ -1,0 +1,202 @@
+// combine.cu -- weighted combine back to token order, and the stand-in expert.
+//
+// a2a-backends page (vincentzed.com/writing/a2a-backends), section 1.1 (the MoE
+// output of a token is the sum of its experts' outputs, each multiplied by its
+// router weight), section 7.1 (the home GPU adds the returned rows in 32-bit
+// floats) and section 7.2 (combine travels as bf16).
+//
+// One warp per (token, 1 KiB column segment): the lanes gather the segment of
+// each of the token's k expert rows (up to 8 rows, 16 loads of 16 bytes per
+// lane in flight), accumulate weight * value with fp32 FMAs in j order, round
+// once to bf16 and stream the result out.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "trace.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCombUnroll = 2;                  // int4 (8 bf16) per lane per segment
+constexpr int kCombSegVec = 32 * kCombUnroll;   // int4 per segment (1 KiB)
+constexpr int kCombBatch = 8;                   // rows whose loads are issued together
+constexpr int kCombThreads = 256;
+
+__device__ __forceinline__ void fma_bf16x8(float *acc, int4 v, float w)
+{
+    const uint32_t u[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float lo = __uint_as_float(u[i] << 16);
+        const float hi = __uint_as_float(u[i] & 0xffff0000u);
+        acc[2 * i] = fmaf(w, lo, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, hi, acc[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ int4 pack_bf16x8(const float *a)
+{
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+        u[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_int4((int)u[0], (int)u[1], (int)u[2], (int)u[3]);
+}
+
+__global__ void __launch_bounds__(kCombThreads) k_combine(const int4 *__restrict__ y, int y_rows,
+                                                          const int32_t *__restrict__ pair_row,
+                                                          const float *__restrict__ w,
+                                                          int64_t N, int k, int V,
+                                                          int4 *__restrict__ out,
+                                                          uint32_t *dev_status)
+{
+    bool bad_row = false;
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    const int64_t ntask = N * nseg;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
+         task += gwarps) {
+        const int64_t n = task / nseg;
+        const int g = (int)(task - n * nseg);
+        int pr = -1;
+        float wj = 0.f;
+        if (lane < k) {
+            pr = __ldg(pair_row + n * k + lane);
+            wj = __ldg(w + n * k + lane);
+            if (pr >= y_rows) {
+                if (g == 0) bad_row = true;
+                pr = -1;
+            }
+        }
+        unsigned vmask = __ballot_sync(kFull, pr >= 0);
+        const int v0 = g * kCombSegVec + lane;
+        float acc[8 * kCombUnroll];
+#pragma unroll
+        for (int i = 0; i < 8 * kCombUnroll; i++) acc[i] = 0.f;
+
+        while (vmask) {
+            // issue the loads of up to kCombBatch rows, then accumulate in j order
+            int4 r[kCombBatch][kCombUnroll];
+            float wb[kCombBatch];
+            int nb = 0;
+#pragma unroll
+            for (int b = 0; b < kCombBatch; b++) {
+                if (vmask) {
+                    const int j = __ffs(vmask) - 1;
+                    vmask &= vmask - 1;
+                    const int row = __shfl_sync(kFull, pr, j);
+                    wb[b] = __shfl_sync(kFull, wj, j);
+                    const int4 *src = y + (int64_t)row * V;
+#pragma unroll
+                    for (int u = 0; u < kCombUnroll; u++) {
+                        const int vi = v0 + 32 * u;
+                        r[b][u] = (vi < V) ? ld_stream(src + vi) : make_int4(0, 0, 0, 0);
+                    }
+                    nb = b + 1;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kCombBatch; b++) {
+                if (b < nb) {
+#pragma unroll
+                    for (int u = 0; u < kCombUnroll; u++) fma_bf16x8(acc + 8 * u, r[b][u], wb[b]);
+                }
+            }
+        }
+        int4 *dst = out + n * V;
+#pragma unroll
+        for (int u = 0; u < kCombUnroll; u++) {
+            const int vi = v0 + 32 * u;
+            if (vi < V) st_stream(dst + vi, pack_bf16x8(acc + 8 * u));
+        }
+    }
+    if (bad_row) flag_status(dev_status, MOE_ERR_INVALID_ARG);
+}
+
+// Stand-in expert: one warp per (row, 2 KiB segment); expert of the row by
+// binary search over the run starts.
+__global__ void __launch_bounds__(256) k_expert_scale(const int4 *__restrict__ recv,
+                                                      const int32_t *__restrict__ expert_offsets,
+                                                      const float *__restrict__ scale, int E,
+                                                      int V, int cap_recv,
+                                                      int4 *__restrict__ y)
+{
+    extern __shared__ int off[];  // [E + 1]
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = __ldg(expert_offsets + i);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int rows = off[E] < cap_recv ? off[E] : cap_recv;
+    const int nseg = (V + 127) / 128;
+    const int64_t ntask = (int64_t)rows * nseg;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
+         task += gwarps) {
+        const int row = (int)(task / nseg);
+        const int g = (int)(task - (int64_t)row * nseg);
+        int lo = 0, hi = E - 1;  // last e with off[e] <= row
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= row) lo = mid;
+            else hi = mid - 1;
+        }
+        const float sc = __ldg(scale + lo);
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int vi = g * 128 + u * 32 + lane;
+            if (vi < V) {
+                const int4 v = recv[(int64_t)row * V + vi];
+                float a[8];
+                const uint32_t uu[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    a[2 * i] = __uint_as_float(uu[i] << 16) * sc;
+                    a[2 * i + 1] = __uint_as_float(uu[i] & 0xffff0000u) * sc;
+                }
+                y[(int64_t)row * V + vi] = pack_bf16x8(a);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_row, const float *w,
+                           int64_t N, int k, int H, uint16_t *out, uint32_t *dev_status,
+                           cudaStream_t st)
+{
+    if (N == 0) return cudaSuccess;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int V = H / 8;
+    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    const int64_t warps = N * nseg;
+    int64_t blocks = (warps + (kCombThreads / 32) - 1) / (kCombThreads / 32);
+    const int64_t wave = (int64_t)di.sm_count * (2048 / kCombThreads);
+    if (blocks > wave) blocks = wave;
+    MOE_TRACED_LAUNCH("k_combine", st,
+                      k_combine<<<(unsigned)blocks, kCombThreads, 0, st>>>(
+                          (const int4 *)y, y_rows, pair_row, w, N, k, V, (int4 *)out, dev_status));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
+                                const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                                cudaStream_t st)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int blocks = di.sm_count * 8;
+    MOE_TRACED_LAUNCH("k_expert_scale", st,
+                      k_expert_scale<<<blocks, 256, (size_t)(E + 1) * sizeof(int), st>>>(
+                          (const int4 *)recv, expert_offsets, scale, E, H / 8, cap_recv, (int4 *)y));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,51 @@
+// launch.h -- internal launchers (one per kernel family); arguments are
+// validated by api.cu before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Per-device launch geometry, queried once per device.
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;
+};
+cudaError_t device_info(DeviceInfo *out);
+
+cudaError_t launch_route_topk(const float *logits, int64_t N, int E, int k, int32_t *ids,
+                              float *w, cudaStream_t st);
+
+struct LayoutWs {
+    int32_t *pc;    // [S][P][C] per-chunk partition counts, then chunk bases
+    int32_t *ec;    // [S][E][C] per-chunk expert counts
+};
+size_t layout_ws_bytes(int S, int T, int E, int P);
+cudaError_t launch_dispatch_layout(const int32_t *ids, int S, int T, int k, int E, int P,
+                                   int32_t *expert_counts, int32_t *part_counts,
+                                   int32_t *part_offsets, int32_t *token_slot, void *ws,
+                                   uint32_t *dev_status, cudaStream_t st);
+
+cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
+                                 const int32_t *token_slot, const int32_t *part_offsets,
+                                 int cap_send, uint16_t *send, int32_t *send_src,
+                                 uint32_t *dev_status, cudaStream_t st);
+
+size_t permute_ws_bytes(int S, int T, int E);
+cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, const int32_t *ids,
+                           int S, int T, int k, int E, int P, int H, int recv_part, int align,
+                           int cap_send, int cap_recv, uint16_t *recv, int32_t *expert_offsets,
+                           int32_t *pair_row, int32_t *recv_pair, void *ws,
+                           uint32_t *dev_status, cudaStream_t st);
+
+cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_row, const float *w,
+                           int64_t N, int k, int H, uint16_t *out, uint32_t *dev_status,
+                           cudaStream_t st);
+
+cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
+                                const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                                cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,107 @@
+// pack.cu -- sender side of dispatch: bit copies of bf16 rows into the send
+// region of every partition that needs the token.
+//
+// a2a-backends page (vincentzed.com/writing/a2a-backends), section 3.2 (fourth
+// step: the rows move), section 5.1 (a region per sender, rows written straight
+// into place) and section 6.1 (one copy per GPU that needs the token).
+//
+// Work unit: one warp per (token, 2 KiB column segment).  The warp reads the
+// segment of x once (16-byte vectors, four per lane in flight) and stores it
+// to each of the token's c <= min(k, P) destination rows.  HBM traffic is the
+// minimum: x read once, c copies written.
+#include "common.cuh"
+#include "launch.h"
+#include "trace.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kPackUnroll = 4;                   // int4 per lane per segment
+constexpr int kPackSegVec = 32 * kPackUnroll;    // int4 per segment (2 KiB)
+constexpr int kPackThreads = 256;
+
+__global__ void __launch_bounds__(kPackThreads) k_pack(const int4 *__restrict__ x, int S, int T,
+                                                       int V, int P,
+                                                       const int32_t *__restrict__ token_slot,
+                                                       const int32_t *__restrict__ part_offsets,
+                                                       int cap_send, int4 *__restrict__ send,
+                                                       int32_t *__restrict__ send_src,
+                                                       uint32_t *dev_status)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+
+    // rows of send_src past the last used row of each source
+    for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
+        const int s = (int)(i / cap_send);
+        const int r = (int)(i - (int64_t)s * cap_send);
+        if (r >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) send_src[i] = -1;
+    }
+
+    const int nseg = (V + kPackSegVec - 1) / kPackSegVec;
+    const int64_t ntask = (int64_t)S * T * nseg;
+    const int64_t gwarps = gthreads >> 5;
+    bool overflow = false;
+    for (int64_t task = gtid >> 5; task < ntask; task += gwarps) {
+        const int64_t n = task / nseg;          // token index s*T + t
+        const int g = (int)(task - n * nseg);   // column segment
+        const int s = (int)(n / T);
+        int slot = -1;
+        if (lane < P) slot = __ldg(token_slot + n * P + lane);
+        const bool ok = slot >= 0 && slot < cap_send;
+        if (slot >= cap_send) overflow = true;
+        unsigned dmask = __ballot_sync(kFull, ok);
+        if (g == 0 && ok) send_src[(int64_t)s * cap_send + slot] = (int32_t)(n - (int64_t)s * T);
+        if (dmask == 0) continue;
+
+        const int4 *src = x + n * V;
+        const int v0 = g * kPackSegVec + lane;
+        int4 r[kPackUnroll];
+#pragma unroll
+        for (int u = 0; u < kPackUnroll; u++) {
+            const int vi = v0 + 32 * u;
+            if (vi < V) r[u] = ld_stream(src + vi);
+        }
+        while (dmask) {
+            const int p = __ffs(dmask) - 1;
+            dmask &= dmask - 1;
+            const int sl = __shfl_sync(kFull, slot, p);
+            int4 *dst = send + ((int64_t)s * cap_send + sl) * V;
+#pragma unroll
+            for (int u = 0; u < kPackUnroll; u++) {
+                const int vi = v0 + 32 * u;
+                if (vi < V) st_cg(dst + vi, r[u]);
+            }
+        }
+    }
+    if (__any_sync(kFull, overflow) && lane == 0) flag_status(dev_status, MOE_ERR_CAPACITY);
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
+                                 const int32_t *token_slot, const int32_t *part_offsets,
+                                 int cap_send, uint16_t *send, int32_t *send_src,
+                                 uint32_t *dev_status, cudaStream_t st)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int V = H / 8;
+    const int nseg = (V + kPackSegVec - 1) / kPackSegVec;
+    const int64_t warps = (int64_t)S * T * nseg;
+    const int64_t want = (warps + (kPackThreads / 32) - 1) / (kPackThreads / 32);
+    int64_t blocks = (int64_t)di.sm_count * (2048 / kPackThreads);
+    if (want < blocks) blocks = want;
+    const int64_t tail_blocks = ((int64_t)S * cap_send + kPackThreads - 1) / kPackThreads;
+    if (blocks < 1) blocks = tail_blocks < 1 ? 1 : (tail_blocks < di.sm_count ? tail_blocks : di.sm_count);
+    MOE_TRACED_LAUNCH("k_pack", st,
+                      k_pack<<<(unsigned)blocks, kPackThreads, 0, st>>>(
+                          (const int4 *)x, S, T, V, P, token_slot, part_offsets, cap_send,
+                          (int4 *)send, send_src, dev_status));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,116 @@
+// route.cu -- top-k routing: router logits -> expert ids + renormalised weights.
+//
+// a2a-backends page (vincentzed.com/writing/a2a-backends), section 1.1: for
+// every token the router produces the ids of the chosen experts and one weight
+// per expert.  Chosen: the k largest logits, in descending order, equal logits
+// resolved to the lower id.  Weights: softmax over the k chosen logits in fp32.
+//
+// One warp per token row.  Lane l holds logits l, l+32, l+64, ... in registers
+// (coalesced 128-byte loads); k rounds of a warp arg-max (value desc, id asc)
+// pick the experts; the winning lane retires its element.
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "trace.h"
+
+namespace moe {
+
+template <int VPL>
+__global__ void __launch_bounds__(256) k_route_topk(const float *__restrict__ logits, int64_t N,
+                                                    int E, int k, int32_t *__restrict__ ids,
+                                                    float *__restrict__ w)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t n = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (n >= N) return;  // uniform per warp
+    const float *row = logits + n * E;
+
+    float v[VPL];
+    unsigned live = 0;  // bit i: element lane+32i is in range and not yet chosen
+#pragma unroll
+    for (int i = 0; i < VPL; i++) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+            v[i] = __ldcs(row + e);
+            live |= 1u << i;
+        } else {
+            v[i] = -INFINITY;
+        }
+    }
+
+    float my_v = 0.f;
+    int my_id = -1;
+    for (int r = 0; r < k; r++) {
+        // best live element of this lane; ids ascend with i, so a strict
+        // comparison keeps the lowest id among equal values
+        float bv = -INFINITY;
+        int bi = INT_MAX, bslot = -1;
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            if ((live >> i) & 1u) {
+                if (bslot < 0 || v[i] > bv) {
+                    bv = v[i];
+                    bi = lane + 32 * i;
+                    bslot = i;
+                }
+            }
+        }
+        float wv = bv;
+        int wi = bi;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, wv, off);
+            const int oi = __shfl_xor_sync(kFull, wi, off);
+            if (ov > wv || (ov == wv && oi < wi)) {
+                wv = ov;
+                wi = oi;
+            }
+        }
+        if (bslot >= 0 && wi == bi) live &= ~(1u << bslot);
+        if (lane == r) {
+            my_v = wv;
+            my_id = wi;
+        }
+    }
+
+    // softmax over the k chosen logits: lane j < k holds choice j
+    const float lmax = __shfl_sync(kFull, my_v, 0);
+    const float ex = (lane < k) ? expf(my_v - lmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < k) {
+        ids[n * k + lane] = my_id;
+        w[n * k + lane] = ex / sum;
+    }
+}
+
+cudaError_t launch_route_topk(const float *logits, int64_t N, int E, int k, int32_t *ids,
+                              float *w, cudaStream_t st)
+{
+    if (N == 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    const unsigned blocks = (unsigned)((N + warps_per_block - 1) / warps_per_block);
+    const int vpl = (E + 31) / 32;
+#define MOE_ROUTE_CASE(V)                                                              \
+    if (vpl <= V) {                                                                    \
+        MOE_TRACED_LAUNCH("k_route_topk", st,                                            \
+            k_route_topk<V><<<blocks, warps_per_block * 32, 0, st>>>(logits, N, E, k, ids, w)); \
+        return cudaGetLastError();                                                     \
+    }
+    MOE_ROUTE_CASE(1)
+    MOE_ROUTE_CASE(2)
+    MOE_ROUTE_CASE(4)
+    MOE_ROUTE_CASE(8)
+    MOE_ROUTE_CASE(12)
+    MOE_ROUTE_CASE(16)
+    MOE_ROUTE_CASE(24)
+    MOE_ROUTE_CASE(32)
+#undef MOE_ROUTE_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

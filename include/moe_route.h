@@ -1,0 +1,237 @@
+/*
+ * moe_route.h -- C ABI of the GB300 MoE token-path library (libmoeroute.so).
+ *
+ * The library implements, on one GPU, the data-parallel hot path of
+ * expert-parallel MoE serving as described on the a2a-backends page
+ * (vincentzed.com/writing/a2a-backends):
+ *
+ *   moe_route_topk          router logits -> top-k expert ids + weights      (section 1.1)
+ *   moe_dispatch_layout     per-expert / per-partition counts, one copy per
+ *                           destination partition, prefix-sum layout        (sections 1.3, 3.2)
+ *   moe_dispatch_pack       bf16 rows -> per-partition send regions          (sections 3.2, 5.1, 6.1)
+ *   moe_permute_to_experts  receiver side: rows -> expert-contiguous runs    (sections 1.5, 3.3, 5.1)
+ *   moe_combine             weighted sum of expert outputs back in token
+ *                           order, fp32 accumulation, bf16 out               (sections 7.1, 7.2)
+ *
+ * Expert-parallel ranks are emulated as partitions of buffers in one GPU's
+ * memory: partition p holds the L = E/P experts p*L .. p*L+L-1 (contiguous
+ * blocks, section 2.1 of the same page).  There is no peer traffic.
+ *
+ * Conventions for every call
+ * --------------------------
+ * - All array pointers are DEVICE pointers into memory the caller owns.  The
+ *   library never allocates, frees or synchronises; every call is enqueued
+ *   on `stream` and returns without waiting, so a chain of calls can be
+ *   captured in a CUDA graph (fixed shapes, fixed addresses, no host reads of
+ *   device counts -- section 1.4 of the page).
+ * - bf16 arrays are passed as uint16_t bit patterns.  Row-major throughout.
+ *   bf16 row arrays (x, send, recv, y, out) must be 16-byte aligned and H must
+ *   be a multiple of 8 (rows are moved in 16-byte vectors).  int32/float
+ *   arrays must be 4-byte aligned.
+ * - Sizes: S >= 1 sources (emulated sending ranks), T >= 0 tokens per source,
+ *   1 <= k <= 32 experts per token, k <= E <= 1024 experts, 1 <= P <= 32
+ *   partitions with E % P == 0, H >= 8, S*T*k < 2^31, row counts < 2^31.
+ *   T == 0 is a valid call that only writes the count/offset outputs.
+ * - Expert ids < 0 mean "not routed": no copy is made and the slot adds
+ *   nothing to the combine (section 2.1, the -1 convention; section 6.3).
+ * - Host return value: MOE_OK, MOE_ERR_INVALID_ARG (bad pointer, size or
+ *   alignment -- nothing is enqueued) or MOE_ERR_CUDA (a launch failed).
+ *   moe_last_error_message() describes the last non-OK return of the
+ *   calling thread.
+ * - Data errors are found on the device and OR-ed into the caller's
+ *   `dev_status` word (device pointer to one uint32_t) as MOE_STATUS_BIT(code):
+ *     MOE_STATUS_BIT(MOE_ERR_INVALID_ARG)   an index input is inconsistent
+ *                                           (a routed pair whose token has no
+ *                                           slot in its partition)
+ *     MOE_STATUS_BIT(MOE_ERR_CAPACITY)      a row did not fit under cap_send or
+ *                                           cap_recv; it was dropped, never
+ *                                           written out of bounds (section 4.3,
+ *                                           9.2: the cap)
+ *     MOE_STATUS_BIT(MOE_ERR_BAD_EXPERT_ID) an id >= E was skipped
+ *   The library only sets bits; the caller clears the word when it wants.
+ *   `dev_status` may be NULL, in which case data errors are not reported.
+ * - Results are deterministic: the same inputs give the same bytes.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_CAPACITY = 2,
+    MOE_ERR_BAD_EXPERT_ID = 3,
+    MOE_ERR_TIMEOUT = 4,
+    MOE_ERR_CUDA = 5
+} moe_status_t;
+
+#define MOE_STATUS_BIT(code) (1u << (code))
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int moe_version(void);
+
+/* Static description of a status code ("ok", "invalid argument", ...). */
+const char *moe_status_string(moe_status_t code);
+
+/* Human-readable reason for the calling thread's last non-OK return
+ * ("" if none).  The string is owned by the library and valid until the
+ * thread's next call. */
+const char *moe_last_error_message(void);
+
+/*
+ * Scratch bytes that moe_dispatch_layout and moe_permute_to_experts need for
+ * the given sizes (the larger of the two).  The caller allocates it (any
+ * device memory, 256-byte aligned) and may reuse it across calls that are
+ * ordered on one stream.  Returns 0 for invalid sizes.
+ */
+size_t moe_workspace_bytes(int S, int T, int k, int E, int P);
+
+/*
+ * Top-k routing (a2a-backends section 1.1: the router gives each token the
+ * ids of its chosen experts and one weight per expert).
+ *   logits  [S][T][E] float32, finite.
+ *   topk_ids[S][T][k] int32 out: the k largest logits of the row in
+ *           descending order; equal logits go to the lower expert id.
+ *   topk_w  [S][T][k] float32 out: softmax over the k chosen logits,
+ *           w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max), computed in fp32.
+ */
+moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k,
+                            int32_t *topk_ids, float *topk_w, cudaStream_t stream);
+
+/*
+ * Dispatch layout (a2a-backends section 1.3, third answer, and section 3.2,
+ * first step: the set of GPUs that hold at least one of a token's experts
+ * and the number of rows each GPU gets).
+ *   topk_ids      [S][T][k] int32 in.
+ *   expert_counts [S][E]    int32 out: pairs (t, j) routed to expert e.
+ *   part_counts   [S][P]    int32 out: tokens with >= 1 expert in partition p
+ *                           (one de-duplicated copy per token and partition).
+ *   part_offsets  [S][P+1]  int32 out: exclusive prefix sum of part_counts;
+ *                           part_offsets[s][P] = copies of source s.
+ *   token_slot    [S][T][P] int32 out: row of token t in source s's send
+ *                           buffer for partition p, or -1.  Within a
+ *                           partition's region rows are in ascending token
+ *                           order: token_slot = part_offsets[s][p] +
+ *                           #{t' < t : t' needs p}.
+ *   ws, ws_bytes  scratch, ws_bytes >= moe_workspace_bytes(S, T, k, E, P).
+ *   dev_status    device uint32 status word (bad ids).
+ * Counting is atomic-free (warp ballots and match groups, block scans).
+ */
+moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, int E, int P,
+                                 int32_t *expert_counts, int32_t *part_counts,
+                                 int32_t *part_offsets, int32_t *token_slot,
+                                 void *ws, size_t ws_bytes, uint32_t *dev_status,
+                                 cudaStream_t stream);
+
+/*
+ * Pack (a2a-backends section 3.2, fourth step; section 5.1: a region for every
+ * sender, rows written straight into place; section 6.1: one copy per GPU
+ * that needs the token).
+ *   x            [S][T][H] bf16 in.
+ *   token_slot   [S][T][P] int32 in (from moe_dispatch_layout).
+ *   part_offsets [S][P+1]  int32 in (from moe_dispatch_layout).
+ *   cap_send     rows of send buffer per source; T*min(k,P) always suffices.
+ *   send         [S][cap_send][H] bf16 out: send[s][token_slot[s][t][p]] =
+ *                x[s][t] (bit copy) for every slot >= 0.  Rows at or beyond
+ *                part_offsets[s][P] are not written.
+ *   send_src     [S][cap_send] int32 out: source token of each row; -1 for
+ *                rows at or beyond part_offsets[s][P].
+ *   Slots >= cap_send are dropped and flag MOE_ERR_CAPACITY.
+ */
+moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
+                               const int32_t *token_slot, const int32_t *part_offsets,
+                               int cap_send, uint16_t *send, int32_t *send_src,
+                               uint32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Receiver permute into expert-contiguous runs (a2a-backends section 1.5:
+ * the contiguous layout, runs optionally padded to a multiple of `align`
+ * rows as DeepGEMM wants 128; section 3.3: one row per (token, local
+ * expert); section 5.1: the copy epilogue with device-side offsets).
+ *   send, token_slot, topk_ids   as produced/consumed above; cap_send as in pack.
+ *   recv_part  receiving partition in [0, P), or -1 for all partitions.
+ *   align      run alignment in rows, 1 <= align <= 1024.
+ *   cap_recv   rows of recv; S*T*k + E*(align-1) always suffices.
+ *   recv       [cap_recv][H] bf16 out.  For each expert e of the receiving
+ *              set in ascending order, its run starts at expert_offsets[e]
+ *              and holds the pairs (s, t, j) with topk_ids[s][t][j] == e in
+ *              ascending (s, t, j) order, each a copy of
+ *              send[s][token_slot[s][t][e / L]]; padding rows are zero.
+ *              Rows at or beyond min(expert_offsets[E], cap_recv) are not
+ *              written.
+ *   expert_offsets [E+1] int32 out: run starts; experts outside the
+ *              receiving set have empty runs.  expert_offsets[E] = rows used
+ *              (may exceed cap_recv, then MOE_ERR_CAPACITY is flagged).
+ *   pair_row   [S][T][k] int32 out: recv row of each pair, or -1 (id < 0,
+ *              expert outside the receiving set, or row >= cap_recv).
+ *   recv_pair  [cap_recv] int32 out: (s*T + t)*k + j for pair rows, -1 for
+ *              padding rows and rows >= expert_offsets[E].
+ *   ws, ws_bytes  scratch, ws_bytes >= moe_workspace_bytes(S, T, k, E, P).
+ * A routed pair whose slot is -1 (inconsistent inputs) or >= cap_send gets a
+ * zero row and flags MOE_ERR_INVALID_ARG or MOE_ERR_CAPACITY respectively.
+ */
+moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
+                                    const int32_t *topk_ids, int S, int T, int k, int E,
+                                    int P, int H, int recv_part, int align, int cap_send,
+                                    int cap_recv, uint16_t *recv, int32_t *expert_offsets,
+                                    int32_t *pair_row, int32_t *recv_pair, void *ws,
+                                    size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Weighted combine (a2a-backends section 1.1: the MoE output is the sum of
+ * the chosen experts' outputs, each multiplied by its weight; section 7.1:
+ * the home side sums in 32-bit floats; section 7.2: bf16 on the wire).
+ *   y        [y_rows][H] bf16 in: expert outputs in the recv layout.
+ *   pair_row [S][T][k] int32 in (from moe_permute_to_experts); entries
+ *            >= y_rows are skipped and flag MOE_ERR_INVALID_ARG.
+ *   topk_w   [S][T][k] float32 in.
+ *   out      [S][T][H] bf16 out: out[s][t] = bf16_rne( sum over j in
+ *            ascending order with pair_row >= 0 of topk_w * float(y[row]) ),
+ *            accumulated with fp32 fused multiply-adds; +0 if no pair.
+ * With a single receiving partition this is that partition's partial
+ * (stage-1) combine; the partials of all partitions add up to the full one.
+ */
+moe_status_t moe_combine(const uint16_t *y, int y_rows, const int32_t *pair_row,
+                         const float *topk_w, int S, int T, int k, int H, uint16_t *out,
+                         uint32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Stand-in expert for tests and benchmarks -- NOT a step of the method (the
+ * pages time dispatch and combine without the expert kernel, a2a-backends
+ * section 8.1).  y[r] = bf16_rne(float(recv[r]) * scale[e]) for every row r
+ * of expert e's run, r < min(expert_offsets[E], cap_recv).
+ *   recv, y [cap_recv][H] bf16; expert_offsets [E+1] int32; scale [E] float32.
+ */
+moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
+                              const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                              cudaStream_t stream);
+
+/*
+ * Per-kernel timing (tracing aid; off by default).  While enabled, every
+ * kernel launch of this library whose name contains `kernel_filter` (all of
+ * them if NULL or "") is bracketed by two CUDA events recorded on the
+ * launch's stream, up to max_records launches.  moe_trace_enable creates the
+ * events (host handles only, no device memory) and clears earlier records;
+ * moe_trace_get(i) waits for record i to finish and returns the kernel name
+ * (static string) and its duration in ms.  Do not enable while a stream is
+ * being captured into a CUDA graph.
+ */
+moe_status_t moe_trace_enable(const char *kernel_filter, int max_records);
+void moe_trace_disable(void);
+void moe_trace_reset(void);
+int moe_trace_count(void);
+moe_status_t moe_trace_get(int i, const char **kernel_name, float *ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

@@ -1,0 +1,137 @@
+"""C ABI checks that need no GPU: the library loads, exports every function that
+include/moe_route.h declares, and its host-side validation rejects bad
+arguments before anything is enqueued (so these calls never reach CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_moe_route_06_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_route.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    m.build()
+    return m.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)) - {"MOE_STATUS_BIT"})
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for f in ("moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack",
+              "moe_permute_to_experts", "moe_combine", "moe_workspace_bytes"):
+        assert f in names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.moe_version() >= 10000
+    assert lib.moe_status_string(0) == b"ok"
+    assert lib.moe_status_string(2) == b"capacity exceeded"
+
+
+def test_workspace_bytes(lib):
+    assert m.moe_workspace_bytes(1, 4096, 6, 384, 8) > 0
+    assert m.moe_workspace_bytes(1, 4096, 6, 384, 8) % 256 == 0
+    assert m.moe_workspace_bytes(1, 8192, 6, 384, 8) >= m.moe_workspace_bytes(1, 4096, 6, 384, 8)
+    assert m.moe_workspace_bytes(1, 0, 6, 384, 8) > 0
+    assert m.moe_workspace_bytes(1, 16, 6, 385, 8) == 0       # E % P != 0
+    assert m.moe_workspace_bytes(0, 16, 6, 384, 8) == 0       # S < 1
+
+
+FAKE = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced: the calls are rejected first
+FAKE_MIS = ctypes.c_void_p((1 << 20) + 2)
+NULL = ctypes.c_void_p(0)
+ST = ctypes.c_void_p(0)
+
+
+def _msg(lib):
+    return lib.moe_last_error_message().decode()
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((FAKE, 0, 4, 16, 2, FAKE, FAKE, ST), "S=0"),
+    ((FAKE, 1, -1, 16, 2, FAKE, FAKE, ST), "T=-1"),
+    ((FAKE, 1, 4, 16, 0, FAKE, FAKE, ST), "k=0"),
+    ((FAKE, 1, 4, 16, 33, FAKE, FAKE, ST), "k=33"),
+    ((FAKE, 1, 4, 2, 3, FAKE, FAKE, ST), "E=2"),
+    ((FAKE, 1, 4, 2048, 3, FAKE, FAKE, ST), "E=2048"),
+    ((NULL, 1, 4, 16, 2, FAKE, FAKE, ST), "null pointer `logits`"),
+    ((FAKE, 1, 4, 16, 2, FAKE_MIS, FAKE, ST), "`topk_ids` is not 4-byte aligned"),
+])
+def test_route_rejects(lib, args, needle):
+    assert lib.moe_route_topk(*args) == m.MOE_ERR_INVALID_ARG
+    assert needle in _msg(lib)
+
+
+def test_layout_rejects(lib):
+    ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
+    good = [FAKE, 1, 64, 2, 16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, ws, FAKE, ST]
+    bad = list(good)
+    bad[5] = 3                                         # E % P != 0
+    assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "multiple of P" in _msg(lib)
+    bad = list(good)
+    bad[5] = 64
+    assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "P=64" in _msg(lib)
+    bad = list(good)
+    bad[11] = ws - 1                                   # workspace too small
+    assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "ws_bytes" in _msg(lib)
+    bad = list(good)
+    bad[10] = ctypes.c_void_p((1 << 20) + 16)          # workspace not 256-byte aligned
+    assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "`ws`" in _msg(lib)
+    bad = list(good)
+    bad[9] = NULL
+    assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "token_slot" in _msg(lib)
+
+
+def test_pack_rejects(lib):
+    good = [FAKE, 1, 64, 256, 4, FAKE, FAKE, 128, FAKE, FAKE, FAKE, ST]
+    bad = list(good)
+    bad[3] = 100                                       # H not a multiple of 8
+    assert lib.moe_dispatch_pack(*bad) == m.MOE_ERR_INVALID_ARG and "H=100" in _msg(lib)
+    bad = list(good)
+    bad[0] = ctypes.c_void_p((1 << 20) + 8)            # rows must be 16-byte aligned
+    assert lib.moe_dispatch_pack(*bad) == m.MOE_ERR_INVALID_ARG and "16-byte" in _msg(lib)
+    bad = list(good)
+    bad[7] = -1
+    assert lib.moe_dispatch_pack(*bad) == m.MOE_ERR_INVALID_ARG and "cap_send" in _msg(lib)
+
+
+def test_permute_rejects(lib):
+    ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
+    good = [FAKE, FAKE, FAKE, 1, 64, 2, 16, 4, 256, -1, 1, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE,
+            ws, FAKE, ST]
+    for idx, val, needle in ((9, 4, "recv_part"), (9, -2, "recv_part"), (10, 0, "align"),
+                             (10, 2048, "align"), (12, -3, "capacities"), (8, 4, "H=4")):
+        bad = list(good)
+        bad[idx] = val
+        assert lib.moe_permute_to_experts(*bad) == m.MOE_ERR_INVALID_ARG, needle
+        assert needle in _msg(lib)
+
+
+def test_combine_and_expert_scale_reject(lib):
+    assert lib.moe_combine(FAKE, 64, FAKE, FAKE, 1, 8, 2, 12, FAKE, NULL, ST) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(NULL, 64, FAKE, FAKE, 1, 8, 2, 16, FAKE, NULL, ST) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(FAKE, -1, FAKE, FAKE, 1, 8, 2, 16, FAKE, NULL, ST) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_scale(FAKE, FAKE, FAKE, 0, 16, 4, FAKE, ST) == m.MOE_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    # the product path has no fallback: a missing library is an error, not a CPU path
+    monkeypatch.setattr(m._build, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(m.MoeLibraryMissing):
+        m.load_library()
