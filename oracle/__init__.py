@@ -57,7 +57,7 @@ def _load():
             lib.oracle_expected_copies.argtypes = [i32, i32, i32]
             lib.oracle_expected_copies.restype = ctypes.c_double
             lib.oracle_route_topk.argtypes = [P, i64, i32, i32, P, P]
-            lib.oracle_dispatch_layout.argtypes = [P, i32, i64, i32, i32, i32, P, P, P, P, P]
+            lib.oracle_dispatch_layout.argtypes = [P, i32, i64, i32, i32, i32, P, P, P, P, P, P]
             lib.oracle_dispatch_pack.argtypes = [P, i32, i64, i32, i32, P, i64, P, P, P]
             lib.oracle_permute_to_experts.argtypes = [P, P, P, i32, i64, i32, i32, i32, i32,
                                                       i32, i32, i64, i64, P, P, P, P, P]
@@ -106,18 +106,19 @@ def route_topk(logits: np.ndarray, k: int):
 
 
 def dispatch_layout(ids: np.ndarray, E: int, P: int) -> dict:
-    """ids int32 [S, T, k] -> expert_counts, part_counts, part_offsets, token_slot, status."""
+    """ids int32 [S, T, k] -> expert_counts, expert_rank, part_counts, part_offsets, token_slot, status."""
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     S, T, k = ids.shape
     out = {
         "expert_counts": np.empty((S, E), np.int32),
+        "expert_rank": np.empty((S, T, k), np.int32),
         "part_counts": np.empty((S, P), np.int32),
         "part_offsets": np.empty((S, P + 1), np.int32),
         "token_slot": np.empty((S, T, P), np.int32),
     }
     st = np.zeros(1, np.uint32)
     _check(_load().oracle_dispatch_layout(_p(ids), S, T, k, E, P, _p(out["expert_counts"]),
-                                          _p(out["part_counts"]), _p(out["part_offsets"]),
+                                          _p(out["expert_rank"]), _p(out["part_counts"]), _p(out["part_offsets"]),
                                           _p(out["token_slot"]), _p(st)), "dispatch_layout")
     out["status"] = int(st[0])
     return out

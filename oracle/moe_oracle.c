@@ -163,6 +163,11 @@ int oracle_route_topk(const float *logits, int64_t N, int E, int k,
  * are "not routed" and skipped; ids >= E are skipped and flagged.
  *
  *   expert_counts[s][e]  = #{(t, j) : ids[s][t][j] == e}
+ *   expert_rank[s][t][j] = #{(t', j') before (t, j) in (token, slot) order :
+ *                            ids[s][t'][j'] == ids[s][t][j]}, or -1 if skipped
+ *                          (the pair's place in its expert's run of source s;
+ *                          the receiver's runs in [a2a] 1.5 / 3.3 are built
+ *                          from it)
  *   part_counts[s][p]    = #{t : token t hits partition p}
  *   part_offsets[s][0]   = 0, part_offsets[s][p+1] = part_offsets[s][p] + part_counts[s][p]
  *   token_slot[s][t][p]  = part_offsets[s][p] + #{t' < t : t' hits p}, or -1
@@ -170,7 +175,7 @@ int oracle_route_topk(const float *logits, int64_t N, int E, int k,
  * Rows of one partition's region are in ascending token order.
  */
 int oracle_dispatch_layout(const int32_t *ids, int S, int64_t T, int k, int E, int P,
-                           int32_t *expert_counts, int32_t *part_counts,
+                           int32_t *expert_counts, int32_t *expert_rank, int32_t *part_counts,
                            int32_t *part_offsets, int32_t *token_slot,
                            uint32_t *status)
 {
@@ -178,8 +183,12 @@ int oracle_dispatch_layout(const int32_t *ids, int S, int64_t T, int k, int E, i
         return -1;
     const int L = E / P;
     char *hit = (char *)malloc((size_t)P);
-    if (!hit)
+    int32_t *seen = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    if (!hit || !seen) {
+        free(hit);
+        free(seen);
         return -2;
+    }
     for (int s = 0; s < S; s++) {
         for (int e = 0; e < E; e++)
             expert_counts[s * E + e] = 0;
@@ -205,6 +214,21 @@ int oracle_dispatch_layout(const int32_t *ids, int S, int64_t T, int k, int E, i
         part_offsets[s * (P + 1) + 0] = 0;
         for (int p = 0; p < P; p++)
             part_offsets[s * (P + 1) + p + 1] = part_offsets[s * (P + 1) + p] + part_counts[s * P + p];
+        /* ranks: walk the pairs in (token, slot) order; a pair's rank is how
+         * many pairs of this source with the same expert were seen before it */
+        for (int e = 0; e < E; e++)
+            seen[e] = 0;
+        for (int64_t t = 0; t < T; t++) {
+            for (int j = 0; j < k; j++) {
+                int64_t q = ((int64_t)s * T + t) * k + j;
+                int32_t e = ids[q];
+                if (e < 0 || e >= E) {
+                    expert_rank[q] = -1;
+                    continue;
+                }
+                expert_rank[q] = seen[e]++;
+            }
+        }
         /* pass 2: slots, ascending token order within each partition */
         for (int p = 0; p < P; p++) {
             int32_t next = part_offsets[s * (P + 1) + p];
@@ -220,6 +244,7 @@ int oracle_dispatch_layout(const int32_t *ids, int S, int64_t T, int k, int E, i
         }
     }
     free(hit);
+    free(seen);
     return 0;
 }
 

@@ -166,12 +166,14 @@ def test_layout_fig1_two_copies():
 
 def _brute_layout(ids, E, P):
     """Independent formulation: list every (partition, token) pair a token needs,
-    sort the list by (partition, token) and number it 0, 1, 2, ..."""
+    sort the list by (partition, token) and number it 0, 1, 2, ...; for expert
+    ranks, number each expert's pairs by sorting their (token, slot) positions."""
     S, T, k = ids.shape
     L = E // P
     slot = -np.ones((S, T, P), np.int64)
     counts = np.zeros((S, P), np.int64)
     ecounts = np.zeros((S, E), np.int64)
+    rank = -np.ones((S, T, k), np.int64)
     for s in range(S):
         need = sorted({(int(e) // L, t) for t in range(T) for e in ids[s, t] if 0 <= e < E})
         for i, (p, t) in enumerate(need):
@@ -180,7 +182,11 @@ def _brute_layout(ids, E, P):
         for e in ids[s].ravel():
             if 0 <= e < E:
                 ecounts[s, e] += 1
-    return slot, counts, ecounts
+        for e in range(E):
+            where = sorted((t, j) for t in range(T) for j in range(k) if ids[s, t, j] == e)
+            for r, (t, j) in enumerate(where):
+                rank[s, t, j] = r
+    return slot, counts, ecounts, rank
 
 
 def test_layout_brute_force_all_tiny_inputs():
@@ -190,10 +196,11 @@ def test_layout_brute_force_all_tiny_inputs():
     for combo in itertools.product(vals, repeat=T * k):
         ids = np.array(combo, np.int32).reshape(1, T, k)
         lay = oracle.dispatch_layout(ids, E, P)
-        slot, counts, ecounts = _brute_layout(ids, E, P)
+        slot, counts, ecounts, rank = _brute_layout(ids, E, P)
         assert np.array_equal(lay["token_slot"], slot), combo
         assert np.array_equal(lay["part_counts"], counts), combo
         assert np.array_equal(lay["expert_counts"], ecounts), combo
+        assert np.array_equal(lay["expert_rank"], rank), combo
         assert np.array_equal(lay["part_offsets"][:, 1:], np.cumsum(counts, axis=1)), combo
         assert (lay["status"] == oracle.BIT_BAD_ID) == (4 in combo), combo
 
@@ -207,10 +214,11 @@ def test_layout_brute_force_random_small():
         k = int(rng.integers(1, min(E, 3) + 1))
         ids = rng.integers(-1, E, size=(S, T, k)).astype(np.int32)
         lay = oracle.dispatch_layout(ids, E, P)
-        slot, counts, ecounts = _brute_layout(ids, E, P)
+        slot, counts, ecounts, rank = _brute_layout(ids, E, P)
         assert np.array_equal(lay["token_slot"], slot)
         assert np.array_equal(lay["part_counts"], counts)
         assert np.array_equal(lay["expert_counts"], ecounts)
+        assert np.array_equal(lay["expert_rank"], rank)
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])
@@ -230,6 +238,13 @@ def test_layout_invariants(name):
             v = sl[sl >= 0]
             lo, hi = lay["part_offsets"][s, p], lay["part_offsets"][s, p + 1]
             assert np.array_equal(v, np.arange(lo, hi))                 # dense, ascending in t
+        # each expert's ranks, read in stable-sort order of its pairs, are 0, 1, 2, ...
+        flat = ids[s].reshape(-1)
+        order = np.argsort(flat, kind="stable")
+        rk = lay["expert_rank"][s].reshape(-1)[order]
+        starts = np.concatenate([[0], np.cumsum(lay["expert_counts"][s])[:-1]])
+        want = np.arange(flat.size) - np.repeat(starts, lay["expert_counts"][s])
+        assert np.array_equal(rk, want)
 
 
 def _mean_copies_sigma(E, P, k, T):
