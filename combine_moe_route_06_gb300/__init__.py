@@ -84,11 +84,11 @@ def load_library() -> ctypes.CDLL:
             "moe_last_error_message": ([], ctypes.c_char_p),
             "moe_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
             "moe_route_topk": ([P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
-            "moe_dispatch_layout": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, sz, P, P],
+            "moe_dispatch_layout": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P, P],
                                     ctypes.c_int),
             "moe_dispatch_pack": ([P, i32, i32, i32, i32, P, P, i32, P, P, P, P], ctypes.c_int),
-            "moe_permute_to_experts": ([P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                        i32, P, P, P, P, P, sz, P, P], ctypes.c_int),
+            "moe_permute_to_experts": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, i32, P, P, P, P, P, sz, P, P], ctypes.c_int),
             "moe_combine": ([P, i32, P, P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
             "moe_expert_scale": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
             "moe_trace_enable": ([ctypes.c_char_p, i32], ctypes.c_int),
@@ -158,15 +158,16 @@ def moe_route_topk(logits, topk_ids, topk_w, stream=None):
                               _dev(topk_w, "topk_w", (torch.float32,), 3), _stream(stream)))
 
 
-def moe_dispatch_layout(topk_ids, E, P, expert_counts, part_counts, part_offsets, token_slot,
-                        ws, dev_status=None, stream=None):
-    """topk_ids i32 [S,T,k] -> expert_counts [S,E], part_counts [S,P], part_offsets [S,P+1],
-    token_slot [S,T,P] (all int32); ws is a uint8 device tensor."""
+def moe_dispatch_layout(topk_ids, E, P, expert_counts, expert_rank, part_counts, part_offsets,
+                        token_slot, ws, dev_status=None, stream=None):
+    """topk_ids i32 [S,T,k] -> expert_counts [S,E], expert_rank [S,T,k], part_counts [S,P],
+    part_offsets [S,P+1], token_slot [S,T,P] (all int32); ws is a uint8 device tensor."""
     lib = load_library()
     S, T, k = topk_ids.shape
     _check(lib.moe_dispatch_layout(
         _dev(topk_ids, "topk_ids", (torch.int32,), 3), S, T, k, E, P,
         _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)),
         _dev(part_counts, "part_counts", (torch.int32,)),
         _dev(part_offsets, "part_offsets", (torch.int32,)),
         _dev(token_slot, "token_slot", (torch.int32,)),
@@ -186,8 +187,9 @@ def moe_dispatch_pack(x, token_slot, part_offsets, send, send_src, dev_status=No
         _status_ptr(dev_status), _stream(stream)))
 
 
-def moe_permute_to_experts(send, token_slot, topk_ids, E, recv_part, align, recv, expert_offsets,
-                           pair_row, recv_pair, ws, dev_status=None, stream=None):
+def moe_permute_to_experts(send, token_slot, topk_ids, expert_counts, expert_rank, E, recv_part,
+                           align, recv, expert_offsets, pair_row, recv_pair, ws, dev_status=None,
+                           stream=None):
     """send bf16 [S,cap_send,H] -> recv bf16 [cap_recv,H] in expert runs, expert_offsets [E+1],
     pair_row [S,T,k], recv_pair [cap_recv]."""
     lib = load_library()
@@ -197,7 +199,9 @@ def moe_permute_to_experts(send, token_slot, topk_ids, E, recv_part, align, recv
     cap_recv = recv.shape[0]
     _check(lib.moe_permute_to_experts(
         _dev(send, "send", _BF16_TYPES, 3), _dev(token_slot, "token_slot", (torch.int32,), 3),
-        _dev(topk_ids, "topk_ids", (torch.int32,), 3), S, T, k, E, P, H, recv_part, align,
+        _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)), S, T, k, E, P, H, recv_part, align,
         cap_send, cap_recv, _dev(recv, "recv", _BF16_TYPES, 2),
         _dev(expert_offsets, "expert_offsets", (torch.int32,)),
         _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
@@ -271,6 +275,7 @@ class MoePath:
         self.topk_ids = torch.empty((S, T, k), **i32)
         self.topk_w = torch.empty((S, T, k), dtype=torch.float32, device=d)
         self.expert_counts = torch.empty((S, E), **i32)
+        self.expert_rank = torch.empty((S, T, k), **i32)
         self.part_counts = torch.empty((S, P), **i32)
         self.part_offsets = torch.empty((S, P + 1), **i32)
         self.token_slot = torch.empty((S, T, P), **i32)
@@ -286,18 +291,74 @@ class MoePath:
         self.dev_status = torch.zeros((1,), **i32)
         self.y = None
 
+    def bind(self, logits, x, stream=None):
+        """Pre-marshal the five calls for fixed input tensors and stream.
+
+        Returns a list of (C function, argument tuple); calling them in order
+        is one step (route, layout, pack, permute, combine) with no per-call
+        Python checks, so the host enqueues far ahead of the GPU.
+        """
+        lib = load_library()
+        st = _stream(stream)
+        S, T, H, E, k, P = self.S, self.T, self.H, self.E, self.k, self.P
+        vp = ctypes.c_void_p
+        ptr = lambda t, name, dt: _dev(t, name, dt)  # noqa: E731
+        if tuple(logits.shape) != (S, T, E) or tuple(x.shape) != (S, T, H):
+            raise ValueError("bind: logits / x shapes do not match the path")
+        stp = vp(self.dev_status.data_ptr())
+        calls = [
+            (lib.moe_route_topk, (ptr(logits, "logits", (torch.float32,)), S, T, E, k,
+                                  vp(self.topk_ids.data_ptr()), vp(self.topk_w.data_ptr()), st)),
+            (lib.moe_dispatch_layout, (vp(self.topk_ids.data_ptr()), S, T, k, E, P,
+                                       vp(self.expert_counts.data_ptr()),
+                                       vp(self.expert_rank.data_ptr()),
+                                       vp(self.part_counts.data_ptr()),
+                                       vp(self.part_offsets.data_ptr()),
+                                       vp(self.token_slot.data_ptr()), vp(self.ws.data_ptr()),
+                                       self.ws.numel(), stp, st)),
+            (lib.moe_dispatch_pack, (ptr(x, "x", _BF16_TYPES), S, T, H, P,
+                                     vp(self.token_slot.data_ptr()),
+                                     vp(self.part_offsets.data_ptr()), self.cap_send,
+                                     vp(self.send.data_ptr()), vp(self.send_src.data_ptr()), stp,
+                                     st)),
+            (lib.moe_permute_to_experts, (vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
+                                          vp(self.topk_ids.data_ptr()),
+                                          vp(self.expert_counts.data_ptr()),
+                                          vp(self.expert_rank.data_ptr()), S, T, k, E, P, H,
+                                          self.recv_part, self.align, self.cap_send,
+                                          self.cap_recv, vp(self.recv.data_ptr()),
+                                          vp(self.expert_offsets.data_ptr()),
+                                          vp(self.pair_row.data_ptr()),
+                                          vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()),
+                                          self.ws.numel(), stp, st)),
+            (lib.moe_combine, (vp(self.recv.data_ptr()), self.cap_recv,
+                               vp(self.pair_row.data_ptr()), vp(self.topk_w.data_ptr()), S, T, k,
+                               H, vp(self.out.data_ptr()), stp, st)),
+        ]
+        return calls
+
+    @staticmethod
+    def run_bound(calls, upto: int | None = None, start: int = 0):
+        """Issue pre-marshalled calls [start, upto); raise on the first non-OK status."""
+        for fn, args in calls[start:upto]:
+            rc = fn(*args)
+            if rc != MOE_OK:
+                _check(rc)
+
     def route(self, logits, stream=None):
         moe_route_topk(logits, self.topk_ids, self.topk_w, stream)
 
     def dispatch(self, x, stream=None):
         """layout + pack + permute (the receiver's copy epilogue is part of dispatch)."""
-        moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts, self.part_counts,
-                            self.part_offsets, self.token_slot, self.ws, self.dev_status, stream)
+        moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts, self.expert_rank,
+                            self.part_counts, self.part_offsets, self.token_slot, self.ws,
+                            self.dev_status, stream)
         moe_dispatch_pack(x, self.token_slot, self.part_offsets, self.send, self.send_src,
                           self.dev_status, stream)
-        moe_permute_to_experts(self.send, self.token_slot, self.topk_ids, self.E, self.recv_part,
-                               self.align, self.recv, self.expert_offsets, self.pair_row,
-                               self.recv_pair, self.ws, self.dev_status, stream)
+        moe_permute_to_experts(self.send, self.token_slot, self.topk_ids, self.expert_counts,
+                               self.expert_rank, self.E, self.recv_part, self.align, self.recv,
+                               self.expert_offsets, self.pair_row, self.recv_pair, self.ws,
+                               self.dev_status, stream)
 
     def expert(self, scale, stream=None):
         if self.y is None:
@@ -318,7 +379,7 @@ class MoePath:
         return self.out
 
     def launches_per_step(self, with_expert=False) -> int:
-        """Kernels one step enqueues (route 1, layout 3 or 1, pack 1, permute 4, combine 1)."""
-        layout = 3 if self.T > 0 else 1
-        n = 1 + layout + 1 + 4 + 1
-        return n + (1 if with_expert else 0)
+        """Kernels one step enqueues (route 1, layout 2, pack 1, permute 2, combine 1)."""
+        if self.T == 0:
+            return 1 + 1 + 2 + (1 if with_expert else 0)
+        return 1 + 2 + 1 + 2 + 1 + (1 if with_expert else 0)

@@ -141,15 +141,17 @@ moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k, int
 }
 
 moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, int E, int P,
-                                 int32_t *expert_counts, int32_t *part_counts,
-                                 int32_t *part_offsets, int32_t *token_slot, void *ws,
-                                 size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream)
+                                 int32_t *expert_counts, int32_t *expert_rank,
+                                 int32_t *part_counts, int32_t *part_offsets, int32_t *token_slot,
+                                 void *ws, size_t ws_bytes, uint32_t *dev_status,
+                                 cudaStream_t stream)
 {
     moe_status_t st = check_sizes(__func__, S, T, k, E, P);
     if (st != MOE_OK) return st;
     const int64_t NT = (int64_t)S * T;
     REQUIRE_ARR(topk_ids, NT * k, 4);
     REQUIRE_ARR(expert_counts, (int64_t)S * E, 4);
+    REQUIRE_ARR(expert_rank, NT * k, 4);
     REQUIRE_ARR(part_counts, (int64_t)S * P, 4);
     REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
     REQUIRE_ARR(token_slot, NT * P, 4);
@@ -157,8 +159,9 @@ moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, i
     const size_t need = moe_workspace_bytes(S, T, k, E, P);
     REQUIRE_ARR(ws, need, 256);
     REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
-    return cuda_status(launch_dispatch_layout(topk_ids, S, T, k, E, P, expert_counts, part_counts,
-                                              part_offsets, token_slot, ws, dev_status, stream),
+    return cuda_status(launch_dispatch_layout(topk_ids, S, T, k, E, P, expert_counts, expert_rank,
+                                              part_counts, part_offsets, token_slot, ws,
+                                              dev_status, stream),
                        __func__);
 }
 
@@ -185,7 +188,8 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
 }
 
 moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
-                                    const int32_t *topk_ids, int S, int T, int k, int E, int P,
+                                    const int32_t *topk_ids, const int32_t *expert_counts,
+                                    const int32_t *expert_rank, int S, int T, int k, int E, int P,
                                     int H, int recv_part, int align, int cap_send, int cap_recv,
                                     uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
                                     int32_t *recv_pair, void *ws, size_t ws_bytes,
@@ -205,6 +209,8 @@ moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_s
     REQUIRE_ARR(send, (int64_t)S * cap_send * H, 16);
     REQUIRE_ARR(token_slot, NT * P, 4);
     REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(expert_counts, (int64_t)S * E, 4);
+    REQUIRE_ARR(expert_rank, NT * k, 4);
     REQUIRE_ARR(recv, (int64_t)cap_recv * H, 16);
     REQUIRE_ARR(expert_offsets, E + 1, 4);
     REQUIRE_ARR(pair_row, NT * k, 4);
@@ -213,9 +219,9 @@ moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_s
     const size_t need = moe_workspace_bytes(S, T, k, E, P);
     REQUIRE_ARR(ws, need, 256);
     REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
-    return cuda_status(launch_permute(send, token_slot, topk_ids, S, T, k, E, P, H, recv_part,
-                                      align, cap_send, cap_recv, recv, expert_offsets, pair_row,
-                                      recv_pair, ws, dev_status, stream),
+    return cuda_status(launch_permute(send, token_slot, topk_ids, expert_counts, expert_rank, S, T,
+                                      k, E, P, H, recv_part, align, cap_send, cap_recv, recv,
+                                      expert_offsets, pair_row, recv_pair, ws, dev_status, stream),
                        __func__);
 }
 

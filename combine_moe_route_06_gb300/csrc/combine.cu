@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kCombThreads) k_combine(const int4 *__restrict
                                                           int4 *__restrict__ out,
                                                           uint32_t *dev_status)
 {
+    pdl_wait();
+    pdl_trigger();
     bool bad_row = false;
     const int lane = threadIdx.x & 31;
     const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -127,6 +129,8 @@ __global__ void __launch_bounds__(256) k_expert_scale(const int4 *__restrict__ r
                                                       int4 *__restrict__ y)
 {
     extern __shared__ int off[];  // [E + 1]
+    pdl_wait();
+    pdl_trigger();
     for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = __ldg(expert_offsets + i);
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -180,9 +184,10 @@ cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_ro
     const int64_t wave = (int64_t)di.sm_count * (2048 / kCombThreads);
     if (blocks > wave) blocks = wave;
     MOE_TRACED_LAUNCH("k_combine", st,
-                      k_combine<<<(unsigned)blocks, kCombThreads, 0, st>>>(
-                          (const int4 *)y, y_rows, pair_row, w, N, k, V, (int4 *)out, dev_status));
-    return cudaGetLastError();
+                      e = launch_pdl(k_combine, dim3((unsigned)blocks), dim3(kCombThreads), 0, st,
+                                     (const int4 *)y, y_rows, pair_row, w, N, k, V, (int4 *)out,
+                                     dev_status));
+    return e;
 }
 
 cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
@@ -194,9 +199,10 @@ cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offs
     if (e != cudaSuccess) return e;
     const int blocks = di.sm_count * 8;
     MOE_TRACED_LAUNCH("k_expert_scale", st,
-                      k_expert_scale<<<blocks, 256, (size_t)(E + 1) * sizeof(int), st>>>(
-                          (const int4 *)recv, expert_offsets, scale, E, H / 8, cap_recv, (int4 *)y));
-    return cudaGetLastError();
+                      e = launch_pdl(k_expert_scale, dim3(blocks), dim3(256),
+                                     (size_t)(E + 1) * sizeof(int), st, (const int4 *)recv,
+                                     expert_offsets, scale, E, H / 8, cap_recv, (int4 *)y));
+    return e;
 }
 
 }  // namespace moe

@@ -81,4 +81,46 @@ __device__ __forceinline__ void st_stream(int4 *p, int4 v)
                  : "memory");
 }
 
+// Programmatic dependent launch (sm_90+): a kernel launched with
+// launch_pdl() may start while the previous kernel of the stream drains; it
+// must call pdl_wait() before touching memory that earlier work reads or
+// writes.  pdl_trigger() lets the next kernel's CTAs be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// Float -> uint32 key with the same order (-0.0 is folded onto +0.0, so equal
+// floats give equal keys).  Key 0 never comes from a finite float.
+__device__ __forceinline__ unsigned float_key(float v)
+{
+    const unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(unsigned k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 }  // namespace moe
+
+#ifndef __CUDACC_RTC__
+#include <utility>
+namespace moe {
+// Launch with programmatic stream serialization allowed (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+}  // namespace moe
+#endif

@@ -18,13 +18,9 @@ cudaError_t device_info(DeviceInfo *out);
 cudaError_t launch_route_topk(const float *logits, int64_t N, int E, int k, int32_t *ids,
                               float *w, cudaStream_t st);
 
-struct LayoutWs {
-    int32_t *pc;    // [S][P][C] per-chunk partition counts, then chunk bases
-    int32_t *ec;    // [S][E][C] per-chunk expert counts
-};
 size_t layout_ws_bytes(int S, int T, int E, int P);
 cudaError_t launch_dispatch_layout(const int32_t *ids, int S, int T, int k, int E, int P,
-                                   int32_t *expert_counts, int32_t *part_counts,
+                                   int32_t *expert_counts, int32_t *expert_rank, int32_t *part_counts,
                                    int32_t *part_offsets, int32_t *token_slot, void *ws,
                                    uint32_t *dev_status, cudaStream_t st);
 
@@ -35,6 +31,7 @@ cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
 
 size_t permute_ws_bytes(int S, int T, int E);
 cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, const int32_t *ids,
+                           const int32_t *expert_counts, const int32_t *expert_rank,
                            int S, int T, int k, int E, int P, int H, int recv_part, int align,
                            int cap_send, int cap_recv, uint16_t *recv, int32_t *expert_offsets,
                            int32_t *pair_row, int32_t *recv_pair, void *ws,

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kPackThreads) k_pack(const int4 *__restrict__ 
                                                        int32_t *__restrict__ send_src,
                                                        uint32_t *dev_status)
 {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -98,10 +100,10 @@ cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
     const int64_t tail_blocks = ((int64_t)S * cap_send + kPackThreads - 1) / kPackThreads;
     if (blocks < 1) blocks = tail_blocks < 1 ? 1 : (tail_blocks < di.sm_count ? tail_blocks : di.sm_count);
     MOE_TRACED_LAUNCH("k_pack", st,
-                      k_pack<<<(unsigned)blocks, kPackThreads, 0, st>>>(
-                          (const int4 *)x, S, T, V, P, token_slot, part_offsets, cap_send,
-                          (int4 *)send, send_src, dev_status));
-    return cudaGetLastError();
+                      e = launch_pdl(k_pack, dim3((unsigned)blocks), dim3(kPackThreads), 0, st,
+                                     (const int4 *)x, S, T, V, P, token_slot, part_offsets,
+                                     cap_send, (int4 *)send, send_src, dev_status));
+    return e;
 }
 
 }  // namespace moe

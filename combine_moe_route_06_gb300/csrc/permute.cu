@@ -6,16 +6,15 @@
 // section 5.1 (DeepEP v2's copy epilogue with do_expand and device offsets).
 //
 // The run order is a stable counting sort of the pairs (s, t, j) by expert id
-// over the receiving partition(s).  Four launches:
-//   1. count (one CTA per 256-token chunk): per-chunk expert histogram from
-//      warp match groups (no atomics), written expert-major [E][G].
-//   2. scan  (one warp per expert): exclusive scan over the chunks, in place;
-//      expert totals.
-//   3. rank  (one CTA per chunk): padded run offsets (every CTA scans the E
-//      totals itself, CTA 0 publishes expert_offsets), then each pair's row =
-//      run start + chunk base + earlier warps + rank inside the warp's match
-//      group.  Writes pair_row and recv_pair.
-//   4. copy  (grid-stride over warps): per (token, 2 KiB column segment) read
+// over the receiving partition(s).  The layout call already ranked every pair
+// inside its source's run of its expert (expert_rank) and counted the runs
+// (expert_counts), so the permute needs no scan over the pairs:
+//   1. map  (one CTA per 1,024 pairs of one source): run starts from the
+//      expert counts (every CTA scans the E padded run lengths itself; CTA 0
+//      publishes expert_offsets), then
+//        row = run start + pairs of the expert in earlier sources + rank.
+//      Writes pair_row and recv_pair.
+//   2. copy (grid-stride over warps): per (token, 2 KiB column segment) read
 //      each received row of the token once and store it to every local pair
 //      row; then zero padding rows and mark unused recv_pair entries.
 #include "common.cuh"
@@ -32,68 +31,12 @@ constexpr int kCopyUnroll = 4;
 constexpr int kCopySegVec = 32 * kCopyUnroll;
 constexpr int kCopyThreads = 256;
 
+constexpr int kMapThreads = 256;
+constexpr int kMapPairs = 4 * kMapThreads;      // pairs per CTA
+
 __device__ __forceinline__ bool in_recv(int e, int E, int L, int recv_part)
 {
     return e >= 0 && e < E && (recv_part < 0 || e / L == recv_part);
-}
-
-// Warp-private histogram of the warp's pairs.  Pairs are visited in
-// lexicographic (token, j) order, 32 at a time: q = it*32 + lane.
-__device__ __forceinline__ void warp_pair_hist(const int32_t *__restrict__ ids, int64_t pair0,
-                                               int64_t npairs, int k, int E, int L, int recv_part,
-                                               int *whist_row, bool &bad)
-{
-    const int lane = threadIdx.x & 31;
-    for (int it = 0; it < k; it++) {
-        const int64_t q = pair0 + it * 32 + lane;
-        const int e = (q < npairs) ? __ldg(ids + q) : -1;
-        if (e >= E) bad = true;
-        const bool ok = in_recv(e, E, L, recv_part);
-        const unsigned grp = __match_any_sync(kFull, ok ? e : -1);
-        if (ok && lane == __ffs(grp) - 1) whist_row[e] += __popc(grp);
-        __syncwarp();
-    }
-}
-
-__global__ void __launch_bounds__(kChunk) k_perm_count(const int32_t *__restrict__ ids,
-                                                       int64_t npairs, int k, int E, int L,
-                                                       int recv_part, int G,
-                                                       int32_t *__restrict__ ws_hist,
-                                                       uint32_t *dev_status)
-{
-    extern __shared__ int whist[];  // [kChunkWarps][E]
-    const int w = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) whist[i] = 0;
-    __syncthreads();
-    const int64_t pair0 = ((int64_t)blockIdx.x * kChunk + w * 32) * k;
-    bool bad = false;
-    warp_pair_hist(ids, pair0, npairs, k, E, L, recv_part, whist + w * E, bad);
-    if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int sum = 0;
-#pragma unroll
-        for (int ww = 0; ww < kChunkWarps; ww++) sum += whist[ww * E + e];
-        ws_hist[(int64_t)e * G + blockIdx.x] = sum;
-    }
-}
-
-// One warp per expert: in-place exclusive scan of its G chunk counts.
-__global__ void __launch_bounds__(256) k_perm_scan(int E, int G, int32_t *__restrict__ ws_hist,
-                                                   int32_t *__restrict__ ws_tot)
-{
-    const int lane = threadIdx.x & 31;
-    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (e >= E) return;
-    int32_t *row = ws_hist + (int64_t)e * G;
-    int carry = 0;
-    for (int g0 = 0; g0 < G; g0 += 32) {
-        const int g = g0 + lane;
-        const int v = (g < G) ? row[g] : 0;
-        const int inc = warp_inclusive_scan(v);
-        if (g < G) row[g] = carry + inc - v;
-        carry += __shfl_sync(kFull, inc, 31);
-    }
-    if (lane == 0) ws_tot[e] = carry;
 }
 
 // Exclusive scan of n <= 1024 values in shared memory by a 256-thread CTA;
@@ -135,80 +78,65 @@ __device__ int block_exclusive_scan_1024(int *a, int n)
     return total;
 }
 
-__global__ void __launch_bounds__(kChunk) k_perm_rank(const int32_t *__restrict__ ids,
-                                                      int64_t npairs, int k, int E, int L,
-                                                      int recv_part, int align, int G,
-                                                      const int32_t *__restrict__ ws_base,
-                                                      const int32_t *__restrict__ ws_tot,
-                                                      int cap_recv,
-                                                      int32_t *__restrict__ expert_offsets,
-                                                      int32_t *__restrict__ pair_row,
-                                                      int32_t *__restrict__ recv_pair,
-                                                      uint32_t *dev_status)
+// grid = S * B CTAs; CTA (s, b) maps pairs [b*kMapPairs, (b+1)*kMapPairs) of source s.
+__global__ void __launch_bounds__(kMapThreads) k_perm_map(
+    const int32_t *__restrict__ ids, const int32_t *__restrict__ expert_counts,
+    const int32_t *__restrict__ expert_rank, int S, int T, int k, int E, int L, int recv_part,
+    int align, int B, int cap_recv, int32_t *__restrict__ expert_offsets,
+    int32_t *__restrict__ ws_tot, int32_t *__restrict__ pair_row,
+    int32_t *__restrict__ recv_pair, uint32_t *dev_status)
 {
     extern __shared__ int sm[];
-    int *off = sm;                 // [E + 1] padded run starts
-    int *whist = sm + (E + 1);     // [kChunkWarps][E]
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // padded run lengths -> run starts (redundantly in every CTA)
+    int *off = sm;          // [E + 1] padded run starts
+    int *sb = sm + E + 1;   // [E] pairs of expert e in sources before s
+    const int s = blockIdx.x / B, b = blockIdx.x % B;
+    pdl_wait();
+    pdl_trigger();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const bool r = (recv_part < 0) || (e / L == recv_part);
-        const int c = __ldg(ws_tot + e);
-        off[e] = r ? (c + align - 1) / align * align : 0;
+        int cnt = 0, before = 0;
+        for (int s2 = 0; s2 < S; s2++) {
+            const int c = __ldg(expert_counts + (int64_t)s2 * E + e);
+            cnt += c;
+            before += (s2 < s) ? c : 0;
+        }
+        off[e] = r ? (cnt + align - 1) / align * align : 0;
+        sb[e] = before;
+        if (blockIdx.x == 0) ws_tot[e] = r ? cnt : 0;
     }
-    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) whist[i] = 0;
     __syncthreads();
     const int total = block_exclusive_scan_1024(off, E);
     if (threadIdx.x == 0) off[E] = total;
     __syncthreads();
-    if (blockIdx.x == 0) {
+    if (blockIdx.x == 0)
         for (int e = threadIdx.x; e <= E; e += blockDim.x) expert_offsets[e] = off[e];
-    }
-    if (npairs == 0) return;
 
-    // pass A: warp totals per expert
-    const int64_t pair0 = ((int64_t)blockIdx.x * kChunk + w * 32) * k;
-    bool bad = false;
-    warp_pair_hist(ids, pair0, npairs, k, E, L, recv_part, whist + w * E, bad);
-    __syncthreads();
-    // warp bases: run start + chunk base + earlier warps of this chunk
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = off[e] + __ldg(ws_base + (int64_t)e * G + blockIdx.x);
-#pragma unroll
-        for (int ww = 0; ww < kChunkWarps; ww++) {
-            const int v = whist[ww * E + e];
-            whist[ww * E + e] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    // pass B: ranks inside the warp, in (token, j) order
-    int *base = whist + w * E;
-    const unsigned lt = lanemask_lt();
-    bool dropped = false;
-    for (int it = 0; it < k; it++) {
-        const int64_t q = pair0 + it * 32 + lane;
-        const int e = (q < npairs) ? __ldg(ids + q) : -1;
-        const bool ok = in_recv(e, E, L, recv_part);
-        const unsigned grp = __match_any_sync(kFull, ok ? e : -1);
+    const int64_t per_src = (int64_t)T * k;
+    const int64_t q0 = (int64_t)s * per_src + (int64_t)b * kMapPairs;
+    const int64_t q1 = min((int64_t)s * per_src + per_src, q0 + kMapPairs);
+    bool dropped = false, bad = false, bad_id = false;
+    for (int64_t q = q0 + threadIdx.x; q < q1; q += blockDim.x) {
+        const int e = __ldg(ids + q);
+        if (e >= E) bad_id = true;
         int row = -1;
-        if (ok) row = base[e] + __popc(grp & lt);
-        __syncwarp();
-        if (ok && lane == __ffs(grp) - 1) base[e] += __popc(grp);
-        __syncwarp();
-        if (q < npairs) {
-            if (ok && row < cap_recv) {
-                pair_row[q] = row;
-                recv_pair[row] = (int32_t)q;
+        if (in_recv(e, E, L, recv_part)) {
+            const int r = __ldg(expert_rank + q);
+            if (r < 0 || r >= __ldg(expert_counts + (int64_t)s * E + e)) {
+                bad = true;             // rank inconsistent with the counts
             } else {
-                pair_row[q] = -1;
-                if (ok) dropped = true;
+                row = off[e] + sb[e] + r;
+                if (row >= cap_recv) {
+                    dropped = true;
+                    row = -1;
+                }
             }
         }
+        pair_row[q] = row;
+        if (row >= 0) recv_pair[row] = (int32_t)q;
     }
-    (void)bad;  // flagged by the count kernel
     if (__syncthreads_or(dropped) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_CAPACITY);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_INVALID_ARG);
+    if (__syncthreads_or(bad_id) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
 }
 
 __global__ void __launch_bounds__(kCopyThreads) k_perm_copy(
@@ -218,6 +146,8 @@ __global__ void __launch_bounds__(kCopyThreads) k_perm_copy(
     const int32_t *__restrict__ expert_offsets, const int32_t *__restrict__ ws_tot,
     int4 *__restrict__ recv, int32_t *__restrict__ recv_pair, uint32_t *dev_status)
 {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -307,12 +237,13 @@ __global__ void __launch_bounds__(kCopyThreads) k_perm_copy(
 
 size_t permute_ws_bytes(int S, int T, int E)
 {
-    const int64_t G = div_up((int64_t)S * T, kChunk);
-    const int64_t h = (int64_t)E * (G > 0 ? G : 1) * 4, t = (int64_t)E * 4;
-    return (size_t)(div_up(h, 256) * 256 + div_up(t, 256) * 256);
+    (void)S;
+    (void)T;
+    return (size_t)(div_up((int64_t)E * 4, 256) * 256);
 }
 
 cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, const int32_t *ids,
+                           const int32_t *expert_counts, const int32_t *expert_rank,
                            int S, int T, int k, int E, int P, int H, int recv_part, int align,
                            int cap_send, int cap_recv, uint16_t *recv, int32_t *expert_offsets,
                            int32_t *pair_row, int32_t *recv_pair, void *ws,
@@ -322,40 +253,17 @@ cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, cons
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
     const int64_t NT = (int64_t)S * T;
-    const int64_t npairs = NT * k;
-    const int G = (int)div_up(NT, kChunk);
     const int L = E / P;
-    const int64_t h_bytes = div_up((int64_t)E * (G > 0 ? G : 1) * 4, 256) * 256;
-    int32_t *ws_hist = (int32_t *)ws;
-    int32_t *ws_tot = (int32_t *)((char *)ws + h_bytes);
+    int32_t *ws_tot = (int32_t *)ws;
 
-    const size_t hist_smem = (size_t)kChunkWarps * E * sizeof(int);
-    if (G > 0) {
-        if (hist_smem > 48 * 1024) {
-            e = cudaFuncSetAttribute(k_perm_count, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)hist_smem);
-            if (e != cudaSuccess) return e;
-        }
-        MOE_TRACED_LAUNCH("k_perm_count", st,
-                          k_perm_count<<<(unsigned)G, kChunk, hist_smem, st>>>(
-                              ids, npairs, k, E, L, recv_part, G, ws_hist, dev_status));
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    MOE_TRACED_LAUNCH("k_perm_scan", st,
-                      k_perm_scan<<<(unsigned)div_up(E, 8), 256, 0, st>>>(E, G, ws_hist, ws_tot));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-    const size_t rank_smem = (size_t)(E + 1 + kChunkWarps * E) * sizeof(int);
-    if (rank_smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(k_perm_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)rank_smem);
-        if (e != cudaSuccess) return e;
-    }
-    MOE_TRACED_LAUNCH("k_perm_rank", st,
-                      k_perm_rank<<<(unsigned)(G > 0 ? G : 1), kChunk, rank_smem, st>>>(
-                          ids, npairs, k, E, L, recv_part, align, G, ws_hist, ws_tot, cap_recv,
-                          expert_offsets, pair_row, recv_pair, dev_status));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int B = (int)(div_up((int64_t)T * k, kMapPairs) > 0 ? div_up((int64_t)T * k, kMapPairs) : 1);
+    const size_t map_smem = (size_t)(2 * E + 1) * sizeof(int);
+    MOE_TRACED_LAUNCH("k_perm_map", st,
+                      e = launch_pdl(k_perm_map, dim3((unsigned)(S * B)), dim3(kMapThreads), map_smem,
+                                     st, ids, expert_counts, expert_rank, S, T, k, E, L, recv_part,
+                                     align, B, cap_recv, expert_offsets, ws_tot, pair_row,
+                                     recv_pair, dev_status));
+    if (e != cudaSuccess) return e;
 
     const int V = H / 8;
     const int nseg = (V + kCopySegVec - 1) / kCopySegVec;
@@ -370,11 +278,12 @@ cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, cons
     if (blocks > wave) blocks = wave;
     if (blocks < 1) blocks = 1;
     MOE_TRACED_LAUNCH("k_perm_copy", st,
-                      k_perm_copy<<<(unsigned)blocks, kCopyThreads, 0, st>>>(
-                          (const int4 *)send, token_slot, ids, pair_row, NT, k, E, L, P, T, V,
-                          recv_part, align, cap_send, cap_recv, expert_offsets, ws_tot,
-                          (int4 *)recv, recv_pair, dev_status));
-    return cudaGetLastError();
+                      e = launch_pdl(k_perm_copy, dim3((unsigned)blocks), dim3(kCopyThreads), 0, st,
+                                     (const int4 *)send, token_slot, ids, (const int32_t *)pair_row,
+                                     NT, k, E, L, P, T, V, recv_part, align, cap_send, cap_recv,
+                                     (const int32_t *)expert_offsets, (const int32_t *)ws_tot,
+                                     (int4 *)recv, recv_pair, dev_status));
+    return e;
 }
 
 }  // namespace moe

@@ -7,7 +7,8 @@
 //
 // One warp per token row.  Lane l holds logits l, l+32, l+64, ... in registers
 // (coalesced 128-byte loads); k rounds of a warp arg-max (value desc, id asc)
-// pick the experts; the winning lane retires its element.
+// pick the experts (one redux.sync max over order-preserving keys, one
+// redux.sync min over the tied ids); the winning lane retires its element.
 #include <float.h>
 #include <limits.h>
 #include <math.h>
@@ -23,60 +24,52 @@ __global__ void __launch_bounds__(256) k_route_topk(const float *__restrict__ lo
                                                     int E, int k, int32_t *__restrict__ ids,
                                                     float *__restrict__ w)
 {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (n >= N) return;  // uniform per warp
     const float *row = logits + n * E;
 
-    float v[VPL];
-    unsigned live = 0;  // bit i: element lane+32i is in range and not yet chosen
+    // order-preserving keys; 0 marks "out of range or already chosen"
+    unsigned key[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; i++) {
         const int e = lane + 32 * i;
-        if (e < E) {
-            v[i] = __ldcs(row + e);
-            live |= 1u << i;
-        } else {
-            v[i] = -INFINITY;
-        }
+        key[i] = (e < E) ? float_key(__ldcs(row + e)) : 0u;
     }
 
-    float my_v = 0.f;
+    unsigned my_key = 0;
     int my_id = -1;
     for (int r = 0; r < k; r++) {
-        // best live element of this lane; ids ascend with i, so a strict
-        // comparison keeps the lowest id among equal values
-        float bv = -INFINITY;
-        int bi = INT_MAX, bslot = -1;
+        // this lane's best live element; ids ascend with i, so a strict
+        // comparison keeps the lowest id among equal keys
+        unsigned bk = 0;
+        int bi = 0;
 #pragma unroll
         for (int i = 0; i < VPL; i++) {
-            if ((live >> i) & 1u) {
-                if (bslot < 0 || v[i] > bv) {
-                    bv = v[i];
-                    bi = lane + 32 * i;
-                    bslot = i;
-                }
+            if (key[i] > bk) {
+                bk = key[i];
+                bi = i;
             }
         }
-        float wv = bv;
-        int wi = bi;
+        // warp arg-max: largest key, then the lowest id holding it
+        const unsigned mx = __reduce_max_sync(kFull, bk);
+        const unsigned cand = (bk == mx) ? (unsigned)(lane + 32 * bi) : 0xffffffffu;
+        const unsigned win = __reduce_min_sync(kFull, cand);
+        if ((int)(win & 31u) == lane) {
 #pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const float ov = __shfl_xor_sync(kFull, wv, off);
-            const int oi = __shfl_xor_sync(kFull, wi, off);
-            if (ov > wv || (ov == wv && oi < wi)) {
-                wv = ov;
-                wi = oi;
-            }
+            for (int i = 0; i < VPL; i++)
+                if (i == (int)(win >> 5)) key[i] = 0u;
         }
-        if (bslot >= 0 && wi == bi) live &= ~(1u << bslot);
         if (lane == r) {
-            my_v = wv;
-            my_id = wi;
+            my_key = mx;
+            my_id = (int)win;
         }
     }
 
     // softmax over the k chosen logits: lane j < k holds choice j
+    const float my_v = key_float(my_key);
     const float lmax = __shfl_sync(kFull, my_v, 0);
     const float ex = (lane < k) ? expf(my_v - lmax) : 0.f;
     float sum = ex;
@@ -97,9 +90,11 @@ cudaError_t launch_route_topk(const float *logits, int64_t N, int E, int k, int3
     const int vpl = (E + 31) / 32;
 #define MOE_ROUTE_CASE(V)                                                              \
     if (vpl <= V) {                                                                    \
+        cudaError_t err;                                                               \
         MOE_TRACED_LAUNCH("k_route_topk", st,                                            \
-            k_route_topk<V><<<blocks, warps_per_block * 32, 0, st>>>(logits, N, E, k, ids, w)); \
-        return cudaGetLastError();                                                     \
+            err = launch_pdl(k_route_topk<V>, dim3(blocks), dim3(warps_per_block * 32), 0, st, \
+                             logits, N, E, k, ids, w));                                \
+        return err;                                                                    \
     }
     MOE_ROUTE_CASE(1)
     MOE_ROUTE_CASE(2)

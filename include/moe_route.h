@@ -112,6 +112,11 @@ moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k,
  * and the number of rows each GPU gets).
  *   topk_ids      [S][T][k] int32 in.
  *   expert_counts [S][E]    int32 out: pairs (t, j) routed to expert e.
+ *   expert_rank   [S][T][k] int32 out: place of pair (t, j) in source s's run
+ *                           of its expert, i.e. #{(t', j') before (t, j) in
+ *                           (token, slot) order with the same expert}; -1 for
+ *                           ids < 0 or >= E.  The receiver's runs (section 1.5)
+ *                           are built from it by moe_permute_to_experts.
  *   part_counts   [S][P]    int32 out: tokens with >= 1 expert in partition p
  *                           (one de-duplicated copy per token and partition).
  *   part_offsets  [S][P+1]  int32 out: exclusive prefix sum of part_counts;
@@ -123,11 +128,12 @@ moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k,
  *                           #{t' < t : t' needs p}.
  *   ws, ws_bytes  scratch, ws_bytes >= moe_workspace_bytes(S, T, k, E, P).
  *   dev_status    device uint32 status word (bad ids).
- * Counting is atomic-free (warp ballots and match groups, block scans).
+ * Counting and ranking are atomic-free (warp ballots and match groups, block
+ * scans), so the outputs are the same bytes on every run.
  */
 moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, int E, int P,
-                                 int32_t *expert_counts, int32_t *part_counts,
-                                 int32_t *part_offsets, int32_t *token_slot,
+                                 int32_t *expert_counts, int32_t *expert_rank,
+                                 int32_t *part_counts, int32_t *part_offsets, int32_t *token_slot,
                                  void *ws, size_t ws_bytes, uint32_t *dev_status,
                                  cudaStream_t stream);
 
@@ -157,6 +163,9 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
  * rows as DeepGEMM wants 128; section 3.3: one row per (token, local
  * expert); section 5.1: the copy epilogue with device-side offsets).
  *   send, token_slot, topk_ids   as produced/consumed above; cap_send as in pack.
+ *   expert_counts, expert_rank   from moe_dispatch_layout for the same topk_ids
+ *              (a pair whose rank is outside [0, expert_counts) is skipped
+ *              and flags MOE_ERR_INVALID_ARG).
  *   recv_part  receiving partition in [0, P), or -1 for all partitions.
  *   align      run alignment in rows, 1 <= align <= 1024.
  *   cap_recv   rows of recv; S*T*k + E*(align-1) always suffices.
@@ -179,7 +188,8 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
  * zero row and flags MOE_ERR_INVALID_ARG or MOE_ERR_CAPACITY respectively.
  */
 moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
-                                    const int32_t *topk_ids, int S, int T, int k, int E,
+                                    const int32_t *topk_ids, const int32_t *expert_counts,
+                                    const int32_t *expert_rank, int S, int T, int k, int E,
                                     int P, int H, int recv_part, int align, int cap_send,
                                     int cap_recv, uint16_t *recv, int32_t *expert_offsets,
                                     int32_t *pair_row, int32_t *recv_pair, void *ws,

@@ -47,12 +47,14 @@ def run_layout(ids: np.ndarray, E: int, P: int):
     S, T, k = ids.shape
     d_ids = i32_dev(ids)
     ec = torch.full((S, E), -7, dtype=torch.int32, device=DEV)
+    er = torch.full((S, T, k), -7, dtype=torch.int32, device=DEV)
     pc = torch.full((S, P), -7, dtype=torch.int32, device=DEV)
     po = torch.full((S, P + 1), -7, dtype=torch.int32, device=DEV)
     ts = torch.full((S, T, P), -7, dtype=torch.int32, device=DEV)
     ws = torch.empty(max(m.moe_workspace_bytes(S, T, k, E, P), 256), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    m.moe_dispatch_layout(d_ids, E, P, ec, pc, po, ts, ws, st)
+    m.moe_dispatch_layout(d_ids, E, P, ec, er, pc, po, ts, ws, st)
     torch.cuda.synchronize()
-    return {"expert_counts": host(ec), "part_counts": host(pc), "part_offsets": host(po),
+    return {"expert_counts": host(ec), "expert_rank": host(er), "part_counts": host(pc),
+            "part_offsets": host(po),
             "token_slot": host(ts), "status": int(st.item())}

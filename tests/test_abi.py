@@ -79,7 +79,7 @@ def test_route_rejects(lib, args, needle):
 
 def test_layout_rejects(lib):
     ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
-    good = [FAKE, 1, 64, 2, 16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, ws, FAKE, ST]
+    good = [FAKE, 1, 64, 2, 16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, FAKE, ST]
     bad = list(good)
     bad[5] = 3                                         # E % P != 0
     assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "multiple of P" in _msg(lib)
@@ -87,14 +87,17 @@ def test_layout_rejects(lib):
     bad[5] = 64
     assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "P=64" in _msg(lib)
     bad = list(good)
-    bad[11] = ws - 1                                   # workspace too small
+    bad[12] = ws - 1                                   # workspace too small
     assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "ws_bytes" in _msg(lib)
     bad = list(good)
-    bad[10] = ctypes.c_void_p((1 << 20) + 16)          # workspace not 256-byte aligned
+    bad[11] = ctypes.c_void_p((1 << 20) + 16)          # workspace not 256-byte aligned
     assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "`ws`" in _msg(lib)
     bad = list(good)
-    bad[9] = NULL
+    bad[10] = NULL
     assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "token_slot" in _msg(lib)
+    bad = list(good)
+    bad[7] = NULL
+    assert lib.moe_dispatch_layout(*bad) == m.MOE_ERR_INVALID_ARG and "expert_rank" in _msg(lib)
 
 
 def test_pack_rejects(lib):
@@ -112,10 +115,11 @@ def test_pack_rejects(lib):
 
 def test_permute_rejects(lib):
     ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
-    good = [FAKE, FAKE, FAKE, 1, 64, 2, 16, 4, 256, -1, 1, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE,
-            ws, FAKE, ST]
-    for idx, val, needle in ((9, 4, "recv_part"), (9, -2, "recv_part"), (10, 0, "align"),
-                             (10, 2048, "align"), (12, -3, "capacities"), (8, 4, "H=4")):
+    good = [FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 2, 16, 4, 256, -1, 1, 128, 128, FAKE, FAKE, FAKE,
+            FAKE, FAKE, ws, FAKE, ST]
+    for idx, val, needle in ((11, 4, "recv_part"), (11, -2, "recv_part"), (12, 0, "align"),
+                             (12, 2048, "align"), (14, -3, "capacities"), (10, 4, "H=4"),
+                             (4, NULL, "expert_rank")):
         bad = list(good)
         bad[idx] = val
         assert lib.moe_permute_to_experts(*bad) == m.MOE_ERR_INVALID_ARG, needle

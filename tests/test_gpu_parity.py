@@ -73,7 +73,7 @@ def test_route_empty():
 def _check_layout(ids, E, P):
     got = run_layout(ids, E, P)
     ref = oracle.dispatch_layout(ids, E, P)
-    for key in ("expert_counts", "part_counts", "part_offsets", "token_slot"):
+    for key in ("expert_counts", "expert_rank", "part_counts", "part_offsets", "token_slot"):
         assert np.array_equal(got[key], ref[key]), key
     assert got["status"] == ref["status"]
 
@@ -143,7 +143,7 @@ def test_pack_parity(name, T, cap):
 # ----------------------------------------------------------------- permute --
 
 def _permute_gpu(send: np.ndarray, token_slot, ids, E, recv_part, align, cap_recv, guard=2,
-                 fill=0x3C3C):
+                 fill=0x3C3C, counts=None, ranks=None):
     S, cap_send, H = send.shape
     _, T, P = token_slot.shape
     k = ids.shape[2]
@@ -155,8 +155,12 @@ def _permute_gpu(send: np.ndarray, token_slot, ids, E, recv_part, align, cap_rec
     rp = rp_full[:cap_recv]
     ws = torch.empty(max(m.moe_workspace_bytes(S, T, k, E, P), 256), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    m.moe_permute_to_experts(bf16_dev(send), i32_dev(token_slot), i32_dev(ids), E, recv_part, align,
-                             recv, eo, pr, rp, ws, st)
+    if counts is None:
+        # counts and ranks of the pairs come from the oracle's layout
+        lay = oracle.dispatch_layout(ids, E, P)
+        counts, ranks = lay["expert_counts"], lay["expert_rank"]
+    m.moe_permute_to_experts(bf16_dev(send), i32_dev(token_slot), i32_dev(ids), i32_dev(counts),
+                             i32_dev(ranks), E, recv_part, align, recv, eo, pr, rp, ws, st)
     torch.cuda.synchronize()
     full = bf16_host(recv_full)
     rpf = host(rp_full)
@@ -165,8 +169,10 @@ def _permute_gpu(send: np.ndarray, token_slot, ids, E, recv_part, align, cap_rec
             "recv_pair": rpf[:cap_recv], "status": int(st.item())}
 
 
-def _check_permute(send, token_slot, ids, E, recv_part, align, cap_recv, fill=0x3C3C):
-    got = _permute_gpu(send, token_slot, ids, E, recv_part, align, cap_recv, fill=fill)
+def _check_permute(send, token_slot, ids, E, recv_part, align, cap_recv, fill=0x3C3C, counts=None,
+                   ranks=None):
+    got = _permute_gpu(send, token_slot, ids, E, recv_part, align, cap_recv, fill=fill,
+                       counts=counts, ranks=ranks)
     H = send.shape[2]
     ref = oracle.permute_to_experts(send, token_slot, ids, E, recv_part=recv_part, align=align,
                                     cap_recv=cap_recv, recv=np.full((cap_recv, H), fill, np.uint16))
@@ -213,6 +219,23 @@ def test_permute_capacity_and_bad_inputs():
     ts[0, 11, p1] = -1
     got = _check_permute(send, ts, ids, w_.E, -1, 1, w_.T * w_.k)
     assert got["status"] & CAP and got["status"] & INC and got["status"] & BAD
+
+
+def test_permute_rejects_inconsistent_ranks():
+    """A rank outside [0, expert_counts) is skipped and flagged, never written out of place."""
+    w_, inp, ids, lay, cap_send = _pack_case("tiny")
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap_send)
+    ranks = lay["expert_rank"].copy()
+    ranks[0, 9, 0] = 10_000
+    ranks[0, 12, 1] = -1
+    got = _permute_gpu(send, lay["token_slot"], ids, w_.E, -1, 1, w_.T * w_.k,
+                       counts=lay["expert_counts"], ranks=ranks)
+    ref = oracle.permute_to_experts(send, lay["token_slot"], ids, w_.E)
+    assert got["status"] & INC
+    bad = np.zeros(ids.shape, bool)
+    bad[0, 9, 0] = bad[0, 12, 1] = True
+    assert np.all(got["pair_row"][bad] == -1)
+    assert np.array_equal(got["pair_row"][~bad], ref["pair_row"][~bad])
 
 
 def test_permute_empty():
@@ -394,3 +417,16 @@ def test_cuda_graph_replay_decode():
     assert np.array_equal(host(path.pair_row), ref["permute"]["pair_row"])
     got = bf16_host(path.out)
     assert close_bf16(got, ref["out"]), worst_rel(got, ref["out"])
+
+
+def test_bound_calls_match_checked_calls():
+    """The pre-marshalled call list (used by the benchmark) gives the same bytes."""
+    w_ = ms.workload("decode")
+    inp = ms.gen_inputs(w_)
+    p1, o1 = _gpu_path(w_, inp)
+    p2 = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P)
+    calls = p2.bind(f32_dev(inp["logits"]), bf16_dev(inp["x"]))
+    m.MoePath.run_bound(calls)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host(p2.out), o1)
+    assert np.array_equal(host(p2.pair_row), host(p1.pair_row))
