@@ -155,9 +155,13 @@ __global__ void __launch_bounds__(kCopyThreads) k_perm_copy(
     const int nseg = (V + kCopySegVec - 1) / kCopySegVec;
     bool cap_flag = false, bad_slot = false;
 
-    // 1. pair rows, one warp per (token, column segment)
+    // 1. pair rows, one warp per (token, column segment).  Tokens are walked
+    //    last to first: the pack kernel wrote the send rows of the last tokens
+    //    most recently, so those reads still hit L2; the rows written here
+    //    last (first tokens) are the ones the combine reads first.
     const int64_t ntask = NT * nseg;
-    for (int64_t task = gtid >> 5; task < ntask; task += gwarps) {
+    for (int64_t rtask = gtid >> 5; rtask < ntask; rtask += gwarps) {
+        const int64_t task = ntask - 1 - rtask;
         const int64_t n = task / nseg;
         const int g = (int)(task - n * nseg);
         int pr = -1, p = -1;
