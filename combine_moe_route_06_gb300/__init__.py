@@ -86,6 +86,8 @@ def load_library() -> ctypes.CDLL:
             "moe_route_topk": ([P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
             "moe_dispatch_layout": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P, P],
                                     ctypes.c_int),
+            "moe_dispatch_layout_static": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P],
+                                           ctypes.c_int),
             "moe_dispatch_pack": ([P, i32, i32, i32, i32, P, P, i32, P, P, P, P], ctypes.c_int),
             "moe_permute_to_experts": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                         i32, i32, P, P, P, P, P, sz, P, P], ctypes.c_int),

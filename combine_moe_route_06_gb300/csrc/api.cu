@@ -69,6 +69,11 @@ moe_status_t check_sizes(const char *fn, int S, int T, int k, int E, int P)
 
 }  // namespace
 
+moe_status_t report(moe_status_t code, const char *message)
+{
+    return fail(code, "%s", message);
+}
+
 cudaError_t device_info(DeviceInfo *out)
 {
     static std::mutex mu;

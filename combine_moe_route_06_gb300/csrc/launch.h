@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/moe_route.h"
+
 namespace moe {
 
 // Per-device launch geometry, queried once per device.
@@ -14,6 +16,9 @@ struct DeviceInfo {
     int max_smem_optin;
 };
 cudaError_t device_info(DeviceInfo *out);
+
+// Record `message` as the calling thread's last error text and return `code`.
+moe_status_t report(moe_status_t code, const char *message);
 
 cudaError_t launch_route_topk(const float *logits, int64_t N, int E, int k, int32_t *ids,
                               float *w, cudaStream_t st);

@@ -138,6 +138,31 @@ moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, i
                                  cudaStream_t stream);
 
 /*
+ * moe_dispatch_layout without a workspace argument.  The pages have no
+ * counterpart to this call; it exists for callers that have no way to
+ * allocate device memory when they call the layout -- for example a plugin
+ * inside a serving engine whose own pool owns every byte of device memory and
+ * forbids side allocations, or plain C code with no allocator at hand.
+ *
+ * Same arguments, outputs and errors as moe_dispatch_layout, minus ws and
+ * ws_bytes.  The scratch is a 4 MiB array built into the library (every GPU
+ * that loads the library keeps it until the process exits); calls whose
+ * moe_workspace_bytes(S, T, k, E, P) exceeds 4 MiB are rejected with
+ * MOE_ERR_INVALID_ARG and a message naming the sizes (with E = 384 and P = 8
+ * that is past about 680,000 tokens in all).  The first call on a device looks
+ * up the array's device address (with that device current) and caches it;
+ * make that first call before capturing any stream.  All calls share the one
+ * array and it keeps the last call's contents (nothing in it needs to start
+ * at zero): calls that can overlap on the GPU -- on different streams, or from
+ * different threads -- race on it and must be ordered by the caller.
+ */
+moe_status_t moe_dispatch_layout_static(const int32_t *topk_ids, int S, int T, int k, int E,
+                                        int P, int32_t *expert_counts, int32_t *expert_rank,
+                                        int32_t *part_counts, int32_t *part_offsets,
+                                        int32_t *token_slot, uint32_t *dev_status,
+                                        cudaStream_t stream);
+
+/*
  * Pack (a2a-backends section 3.2, fourth step; section 5.1: a region for every
  * sender, rows written straight into place; section 6.1: one copy per GPU
  * that needs the token).
