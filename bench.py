@@ -401,6 +401,20 @@ def run_ours(args, world, rank, local):
         stage_ms = {name: [e[c].elapsed_time(e[c + 1]) for e in eb]
                     for c, name in enumerate(("route", "layout", "pack", "permute", "combine"))}
 
+        # ---------------- per-kernel times (diagnostic; events around every launch) --
+        m.trace_enable(None, max_records=Kb * 16)
+        m.trace_reset()
+        torch.cuda.synchronize()
+        for i in range(Kb):
+            flush_l2()
+            m.MoePath.run_bound(calls)
+        torch.cuda.synchronize()
+        kern = {}
+        for name, ms_ in m.trace_records():
+            kern.setdefault(name, []).append(ms_)
+        m.trace_disable()
+        kernels_us = {name: round(1e3 * statistics.median(v), 2) for name, v in kern.items()}
+
         # ---------------- end to end: pinned host in, pinned host out --------
         Ke = max(10, min(K, 200))
         ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
@@ -457,6 +471,8 @@ def run_ours(args, world, rank, local):
                     "min": round(1e3 * min(step_ms), 2), "max": round(1e3 * max(step_ms), 2)},
         "stages_us_median": {k_: round(1e3 * statistics.median(v), 2) for k_, v in stage_ms.items()},
         "stages_note": "separate loop with events between calls (breaks launch overlap)",
+        "kernels_us_median": kernels_us,
+        "kernels_note": "separate loop with events around every launch (includes launch latency)",
         "stage_bytes": {k_: b[k_] for k_ in ("route", "layout", "pack", "permute", "combine")},
         "copies_per_token": round(copies / (w.S * w.T), 4),
         "pairs_recv": pairs_recv,
