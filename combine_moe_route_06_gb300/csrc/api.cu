@@ -69,6 +69,38 @@ moe_status_t check_sizes(const char *fn, int S, int T, int k, int E, int P)
 
 }  // namespace
 
+int resident_grid(const void *kernel, int threads, size_t smem)
+{
+    struct Key {
+        const void *k;
+        int dev, threads;
+        size_t smem;
+    };
+    static std::mutex mu;
+    static Key keys[64];
+    static int vals[64];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; i++)
+        if (keys[i].k == kernel && keys[i].dev == dev && keys[i].threads == threads &&
+            keys[i].smem == smem)
+            return vals[i];
+    DeviceInfo di;
+    int per_sm = 0;
+    if (device_info(&di) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
+        return 0;
+    const int v = (per_sm > 0 ? per_sm : 1) * di.sm_count;
+    if (used < 64) {
+        keys[used] = {kernel, dev, threads, smem};
+        vals[used] = v;
+        used++;
+    }
+    return v;
+}
+
 moe_status_t report(moe_status_t code, const char *message)
 {
     return fail(code, "%s", message);

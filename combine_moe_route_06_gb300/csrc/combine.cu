@@ -181,7 +181,8 @@ cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_ro
     const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
     const int64_t warps = N * nseg;
     int64_t blocks = (warps + (kCombThreads / 32) - 1) / (kCombThreads / 32);
-    const int64_t wave = (int64_t)di.sm_count * (2048 / kCombThreads);
+    const int resident = resident_grid((const void *)k_combine, kCombThreads, 0);
+    const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kCombThreads);
     if (blocks > wave) blocks = wave;
     MOE_TRACED_LAUNCH("k_combine", st,
                       e = launch_pdl(k_combine, dim3((unsigned)blocks), dim3(kCombThreads), 0, st,

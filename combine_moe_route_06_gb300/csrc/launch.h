@@ -17,6 +17,12 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo *out);
 
+// CTAs of `kernel` that fit on the whole device at once (SM count x blocks
+// per SM for this block size and dynamic shared memory); cached per device
+// and kernel.  Persistent grid-stride kernels launch exactly this many, so no
+// second wave leaves a tail.  Returns 0 if the query fails.
+int resident_grid(const void *kernel, int threads, size_t smem);
+
 // Record `message` as the calling thread's last error text and return `code`.
 moe_status_t report(moe_status_t code, const char *message);
 

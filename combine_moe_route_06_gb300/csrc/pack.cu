@@ -95,7 +95,8 @@ cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
     const int nseg = (V + kPackSegVec - 1) / kPackSegVec;
     const int64_t warps = (int64_t)S * T * nseg;
     const int64_t want = (warps + (kPackThreads / 32) - 1) / (kPackThreads / 32);
-    int64_t blocks = (int64_t)di.sm_count * (2048 / kPackThreads);
+    const int resident = resident_grid((const void *)k_pack, kPackThreads, 0);
+    int64_t blocks = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPackThreads);
     if (want < blocks) blocks = want;
     const int64_t tail_blocks = ((int64_t)S * cap_send + kPackThreads - 1) / kPackThreads;
     if (blocks < 1) blocks = tail_blocks < 1 ? 1 : (tail_blocks < di.sm_count ? tail_blocks : di.sm_count);

@@ -79,6 +79,7 @@ __device__ int block_exclusive_scan_1024(int *a, int n)
 }
 
 // grid = S * B CTAs; CTA (s, b) maps pairs [b*kMapPairs, (b+1)*kMapPairs) of source s.
+// Every global load is issued before the first barrier so their latencies overlap.
 __global__ void __launch_bounds__(kMapThreads) k_perm_map(
     const int32_t *__restrict__ ids, const int32_t *__restrict__ expert_counts,
     const int32_t *__restrict__ expert_rank, int S, int T, int k, int E, int L, int recv_part,
@@ -87,21 +88,36 @@ __global__ void __launch_bounds__(kMapThreads) k_perm_map(
     int32_t *__restrict__ recv_pair, uint32_t *dev_status)
 {
     extern __shared__ int sm[];
-    int *off = sm;          // [E + 1] padded run starts
-    int *sb = sm + E + 1;   // [E] pairs of expert e in sources before s
+    int *off = sm;              // [E + 1] padded run starts
+    int *sb = sm + E + 1;       // [E] pairs of expert e in sources before s
+    int *own = sb + E;          // [E] pairs of expert e in source s
+    constexpr int kPer = kMapPairs / kMapThreads;
     const int s = blockIdx.x / B, b = blockIdx.x % B;
+    const int64_t per_src = (int64_t)T * k;
+    const int64_t q0 = (int64_t)s * per_src + (int64_t)b * kMapPairs;
+    const int64_t q1 = min((int64_t)s * per_src + per_src, q0 + kMapPairs);
     pdl_wait();
     pdl_trigger();
+
+    int e_[kPer], r_[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        const int64_t q = q0 + threadIdx.x + i * kMapThreads;
+        e_[i] = (q < q1) ? __ldg(ids + q) : -1;
+        r_[i] = (q < q1) ? __ldg(expert_rank + q) : -1;
+    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const bool r = (recv_part < 0) || (e / L == recv_part);
-        int cnt = 0, before = 0;
+        int cnt = 0, before = 0, mine = 0;
         for (int s2 = 0; s2 < S; s2++) {
             const int c = __ldg(expert_counts + (int64_t)s2 * E + e);
             cnt += c;
             before += (s2 < s) ? c : 0;
+            mine = (s2 == s) ? c : mine;
         }
         off[e] = r ? (cnt + align - 1) / align * align : 0;
         sb[e] = before;
+        own[e] = mine;
         if (blockIdx.x == 0) ws_tot[e] = r ? cnt : 0;
     }
     __syncthreads();
@@ -111,17 +127,17 @@ __global__ void __launch_bounds__(kMapThreads) k_perm_map(
     if (blockIdx.x == 0)
         for (int e = threadIdx.x; e <= E; e += blockDim.x) expert_offsets[e] = off[e];
 
-    const int64_t per_src = (int64_t)T * k;
-    const int64_t q0 = (int64_t)s * per_src + (int64_t)b * kMapPairs;
-    const int64_t q1 = min((int64_t)s * per_src + per_src, q0 + kMapPairs);
     bool dropped = false, bad = false, bad_id = false;
-    for (int64_t q = q0 + threadIdx.x; q < q1; q += blockDim.x) {
-        const int e = __ldg(ids + q);
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        const int64_t q = q0 + threadIdx.x + i * kMapThreads;
+        if (q >= q1) continue;
+        const int e = e_[i];
         if (e >= E) bad_id = true;
         int row = -1;
         if (in_recv(e, E, L, recv_part)) {
-            const int r = __ldg(expert_rank + q);
-            if (r < 0 || r >= __ldg(expert_counts + (int64_t)s * E + e)) {
+            const int r = r_[i];
+            if (r < 0 || r >= own[e]) {
                 bad = true;             // rank inconsistent with the counts
             } else {
                 row = off[e] + sb[e] + r;
@@ -261,7 +277,7 @@ cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, cons
     int32_t *ws_tot = (int32_t *)ws;
 
     const int B = (int)(div_up((int64_t)T * k, kMapPairs) > 0 ? div_up((int64_t)T * k, kMapPairs) : 1);
-    const size_t map_smem = (size_t)(2 * E + 1) * sizeof(int);
+    const size_t map_smem = (size_t)(3 * E + 1) * sizeof(int);
     MOE_TRACED_LAUNCH("k_perm_map", st,
                       e = launch_pdl(k_perm_map, dim3((unsigned)(S * B)), dim3(kMapThreads), map_smem,
                                      st, ids, expert_counts, expert_rank, S, T, k, E, L, recv_part,
@@ -272,9 +288,10 @@ cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, cons
     const int V = H / 8;
     const int nseg = (V + kCopySegVec - 1) / kCopySegVec;
     const int64_t warps = NT * nseg + (align > 1 ? (int64_t)E * (align - 1) * nseg : 0);
-    // persistent grid: at most one full wave; at least enough threads for the
-    // recv_pair tail (capped at one CTA per SM)
-    const int64_t wave = (int64_t)di.sm_count * (2048 / kCopyThreads);
+    // persistent grid: at most the CTAs that fit at once; at least enough
+    // threads for the recv_pair tail (capped at one CTA per SM)
+    const int resident = resident_grid((const void *)k_perm_copy, kCopyThreads, 0);
+    const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kCopyThreads);
     int64_t blocks = div_up(warps, kCopyThreads / 32);
     const int64_t tail = div_up(cap_recv, kCopyThreads);
     const int64_t tail_blocks = tail < di.sm_count ? tail : di.sm_count;

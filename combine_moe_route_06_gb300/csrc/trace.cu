@@ -5,7 +5,8 @@
 // kernel name contains `filter` (all launches if NULL/empty) is bracketed by an
 // event pair recorded on the launch's own stream.  Records beyond max_records
 // are not taken.  moe_trace_get waits for a record's stop event and returns its
-// duration.  Not meant for use during stream capture.
+// duration.  A launch captured into a CUDA graph gets event nodes in the graph:
+// every replay re-records them, and moe_trace_get returns the latest replay.
 #include <string.h>
 
 #include <mutex>
@@ -40,6 +41,16 @@ TraceState &state()
     return s;
 }
 
+// Record `ev` on `st`; inside a stream capture the record becomes an event node
+// of the graph (re-recorded on every replay).
+cudaError_t record(cudaEvent_t ev, cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+    return cudaEventRecord(ev, st);
+}
+
 void destroy_events(TraceState &s)
 {
     for (cudaEvent_t e : s.ev) cudaEventDestroy(e);
@@ -59,7 +70,7 @@ void trace_begin(const char *kernel, cudaStream_t st)
     if (!s.filter.empty() && strstr(kernel, s.filter.c_str()) == nullptr) return;
     const int idx = (int)s.rec.size();
     if (2 * idx + 1 >= (int)s.ev.size()) return;
-    if (cudaEventRecord(s.ev[2 * idx], st) != cudaSuccess) return;
+    if (record(s.ev[2 * idx], st) != cudaSuccess) return;
     s.rec.push_back({kernel, idx});
     s.pending = idx;
 }
@@ -69,7 +80,7 @@ void trace_end(cudaStream_t st)
     TraceState &s = state();
     std::lock_guard<std::mutex> lock(s.mu);
     if (s.pending < 0) return;
-    cudaEventRecord(s.ev[2 * s.pending + 1], st);
+    record(s.ev[2 * s.pending + 1], st);
     s.pending = -1;
 }
 

@@ -256,8 +256,9 @@ moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offset
  * launch's stream, up to max_records launches.  moe_trace_enable creates the
  * events (host handles only, no device memory) and clears earlier records;
  * moe_trace_get(i) waits for record i to finish and returns the kernel name
- * (static string) and its duration in ms.  Do not enable while a stream is
- * being captured into a CUDA graph.
+ * (static string) and its duration in ms.  Launches captured into a CUDA graph
+ * while tracing is on get event nodes in the graph; each replay re-records
+ * them and moe_trace_get returns the latest replay's duration.
  */
 moe_status_t moe_trace_enable(const char *kernel_filter, int max_records);
 void moe_trace_disable(void);

@@ -430,3 +430,32 @@ def test_bound_calls_match_checked_calls():
     torch.cuda.synchronize()
     assert np.array_equal(bf16_host(p2.out), o1)
     assert np.array_equal(host(p2.pair_row), host(p1.pair_row))
+
+
+def test_trace_inside_cuda_graph():
+    """With tracing on during capture, each replay re-records the traced kernel's events."""
+    w_ = ms.workload("decode")
+    inp = ms.gen_inputs(w_)
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P)
+    logits, x = f32_dev(inp["logits"]), bf16_dev(inp["x"])
+    s = torch.cuda.Stream()
+    calls = path.bind(logits, x, s)
+    with torch.cuda.stream(s):
+        m.MoePath.run_bound(calls)
+    torch.cuda.synchronize()
+    m.trace_enable("k_perm_copy", 4)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            m.MoePath.run_bound(calls)
+        for _ in range(2):
+            g.replay()
+            torch.cuda.synchronize()
+            recs = m.trace_records()
+            assert [r[0] for r in recs] == ["k_perm_copy"] and recs[0][1] > 0
+        del g
+        torch.cuda.synchronize()
+    finally:
+        m.trace_disable()
+    ref = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, None)
+    assert close_bf16(bf16_host(path.out), ref["out"])
