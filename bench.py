@@ -415,25 +415,68 @@ def run_ours(args, world, rank, local):
         value = bytes_all / (job_ms * 1e-3) / 1e9
 
         # ---------------- end to end: pinned host in, pinned host out --------
+        # Every step copies its logits and x in from pinned host memory and its
+        # output back out.  Steps are pipelined as in a serving loop: two sets
+        # of buffers, H2D on one stream, the step on another, D2H on a third,
+        # ordered by events, so copies of one step overlap the next step.
         Ke = max(10, min(K, 200))
-        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+        s_in = torch.cuda.Stream(device=dev)
+        s_out = torch.cuda.Stream(device=dev)
+        path2 = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev)
+        logits2 = torch.empty_like(logits)
+        x2 = torch.empty_like(x)
+        h_out2 = torch.empty_like(h_out).pin_memory()
+        calls2 = path2.bind(logits2, x2, stream)
+        with torch.cuda.stream(stream):
+            m.MoePath.run_bound(calls2)            # warm the second set once
+        torch.cuda.synchronize()
+        sets = [(logits, x, path, h_out), (logits2, x2, path2, h_out2)]
+        if graph is not None:
+            graph2 = torch.cuda.CUDAGraph()
+            cap2 = torch.cuda.Stream(device=dev)
+            with torch.cuda.graph(graph2, stream=cap2):
+                m.MoePath.run_bound(path2.bind(logits2, x2, cap2))
+            torch.cuda.synchronize()
+            steps = [graph.replay, graph2.replay]
+        else:
+            steps = [lambda: m.MoePath.run_bound(calls), lambda: m.MoePath.run_bound(calls2)]
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
+        e_start.record(s_in)
         for i in range(Ke):
-            flush_l2()
-            ee[i][0].record(stream)
-            logits.copy_(h_logits, non_blocking=True)
-            x.view(torch.int16).copy_(h_x, non_blocking=True)
-            run_step()
-            h_out.copy_(path.out.view(torch.int16), non_blocking=True)
-            ee[i][1].record(stream)
+            b_ = i % 2
+            lg, xx, pth, ho = sets[b_]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[b_])   # step i-2 has read this set's inputs
+                lg.copy_(h_logits, non_blocking=True)
+                xx.view(torch.int16).copy_(h_x, non_blocking=True)
+                ev_in[b_].record(s_in)
+            stream.wait_event(ev_in[b_])
+            if i >= 2:
+                stream.wait_event(ev_out[b_])      # step i-2's output has been read out
+            with torch.cuda.stream(stream):
+                steps[b_]()
+                ev_comp[b_].record(stream)
+            s_out.wait_event(ev_comp[b_])
+            with torch.cuda.stream(s_out):
+                ho.copy_(pth.out.view(torch.int16), non_blocking=True)
+                ev_out[b_].record(s_out)
+        e_end.record(s_out)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(sum(p[0].elapsed_time(p[1]) for p in ee), dist, dev)
+        e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dist, dev)
         e2e_bytes = sum_over_ranks(float(b["step"]) * Ke, dist, dev)
         e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
-        out_ok = bool(np.array_equal(h_out.numpy().view(np.uint16)[0, :4], path.out[0, :4].view(
+        out_ok = bool(np.array_equal(h_out2.numpy().view(np.uint16), path2.out.view(
             torch.int16).cpu().numpy().view(np.uint16)))
+        graph2 = None
+        del path2
 
         # the graph's event nodes use the trace's events: release both before the
         # eager diagnostics re-enable tracing
@@ -521,7 +564,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
                 "d2h_bytes_per_step": int(h_out.numel() * 2), "steps": Ke,
-                "ms_per_step": round(e2e_ms / Ke, 4), "readback_ok": out_ok},
+                "ms_per_step": round(e2e_ms / Ke, 4), "readback_ok": out_ok,
+                "how": "pinned H2D -> step -> D2H every step; steps pipelined on 3 streams "
+                       "with 2 buffer sets; no L2 flush (each step moves ~1 GB)"},
         "gpu_launches": launches * K,
         "launch_mode": "eager" if args.eager else "cuda_graph_replay",
         "host_enqueue_us_per_step": round(host_enqueue_us, 1),

@@ -381,7 +381,8 @@ class MoePath:
         return self.out
 
     def launches_per_step(self, with_expert=False) -> int:
-        """Kernels one step enqueues (route 1, layout 2, pack 1, permute 2, combine 1)."""
+        """Kernels one step enqueues (route 1, layout 2 (1 if T <= 256), pack 1, permute 2, combine 1)."""
         if self.T == 0:
             return 1 + 1 + 2 + (1 if with_expert else 0)
-        return 1 + 2 + 1 + 2 + 1 + (1 if with_expert else 0)
+        layout = 1 if self.T <= 256 else 2
+        return 1 + layout + 1 + 2 + 1 + (1 if with_expert else 0)

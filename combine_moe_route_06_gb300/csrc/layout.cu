@@ -61,20 +61,28 @@ inline size_t local_smem(int k, int E)
 // Chunk-local layout of 256 tokens.  Writes chunk-local slots (rank among the
 // chunk's tokens that need partition p) and chunk-local expert ranks into the
 // outputs, and the chunk's partition and expert counts into the workspace.
+// With one chunk per source (C == 1, e.g. a decode step) the chunk-local values
+// are already final: the kernel then adds the partition offsets itself and
+// publishes the counts, and no fix-up kernel runs.
 __global__ void __launch_bounds__(kChunk) k_layout_local(const int32_t *__restrict__ ids, int T,
                                                          int k, int E, int P, int C,
                                                          int32_t *__restrict__ ws_pc,
                                                          int32_t *__restrict__ ws_ec,
                                                          int32_t *__restrict__ expert_rank,
                                                          int32_t *__restrict__ token_slot,
+                                                         int32_t *__restrict__ expert_counts,
+                                                         int32_t *__restrict__ part_counts,
+                                                         int32_t *__restrict__ part_offsets,
                                                          uint32_t *dev_status)
 {
+    const bool single = (C == 1);
     extern __shared__ int sm[];
     int *ids_s = sm;                          // [kChunk * k] the chunk's ids, (token, slot) order
     int *whist = sm + kChunk * k;             // [kChunkWarps][E] per-warp expert counts
     unsigned *wmask = (unsigned *)(whist + kChunkWarps * E);  // [kChunkWarps][E] lanes with e
     int *part_s = (int *)(wmask + kChunkWarps * E);           // [E] partition of each expert
     __shared__ int wpart[kChunkWarps][kMaxP]; // per-warp partition counts, then bases
+    __shared__ int ptot[kMaxP], poff[kMaxP + 1];
     const int s = blockIdx.x / C, c = blockIdx.x % C;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = E / P;
@@ -134,6 +142,7 @@ __global__ void __launch_bounds__(kChunk) k_layout_local(const int32_t *__restri
             run += v;
         }
         ws_pc[((int64_t)s * P + p) * C + c] = run;
+        ptot[p] = run;
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
@@ -144,15 +153,30 @@ __global__ void __launch_bounds__(kChunk) k_layout_local(const int32_t *__restri
             run += v;
         }
         ws_ec[((int64_t)s * C + c) * E + e] = run;
+        if (single) expert_counts[(int64_t)s * E + e] = run;
     }
     __syncthreads();
+    if (single) {
+        if (threadIdx.x == 0) {
+            int run = 0;
+            for (int p = 0; p < P; p++) {
+                poff[p] = run;
+                run += ptot[p];
+            }
+            poff[P] = run;
+        }
+        __syncthreads();
+        if (threadIdx.x < P) part_counts[(int64_t)s * P + threadIdx.x] = ptot[threadIdx.x];
+        if (threadIdx.x <= P) part_offsets[(int64_t)s * (P + 1) + threadIdx.x] = poff[threadIdx.x];
+    }
 
     // chunk-local slots
     const unsigned lt = lanemask_lt();
     int32_t *slot = token_slot + ((int64_t)s * T + t0 + threadIdx.x) * P;
     for (int p = 0; p < P; p++) {
         const unsigned b = __ballot_sync(kFull, (mask >> p) & 1u);
-        if (valid_t) slot[p] = ((mask >> p) & 1u) ? wpart[w][p] + __popc(b & lt) : -1;
+        if (valid_t)
+            slot[p] = ((mask >> p) & 1u) ? (single ? poff[p] : 0) + wpart[w][p] + __popc(b & lt) : -1;
     }
 
     // chunk-local expert ranks, pairs in (token, slot) order: warp base +
@@ -354,8 +378,9 @@ cudaError_t launch_dispatch_layout(const int32_t *ids, int S, int T, int k, int 
     MOE_TRACED_LAUNCH("k_layout_local", st,
                       e = launch_pdl(k_layout_local, dim3((unsigned)(S * C)), dim3(kChunk), smem1,
                                      st, ids, T, k, E, P, C, ws_pc, ws_ec, expert_rank,
-                                     token_slot, dev_status));
-    if (e != cudaSuccess) return e;
+                                     token_slot, expert_counts, part_counts, part_offsets,
+                                     dev_status));
+    if (e != cudaSuccess || C == 1) return e;
     MOE_TRACED_LAUNCH("k_layout_fix", st,
                       e = launch_pdl(k_layout_fix, dim3((unsigned)(S * C)), dim3(kChunk), smem2,
                                      st, ids, T, k, E, P, C, (const int32_t *)ws_pc,

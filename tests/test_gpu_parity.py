@@ -87,7 +87,8 @@ def test_layout_parity(name):
 
 @pytest.mark.parametrize("S,T,k,E,P", [(1, 1, 2, 16, 4), (1, 255, 3, 12, 3), (1, 257, 3, 12, 3),
                                        (3, 513, 2, 32, 32), (2, 1000, 8, 64, 1),
-                                       (1, 700, 32, 1024, 32), (2, 0, 2, 16, 4)])
+                                       (1, 700, 32, 1024, 32), (2, 0, 2, 16, 4),
+                                       (4, 200, 3, 12, 3), (3, 256, 6, 384, 8)])
 def test_layout_ragged_and_extremes(S, T, k, E, P):
     rng = np.random.default_rng(S * 1000 + T)
     ids = rng.integers(0, E, size=(S, T, k)).astype(np.int32)
