@@ -36,6 +36,11 @@ import moe_synth as ms  # noqa: E402
 METRIC = "dispatch+combine HBM GB/s and rows/s at 4096-token prefill; % of HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT = "k_perm_copy"
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_perm_copy
+# launch in the prefill pipeline, from an ncu capture with the L2 left as the
+# previous kernel left it (--cache-control none).  Taken on the current kernel;
+# it must be re-measured whenever k_perm_copy changes.
+DOMINANT_TRAFFIC = {"prefill": 142.5e6 + 252.3e6}
 
 
 # ------------------------------------------------------------ byte model --
@@ -557,7 +562,7 @@ def run_ours(args, world, rank, local):
                      "achieved": round(dom_achieved, 1) if dom_achieved else None,
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(dom_achieved / peak, 4) if dom_achieved else None,
-                     "traffic": None, "bytes_per_launch": b["perm_copy"],
+                     "traffic": DOMINANT_TRAFFIC.get(w.name), "bytes_per_launch": b["perm_copy"],
                      "us_per_launch": round(1e3 * dom_ms, 2) if dom_ms else None,
                      "launches_timed": len(recs)},
         "cpu_baseline": cpu,
