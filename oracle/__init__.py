@@ -62,9 +62,12 @@ def _load():
             lib.oracle_permute_to_experts.argtypes = [P, P, P, i32, i64, i32, i32, i32, i32,
                                                       i32, i32, i64, i64, P, P, P, P, P]
             lib.oracle_expert_scale.argtypes = [P, P, P, i32, i32, i64, P]
+            lib.oracle_permute_masked.argtypes = [P, P, P, i32, i64, i32, i32, i32, i32, i32,
+                                                  i64, i64, P, P, P, P, P]
             lib.oracle_combine.argtypes = [P, P, P, i32, i64, i32, i32, P]
             for f in ("oracle_route_topk", "oracle_dispatch_layout", "oracle_dispatch_pack",
-                      "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine"):
+                      "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine",
+                      "oracle_permute_masked"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -172,6 +175,34 @@ def permute_to_experts(send: np.ndarray, token_slot: np.ndarray, ids: np.ndarray
         _p(send), _p(token_slot), _p(ids), S, T, k, E, P, H, recv_part, align, cap_send,
         cap_recv, _p(recv), _p(out["expert_offsets"]), _p(out["pair_row"]),
         _p(out["recv_pair"]), _p(st)), "permute_to_experts")
+    out["status"] = int(st[0])
+    return out
+
+
+def permute_masked(send: np.ndarray, token_slot: np.ndarray, ids: np.ndarray, E: int,
+                   recv_part: int, block_rows: int, recv: np.ndarray | None = None) -> dict:
+    """Masked receive layout: one block of block_rows rows per expert of the receiving set.
+
+    Returns recv [blocks*block_rows, H], masked_counts [blocks], pair_row, recv_pair, status.
+    Rows past each block's count keep the contents of the `recv` passed in.
+    """
+    send = np.ascontiguousarray(send, dtype=np.uint16)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    S, cap_send, H = send.shape
+    _, T, P = token_slot.shape
+    k = ids.shape[2]
+    nb = E if recv_part < 0 else E // P
+    if recv is None:
+        recv = np.zeros((nb * block_rows, H), np.uint16)
+    out = {"recv": recv, "masked_counts": np.empty(nb, np.int32),
+           "pair_row": np.empty((S, T, k), np.int32),
+           "recv_pair": np.empty(nb * block_rows, np.int32)}
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_permute_masked(
+        _p(send), _p(token_slot), _p(ids), S, T, k, E, P, H, recv_part, block_rows, cap_send,
+        _p(recv), _p(out["masked_counts"]), _p(out["pair_row"]), _p(out["recv_pair"]), _p(st)),
+        "permute_masked")
     out["status"] = int(st[0])
     return out
 

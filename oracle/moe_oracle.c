@@ -391,6 +391,74 @@ int oracle_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
     return 0;
 }
 
+/* ------------------------------------------- masked layout, [a2a] 4.1-4.2 */
+
+/*
+ * The masked receive layout of DeepEP's low-latency mode ([a2a] 4.1: a region
+ * per (local expert, sender) with room for the cap; 4.2: the receiver packs
+ * each expert's rows together and writes a per-expert count, the output has a
+ * fixed shape, 48 x 8 x 128 rows for the decode example; 5.2: SGLang's masked
+ * kernel expects these fixed-size blocks).
+ *
+ * Every expert of the receiving set gets a block of block_rows rows; block b
+ * holds expert e = b (recv_part < 0) or e = recv_part*L + b.  The pairs of
+ * expert e, in ascending (s, t, j) order, fill the block from row 0; pairs
+ * past the block's end are dropped (pair_row -1, capacity flag).
+ *   masked_counts[b]            = rows of the block in use (<= block_rows)
+ *   recv[b*block_rows + i]      = send[s][token_slot[s][t][part(e)]] of the i-th pair
+ *   pair_row[s][t][j]           = its row, or -1
+ *   recv_pair[b*block_rows + i] = (s*T + t)*k + j for used rows, -1 otherwise
+ * Rows past masked_counts[b] are not written.  Missing source slots behave as
+ * in the contiguous layout (zero row, flagged).
+ */
+int oracle_permute_masked(const uint16_t *send, const int32_t *token_slot, const int32_t *ids,
+                          int S, int64_t T, int k, int E, int P, int H, int recv_part,
+                          int64_t block_rows, int64_t cap_send, uint16_t *recv,
+                          int32_t *masked_counts, int32_t *pair_row, int32_t *recv_pair,
+                          uint32_t *status)
+{
+    if (P < 1 || E % P != 0 || recv_part < -1 || recv_part >= P || block_rows < 0)
+        return -1;
+    const int L = E / P;
+    const int nb = recv_part < 0 ? E : L;
+    const int e0 = recv_part < 0 ? 0 : recv_part * L;
+    for (int b = 0; b < nb; b++)
+        masked_counts[b] = 0;
+    for (int64_t r = 0; r < (int64_t)nb * block_rows; r++)
+        recv_pair[r] = -1;
+    for (int s = 0; s < S; s++) {
+        for (int64_t t = 0; t < T; t++) {
+            for (int j = 0; j < k; j++) {
+                int64_t q = ((int64_t)s * T + t) * k + j;
+                int32_t e = ids[q];
+                pair_row[q] = -1;
+                if (e >= E)
+                    *status |= ORC_BIT_BAD_ID;
+                if (e < 0 || e >= E || e < e0 || e >= e0 + nb)
+                    continue;
+                int b = e - e0;
+                if (masked_counts[b] >= block_rows) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue;
+                }
+                int64_t row = (int64_t)b * block_rows + masked_counts[b];
+                masked_counts[b]++;
+                pair_row[q] = (int32_t)row;
+                recv_pair[row] = (int32_t)q;
+                int32_t slot = token_slot[((int64_t)s * T + t) * P + e / L];
+                if (slot < 0 || slot >= cap_send) {
+                    *status |= (slot < 0) ? ORC_BIT_INCONSISTENT : ORC_BIT_CAPACITY;
+                    memset(recv + row * H, 0, sizeof(uint16_t) * (size_t)H);
+                    continue;
+                }
+                memcpy(recv + row * H, send + ((int64_t)s * cap_send + slot) * H,
+                       sizeof(uint16_t) * (size_t)H);
+            }
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------ stand-in expert -- */
 
 /*

@@ -490,3 +490,67 @@ def test_expert_scale_exact_products():
         rows = per["recv"][off[e]:off[e + 1]]
         want = ms.bf16_bits_from_f32(ms.f32_from_bf16_bits(rows) * np.float32(inp["scales"][e]))
         assert np.array_equal(r["y"][off[e]:off[e + 1]], want)
+
+
+# ------------------------------------------------- masked layout (a2a 4.1, 4.2) --
+
+def _decode_from_8_sources(seed_index=11):
+    w_ = ms.workload("decode", S=8, index=seed_index)
+    inp = ms.gen_inputs(w_)
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap_send = w_.T * min(w_.k, w_.P)
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap_send)
+    return w_, inp, ids, lay, send
+
+
+def test_masked_shape_and_mean_rows():
+    g = _golden("masked_rows.json")
+    w_, inp, ids, lay, send = _decode_from_8_sources()
+    assert (w_.E // w_.P, w_.S, w_.T) == (g["local_experts"], g["gpus"], g["decode_rows_per_gpu"])
+    block = g["gpus"] * g["cap"]
+    total = 0
+    for p in range(w_.P):
+        per = oracle.permute_masked(send, lay["token_slot"], ids, w_.E, p, block)
+        assert per["recv"].shape[0] == g["rows"]                 # 48 x 8 x 128 rows of room
+        assert per["status"] == 0
+        total += int(per["masked_counts"].sum())
+    # every pair lands on exactly one receiver: the mean over receivers is S*T*k/P = 384
+    assert total / w_.P == g["arriving_rows_mean"]
+
+
+@pytest.mark.parametrize("recv_part", [0, 5, -1])
+def test_masked_equals_contiguous_runs(recv_part):
+    w_, inp, ids, lay, send = _decode_from_8_sources()
+    block = 1024
+    m_ = oracle.permute_masked(send, lay["token_slot"], ids, w_.E, recv_part, block)
+    c_ = oracle.permute_to_experts(send, lay["token_slot"], ids, w_.E, recv_part=recv_part)
+    L = w_.E // w_.P
+    e0 = 0 if recv_part < 0 else recv_part * L
+    off = c_["expert_offsets"]
+    for b in range(m_["masked_counts"].size):
+        e = e0 + b
+        n = int(m_["masked_counts"][b])
+        assert n == off[e + 1] - off[e]
+        rows = slice(b * block, b * block + n)
+        assert np.array_equal(m_["recv"][rows], c_["recv"][off[e]:off[e + 1]])
+        assert np.array_equal(m_["recv_pair"][rows], c_["recv_pair"][off[e]:off[e + 1]])
+        assert np.all(m_["recv_pair"][b * block + n:(b + 1) * block] == -1)
+    valid = c_["pair_row"] >= 0
+    assert np.array_equal(m_["pair_row"] >= 0, valid)
+
+
+def test_masked_overflow_keeps_first_pairs():
+    w_, inp, ids, lay, send = _decode_from_8_sources()
+    block = 4
+    per = oracle.permute_masked(send, lay["token_slot"], ids, w_.E, 2, block)
+    assert per["status"] == oracle.BIT_CAPACITY
+    L = w_.E // w_.P
+    flat = ids.reshape(-1)
+    for b in range(L):
+        e = 2 * L + b
+        q = np.nonzero(flat == e)[0]                # pairs of e in (s, t, j) order
+        keep = q[:block]
+        assert per["masked_counts"][b] == keep.size
+        assert np.array_equal(per["recv_pair"][b * block:b * block + keep.size], keep)
+        assert np.all(per["pair_row"].reshape(-1)[q[block:]] == -1)
