@@ -26,7 +26,7 @@ __all__ = [
     "MOE_ERR_TIMEOUT", "MOE_ERR_CUDA", "status_bit", "MoeError", "MoeLibraryMissing",
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
-    "moe_combine", "moe_expert_scale", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "MoePath", "trace_enable", "trace_disable", "trace_reset",
     "trace_records",
 ]
 
@@ -92,6 +92,8 @@ def load_library() -> ctypes.CDLL:
             "moe_permute_to_experts": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                         i32, i32, P, P, P, P, P, sz, P, P], ctypes.c_int),
             "moe_combine": ([P, i32, P, P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
+            "moe_permute_to_experts_masked": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                               i32, i32, P, P, P, P, P, P], ctypes.c_int),
             "moe_expert_scale": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
             "moe_trace_enable": ([ctypes.c_char_p, i32], ctypes.c_int),
             "moe_trace_disable": ([], None),
@@ -208,6 +210,26 @@ def moe_permute_to_experts(send, token_slot, topk_ids, expert_counts, expert_ran
         _dev(expert_offsets, "expert_offsets", (torch.int32,)),
         _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
         _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_permute_to_experts_masked(send, token_slot, topk_ids, expert_counts, expert_rank, E,
+                                  recv_part, block_rows, recv, masked_counts, pair_row, recv_pair,
+                                  dev_status=None, stream=None):
+    """Masked layout: recv bf16 [blocks*block_rows, H] with one fixed block per expert of the
+    receiving set, masked_counts [blocks], pair_row [S,T,k], recv_pair [blocks*block_rows]."""
+    lib = load_library()
+    S, cap_send, H = send.shape
+    _, T, P = token_slot.shape
+    k = topk_ids.shape[2]
+    _check(lib.moe_permute_to_experts_masked(
+        _dev(send, "send", _BF16_TYPES, 3), _dev(token_slot, "token_slot", (torch.int32,), 3),
+        _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)), S, T, k, E, P, H, recv_part,
+        block_rows, cap_send, _dev(recv, "recv", _BF16_TYPES, 2),
+        _dev(masked_counts, "masked_counts", (torch.int32,)),
+        _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
+        _status_ptr(dev_status), _stream(stream)))
 
 
 def moe_combine(y, pair_row, topk_w, out, dev_status=None, stream=None):

@@ -48,6 +48,13 @@ cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, cons
                            int32_t *pair_row, int32_t *recv_pair, void *ws,
                            uint32_t *dev_status, cudaStream_t st);
 
+cudaError_t launch_permute_masked(const uint16_t *send, const int32_t *token_slot,
+                                  const int32_t *ids, const int32_t *expert_counts,
+                                  const int32_t *expert_rank, int S, int T, int k, int E, int P,
+                                  int H, int recv_part, int block_rows, int cap_send,
+                                  uint16_t *recv, int32_t *masked_counts, int32_t *pair_row,
+                                  int32_t *recv_pair, uint32_t *dev_status, cudaStream_t st);
+
 cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_row, const float *w,
                            int64_t N, int k, int H, uint16_t *out, uint32_t *dev_status,
                            cudaStream_t st);

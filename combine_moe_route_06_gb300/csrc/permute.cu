@@ -155,11 +155,88 @@ __global__ void __launch_bounds__(kMapThreads) k_perm_map(
     if (__syncthreads_or(bad_id) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
 }
 
+// Masked layout map (DeepEP low-latency style, fixed block per expert): grid =
+// S * B CTAs as in k_perm_map; block b holds expert e0 + b.  Every CTA also
+// marks a share of the unused block rows in recv_pair.
+__global__ void __launch_bounds__(kMapThreads) k_perm_map_masked(
+    const int32_t *__restrict__ ids, const int32_t *__restrict__ expert_counts,
+    const int32_t *__restrict__ expert_rank, int S, int T, int k, int E, int e0, int nb,
+    int B, int block_rows, int32_t *__restrict__ masked_counts, int32_t *__restrict__ pair_row,
+    int32_t *__restrict__ recv_pair, uint32_t *dev_status)
+{
+    extern __shared__ int sm[];
+    int *cnt = sm;           // [nb] rows of block b in use
+    int *sb = sm + nb;       // [nb] pairs of its expert in sources before s
+    int *own = sb + nb;      // [nb] pairs of its expert in source s
+    constexpr int kPer = kMapPairs / kMapThreads;
+    const int s = blockIdx.x / B, b = blockIdx.x % B;
+    const int64_t per_src = (int64_t)T * k;
+    const int64_t q0 = (int64_t)s * per_src + (int64_t)b * kMapPairs;
+    const int64_t q1 = min((int64_t)s * per_src + per_src, q0 + kMapPairs);
+    pdl_wait();
+    pdl_trigger();
+
+    int e_[kPer], r_[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        const int64_t q = q0 + threadIdx.x + i * kMapThreads;
+        e_[i] = (q < q1) ? __ldg(ids + q) : -1;
+        r_[i] = (q < q1) ? __ldg(expert_rank + q) : -1;
+    }
+    for (int bb = threadIdx.x; bb < nb; bb += blockDim.x) {
+        const int e = e0 + bb;
+        int total = 0, before = 0, mine = 0;
+        for (int s2 = 0; s2 < S; s2++) {
+            const int c = __ldg(expert_counts + (int64_t)s2 * E + e);
+            total += c;
+            before += (s2 < s) ? c : 0;
+            mine = (s2 == s) ? c : mine;
+        }
+        cnt[bb] = min(total, block_rows);
+        sb[bb] = before;
+        own[bb] = mine;
+        if (blockIdx.x == 0) masked_counts[bb] = cnt[bb];
+    }
+    __syncthreads();
+
+    bool dropped = false, bad = false, bad_id = false;
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        const int64_t q = q0 + threadIdx.x + i * kMapThreads;
+        if (q >= q1) continue;
+        const int e = e_[i];
+        if (e >= E) bad_id = true;
+        int row = -1;
+        if (e >= e0 && e < e0 + nb) {
+            const int bb = e - e0, r = r_[i];
+            if (r < 0 || r >= own[bb]) {
+                bad = true;
+            } else if (sb[bb] + r >= block_rows) {
+                dropped = true;
+            } else {
+                row = bb * block_rows + sb[bb] + r;
+            }
+        }
+        pair_row[q] = row;
+        if (row >= 0) recv_pair[row] = (int32_t)q;
+    }
+    // unused rows of every block: recv_pair = -1 (spread over all CTAs)
+    const int64_t rows = (int64_t)nb * block_rows;
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+         r += (int64_t)gridDim.x * blockDim.x) {
+        const int bb = (int)(r / block_rows);
+        if (r - (int64_t)bb * block_rows >= cnt[bb]) recv_pair[r] = -1;
+    }
+    if (__syncthreads_or(dropped) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_CAPACITY);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_INVALID_ARG);
+    if (__syncthreads_or(bad_id) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
+}
+
 __global__ void __launch_bounds__(kCopyThreads) k_perm_copy(
     const int4 *__restrict__ send, const int32_t *__restrict__ token_slot,
     const int32_t *__restrict__ ids, const int32_t *__restrict__ pair_row, int64_t NT, int k,
-    int E, int L, int P, int T, int V, int recv_part, int align, int cap_send, int cap_recv,
-    const int32_t *__restrict__ expert_offsets, const int32_t *__restrict__ ws_tot,
+    int E, int L, int P, int T, int V, int recv_part, int align, int fill, int cap_send,
+    int cap_recv, const int32_t *__restrict__ expert_offsets, const int32_t *__restrict__ ws_tot,
     int4 *__restrict__ recv, int32_t *__restrict__ recv_pair, uint32_t *dev_status)
 {
     pdl_wait();
@@ -223,7 +300,7 @@ __global__ void __launch_bounds__(kCopyThreads) k_perm_copy(
     }
 
     // 2. padding rows: warp task (expert, padding row index, segment)
-    if (align > 1) {
+    if (fill && align > 1) {
         const int64_t ptask = (int64_t)E * (align - 1) * nseg;
         for (int64_t task = gtid >> 5; task < ptask; task += gwarps) {
             const int g = (int)(task % nseg);
@@ -246,8 +323,10 @@ __global__ void __launch_bounds__(kCopyThreads) k_perm_copy(
     }
 
     // 3. recv_pair entries past the used rows
-    const int used = __ldg(expert_offsets + E);
-    for (int64_t r = (int64_t)used + gtid; r < cap_recv; r += gthreads) recv_pair[r] = -1;
+    if (fill) {
+        const int used = __ldg(expert_offsets + E);
+        for (int64_t r = (int64_t)used + gtid; r < cap_recv; r += gthreads) recv_pair[r] = -1;
+    }
 
     if (cap_flag) flag_status(dev_status, MOE_ERR_CAPACITY);
     if (bad_slot) flag_status(dev_status, MOE_ERR_INVALID_ARG);
@@ -301,8 +380,46 @@ cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, cons
     MOE_TRACED_LAUNCH("k_perm_copy", st,
                       e = launch_pdl(k_perm_copy, dim3((unsigned)blocks), dim3(kCopyThreads), 0, st,
                                      (const int4 *)send, token_slot, ids, (const int32_t *)pair_row,
-                                     NT, k, E, L, P, T, V, recv_part, align, cap_send, cap_recv,
+                                     NT, k, E, L, P, T, V, recv_part, align, 1, cap_send, cap_recv,
                                      (const int32_t *)expert_offsets, (const int32_t *)ws_tot,
+                                     (int4 *)recv, recv_pair, dev_status));
+    return e;
+}
+
+cudaError_t launch_permute_masked(const uint16_t *send, const int32_t *token_slot,
+                                  const int32_t *ids, const int32_t *expert_counts,
+                                  const int32_t *expert_rank, int S, int T, int k, int E, int P,
+                                  int H, int recv_part, int block_rows, int cap_send,
+                                  uint16_t *recv, int32_t *masked_counts, int32_t *pair_row,
+                                  int32_t *recv_pair, uint32_t *dev_status, cudaStream_t st)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int64_t NT = (int64_t)S * T;
+    const int L = E / P;
+    const int nb = recv_part < 0 ? E : L;
+    const int e0 = recv_part < 0 ? 0 : recv_part * L;
+    const int B = (int)(div_up((int64_t)T * k, kMapPairs) > 0 ? div_up((int64_t)T * k, kMapPairs) : 1);
+    const size_t smem = (size_t)(3 * nb) * sizeof(int);
+    MOE_TRACED_LAUNCH("k_perm_map_masked", st,
+                      e = launch_pdl(k_perm_map_masked, dim3((unsigned)(S * B)), dim3(kMapThreads),
+                                     smem, st, ids, expert_counts, expert_rank, S, T, k, E, e0, nb,
+                                     B, block_rows, masked_counts, pair_row, recv_pair, dev_status));
+    if (e != cudaSuccess || NT == 0) return e;
+    const int V = H / 8;
+    const int nseg = (V + kCopySegVec - 1) / kCopySegVec;
+    const int resident = resident_grid((const void *)k_perm_copy, kCopyThreads, 0);
+    int64_t blocks = div_up(NT * nseg, kCopyThreads / 32);
+    const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kCopyThreads);
+    if (blocks > wave) blocks = wave;
+    if (blocks < 1) blocks = 1;
+    const int cap_recv = nb * block_rows;
+    MOE_TRACED_LAUNCH("k_perm_copy", st,
+                      e = launch_pdl(k_perm_copy, dim3((unsigned)blocks), dim3(kCopyThreads), 0, st,
+                                     (const int4 *)send, token_slot, ids, (const int32_t *)pair_row,
+                                     NT, k, E, L, P, T, V, recv_part, 1, 0, cap_send, cap_recv,
+                                     (const int32_t *)nullptr, (const int32_t *)nullptr,
                                      (int4 *)recv, recv_pair, dev_status));
     return e;
 }

@@ -221,6 +221,33 @@ moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_s
                                     size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Masked receive layout (a2a-backends section 4.1: a region per (local expert,
+ * sender) with room for the cap; section 4.2: the receiver packs each expert's
+ * rows together, writes a per-expert count on the device, and the output has a
+ * fixed shape -- 48 x 8 x 128 rows for the decode example; section 5.2: the
+ * masked expert kernel reads fixed-size blocks).
+ *   Same inputs as moe_permute_to_experts.  The receiving set (recv_part, or
+ *   all experts if -1) has nb experts; expert b of the set owns rows
+ *   [b*block_rows, (b+1)*block_rows) of recv.
+ *   recv          [nb*block_rows][H] bf16 out: the pairs of each expert in
+ *                 ascending (s, t, j) order from the first row of its block;
+ *                 rows past masked_counts[b] are not written.
+ *   masked_counts [nb] int32 out: rows of each block in use (<= block_rows).
+ *   pair_row      [S][T][k] int32 out: row of each pair or -1.
+ *   recv_pair     [nb*block_rows] int32 out: pair id of used rows, -1 otherwise.
+ * Pairs past a block's end are dropped and flag MOE_ERR_CAPACITY (the page's
+ * "the call fails if the batch is larger than the cap", here without failing).
+ * Needs no workspace.  moe_combine reads this layout through pair_row.
+ */
+moe_status_t moe_permute_to_experts_masked(const uint16_t *send, const int32_t *token_slot,
+                                           const int32_t *topk_ids, const int32_t *expert_counts,
+                                           const int32_t *expert_rank, int S, int T, int k,
+                                           int E, int P, int H, int recv_part, int block_rows,
+                                           int cap_send, uint16_t *recv, int32_t *masked_counts,
+                                           int32_t *pair_row, int32_t *recv_pair,
+                                           uint32_t *dev_status, cudaStream_t stream);
+
+/*
  * Weighted combine (a2a-backends section 1.1: the MoE output is the sum of
  * the chosen experts' outputs, each multiplied by its weight; section 7.1:
  * the home side sums in 32-bit floats; section 7.2: bf16 on the wire).

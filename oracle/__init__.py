@@ -64,10 +64,14 @@ def _load():
             lib.oracle_expert_scale.argtypes = [P, P, P, i32, i32, i64, P]
             lib.oracle_permute_masked.argtypes = [P, P, P, i32, i64, i32, i32, i32, i32, i32,
                                                   i64, i64, P, P, P, P, P]
+            lib.oracle_combine_stage1.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32, i32,
+                                                  i32, i64, P, P]
+            lib.oracle_combine_stage2.argtypes = [P, P, i32, i64, i32, i32, i64, P, P]
             lib.oracle_combine.argtypes = [P, P, P, i32, i64, i32, i32, P]
             for f in ("oracle_route_topk", "oracle_dispatch_layout", "oracle_dispatch_pack",
                       "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine",
-                      "oracle_permute_masked"):
+                      "oracle_permute_masked", "oracle_combine_stage1",
+                      "oracle_combine_stage2"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -232,6 +236,43 @@ def combine(y: np.ndarray, pair_row: np.ndarray, w: np.ndarray) -> np.ndarray:
     out = np.empty((S, T, H), np.uint16)
     _check(_load().oracle_combine(_p(y), _p(pair_row), _p(w), S, T, k, H, _p(out)), "combine")
     return out
+
+
+def combine_stage1(y: np.ndarray, pair_row: np.ndarray, w: np.ndarray, ids: np.ndarray,
+                   token_slot: np.ndarray, E: int, cap_send: int, recv_part: int = -1,
+                   ret: np.ndarray | None = None):
+    """Stage 1 of the split combine: one pre-added bf16 row per (token, partition) slot.
+
+    Returns (ret [S, cap_send, H], status); rows without a slot keep the `ret` passed in.
+    """
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    pair_row = np.ascontiguousarray(pair_row, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    S, T, k = pair_row.shape
+    P = token_slot.shape[2]
+    H = y.shape[1]
+    if ret is None:
+        ret = np.zeros((S, cap_send, H), np.uint16)
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_combine_stage1(_p(y), _p(pair_row), _p(w), _p(ids), _p(token_slot), S, T,
+                                         k, E, P, H, recv_part, cap_send, _p(ret), _p(st)),
+           "combine_stage1")
+    return ret, int(st[0])
+
+
+def combine_stage2(ret: np.ndarray, token_slot: np.ndarray):
+    """Stage 2: out[s, t] = bf16(sum of the token's returned rows), double sum; (out, status)."""
+    ret = np.ascontiguousarray(ret, dtype=np.uint16)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    S, cap_send, H = ret.shape
+    _, T, P = token_slot.shape
+    out = np.empty((S, T, H), np.uint16)
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_combine_stage2(_p(ret), _p(token_slot), S, T, P, H, cap_send, _p(out),
+                                         _p(st)), "combine_stage2")
+    return out, int(st[0])
 
 
 def run_path(x: np.ndarray, logits: np.ndarray, E: int, k: int, P: int, scales: np.ndarray | None,

@@ -514,3 +514,95 @@ int oracle_combine(const uint16_t *y, const int32_t *pair_row, const float *w,
     free(acc);
     return 0;
 }
+
+/* --------------------------------------------- two-stage combine, [a2a] 7.1 */
+
+/*
+ * [a2a] 7.1 splits a token's weighted sum into a sum over the experts that sit
+ * on one GPU (stage 1, before the rows travel back; DeepEP's combine and
+ * FlashInfer's routed kernel pre-add there) and a sum over the GPUs at home
+ * (stage 2, in 32-bit floats for FlashInfer).  Each token then returns as many
+ * rows as it sent: one per destination partition.  Rows travel as bf16
+ * ([a2a] 7.2), so stage 1 rounds once to bf16.
+ *
+ * Stage 1, for every (s, t, p) with p in the receiving set and a send slot
+ * 0 <= slot < cap_send:
+ *   ret[s][slot] = bf16( sum over j with part(ids[s][t][j]) == p and
+ *                        pair_row >= 0 of w[s][t][j] * y[pair_row] )   (double sum)
+ * Stage 2:
+ *   out[s][t] = bf16( sum over p with 0 <= token_slot[s][t][p] < cap_send of
+ *                     ret[s][token_slot[s][t][p]] )                  (double sum)
+ * A token without slots gets +0.  Slots >= cap_send flag capacity.
+ */
+int oracle_combine_stage1(const uint16_t *y, const int32_t *pair_row, const float *w,
+                          const int32_t *ids, const int32_t *token_slot, int S, int64_t T, int k,
+                          int E, int P, int H, int recv_part, int64_t cap_send, uint16_t *ret,
+                          uint32_t *status)
+{
+    if (P < 1 || E % P != 0 || recv_part < -1 || recv_part >= P)
+        return -1;
+    const int L = E / P;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    if (!acc)
+        return -2;
+    for (int s = 0; s < S; s++) {
+        for (int64_t t = 0; t < T; t++) {
+            const int64_t n = (int64_t)s * T + t;
+            for (int p = 0; p < P; p++) {
+                if (recv_part >= 0 && p != recv_part)
+                    continue;
+                int32_t slot = token_slot[n * P + p];
+                if (slot < 0)
+                    continue;
+                if (slot >= cap_send) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue;
+                }
+                for (int h = 0; h < H; h++)
+                    acc[h] = 0.0;
+                for (int j = 0; j < k; j++) {
+                    int32_t e = ids[n * k + j], r = pair_row[n * k + j];
+                    if (e < 0 || e >= E || e / L != p || r < 0)
+                        continue;
+                    double wj = (double)w[n * k + j];
+                    for (int h = 0; h < H; h++)
+                        acc[h] += wj * oracle_bf16_to_double(y[(int64_t)r * H + h]);
+                }
+                for (int h = 0; h < H; h++)
+                    ret[((int64_t)s * cap_send + slot) * H + h] = oracle_bf16_from_double(acc[h]);
+            }
+        }
+    }
+    free(acc);
+    return 0;
+}
+
+int oracle_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int64_t T,
+                          int P, int H, int64_t cap_send, uint16_t *out, uint32_t *status)
+{
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    if (!acc)
+        return -2;
+    for (int s = 0; s < S; s++) {
+        for (int64_t t = 0; t < T; t++) {
+            const int64_t n = (int64_t)s * T + t;
+            for (int h = 0; h < H; h++)
+                acc[h] = 0.0;
+            for (int p = 0; p < P; p++) {
+                int32_t slot = token_slot[n * P + p];
+                if (slot < 0)
+                    continue;
+                if (slot >= cap_send) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue;
+                }
+                for (int h = 0; h < H; h++)
+                    acc[h] += oracle_bf16_to_double(ret[((int64_t)s * cap_send + slot) * H + h]);
+            }
+            for (int h = 0; h < H; h++)
+                out[n * H + h] = oracle_bf16_from_double(acc[h]);
+        }
+    }
+    free(acc);
+    return 0;
+}

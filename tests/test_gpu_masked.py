@@ -1,0 +1,109 @@
+"""Masked receive layout (a2a-backends sections 4.1-4.2) on the GPU vs the oracle.
+
+Bit-exact: counts, pair rows, recv_pair and every used row; rows past each
+block's count are not written (checked with a canary fill on both sides).
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_moe_route_06_gb300 as m
+import moe_synth as ms
+import oracle
+from gpu_util import DEV, bf16_dev, bf16_host, close_bf16, f32_dev, host, i32_dev
+
+pytestmark = pytest.mark.gpu
+
+CAP = m.status_bit(m.MOE_ERR_CAPACITY)
+FILL = 0x5A5A
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load_library()
+
+
+def _case(name, S=None, index=None):
+    kw = {}
+    if S is not None:
+        kw["S"] = S
+    if index is not None:
+        kw["index"] = index
+    w_ = ms.workload(name, **kw)
+    inp = ms.gen_inputs(w_)
+    ids, wt = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap_send = w_.T * min(w_.k, w_.P)
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap_send)
+    return w_, inp, ids, wt, lay, send
+
+
+def _masked_gpu(send, lay, ids, E, recv_part, block_rows):
+    S, cap_send, H = send.shape
+    _, T, P = lay["token_slot"].shape
+    k = ids.shape[2]
+    nb = E if recv_part < 0 else E // P
+    recv = bf16_dev(np.full((nb * block_rows, H), FILL, np.uint16))
+    counts = torch.full((nb,), -7, dtype=torch.int32, device=DEV)
+    pr = torch.full((S, T, k), -7, dtype=torch.int32, device=DEV)
+    rp = torch.full((nb * block_rows,), -7, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.moe_permute_to_experts_masked(bf16_dev(send), i32_dev(lay["token_slot"]), i32_dev(ids),
+                                    i32_dev(lay["expert_counts"]), i32_dev(lay["expert_rank"]), E,
+                                    recv_part, block_rows, recv, counts, pr, rp, st)
+    torch.cuda.synchronize()
+    return {"recv": bf16_host(recv), "masked_counts": host(counts), "pair_row": host(pr),
+            "recv_pair": host(rp), "status": int(st.item()), "recv_dev": recv, "pair_row_dev": pr}
+
+
+def _check(send, lay, ids, E, recv_part, block_rows):
+    got = _masked_gpu(send, lay, ids, E, recv_part, block_rows)
+    H = send.shape[2]
+    nb = E if recv_part < 0 else E // lay["token_slot"].shape[2]
+    ref = oracle.permute_masked(send, lay["token_slot"], ids, E, recv_part, block_rows,
+                                recv=np.full((nb * block_rows, H), FILL, np.uint16))
+    for key in ("masked_counts", "pair_row", "recv_pair"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert np.array_equal(got["recv"], ref["recv"])
+    assert got["status"] == ref["status"]
+    return got, ref
+
+
+@pytest.mark.parametrize("recv_part,block_rows", [(0, 1024), (5, 1024), (-1, 64), (3, 4)])
+def test_masked_decode_from_8_sources(recv_part, block_rows):
+    w_, inp, ids, wt, lay, send = _case("decode", S=8, index=11)
+    got, ref = _check(send, lay, ids, w_.E, recv_part, block_rows)
+    if block_rows == 4:
+        assert got["status"] & CAP
+
+
+@pytest.mark.parametrize("block_rows", [128, 32])
+def test_masked_prefill_all_experts(block_rows):
+    w_, inp, ids, wt, lay, send = _case("prefill")
+    _check(send, lay, ids, w_.E, -1, block_rows)
+
+
+def test_masked_tiny_ragged():
+    w_, inp, ids, wt, lay, send = _case("tiny", S=3)
+    for rp, br in ((-1, 40), (1, 200), (2, 7)):
+        _check(send, lay, ids, w_.E, rp, br)
+
+
+def test_combine_over_masked_equals_combine_over_contiguous():
+    """The combine reads either layout through pair_row and returns the same bytes."""
+    w_, inp, ids, wt, lay, send = _case("decode")
+    got = _masked_gpu(send, lay, ids, w_.E, -1, 64)
+    assert got["status"] == 0
+    w32 = torch.from_numpy(wt.astype(np.float32)).to(DEV)
+    out_m = torch.zeros((w_.S, w_.T, w_.H), dtype=torch.bfloat16, device=DEV)
+    m.moe_combine(got["recv_dev"], got["pair_row_dev"], w32, out_m)
+    per = oracle.permute_to_experts(send, lay["token_slot"], ids, w_.E)
+    out_c = torch.zeros_like(out_m)
+    m.moe_combine(bf16_dev(per["recv"]), i32_dev(per["pair_row"]), w32, out_c)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host(out_m), bf16_host(out_c))
+    ref = oracle.combine(per["recv"], per["pair_row"], wt.astype(np.float32))
+    assert close_bf16(bf16_host(out_m), ref)

@@ -554,3 +554,57 @@ def test_masked_overflow_keeps_first_pairs():
         assert per["masked_counts"][b] == keep.size
         assert np.array_equal(per["recv_pair"][b * block:b * block + keep.size], keep)
         assert np.all(per["pair_row"].reshape(-1)[q[block:]] == -1)
+
+
+# ------------------------------------------------ two-stage combine (a2a 7.1) --
+
+def _staged(name, scales_identity=False, S=None):
+    w_ = ms.workload(name) if S is None else ms.workload(name, S=S)
+    inp = ms.gen_inputs(w_)
+    sc = ms.gen_scales(w_, identity=scales_identity)
+    r = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, sc)
+    cap_send = w_.T * min(w_.k, w_.P)
+    w32 = r["w"].astype(np.float32)
+    ret, st1 = oracle.combine_stage1(r["y"], r["permute"]["pair_row"], w32, r["ids"],
+                                     r["layout"]["token_slot"], w_.E, cap_send)
+    out, st2 = oracle.combine_stage2(ret, r["layout"]["token_slot"])
+    return w_, inp, r, ret, out, st1 | st2
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_two_stage_matches_single_stage(name):
+    w_, inp, r, ret, out, st = _staged(name)
+    assert st == 0
+    ref = ms.f32_from_bf16_bits(r["out"]).astype(np.float64)
+    got = ms.f32_from_bf16_bits(out).astype(np.float64)
+    # one extra bf16 rounding per partial row (at most min(k, P) of them)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -6 * np.maximum(np.abs(ref), 1e-3))
+
+
+def test_two_stage_returns_one_row_per_copy():
+    # a2a 7.1: each way returns as many rows as it sent (one per destination partition)
+    w_, inp, r, ret, out, st = _staged("tiny", S=2)
+    lay = r["layout"]
+    for s in range(w_.S):
+        used = int(lay["part_offsets"][s, -1])
+        slots = lay["token_slot"][s]
+        assert (slots >= 0).sum() == used
+        # every used return row is the pre-added sum of that partition's experts
+        L = w_.E // w_.P
+        t, p = 5, int(np.nonzero(slots[5] >= 0)[0][0])
+        row = ret[s, slots[t, p]]
+        ids = r["ids"][s, t]
+        pr = r["permute"]["pair_row"][s, t]
+        wt = r["w"][s, t].astype(np.float32).astype(np.float64)
+        acc = sum(wt[j] * ms.f32_from_bf16_bits(r["y"][pr[j]]).astype(np.float64)
+                  for j in range(w_.k) if ids[j] // L == p)
+        # rounded once from double (the bf16 rounding itself is pinned above)
+        want = np.array([oracle.bf16_from_double(float(v)) for v in acc], np.uint16)
+        assert np.array_equal(row, want)
+
+
+def test_two_stage_identity_round_trip_close():
+    w_, inp, r, ret, out, st = _staged("decode", scales_identity=True)
+    x = ms.f32_from_bf16_bits(inp["x"]).astype(np.float64)
+    got = ms.f32_from_bf16_bits(out).astype(np.float64)
+    assert np.all(np.abs(got - x) <= 2.0 ** -6 * np.maximum(np.abs(x), 1e-3))
