@@ -26,7 +26,8 @@ __all__ = [
     "MOE_ERR_TIMEOUT", "MOE_ERR_CUDA", "status_bit", "MoeError", "MoeLibraryMissing",
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
-    "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
+    "moe_combine_stage2", "MoePath", "trace_enable", "trace_disable", "trace_reset",
     "trace_records",
 ]
 
@@ -92,6 +93,9 @@ def load_library() -> ctypes.CDLL:
             "moe_permute_to_experts": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                         i32, i32, P, P, P, P, P, sz, P, P], ctypes.c_int),
             "moe_combine": ([P, i32, P, P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
+            "moe_combine_stage1": ([P, i32, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P,
+                                    P, P], ctypes.c_int),
+            "moe_combine_stage2": ([P, P, i32, i32, i32, i32, i32, P, P, P], ctypes.c_int),
             "moe_permute_to_experts_masked": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                i32, i32, P, P, P, P, P, P], ctypes.c_int),
             "moe_expert_scale": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
@@ -242,6 +246,31 @@ def moe_combine(y, pair_row, topk_w, out, dev_status=None, stream=None):
                            _dev(topk_w, "topk_w", (torch.float32,), 3), S, T, k, H,
                            _dev(out, "out", _BF16_TYPES, 3), _status_ptr(dev_status),
                            _stream(stream)))
+
+
+def moe_combine_stage1(y, pair_row, topk_w, topk_ids, token_slot, E, recv_part, ret,
+                       dev_status=None, stream=None):
+    """Pre-add per (token, partition) slot: ret bf16 [S, cap_send, H] in the send layout."""
+    lib = load_library()
+    S, T, k = pair_row.shape
+    P = token_slot.shape[2]
+    _, cap_send, H = ret.shape
+    _check(lib.moe_combine_stage1(
+        _dev(y, "y", _BF16_TYPES, 2), y.shape[0], _dev(pair_row, "pair_row", (torch.int32,), 3),
+        _dev(topk_w, "topk_w", (torch.float32,), 3), _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+        _dev(token_slot, "token_slot", (torch.int32,), 3), S, T, k, E, P, H, recv_part, cap_send,
+        _dev(ret, "ret", _BF16_TYPES, 3), _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_combine_stage2(ret, token_slot, out, dev_status=None, stream=None):
+    """Home-side sum of a token's returned rows: out bf16 [S, T, H]."""
+    lib = load_library()
+    S, cap_send, H = ret.shape
+    _, T, P = token_slot.shape
+    _check(lib.moe_combine_stage2(
+        _dev(ret, "ret", _BF16_TYPES, 3), _dev(token_slot, "token_slot", (torch.int32,), 3), S, T,
+        P, H, cap_send, _dev(out, "out", _BF16_TYPES, 3), _status_ptr(dev_status),
+        _stream(stream)))
 
 
 def moe_expert_scale(recv, expert_offsets, scale, y, stream=None):

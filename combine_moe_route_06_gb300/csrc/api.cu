@@ -317,6 +317,52 @@ moe_status_t moe_combine(const uint16_t *y, int y_rows, const int32_t *pair_row,
         launch_combine(y, y_rows, pair_row, topk_w, NT, k, H, out, dev_status, stream), __func__);
 }
 
+moe_status_t moe_combine_stage1(const uint16_t *y, int y_rows, const int32_t *pair_row,
+                                const float *topk_w, const int32_t *topk_ids,
+                                const int32_t *token_slot, int S, int T, int k, int E, int P,
+                                int H, int recv_part, int cap_send, uint16_t *ret,
+                                uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, P)", __func__,
+            recv_part);
+    REQUIRE(y_rows >= 0 && cap_send >= 0, "%s: y_rows and cap_send must be >= 0", __func__);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(y, (int64_t)y_rows * H, 16);
+    REQUIRE_ARR(pair_row, NT * k, 4);
+    REQUIRE_ARR(topk_w, NT * k, 4);
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(ret, (int64_t)S * cap_send * H, 16);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(launch_combine_stage1(y, y_rows, pair_row, topk_w, topk_ids, token_slot, S,
+                                             T, k, E, P, H, recv_part, cap_send, ret, dev_status,
+                                             stream),
+                       __func__);
+}
+
+moe_status_t moe_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
+                                int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
+                                cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(ret, (int64_t)S * cap_send * H, 16);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(out, NT * H, 16);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(
+        launch_combine_stage2(ret, token_slot, S, T, P, H, cap_send, out, dev_status, stream),
+        __func__);
+}
+
 moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
                               const float *scale, int E, int H, int cap_recv, uint16_t *y,
                               cudaStream_t stream)

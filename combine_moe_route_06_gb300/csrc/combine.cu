@@ -120,6 +120,166 @@ __global__ void __launch_bounds__(kCombThreads) k_combine(const int4 *__restrict
     if (bad_row) flag_status(dev_status, MOE_ERR_INVALID_ARG);
 }
 
+// Stage 1 of the split combine (a2a-backends section 7.1): one warp per
+// (token, 1 KiB segment); for every partition of the receiving set that holds
+// a send slot of the token, the weighted sum of the token's experts in that
+// partition (fp32 FMAs in j order) is rounded once to bf16 and written to the
+// slot's row of `ret` (send layout: the rows travel back the way they came).
+__global__ void __launch_bounds__(kCombThreads) k_combine_stage1(
+    const int4 *__restrict__ y, int y_rows, const int32_t *__restrict__ pair_row,
+    const float *__restrict__ w, const int32_t *__restrict__ ids,
+    const int32_t *__restrict__ token_slot, int64_t N, int T, int k, int E, int L, int P, int V,
+    int recv_part, int cap_send, int4 *__restrict__ ret, uint32_t *dev_status)
+{
+    pdl_wait();
+    pdl_trigger();
+    bool bad_row = false, cap_flag = false;
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    const int64_t ntask = N * nseg;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
+         task += gwarps) {
+        const int64_t n = task / nseg;
+        const int g = (int)(task - n * nseg);
+        const int s = (int)(n / T);
+        int pr = -1, pj = -1, slot = -1;
+        float wj = 0.f;
+        if (lane < k) {
+            pr = __ldg(pair_row + n * k + lane);
+            wj = __ldg(w + n * k + lane);
+            const int e = __ldg(ids + n * k + lane);
+            if (e >= 0 && e < E) pj = e / L;
+            if (pr >= y_rows) {
+                if (g == 0) bad_row = true;
+                pr = -1;
+            }
+        }
+        bool in_r = false;
+        if (lane < P) {
+            slot = __ldg(token_slot + n * P + lane);
+            in_r = (recv_part < 0 || lane == recv_part) && slot >= 0;
+            if (in_r && slot >= cap_send) {
+                if (g == 0) cap_flag = true;
+                in_r = false;
+            }
+        }
+        unsigned smask = __ballot_sync(kFull, in_r);
+        const int v0 = g * kCombSegVec + lane;
+        while (smask) {
+            const int p0 = __ffs(smask) - 1;
+            smask &= smask - 1;
+            const int slot0 = __shfl_sync(kFull, slot, p0);
+            unsigned jmask = __ballot_sync(kFull, pr >= 0 && pj == p0);
+            float acc[8 * kCombUnroll];
+#pragma unroll
+            for (int i = 0; i < 8 * kCombUnroll; i++) acc[i] = 0.f;
+            while (jmask) {
+                int4 r[kCombBatch][kCombUnroll];
+                float wb[kCombBatch];
+                int nb = 0;
+#pragma unroll
+                for (int b = 0; b < kCombBatch; b++) {
+                    if (jmask) {
+                        const int j = __ffs(jmask) - 1;
+                        jmask &= jmask - 1;
+                        const int row = __shfl_sync(kFull, pr, j);
+                        wb[b] = __shfl_sync(kFull, wj, j);
+                        const int4 *src = y + (int64_t)row * V;
+#pragma unroll
+                        for (int u = 0; u < kCombUnroll; u++) {
+                            const int vi = v0 + 32 * u;
+                            r[b][u] = (vi < V) ? ld_stream(src + vi) : make_int4(0, 0, 0, 0);
+                        }
+                        nb = b + 1;
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kCombBatch; b++) {
+                    if (b < nb) {
+#pragma unroll
+                        for (int u = 0; u < kCombUnroll; u++) fma_bf16x8(acc + 8 * u, r[b][u], wb[b]);
+                    }
+                }
+            }
+            int4 *dst = ret + ((int64_t)s * cap_send + slot0) * V;
+#pragma unroll
+            for (int u = 0; u < kCombUnroll; u++) {
+                const int vi = v0 + 32 * u;
+                if (vi < V) st_cg(dst + vi, pack_bf16x8(acc + 8 * u));
+            }
+        }
+    }
+    if (bad_row) flag_status(dev_status, MOE_ERR_INVALID_ARG);
+    if (cap_flag) flag_status(dev_status, MOE_ERR_CAPACITY);
+}
+
+// Stage 2: one warp per (token, 1 KiB segment); the token's returned rows (one
+// per send slot, partitions in ascending order) summed with fp32 adds, one bf16
+// rounding.
+__global__ void __launch_bounds__(kCombThreads) k_combine_stage2(
+    const int4 *__restrict__ ret, const int32_t *__restrict__ token_slot, int64_t N, int T,
+    int P, int V, int cap_send, int4 *__restrict__ out, uint32_t *dev_status)
+{
+    pdl_wait();
+    pdl_trigger();
+    bool cap_flag = false;
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    const int64_t ntask = N * nseg;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
+         task += gwarps) {
+        const int64_t n = task / nseg;
+        const int g = (int)(task - n * nseg);
+        const int s = (int)(n / T);
+        int slot = -1;
+        if (lane < P) slot = __ldg(token_slot + n * P + lane);
+        if (slot >= cap_send) {
+            if (g == 0) cap_flag = true;
+            slot = -1;
+        }
+        unsigned vmask = __ballot_sync(kFull, slot >= 0);
+        const int v0 = g * kCombSegVec + lane;
+        float acc[8 * kCombUnroll];
+#pragma unroll
+        for (int i = 0; i < 8 * kCombUnroll; i++) acc[i] = 0.f;
+        while (vmask) {
+            int4 r[kCombBatch][kCombUnroll];
+            int nb = 0;
+#pragma unroll
+            for (int b = 0; b < kCombBatch; b++) {
+                if (vmask) {
+                    const int p = __ffs(vmask) - 1;
+                    vmask &= vmask - 1;
+                    const int sl = __shfl_sync(kFull, slot, p);
+                    const int4 *src = ret + ((int64_t)s * cap_send + sl) * V;
+#pragma unroll
+                    for (int u = 0; u < kCombUnroll; u++) {
+                        const int vi = v0 + 32 * u;
+                        r[b][u] = (vi < V) ? ld_stream(src + vi) : make_int4(0, 0, 0, 0);
+                    }
+                    nb = b + 1;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kCombBatch; b++) {
+                if (b < nb) {
+#pragma unroll
+                    for (int u = 0; u < kCombUnroll; u++) fma_bf16x8(acc + 8 * u, r[b][u], 1.f);
+                }
+            }
+        }
+        int4 *dst = out + n * V;
+#pragma unroll
+        for (int u = 0; u < kCombUnroll; u++) {
+            const int vi = v0 + 32 * u;
+            if (vi < V) st_stream(dst + vi, pack_bf16x8(acc + 8 * u));
+        }
+    }
+    if (cap_flag) flag_status(dev_status, MOE_ERR_CAPACITY);
+}
+
 // Stand-in expert: one warp per (row, 2 KiB segment); expert of the row by
 // binary search over the run starts.
 __global__ void __launch_bounds__(256) k_expert_scale(const int4 *__restrict__ recv,
@@ -203,6 +363,46 @@ cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offs
                       e = launch_pdl(k_expert_scale, dim3(blocks), dim3(256),
                                      (size_t)(E + 1) * sizeof(int), st, (const int4 *)recv,
                                      expert_offsets, scale, E, H / 8, cap_recv, (int4 *)y));
+    return e;
+}
+
+cudaError_t launch_combine_stage1(const uint16_t *y, int y_rows, const int32_t *pair_row,
+                                  const float *w, const int32_t *ids, const int32_t *token_slot,
+                                  int S, int T, int k, int E, int P, int H, int recv_part,
+                                  int cap_send, uint16_t *ret, uint32_t *dev_status, cudaStream_t st)
+{
+    const int64_t N = (int64_t)S * T;
+    if (N == 0) return cudaSuccess;
+    const int V = H / 8;
+    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    int64_t blocks = (N * nseg + (kCombThreads / 32) - 1) / (kCombThreads / 32);
+    const int resident = resident_grid((const void *)k_combine_stage1, kCombThreads, 0);
+    if (resident > 0 && blocks > resident) blocks = resident;
+    cudaError_t e;
+    MOE_TRACED_LAUNCH("k_combine_stage1", st,
+                      e = launch_pdl(k_combine_stage1, dim3((unsigned)blocks), dim3(kCombThreads),
+                                     0, st, (const int4 *)y, y_rows, pair_row, w, ids, token_slot,
+                                     N, T, k, E, E / P, P, V, recv_part, cap_send, (int4 *)ret,
+                                     dev_status));
+    return e;
+}
+
+cudaError_t launch_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
+                                  int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
+                                  cudaStream_t st)
+{
+    const int64_t N = (int64_t)S * T;
+    if (N == 0) return cudaSuccess;
+    const int V = H / 8;
+    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    int64_t blocks = (N * nseg + (kCombThreads / 32) - 1) / (kCombThreads / 32);
+    const int resident = resident_grid((const void *)k_combine_stage2, kCombThreads, 0);
+    if (resident > 0 && blocks > resident) blocks = resident;
+    cudaError_t e;
+    MOE_TRACED_LAUNCH("k_combine_stage2", st,
+                      e = launch_pdl(k_combine_stage2, dim3((unsigned)blocks), dim3(kCombThreads),
+                                     0, st, (const int4 *)ret, token_slot, N, T, P, V, cap_send,
+                                     (int4 *)out, dev_status));
     return e;
 }
 

@@ -59,6 +59,15 @@ cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_ro
                            int64_t N, int k, int H, uint16_t *out, uint32_t *dev_status,
                            cudaStream_t st);
 
+cudaError_t launch_combine_stage1(const uint16_t *y, int y_rows, const int32_t *pair_row,
+                                  const float *w, const int32_t *ids, const int32_t *token_slot,
+                                  int S, int T, int k, int E, int P, int H, int recv_part,
+                                  int cap_send, uint16_t *ret, uint32_t *dev_status,
+                                  cudaStream_t st);
+cudaError_t launch_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
+                                  int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
+                                  cudaStream_t st);
+
 cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
                                 const float *scale, int E, int H, int cap_recv, uint16_t *y,
                                 cudaStream_t st);

@@ -266,6 +266,37 @@ moe_status_t moe_combine(const uint16_t *y, int y_rows, const int32_t *pair_row,
                          uint32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Two-stage combine (a2a-backends section 7.1: the weighted sum over a token's
+ * experts splits into a sum over the experts that sit on one GPU, taken before
+ * the rows travel back -- DeepEP's combine and FlashInfer's routed kernel
+ * pre-add there -- and a sum over GPUs at home; each token then returns as
+ * many rows as it sent, about 4.43 instead of 6 for the page's model;
+ * section 7.2: the returned rows are bf16).
+ *
+ * moe_combine_stage1 (expert side), for every (s, t, p) with p in the
+ * receiving set (recv_part, or all partitions if -1) and a send slot
+ * 0 <= token_slot[s][t][p] < cap_send:
+ *   ret[s][slot] = bf16_rne( sum over j in ascending order with pair_row >= 0
+ *                  and topk_ids[s][t][j] in partition p of topk_w * float(y[row]) )
+ *   y [y_rows][H] bf16 (expert outputs, contiguous or masked layout, addressed
+ *   by pair_row); ret [S][cap_send][H] bf16 (the send layout).  Rows of ret
+ *   without such a slot are not written.  pair_row >= y_rows is skipped and
+ *   flags MOE_ERR_INVALID_ARG.
+ * moe_combine_stage2 (home side):
+ *   out[s][t] = bf16_rne( sum over p ascending with 0 <= token_slot < cap_send
+ *               of float(ret[s][token_slot[s][t][p]]) ), fp32 adds; +0 if none.
+ * Slots >= cap_send flag MOE_ERR_CAPACITY in both stages.
+ */
+moe_status_t moe_combine_stage1(const uint16_t *y, int y_rows, const int32_t *pair_row,
+                                const float *topk_w, const int32_t *topk_ids,
+                                const int32_t *token_slot, int S, int T, int k, int E, int P,
+                                int H, int recv_part, int cap_send, uint16_t *ret,
+                                uint32_t *dev_status, cudaStream_t stream);
+moe_status_t moe_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
+                                int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
+                                cudaStream_t stream);
+
+/*
  * Stand-in expert for tests and benchmarks -- NOT a step of the method (the
  * pages time dispatch and combine without the expert kernel, a2a-backends
  * section 8.1).  y[r] = bf16_rne(float(recv[r]) * scale[e]) for every row r
