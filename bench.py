@@ -45,11 +45,13 @@ DOMINANT_TRAFFIC = {"prefill": 142.5e6 + 252.3e6}
 
 # ------------------------------------------------------------ byte model --
 
-def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv):
+def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_stage=False):
     """Bytes each call must read + write at minimum.
 
     copies: rows packed (sum of part_offsets[s][P]); copies_recv: packed rows
     bound for the receiving partition(s); pairs_recv: permuted pair rows.
+    two_stage: the combine pre-adds per (token, partition) slot (copies_recv
+    rows written and read back) before the per-token sum.
     """
     NT = S * T
     b = {
@@ -59,6 +61,9 @@ def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv):
         "permute": copies_recv * H * 2 + pairs_recv * H * 2 + NT * k * 8,
         "combine": pairs_recv * H * 2 + NT * k * 8 + NT * H * 2,
     }
+    if two_stage:
+        b["combine"] = (pairs_recv * H * 2 + NT * k * 12 + copies_recv * H * 2      # stage 1
+                        + copies_recv * H * 2 + NT * P * 4 + NT * H * 2)            # stage 2
     b["dispatch_combine"] = b["layout"] + b["pack"] + b["permute"] + b["combine"]
     b["step"] = b["route"] + b["dispatch_combine"]
     b["perm_copy"] = copies_recv * H * 2 + pairs_recv * H * 2 + NT * k * 8
@@ -266,14 +271,33 @@ def run_reference(args, world, rank):
     return 0
 
 
-def workload_config(w, l2):
+def workload_config(w, l2, variant="contiguous"):
     return {"workload": f"{w.name}: S={w.S} T={w.T} H={w.H} bf16, E={w.E} top-{w.k}, "
                         f"P={w.P} partitions, recv_part={w.recv_part}",
+            "variant": variant,
             "tokens_per_rank": w.S * w.T, "hidden": w.H, "experts": w.E, "topk": w.k,
             "partitions": w.P, "l2": l2, "value_scope": "route+layout+pack+permute+combine"}
 
 
 # ------------------------------------------------------------ GPU arm --
+
+VARIANTS = {
+    "contiguous": {},
+    "masked": {"layout": "masked"},
+    "two_stage": {"combine": "two_stage"},
+}
+
+
+def path_kwargs(args, w):
+    """MoePath options of the --variant.  Masked blocks default to room for four
+    times the mean pairs per expert (at least 64 rows, at most every token of
+    every source); the JSON line's dev_status shows whether any pair was dropped."""
+    kw = dict(VARIANTS[args.variant])
+    if kw.get("layout") == "masked":
+        mean = -(-w.S * w.T * w.k // w.E)
+        kw["block_rows"] = args.block_rows or min(w.S * w.T, max(64, 4 * mean))
+    return kw
+
 
 def run_profile(args, local):
     """Small, quiet run for ncu: warm-up + K steps of the bound path, no flush
@@ -288,7 +312,8 @@ def run_profile(args, local):
     w = ms.workload(args.workload)
     inp = ms.gen_inputs(w)
     stream = torch.cuda.Stream(device=dev)
-    path = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev)
+    path = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev,
+                     **path_kwargs(args, w))
     logits = torch.from_numpy(inp["logits"]).to(dev)
     x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     calls = path.bind(logits, x, stream)
@@ -315,7 +340,8 @@ def run_ours(args, world, rank, local):
     w = rank_workload(args.workload, rank)
     inp = ms.gen_inputs(w)
     stream = torch.cuda.Stream(device=dev)
-    path = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev)
+    pkw = path_kwargs(args, w)
+    path = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev, **pkw)
     logits = torch.from_numpy(inp["logits"]).to(dev)
     x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)   # 1 GiB > L2 (~126 MiB)
@@ -348,8 +374,9 @@ def run_ours(args, world, rank, local):
         status = int(path.dev_status.item())
         copies = int(path.part_offsets[:, -1].sum().item())
         copies_recv = copies if w.recv_part < 0 else int(path.part_counts[:, w.recv_part].sum().item())
-        pairs_recv = int(path.expert_offsets[-1].item())
-        b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv)
+        pairs_recv = int((path.pair_row >= 0).sum().item())
+        b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv,
+                              two_stage=(args.variant == "two_stage"))
 
         # ---------------- the step as a CUDA graph (fixed shapes and addresses) ---
         # The five calls are recorded once and replayed, as a serving engine
@@ -427,7 +454,7 @@ def run_ours(args, world, rank, local):
         Ke = max(10, min(K, 200))
         s_in = torch.cuda.Stream(device=dev)
         s_out = torch.cuda.Stream(device=dev)
-        path2 = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev)
+        path2 = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev, **pkw)
         logits2 = torch.empty_like(logits)
         x2 = torch.empty_like(x)
         h_out2 = torch.empty_like(h_out).pin_memory()
@@ -491,7 +518,8 @@ def run_ours(args, world, rank, local):
 
         # ---------------- per-stage breakdown (diagnostic; events between calls) --
         Kb = max(10, min(K, 200))
-        eb = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Kb)]
+        eb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+              for _ in range(Kb)]
         torch.cuda.synchronize()
         for i in range(Kb):
             flush_l2()
@@ -500,8 +528,9 @@ def run_ours(args, world, rank, local):
                 fn(*a)
                 eb[i][c + 1].record(stream)
         torch.cuda.synchronize()
+        names = [fn.__name__.replace("moe_", "").replace("dispatch_", "") for fn, _ in calls]
         stage_ms = {name: [e[c].elapsed_time(e[c + 1]) for e in eb]
-                    for c, name in enumerate(("route", "layout", "pack", "permute", "combine"))}
+                    for c, name in enumerate(names)}
 
         # ---------------- per-kernel times (diagnostic; events around every launch) --
         m.trace_enable(None, max_records=Kb * 16)
@@ -525,7 +554,7 @@ def run_ours(args, world, rank, local):
     peak, peak_src = measured_peak()
     dom_ms = statistics.fmean(recs) if recs else None
     dom_achieved = (b["perm_copy"] / (dom_ms * 1e-3) / 1e9) if dom_ms else None
-    route_med = statistics.median(stage_ms["route"])
+    route_med = statistics.median(stage_ms["route_topk"])
     dc_ms = [max(s_ - route_med, 1e-6) for s_ in step_ms]
     dc_gbs = b["dispatch_combine"] * K / (sum(dc_ms) * 1e-3) / 1e9
 
@@ -541,7 +570,8 @@ def run_ours(args, world, rank, local):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(job_ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(w, "flushed before every timed step: 1 GiB write, then 256 MiB read (clean lines)"),
+        "config": workload_config(w, "flushed before every timed step: 1 GiB write, then 256 MiB read (clean lines)",
+                                  args.variant),
         "rows_per_s": round(rows_all / (job_ms * 1e-3), 1),
         "frac_of_hbm_peak": round(value / peak, 4),
         "dispatch_combine": {"gbs": round(dc_gbs, 2), "us_median": round(1e3 * statistics.median(dc_ms), 2),
@@ -562,7 +592,8 @@ def run_ours(args, world, rank, local):
                      "achieved": round(dom_achieved, 1) if dom_achieved else None,
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(dom_achieved / peak, 4) if dom_achieved else None,
-                     "traffic": DOMINANT_TRAFFIC.get(w.name), "bytes_per_launch": b["perm_copy"],
+                     "traffic": (DOMINANT_TRAFFIC.get(w.name) if args.variant == "contiguous" else None),
+                     "bytes_per_launch": b["perm_copy"],
                      "us_per_launch": round(1e3 * dom_ms, 2) if dom_ms else None,
                      "launches_timed": len(recs)},
         "cpu_baseline": cpu,
@@ -592,6 +623,11 @@ def main(argv=None):
     ap.add_argument("--workload", default="prefill", choices=sorted(ms.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--variant", default="contiguous", choices=sorted(VARIANTS),
+                    help="receive layout / combine form: contiguous runs + one-stage combine "
+                         "(default), masked blocks, or a two-stage combine")
+    ap.add_argument("--block-rows", type=int, default=0,
+                    help="rows per expert block of the masked layout (default S*T)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the calls from the host every step instead of replaying a CUDA graph")
     ap.add_argument("--profile", action="store_true",

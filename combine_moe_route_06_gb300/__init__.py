@@ -318,11 +318,25 @@ class MoePath:
     """
 
     def __init__(self, S, T, H, E, k, P, recv_part=-1, align=1, cap_send=None, cap_recv=None,
-                 device="cuda"):
+                 device="cuda", layout="contiguous", block_rows=None, combine="single"):
+        """layout: "contiguous" (expert runs, moe_permute_to_experts) or "masked" (one
+        block of block_rows rows per expert, moe_permute_to_experts_masked).
+        combine: "single" (moe_combine) or "two_stage" (moe_combine_stage1 + stage2)."""
+        if layout not in ("contiguous", "masked") or combine not in ("single", "two_stage"):
+            raise ValueError("layout must be contiguous|masked, combine single|two_stage")
         self.S, self.T, self.H, self.E, self.k, self.P = S, T, H, E, k, P
         self.recv_part, self.align = recv_part, align
+        self.layout, self.combine_mode = layout, combine
         self.cap_send = T * min(k, P) if cap_send is None else cap_send
-        self.cap_recv = S * T * k + E * (align - 1) if cap_recv is None else cap_recv
+        self.n_blocks = E if recv_part < 0 else E // P
+        if layout == "masked":
+            if block_rows is None:
+                raise ValueError("the masked layout needs block_rows")
+            self.block_rows = block_rows
+            self.cap_recv = self.n_blocks * block_rows
+        else:
+            self.block_rows = None
+            self.cap_recv = S * T * k + E * (align - 1) if cap_recv is None else cap_recv
         d = torch.device(device)
         i32 = dict(dtype=torch.int32, device=d)
         self.topk_ids = torch.empty((S, T, k), **i32)
@@ -342,6 +356,9 @@ class MoePath:
         ws = moe_workspace_bytes(S, T, k, E, P)
         self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=d)
         self.dev_status = torch.zeros((1,), **i32)
+        self.masked_counts = torch.empty((self.n_blocks,), **i32) if layout == "masked" else None
+        self.ret = (torch.empty((S, self.cap_send, H), dtype=torch.bfloat16, device=d)
+                    if combine == "two_stage" else None)
         self.y = None
 
     def bind(self, logits, x, stream=None):
@@ -374,20 +391,36 @@ class MoePath:
                                      vp(self.part_offsets.data_ptr()), self.cap_send,
                                      vp(self.send.data_ptr()), vp(self.send_src.data_ptr()), stp,
                                      st)),
-            (lib.moe_permute_to_experts, (vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
-                                          vp(self.topk_ids.data_ptr()),
-                                          vp(self.expert_counts.data_ptr()),
-                                          vp(self.expert_rank.data_ptr()), S, T, k, E, P, H,
-                                          self.recv_part, self.align, self.cap_send,
-                                          self.cap_recv, vp(self.recv.data_ptr()),
-                                          vp(self.expert_offsets.data_ptr()),
-                                          vp(self.pair_row.data_ptr()),
-                                          vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()),
-                                          self.ws.numel(), stp, st)),
-            (lib.moe_combine, (vp(self.recv.data_ptr()), self.cap_recv,
-                               vp(self.pair_row.data_ptr()), vp(self.topk_w.data_ptr()), S, T, k,
-                               H, vp(self.out.data_ptr()), stp, st)),
         ]
+        if self.layout == "masked":
+            calls.append((lib.moe_permute_to_experts_masked, (
+                vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
+                vp(self.topk_ids.data_ptr()), vp(self.expert_counts.data_ptr()),
+                vp(self.expert_rank.data_ptr()), S, T, k, E, P, H, self.recv_part,
+                self.block_rows, self.cap_send, vp(self.recv.data_ptr()),
+                vp(self.masked_counts.data_ptr()), vp(self.pair_row.data_ptr()),
+                vp(self.recv_pair.data_ptr()), stp, st)))
+        else:
+            calls.append((lib.moe_permute_to_experts, (
+                vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
+                vp(self.topk_ids.data_ptr()), vp(self.expert_counts.data_ptr()),
+                vp(self.expert_rank.data_ptr()), S, T, k, E, P, H, self.recv_part, self.align,
+                self.cap_send, self.cap_recv, vp(self.recv.data_ptr()),
+                vp(self.expert_offsets.data_ptr()), vp(self.pair_row.data_ptr()),
+                vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st)))
+        if self.combine_mode == "two_stage":
+            calls.append((lib.moe_combine_stage1, (
+                vp(self.recv.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
+                vp(self.topk_w.data_ptr()), vp(self.topk_ids.data_ptr()),
+                vp(self.token_slot.data_ptr()), S, T, k, E, P, H, self.recv_part, self.cap_send,
+                vp(self.ret.data_ptr()), stp, st)))
+            calls.append((lib.moe_combine_stage2, (
+                vp(self.ret.data_ptr()), vp(self.token_slot.data_ptr()), S, T, P, H,
+                self.cap_send, vp(self.out.data_ptr()), stp, st)))
+        else:
+            calls.append((lib.moe_combine, (
+                vp(self.recv.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
+                vp(self.topk_w.data_ptr()), S, T, k, H, vp(self.out.data_ptr()), stp, st)))
         return calls
 
     @staticmethod
@@ -408,20 +441,34 @@ class MoePath:
                             self.dev_status, stream)
         moe_dispatch_pack(x, self.token_slot, self.part_offsets, self.send, self.send_src,
                           self.dev_status, stream)
-        moe_permute_to_experts(self.send, self.token_slot, self.topk_ids, self.expert_counts,
-                               self.expert_rank, self.E, self.recv_part, self.align, self.recv,
-                               self.expert_offsets, self.pair_row, self.recv_pair, self.ws,
-                               self.dev_status, stream)
+        if self.layout == "masked":
+            moe_permute_to_experts_masked(self.send, self.token_slot, self.topk_ids,
+                                          self.expert_counts, self.expert_rank, self.E,
+                                          self.recv_part, self.block_rows, self.recv,
+                                          self.masked_counts, self.pair_row, self.recv_pair,
+                                          self.dev_status, stream)
+        else:
+            moe_permute_to_experts(self.send, self.token_slot, self.topk_ids, self.expert_counts,
+                                   self.expert_rank, self.E, self.recv_part, self.align, self.recv,
+                                   self.expert_offsets, self.pair_row, self.recv_pair, self.ws,
+                                   self.dev_status, stream)
 
     def expert(self, scale, stream=None):
+        if self.layout != "contiguous":
+            raise ValueError("the stand-in expert reads contiguous expert runs")
         if self.y is None:
             self.y = torch.empty_like(self.recv)
         moe_expert_scale(self.recv, self.expert_offsets, scale, self.y, stream)
         return self.y
 
     def combine(self, y=None, stream=None):
-        moe_combine(self.recv if y is None else y, self.pair_row, self.topk_w, self.out,
-                    self.dev_status, stream)
+        y = self.recv if y is None else y
+        if self.combine_mode == "two_stage":
+            moe_combine_stage1(y, self.pair_row, self.topk_w, self.topk_ids, self.token_slot,
+                               self.E, self.recv_part, self.ret, self.dev_status, stream)
+            moe_combine_stage2(self.ret, self.token_slot, self.out, self.dev_status, stream)
+        else:
+            moe_combine(y, self.pair_row, self.topk_w, self.out, self.dev_status, stream)
 
     def step(self, logits, x, scale=None, stream=None):
         """route -> layout -> pack -> permute -> [stand-in expert] -> combine; returns out."""
@@ -432,8 +479,10 @@ class MoePath:
         return self.out
 
     def launches_per_step(self, with_expert=False) -> int:
-        """Kernels one step enqueues (route 1, layout 2 (1 if T <= 256), pack 1, permute 2, combine 1)."""
+        """Kernels one step enqueues: route 1, layout 2 (1 if T <= 256), pack 1, permute 2
+        (map + copy), combine 1 (2 when split into two stages)."""
         if self.T == 0:
             return 1 + 1 + 2 + (1 if with_expert else 0)
         layout = 1 if self.T <= 256 else 2
-        return 1 + layout + 1 + 2 + 1 + (1 if with_expert else 0)
+        comb = 2 if self.combine_mode == "two_stage" else 1
+        return 1 + layout + 1 + 2 + comb + (1 if with_expert else 0)

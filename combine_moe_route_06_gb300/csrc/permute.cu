@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(kMapThreads) k_perm_map(
     if (__syncthreads_or(bad_id) && threadIdx.x == 0) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
 }
 
-// Masked layout map (DeepEP low-latency style, fixed block per expert): grid =
-// S * B CTAs as in k_perm_map; block b holds expert e0 + b.  Every CTA also
-// marks a share of the unused block rows in recv_pair.
+// Masked layout map (DeepEP low-latency style, fixed block per expert): the
+// first S * B CTAs map pairs as in k_perm_map; block b holds expert e0 + b.
+// Every CTA (including extra ones launched for large blocks) marks a share of
+// the unused block rows in recv_pair.
 __global__ void __launch_bounds__(kMapThreads) k_perm_map_masked(
     const int32_t *__restrict__ ids, const int32_t *__restrict__ expert_counts,
     const int32_t *__restrict__ expert_rank, int S, int T, int k, int E, int e0, int nb,
@@ -169,10 +170,11 @@ __global__ void __launch_bounds__(kMapThreads) k_perm_map_masked(
     int *sb = sm + nb;       // [nb] pairs of its expert in sources before s
     int *own = sb + nb;      // [nb] pairs of its expert in source s
     constexpr int kPer = kMapPairs / kMapThreads;
-    const int s = blockIdx.x / B, b = blockIdx.x % B;
+    const bool mapper = blockIdx.x < S * B;       // extra CTAs only mark unused rows
+    const int s = mapper ? blockIdx.x / B : 0, b = mapper ? blockIdx.x % B : 0;
     const int64_t per_src = (int64_t)T * k;
     const int64_t q0 = (int64_t)s * per_src + (int64_t)b * kMapPairs;
-    const int64_t q1 = min((int64_t)s * per_src + per_src, q0 + kMapPairs);
+    const int64_t q1 = mapper ? min((int64_t)s * per_src + per_src, q0 + kMapPairs) : q0;
     pdl_wait();
     pdl_trigger();
 
@@ -402,8 +404,12 @@ cudaError_t launch_permute_masked(const uint16_t *send, const int32_t *token_slo
     const int e0 = recv_part < 0 ? 0 : recv_part * L;
     const int B = (int)(div_up((int64_t)T * k, kMapPairs) > 0 ? div_up((int64_t)T * k, kMapPairs) : 1);
     const size_t smem = (size_t)(3 * nb) * sizeof(int);
+    // enough CTAs that each marks at most ~2,048 unused block rows
+    int64_t grid = (int64_t)S * B;
+    const int64_t mark = div_up((int64_t)nb * block_rows, 8 * kMapThreads);
+    if (grid < mark) grid = mark < di.sm_count ? mark : di.sm_count;
     MOE_TRACED_LAUNCH("k_perm_map_masked", st,
-                      e = launch_pdl(k_perm_map_masked, dim3((unsigned)(S * B)), dim3(kMapThreads),
+                      e = launch_pdl(k_perm_map_masked, dim3((unsigned)grid), dim3(kMapThreads),
                                      smem, st, ids, expert_counts, expert_rank, S, T, k, E, e0, nb,
                                      B, block_rows, masked_counts, pair_row, recv_pair, dev_status));
     if (e != cudaSuccess || NT == 0) return e;
