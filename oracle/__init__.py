@@ -67,11 +67,18 @@ def _load():
             lib.oracle_combine_stage1.argtypes = [P, P, P, P, P, i32, i64, i32, i32, i32, i32,
                                                   i32, i64, P, P]
             lib.oracle_combine_stage2.argtypes = [P, P, i32, i64, i32, i32, i64, P, P]
+            lib.oracle_e4m3_from_double.argtypes = [ctypes.c_double]
+            lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = ctypes.c_double
+            lib.oracle_quantize_mxfp8_block.argtypes = [P, P, P]
+            lib.oracle_quantize_mxfp8_block.restype = None
+            lib.oracle_dispatch_pack_mxfp8.argtypes = [P, i32, i64, i32, i32, P, i64, P, P, P, P]
             lib.oracle_combine.argtypes = [P, P, P, i32, i64, i32, i32, P]
             for f in ("oracle_route_topk", "oracle_dispatch_layout", "oracle_dispatch_pack",
                       "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine",
                       "oracle_permute_masked", "oracle_combine_stage1",
-                      "oracle_combine_stage2"):
+                      "oracle_combine_stage2", "oracle_dispatch_pack_mxfp8"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -273,6 +280,47 @@ def combine_stage2(ret: np.ndarray, token_slot: np.ndarray):
     _check(_load().oracle_combine_stage2(_p(ret), _p(token_slot), S, T, P, H, cap_send, _p(out),
                                          _p(st)), "combine_stage2")
     return out, int(st[0])
+
+
+def e4m3_from_double(v: float) -> int:
+    return int(_load().oracle_e4m3_from_double(float(v)))
+
+
+def e4m3_to_double(b: int) -> float:
+    return float(_load().oracle_e4m3_to_double(int(b)))
+
+
+def quantize_mxfp8(row: np.ndarray):
+    """bf16 bits [H] (H % 32 == 0) -> (codes uint8 [H], scales uint8 [H/32])."""
+    row = np.ascontiguousarray(row, dtype=np.uint16)
+    H = row.shape[0]
+    codes = np.empty(H, np.uint8)
+    scales = np.empty(H // 32, np.uint8)
+    lib = _load()
+    for b in range(H // 32):
+        lib.oracle_quantize_mxfp8_block(
+            ctypes.c_void_p(row.ctypes.data + 64 * b), ctypes.c_void_p(codes.ctypes.data + 32 * b),
+            ctypes.c_void_p(scales.ctypes.data + b))
+    return codes, scales
+
+
+def dispatch_pack_mxfp8(x: np.ndarray, token_slot: np.ndarray, cap_send: int,
+                        send_q: np.ndarray | None = None, send_scale: np.ndarray | None = None):
+    """Pack with MXFP8 rows -> (send_q [S, cap, H] u8, send_scale [S, cap, H/32] u8, send_src, status)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    S, T, H = x.shape
+    P = token_slot.shape[2]
+    if send_q is None:
+        send_q = np.zeros((S, cap_send, H), np.uint8)
+    if send_scale is None:
+        send_scale = np.zeros((S, cap_send, H // 32), np.uint8)
+    send_src = np.empty((S, cap_send), np.int32)
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_dispatch_pack_mxfp8(_p(x), S, T, H, P, _p(token_slot), cap_send,
+                                              _p(send_q), _p(send_scale), _p(send_src), _p(st)),
+           "dispatch_pack_mxfp8")
+    return send_q, send_scale, send_src, int(st[0])
 
 
 def run_path(x: np.ndarray, logits: np.ndarray, E: int, k: int, P: int, scales: np.ndarray | None,

@@ -606,3 +606,130 @@ int oracle_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S,
     free(acc);
     return 0;
 }
+
+/* ---------------------------------------- FP8 dispatch rows, [a2a] 7.2 */
+
+/*
+ * [a2a] 7.2: expert kernels that quantize their input anyway can take rows
+ * already quantized, so a token is converted before it is sent; an FP8 row of
+ * DeepSeek-V4.1-Flash is 5,280 bytes: 5,120 one-byte values plus a one-byte
+ * scale for every 32 values.  The pages fix the sizes, not the encoding; the
+ * reading taken here is the OCP microscaling format MXFP8: E4M3 elements and
+ * an E8M0 (power-of-two) scale per block of 32 values.
+ *
+ * E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities,
+ * S.1111.111 is NaN): normal values (1 + m/8) * 2^e for e in [-6, 8] up to
+ * 448, subnormals (m/8) * 2^-6.  Conversion: round to nearest, ties to even,
+ * on that grid; magnitudes above 448 saturate to 448.
+ */
+uint8_t oracle_e4m3_from_double(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    if (isnan(v))
+        return 0x7Fu;
+    double a = fabs(v);
+    if (a >= 448.0)
+        return sign | 0x7Eu;
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);                       /* a in [2^(ex-1), 2^ex) */
+    int e = ex - 1;
+    if (e < -6)
+        e = -6;                          /* subnormal range shares the 2^-9 quantum */
+    double q = ldexp(1.0, e - 3);
+    double r = nearbyint(a / q) * q;     /* ties to even */
+    if (r > 448.0)
+        r = 448.0;
+    if (r == 0.0)
+        return sign;
+    /* encode r */
+    int er;
+    frexp(r, &er);
+    int eu = er - 1;                     /* r in [2^eu, 2^(eu+1)) */
+    if (eu < -6) {                       /* subnormal: r = m * 2^-9 */
+        int m = (int)nearbyint(r / ldexp(1.0, -9));
+        return sign | (uint8_t)m;
+    }
+    int m = (int)nearbyint((r / ldexp(1.0, eu) - 1.0) * 8.0);
+    return sign | (uint8_t)(((eu + 7) << 3) | m);
+}
+
+double oracle_e4m3_to_double(uint8_t b)
+{
+    int sign = b >> 7, E = (b >> 3) & 0xF, m = b & 7;
+    if (E == 15 && m == 7)
+        return NAN;
+    double v = (E == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, E - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * One MXFP8 block of 32 bf16 values: shared exponent
+ *   X = 2^(floor(log2(max |v|)) - 8)        (8 = exponent of E4M3's largest power of two)
+ * clamped to [2^-127, 2^127], stored as the E8M0 byte (exponent + 127); each
+ * element is e4m3(v / X).  An all-zero block gets the smallest scale (byte 0).
+ */
+void oracle_quantize_mxfp8_block(const uint16_t *v, uint8_t *codes, uint8_t *scale)
+{
+    double amax = 0.0;
+    for (int i = 0; i < 32; i++) {
+        double a = fabs(oracle_bf16_to_double(v[i]));
+        if (a > amax)
+            amax = a;
+    }
+    int se = -127;
+    if (amax > 0.0) {
+        int ex;
+        frexp(amax, &ex);                /* amax in [2^(ex-1), 2^ex) */
+        se = (ex - 1) - 8;
+        if (se < -127)
+            se = -127;
+        if (se > 127)
+            se = 127;
+    }
+    *scale = (uint8_t)(se + 127);
+    for (int i = 0; i < 32; i++)
+        codes[i] = oracle_e4m3_from_double(ldexp(oracle_bf16_to_double(v[i]), -se));
+}
+
+/*
+ * Pack with the rows quantized on the way: every (token, partition) slot gets
+ * the token's MXFP8 codes (send_q[s][slot][0..H)) and block scales
+ * (send_scale[s][slot][0..H/32)); send_src and capacity as in
+ * oracle_dispatch_pack.  H must be a multiple of 32.
+ */
+int oracle_dispatch_pack_mxfp8(const uint16_t *x, int S, int64_t T, int H, int P,
+                               const int32_t *token_slot, int64_t cap_send, uint8_t *send_q,
+                               uint8_t *send_scale, int32_t *send_src, uint32_t *status)
+{
+    if (H % 32 != 0)
+        return -1;
+    const int nb = H / 32;
+    uint8_t *q = (uint8_t *)malloc((size_t)H + (size_t)nb);
+    if (!q)
+        return -2;
+    for (int s = 0; s < S; s++) {
+        for (int64_t r = 0; r < cap_send; r++)
+            send_src[(int64_t)s * cap_send + r] = -1;
+        for (int64_t t = 0; t < T; t++) {
+            const uint16_t *row = x + ((int64_t)s * T + t) * H;
+            for (int b = 0; b < nb; b++)
+                oracle_quantize_mxfp8_block(row + 32 * b, q + 32 * b, q + H + b);
+            for (int p = 0; p < P; p++) {
+                int32_t slot = token_slot[((int64_t)s * T + t) * P + p];
+                if (slot < 0)
+                    continue;
+                if (slot >= cap_send) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue;
+                }
+                memcpy(send_q + ((int64_t)s * cap_send + slot) * H, q, (size_t)H);
+                memcpy(send_scale + ((int64_t)s * cap_send + slot) * nb, q + H, (size_t)nb);
+                send_src[(int64_t)s * cap_send + slot] = (int32_t)t;
+            }
+        }
+    }
+    free(q);
+    return 0;
+}

@@ -608,3 +608,72 @@ def test_two_stage_identity_round_trip_close():
     x = ms.f32_from_bf16_bits(inp["x"]).astype(np.float64)
     got = ms.f32_from_bf16_bits(out).astype(np.float64)
     assert np.all(np.abs(got - x) <= 2.0 ** -6 * np.maximum(np.abs(x), 1e-3))
+
+
+# ---------------------------------------------- FP8 dispatch rows (a2a 7.2) --
+
+def test_quantized_row_sizes():
+    g = _golden("quantized_row_bytes.json")
+    H = g["hidden"]
+    assert 2 * H == g["bf16_bytes"]
+    x = ms.gen_x(ms.workload("prefill"), T=1)[0, 0]
+    codes, scales = oracle.quantize_mxfp8(x)
+    assert codes.nbytes + scales.nbytes == g["fp8_bytes"]              # MXFP8: 1 B per 32
+    assert H + H // g["deepep_v1_block"] * g["deepep_v1_scale_bytes"] == g["fp8_bytes"]
+    assert H // 2 + H // g["nvfp4_block"] == g["nvfp4_bytes"]
+
+
+def test_e4m3_matches_torch_in_range():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    v = (rng.standard_normal(20000) * np.exp(rng.uniform(-9, 6, 20000))).astype(np.float32)
+    v = v[np.abs(v) <= 448.0]
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_double(float(a)) for a in v], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_e4m3_round_trip_and_saturation():
+    for b in range(256):
+        if (b & 0x7F) == 0x7F:
+            continue                                                    # NaN codes
+        v = oracle.e4m3_to_double(b)
+        assert oracle.e4m3_from_double(v) == b                          # -0.0 keeps its sign
+    assert oracle.e4m3_to_double(0x7E) == 448.0 and oracle.e4m3_to_double(0x01) == 2.0 ** -9
+    for v in (448.0, 449.0, 480.0, 1e30):
+        assert oracle.e4m3_from_double(v) == 0x7E and oracle.e4m3_from_double(-v) == 0xFE
+
+
+def test_mxfp8_scale_rule_and_error_bound():
+    w_ = ms.workload("prefill")
+    x = ms.gen_x(w_, T=4)[0]
+    xf = ms.f32_from_bf16_bits(x).astype(np.float64)
+    for t in range(4):
+        codes, scales = oracle.quantize_mxfp8(x[t])
+        for b in range(w_.H // 32):
+            blk = xf[t, 32 * b:32 * (b + 1)]
+            amax = np.abs(blk).max()
+            se = (math.frexp(amax)[1] - 1) - 8                          # floor(log2 amax) - 8
+            assert scales[b] == se + 127
+            X = 2.0 ** se
+            deq = np.array([oracle.e4m3_to_double(c) for c in codes[32 * b:32 * (b + 1)]]) * X
+            sat = np.abs(blk) > 448 * X
+            bound = np.maximum(np.abs(blk) * 2.0 ** -4, X * 2.0 ** -10)
+            assert np.all(np.abs(deq - blk)[~sat] <= bound[~sat])
+            assert np.all(np.abs(deq[sat]) == 448 * X)
+
+
+def test_pack_mxfp8_places_quantized_rows():
+    w_ = ms.workload("tiny")
+    inp = ms.gen_inputs(w_)
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap = w_.T * min(w_.k, w_.P)
+    q, sc, src, st = oracle.dispatch_pack_mxfp8(inp["x"], lay["token_slot"], cap)
+    assert st == 0
+    used = lay["part_offsets"][0, -1]
+    for r in (0, 7, used - 1):
+        codes, scales = oracle.quantize_mxfp8(inp["x"][0, src[0, r]])
+        assert np.array_equal(q[0, r], codes) and np.array_equal(sc[0, r], scales)
+    _, src_bf16, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap)
+    assert np.array_equal(src, src_bf16)
