@@ -73,12 +73,14 @@ def _load():
             lib.oracle_e4m3_to_double.restype = ctypes.c_double
             lib.oracle_quantize_mxfp8_block.argtypes = [P, P, P]
             lib.oracle_quantize_mxfp8_block.restype = None
-            lib.oracle_dispatch_pack_mxfp8.argtypes = [P, i32, i64, i32, i32, P, i64, P, P, P, P]
+            lib.oracle_dispatch_pack_mxfp8.argtypes = [P, i32, i64, i32, i32, P, i64, P, P, P]
+            lib.oracle_expert_scale_mxfp8.argtypes = [P, P, P, i32, i32, i64, P]
             lib.oracle_combine.argtypes = [P, P, P, i32, i64, i32, i32, P]
             for f in ("oracle_route_topk", "oracle_dispatch_layout", "oracle_dispatch_pack",
                       "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine",
                       "oracle_permute_masked", "oracle_combine_stage1",
-                      "oracle_combine_stage2", "oracle_dispatch_pack_mxfp8"):
+                      "oracle_combine_stage2", "oracle_dispatch_pack_mxfp8",
+                      "oracle_expert_scale_mxfp8"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -305,22 +307,42 @@ def quantize_mxfp8(row: np.ndarray):
 
 
 def dispatch_pack_mxfp8(x: np.ndarray, token_slot: np.ndarray, cap_send: int,
-                        send_q: np.ndarray | None = None, send_scale: np.ndarray | None = None):
-    """Pack with MXFP8 rows -> (send_q [S, cap, H] u8, send_scale [S, cap, H/32] u8, send_src, status)."""
+                        send_q: np.ndarray | None = None):
+    """Pack with MXFP8 records -> (send_q uint8 [S, cap, H + H/32], send_src, status).
+
+    A record is the H E4M3 codes followed by the H/32 E8M0 block scales.
+    """
     x = np.ascontiguousarray(x, dtype=np.uint16)
     token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
     S, T, H = x.shape
     P = token_slot.shape[2]
     if send_q is None:
-        send_q = np.zeros((S, cap_send, H), np.uint8)
-    if send_scale is None:
-        send_scale = np.zeros((S, cap_send, H // 32), np.uint8)
+        send_q = np.zeros((S, cap_send, H + H // 32), np.uint8)
     send_src = np.empty((S, cap_send), np.int32)
     st = np.zeros(1, np.uint32)
     _check(_load().oracle_dispatch_pack_mxfp8(_p(x), S, T, H, P, _p(token_slot), cap_send,
-                                              _p(send_q), _p(send_scale), _p(send_src), _p(st)),
+                                              _p(send_q), _p(send_src), _p(st)),
            "dispatch_pack_mxfp8")
-    return send_q, send_scale, send_src, int(st[0])
+    return send_q, send_src, int(st[0])
+
+
+def expert_scale_mxfp8(recv_q: np.ndarray, expert_offsets: np.ndarray, scale: np.ndarray,
+                       y: np.ndarray | None = None) -> np.ndarray:
+    """Dequantizing stand-in expert: recv_q uint8 [cap, H + H/32] -> y bf16 bits [cap, H].
+
+    Rows outside every expert run keep the contents of the `y` passed in (zeros if none).
+    """
+    recv_q = np.ascontiguousarray(recv_q, dtype=np.uint8)
+    cap, rb = recv_q.shape
+    H = rb * 32 // 33
+    assert H + H // 32 == rb
+    E = expert_offsets.shape[0] - 1
+    if y is None:
+        y = np.zeros((cap, H), np.uint16)
+    _check(_load().oracle_expert_scale_mxfp8(_p(recv_q), _p(np.ascontiguousarray(expert_offsets, np.int32)),
+                                             _p(np.ascontiguousarray(scale, np.float32)), E, H, cap, _p(y)),
+           "expert_scale_mxfp8")
+    return y
 
 
 def run_path(x: np.ndarray, logits: np.ndarray, E: int, k: int, P: int, scales: np.ndarray | None,

@@ -694,19 +694,21 @@ void oracle_quantize_mxfp8_block(const uint16_t *v, uint8_t *codes, uint8_t *sca
 }
 
 /*
- * Pack with the rows quantized on the way: every (token, partition) slot gets
- * the token's MXFP8 codes (send_q[s][slot][0..H)) and block scales
- * (send_scale[s][slot][0..H/32)); send_src and capacity as in
- * oracle_dispatch_pack.  H must be a multiple of 32.
+ * Pack with the rows quantized on the way ([a2a] 7.2).  A quantized row is one
+ * record of H + H/32 bytes, the page's 5,280 bytes for H = 5,120: the H E4M3
+ * codes, then the H/32 E8M0 block scales.  Every (token, partition) slot gets
+ * the token's record at send_q[s][slot][0 .. H + H/32); send_src and the
+ * capacity rule are those of oracle_dispatch_pack.  H must be a multiple of 32.
  */
 int oracle_dispatch_pack_mxfp8(const uint16_t *x, int S, int64_t T, int H, int P,
                                const int32_t *token_slot, int64_t cap_send, uint8_t *send_q,
-                               uint8_t *send_scale, int32_t *send_src, uint32_t *status)
+                               int32_t *send_src, uint32_t *status)
 {
     if (H % 32 != 0)
         return -1;
     const int nb = H / 32;
-    uint8_t *q = (uint8_t *)malloc((size_t)H + (size_t)nb);
+    const int64_t rb = (int64_t)H + nb;
+    uint8_t *q = (uint8_t *)malloc((size_t)rb);
     if (!q)
         return -2;
     for (int s = 0; s < S; s++) {
@@ -724,12 +726,36 @@ int oracle_dispatch_pack_mxfp8(const uint16_t *x, int S, int64_t T, int H, int P
                     *status |= ORC_BIT_CAPACITY;
                     continue;
                 }
-                memcpy(send_q + ((int64_t)s * cap_send + slot) * H, q, (size_t)H);
-                memcpy(send_scale + ((int64_t)s * cap_send + slot) * nb, q + H, (size_t)nb);
+                memcpy(send_q + ((int64_t)s * cap_send + slot) * rb, q, (size_t)rb);
                 send_src[(int64_t)s * cap_send + slot] = (int32_t)t;
             }
         }
     }
     free(q);
+    return 0;
+}
+
+/*
+ * Stand-in expert on quantized rows: the receiver dequantizes each value of a
+ * record (code times 2^(scale byte - 127)) and applies the same per-expert
+ * scale as oracle_expert_scale, rounding once to bf16:
+ *   y[r][h] = bf16( s_e * e4m3(code[r][h]) * 2^(scale[r][h/32] - 127) )
+ * for the rows r of expert e's run.  recv_q rows are H + H/32 bytes.
+ */
+int oracle_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offsets,
+                              const float *scale, int E, int H, int64_t cap_recv, uint16_t *y)
+{
+    if (H % 32 != 0)
+        return -1;
+    const int64_t rb = (int64_t)H + H / 32;
+    for (int e = 0; e < E; e++) {
+        for (int64_t r = expert_offsets[e]; r < expert_offsets[e + 1] && r < cap_recv; r++) {
+            const uint8_t *rec = recv_q + r * rb;
+            for (int h = 0; h < H; h++) {
+                double v = oracle_e4m3_to_double(rec[h]) * ldexp(1.0, (int)rec[H + h / 32] - 127);
+                y[r * H + h] = oracle_bf16_from_double(v * (double)scale[e]);
+            }
+        }
+    }
     return 0;
 }

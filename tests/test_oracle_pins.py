@@ -621,6 +621,10 @@ def test_quantized_row_sizes():
     assert codes.nbytes + scales.nbytes == g["fp8_bytes"]              # MXFP8: 1 B per 32
     assert H + H // g["deepep_v1_block"] * g["deepep_v1_scale_bytes"] == g["fp8_bytes"]
     assert H // 2 + H // g["nvfp4_block"] == g["nvfp4_bytes"]
+    # one packed record per (token, partition) is exactly the page's FP8 row
+    ts = np.zeros((1, 1, 1), np.int32)
+    q, src, st = oracle.dispatch_pack_mxfp8(ms.gen_x(ms.workload("prefill"), T=1), ts, 1)
+    assert q.shape == (1, 1, g["fp8_bytes"]) and st == 0 and src[0, 0] == 0
 
 
 def test_e4m3_matches_torch_in_range():
@@ -669,11 +673,49 @@ def test_pack_mxfp8_places_quantized_rows():
     ids, _ = oracle.route_topk(inp["logits"], w_.k)
     lay = oracle.dispatch_layout(ids, w_.E, w_.P)
     cap = w_.T * min(w_.k, w_.P)
-    q, sc, src, st = oracle.dispatch_pack_mxfp8(inp["x"], lay["token_slot"], cap)
+    q, src, st = oracle.dispatch_pack_mxfp8(inp["x"], lay["token_slot"], cap)
     assert st == 0
     used = lay["part_offsets"][0, -1]
     for r in (0, 7, used - 1):
         codes, scales = oracle.quantize_mxfp8(inp["x"][0, src[0, r]])
-        assert np.array_equal(q[0, r], codes) and np.array_equal(sc[0, r], scales)
+        assert np.array_equal(q[0, r], np.concatenate([codes, scales]))
     _, src_bf16, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap)
     assert np.array_equal(src, src_bf16)
+    assert np.all(q[0, used:] == 0)                                      # unused rows untouched
+
+
+def test_expert_scale_mxfp8_hand_values():
+    # two records of H = 32: codes and scale bytes chosen by hand, values worked out
+    # from the E4M3 / E8M0 definitions (1.m x 2^(E-7); 2^(byte-127))
+    H = 32
+    rec = np.zeros((3, H + 1), np.uint8)
+    rec[0, :4] = [0x7E, 0x38, 0xB0, 0x01]     # 448, 1.0, -0.5, 2^-9
+    rec[0, H] = 127                            # X = 1
+    rec[1, :2] = [0x3C, 0xFE]                  # 1.5, -448
+    rec[1, H] = 127 + 3                        # X = 8
+    rec[2, :] = 0x38
+    rec[2, H] = 127
+    eo = np.array([0, 1, 2], np.int32)         # expert 0: row 0; expert 1: row 1; row 2 outside
+    y = oracle.expert_scale_mxfp8(rec, eo, np.array([1.0, 0.5], np.float32),
+                                  y=np.full((3, H), 0x1234, np.uint16))
+    got = ms.f32_from_bf16_bits(y).astype(np.float64)
+    assert list(got[0, :4]) == [448.0, 1.0, -0.5, 2.0 ** -9] and np.all(got[0, 4:] == 0)
+    assert list(got[1, :2]) == [1.5 * 8 * 0.5, -448 * 8 * 0.5] and np.all(got[1, 2:] == 0)
+    assert np.all(y[2] == 0x1234)
+
+
+def test_expert_scale_mxfp8_reduces_to_bf16_expert():
+    # a record whose values are all exact in E4M3 dequantizes to those values: the
+    # quantized expert must then equal the bf16 expert on the same rows
+    rng = np.random.default_rng(3)
+    H, R = 64, 40
+    mant = rng.integers(8, 16, size=(R, H))                # 1.m in eighths: 3 mantissa bits
+    expo = rng.integers(-3, 3, size=(R, H))                # |v| <= 7.5
+    v = np.where(rng.random((R, H)) < 0.5, -1.0, 1.0) * mant / 8.0 * 2.0 ** expo
+    v[:, ::32] = 14.0 * np.sign(v[:, ::32])                # amax 14 per block: X = 2^-5, 14/X = 448
+    bits = ms.bf16_bits_from_f32(v.astype(np.float32))
+    rec = np.stack([np.concatenate(oracle.quantize_mxfp8(r)) for r in bits])
+    assert np.all(rec[:, H:] == 127 - 5)
+    eo = np.array([0, 17, R], np.int32)
+    s = np.array([0.25, 3.0], np.float32)
+    assert np.array_equal(oracle.expert_scale_mxfp8(rec, eo, s), oracle.expert_scale(bits, eo, s))
