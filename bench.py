@@ -45,28 +45,35 @@ DOMINANT_TRAFFIC = {"prefill": 142.5e6 + 252.3e6}
 
 # ------------------------------------------------------------ byte model --
 
-def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_stage=False):
+def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_stage=False,
+                      mxfp8=False):
     """Bytes each call must read + write at minimum.
 
     copies: rows packed (sum of part_offsets[s][P]); copies_recv: packed rows
     bound for the receiving partition(s); pairs_recv: permuted pair rows.
     two_stage: the combine pre-adds per (token, partition) slot (copies_recv
     rows written and read back) before the per-token sum.
+    mxfp8: packed and permuted rows are MXFP8 records of H + H/32 bytes, and
+    the stand-in expert that dequantizes them (pair records in, bf16 rows out)
+    is part of the step.
     """
     NT = S * T
+    R = H + H // 32 if mxfp8 else 2 * H          # bytes of one moved row
     b = {
         "route": NT * E * 4 + NT * k * 8,
         "layout": NT * k * 4 + NT * P * 4 + S * (E + 2 * P + 1) * 4,
-        "pack": NT * H * 2 + copies * H * 2 + copies * 4,
-        "permute": copies_recv * H * 2 + pairs_recv * H * 2 + NT * k * 8,
+        "pack": NT * H * 2 + copies * R + copies * 4,
+        "permute": copies_recv * R + pairs_recv * R + NT * k * 8,
         "combine": pairs_recv * H * 2 + NT * k * 8 + NT * H * 2,
     }
+    if mxfp8:
+        b["expert"] = pairs_recv * R + pairs_recv * H * 2
     if two_stage:
         b["combine"] = (pairs_recv * H * 2 + NT * k * 12 + copies_recv * H * 2      # stage 1
                         + copies_recv * H * 2 + NT * P * 4 + NT * H * 2)            # stage 2
-    b["dispatch_combine"] = b["layout"] + b["pack"] + b["permute"] + b["combine"]
+    b["dispatch_combine"] = b["layout"] + b["pack"] + b["permute"] + b["combine"] + b.get("expert", 0)
     b["step"] = b["route"] + b["dispatch_combine"]
-    b["perm_copy"] = copies_recv * H * 2 + pairs_recv * H * 2 + NT * k * 8
+    b["perm_copy"] = copies_recv * R + pairs_recv * R + NT * k * 8
     return b
 
 
@@ -272,11 +279,14 @@ def run_reference(args, world, rank):
 
 
 def workload_config(w, l2, variant="contiguous"):
+    scope = "route+layout+pack+permute+combine"
+    if variant == "mxfp8":
+        scope = "route+layout+pack(MXFP8 records)+permute+dequantizing stand-in expert+combine"
     return {"workload": f"{w.name}: S={w.S} T={w.T} H={w.H} bf16, E={w.E} top-{w.k}, "
                         f"P={w.P} partitions, recv_part={w.recv_part}",
             "variant": variant,
             "tokens_per_rank": w.S * w.T, "hidden": w.H, "experts": w.E, "topk": w.k,
-            "partitions": w.P, "l2": l2, "value_scope": "route+layout+pack+permute+combine"}
+            "partitions": w.P, "l2": l2, "value_scope": scope}
 
 
 # ------------------------------------------------------------ GPU arm --
@@ -285,6 +295,7 @@ VARIANTS = {
     "contiguous": {},
     "masked": {"layout": "masked"},
     "two_stage": {"combine": "two_stage"},
+    "mxfp8": {"quant": "mxfp8"},
 }
 
 
@@ -376,7 +387,8 @@ def run_ours(args, world, rank, local):
         copies_recv = copies if w.recv_part < 0 else int(path.part_counts[:, w.recv_part].sum().item())
         pairs_recv = int((path.pair_row >= 0).sum().item())
         b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv,
-                              two_stage=(args.variant == "two_stage"))
+                              two_stage=(args.variant == "two_stage"),
+                              mxfp8=(args.variant == "mxfp8"))
 
         # ---------------- the step as a CUDA graph (fixed shapes and addresses) ---
         # The five calls are recorded once and replayed, as a serving engine
@@ -568,7 +580,8 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(job_ms / K, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.variant != "mxfp8" else "bf16/e4m3",
         "data": "synthetic",
         "config": workload_config(w, "flushed before every timed step: 1 GiB write, then 256 MiB read (clean lines)",
                                   args.variant),
@@ -584,7 +597,8 @@ def run_ours(args, world, rank, local):
         "stages_note": "separate loop with events between calls (breaks launch overlap)",
         "kernels_us_median": kernels_us,
         "kernels_note": "separate loop with events around every launch (includes launch latency)",
-        "stage_bytes": {k_: b[k_] for k_ in ("route", "layout", "pack", "permute", "combine")},
+        "stage_bytes": {k_: b[k_] for k_ in ("route", "layout", "pack", "permute", "expert", "combine")
+                        if k_ in b},
         "copies_per_token": round(copies / (w.S * w.T), 4),
         "pairs_recv": pairs_recv,
         "dev_status": status,

@@ -27,7 +27,7 @@ __all__ = [
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
-    "moe_combine_stage2", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8", "MoePath", "trace_enable", "trace_disable", "trace_reset",
     "trace_records",
 ]
 
@@ -96,6 +96,9 @@ def load_library() -> ctypes.CDLL:
             "moe_combine_stage1": ([P, i32, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P,
                                     P, P], ctypes.c_int),
             "moe_combine_stage2": ([P, P, i32, i32, i32, i32, i32, P, P, P], ctypes.c_int),
+            "moe_dispatch_pack_mxfp8": ([P, i32, i32, i32, i32, P, P, i32, P, P, P, P],
+                                         ctypes.c_int),
+            "moe_expert_scale_mxfp8": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
             "moe_permute_to_experts_masked": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                i32, i32, P, P, P, P, P, P], ctypes.c_int),
             "moe_expert_scale": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
@@ -195,6 +198,27 @@ def moe_dispatch_pack(x, token_slot, part_offsets, send, send_src, dev_status=No
         _status_ptr(dev_status), _stream(stream)))
 
 
+def mxfp8_record_bytes(H: int) -> int:
+    """Bytes of one MXFP8 row record: H E4M3 codes, then H/32 E8M0 block scales."""
+    return H + H // 32
+
+
+def moe_dispatch_pack_mxfp8(x, token_slot, part_offsets, send_q, send_src, dev_status=None,
+                            stream=None):
+    """x bf16 [S,T,H] -> send_q uint8 [S,cap_send,H+H/32] MXFP8 records, send_src i32 [S,cap_send]."""
+    lib = load_library()
+    S, T, H = x.shape
+    P = token_slot.shape[2]
+    cap_send = send_q.shape[1]
+    if send_q.shape[2] != mxfp8_record_bytes(H):
+        raise ValueError(f"send_q rows must be {mxfp8_record_bytes(H)} bytes for H={H}")
+    _check(lib.moe_dispatch_pack_mxfp8(
+        _dev(x, "x", _BF16_TYPES, 3), S, T, H, P, _dev(token_slot, "token_slot", (torch.int32,), 3),
+        _dev(part_offsets, "part_offsets", (torch.int32,)), cap_send,
+        _dev(send_q, "send_q", (torch.uint8,), 3), _dev(send_src, "send_src", (torch.int32,)),
+        _status_ptr(dev_status), _stream(stream)))
+
+
 def moe_permute_to_experts(send, token_slot, topk_ids, expert_counts, expert_rank, E, recv_part,
                            align, recv, expert_offsets, pair_row, recv_pair, ws, dev_status=None,
                            stream=None):
@@ -284,6 +308,20 @@ def moe_expert_scale(recv, expert_offsets, scale, y, stream=None):
                                 _dev(y, "y", _BF16_TYPES, 2), _stream(stream)))
 
 
+def moe_expert_scale_mxfp8(recv_q, expert_offsets, scale, y, stream=None):
+    """Stand-in expert on MXFP8 records: y[r] = bf16(scale[e] * dequant(recv_q[r]))."""
+    lib = load_library()
+    cap_recv, H = y.shape
+    if tuple(recv_q.shape) != (cap_recv, mxfp8_record_bytes(H)):
+        raise ValueError("recv_q must be [cap_recv, H + H/32] uint8")
+    E = scale.shape[0]
+    _check(lib.moe_expert_scale_mxfp8(
+        _dev(recv_q, "recv_q", (torch.uint8,), 2),
+        _dev(expert_offsets, "expert_offsets", (torch.int32,)),
+        _dev(scale, "scale", (torch.float32,)), E, H, cap_recv, _dev(y, "y", _BF16_TYPES, 2),
+        _stream(stream)))
+
+
 def trace_enable(kernel_filter: str | None = None, max_records: int = 4096):
     """Bracket this library's kernel launches (names containing kernel_filter) with CUDA events."""
     lib = load_library()
@@ -318,15 +356,25 @@ class MoePath:
     """
 
     def __init__(self, S, T, H, E, k, P, recv_part=-1, align=1, cap_send=None, cap_recv=None,
-                 device="cuda", layout="contiguous", block_rows=None, combine="single"):
+                 device="cuda", layout="contiguous", block_rows=None, combine="single",
+                 quant="none"):
         """layout: "contiguous" (expert runs, moe_permute_to_experts) or "masked" (one
         block of block_rows rows per expert, moe_permute_to_experts_masked).
-        combine: "single" (moe_combine) or "two_stage" (moe_combine_stage1 + stage2)."""
+        combine: "single" (moe_combine) or "two_stage" (moe_combine_stage1 + stage2).
+        quant: "none" (bf16 rows) or "mxfp8" (rows sent as MXFP8 records; the
+        receiver's stand-in expert dequantizes them, so every step runs it)."""
         if layout not in ("contiguous", "masked") or combine not in ("single", "two_stage"):
             raise ValueError("layout must be contiguous|masked, combine single|two_stage")
+        if quant not in ("none", "mxfp8"):
+            raise ValueError("quant must be none|mxfp8")
+        if quant == "mxfp8" and (H % 512 != 0 or layout != "contiguous"):
+            raise ValueError("mxfp8 rows need H % 512 == 0 and the contiguous layout")
         self.S, self.T, self.H, self.E, self.k, self.P = S, T, H, E, k, P
         self.recv_part, self.align = recv_part, align
-        self.layout, self.combine_mode = layout, combine
+        self.layout, self.combine_mode, self.quant = layout, combine, quant
+        # row width as the permute sees it: bf16 slots per row
+        self.row_bytes = mxfp8_record_bytes(H) if quant == "mxfp8" else 2 * H
+        self.Hp = self.row_bytes // 2
         self.cap_send = T * min(k, P) if cap_send is None else cap_send
         self.n_blocks = E if recv_part < 0 else E // P
         if layout == "masked":
@@ -346,9 +394,11 @@ class MoePath:
         self.part_counts = torch.empty((S, P), **i32)
         self.part_offsets = torch.empty((S, P + 1), **i32)
         self.token_slot = torch.empty((S, T, P), **i32)
-        self.send = torch.empty((S, self.cap_send, H), dtype=torch.bfloat16, device=d)
+        row_dt = torch.uint8 if quant == "mxfp8" else torch.bfloat16
+        row_w = self.row_bytes if quant == "mxfp8" else H
+        self.send = torch.empty((S, self.cap_send, row_w), dtype=row_dt, device=d)
         self.send_src = torch.empty((S, self.cap_send), **i32)
-        self.recv = torch.empty((self.cap_recv, H), dtype=torch.bfloat16, device=d)
+        self.recv = torch.empty((self.cap_recv, row_w), dtype=row_dt, device=d)
         self.expert_offsets = torch.empty((E + 1,), **i32)
         self.pair_row = torch.empty((S, T, k), **i32)
         self.recv_pair = torch.empty((self.cap_recv,), **i32)
@@ -360,13 +410,17 @@ class MoePath:
         self.ret = (torch.empty((S, self.cap_send, H), dtype=torch.bfloat16, device=d)
                     if combine == "two_stage" else None)
         self.y = None
+        if quant == "mxfp8":
+            self.y = torch.empty((self.cap_recv, H), dtype=torch.bfloat16, device=d)
+            self.unit_scale = torch.ones((E,), dtype=torch.float32, device=d)
 
-    def bind(self, logits, x, stream=None):
-        """Pre-marshal the five calls for fixed input tensors and stream.
+    def bind(self, logits, x, stream=None, scale=None):
+        """Pre-marshal the calls of one step for fixed input tensors and stream.
 
         Returns a list of (C function, argument tuple); calling them in order
-        is one step (route, layout, pack, permute, combine) with no per-call
-        Python checks, so the host enqueues far ahead of the GPU.
+        is one step (route, layout, pack, permute, [dequantizing stand-in
+        expert with MXFP8 rows], combine) with no per-call Python checks, so
+        the host enqueues far ahead of the GPU.
         """
         lib = load_library()
         st = _stream(stream)
@@ -376,6 +430,7 @@ class MoePath:
         if tuple(logits.shape) != (S, T, E) or tuple(x.shape) != (S, T, H):
             raise ValueError("bind: logits / x shapes do not match the path")
         stp = vp(self.dev_status.data_ptr())
+        Hp = self.Hp
         calls = [
             (lib.moe_route_topk, (ptr(logits, "logits", (torch.float32,)), S, T, E, k,
                                   vp(self.topk_ids.data_ptr()), vp(self.topk_w.data_ptr()), st)),
@@ -386,12 +441,17 @@ class MoePath:
                                        vp(self.part_offsets.data_ptr()),
                                        vp(self.token_slot.data_ptr()), vp(self.ws.data_ptr()),
                                        self.ws.numel(), stp, st)),
-            (lib.moe_dispatch_pack, (ptr(x, "x", _BF16_TYPES), S, T, H, P,
-                                     vp(self.token_slot.data_ptr()),
-                                     vp(self.part_offsets.data_ptr()), self.cap_send,
-                                     vp(self.send.data_ptr()), vp(self.send_src.data_ptr()), stp,
-                                     st)),
         ]
+        if self.quant == "mxfp8":
+            calls.append((lib.moe_dispatch_pack_mxfp8, (
+                ptr(x, "x", _BF16_TYPES), S, T, H, P, vp(self.token_slot.data_ptr()),
+                vp(self.part_offsets.data_ptr()), self.cap_send, vp(self.send.data_ptr()),
+                vp(self.send_src.data_ptr()), stp, st)))
+        else:
+            calls.append((lib.moe_dispatch_pack, (
+                ptr(x, "x", _BF16_TYPES), S, T, H, P, vp(self.token_slot.data_ptr()),
+                vp(self.part_offsets.data_ptr()), self.cap_send, vp(self.send.data_ptr()),
+                vp(self.send_src.data_ptr()), stp, st)))
         if self.layout == "masked":
             calls.append((lib.moe_permute_to_experts_masked, (
                 vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
@@ -404,13 +464,21 @@ class MoePath:
             calls.append((lib.moe_permute_to_experts, (
                 vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
                 vp(self.topk_ids.data_ptr()), vp(self.expert_counts.data_ptr()),
-                vp(self.expert_rank.data_ptr()), S, T, k, E, P, H, self.recv_part, self.align,
+                vp(self.expert_rank.data_ptr()), S, T, k, E, P, Hp, self.recv_part, self.align,
                 self.cap_send, self.cap_recv, vp(self.recv.data_ptr()),
                 vp(self.expert_offsets.data_ptr()), vp(self.pair_row.data_ptr()),
                 vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st)))
+        y = self.recv
+        if self.quant == "mxfp8":
+            sc = self.unit_scale if scale is None else scale
+            calls.append((lib.moe_expert_scale_mxfp8, (
+                vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()),
+                ptr(sc, "scale", (torch.float32,)), E, H, self.cap_recv, vp(self.y.data_ptr()),
+                st)))
+            y = self.y
         if self.combine_mode == "two_stage":
             calls.append((lib.moe_combine_stage1, (
-                vp(self.recv.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
+                vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
                 vp(self.topk_w.data_ptr()), vp(self.topk_ids.data_ptr()),
                 vp(self.token_slot.data_ptr()), S, T, k, E, P, H, self.recv_part, self.cap_send,
                 vp(self.ret.data_ptr()), stp, st)))
@@ -419,7 +487,7 @@ class MoePath:
                 self.cap_send, vp(self.out.data_ptr()), stp, st)))
         else:
             calls.append((lib.moe_combine, (
-                vp(self.recv.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
+                vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
                 vp(self.topk_w.data_ptr()), S, T, k, H, vp(self.out.data_ptr()), stp, st)))
         return calls
 
@@ -439,6 +507,15 @@ class MoePath:
         moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts, self.expert_rank,
                             self.part_counts, self.part_offsets, self.token_slot, self.ws,
                             self.dev_status, stream)
+        if self.quant == "mxfp8":
+            moe_dispatch_pack_mxfp8(x, self.token_slot, self.part_offsets, self.send,
+                                    self.send_src, self.dev_status, stream)
+            moe_permute_to_experts(self.send.view(torch.bfloat16), self.token_slot, self.topk_ids,
+                                   self.expert_counts, self.expert_rank, self.E, self.recv_part,
+                                   self.align, self.recv.view(torch.bfloat16),
+                                   self.expert_offsets, self.pair_row, self.recv_pair, self.ws,
+                                   self.dev_status, stream)
+            return
         moe_dispatch_pack(x, self.token_slot, self.part_offsets, self.send, self.send_src,
                           self.dev_status, stream)
         if self.layout == "masked":
@@ -456,13 +533,18 @@ class MoePath:
     def expert(self, scale, stream=None):
         if self.layout != "contiguous":
             raise ValueError("the stand-in expert reads contiguous expert runs")
+        if self.quant == "mxfp8":
+            sc = self.unit_scale if scale is None else scale
+            moe_expert_scale_mxfp8(self.recv, self.expert_offsets, sc, self.y, stream)
+            return self.y
         if self.y is None:
             self.y = torch.empty_like(self.recv)
         moe_expert_scale(self.recv, self.expert_offsets, scale, self.y, stream)
         return self.y
 
     def combine(self, y=None, stream=None):
-        y = self.recv if y is None else y
+        if y is None:
+            y = self.y if self.quant == "mxfp8" else self.recv
         if self.combine_mode == "two_stage":
             moe_combine_stage1(y, self.pair_row, self.topk_w, self.topk_ids, self.token_slot,
                                self.E, self.recv_part, self.ret, self.dev_status, stream)
@@ -474,13 +556,15 @@ class MoePath:
         """route -> layout -> pack -> permute -> [stand-in expert] -> combine; returns out."""
         self.route(logits, stream)
         self.dispatch(x, stream)
-        y = self.expert(scale, stream) if scale is not None else None
+        y = self.expert(scale, stream) if scale is not None or self.quant == "mxfp8" else None
         self.combine(y, stream)
         return self.out
 
     def launches_per_step(self, with_expert=False) -> int:
         """Kernels one step enqueues: route 1, layout 2 (1 if T <= 256), pack 1, permute 2
-        (map + copy), combine 1 (2 when split into two stages)."""
+        (map + copy), stand-in expert 1 (always with MXFP8 rows), combine 1 (2 when split
+        into two stages)."""
+        with_expert = with_expert or self.quant == "mxfp8"
         if self.T == 0:
             return 1 + 1 + 2 + (1 if with_expert else 0)
         layout = 1 if self.T <= 256 else 2

@@ -224,6 +224,29 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                        __func__);
 }
 
+moe_status_t moe_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, int P,
+                                     const int32_t *token_slot, const int32_t *part_offsets,
+                                     int cap_send, uint8_t *send_q, int32_t *send_src,
+                                     uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
+    REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    const int64_t rb = (int64_t)H + H / 32;
+    REQUIRE_ARR(x, NT * H, 16);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(send_q, (int64_t)S * cap_send * rb, 8);
+    REQUIRE_ARR(send_src, (int64_t)S * cap_send, 4);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(launch_dispatch_pack_mxfp8(x, S, T, H, P, token_slot, part_offsets,
+                                                  cap_send, send_q, send_src, dev_status, stream),
+                       __func__);
+}
+
 moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
                                     const int32_t *topk_ids, const int32_t *expert_counts,
                                     const int32_t *expert_rank, int S, int T, int k, int E, int P,
@@ -376,6 +399,22 @@ moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offset
     REQUIRE_ARR(y, (int64_t)cap_recv * H, 16);
     return cuda_status(
         launch_expert_scale(recv, expert_offsets, scale, E, H, cap_recv, y, stream), __func__);
+}
+
+moe_status_t moe_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                    const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                                    cudaStream_t stream)
+{
+    REQUIRE(E >= 1 && E <= kMaxE, "%s: E=%d must be in [1, %d]", __func__, E, kMaxE);
+    REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
+    REQUIRE(cap_recv >= 0, "%s: cap_recv=%d must be >= 0", __func__, cap_recv);
+    REQUIRE_ARR(recv_q, (int64_t)cap_recv * (H + H / 32), 8);
+    REQUIRE_ARR(expert_offsets, E + 1, 4);
+    REQUIRE_ARR(scale, E, 4);
+    REQUIRE_ARR(y, (int64_t)cap_recv * H, 16);
+    return cuda_status(
+        launch_expert_scale_mxfp8(recv_q, expert_offsets, scale, E, H, cap_recv, y, stream),
+        __func__);
 }
 
 }  // extern "C"

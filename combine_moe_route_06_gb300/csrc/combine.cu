@@ -11,6 +11,8 @@
 // once to bf16 and stream the result out.
 #include <cuda_bf16.h>
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "launch.h"
 #include "trace.h"
@@ -327,6 +329,76 @@ __global__ void __launch_bounds__(256) k_expert_scale(const int4 *__restrict__ r
     }
 }
 
+// Stand-in expert on MXFP8 records (codes, then one E8M0 byte per 32 values):
+//   y = bf16( s_e * e4m3(code) * 2^(scale - 127) )
+// One warp per (row, 1,024-value segment); each lane decodes 8 codes.  The
+// code times s_e is rounded once to fp32; the power of two is applied in two
+// exact halves so that only a result below the normal range rounds again.
+__global__ void __launch_bounds__(256) k_expert_scale_mxfp8(
+    const uint8_t *__restrict__ recv_q, const int32_t *__restrict__ expert_offsets,
+    const float *__restrict__ scale, int E, int V, int cap_recv, int4 *__restrict__ y)
+{
+    extern __shared__ int off[];  // [E + 1]
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = __ldg(expert_offsets + i);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int rows = off[E] < cap_recv ? off[E] : cap_recv;
+    const int64_t rb = (int64_t)V * 8 + V / 4;
+    const int nseg = (V + 127) / 128;
+    const int64_t ntask = (int64_t)rows * nseg;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
+         task += gwarps) {
+        const int row = (int)(task / nseg);
+        const int g = (int)(task - (int64_t)row * nseg);
+        int lo = 0, hi = E - 1;  // last e with off[e] <= row
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= row) lo = mid;
+            else hi = mid - 1;
+        }
+        const float sc = __ldg(scale + lo);
+        const uint8_t *rec = recv_q + (int64_t)row * rb;
+        uint2 c[4];
+        int sb[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int vi = g * 128 + u * 32 + lane;
+            c[u] = make_uint2(0, 0);
+            sb[u] = 127;
+            if (vi < V) {
+                c[u] = ld_stream(reinterpret_cast<const uint2 *>(rec) + vi);
+                sb[u] = __ldg(rec + (int64_t)V * 8 + (vi >> 2));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int vi = g * 128 + u * 32 + lane;
+            if (vi >= V) continue;
+            const int k2 = sb[u] - 127;
+            const int k1 = k2 / 2;
+            const float f1 = __uint_as_float((uint32_t)(127 + k1) << 23);
+            const float f2 = __uint_as_float((uint32_t)(127 + k2 - k1) << 23);
+            const uint32_t w[2] = {c[u].x, c[u].y};
+            float a[8];
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                        (__nv_fp8x2_storage_t)(w[i] >> (16 * h)), __NV_E4M3);
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                    a[4 * i + 2 * h] = (f.x * sc) * f1 * f2;
+                    a[4 * i + 2 * h + 1] = (f.y * sc) * f1 * f2;
+                }
+            }
+            st_cg(y + (int64_t)row * V + vi, pack_bf16x8(a));
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_row, const float *w,
@@ -403,6 +475,22 @@ cudaError_t launch_combine_stage2(const uint16_t *ret, const int32_t *token_slot
                       e = launch_pdl(k_combine_stage2, dim3((unsigned)blocks), dim3(kCombThreads),
                                      0, st, (const int4 *)ret, token_slot, N, T, P, V, cap_send,
                                      (int4 *)out, dev_status));
+    return e;
+}
+
+cudaError_t launch_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                      const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                                      cudaStream_t st)
+{
+    if (cap_recv == 0) return cudaSuccess;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int blocks = di.sm_count * 8;
+    MOE_TRACED_LAUNCH("k_expert_scale_mxfp8", st,
+                      e = launch_pdl(k_expert_scale_mxfp8, dim3(blocks), dim3(256),
+                                     (size_t)(E + 1) * sizeof(int), st, recv_q, expert_offsets,
+                                     scale, E, H / 8, cap_recv, (int4 *)y));
     return e;
 }
 

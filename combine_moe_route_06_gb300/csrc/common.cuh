@@ -58,6 +58,12 @@ __device__ __forceinline__ int4 ld_stream(const int4 *p)
                  : "l"(p));
     return v;
 }
+__device__ __forceinline__ uint2 ld_stream(const uint2 *p)
+{
+    uint2 v;
+    asm volatile("ld.global.cs.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
 // Intermediate buffers that the next kernel reads: keep in L2 (cache global).
 __device__ __forceinline__ int4 ld_cg(const int4 *p)
 {

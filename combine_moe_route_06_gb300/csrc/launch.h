@@ -40,6 +40,14 @@ cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                                  int cap_send, uint16_t *send, int32_t *send_src,
                                  uint32_t *dev_status, cudaStream_t st);
 
+cudaError_t launch_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, int P,
+                                       const int32_t *token_slot, const int32_t *part_offsets,
+                                       int cap_send, uint8_t *send_q, int32_t *send_src,
+                                       uint32_t *dev_status, cudaStream_t st);
+cudaError_t launch_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                      const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                                      cudaStream_t st);
+
 size_t permute_ws_bytes(int S, int T, int E);
 cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, const int32_t *ids,
                            const int32_t *expert_counts, const int32_t *expert_rank,

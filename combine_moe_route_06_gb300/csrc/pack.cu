@@ -9,6 +9,8 @@
 // segment of x once (16-byte vectors, four per lane in flight) and stores it
 // to each of the token's c <= min(k, P) destination rows.  HBM traffic is the
 // minimum: x read once, c copies written.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "launch.h"
 #include "trace.h"
@@ -81,6 +83,106 @@ __global__ void __launch_bounds__(kPackThreads) k_pack(const int4 *__restrict__ 
     if (__any_sync(kFull, overflow) && lane == 0) flag_status(dev_status, MOE_ERR_CAPACITY);
 }
 
+// Pack with MXFP8 records (a2a-backends section 7.2: tokens are converted
+// before they are sent; an FP8 row is 5,280 bytes for 5,120 values, one scale
+// byte per 32).  A record is H E4M3 codes followed by H/32 E8M0 scales,
+//   X = 2^(floor(log2 max|v|) - 8), code = e4m3_rn_satfinite(v / X).
+// One warp per (token, 1,024-value segment); lanes 4b..4b+3 hold one 32-value
+// block for each of the four 16-byte loads.  The row is quantized once and
+// stored to every destination slot.  Finite inputs give se <= 120, so the
+// 2^-se factor below is a normal float.
+constexpr int kQSegVec = 32 * kPackUnroll;   // int4 (8 values) per segment
+
+__device__ __forceinline__ int mx_shared_exp(float amax)
+{
+    if (amax == 0.f) return -127;
+    const unsigned bits = __float_as_uint(amax);
+    const int field = (int)((bits >> 23) & 0xFFu);
+    const int e = field ? field - 127 : (31 - __clz((int)(bits & 0x7FFFFFu))) - 149;
+    const int se = e - 8;
+    return se < -127 ? -127 : (se > 127 ? 127 : se);
+}
+
+__global__ void __launch_bounds__(kPackThreads) k_pack_mxfp8(
+    const int4 *__restrict__ x, int S, int T, int V, int P, const int32_t *__restrict__ token_slot,
+    const int32_t *__restrict__ part_offsets, int cap_send, uint8_t *__restrict__ send_q,
+    int32_t *__restrict__ send_src, uint32_t *dev_status)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
+        const int s = (int)(i / cap_send);
+        const int r = (int)(i - (int64_t)s * cap_send);
+        if (r >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) send_src[i] = -1;
+    }
+    const int64_t rb = (int64_t)V * 8 + V / 4;  // record bytes: codes, then scales
+    const int nseg = (V + kQSegVec - 1) / kQSegVec;
+    const int64_t ntask = (int64_t)S * T * nseg;
+    const int64_t gwarps = gthreads >> 5;
+    bool overflow = false;
+    for (int64_t task = gtid >> 5; task < ntask; task += gwarps) {
+        const int64_t n = task / nseg;
+        const int g = (int)(task - n * nseg);
+        const int s = (int)(n / T);
+        int slot = -1;
+        if (lane < P) slot = __ldg(token_slot + n * P + lane);
+        const bool ok = slot >= 0 && slot < cap_send;
+        if (slot >= cap_send) overflow = true;
+        unsigned dmask = __ballot_sync(kFull, ok);
+        if (g == 0 && ok) send_src[(int64_t)s * cap_send + slot] = (int32_t)(n - (int64_t)s * T);
+        if (dmask == 0) continue;
+
+        const int v0 = g * kQSegVec + lane;
+        uint2 code[kPackUnroll];
+        uint8_t scale[kPackUnroll];
+#pragma unroll
+        for (int u = 0; u < kPackUnroll; u++) {
+            const int vi = v0 + 32 * u;
+            int4 v = make_int4(0, 0, 0, 0);
+            if (vi < V) v = ld_stream(x + n * V + vi);
+            const uint32_t w4[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+            float f[8];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                f[2 * i] = __uint_as_float(w4[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+            const int se = mx_shared_exp(amax);
+            const float inv = __uint_as_float((uint32_t)(127 - se) << 23);   // 2^-se, exact
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                lo |= (uint32_t)__nv_cvt_float_to_fp8(f[i] * inv, __NV_SATFINITE, __NV_E4M3) << (8 * i);
+                hi |= (uint32_t)__nv_cvt_float_to_fp8(f[4 + i] * inv, __NV_SATFINITE, __NV_E4M3) << (8 * i);
+            }
+            code[u] = make_uint2(lo, hi);
+            scale[u] = (uint8_t)(se + 127);
+        }
+        while (dmask) {
+            const int p = __ffs(dmask) - 1;
+            dmask &= dmask - 1;
+            const int sl = __shfl_sync(kFull, slot, p);
+            uint8_t *rec = send_q + ((int64_t)s * cap_send + sl) * rb;
+#pragma unroll
+            for (int u = 0; u < kPackUnroll; u++) {
+                const int vi = v0 + 32 * u;
+                if (vi < V) {
+                    reinterpret_cast<uint2 *>(rec)[vi] = code[u];
+                    if ((vi & 3) == 0) rec[(int64_t)V * 8 + (vi >> 2)] = scale[u];
+                }
+            }
+        }
+    }
+    if (__any_sync(kFull, overflow) && lane == 0) flag_status(dev_status, MOE_ERR_CAPACITY);
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
@@ -104,6 +206,30 @@ cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                       e = launch_pdl(k_pack, dim3((unsigned)blocks), dim3(kPackThreads), 0, st,
                                      (const int4 *)x, S, T, V, P, token_slot, part_offsets,
                                      cap_send, (int4 *)send, send_src, dev_status));
+    return e;
+}
+
+cudaError_t launch_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, int P,
+                                       const int32_t *token_slot, const int32_t *part_offsets,
+                                       int cap_send, uint8_t *send_q, int32_t *send_src,
+                                       uint32_t *dev_status, cudaStream_t st)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int V = H / 8;
+    const int nseg = (V + kQSegVec - 1) / kQSegVec;
+    const int64_t warps = (int64_t)S * T * nseg;
+    const int64_t want = (warps + (kPackThreads / 32) - 1) / (kPackThreads / 32);
+    const int resident = resident_grid((const void *)k_pack_mxfp8, kPackThreads, 0);
+    int64_t blocks = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPackThreads);
+    if (want < blocks) blocks = want;
+    const int64_t tail_blocks = ((int64_t)S * cap_send + kPackThreads - 1) / kPackThreads;
+    if (blocks < 1) blocks = tail_blocks < 1 ? 1 : (tail_blocks < di.sm_count ? tail_blocks : di.sm_count);
+    MOE_TRACED_LAUNCH("k_pack_mxfp8", st,
+                      e = launch_pdl(k_pack_mxfp8, dim3((unsigned)blocks), dim3(kPackThreads), 0, st,
+                                     (const int4 *)x, S, T, V, P, token_slot, part_offsets,
+                                     cap_send, send_q, send_src, dev_status));
     return e;
 }
 

@@ -183,6 +183,30 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                                uint32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Pack with the rows quantized on the way (a2a-backends section 7.2: expert
+ * kernels that quantize their input anyway can take rows already quantized,
+ * so a token is converted before it is sent; a DeepSeek-V4.1-Flash FP8 row is
+ * 5,280 bytes: 5,120 one-byte values and a one-byte scale per 32 values).
+ * A quantized row is one record of H + H/32 bytes: the H E4M3 codes, then the
+ * H/32 E8M0 block scales.  Encoding (the page fixes only the sizes): OCP
+ * MXFP8, per block of 32 values
+ *   X = 2^(floor(log2 max|v|) - 8), clamped to [2^-127, 2^127]; scale byte = log2 X + 127
+ *   code_i = e4m3(v_i / X), round to nearest even, magnitudes above 448 -> 448
+ * An all-zero block gets scale byte 0.  x must be finite.
+ *   x            [S][T][H] bf16 in; H a multiple of 256 (8-byte aligned records).
+ *   send_q       [S][cap_send][H + H/32] uint8 out, 8-byte aligned.  Rows that no
+ *                slot names are not written.
+ *   token_slot, part_offsets, cap_send, send_src, dev_status: as moe_dispatch_pack.
+ * The records move through moe_permute_to_experts(_masked) as opaque rows of
+ * (H + H/32)/2 bf16 slots, which needs H % 512 == 0.
+ * Errors: as moe_dispatch_pack.
+ */
+moe_status_t moe_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, int P,
+                                     const int32_t *token_slot, const int32_t *part_offsets,
+                                     int cap_send, uint8_t *send_q, int32_t *send_src,
+                                     uint32_t *dev_status, cudaStream_t stream);
+
+/*
  * Receiver permute into expert-contiguous runs (a2a-backends section 1.5:
  * the contiguous layout, runs optionally padded to a multiple of `align`
  * rows as DeepGEMM wants 128; section 3.3: one row per (token, local
@@ -306,6 +330,21 @@ moe_status_t moe_combine_stage2(const uint16_t *ret, const int32_t *token_slot, 
 moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
                               const float *scale, int E, int H, int cap_recv, uint16_t *y,
                               cudaStream_t stream);
+
+/*
+ * Stand-in expert on MXFP8 records (harness, like moe_expert_scale): for each
+ * row r of expert e's run, y[r][h] = bf16( scale[e] * e4m3(code[r][h]) *
+ * 2^(scale_byte[r][h/32] - 127) ).  The product code * scale[e] is rounded to
+ * fp32 before the power of two, so y may differ from the exactly rounded value
+ * by one bf16 unit.
+ *   recv_q  [cap_recv][H + H/32] uint8 records (moe_dispatch_pack_mxfp8), 8-byte aligned.
+ *   y       [cap_recv][H] bf16 out, 16-byte aligned; rows at or beyond
+ *           min(expert_offsets[E], cap_recv) are not written.
+ *   H a multiple of 256.  Errors: MOE_ERR_INVALID_ARG / MOE_ERR_CUDA.
+ */
+moe_status_t moe_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                    const float *scale, int E, int H, int cap_recv, uint16_t *y,
+                                    cudaStream_t stream);
 
 /*
  * Per-kernel timing (tracing aid; off by default).  While enabled, every
