@@ -75,12 +75,15 @@ def _load():
             lib.oracle_quantize_mxfp8_block.restype = None
             lib.oracle_dispatch_pack_mxfp8.argtypes = [P, i32, i64, i32, i32, P, i64, P, P, P]
             lib.oracle_expert_scale_mxfp8.argtypes = [P, P, P, i32, i32, i64, P]
+            lib.oracle_plan_placement.argtypes = [P, i32, i32, i32, P, P, P, P]
+            lib.oracle_map_replicas.argtypes = [P, i32, i64, i32, i32, P, P, i32, P]
             lib.oracle_combine.argtypes = [P, P, P, i32, i64, i32, i32, P]
             for f in ("oracle_route_topk", "oracle_dispatch_layout", "oracle_dispatch_pack",
                       "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine",
                       "oracle_permute_masked", "oracle_combine_stage1",
                       "oracle_combine_stage2", "oracle_dispatch_pack_mxfp8",
-                      "oracle_expert_scale_mxfp8"):
+                      "oracle_expert_scale_mxfp8", "oracle_plan_placement",
+                      "oracle_map_replicas"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -343,6 +346,40 @@ def expert_scale_mxfp8(recv_q: np.ndarray, expert_offsets: np.ndarray, scale: np
                                              _p(np.ascontiguousarray(scale, np.float32)), E, H, cap, _p(y)),
            "expert_scale_mxfp8")
     return y
+
+
+def plan_placement(load: np.ndarray, P: int, R: int) -> dict:
+    """Placement by load plus redundant copies of the busiest experts.
+
+    load int64 [E] (pairs per logical expert in a past batch), P partitions, R
+    spare slots per partition.  Returns copy_offsets [E+1], copy_slots
+    [n_copies] (physical slots, original first), slot_expert [P*(E/P+R)]
+    (-1 = empty), part_load [P], Lp = E/P + R and E_phys = P*Lp.
+    """
+    load = np.ascontiguousarray(load, dtype=np.int64)
+    E = load.shape[0]
+    Lp = E // P + R
+    co = np.empty(E + 1, np.int32)
+    cs = np.full(E + P * R, -1, np.int32)
+    se = np.empty(P * Lp, np.int32)
+    pl = np.empty(P, np.int64)
+    _check(_load().oracle_plan_placement(_p(load), E, P, R, _p(co), _p(cs), _p(se), _p(pl)),
+           "plan_placement")
+    return {"copy_offsets": co, "copy_slots": cs[:co[-1]].copy(), "slot_expert": se,
+            "part_load": pl, "Lp": Lp, "E_phys": P * Lp}
+
+
+def map_replicas(ids: np.ndarray, E: int, copy_offsets: np.ndarray, copy_slots: np.ndarray,
+                 E_phys: int) -> np.ndarray:
+    """Physical expert of every pair: the r-th pair of e from a source -> copy r mod n_e."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    S, T, k = ids.shape
+    phys = np.empty_like(ids)
+    _check(_load().oracle_map_replicas(_p(ids), S, T, k, E,
+                                       _p(np.ascontiguousarray(copy_offsets, np.int32)),
+                                       _p(np.ascontiguousarray(copy_slots, np.int32)), E_phys,
+                                       _p(phys)), "map_replicas")
+    return phys
 
 
 def run_path(x: np.ndarray, logits: np.ndarray, E: int, k: int, P: int, scales: np.ndarray | None,

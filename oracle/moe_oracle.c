@@ -759,3 +759,181 @@ int oracle_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offse
     }
     return 0;
 }
+
+/* ------------------------------------------ expert placement, [b1g] 6 -- */
+
+/*
+ * Share of copy c of an expert with `load` pairs and n copies when the r-th
+ * pair goes to copy r mod n: the number of r in [0, load) with r % n == c.
+ */
+static int64_t oracle_copy_share(int64_t load, int n, int c)
+{
+    return load > c ? (load - c + n - 1) / n : 0;
+}
+
+/*
+ * [b1g] 6, "The fix: place experts by load, and copy the hot ones":
+ *  1. placement by load -- the heaviest expert first, each on the least
+ *     loaded partition (GPU) that still has one of its E/P regular slots;
+ *  2. redundant copies -- every partition has R spare slots; repeatedly take
+ *     the busiest partition, its busiest expert (largest share), and copy it
+ *     to the least loaded partition with a free spare slot; the expert's
+ *     pairs are then split evenly over its copies.  A copy is kept only if
+ *     it does not make a new busiest partition, i.e. the receiving
+ *     partition's new load stays below the old maximum; the first copy that
+ *     fails this test ends the loop, as does running out of spare slots.
+ * Readings: loads are integer pair counts and the even split is the one the
+ * layout implements (share of copy c = #{r < load : r mod n = c}); ties go to
+ * the lower expert id and the lower partition; a partition never holds two
+ * copies of one expert.
+ * Physical slots: partition p owns slots [p*Lp, (p+1)*Lp), Lp = E/P + R,
+ * filled in the order experts arrive there (regular slots first, then the
+ * copies).  Outputs: copy_offsets[E+1] and copy_slots[] (CSR of each
+ * expert's slots, original first, copies in the order they were made),
+ * slot_expert[P*Lp] (-1 = empty), part_load[P] (loads after the copies).
+ */
+int oracle_plan_placement(const int64_t *load, int E, int P, int R, int32_t *copy_offsets,
+                          int32_t *copy_slots, int32_t *slot_expert, int64_t *part_load)
+{
+    if (E < 1 || P < 1 || E % P != 0 || R < 0)
+        return -1;
+    const int Lb = E / P, Lp = E / P + R;
+    int *order = (int *)malloc(sizeof(int) * (size_t)E);
+    int *ncopy = (int *)calloc((size_t)E, sizeof(int));
+    int32_t *slots = (int32_t *)malloc(sizeof(int32_t) * (size_t)E * (size_t)(P + 1));
+    int *used = (int *)calloc((size_t)P, sizeof(int));
+    if (!order || !ncopy || !slots || !used)
+        return -2;
+    for (int i = 0; i < P * Lp; i++)
+        slot_expert[i] = -1;
+    /* 1. heaviest first (selection by scanning: ties to the lower id) */
+    char *taken = (char *)calloc((size_t)E, 1);
+    for (int i = 0; i < E; i++) {
+        int best = -1;
+        for (int e = 0; e < E; e++)
+            if (!taken[e] && (best < 0 || load[e] > load[best]))
+                best = e;
+        taken[best] = 1;
+        order[i] = best;
+    }
+    free(taken);
+    for (int p = 0; p < P; p++)
+        part_load[p] = 0;
+    for (int i = 0; i < E; i++) {
+        const int e = order[i];
+        int q = -1;
+        for (int p = 0; p < P; p++)
+            if (used[p] < Lb && (q < 0 || part_load[p] < part_load[q]))
+                q = p;
+        const int s = q * Lp + used[q]++;
+        slot_expert[s] = e;
+        slots[(size_t)e * (P + 1)] = s;
+        ncopy[e] = 1;
+        part_load[q] += load[e];
+    }
+    /* 2. copies */
+    for (;;) {
+        /* loads from the current copies */
+        for (int p = 0; p < P; p++)
+            part_load[p] = 0;
+        for (int e = 0; e < E; e++)
+            for (int c = 0; c < ncopy[e]; c++)
+                part_load[slots[(size_t)e * (P + 1) + c] / Lp] += oracle_copy_share(load[e], ncopy[e], c);
+        int g = 0;
+        for (int p = 1; p < P; p++)
+            if (part_load[p] > part_load[g])
+                g = p;
+        int best = -1;
+        int64_t best_share = -1;
+        for (int e = 0; e < E; e++)
+            for (int c = 0; c < ncopy[e]; c++)
+                if (slots[(size_t)e * (P + 1) + c] / Lp == g) {
+                    const int64_t sh = oracle_copy_share(load[e], ncopy[e], c);
+                    if (sh > best_share) {
+                        best_share = sh;
+                        best = e;
+                    }
+                }
+        if (best < 0)
+            break;
+        int tgt = -1;
+        for (int p = 0; p < P; p++) {
+            if (used[p] >= Lp)
+                continue;
+            int holds = 0;
+            for (int c = 0; c < ncopy[best]; c++)
+                if (slots[(size_t)best * (P + 1) + c] / Lp == p)
+                    holds = 1;
+            if (holds)
+                continue;
+            if (tgt < 0 || part_load[p] < part_load[tgt])
+                tgt = p;
+        }
+        if (tgt < 0)
+            break;
+        /* the receiving partition's load with one more copy of `best` */
+        const int n1 = ncopy[best] + 1;
+        const int64_t new_tgt = part_load[tgt] + oracle_copy_share(load[best], n1, n1 - 1);
+        if (!(new_tgt < part_load[g]))
+            break;
+        const int s = tgt * Lp + used[tgt]++;
+        slot_expert[s] = best;
+        slots[(size_t)best * (P + 1) + ncopy[best]] = s;
+        ncopy[best] = n1;
+    }
+    /* final loads and the CSR */
+    for (int p = 0; p < P; p++)
+        part_load[p] = 0;
+    int o = 0;
+    for (int e = 0; e < E; e++) {
+        copy_offsets[e] = o;
+        for (int c = 0; c < ncopy[e]; c++) {
+            const int32_t s = slots[(size_t)e * (P + 1) + c];
+            copy_slots[o++] = s;
+            part_load[s / Lp] += oracle_copy_share(load[e], ncopy[e], c);
+        }
+    }
+    copy_offsets[E] = o;
+    free(order);
+    free(ncopy);
+    free(slots);
+    free(used);
+    return 0;
+}
+
+/*
+ * Physical expert of every pair under a placement ([b1g] 6: the expert's
+ * pairs are split evenly over its copies): for each source, the r-th pair of
+ * logical expert e in (t, j) order goes to copy r mod n_e, i.e.
+ *   phys[s][t][j] = copy_slots[copy_offsets[e] + (r mod n_e)].
+ * Ids < 0 stay -1 (not routed); ids >= E become E_phys (an invalid physical
+ * id, so the layout that follows flags it).
+ */
+int oracle_map_replicas(const int32_t *ids, int S, int64_t T, int k, int E,
+                        const int32_t *copy_offsets, const int32_t *copy_slots, int E_phys,
+                        int32_t *phys)
+{
+    int64_t *seen = (int64_t *)malloc(sizeof(int64_t) * (size_t)E);
+    if (!seen)
+        return -2;
+    for (int s = 0; s < S; s++) {
+        for (int e = 0; e < E; e++)
+            seen[e] = 0;
+        for (int64_t t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                const int64_t i = ((int64_t)s * T + t) * k + j;
+                const int32_t e = ids[i];
+                if (e < 0) {
+                    phys[i] = -1;
+                } else if (e >= E) {
+                    phys[i] = E_phys;
+                } else {
+                    const int n = copy_offsets[e + 1] - copy_offsets[e];
+                    phys[i] = copy_slots[copy_offsets[e] + (int)(seen[e] % n)];
+                    seen[e]++;
+                }
+            }
+    }
+    free(seen);
+    return 0;
+}

@@ -719,3 +719,102 @@ def test_expert_scale_mxfp8_reduces_to_bf16_expert():
     eo = np.array([0, 17, R], np.int32)
     s = np.array([0.25, 3.0], np.float32)
     assert np.array_equal(oracle.expert_scale_mxfp8(rec, eo, s), oracle.expert_scale(bits, eo, s))
+
+
+# ------------------------------ expert placement and copies (b1g section 6) --
+
+def _check_plan_invariants(load, P, R, plan):
+    E = load.size
+    Lb, Lp = E // P, E // P + R
+    co, cs, se = plan["copy_offsets"], plan["copy_slots"], plan["slot_expert"]
+    assert co[0] == 0 and np.all(np.diff(co) >= 1)               # every expert has a slot
+    assert co[-1] <= E + P * R
+    for e in range(E):
+        sl = cs[co[e]:co[e + 1]]
+        assert np.all(se[sl] == e)
+        assert len(set(sl // Lp)) == sl.size                     # one copy per partition at most
+        assert sl[0] % Lp < Lb                                   # the original in a regular slot
+        assert np.all(sl[1:] % Lp >= Lb)                         # copies in spare slots
+    assert np.sum(se >= 0) == co[-1]
+    # loads: the even split of every expert over its copies, summed per partition
+    want = np.zeros(P, np.int64)
+    for e in range(E):
+        n = co[e + 1] - co[e]
+        for c, s_ in enumerate(cs[co[e]:co[e + 1]]):
+            want[s_ // Lp] += len(range(c, int(load[e]), n))
+    assert np.array_equal(plan["part_load"], want)
+    assert plan["part_load"].sum() == load.sum()
+
+
+def test_placement_hand_example():
+    g = _golden("placement_hand.json")
+    load = np.array(g["load"], np.int64)
+    plan = oracle.plan_placement(load, g["P"], g["R"])
+    for key in ("copy_offsets", "copy_slots", "slot_expert", "part_load"):
+        assert plan[key].tolist() == g[key], key
+    _check_plan_invariants(load, g["P"], g["R"], plan)
+
+
+@pytest.mark.parametrize("E,P,R,seed", [(16, 4, 0, 1), (16, 4, 2, 2), (64, 8, 4, 3),
+                                        (384, 8, 4, 4), (8, 8, 3, 5), (64, 64, 1, 6)])
+def test_placement_invariants_and_gain(E, P, R, seed):
+    rng = np.random.default_rng(seed)
+    p = (np.arange(E) + 1.0) ** -1.2
+    load = rng.multinomial(E * 40, p / p.sum()).astype(np.int64)
+    rng.shuffle(load)
+    plan = oracle.plan_placement(load, P, R)
+    _check_plan_invariants(load, P, R, plan)
+    # contiguous placement (expert e on partition e // (E/P)) as the baseline
+    base = np.bincount(np.arange(E) // (E // P), weights=load, minlength=P)
+    only = oracle.plan_placement(load, P, 0)
+    assert only["copy_offsets"][-1] == E                          # R = 0: no copies
+    assert plan["part_load"].max() <= only["part_load"].max()     # copies never raise the max
+    if E > P:
+        assert only["part_load"].max() <= base.max()              # greedy beats contiguous here
+    else:
+        # one expert per partition: placement cannot help, only copies can
+        assert only["part_load"].max() == load.max()
+        if R > 0:
+            assert plan["part_load"].max() < load.max()
+
+
+def test_map_replicas_identity_and_skips():
+    rng = np.random.default_rng(11)
+    E = 16
+    ids = rng.integers(-1, E + 2, size=(2, 50, 3)).astype(np.int32)
+    co, cs = np.arange(E + 1, dtype=np.int32), np.arange(E, dtype=np.int32)
+    phys = oracle.map_replicas(ids, E, co, cs, E)
+    assert np.array_equal(phys[(ids >= 0) & (ids < E)], ids[(ids >= 0) & (ids < E)])
+    assert np.all(phys[ids < 0] == -1) and np.all(phys[ids >= E] == E)
+
+
+def test_map_replicas_round_robin_split():
+    rng = np.random.default_rng(12)
+    E, P, R = 16, 4, 2
+    ids = rng.integers(0, E, size=(3, 200, 4)).astype(np.int32)
+    load = np.bincount(ids[0].ravel(), minlength=E).astype(np.int64)
+    plan = oracle.plan_placement(load, P, R)
+    co, cs = plan["copy_offsets"], plan["copy_slots"]
+    phys = oracle.map_replicas(ids, E, co, cs, plan["E_phys"])
+    assert np.array_equal(plan["slot_expert"][phys], ids)         # a copy of the right expert
+    for s in range(3):
+        flat_ids, flat_ph = ids[s].ravel(), phys[s].ravel()       # (t, j) order
+        for e in range(E):
+            got = flat_ph[flat_ids == e]
+            n = co[e + 1] - co[e]
+            want = cs[co[e] + np.arange(got.size) % n]            # r-th pair -> copy r mod n
+            assert np.array_equal(got, want)
+    # on the batch the plan was made from, the partition loads are the plan's
+    lay = oracle.dispatch_layout(phys[:1], plan["E_phys"], P)
+    pairs_per_part = lay["expert_counts"][0].reshape(P, -1).sum(axis=1)
+    assert np.array_equal(pairs_per_part, plan["part_load"])
+
+
+def test_placement_rejects_a_copy_that_ties_the_busiest():
+    # e0 (6) on p0, e1 (3) on p1; copying e0 to p1 would give p1 3 + 3 = 6, equal to the
+    # busiest partition's 6: that is a new busiest partition, so no copy is kept
+    plan = oracle.plan_placement(np.array([6, 3], np.int64), 2, 1)
+    assert plan["copy_offsets"].tolist() == [0, 1, 2] and plan["part_load"].tolist() == [6, 3]
+    # with 7 the copy brings p1 to 3 + 3 = 6 < 7 and is kept; p0 keeps the larger share
+    plan = oracle.plan_placement(np.array([7, 3], np.int64), 2, 1)
+    assert plan["copy_offsets"].tolist() == [0, 2, 3] and plan["part_load"].tolist() == [4, 6]
