@@ -17,6 +17,7 @@ its own batch (weak scaling, no data-path collective); rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -296,7 +297,26 @@ VARIANTS = {
     "masked": {"layout": "masked"},
     "two_stage": {"combine": "two_stage"},
     "mxfp8": {"quant": "mxfp8"},
+    "placed": {},          # placement planned from another batch; see plan_for()
 }
+
+
+def plan_for(m, torch, w, dev, spare):
+    """Placement by load with `spare` copy slots per partition, planned from
+    the routing of another batch of the same workload (a plan is made from
+    past load and used on new traffic).  Returns the Placement and the
+    receiving partition to time: the busiest one under the plan when the
+    workload times a single receiver, else -1 (all partitions)."""
+    past = dataclasses.replace(w, index=w.index + 7919)
+    tmp = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, device=dev)
+    tmp.route(torch.from_numpy(ms.gen_logits(past)).to(dev))
+    m.moe_dispatch_layout(tmp.topk_ids, w.E, w.P, tmp.expert_counts, tmp.expert_rank,
+                          tmp.part_counts, tmp.part_offsets, tmp.token_slot, tmp.ws, tmp.dev_status)
+    load = tmp.expert_counts.sum(dim=0).cpu().numpy().astype(np.int64)
+    del tmp
+    pl = m.moe_plan_placement(load, w.P, spare)
+    recv_part = int(np.argmax(pl.part_load)) if w.recv_part >= 0 else -1
+    return pl, recv_part
 
 
 def path_kwargs(args, w):
@@ -352,6 +372,14 @@ def run_ours(args, world, rank, local):
     inp = ms.gen_inputs(w)
     stream = torch.cuda.Stream(device=dev)
     pkw = path_kwargs(args, w)
+    placement_info = None
+    if args.variant == "placed":
+        pl, rp = plan_for(m, torch, w, dev, args.spare)
+        pkw["placement"] = pl
+        w = dataclasses.replace(w, recv_part=rp)
+        placement_info = {"spare_slots_per_partition": args.spare, "recv_part": rp,
+                          "physical_experts": pl.E_phys, "copies": int(pl.copy_offsets[-1]) - w.E,
+                          "learned_from": "expert counts of another batch of the workload (index + 7919)"}
     path = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev, **pkw)
     logits = torch.from_numpy(inp["logits"]).to(dev)
     x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
@@ -389,6 +417,16 @@ def run_ours(args, world, rank, local):
         b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv,
                               two_stage=(args.variant == "two_stage"),
                               mxfp8=(args.variant == "mxfp8"))
+        if placement_info is not None:
+            # pairs per partition on the timed batch: contiguous blocks vs the placement
+            ids_h = path.topk_ids.cpu().numpy()
+            logical = np.bincount(ids_h[ids_h >= 0], minlength=w.E)
+            contiguous = logical.reshape(w.P, -1).sum(axis=1)
+            placed = path.expert_counts.sum(dim=0).cpu().numpy().reshape(w.P, -1).sum(axis=1)
+            placement_info["pairs_per_partition"] = {
+                "contiguous_max_over_mean": round(float(contiguous.max() / contiguous.mean()), 4),
+                "placed_max_over_mean": round(float(placed.max() / placed.mean()), 4),
+                "placed_max_partition": int(np.argmax(placed))}
 
         # ---------------- the step as a CUDA graph (fixed shapes and addresses) ---
         # The five calls are recorded once and replayed, as a serving engine
@@ -611,6 +649,7 @@ def run_ours(args, world, rank, local):
                      "us_per_launch": round(1e3 * dom_ms, 2) if dom_ms else None,
                      "launches_timed": len(recs)},
         "cpu_baseline": cpu,
+        **({"placement": placement_info} if placement_info is not None else {}),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
                 "d2h_bytes_per_step": int(h_out.numel() * 2), "steps": Ke,
@@ -638,8 +677,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--variant", default="contiguous", choices=sorted(VARIANTS),
-                    help="receive layout / combine form: contiguous runs + one-stage combine "
-                         "(default), masked blocks, or a two-stage combine")
+                    help="contiguous runs + one-stage combine (default), masked blocks, a "
+                         "two-stage combine, MXFP8 rows, or experts placed by load with copies")
+    ap.add_argument("--spare", type=int, default=4,
+                    help="spare copy slots per partition for --variant placed")
     ap.add_argument("--block-rows", type=int, default=0,
                     help="rows per expert block of the masked layout (default S*T)")
     ap.add_argument("--eager", action="store_true",

@@ -17,6 +17,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 from . import _build
@@ -27,7 +28,8 @@ __all__ = [
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
-    "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
+    "moe_plan_placement", "moe_workspace_bytes_mapped", "moe_dispatch_layout_mapped", "Placement", "MoePath", "trace_enable", "trace_disable", "trace_reset",
     "trace_records",
 ]
 
@@ -99,6 +101,10 @@ def load_library() -> ctypes.CDLL:
             "moe_dispatch_pack_mxfp8": ([P, i32, i32, i32, i32, P, P, i32, P, P, P, P],
                                          ctypes.c_int),
             "moe_expert_scale_mxfp8": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
+            "moe_plan_placement": ([P, i32, i32, i32, P, P, P, P], ctypes.c_int),
+            "moe_workspace_bytes_mapped": ([i32, i32, i32, i32, i32, i32], ctypes.c_size_t),
+            "moe_dispatch_layout_mapped": ([P, i32, i32, i32, i32, i32, i32, P, P, i32, P, P, P, P,
+                                            P, P, P, ctypes.c_size_t, P, P], ctypes.c_int),
             "moe_permute_to_experts_masked": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                i32, i32, P, P, P, P, P, P], ctypes.c_int),
             "moe_expert_scale": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
@@ -217,6 +223,68 @@ def moe_dispatch_pack_mxfp8(x, token_slot, part_offsets, send_q, send_src, dev_s
         _dev(part_offsets, "part_offsets", (torch.int32,)), cap_send,
         _dev(send_q, "send_q", (torch.uint8,), 3), _dev(send_src, "send_src", (torch.int32,)),
         _status_ptr(dev_status), _stream(stream)))
+
+
+class Placement:
+    """A placement of E logical experts on P partitions with Lp slots each.
+
+    copy_offsets [E+1] / copy_slots [n] (CSR of each expert's physical slots),
+    slot_expert [P*Lp] (-1 = empty) and part_load [P] (predicted pairs), all
+    host numpy arrays; `to(device)` gives the device copies the layout reads.
+    """
+
+    def __init__(self, copy_offsets, copy_slots, slot_expert, part_load, P, Lp):
+        self.copy_offsets = np.ascontiguousarray(copy_offsets, np.int32)
+        self.copy_slots = np.ascontiguousarray(copy_slots, np.int32)
+        self.slot_expert = np.ascontiguousarray(slot_expert, np.int32)
+        self.part_load = np.ascontiguousarray(part_load, np.int64)
+        self.E = self.copy_offsets.size - 1
+        self.P, self.Lp = P, Lp
+        self.E_phys = P * Lp
+
+    def to(self, device):
+        d = torch.device(device)
+        return (torch.from_numpy(self.copy_offsets).to(d), torch.from_numpy(self.copy_slots).to(d),
+                torch.from_numpy(self.slot_expert).to(d))
+
+
+def moe_plan_placement(load, P: int, R: int) -> Placement:
+    """Host planner: load int64 [E] (pairs per logical expert) -> Placement."""
+    lib = load_library()
+    load = np.ascontiguousarray(load, np.int64)
+    E = load.size
+    Lp = E // P + R
+    co = np.empty(E + 1, np.int32)
+    cs = np.empty(E + P * R, np.int32)
+    se = np.empty(P * Lp, np.int32)
+    pl = np.empty(P, np.int64)
+    vp = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
+    _check(lib.moe_plan_placement(vp(load), E, P, R, vp(co), vp(cs), vp(se), vp(pl)))
+    return Placement(co, cs[:co[-1]], se, pl, P, Lp)
+
+
+def moe_workspace_bytes_mapped(S: int, T: int, k: int, E: int, P: int, Lp: int) -> int:
+    return int(load_library().moe_workspace_bytes_mapped(S, T, k, E, P, Lp))
+
+
+def moe_dispatch_layout_mapped(topk_ids, E, P, Lp, copy_offsets, copy_slots, phys_ids,
+                               expert_counts, expert_rank, part_counts, part_offsets, token_slot,
+                               ws, dev_status=None, stream=None):
+    """Layout over a placement: topk_ids [S,T,k] logical -> phys_ids [S,T,k] physical slots,
+    expert_counts [S,P*Lp] and the other outputs of moe_dispatch_layout over phys_ids."""
+    lib = load_library()
+    S, T, k = topk_ids.shape
+    _check(lib.moe_dispatch_layout_mapped(
+        _dev(topk_ids, "topk_ids", (torch.int32,), 3), S, T, k, E, P, Lp,
+        _dev(copy_offsets, "copy_offsets", (torch.int32,)),
+        _dev(copy_slots, "copy_slots", (torch.int32,)), copy_slots.numel(),
+        _dev(phys_ids, "phys_ids", (torch.int32,), 3),
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)),
+        _dev(part_counts, "part_counts", (torch.int32,)),
+        _dev(part_offsets, "part_offsets", (torch.int32,)),
+        _dev(token_slot, "token_slot", (torch.int32,), 3), _dev(ws, "ws", (torch.uint8,)),
+        ws.numel(), _status_ptr(dev_status), _stream(stream)))
 
 
 def moe_permute_to_experts(send, token_slot, topk_ids, expert_counts, expert_rank, E, recv_part,
@@ -357,26 +425,35 @@ class MoePath:
 
     def __init__(self, S, T, H, E, k, P, recv_part=-1, align=1, cap_send=None, cap_recv=None,
                  device="cuda", layout="contiguous", block_rows=None, combine="single",
-                 quant="none"):
+                 quant="none", placement: "Placement | None" = None):
         """layout: "contiguous" (expert runs, moe_permute_to_experts) or "masked" (one
         block of block_rows rows per expert, moe_permute_to_experts_masked).
         combine: "single" (moe_combine) or "two_stage" (moe_combine_stage1 + stage2).
         quant: "none" (bf16 rows) or "mxfp8" (rows sent as MXFP8 records; the
-        receiver's stand-in expert dequantizes them, so every step runs it)."""
+        receiver's stand-in expert dequantizes them, so every step runs it).
+        placement: a Placement (moe_plan_placement) -- the layout then maps each
+        pair to a physical expert slot and everything after it works on the
+        P*Lp physical experts; None keeps expert e in slot e."""
         if layout not in ("contiguous", "masked") or combine not in ("single", "two_stage"):
             raise ValueError("layout must be contiguous|masked, combine single|two_stage")
         if quant not in ("none", "mxfp8"):
             raise ValueError("quant must be none|mxfp8")
         if quant == "mxfp8" and (H % 512 != 0 or layout != "contiguous"):
             raise ValueError("mxfp8 rows need H % 512 == 0 and the contiguous layout")
+        if placement is not None and (placement.E != E or placement.P != P):
+            raise ValueError("the placement is for another E or P")
         self.S, self.T, self.H, self.E, self.k, self.P = S, T, H, E, k, P
+        self.placement = placement
+        # experts as the layout's outputs and every later call see them
+        self.Ep = placement.E_phys if placement is not None else E
         self.recv_part, self.align = recv_part, align
         self.layout, self.combine_mode, self.quant = layout, combine, quant
         # row width as the permute sees it: bf16 slots per row
         self.row_bytes = mxfp8_record_bytes(H) if quant == "mxfp8" else 2 * H
         self.Hp = self.row_bytes // 2
         self.cap_send = T * min(k, P) if cap_send is None else cap_send
-        self.n_blocks = E if recv_part < 0 else E // P
+        Ep = self.Ep
+        self.n_blocks = Ep if recv_part < 0 else Ep // P
         if layout == "masked":
             if block_rows is None:
                 raise ValueError("the masked layout needs block_rows")
@@ -384,12 +461,16 @@ class MoePath:
             self.cap_recv = self.n_blocks * block_rows
         else:
             self.block_rows = None
-            self.cap_recv = S * T * k + E * (align - 1) if cap_recv is None else cap_recv
+            self.cap_recv = S * T * k + Ep * (align - 1) if cap_recv is None else cap_recv
         d = torch.device(device)
         i32 = dict(dtype=torch.int32, device=d)
         self.topk_ids = torch.empty((S, T, k), **i32)
         self.topk_w = torch.empty((S, T, k), dtype=torch.float32, device=d)
-        self.expert_counts = torch.empty((S, E), **i32)
+        self.expert_counts = torch.empty((S, Ep), **i32)
+        # ids of the pairs after the layout: physical slots under a placement
+        self.phys_ids = torch.empty((S, T, k), **i32) if placement is not None else self.topk_ids
+        if placement is not None:
+            self.copy_offsets, self.copy_slots, self.slot_expert = placement.to(d)
         self.expert_rank = torch.empty((S, T, k), **i32)
         self.part_counts = torch.empty((S, P), **i32)
         self.part_offsets = torch.empty((S, P + 1), **i32)
@@ -399,11 +480,13 @@ class MoePath:
         self.send = torch.empty((S, self.cap_send, row_w), dtype=row_dt, device=d)
         self.send_src = torch.empty((S, self.cap_send), **i32)
         self.recv = torch.empty((self.cap_recv, row_w), dtype=row_dt, device=d)
-        self.expert_offsets = torch.empty((E + 1,), **i32)
+        self.expert_offsets = torch.empty((Ep + 1,), **i32)
         self.pair_row = torch.empty((S, T, k), **i32)
         self.recv_pair = torch.empty((self.cap_recv,), **i32)
         self.out = torch.empty((S, T, H), dtype=torch.bfloat16, device=d)
-        ws = moe_workspace_bytes(S, T, k, E, P)
+        ws = moe_workspace_bytes(S, T, k, Ep, P)
+        if placement is not None:
+            ws = max(ws, moe_workspace_bytes_mapped(S, T, k, E, P, placement.Lp))
         self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=d)
         self.dev_status = torch.zeros((1,), **i32)
         self.masked_counts = torch.empty((self.n_blocks,), **i32) if layout == "masked" else None
@@ -412,7 +495,7 @@ class MoePath:
         self.y = None
         if quant == "mxfp8":
             self.y = torch.empty((self.cap_recv, H), dtype=torch.bfloat16, device=d)
-            self.unit_scale = torch.ones((E,), dtype=torch.float32, device=d)
+            self.unit_scale = torch.ones((Ep,), dtype=torch.float32, device=d)
 
     def bind(self, logits, x, stream=None, scale=None):
         """Pre-marshal the calls of one step for fixed input tensors and stream.
@@ -430,18 +513,23 @@ class MoePath:
         if tuple(logits.shape) != (S, T, E) or tuple(x.shape) != (S, T, H):
             raise ValueError("bind: logits / x shapes do not match the path")
         stp = vp(self.dev_status.data_ptr())
-        Hp = self.Hp
+        Hp, Ep = self.Hp, self.Ep
+        ids_p = vp(self.phys_ids.data_ptr())
         calls = [
             (lib.moe_route_topk, (ptr(logits, "logits", (torch.float32,)), S, T, E, k,
                                   vp(self.topk_ids.data_ptr()), vp(self.topk_w.data_ptr()), st)),
-            (lib.moe_dispatch_layout, (vp(self.topk_ids.data_ptr()), S, T, k, E, P,
-                                       vp(self.expert_counts.data_ptr()),
-                                       vp(self.expert_rank.data_ptr()),
-                                       vp(self.part_counts.data_ptr()),
-                                       vp(self.part_offsets.data_ptr()),
-                                       vp(self.token_slot.data_ptr()), vp(self.ws.data_ptr()),
-                                       self.ws.numel(), stp, st)),
         ]
+        outs = (vp(self.expert_counts.data_ptr()), vp(self.expert_rank.data_ptr()),
+                vp(self.part_counts.data_ptr()), vp(self.part_offsets.data_ptr()),
+                vp(self.token_slot.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st)
+        if self.placement is not None:
+            calls.append((lib.moe_dispatch_layout_mapped, (
+                vp(self.topk_ids.data_ptr()), S, T, k, E, P, self.placement.Lp,
+                vp(self.copy_offsets.data_ptr()), vp(self.copy_slots.data_ptr()),
+                self.copy_slots.numel(), ids_p) + outs))
+        else:
+            calls.append((lib.moe_dispatch_layout, (vp(self.topk_ids.data_ptr()), S, T, k, E, P)
+                          + outs))
         if self.quant == "mxfp8":
             calls.append((lib.moe_dispatch_pack_mxfp8, (
                 ptr(x, "x", _BF16_TYPES), S, T, H, P, vp(self.token_slot.data_ptr()),
@@ -455,32 +543,33 @@ class MoePath:
         if self.layout == "masked":
             calls.append((lib.moe_permute_to_experts_masked, (
                 vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
-                vp(self.topk_ids.data_ptr()), vp(self.expert_counts.data_ptr()),
-                vp(self.expert_rank.data_ptr()), S, T, k, E, P, H, self.recv_part,
+                ids_p, vp(self.expert_counts.data_ptr()),
+                vp(self.expert_rank.data_ptr()), S, T, k, Ep, P, H, self.recv_part,
                 self.block_rows, self.cap_send, vp(self.recv.data_ptr()),
                 vp(self.masked_counts.data_ptr()), vp(self.pair_row.data_ptr()),
                 vp(self.recv_pair.data_ptr()), stp, st)))
         else:
             calls.append((lib.moe_permute_to_experts, (
                 vp(self.send.data_ptr()), vp(self.token_slot.data_ptr()),
-                vp(self.topk_ids.data_ptr()), vp(self.expert_counts.data_ptr()),
-                vp(self.expert_rank.data_ptr()), S, T, k, E, P, Hp, self.recv_part, self.align,
+                ids_p, vp(self.expert_counts.data_ptr()),
+                vp(self.expert_rank.data_ptr()), S, T, k, Ep, P, Hp, self.recv_part, self.align,
                 self.cap_send, self.cap_recv, vp(self.recv.data_ptr()),
                 vp(self.expert_offsets.data_ptr()), vp(self.pair_row.data_ptr()),
                 vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st)))
         y = self.recv
         if self.quant == "mxfp8":
-            sc = self.unit_scale if scale is None else scale
+            # the bound call keeps a pointer: hold the per-slot scales on the path
+            self._bound_scale = self.unit_scale if scale is None else self.slot_scale(scale)
             calls.append((lib.moe_expert_scale_mxfp8, (
                 vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()),
-                ptr(sc, "scale", (torch.float32,)), E, H, self.cap_recv, vp(self.y.data_ptr()),
-                st)))
+                ptr(self._bound_scale, "scale", (torch.float32,)), Ep, H, self.cap_recv,
+                vp(self.y.data_ptr()), st)))
             y = self.y
         if self.combine_mode == "two_stage":
             calls.append((lib.moe_combine_stage1, (
                 vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
-                vp(self.topk_w.data_ptr()), vp(self.topk_ids.data_ptr()),
-                vp(self.token_slot.data_ptr()), S, T, k, E, P, H, self.recv_part, self.cap_send,
+                vp(self.topk_w.data_ptr()), ids_p,
+                vp(self.token_slot.data_ptr()), S, T, k, Ep, P, H, self.recv_part, self.cap_send,
                 vp(self.ret.data_ptr()), stp, st)))
             calls.append((lib.moe_combine_stage2, (
                 vp(self.ret.data_ptr()), vp(self.token_slot.data_ptr()), S, T, P, H,
@@ -504,14 +593,21 @@ class MoePath:
 
     def dispatch(self, x, stream=None):
         """layout + pack + permute (the receiver's copy epilogue is part of dispatch)."""
-        moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts, self.expert_rank,
-                            self.part_counts, self.part_offsets, self.token_slot, self.ws,
-                            self.dev_status, stream)
+        if self.placement is not None:
+            moe_dispatch_layout_mapped(self.topk_ids, self.E, self.P, self.placement.Lp,
+                                       self.copy_offsets, self.copy_slots, self.phys_ids,
+                                       self.expert_counts, self.expert_rank, self.part_counts,
+                                       self.part_offsets, self.token_slot, self.ws,
+                                       self.dev_status, stream)
+        else:
+            moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts,
+                                self.expert_rank, self.part_counts, self.part_offsets,
+                                self.token_slot, self.ws, self.dev_status, stream)
         if self.quant == "mxfp8":
             moe_dispatch_pack_mxfp8(x, self.token_slot, self.part_offsets, self.send,
                                     self.send_src, self.dev_status, stream)
-            moe_permute_to_experts(self.send.view(torch.bfloat16), self.token_slot, self.topk_ids,
-                                   self.expert_counts, self.expert_rank, self.E, self.recv_part,
+            moe_permute_to_experts(self.send.view(torch.bfloat16), self.token_slot, self.phys_ids,
+                                   self.expert_counts, self.expert_rank, self.Ep, self.recv_part,
                                    self.align, self.recv.view(torch.bfloat16),
                                    self.expert_offsets, self.pair_row, self.recv_pair, self.ws,
                                    self.dev_status, stream)
@@ -519,35 +615,43 @@ class MoePath:
         moe_dispatch_pack(x, self.token_slot, self.part_offsets, self.send, self.send_src,
                           self.dev_status, stream)
         if self.layout == "masked":
-            moe_permute_to_experts_masked(self.send, self.token_slot, self.topk_ids,
-                                          self.expert_counts, self.expert_rank, self.E,
+            moe_permute_to_experts_masked(self.send, self.token_slot, self.phys_ids,
+                                          self.expert_counts, self.expert_rank, self.Ep,
                                           self.recv_part, self.block_rows, self.recv,
                                           self.masked_counts, self.pair_row, self.recv_pair,
                                           self.dev_status, stream)
         else:
-            moe_permute_to_experts(self.send, self.token_slot, self.topk_ids, self.expert_counts,
-                                   self.expert_rank, self.E, self.recv_part, self.align, self.recv,
+            moe_permute_to_experts(self.send, self.token_slot, self.phys_ids, self.expert_counts,
+                                   self.expert_rank, self.Ep, self.recv_part, self.align, self.recv,
                                    self.expert_offsets, self.pair_row, self.recv_pair, self.ws,
                                    self.dev_status, stream)
+
+    def slot_scale(self, scale):
+        """Stand-in expert scales per logical expert -> per expert slot (a copy
+        computes what its original computes; empty slots get 0)."""
+        if self.placement is None:
+            return scale
+        se = self.slot_expert
+        return torch.where(se >= 0, scale[se.clamp(min=0).long()], torch.zeros_like(scale[:1]))
 
     def expert(self, scale, stream=None):
         if self.layout != "contiguous":
             raise ValueError("the stand-in expert reads contiguous expert runs")
         if self.quant == "mxfp8":
-            sc = self.unit_scale if scale is None else scale
+            sc = self.unit_scale if scale is None else self.slot_scale(scale)
             moe_expert_scale_mxfp8(self.recv, self.expert_offsets, sc, self.y, stream)
             return self.y
         if self.y is None:
             self.y = torch.empty_like(self.recv)
-        moe_expert_scale(self.recv, self.expert_offsets, scale, self.y, stream)
+        moe_expert_scale(self.recv, self.expert_offsets, self.slot_scale(scale), self.y, stream)
         return self.y
 
     def combine(self, y=None, stream=None):
         if y is None:
             y = self.y if self.quant == "mxfp8" else self.recv
         if self.combine_mode == "two_stage":
-            moe_combine_stage1(y, self.pair_row, self.topk_w, self.topk_ids, self.token_slot,
-                               self.E, self.recv_part, self.ret, self.dev_status, stream)
+            moe_combine_stage1(y, self.pair_row, self.topk_w, self.phys_ids, self.token_slot,
+                               self.Ep, self.recv_part, self.ret, self.dev_status, stream)
             moe_combine_stage2(self.ret, self.token_slot, self.out, self.dev_status, stream)
         else:
             moe_combine(y, self.pair_row, self.topk_w, self.out, self.dev_status, stream)
@@ -561,12 +665,15 @@ class MoePath:
         return self.out
 
     def launches_per_step(self, with_expert=False) -> int:
-        """Kernels one step enqueues: route 1, layout 2 (1 if T <= 256), pack 1, permute 2
-        (map + copy), stand-in expert 1 (always with MXFP8 rows), combine 1 (2 when split
-        into two stages)."""
+        """Kernels one step enqueues: route 1, layout 2 (1 if T <= 256; twice that plus the
+        replica map under a placement), pack 1, permute 2 (map + copy), stand-in expert 1
+        (always with MXFP8 rows), combine 1 (2 when split into two stages)."""
         with_expert = with_expert or self.quant == "mxfp8"
+        mapped = self.placement is not None
         if self.T == 0:
-            return 1 + 1 + 2 + (1 if with_expert else 0)
+            return 1 + (2 if mapped else 1) + 2 + (1 if with_expert else 0)
         layout = 1 if self.T <= 256 else 2
+        if mapped:
+            layout = 2 * layout + 1
         comb = 2 if self.combine_mode == "two_stage" else 1
         return 1 + layout + 1 + 2 + comb + (1 if with_expert else 0)

@@ -417,4 +417,65 @@ moe_status_t moe_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert
         __func__);
 }
 
+moe_status_t moe_plan_placement(const int64_t *load, int E, int P, int R, int32_t *copy_offsets,
+                                int32_t *copy_slots, int32_t *slot_expert, int64_t *part_load)
+{
+    REQUIRE(E >= 1 && E <= kMaxE, "%s: E=%d must be in [1, %d]", __func__, E, kMaxE);
+    REQUIRE(P >= 1 && P <= kMaxP, "%s: P=%d must be in [1, %d]", __func__, P, kMaxP);
+    REQUIRE(E % P == 0, "%s: E=%d must be a multiple of P=%d", __func__, E, P);
+    REQUIRE(R >= 0 && (int64_t)P * (E / P + R) <= kMaxE,
+            "%s: R=%d: P*(E/P+R) slots must be at most %d", __func__, R, kMaxE);
+    REQUIRE(load && copy_offsets && copy_slots && slot_expert && part_load,
+            "%s: null pointer", __func__);
+    for (int e = 0; e < E; e++)
+        REQUIRE(load[e] >= 0, "%s: load[%d] < 0", __func__, e);
+    plan_placement(load, E, P, R, copy_offsets, copy_slots, slot_expert, part_load);
+    return MOE_OK;
+}
+
+size_t moe_workspace_bytes_mapped(int S, int T, int k, int E, int P, int Lp)
+{
+    if (check_sizes("moe_workspace_bytes_mapped", S, T, k, E, P) != MOE_OK) return 0;
+    if (Lp < E / P || (int64_t)P * Lp > kMaxE) return 0;
+    return mapped_ws_bytes(S, T, k, E, P, P * Lp);
+}
+
+moe_status_t moe_dispatch_layout_mapped(const int32_t *topk_ids, int S, int T, int k, int E,
+                                        int P, int Lp, const int32_t *copy_offsets,
+                                        const int32_t *copy_slots, int n_copies,
+                                        int32_t *phys_ids, int32_t *expert_counts,
+                                        int32_t *expert_rank, int32_t *part_counts,
+                                        int32_t *part_offsets, int32_t *token_slot, void *ws,
+                                        size_t ws_bytes, uint32_t *dev_status,
+                                        cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(Lp >= E / P && (int64_t)P * Lp <= kMaxE,
+            "%s: Lp=%d must be in [E/P, %d/P]", __func__, Lp, kMaxE);
+    REQUIRE(n_copies >= E && n_copies <= P * Lp, "%s: n_copies=%d must be in [E, P*Lp]",
+            __func__, n_copies);
+    const int E_phys = P * Lp;
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(copy_offsets, E + 1, 4);
+    REQUIRE_ARR(copy_slots, n_copies, 4);
+    REQUIRE_ARR(phys_ids, NT * k, 4);
+    REQUIRE_ARR(expert_counts, (int64_t)S * E_phys, 4);
+    REQUIRE_ARR(expert_rank, NT * k, 4);
+    REQUIRE_ARR(part_counts, (int64_t)S * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_STATUS(dev_status);
+    const size_t need = mapped_ws_bytes(S, T, k, E, P, E_phys);
+    REQUIRE_ARR(ws, need, 256);
+    REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
+    return cuda_status(launch_dispatch_layout_mapped(topk_ids, S, T, k, E, P, E_phys,
+                                                     copy_offsets, copy_slots, n_copies, phys_ids,
+                                                     expert_counts, expert_rank, part_counts,
+                                                     part_offsets, token_slot, ws, dev_status,
+                                                     stream),
+                       __func__);
+}
+
 }  // extern "C"

@@ -48,6 +48,19 @@ cudaError_t launch_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expe
                                       const float *scale, int E, int H, int cap_recv, uint16_t *y,
                                       cudaStream_t st);
 
+// Expert placement by load with redundant copies (host) and the layout over a
+// placement (device).  plan_placement returns the number of slots used.
+int plan_placement(const int64_t *load, int E, int P, int R, int32_t *copy_offsets,
+                   int32_t *copy_slots, int32_t *slot_expert, int64_t *part_load);
+size_t mapped_ws_bytes(int S, int T, int k, int E, int P, int E_phys);
+cudaError_t launch_dispatch_layout_mapped(const int32_t *ids, int S, int T, int k, int E, int P,
+                                          int E_phys, const int32_t *copy_offsets,
+                                          const int32_t *copy_slots, int n_copies,
+                                          int32_t *phys, int32_t *expert_counts,
+                                          int32_t *expert_rank, int32_t *part_counts,
+                                          int32_t *part_offsets, int32_t *token_slot, void *ws,
+                                          uint32_t *dev_status, cudaStream_t st);
+
 size_t permute_ws_bytes(int S, int T, int E);
 cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, const int32_t *ids,
                            const int32_t *expert_counts, const int32_t *expert_rank,

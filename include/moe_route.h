@@ -183,6 +183,63 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                                uint32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Expert placement by load with redundant copies of the hot experts ("Beyond
+ * One GPU", section 6, "The fix: place experts by load, and copy the hot
+ * ones").  HOST function: all pointers are host memory; no GPU is used.
+ *  1. Heaviest expert first (equal loads: lower id first), each onto the
+ *     least-loaded partition (equal loads: lower index) that still has one of
+ *     its E/P regular slots free.
+ *  2. Every partition also has R spare slots.  Repeatedly: take the busiest
+ *     partition (ties: lower index) and its expert with the largest share
+ *     (ties: lower id); copy it to the least-loaded partition that has a
+ *     spare slot free and no copy of it yet.  The copy is kept only if that
+ *     partition's new load stays below the busiest partition's load; the
+ *     first copy that fails this, or the lack of a free spare slot, ends it.
+ * Loads are integer pair counts split over an expert's n copies as the
+ * mapped layout splits them: copy c carries ceil((load - c) / n).
+ *   load          [E] int64 in: pairs per logical expert in a past batch.
+ *   copy_offsets  [E+1] int32 out; copy_slots [E + P*R] int32 out: the slots
+ *                 of expert e are copy_slots[copy_offsets[e] .. copy_offsets[e+1]),
+ *                 the original first, then its copies in the order made.
+ *   slot_expert   [P*(E/P+R)] int32 out: logical expert in each physical slot,
+ *                 -1 if empty.  Partition p owns slots [p*Lp, (p+1)*Lp),
+ *                 Lp = E/P + R, filled in the order experts arrive there.
+ *   part_load     [P] int64 out: pairs per partition after the copies.
+ * Errors: MOE_ERR_INVALID_ARG (E % P != 0, P*Lp > 1024, a negative load, null).
+ */
+moe_status_t moe_plan_placement(const int64_t *load, int E, int P, int R, int32_t *copy_offsets,
+                                int32_t *copy_slots, int32_t *slot_expert, int64_t *part_load);
+
+/*
+ * Dispatch layout over a placement (same section: a replicated expert's
+ * tokens are split evenly between its copies).  For each source, the r-th
+ * pair of logical expert e in (token, choice) order goes to physical slot
+ *   phys_ids[s][t][j] = copy_slots[copy_offsets[e] + (r mod n_e)],
+ * n_e = copy_offsets[e+1] - copy_offsets[e]; ids < 0 give -1, ids >= E give
+ * P*Lp (flagged MOE_ERR_BAD_EXPERT_ID).  The outputs are then exactly those
+ * of moe_dispatch_layout over phys_ids with P*Lp experts (partition of a
+ * slot = slot / Lp), so moe_permute_to_experts and the combine run unchanged
+ * with E = P*Lp and topk_ids = phys_ids.
+ *   copy_offsets [E+1], copy_slots [n_copies] int32 device arrays (from
+ *   moe_plan_placement or the caller); a copy list that leaves
+ *   [0, n_copies) or a slot outside [0, P*Lp) flags MOE_ERR_INVALID_ARG and
+ *   the pair becomes -1.
+ *   expert_counts [S][P*Lp]; the other outputs as moe_dispatch_layout.
+ *   ws: moe_workspace_bytes_mapped(S, T, k, E, P, Lp) bytes, 256-byte aligned.
+ * Five kernels: the layout over logical ids (for the ranks r), the map, the
+ * layout over physical ids.
+ */
+size_t moe_workspace_bytes_mapped(int S, int T, int k, int E, int P, int Lp);
+moe_status_t moe_dispatch_layout_mapped(const int32_t *topk_ids, int S, int T, int k, int E,
+                                        int P, int Lp, const int32_t *copy_offsets,
+                                        const int32_t *copy_slots, int n_copies,
+                                        int32_t *phys_ids, int32_t *expert_counts,
+                                        int32_t *expert_rank, int32_t *part_counts,
+                                        int32_t *part_offsets, int32_t *token_slot, void *ws,
+                                        size_t ws_bytes, uint32_t *dev_status,
+                                        cudaStream_t stream);
+
+/*
  * Pack with the rows quantized on the way (a2a-backends section 7.2: expert
  * kernels that quantize their input anyway can take rows already quantized,
  * so a token is converted before it is sent; a DeepSeek-V4.1-Flash FP8 row is

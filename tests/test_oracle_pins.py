@@ -818,3 +818,26 @@ def test_placement_rejects_a_copy_that_ties_the_busiest():
     # with 7 the copy brings p1 to 3 + 3 = 6 < 7 and is kept; p0 keeps the larger share
     plan = oracle.plan_placement(np.array([7, 3], np.int64), 2, 1)
     assert plan["copy_offsets"].tolist() == [0, 2, 3] and plan["part_load"].tolist() == [4, 6]
+
+
+def test_placed_path_output_equals_unplaced():
+    # copies of an expert compute what the expert computes, so moving pairs between
+    # copies (and experts between partitions) leaves the combined output unchanged
+    w_ = ms.workload("tiny", E=32, P=32, k=4, zipf_s=1.2, T=600)
+    inp = ms.gen_inputs(w_)
+    ids, wts = oracle.route_topk(inp["logits"], w_.k)
+    plan = oracle.plan_placement(np.bincount(ids.ravel(), minlength=w_.E).astype(np.int64), w_.P, 2)
+    assert plan["copy_offsets"][-1] > w_.E
+    phys = oracle.map_replicas(ids, w_.E, plan["copy_offsets"], plan["copy_slots"], plan["E_phys"])
+    lay = oracle.dispatch_layout(phys, plan["E_phys"], w_.P)
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], w_.T * min(w_.k, w_.P))
+    per = oracle.permute_to_experts(send, lay["token_slot"], phys, plan["E_phys"])
+    se = plan["slot_expert"]
+    y = oracle.expert_scale(per["recv"], per["expert_offsets"],
+                            np.where(se >= 0, inp["scales"][np.maximum(se, 0)], 0).astype(np.float32))
+    ref = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, inp["scales"])
+    assert np.array_equal(oracle.combine(y, per["pair_row"], wts), ref["out"])
+    # and the busiest partition carries less than under contiguous blocks
+    cont = np.bincount(ids.ravel(), minlength=w_.E).reshape(w_.P, -1).sum(axis=1)
+    placed = lay["expert_counts"][0].reshape(w_.P, -1).sum(axis=1)
+    assert placed.max() < cont.max()
