@@ -77,13 +77,18 @@ def _load():
             lib.oracle_expert_scale_mxfp8.argtypes = [P, P, P, i32, i32, i64, P]
             lib.oracle_plan_placement.argtypes = [P, i32, i32, i32, P, P, P, P]
             lib.oracle_map_replicas.argtypes = [P, i32, i64, i32, i32, P, P, i32, P]
+            lib.oracle_dispatch_pack_routed.argtypes = [P, P, P, i32, i64, i32, i32, i32, P, i64,
+                                                        P, P, P, P, P]
+            lib.oracle_routed_expert_stage1.argtypes = [P, P, P, P, i32, i64, i32, i32, i32, i32,
+                                                        i32, P, P, P]
             lib.oracle_combine.argtypes = [P, P, P, i32, i64, i32, i32, P]
             for f in ("oracle_route_topk", "oracle_dispatch_layout", "oracle_dispatch_pack",
                       "oracle_permute_to_experts", "oracle_expert_scale", "oracle_combine",
                       "oracle_permute_masked", "oracle_combine_stage1",
                       "oracle_combine_stage2", "oracle_dispatch_pack_mxfp8",
                       "oracle_expert_scale_mxfp8", "oracle_plan_placement",
-                      "oracle_map_replicas"):
+                      "oracle_map_replicas", "oracle_dispatch_pack_routed",
+                      "oracle_routed_expert_stage1"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -380,6 +385,53 @@ def map_replicas(ids: np.ndarray, E: int, copy_offsets: np.ndarray, copy_slots: 
                                        _p(np.ascontiguousarray(copy_slots, np.int32)), E_phys,
                                        _p(phys)), "map_replicas")
     return phys
+
+
+def dispatch_pack_routed(x: np.ndarray, ids: np.ndarray, w: np.ndarray, token_slot: np.ndarray,
+                         cap_send: int, send: np.ndarray | None = None):
+    """Pack with the routing payload -> (send, send_src, send_ids [S,cap,k], send_w [S,cap,k], status)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    S, T, H = x.shape
+    k = ids.shape[2]
+    P = token_slot.shape[2]
+    if send is None:
+        send = np.zeros((S, cap_send, H), np.uint16)
+    send_src = np.empty((S, cap_send), np.int32)
+    send_ids = np.empty((S, cap_send, k), np.int32)
+    send_w = np.empty((S, cap_send, k), np.float32)
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_dispatch_pack_routed(_p(x), _p(ids), _p(w), S, T, H, k, P, _p(token_slot),
+                                               cap_send, _p(send), _p(send_src), _p(send_ids),
+                                               _p(send_w), _p(st)), "dispatch_pack_routed")
+    return send, send_src, send_ids, send_w, int(st[0])
+
+
+def routed_expert_stage1(send: np.ndarray, send_ids: np.ndarray, send_w: np.ndarray,
+                         part_offsets: np.ndarray, E: int, recv_part: int = -1,
+                         scale: np.ndarray | None = None, ret: np.ndarray | None = None):
+    """Routed stand-in expert + stage-1 pre-add per row -> (ret [S, cap, H], status).
+
+    Rows outside the receiving partitions' regions keep the `ret` passed in (zeros if none).
+    """
+    send = np.ascontiguousarray(send, dtype=np.uint16)
+    send_ids = np.ascontiguousarray(send_ids, dtype=np.int32)
+    send_w = np.ascontiguousarray(send_w, dtype=np.float32)
+    part_offsets = np.ascontiguousarray(part_offsets, dtype=np.int32)
+    S, cap, H = send.shape
+    k = send_ids.shape[2]
+    P = part_offsets.shape[1] - 1
+    if ret is None:
+        ret = np.zeros_like(send)
+    sc = None if scale is None else np.ascontiguousarray(scale, dtype=np.float32)
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_routed_expert_stage1(_p(send), _p(send_ids), _p(send_w), _p(part_offsets),
+                                               S, cap, k, E, P, H, recv_part,
+                                               None if sc is None else _p(sc), _p(ret), _p(st)),
+           "routed_expert_stage1")
+    return ret, int(st[0])
 
 
 def run_path(x: np.ndarray, logits: np.ndarray, E: int, k: int, P: int, scales: np.ndarray | None,

@@ -937,3 +937,88 @@ int oracle_map_replicas(const int32_t *ids, int S, int64_t T, int k, int E,
     free(seen);
     return 0;
 }
+
+/* --------------------------------------- routed payload, [a2a] 6.1, 7.1 -- */
+
+/*
+ * [a2a] 6.1: next to the hidden state the sender writes the token's expert
+ * ids and weights (payloads = hidden state, top-k ids, top-k weights), so the
+ * receiver need not group anything.  Rows go where oracle_dispatch_pack puts
+ * them; every written row also gets the token's k ids and weights:
+ *   send_ids[s][slot][j] = ids[s][t][j],  send_w[s][slot][j] = w[s][t][j]
+ * Rows no slot names are empty and carry the invalid id -1 and weight 0
+ * ([a2a] 6.3: empty slots are marked with an invalid expert id).
+ */
+int oracle_dispatch_pack_routed(const uint16_t *x, const int32_t *ids, const float *w, int S,
+                                int64_t T, int H, int k, int P, const int32_t *token_slot,
+                                int64_t cap_send, uint16_t *send, int32_t *send_src,
+                                int32_t *send_ids, float *send_w, uint32_t *status)
+{
+    int rc = oracle_dispatch_pack(x, S, T, H, P, token_slot, cap_send, send, send_src, status);
+    if (rc != 0)
+        return rc;
+    for (int s = 0; s < S; s++)
+        for (int64_t r = 0; r < cap_send; r++) {
+            const int64_t row = (int64_t)s * cap_send + r;
+            const int32_t t = send_src[row];
+            for (int j = 0; j < k; j++) {
+                send_ids[row * k + j] = t < 0 ? -1 : ids[((int64_t)s * T + t) * k + j];
+                send_w[row * k + j] = t < 0 ? 0.0f : w[((int64_t)s * T + t) * k + j];
+            }
+        }
+    return 0;
+}
+
+/*
+ * [a2a] 6.1 / 7.1: the routed expert kernel takes the rows in arrival order,
+ * reads each row's ids, runs the experts of its own GPU and already produces
+ * the weighted sum over them -- stage 1 of the combine -- in that GPU's
+ * workspace.  With the stand-in expert (y = bf16(x * scale[e]); identity
+ * when scale is NULL), for every row r of partition p's region of source s,
+ * r in [part_offsets[s][p], part_offsets[s][p+1]), p in the receiving set:
+ *   ret[s][r] = bf16( sum over ascending j with send_ids[s][r][j] in p
+ *                     of send_w[s][r][j] * y_j ),   y_j = bf16(send[s][r] * scale[e_j])
+ * summed in double.  Other rows of ret are not written; ids >= E are skipped
+ * and flagged.
+ */
+int oracle_routed_expert_stage1(const uint16_t *send, const int32_t *send_ids, const float *send_w,
+                                const int32_t *part_offsets, int S, int64_t cap_send, int k,
+                                int E, int P, int H, int recv_part, const float *scale,
+                                uint16_t *ret, uint32_t *status)
+{
+    if (P < 1 || E % P != 0 || recv_part < -1 || recv_part >= P)
+        return -1;
+    const int L = E / P;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    if (!acc)
+        return -2;
+    for (int s = 0; s < S; s++)
+        for (int p = 0; p < P; p++) {
+            if (recv_part >= 0 && p != recv_part)
+                continue;
+            const int32_t *po = part_offsets + (int64_t)s * (P + 1);
+            for (int64_t r = po[p]; r < po[p + 1] && r < cap_send; r++) {
+                const int64_t row = (int64_t)s * cap_send + r;
+                for (int h = 0; h < H; h++)
+                    acc[h] = 0.0;
+                for (int j = 0; j < k; j++) {
+                    const int32_t e = send_ids[row * k + j];
+                    if (e >= E)
+                        *status |= ORC_BIT_BAD_ID;
+                    if (e < 0 || e >= E || e / L != p)
+                        continue;
+                    const double wj = (double)send_w[row * k + j];
+                    for (int h = 0; h < H; h++) {
+                        double v = oracle_bf16_to_double(send[row * H + h]);
+                        if (scale)
+                            v = oracle_bf16_to_double(oracle_bf16_from_double(v * (double)scale[e]));
+                        acc[h] += wj * v;
+                    }
+                }
+                for (int h = 0; h < H; h++)
+                    ret[row * H + h] = oracle_bf16_from_double(acc[h]);
+            }
+        }
+    free(acc);
+    return 0;
+}

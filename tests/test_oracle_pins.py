@@ -841,3 +841,70 @@ def test_placed_path_output_equals_unplaced():
     cont = np.bincount(ids.ravel(), minlength=w_.E).reshape(w_.P, -1).sum(axis=1)
     placed = lay["expert_counts"][0].reshape(w_.P, -1).sum(axis=1)
     assert placed.max() < cont.max()
+
+
+# ------------------------------------------- routed payload (a2a 6.1, 7.1) --
+
+def _routed_case(name, **over):
+    w_ = ms.workload(name, **over)
+    inp = ms.gen_inputs(w_)
+    ids, wts = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap = w_.T * min(w_.k, w_.P) + 3                       # three rows no slot names
+    return w_, inp, ids, wts, lay, cap
+
+
+def test_routed_pack_carries_the_tokens_routing():
+    w_, inp, ids, wts, lay, cap = _routed_case("tiny", S=2, T=90)
+    send, src, sid, sw, st = oracle.dispatch_pack_routed(inp["x"], ids, wts, lay["token_slot"], cap)
+    ref_send, ref_src, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap)
+    assert st == 0 and np.array_equal(send, ref_send) and np.array_equal(src, ref_src)
+    for s in range(w_.S):
+        used = src[s] >= 0
+        assert np.array_equal(sid[s][used], ids[s][src[s][used]])
+        assert np.array_equal(sw[s][used], wts[s][src[s][used]].astype(np.float32))
+        assert np.all(sid[s][~used] == -1) and np.all(sw[s][~used] == 0)
+        assert (~used).sum() >= 3
+
+
+@pytest.mark.parametrize("name,over,recv_part", [("tiny", {}, -1), ("tiny", {"S": 3, "T": 70}, 1),
+                                                 ("decode", {}, -1), ("decode", {}, 6)])
+def test_routed_stage1_equals_permuted_stage1(name, over, recv_part):
+    # two formulations of the per-partition pre-add: over rows in arrival order with
+    # their ids (routed), and over the expert-sorted pair rows (permute + stand-in expert)
+    w_, inp, ids, wts, lay, cap = _routed_case(name, **over)
+    send, _, sid, sw, _ = oracle.dispatch_pack_routed(inp["x"], ids, wts, lay["token_slot"], cap)
+    fill = np.full_like(send, 0x1357)
+    got, st = oracle.routed_expert_stage1(send, sid, sw, lay["part_offsets"], w_.E, recv_part,
+                                          inp["scales"], ret=fill.copy())
+    per = oracle.permute_to_experts(send, lay["token_slot"], ids, w_.E, recv_part=recv_part)
+    y = oracle.expert_scale(per["recv"], per["expert_offsets"], inp["scales"])
+    want, st2 = oracle.combine_stage1(y, per["pair_row"], wts, ids, lay["token_slot"], w_.E, cap,
+                                      recv_part=recv_part, ret=fill.copy())
+    assert st == st2 == 0
+    assert np.array_equal(got, want)
+
+
+def test_routed_round_trip_is_the_combine():
+    w_, inp, ids, wts, lay, cap = _routed_case("decode")
+    send, _, sid, sw, _ = oracle.dispatch_pack_routed(inp["x"], ids, wts, lay["token_slot"], cap)
+    ret, _ = oracle.routed_expert_stage1(send, sid, sw, lay["part_offsets"], w_.E)
+    out, st = oracle.combine_stage2(ret, lay["token_slot"])
+    assert st == 0
+    # identity expert: the per-partition weights add up to 1, so out ~ x
+    x = ms.f32_from_bf16_bits(inp["x"]).astype(np.float64)
+    got = ms.f32_from_bf16_bits(out).astype(np.float64)
+    assert np.all(np.abs(got - x) <= 2.0 ** -6 * np.maximum(np.abs(x), 1e-3))
+
+
+def test_routed_stage1_skips_empty_and_flags_bad_ids():
+    w_, inp, ids, wts, lay, cap = _routed_case("tiny", T=40)
+    send, _, sid, sw, _ = oracle.dispatch_pack_routed(inp["x"], ids, wts, lay["token_slot"], cap)
+    sid = sid.copy()
+    r0 = int(lay["part_offsets"][0, 2])                    # first row of partition 2
+    sid[0, r0, 0] = w_.E + 4
+    fill = np.full_like(send, 0x2468)
+    ret, st = oracle.routed_expert_stage1(send, sid, sw, lay["part_offsets"], w_.E, ret=fill.copy())
+    assert st == oracle.BIT_BAD_ID
+    used = int(lay["part_offsets"][0, -1])
+    assert np.all(ret[0, used:] == 0x2468)                 # empty rows are not written
