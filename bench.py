@@ -37,6 +37,11 @@ import moe_synth as ms  # noqa: E402
 METRIC = "dispatch+combine HBM GB/s and rows/s at 4096-token prefill; % of HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT = "k_perm_copy"
+# The kernel the roofline line reports for each variant (the longest one of the
+# step) and the key of its algorithmic bytes per launch in algorithmic_bytes().
+DOMINANT_BY_VARIANT = {"two_stage": ("k_combine_stage1", "stage1"),
+                       "mxfp8": ("k_expert_scale_mxfp8", "expert"),
+                       "routed": ("k_routed_stage1", "stage1")}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_perm_copy
 # launch in the prefill pipeline, from an ncu capture with the L2 left as the
 # previous kernel left it (--cache-control none).  Taken on the current kernel;
@@ -47,7 +52,7 @@ DOMINANT_TRAFFIC = {"prefill": 142.5e6 + 252.3e6}
 # ------------------------------------------------------------ byte model --
 
 def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_stage=False,
-                      mxfp8=False):
+                      mxfp8=False, routed=False):
     """Bytes each call must read + write at minimum.
 
     copies: rows packed (sum of part_offsets[s][P]); copies_recv: packed rows
@@ -57,6 +62,9 @@ def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_sta
     mxfp8: packed and permuted rows are MXFP8 records of H + H/32 bytes, and
     the stand-in expert that dequantizes them (pair records in, bf16 rows out)
     is part of the step.
+    routed: rows carry the token's ids and weights (8 bytes per choice), nothing
+    is permuted, the routed expert pre-adds straight from the received rows
+    (copies_recv rows in and out) and the home side sums them (stage 2).
     """
     NT = S * T
     R = H + H // 32 if mxfp8 else 2 * H          # bytes of one moved row
@@ -72,6 +80,12 @@ def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_sta
     if two_stage:
         b["combine"] = (pairs_recv * H * 2 + NT * k * 12 + copies_recv * H * 2      # stage 1
                         + copies_recv * H * 2 + NT * P * 4 + NT * H * 2)            # stage 2
+        b["stage1"] = pairs_recv * H * 2 + NT * k * 12 + copies_recv * H * 2
+    if routed:
+        b["pack"] += copies * k * 8
+        b["permute"] = 0
+        b["stage1"] = copies_recv * (H * 2 + k * 8) + copies_recv * H * 2
+        b["combine"] = b["stage1"] + copies_recv * H * 2 + NT * P * 4 + NT * H * 2
     b["dispatch_combine"] = b["layout"] + b["pack"] + b["permute"] + b["combine"] + b.get("expert", 0)
     b["step"] = b["route"] + b["dispatch_combine"]
     b["perm_copy"] = copies_recv * R + pairs_recv * R + NT * k * 8
@@ -281,6 +295,8 @@ def run_reference(args, world, rank):
 
 def workload_config(w, l2, variant="contiguous"):
     scope = "route+layout+pack+permute+combine"
+    if variant == "routed":
+        scope = "route+layout+pack(rows with ids and weights)+routed pre-add+home sum"
     if variant == "mxfp8":
         scope = "route+layout+pack(MXFP8 records)+permute+dequantizing stand-in expert+combine"
     return {"workload": f"{w.name}: S={w.S} T={w.T} H={w.H} bf16, E={w.E} top-{w.k}, "
@@ -298,6 +314,7 @@ VARIANTS = {
     "two_stage": {"combine": "two_stage"},
     "mxfp8": {"quant": "mxfp8"},
     "placed": {},          # placement planned from another batch; see plan_for()
+    "routed": {"layout": "routed"},
 }
 
 
@@ -413,10 +430,20 @@ def run_ours(args, world, rank, local):
         status = int(path.dev_status.item())
         copies = int(path.part_offsets[:, -1].sum().item())
         copies_recv = copies if w.recv_part < 0 else int(path.part_counts[:, w.recv_part].sum().item())
-        pairs_recv = int((path.pair_row >= 0).sum().item())
+        if args.variant == "routed":
+            # no pair rows are formed: count the pairs whose expert the receivers hold
+            ids_d = path.topk_ids
+            if w.recv_part >= 0:
+                L_ = w.E // w.P
+                pairs_recv = int(((ids_d >= w.recv_part * L_) & (ids_d < (w.recv_part + 1) * L_)).sum().item())
+            else:
+                pairs_recv = int(((ids_d >= 0) & (ids_d < w.E)).sum().item())
+        else:
+            pairs_recv = int((path.pair_row >= 0).sum().item())
         b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv,
                               two_stage=(args.variant == "two_stage"),
-                              mxfp8=(args.variant == "mxfp8"))
+                              mxfp8=(args.variant == "mxfp8"), routed=(args.variant == "routed"))
+        dom_name, dom_key = DOMINANT_BY_VARIANT.get(args.variant, (DOMINANT, "perm_copy"))
         if placement_info is not None:
             # pairs per partition on the timed batch: contiguous blocks vs the placement
             ids_h = path.topk_ids.cpu().numpy()
@@ -435,7 +462,7 @@ def run_ours(args, world, rank, local):
         K = args.steps
         graph = None
         if not args.eager:
-            m.trace_enable(DOMINANT, max_records=8)
+            m.trace_enable(dom_name, max_records=8)
             m.trace_reset()
             cap = torch.cuda.Stream(device=dev)
             calls_cap = path.bind(logits, x, cap)
@@ -456,7 +483,7 @@ def run_ours(args, world, rank, local):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         sampler = ClockSampler(physical_gpu_index(local)) if rank == 0 else None
         if graph is None:
-            m.trace_enable(DOMINANT, max_records=K + 8)
+            m.trace_enable(dom_name, max_records=K + 8)
             m.trace_reset()
         recs = []
         if dist is not None:
@@ -478,7 +505,7 @@ def run_ours(args, world, rank, local):
             if graph is not None:
                 # the graph's event nodes are re-recorded by every replay: read them now
                 e[1].synchronize()
-                recs += [ms_ for name, ms_ in m.trace_records() if name == DOMINANT]
+                recs += [ms_ for name, ms_ in m.trace_records() if name == dom_name]
         host_enqueue_us = (time.perf_counter() - t_host0) * 1e6 / K
         torch.cuda.synchronize()
         t_loop1 = time.perf_counter()
@@ -487,7 +514,7 @@ def run_ours(args, world, rank, local):
         clocks = sampler.stop(t_loop0, t_loop1) if sampler else None
         del flush2
         if graph is None:
-            recs = [ms_ for name, ms_ in m.trace_records() if name == DOMINANT]
+            recs = [ms_ for name, ms_ in m.trace_records() if name == dom_name]
 
         step_ms = [e[0].elapsed_time(e[1]) for e in ev]
         total_ms = sum(step_ms)
@@ -603,7 +630,7 @@ def run_ours(args, world, rank, local):
 
     peak, peak_src = measured_peak()
     dom_ms = statistics.fmean(recs) if recs else None
-    dom_achieved = (b["perm_copy"] / (dom_ms * 1e-3) / 1e9) if dom_ms else None
+    dom_achieved = (b[dom_key] / (dom_ms * 1e-3) / 1e9) if dom_ms else None
     route_med = statistics.median(stage_ms["route_topk"])
     dc_ms = [max(s_ - route_med, 1e-6) for s_ in step_ms]
     dc_gbs = b["dispatch_combine"] * K / (sum(dc_ms) * 1e-3) / 1e9
@@ -640,12 +667,12 @@ def run_ours(args, world, rank, local):
         "copies_per_token": round(copies / (w.S * w.T), 4),
         "pairs_recv": pairs_recv,
         "dev_status": status,
-        "roofline": {"kernel": DOMINANT, "bound": "hbm",
+        "roofline": {"kernel": dom_name, "bound": "hbm",
                      "achieved": round(dom_achieved, 1) if dom_achieved else None,
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(dom_achieved / peak, 4) if dom_achieved else None,
                      "traffic": (DOMINANT_TRAFFIC.get(w.name) if args.variant == "contiguous" else None),
-                     "bytes_per_launch": b["perm_copy"],
+                     "bytes_per_launch": b[dom_key],
                      "us_per_launch": round(1e3 * dom_ms, 2) if dom_ms else None,
                      "launches_timed": len(recs)},
         "cpu_baseline": cpu,
@@ -678,7 +705,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--variant", default="contiguous", choices=sorted(VARIANTS),
                     help="contiguous runs + one-stage combine (default), masked blocks, a "
-                         "two-stage combine, MXFP8 rows, or experts placed by load with copies")
+                         "two-stage combine, MXFP8 rows, experts placed by load with copies, or "
+                         "routed rows (ids and weights with each row, no permute)")
     ap.add_argument("--spare", type=int, default=4,
                     help="spare copy slots per partition for --variant placed")
     ap.add_argument("--block-rows", type=int, default=0,

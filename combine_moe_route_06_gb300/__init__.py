@@ -29,7 +29,8 @@ __all__ = [
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
     "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
-    "moe_plan_placement", "moe_workspace_bytes_mapped", "moe_dispatch_layout_mapped", "Placement", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "moe_plan_placement", "moe_workspace_bytes_mapped", "moe_dispatch_layout_mapped", "Placement",
+    "moe_dispatch_pack_routed", "moe_routed_expert_stage1", "MoePath", "trace_enable", "trace_disable", "trace_reset",
     "trace_records",
 ]
 
@@ -97,11 +98,15 @@ def load_library() -> ctypes.CDLL:
             "moe_combine": ([P, i32, P, P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
             "moe_combine_stage1": ([P, i32, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P,
                                     P, P], ctypes.c_int),
-            "moe_combine_stage2": ([P, P, i32, i32, i32, i32, i32, P, P, P], ctypes.c_int),
+            "moe_combine_stage2": ([P, P, i32, i32, i32, i32, i32, i32, P, P, P], ctypes.c_int),
             "moe_dispatch_pack_mxfp8": ([P, i32, i32, i32, i32, P, P, i32, P, P, P, P],
                                          ctypes.c_int),
             "moe_expert_scale_mxfp8": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
             "moe_plan_placement": ([P, i32, i32, i32, P, P, P, P], ctypes.c_int),
+            "moe_dispatch_pack_routed": ([P, P, P, i32, i32, i32, i32, i32, P, P, i32, P, P, P, P,
+                                          P, P], ctypes.c_int),
+            "moe_routed_expert_stage1": ([P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P, P,
+                                          P, P], ctypes.c_int),
             "moe_workspace_bytes_mapped": ([i32, i32, i32, i32, i32, i32], ctypes.c_size_t),
             "moe_dispatch_layout_mapped": ([P, i32, i32, i32, i32, i32, i32, P, P, i32, P, P, P, P,
                                             P, P, P, ctypes.c_size_t, P, P], ctypes.c_int),
@@ -223,6 +228,41 @@ def moe_dispatch_pack_mxfp8(x, token_slot, part_offsets, send_q, send_src, dev_s
         _dev(part_offsets, "part_offsets", (torch.int32,)), cap_send,
         _dev(send_q, "send_q", (torch.uint8,), 3), _dev(send_src, "send_src", (torch.int32,)),
         _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_pack_routed(x, topk_ids, topk_w, token_slot, part_offsets, send, send_src,
+                             send_ids, send_w, dev_status=None, stream=None):
+    """moe_dispatch_pack plus each row's routing: send_ids i32 / send_w f32 [S,cap_send,k]."""
+    lib = load_library()
+    S, T, H = x.shape
+    k = topk_ids.shape[2]
+    P = token_slot.shape[2]
+    cap_send = send.shape[1]
+    _check(lib.moe_dispatch_pack_routed(
+        _dev(x, "x", _BF16_TYPES, 3), _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+        _dev(topk_w, "topk_w", (torch.float32,), 3), S, T, H, k, P,
+        _dev(token_slot, "token_slot", (torch.int32,), 3),
+        _dev(part_offsets, "part_offsets", (torch.int32,)), cap_send,
+        _dev(send, "send", _BF16_TYPES, 3), _dev(send_src, "send_src", (torch.int32,)),
+        _dev(send_ids, "send_ids", (torch.int32,), 3), _dev(send_w, "send_w", (torch.float32,), 3),
+        _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_routed_expert_stage1(send, send_ids, send_w, part_offsets, T, E, recv_part, scale, ret,
+                             dev_status=None, stream=None):
+    """Routed stand-in expert + stage-1 pre-add: ret [S,cap_send,H] per received row;
+    T tokens per source; scale None = identity expert."""
+    lib = load_library()
+    S, cap_send, H = send.shape
+    k = send_ids.shape[2]
+    P = part_offsets.shape[1] - 1
+    sc = None if scale is None else _dev(scale, "scale", (torch.float32,))
+    _check(lib.moe_routed_expert_stage1(
+        _dev(send, "send", _BF16_TYPES, 3), _dev(send_ids, "send_ids", (torch.int32,), 3),
+        _dev(send_w, "send_w", (torch.float32,), 3),
+        _dev(part_offsets, "part_offsets", (torch.int32,)), S, T, cap_send, k, E, P, H,
+        recv_part, sc, _dev(ret, "ret", _BF16_TYPES, 3), _status_ptr(dev_status),
+        _stream(stream)))
 
 
 class Placement:
@@ -354,14 +394,14 @@ def moe_combine_stage1(y, pair_row, topk_w, topk_ids, token_slot, E, recv_part, 
         _dev(ret, "ret", _BF16_TYPES, 3), _status_ptr(dev_status), _stream(stream)))
 
 
-def moe_combine_stage2(ret, token_slot, out, dev_status=None, stream=None):
-    """Home-side sum of a token's returned rows: out bf16 [S, T, H]."""
+def moe_combine_stage2(ret, token_slot, out, dev_status=None, stream=None, recv_part=-1):
+    """Home-side sum of a token's returned rows (from the receiving set): out bf16 [S, T, H]."""
     lib = load_library()
     S, cap_send, H = ret.shape
     _, T, P = token_slot.shape
     _check(lib.moe_combine_stage2(
         _dev(ret, "ret", _BF16_TYPES, 3), _dev(token_slot, "token_slot", (torch.int32,), 3), S, T,
-        P, H, cap_send, _dev(out, "out", _BF16_TYPES, 3), _status_ptr(dev_status),
+        P, H, recv_part, cap_send, _dev(out, "out", _BF16_TYPES, 3), _status_ptr(dev_status),
         _stream(stream)))
 
 
@@ -426,16 +466,22 @@ class MoePath:
     def __init__(self, S, T, H, E, k, P, recv_part=-1, align=1, cap_send=None, cap_recv=None,
                  device="cuda", layout="contiguous", block_rows=None, combine="single",
                  quant="none", placement: "Placement | None" = None):
-        """layout: "contiguous" (expert runs, moe_permute_to_experts) or "masked" (one
-        block of block_rows rows per expert, moe_permute_to_experts_masked).
+        """layout: "contiguous" (expert runs, moe_permute_to_experts), "masked" (one
+        block of block_rows rows per expert, moe_permute_to_experts_masked) or "routed"
+        (no permute: rows carry their ids and weights, moe_dispatch_pack_routed, and
+        moe_routed_expert_stage1 + moe_combine_stage2 replace the expert and combine).
         combine: "single" (moe_combine) or "two_stage" (moe_combine_stage1 + stage2).
         quant: "none" (bf16 rows) or "mxfp8" (rows sent as MXFP8 records; the
         receiver's stand-in expert dequantizes them, so every step runs it).
         placement: a Placement (moe_plan_placement) -- the layout then maps each
         pair to a physical expert slot and everything after it works on the
         P*Lp physical experts; None keeps expert e in slot e."""
-        if layout not in ("contiguous", "masked") or combine not in ("single", "two_stage"):
-            raise ValueError("layout must be contiguous|masked, combine single|two_stage")
+        if layout not in ("contiguous", "masked", "routed") or combine not in ("single", "two_stage"):
+            raise ValueError("layout must be contiguous|masked|routed, combine single|two_stage")
+        if layout == "routed":
+            if quant != "none":
+                raise ValueError("the routed layout carries bf16 rows")
+            combine = "two_stage"          # the routed expert produces stage 1 itself
         if quant not in ("none", "mxfp8"):
             raise ValueError("quant must be none|mxfp8")
         if quant == "mxfp8" and (H % 512 != 0 or layout != "contiguous"):
@@ -459,6 +505,9 @@ class MoePath:
                 raise ValueError("the masked layout needs block_rows")
             self.block_rows = block_rows
             self.cap_recv = self.n_blocks * block_rows
+        elif layout == "routed":
+            self.block_rows = None
+            self.cap_recv = 0              # no receive buffer: rows stay where they arrive
         else:
             self.block_rows = None
             self.cap_recv = S * T * k + Ep * (align - 1) if cap_recv is None else cap_recv
@@ -492,6 +541,9 @@ class MoePath:
         self.masked_counts = torch.empty((self.n_blocks,), **i32) if layout == "masked" else None
         self.ret = (torch.empty((S, self.cap_send, H), dtype=torch.bfloat16, device=d)
                     if combine == "two_stage" else None)
+        if layout == "routed":
+            self.send_ids = torch.empty((S, self.cap_send, k), **i32)
+            self.send_w = torch.empty((S, self.cap_send, k), dtype=torch.float32, device=d)
         self.y = None
         if quant == "mxfp8":
             self.y = torch.empty((self.cap_recv, H), dtype=torch.bfloat16, device=d)
@@ -530,6 +582,24 @@ class MoePath:
         else:
             calls.append((lib.moe_dispatch_layout, (vp(self.topk_ids.data_ptr()), S, T, k, E, P)
                           + outs))
+        if self.layout == "routed":
+            calls.append((lib.moe_dispatch_pack_routed, (
+                ptr(x, "x", _BF16_TYPES), vp(self.topk_ids.data_ptr()),
+                vp(self.topk_w.data_ptr()), S, T, H, k, P, vp(self.token_slot.data_ptr()),
+                vp(self.part_offsets.data_ptr()), self.cap_send, vp(self.send.data_ptr()),
+                vp(self.send_src.data_ptr()), vp(self.send_ids.data_ptr()),
+                vp(self.send_w.data_ptr()), stp, st)))
+            self._bound_scale = None if scale is None else self.slot_scale(scale)
+            sc = vp(None) if self._bound_scale is None else ptr(self._bound_scale, "scale",
+                                                                  (torch.float32,))
+            calls.append((lib.moe_routed_expert_stage1, (
+                vp(self.send.data_ptr()), vp(self.send_ids.data_ptr()),
+                vp(self.send_w.data_ptr()), vp(self.part_offsets.data_ptr()), S, T, self.cap_send,
+                k, Ep, P, H, self.recv_part, sc, vp(self.ret.data_ptr()), stp, st)))
+            calls.append((lib.moe_combine_stage2, (
+                vp(self.ret.data_ptr()), vp(self.token_slot.data_ptr()), S, T, P, H,
+                self.recv_part, self.cap_send, vp(self.out.data_ptr()), stp, st)))
+            return calls
         if self.quant == "mxfp8":
             calls.append((lib.moe_dispatch_pack_mxfp8, (
                 ptr(x, "x", _BF16_TYPES), S, T, H, P, vp(self.token_slot.data_ptr()),
@@ -573,7 +643,7 @@ class MoePath:
                 vp(self.ret.data_ptr()), stp, st)))
             calls.append((lib.moe_combine_stage2, (
                 vp(self.ret.data_ptr()), vp(self.token_slot.data_ptr()), S, T, P, H,
-                self.cap_send, vp(self.out.data_ptr()), stp, st)))
+                self.recv_part, self.cap_send, vp(self.out.data_ptr()), stp, st)))
         else:
             calls.append((lib.moe_combine, (
                 vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
@@ -603,6 +673,11 @@ class MoePath:
             moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts,
                                 self.expert_rank, self.part_counts, self.part_offsets,
                                 self.token_slot, self.ws, self.dev_status, stream)
+        if self.layout == "routed":
+            moe_dispatch_pack_routed(x, self.topk_ids, self.topk_w, self.token_slot,
+                                     self.part_offsets, self.send, self.send_src, self.send_ids,
+                                     self.send_w, self.dev_status, stream)
+            return
         if self.quant == "mxfp8":
             moe_dispatch_pack_mxfp8(x, self.token_slot, self.part_offsets, self.send,
                                     self.send_src, self.dev_status, stream)
@@ -652,14 +727,26 @@ class MoePath:
         if self.combine_mode == "two_stage":
             moe_combine_stage1(y, self.pair_row, self.topk_w, self.phys_ids, self.token_slot,
                                self.Ep, self.recv_part, self.ret, self.dev_status, stream)
-            moe_combine_stage2(self.ret, self.token_slot, self.out, self.dev_status, stream)
+            moe_combine_stage2(self.ret, self.token_slot, self.out, self.dev_status, stream,
+                               recv_part=self.recv_part)
         else:
             moe_combine(y, self.pair_row, self.topk_w, self.out, self.dev_status, stream)
+
+    def routed_combine(self, scale=None, stream=None):
+        """Routed layout: the routed stand-in expert with the stage-1 pre-add, then stage 2."""
+        sc = None if scale is None else self.slot_scale(scale)
+        moe_routed_expert_stage1(self.send, self.send_ids, self.send_w, self.part_offsets, self.T,
+                                 self.Ep, self.recv_part, sc, self.ret, self.dev_status, stream)
+        moe_combine_stage2(self.ret, self.token_slot, self.out, self.dev_status, stream,
+                               recv_part=self.recv_part)
 
     def step(self, logits, x, scale=None, stream=None):
         """route -> layout -> pack -> permute -> [stand-in expert] -> combine; returns out."""
         self.route(logits, stream)
         self.dispatch(x, stream)
+        if self.layout == "routed":
+            self.routed_combine(scale, stream)
+            return self.out
         y = self.expert(scale, stream) if scale is not None or self.quant == "mxfp8" else None
         self.combine(y, stream)
         return self.out
@@ -670,6 +757,13 @@ class MoePath:
         (always with MXFP8 rows), combine 1 (2 when split into two stages)."""
         with_expert = with_expert or self.quant == "mxfp8"
         mapped = self.placement is not None
+        if self.layout == "routed":
+            if self.T == 0:                # the two receive-side calls launch nothing
+                return 1 + (2 if mapped else 1) + 1
+            layout = 1 if self.T <= 256 else 2
+            if mapped:
+                layout = 2 * layout + 1
+            return 1 + layout + 1 + 1 + 1
         if self.T == 0:
             return 1 + (2 if mapped else 1) + 2 + (1 if with_expert else 0)
         layout = 1 if self.T <= 256 else 2

@@ -368,11 +368,13 @@ moe_status_t moe_combine_stage1(const uint16_t *y, int y_rows, const int32_t *pa
 }
 
 moe_status_t moe_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
-                                int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
-                                cudaStream_t stream)
+                                int P, int H, int recv_part, int cap_send, uint16_t *out,
+                                uint32_t *dev_status, cudaStream_t stream)
 {
     moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
     if (st != MOE_OK) return st;
+    REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, %d)", __func__,
+            recv_part, P);
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
     REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
     REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
@@ -382,7 +384,8 @@ moe_status_t moe_combine_stage2(const uint16_t *ret, const int32_t *token_slot, 
     REQUIRE_ARR(out, NT * H, 16);
     REQUIRE_STATUS(dev_status);
     return cuda_status(
-        launch_combine_stage2(ret, token_slot, S, T, P, H, cap_send, out, dev_status, stream),
+        launch_combine_stage2(ret, token_slot, S, T, P, H, recv_part, cap_send, out, dev_status,
+                              stream),
         __func__);
 }
 
@@ -475,6 +478,65 @@ moe_status_t moe_dispatch_layout_mapped(const int32_t *topk_ids, int S, int T, i
                                                      expert_counts, expert_rank, part_counts,
                                                      part_offsets, token_slot, ws, dev_status,
                                                      stream),
+                       __func__);
+}
+
+moe_status_t moe_dispatch_pack_routed(const uint16_t *x, const int32_t *topk_ids,
+                                      const float *topk_w, int S, int T, int H, int k, int P,
+                                      const int32_t *token_slot, const int32_t *part_offsets,
+                                      int cap_send, uint16_t *send, int32_t *send_src,
+                                      int32_t *send_ids, float *send_w, uint32_t *dev_status,
+                                      cudaStream_t stream)
+{
+    REQUIRE(S >= 1 && T >= 0, "%s: S=%d, T=%d", __func__, S, T);
+    REQUIRE(k >= 1 && k <= kMaxK, "%s: k=%d must be in [1, %d]", __func__, k, kMaxK);
+    REQUIRE(P >= 1 && P <= kMaxP, "%s: P=%d must be in [1, %d]", __func__, P, kMaxP);
+    REQUIRE((int64_t)S * T * (k > P ? k : P) < ((int64_t)1 << 31), "%s: S*T*max(k,P) too large",
+            __func__);
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
+    REQUIRE((int64_t)S * cap_send * k < ((int64_t)1 << 31), "%s: S*cap_send*k must be < 2^31",
+            __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(x, NT * H, 16);
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(topk_w, NT * k, 4);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(send, (int64_t)S * cap_send * H, 16);
+    REQUIRE_ARR(send_src, (int64_t)S * cap_send, 4);
+    REQUIRE_ARR(send_ids, (int64_t)S * cap_send * k, 4);
+    REQUIRE_ARR(send_w, (int64_t)S * cap_send * k, 4);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(launch_dispatch_pack(x, S, T, H, P, token_slot, part_offsets, cap_send, send,
+                                            send_src, dev_status, stream, topk_ids, topk_w, k,
+                                            send_ids, send_w),
+                       __func__);
+}
+
+moe_status_t moe_routed_expert_stage1(const uint16_t *send, const int32_t *send_ids,
+                                      const float *send_w, const int32_t *part_offsets, int S,
+                                      int T, int cap_send, int k, int E, int P, int H,
+                                      int recv_part, const float *scale, uint16_t *ret,
+                                      uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, %d)", __func__,
+            recv_part, P);
+    const int64_t rows = (int64_t)S * cap_send;
+    REQUIRE_ARR(send, rows * H, 16);
+    REQUIRE_ARR(send_ids, rows * k, 4);
+    REQUIRE_ARR(send_w, rows * k, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    if (scale) REQUIRE_ARR(scale, E, 4);
+    REQUIRE_ARR(ret, rows * H, 16);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(launch_routed_stage1(send, send_ids, send_w, part_offsets, S, T, cap_send, k,
+                                            E, P, H, recv_part, scale, ret, dev_status, stream),
                        __func__);
 }
 

@@ -25,6 +25,14 @@ constexpr int kCombUnroll = 2;                  // int4 (8 bf16) per lane per se
 constexpr int kCombSegVec = 32 * kCombUnroll;   // int4 per segment (1 KiB)
 constexpr int kCombBatch = 8;                   // rows whose loads are issued together
 constexpr int kCombThreads = 256;
+// The stage kernels read one or a few rows per warp task, so they take wider
+// segments (2 KiB) and smaller batches than k_combine to keep enough bytes in
+// flight at the occupancy their registers allow.
+constexpr int kStageUnroll = 4;
+constexpr int kRoutedUnroll = 8;
+constexpr int kStageBatch = 2;
+constexpr int kStage2Unroll = 2;
+constexpr int kStage2Batch = 8;
 
 __device__ __forceinline__ void fma_bf16x8(float *acc, int4 v, float w)
 {
@@ -127,6 +135,7 @@ __global__ void __launch_bounds__(kCombThreads) k_combine(const int4 *__restrict
 // a send slot of the token, the weighted sum of the token's experts in that
 // partition (fp32 FMAs in j order) is rounded once to bf16 and written to the
 // slot's row of `ret` (send layout: the rows travel back the way they came).
+template <int U, int B>
 __global__ void __launch_bounds__(kCombThreads) k_combine_stage1(
     const int4 *__restrict__ y, int y_rows, const int32_t *__restrict__ pair_row,
     const float *__restrict__ w, const int32_t *__restrict__ ids,
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage1(
     bool bad_row = false, cap_flag = false;
     const int lane = threadIdx.x & 31;
     const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    const int nseg = (V + (32 * U) - 1) / (32 * U);
     const int64_t ntask = N * nseg;
     for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
          task += gwarps) {
@@ -167,21 +176,21 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage1(
             }
         }
         unsigned smask = __ballot_sync(kFull, in_r);
-        const int v0 = g * kCombSegVec + lane;
+        const int v0 = g * (32 * U) + lane;
         while (smask) {
             const int p0 = __ffs(smask) - 1;
             smask &= smask - 1;
             const int slot0 = __shfl_sync(kFull, slot, p0);
             unsigned jmask = __ballot_sync(kFull, pr >= 0 && pj == p0);
-            float acc[8 * kCombUnroll];
+            float acc[8 * U];
 #pragma unroll
-            for (int i = 0; i < 8 * kCombUnroll; i++) acc[i] = 0.f;
+            for (int i = 0; i < 8 * U; i++) acc[i] = 0.f;
             while (jmask) {
-                int4 r[kCombBatch][kCombUnroll];
-                float wb[kCombBatch];
+                int4 r[B][U];
+                float wb[B];
                 int nb = 0;
 #pragma unroll
-                for (int b = 0; b < kCombBatch; b++) {
+                for (int b = 0; b < B; b++) {
                     if (jmask) {
                         const int j = __ffs(jmask) - 1;
                         jmask &= jmask - 1;
@@ -189,7 +198,7 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage1(
                         wb[b] = __shfl_sync(kFull, wj, j);
                         const int4 *src = y + (int64_t)row * V;
 #pragma unroll
-                        for (int u = 0; u < kCombUnroll; u++) {
+                        for (int u = 0; u < U; u++) {
                             const int vi = v0 + 32 * u;
                             r[b][u] = (vi < V) ? ld_stream(src + vi) : make_int4(0, 0, 0, 0);
                         }
@@ -197,16 +206,16 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage1(
                     }
                 }
 #pragma unroll
-                for (int b = 0; b < kCombBatch; b++) {
+                for (int b = 0; b < B; b++) {
                     if (b < nb) {
 #pragma unroll
-                        for (int u = 0; u < kCombUnroll; u++) fma_bf16x8(acc + 8 * u, r[b][u], wb[b]);
+                        for (int u = 0; u < U; u++) fma_bf16x8(acc + 8 * u, r[b][u], wb[b]);
                     }
                 }
             }
             int4 *dst = ret + ((int64_t)s * cap_send + slot0) * V;
 #pragma unroll
-            for (int u = 0; u < kCombUnroll; u++) {
+            for (int u = 0; u < U; u++) {
                 const int vi = v0 + 32 * u;
                 if (vi < V) st_cg(dst + vi, pack_bf16x8(acc + 8 * u));
             }
@@ -216,19 +225,117 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage1(
     if (cap_flag) flag_status(dev_status, MOE_ERR_CAPACITY);
 }
 
+// Routed expert with the stage-1 pre-add (a2a-backends section 6.1: the rows
+// arrive in sender order with their routing and a routed expert kernel picks
+// its experts from the ids; section 7.1: it already produces the weighted sum
+// per GPU).  Stand-in expert y_j = bf16(x * scale[e_j]) (x itself when scale
+// is null).  One warp per (send row, 1 KiB segment): the row is read once and
+// each of its experts on the row's partition adds w_j * y_j in ascending j
+// with fp32 FMAs -- the same operations, in the same order, as the stand-in
+// expert followed by k_combine_stage1, so the two paths give the same bytes.
+template <int U, bool SCALED>
+__global__ void __launch_bounds__(kCombThreads) k_routed_stage1(
+    const int4 *__restrict__ send, const int32_t *__restrict__ send_ids,
+    const float *__restrict__ send_w, const int32_t *__restrict__ part_offsets, int S,
+    int cap_send, int span, int k, int E, int L, int P, int V, int recv_part,
+    const float *__restrict__ scale, int4 *__restrict__ ret, uint32_t *dev_status)
+{
+    pdl_wait();
+    pdl_trigger();
+    bool bad_id = false;
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nseg = (V + (32 * U) - 1) / (32 * U);
+    // Tasks: (source, i, segment) for i < span.  With one receiving partition
+    // i indexes that partition's region of the source (span = at most T rows);
+    // otherwise i is the send row itself (span = cap_send).
+    const int64_t ntask = (int64_t)S * span * nseg;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
+         task += gwarps) {
+        const int64_t q = task / nseg;
+        const int g = (int)(task - q * nseg);
+        const int s = (int)(q / span);
+        const int i = (int)(q - (int64_t)s * span);
+        const int32_t *po = part_offsets + (int64_t)s * (P + 1);
+        int r, p;
+        if (recv_part >= 0) {
+            r = __ldg(po + recv_part) + i;
+            if (r >= __ldg(po + recv_part + 1) || r >= cap_send) continue;
+            p = recv_part;
+        } else {
+            // partition of the row: the number of region ends at or below it
+            r = i;
+            const int end = lane < P ? __ldg(po + lane + 1) : 0x7fffffff;
+            p = __popc(__ballot_sync(kFull, end <= r));
+            if (p >= P) continue;                                   // empty row
+        }
+        const int64_t row = (int64_t)s * cap_send + r;
+        int e = -1;
+        float wj = 0.f, sj = 1.f;
+        if (lane < k) {
+            e = __ldg(send_ids + row * k + lane);
+            wj = __ldg(send_w + row * k + lane);
+            if (e >= E && g == 0) bad_id = true;
+            if (e >= 0 && e < E && e / L == p) {
+                if (SCALED) sj = __ldg(scale + e);
+            } else {
+                e = -1;
+            }
+        }
+        unsigned jmask = __ballot_sync(kFull, e >= 0);
+        const int v0 = g * (32 * U) + lane;
+        int4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int vi = v0 + 32 * u;
+            x[u] = (vi < V && jmask) ? ld_stream(send + row * V + vi) : make_int4(0, 0, 0, 0);
+        }
+        // column-outer: each 16-byte column is finished over all the row's experts
+        // before the next, so only 8 accumulators are live (the per-element order
+        // of the sum over j is unchanged)
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) acc[i] = 0.f;
+            for (unsigned m = jmask; m; m &= m - 1) {
+                const int j = __ffs(m) - 1;
+                const float wb = __shfl_sync(kFull, wj, j);
+                int4 y = x[u];
+                if (SCALED) {
+                    const float sb = __shfl_sync(kFull, sj, j);
+                    float a[8];
+                    const uint32_t uu[4] = {(uint32_t)y.x, (uint32_t)y.y, (uint32_t)y.z, (uint32_t)y.w};
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        a[2 * i] = __uint_as_float(uu[i] << 16) * sb;
+                        a[2 * i + 1] = __uint_as_float(uu[i] & 0xffff0000u) * sb;
+                    }
+                    y = pack_bf16x8(a);
+                }
+                fma_bf16x8(acc, y, wb);
+            }
+            const int vi = v0 + 32 * u;
+            if (vi < V) st_cg(ret + row * V + vi, pack_bf16x8(acc));
+        }
+    }
+    if (bad_id) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
+}
+
 // Stage 2: one warp per (token, 1 KiB segment); the token's returned rows (one
 // per send slot, partitions in ascending order) summed with fp32 adds, one bf16
 // rounding.
+template <int U, int B>
 __global__ void __launch_bounds__(kCombThreads) k_combine_stage2(
     const int4 *__restrict__ ret, const int32_t *__restrict__ token_slot, int64_t N, int T,
-    int P, int V, int cap_send, int4 *__restrict__ out, uint32_t *dev_status)
+    int P, int V, int recv_part, int cap_send, int4 *__restrict__ out, uint32_t *dev_status)
 {
     pdl_wait();
     pdl_trigger();
     bool cap_flag = false;
     const int lane = threadIdx.x & 31;
     const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    const int nseg = (V + (32 * U) - 1) / (32 * U);
     const int64_t ntask = N * nseg;
     for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
          task += gwarps) {
@@ -236,28 +343,52 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage2(
         const int g = (int)(task - n * nseg);
         const int s = (int)(n / T);
         int slot = -1;
-        if (lane < P) slot = __ldg(token_slot + n * P + lane);
+        if (lane < P && (recv_part < 0 || lane == recv_part)) slot = __ldg(token_slot + n * P + lane);
         if (slot >= cap_send) {
             if (g == 0) cap_flag = true;
             slot = -1;
         }
         unsigned vmask = __ballot_sync(kFull, slot >= 0);
-        const int v0 = g * kCombSegVec + lane;
-        float acc[8 * kCombUnroll];
+        const int v0 = g * (32 * U) + lane;
+        if constexpr (B == 1) {
+            // launched only when one partition returns rows: at most one row per
+            // token, so each 16-byte column is finished on its own (8 accumulators)
+            int4 r[U];
+            int sl = -1;
+            if (vmask) sl = __shfl_sync(kFull, slot, __ffs(vmask) - 1);
+            const int4 *src = ret + ((int64_t)s * cap_send + (sl < 0 ? 0 : sl)) * V;
 #pragma unroll
-        for (int i = 0; i < 8 * kCombUnroll; i++) acc[i] = 0.f;
+            for (int u = 0; u < U; u++) {
+                const int vi = v0 + 32 * u;
+                r[u] = (vi < V && sl >= 0) ? ld_stream(src + vi) : make_int4(0, 0, 0, 0);
+            }
+            int4 *dst = out + n * V;
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                float acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[i] = 0.f;
+                if (sl >= 0) fma_bf16x8(acc, r[u], 1.f);
+                const int vi = v0 + 32 * u;
+                if (vi < V) st_stream(dst + vi, pack_bf16x8(acc));
+            }
+            continue;
+        }
+        float acc[8 * U];
+#pragma unroll
+        for (int i = 0; i < 8 * U; i++) acc[i] = 0.f;
         while (vmask) {
-            int4 r[kCombBatch][kCombUnroll];
+            int4 r[B][U];
             int nb = 0;
 #pragma unroll
-            for (int b = 0; b < kCombBatch; b++) {
+            for (int b = 0; b < B; b++) {
                 if (vmask) {
                     const int p = __ffs(vmask) - 1;
                     vmask &= vmask - 1;
                     const int sl = __shfl_sync(kFull, slot, p);
                     const int4 *src = ret + ((int64_t)s * cap_send + sl) * V;
 #pragma unroll
-                    for (int u = 0; u < kCombUnroll; u++) {
+                    for (int u = 0; u < U; u++) {
                         const int vi = v0 + 32 * u;
                         r[b][u] = (vi < V) ? ld_stream(src + vi) : make_int4(0, 0, 0, 0);
                     }
@@ -265,16 +396,16 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage2(
                 }
             }
 #pragma unroll
-            for (int b = 0; b < kCombBatch; b++) {
+            for (int b = 0; b < B; b++) {
                 if (b < nb) {
 #pragma unroll
-                    for (int u = 0; u < kCombUnroll; u++) fma_bf16x8(acc + 8 * u, r[b][u], 1.f);
+                    for (int u = 0; u < U; u++) fma_bf16x8(acc + 8 * u, r[b][u], 1.f);
                 }
             }
         }
         int4 *dst = out + n * V;
 #pragma unroll
-        for (int u = 0; u < kCombUnroll; u++) {
+        for (int u = 0; u < U; u++) {
             const int vi = v0 + 32 * u;
             if (vi < V) st_stream(dst + vi, pack_bf16x8(acc + 8 * u));
         }
@@ -446,13 +577,14 @@ cudaError_t launch_combine_stage1(const uint16_t *y, int y_rows, const int32_t *
     const int64_t N = (int64_t)S * T;
     if (N == 0) return cudaSuccess;
     const int V = H / 8;
-    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    constexpr int U = kStageUnroll, B = kStageBatch;
+    const int nseg = (V + 32 * U - 1) / (32 * U);
     int64_t blocks = (N * nseg + (kCombThreads / 32) - 1) / (kCombThreads / 32);
-    const int resident = resident_grid((const void *)k_combine_stage1, kCombThreads, 0);
+    const int resident = resident_grid((const void *)k_combine_stage1<U, B>, kCombThreads, 0);
     if (resident > 0 && blocks > resident) blocks = resident;
     cudaError_t e;
     MOE_TRACED_LAUNCH("k_combine_stage1", st,
-                      e = launch_pdl(k_combine_stage1, dim3((unsigned)blocks), dim3(kCombThreads),
+                      e = launch_pdl(k_combine_stage1<U, B>, dim3((unsigned)blocks), dim3(kCombThreads),
                                      0, st, (const int4 *)y, y_rows, pair_row, w, ids, token_slot,
                                      N, T, k, E, E / P, P, V, recv_part, cap_send, (int4 *)ret,
                                      dev_status));
@@ -460,21 +592,34 @@ cudaError_t launch_combine_stage1(const uint16_t *y, int y_rows, const int32_t *
 }
 
 cudaError_t launch_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
-                                  int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
-                                  cudaStream_t st)
+                                  int P, int H, int recv_part, int cap_send, uint16_t *out,
+                                  uint32_t *dev_status, cudaStream_t st)
 {
     const int64_t N = (int64_t)S * T;
     if (N == 0) return cudaSuccess;
     const int V = H / 8;
-    const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
+    // one returned row per token from a single receiving partition, up to P otherwise
+    const bool one = recv_part >= 0 || P == 1;
+    const void *kfn = one ? (const void *)k_combine_stage2<kRoutedUnroll, 1>
+                          : (const void *)k_combine_stage2<kStage2Unroll, kStage2Batch>;
+    const int U = one ? kRoutedUnroll : kStage2Unroll;
+    const int nseg = (V + 32 * U - 1) / (32 * U);
     int64_t blocks = (N * nseg + (kCombThreads / 32) - 1) / (kCombThreads / 32);
-    const int resident = resident_grid((const void *)k_combine_stage2, kCombThreads, 0);
+    const int resident = resident_grid(kfn, kCombThreads, 0);
     if (resident > 0 && blocks > resident) blocks = resident;
     cudaError_t e;
-    MOE_TRACED_LAUNCH("k_combine_stage2", st,
-                      e = launch_pdl(k_combine_stage2, dim3((unsigned)blocks), dim3(kCombThreads),
-                                     0, st, (const int4 *)ret, token_slot, N, T, P, V, cap_send,
-                                     (int4 *)out, dev_status));
+    if (one) {
+        MOE_TRACED_LAUNCH("k_combine_stage2", st,
+                          e = launch_pdl(k_combine_stage2<kRoutedUnroll, 1>, dim3((unsigned)blocks),
+                                         dim3(kCombThreads), 0, st, (const int4 *)ret, token_slot,
+                                         N, T, P, V, recv_part, cap_send, (int4 *)out, dev_status));
+    } else {
+        MOE_TRACED_LAUNCH("k_combine_stage2", st,
+                          e = launch_pdl(k_combine_stage2<kStage2Unroll, kStage2Batch>,
+                                         dim3((unsigned)blocks), dim3(kCombThreads), 0, st,
+                                         (const int4 *)ret, token_slot, N, T, P, V, recv_part,
+                                         cap_send, (int4 *)out, dev_status));
+    }
     return e;
 }
 
@@ -491,6 +636,40 @@ cudaError_t launch_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expe
                       e = launch_pdl(k_expert_scale_mxfp8, dim3(blocks), dim3(256),
                                      (size_t)(E + 1) * sizeof(int), st, recv_q, expert_offsets,
                                      scale, E, H / 8, cap_recv, (int4 *)y));
+    return e;
+}
+
+cudaError_t launch_routed_stage1(const uint16_t *send, const int32_t *send_ids,
+                                 const float *send_w, const int32_t *part_offsets, int S, int T,
+                                 int cap_send, int k, int E, int P, int H, int recv_part,
+                                 const float *scale, uint16_t *ret, uint32_t *dev_status,
+                                 cudaStream_t st)
+{
+    const int span = recv_part >= 0 ? (T < cap_send ? T : cap_send) : cap_send;
+    const int64_t rows = (int64_t)S * span;
+    if (rows == 0) return cudaSuccess;
+    const int V = H / 8;
+    constexpr int U = kRoutedUnroll;
+    const int nseg = (V + 32 * U - 1) / (32 * U);
+    int64_t blocks = (rows * nseg + (kCombThreads / 32) - 1) / (kCombThreads / 32);
+    const void *kfn = scale ? (const void *)k_routed_stage1<U, true>
+                            : (const void *)k_routed_stage1<U, false>;
+    const int resident = resident_grid(kfn, kCombThreads, 0);
+    if (resident > 0 && blocks > resident) blocks = resident;
+    cudaError_t e;
+    if (scale) {
+        MOE_TRACED_LAUNCH("k_routed_stage1", st,
+                          e = launch_pdl(k_routed_stage1<U, true>, dim3((unsigned)blocks),
+                                         dim3(kCombThreads), 0, st, (const int4 *)send, send_ids,
+                                         send_w, part_offsets, S, cap_send, span, k, E, E / P, P, V,
+                                         recv_part, scale, (int4 *)ret, dev_status));
+    } else {
+        MOE_TRACED_LAUNCH("k_routed_stage1", st,
+                          e = launch_pdl(k_routed_stage1<U, false>, dim3((unsigned)blocks),
+                                         dim3(kCombThreads), 0, st, (const int4 *)send, send_ids,
+                                         send_w, part_offsets, S, cap_send, span, k, E, E / P, P, V,
+                                         recv_part, scale, (int4 *)ret, dev_status));
+    }
     return e;
 }
 

@@ -35,10 +35,18 @@ cudaError_t launch_dispatch_layout(const int32_t *ids, int S, int T, int k, int 
                                    int32_t *part_offsets, int32_t *token_slot, void *ws,
                                    uint32_t *dev_status, cudaStream_t st);
 
+// With send_ids != nullptr the rows also carry the tokens' ids and weights.
 cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                                  const int32_t *token_slot, const int32_t *part_offsets,
                                  int cap_send, uint16_t *send, int32_t *send_src,
-                                 uint32_t *dev_status, cudaStream_t st);
+                                 uint32_t *dev_status, cudaStream_t st,
+                                 const int32_t *ids = nullptr, const float *w = nullptr, int k = 0,
+                                 int32_t *send_ids = nullptr, float *send_w = nullptr);
+cudaError_t launch_routed_stage1(const uint16_t *send, const int32_t *send_ids,
+                                 const float *send_w, const int32_t *part_offsets, int S, int T,
+                                 int cap_send, int k, int E, int P, int H, int recv_part,
+                                 const float *scale, uint16_t *ret, uint32_t *dev_status,
+                                 cudaStream_t st);
 
 cudaError_t launch_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, int P,
                                        const int32_t *token_slot, const int32_t *part_offsets,
@@ -86,8 +94,8 @@ cudaError_t launch_combine_stage1(const uint16_t *y, int y_rows, const int32_t *
                                   int cap_send, uint16_t *ret, uint32_t *dev_status,
                                   cudaStream_t st);
 cudaError_t launch_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
-                                  int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
-                                  cudaStream_t st);
+                                  int P, int H, int recv_part, int cap_send, uint16_t *out,
+                                  uint32_t *dev_status, cudaStream_t st);
 
 cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
                                 const float *scale, int E, int H, int cap_recv, uint16_t *y,

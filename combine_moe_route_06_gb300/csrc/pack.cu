@@ -23,13 +23,22 @@ constexpr int kPackUnroll = 4;                   // int4 per lane per segment
 constexpr int kPackSegVec = 32 * kPackUnroll;    // int4 per segment (2 KiB)
 constexpr int kPackThreads = 256;
 
+// ROUTED: each written row also carries the token's k expert ids and weights
+// (a2a-backends section 6.1: payloads are the hidden state, the top-k ids and
+// the top-k weights); rows no slot names carry id -1 and weight 0 (section
+// 6.3: empty slots have an invalid expert id).
+template <bool ROUTED>
 __global__ void __launch_bounds__(kPackThreads) k_pack(const int4 *__restrict__ x, int S, int T,
                                                        int V, int P,
                                                        const int32_t *__restrict__ token_slot,
                                                        const int32_t *__restrict__ part_offsets,
                                                        int cap_send, int4 *__restrict__ send,
                                                        int32_t *__restrict__ send_src,
-                                                       uint32_t *dev_status)
+                                                       uint32_t *dev_status,
+                                                       const int32_t *__restrict__ ids,
+                                                       const float *__restrict__ w, int k,
+                                                       int32_t *__restrict__ send_ids,
+                                                       float *__restrict__ send_w)
 {
     pdl_wait();
     pdl_trigger();
@@ -41,7 +50,15 @@ __global__ void __launch_bounds__(kPackThreads) k_pack(const int4 *__restrict__ 
     for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
         const int s = (int)(i / cap_send);
         const int r = (int)(i - (int64_t)s * cap_send);
-        if (r >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) send_src[i] = -1;
+        if (r >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) {
+            send_src[i] = -1;
+            if (ROUTED) {
+                for (int j = 0; j < k; j++) {
+                    send_ids[i * k + j] = -1;
+                    send_w[i * k + j] = 0.f;
+                }
+            }
+        }
     }
 
     const int nseg = (V + kPackSegVec - 1) / kPackSegVec;
@@ -59,6 +76,22 @@ __global__ void __launch_bounds__(kPackThreads) k_pack(const int4 *__restrict__ 
         unsigned dmask = __ballot_sync(kFull, ok);
         if (g == 0 && ok) send_src[(int64_t)s * cap_send + slot] = (int32_t)(n - (int64_t)s * T);
         if (dmask == 0) continue;
+        if (ROUTED && g == 0) {
+            int id = -1;
+            float wt = 0.f;
+            if (lane < k) {
+                id = __ldg(ids + n * k + lane);
+                wt = __ldg(w + n * k + lane);
+            }
+            for (unsigned m = dmask; m; m &= m - 1) {
+                const int sl = __shfl_sync(kFull, slot, __ffs(m) - 1);
+                if (lane < k) {
+                    const int64_t o = ((int64_t)s * cap_send + sl) * k + lane;
+                    send_ids[o] = id;
+                    send_w[o] = wt;
+                }
+            }
+        }
 
         const int4 *src = x + n * V;
         const int v0 = g * kPackSegVec + lane;
@@ -188,7 +221,8 @@ __global__ void __launch_bounds__(kPackThreads) k_pack_mxfp8(
 cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                                  const int32_t *token_slot, const int32_t *part_offsets,
                                  int cap_send, uint16_t *send, int32_t *send_src,
-                                 uint32_t *dev_status, cudaStream_t st)
+                                 uint32_t *dev_status, cudaStream_t st, const int32_t *ids,
+                                 const float *w, int k, int32_t *send_ids, float *send_w)
 {
     DeviceInfo di;
     cudaError_t e = device_info(&di);
@@ -197,15 +231,25 @@ cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
     const int nseg = (V + kPackSegVec - 1) / kPackSegVec;
     const int64_t warps = (int64_t)S * T * nseg;
     const int64_t want = (warps + (kPackThreads / 32) - 1) / (kPackThreads / 32);
-    const int resident = resident_grid((const void *)k_pack, kPackThreads, 0);
+    const int resident = resident_grid((const void *)k_pack<false>, kPackThreads, 0);
     int64_t blocks = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPackThreads);
     if (want < blocks) blocks = want;
     const int64_t tail_blocks = ((int64_t)S * cap_send + kPackThreads - 1) / kPackThreads;
     if (blocks < 1) blocks = tail_blocks < 1 ? 1 : (tail_blocks < di.sm_count ? tail_blocks : di.sm_count);
-    MOE_TRACED_LAUNCH("k_pack", st,
-                      e = launch_pdl(k_pack, dim3((unsigned)blocks), dim3(kPackThreads), 0, st,
-                                     (const int4 *)x, S, T, V, P, token_slot, part_offsets,
-                                     cap_send, (int4 *)send, send_src, dev_status));
+    if (send_ids == nullptr) {
+        MOE_TRACED_LAUNCH("k_pack", st,
+                          e = launch_pdl(k_pack<false>, dim3((unsigned)blocks), dim3(kPackThreads), 0,
+                                         st, (const int4 *)x, S, T, V, P, token_slot, part_offsets,
+                                         cap_send, (int4 *)send, send_src, dev_status,
+                                         (const int32_t *)nullptr, (const float *)nullptr, 0,
+                                         (int32_t *)nullptr, (float *)nullptr));
+    } else {
+        MOE_TRACED_LAUNCH("k_pack_routed", st,
+                          e = launch_pdl(k_pack<true>, dim3((unsigned)blocks), dim3(kPackThreads), 0,
+                                         st, (const int4 *)x, S, T, V, P, token_slot, part_offsets,
+                                         cap_send, (int4 *)send, send_src, dev_status, ids, w, k,
+                                         send_ids, send_w));
+    }
     return e;
 }
 

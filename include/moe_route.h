@@ -183,6 +183,52 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                                uint32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Routed payload (a2a-backends section 6.1: next to the hidden state the
+ * sender writes the token's expert ids and weights -- payloads = hidden
+ * state, top-k ids, top-k weights -- so the receiver groups nothing and hands
+ * the rows to a routed expert kernel; section 6.3: empty slots carry an
+ * invalid expert id so the kernel skips them).
+ * moe_dispatch_pack_routed: moe_dispatch_pack plus, for every written row,
+ *   send_ids[s][slot][j] = topk_ids[s][t][j], send_w[s][slot][j] = topk_w[s][t][j]
+ * and id -1 / weight 0 for rows no slot names.
+ *   topk_ids, topk_w [S][T][k]; send_ids [S][cap_send][k] int32 out;
+ *   send_w [S][cap_send][k] float32 out; the rest as moe_dispatch_pack.
+ * Rows stay where moe_dispatch_pack puts them: partition p's rows from source
+ * s are [part_offsets[s][p], part_offsets[s][p+1]) in token order -- the
+ * page's block of rows per sender, without padding to the largest batch.
+ */
+moe_status_t moe_dispatch_pack_routed(const uint16_t *x, const int32_t *topk_ids,
+                                      const float *topk_w, int S, int T, int H, int k, int P,
+                                      const int32_t *token_slot, const int32_t *part_offsets,
+                                      int cap_send, uint16_t *send, int32_t *send_src,
+                                      int32_t *send_ids, float *send_w, uint32_t *dev_status,
+                                      cudaStream_t stream);
+
+/*
+ * Routed expert with the first combine stage (a2a-backends section 6.1: the
+ * routed expert kernel reads each row's ids and selects its experts itself;
+ * section 7.1: it already produces the weighted sum per GPU, which the home
+ * side then adds up with moe_combine_stage2).  Stand-in expert (tests and
+ * benchmarks, like moe_expert_scale): y_j = bf16(x * scale[e_j]), or x when
+ * scale is NULL.  For every row r of partition p's region of source s, p in
+ * the receiving set (recv_part, or all partitions if -1):
+ *   ret[s][r] = bf16_rne( sum over ascending j with send_ids[s][r][j] in
+ *               partition p of send_w[s][r][j] * y_j ), fp32 fused multiply-adds
+ * -- the same bytes as moe_expert_scale + moe_combine_stage1 over the
+ * permuted rows.  Rows outside the receiving regions are not written; ids >= E
+ * are skipped and flag MOE_ERR_BAD_EXPERT_ID.
+ *   send [S][cap_send][H] bf16; send_ids, send_w [S][cap_send][k];
+ *   part_offsets [S][P+1]; scale [E] float32 or NULL; ret [S][cap_send][H] bf16 out.
+ *   T: tokens per source (a partition's region of one source holds at most T
+ *   rows, which bounds the work when one partition receives).
+ */
+moe_status_t moe_routed_expert_stage1(const uint16_t *send, const int32_t *send_ids,
+                                      const float *send_w, const int32_t *part_offsets, int S,
+                                      int T, int cap_send, int k, int E, int P, int H,
+                                      int recv_part, const float *scale, uint16_t *ret,
+                                      uint32_t *dev_status, cudaStream_t stream);
+
+/*
  * Expert placement by load with redundant copies of the hot experts ("Beyond
  * One GPU", section 6, "The fix: place experts by load, and copy the hot
  * ones").  HOST function: all pointers are host memory; no GPU is used.
@@ -363,7 +409,9 @@ moe_status_t moe_combine(const uint16_t *y, int y_rows, const int32_t *pair_row,
  *   by pair_row); ret [S][cap_send][H] bf16 (the send layout).  Rows of ret
  *   without such a slot are not written.  pair_row >= y_rows is skipped and
  *   flags MOE_ERR_INVALID_ARG.
- * moe_combine_stage2 (home side):
+ * moe_combine_stage2 (home side): over the partitions p of the receiving set
+ * (recv_part, or all if -1 -- with one receiving partition only its rows come
+ * back, so the result is that partition's partial combine):
  *   out[s][t] = bf16_rne( sum over p ascending with 0 <= token_slot < cap_send
  *               of float(ret[s][token_slot[s][t][p]]) ), fp32 adds; +0 if none.
  * Slots >= cap_send flag MOE_ERR_CAPACITY in both stages.
@@ -374,8 +422,8 @@ moe_status_t moe_combine_stage1(const uint16_t *y, int y_rows, const int32_t *pa
                                 int H, int recv_part, int cap_send, uint16_t *ret,
                                 uint32_t *dev_status, cudaStream_t stream);
 moe_status_t moe_combine_stage2(const uint16_t *ret, const int32_t *token_slot, int S, int T,
-                                int P, int H, int cap_send, uint16_t *out, uint32_t *dev_status,
-                                cudaStream_t stream);
+                                int P, int H, int recv_part, int cap_send, uint16_t *out,
+                                uint32_t *dev_status, cudaStream_t stream);
 
 /*
  * Stand-in expert for tests and benchmarks -- NOT a step of the method (the
