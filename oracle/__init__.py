@@ -77,6 +77,15 @@ def _load():
             lib.oracle_expert_scale_mxfp8.argtypes = [P, P, P, i32, i32, i64, P]
             lib.oracle_plan_placement.argtypes = [P, i32, i32, i32, P, P, P, P]
             lib.oracle_map_replicas.argtypes = [P, i32, i64, i32, i32, P, P, i32, P]
+            lib.oracle_e2m1_from_double.argtypes = [ctypes.c_double]
+            lib.oracle_e2m1_from_double.restype = ctypes.c_uint8
+            lib.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_to_double.restype = ctypes.c_double
+            lib.oracle_quantize_nvfp4_block.argtypes = [P, ctypes.c_float, P, P]
+            lib.oracle_quantize_nvfp4_block.restype = None
+            lib.oracle_dispatch_pack_nvfp4.argtypes = [P, i32, i64, i32, i32, ctypes.c_float, P, i64,
+                                                       P, P, P]
+            lib.oracle_expert_scale_nvfp4.argtypes = [P, P, P, i32, i32, ctypes.c_float, i64, P]
             lib.oracle_dispatch_pack_routed.argtypes = [P, P, P, i32, i64, i32, i32, i32, P, i64,
                                                         P, P, P, P, P]
             lib.oracle_routed_expert_stage1.argtypes = [P, P, P, P, i32, i64, i32, i32, i32, i32,
@@ -88,7 +97,8 @@ def _load():
                       "oracle_combine_stage2", "oracle_dispatch_pack_mxfp8",
                       "oracle_expert_scale_mxfp8", "oracle_plan_placement",
                       "oracle_map_replicas", "oracle_dispatch_pack_routed",
-                      "oracle_routed_expert_stage1"):
+                      "oracle_routed_expert_stage1", "oracle_dispatch_pack_nvfp4",
+                      "oracle_expert_scale_nvfp4"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -432,6 +442,64 @@ def routed_expert_stage1(send: np.ndarray, send_ids: np.ndarray, send_w: np.ndar
                                                None if sc is None else _p(sc), _p(ret), _p(st)),
            "routed_expert_stage1")
     return ret, int(st[0])
+
+
+def e2m1_from_double(v: float) -> int:
+    return int(_load().oracle_e2m1_from_double(float(v)))
+
+
+def e2m1_to_double(c: int) -> float:
+    return float(_load().oracle_e2m1_to_double(int(c)))
+
+
+def quantize_nvfp4(row: np.ndarray, g: float = 1.0):
+    """bf16 bits [H] (H % 16 == 0), tensor scale g -> (codes uint8 [H/2], two per byte,
+    scales uint8 [H/16])."""
+    row = np.ascontiguousarray(row, dtype=np.uint16)
+    H = row.shape[0]
+    codes = np.empty(H // 2, np.uint8)
+    scales = np.empty(H // 16, np.uint8)
+    lib = _load()
+    for b in range(H // 16):
+        lib.oracle_quantize_nvfp4_block(
+            ctypes.c_void_p(row.ctypes.data + 32 * b), float(g),
+            ctypes.c_void_p(codes.ctypes.data + 8 * b),
+            ctypes.c_void_p(scales.ctypes.data + b))
+    return codes, scales
+
+
+def dispatch_pack_nvfp4(x: np.ndarray, token_slot: np.ndarray, cap_send: int, g: float = 1.0,
+                        send_q: np.ndarray | None = None):
+    """Pack with NVFP4 records -> (send_q uint8 [S, cap, H/2 + H/16], send_src, status)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    token_slot = np.ascontiguousarray(token_slot, dtype=np.int32)
+    S, T, H = x.shape
+    P = token_slot.shape[2]
+    if send_q is None:
+        send_q = np.zeros((S, cap_send, H // 2 + H // 16), np.uint8)
+    send_src = np.empty((S, cap_send), np.int32)
+    st = np.zeros(1, np.uint32)
+    _check(_load().oracle_dispatch_pack_nvfp4(_p(x), S, T, H, P, float(g), _p(token_slot), cap_send,
+                                              _p(send_q), _p(send_src), _p(st)),
+           "dispatch_pack_nvfp4")
+    return send_q, send_src, int(st[0])
+
+
+def expert_scale_nvfp4(recv_q: np.ndarray, expert_offsets: np.ndarray, scale: np.ndarray,
+                       g: float = 1.0, y: np.ndarray | None = None) -> np.ndarray:
+    """Dequantizing stand-in expert: recv_q uint8 [cap, H/2 + H/16] -> y bf16 bits [cap, H]."""
+    recv_q = np.ascontiguousarray(recv_q, dtype=np.uint8)
+    cap, rb = recv_q.shape
+    H = rb * 16 // 9
+    assert H // 2 + H // 16 == rb
+    E = expert_offsets.shape[0] - 1
+    if y is None:
+        y = np.zeros((cap, H), np.uint16)
+    _check(_load().oracle_expert_scale_nvfp4(_p(recv_q), _p(np.ascontiguousarray(expert_offsets, np.int32)),
+                                             _p(np.ascontiguousarray(scale, np.float32)), E, H, float(g),
+                                             cap, _p(y)),
+           "expert_scale_nvfp4")
+    return y
 
 
 def run_path(x: np.ndarray, logits: np.ndarray, E: int, k: int, P: int, scales: np.ndarray | None,

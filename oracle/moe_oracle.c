@@ -1022,3 +1022,132 @@ int oracle_routed_expert_stage1(const uint16_t *send, const int32_t *send_ids, c
     free(acc);
     return 0;
 }
+
+/* --------------------------------------------- NVFP4 rows, [a2a] 7.2 -- */
+
+/*
+ * E2M1 (4 bits: sign, 2 exponent bits with bias 1, 1 mantissa bit): the
+ * magnitudes 0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6.  Encoding rounds to the
+ * nearest magnitude, ties to the even code (mantissa bit 0), magnitudes
+ * above 6 become 6, and the sign is kept (also for zero).
+ */
+static const double oracle_e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double oracle_e2m1_to_double(uint8_t c)
+{
+    const double m = oracle_e2m1_mag[c & 7];
+    return (c & 8) ? -m : m;
+}
+
+uint8_t oracle_e2m1_from_double(double v)
+{
+    const uint8_t sign = signbit(v) ? 8u : 0u;
+    double a = fabs(v);
+    if (a >= 6.0)
+        return sign | 7u;
+    int best = 0;
+    for (int c = 1; c < 8; c++) {
+        const double d = fabs(oracle_e2m1_mag[c] - a), db = fabs(oracle_e2m1_mag[best] - a);
+        if (d < db || (d == db && (c & 1) == 0))
+            best = c;
+    }
+    return sign | (uint8_t)best;
+}
+
+/*
+ * One NVFP4 block of 16 bf16 values ([a2a] 7.2: a one-byte scale for every 16
+ * values).  Reading (the page gives only the size): NVIDIA's NVFP4 -- E2M1
+ * values, an E4M3 scale per 16 values and one fp32 scale g for the whole
+ * tensor (given by the caller; it is not part of a row):
+ *   s = e4m3( fp32(amax / fp32(6 g)) ),   code_i = e2m1( fp32(v_i / fp32(s g)) )
+ * and all codes 0 when s is 0.  Every product and quotient is taken in fp32:
+ * they decide integer codes, and fp32 is the precision of the GPU kernel.
+ * Codes are packed two per byte, element 2i in the low nibble.
+ */
+void oracle_quantize_nvfp4_block(const uint16_t *v, float g, uint8_t *codes, uint8_t *scale)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 16; i++) {
+        const float a = (float)fabs(oracle_bf16_to_double(v[i]));
+        if (a > amax)
+            amax = a;
+    }
+    const float d = 6.0f * g;
+    const float t = amax / d;
+    *scale = oracle_e4m3_from_double((double)t);
+    const float sg = (float)oracle_e4m3_to_double(*scale) * g;
+    for (int i = 0; i < 8; i++) {
+        uint8_t c[2];
+        for (int h = 0; h < 2; h++) {
+            const float x = (float)oracle_bf16_to_double(v[2 * i + h]);
+            c[h] = sg == 0.0f ? 0u : oracle_e2m1_from_double((double)(x / sg));
+        }
+        codes[i] = (uint8_t)(c[0] | (c[1] << 4));
+    }
+}
+
+/*
+ * Pack with NVFP4 records ([a2a] 7.2): a record is H/2 bytes of codes
+ * followed by H/16 bytes of block scales -- 2,880 bytes for H = 5,120, the
+ * page's NVFP4 row.  Placement, send_src and capacity as oracle_dispatch_pack.
+ * H must be a multiple of 16.
+ */
+int oracle_dispatch_pack_nvfp4(const uint16_t *x, int S, int64_t T, int H, int P, float g,
+                               const int32_t *token_slot, int64_t cap_send, uint8_t *send_q,
+                               int32_t *send_src, uint32_t *status)
+{
+    if (H % 16 != 0)
+        return -1;
+    const int nb = H / 16;
+    const int64_t rb = (int64_t)H / 2 + nb;
+    uint8_t *q = (uint8_t *)malloc((size_t)rb);
+    if (!q)
+        return -2;
+    for (int s = 0; s < S; s++) {
+        for (int64_t r = 0; r < cap_send; r++)
+            send_src[(int64_t)s * cap_send + r] = -1;
+        for (int64_t t = 0; t < T; t++) {
+            const uint16_t *row = x + ((int64_t)s * T + t) * H;
+            for (int b = 0; b < nb; b++)
+                oracle_quantize_nvfp4_block(row + 16 * b, g, q + 8 * b, q + H / 2 + b);
+            for (int p = 0; p < P; p++) {
+                int32_t slot = token_slot[((int64_t)s * T + t) * P + p];
+                if (slot < 0)
+                    continue;
+                if (slot >= cap_send) {
+                    *status |= ORC_BIT_CAPACITY;
+                    continue;
+                }
+                memcpy(send_q + ((int64_t)s * cap_send + slot) * rb, q, (size_t)rb);
+                send_src[(int64_t)s * cap_send + slot] = (int32_t)t;
+            }
+        }
+    }
+    free(q);
+    return 0;
+}
+
+/*
+ * Stand-in expert on NVFP4 records (as oracle_expert_scale_mxfp8):
+ *   y[r][h] = bf16( s_e * e2m1(code[r][h]) * e4m3(scale[r][h/16]) * g )
+ */
+int oracle_expert_scale_nvfp4(const uint8_t *recv_q, const int32_t *expert_offsets,
+                              const float *scale, int E, int H, float g, int64_t cap_recv,
+                              uint16_t *y)
+{
+    if (H % 16 != 0)
+        return -1;
+    const int64_t rb = (int64_t)H / 2 + H / 16;
+    for (int e = 0; e < E; e++) {
+        for (int64_t r = expert_offsets[e]; r < expert_offsets[e + 1] && r < cap_recv; r++) {
+            const uint8_t *rec = recv_q + r * rb;
+            for (int h = 0; h < H; h++) {
+                const uint8_t c = (uint8_t)((rec[h / 2] >> (4 * (h & 1))) & 0xF);
+                const double v = oracle_e2m1_to_double(c) * oracle_e4m3_to_double(rec[H / 2 + h / 16]) *
+                                  (double)g;
+                y[r * H + h] = oracle_bf16_from_double(v * (double)scale[e]);
+            }
+        }
+    }
+    return 0;
+}

@@ -908,3 +908,97 @@ def test_routed_stage1_skips_empty_and_flags_bad_ids():
     assert st == oracle.BIT_BAD_ID
     used = int(lay["part_offsets"][0, -1])
     assert np.all(ret[0, used:] == 0x2468)                 # empty rows are not written
+
+
+# ------------------------------------------------- NVFP4 rows (a2a 7.2) --
+
+def test_e2m1_table_ties_and_saturation():
+    # E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit -> 0, 0.5, 1, 1.5, 2, 3, 4, 6
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert [oracle.e2m1_to_double(c) for c in range(8)] == mags
+    assert [oracle.e2m1_to_double(c + 8) for c in range(8)] == [-m for m in mags]
+    for c in range(16):
+        assert oracle.e2m1_from_double(oracle.e2m1_to_double(c)) == c     # -0 keeps its sign
+    # midpoints go to the code with mantissa bit 0
+    ties = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0}
+    for v, want in ties.items():
+        assert oracle.e2m1_to_double(oracle.e2m1_from_double(v)) == want
+        assert oracle.e2m1_to_double(oracle.e2m1_from_double(-v)) == -want
+    for v in (6.0, 6.5, 7.0, 1e30):
+        assert oracle.e2m1_from_double(v) == 7 and oracle.e2m1_from_double(-v) == 15
+    assert oracle.e2m1_from_double(0.2) == 0 and oracle.e2m1_from_double(-0.2) == 8
+
+
+def test_nvfp4_row_size_and_hand_block():
+    g = _golden("quantized_row_bytes.json")
+    H = g["hidden"]
+    codes, scales = oracle.quantize_nvfp4(ms.gen_x(ms.workload("prefill"), T=1)[0, 0])
+    assert codes.nbytes + scales.nbytes == g["nvfp4_bytes"]                # 1 B scale per 16
+    ts = np.zeros((1, 1, 1), np.int32)
+    q, _, _ = oracle.dispatch_pack_nvfp4(ms.gen_x(ms.workload("prefill"), T=1), ts, 1)
+    assert q.shape == (1, 1, g["nvfp4_bytes"])
+    # a block with max |v| = 6: s = e4m3(6/6) = 1.0 (byte 0x38), codes are e2m1(v)
+    v = np.zeros(16, np.float32)
+    v[:8] = [6.0, 3.0, -1.5, 0.25, 0.75, -5.0, 0.5, 2.5]
+    c, s = oracle.quantize_nvfp4(ms.bf16_bits_from_f32(v))
+    assert s.tolist() == [0x38]
+    nib = [(c[i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+    assert [oracle.e2m1_to_double(n) for n in nib[:8]] == [6.0, 3.0, -1.5, 0.0, 1.0, -4.0, 0.5, 2.0]
+    assert nib[8:] == [0] * 8
+    # max |v| = 12: s = 2 (byte 0x40), 9 -> 4.5 -> 4 (tie at 5? no: 4.5 is between 4 and 6 -> 4)
+    v = np.zeros(16, np.float32)
+    v[:3] = [12.0, 9.0, -0.5]
+    c, s = oracle.quantize_nvfp4(ms.bf16_bits_from_f32(v))
+    assert s.tolist() == [0x40]
+    nib = [(c[i // 2] >> (4 * (i % 2))) & 0xF for i in range(3)]
+    assert [oracle.e2m1_to_double(n) * 2.0 for n in nib] == [12.0, 8.0, -0.0]
+    # an all-zero block: scale byte 0 and zero codes
+    c, s = oracle.quantize_nvfp4(np.zeros(16, np.uint16))
+    assert s.tolist() == [0] and c.tolist() == [0] * 8
+
+
+@pytest.mark.parametrize("g", [1.0, 2.0 ** -12, 0.37])
+def test_nvfp4_error_bound(g):
+    rng = np.random.default_rng(21)
+    x = ms.bf16_bits_from_f32((rng.standard_normal((64, 256)) * np.exp(rng.uniform(-6, 6, (64, 1))))
+                              .astype(np.float32))
+    flushed = 0
+    for t in range(64):
+        codes, scales = oracle.quantize_nvfp4(x[t], g)
+        vals = ms.f32_from_bf16_bits(x[t]).astype(np.float64)
+        for b in range(16):
+            sg = oracle.e4m3_to_double(int(scales[b])) * g
+            blk = vals[16 * b:16 * (b + 1)]
+            nib = [(codes[8 * b + i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+            deq = np.array([oracle.e2m1_to_double(n) for n in nib]) * sg
+            if sg == 0:
+                # the block scale rounds to zero only below half the smallest E4M3 value
+                assert np.abs(blk).max() / (6 * g) <= 2.0 ** -10 and np.all(deq == 0)
+                flushed += 1
+                continue
+            q = np.abs(blk) / sg
+            # half the E2M1 spacing (0.25 below 2, q/4 above), plus what saturation at 6 cuts
+            bound = sg * (np.maximum(0.25, q / 4) + np.maximum(0.0, q - 6)) * (1 + 1e-6)
+            assert np.all(np.abs(deq - blk) <= bound)
+    if g == 1.0:
+        assert flushed > 0          # the tensor scale is what keeps small blocks alive
+    if g == 2.0 ** -12:
+        assert flushed == 0
+
+
+def test_expert_scale_nvfp4_reduces_to_bf16_expert():
+    rng = np.random.default_rng(4)
+    H, R = 64, 30
+    mags = np.array([0.5, 1.0, 1.5, 2.0, 3.0, 4.0])
+    v = rng.choice(mags, size=(R, H)) * np.where(rng.random((R, H)) < 0.5, -1, 1)
+    v[:, ::16] = 6.0                                       # amax 6 per block: s = 1 exactly
+    bits = ms.bf16_bits_from_f32(v.astype(np.float32))
+    rec = np.stack([np.concatenate(oracle.quantize_nvfp4(r)) for r in bits])
+    assert np.all(rec[:, H // 2:] == 0x38)
+    eo = np.array([0, 11, R], np.int32)
+    s = np.array([0.75, 2.5], np.float32)
+    assert np.array_equal(oracle.expert_scale_nvfp4(rec, eo, s), oracle.expert_scale(bits, eo, s))
+    # the same values at a tensor scale of 2^-3: scales step up by 3 binades, output unchanged
+    rec3 = np.stack([np.concatenate(oracle.quantize_nvfp4(r, 0.125)) for r in bits])
+    assert np.all(rec3[:, H // 2:] == 0x38 + (3 << 3))
+    assert np.array_equal(oracle.expert_scale_nvfp4(rec3, eo, s, g=0.125), oracle.expert_scale(bits, eo, s))
