@@ -41,6 +41,7 @@ DOMINANT = "k_perm_copy"
 # step) and the key of its algorithmic bytes per launch in algorithmic_bytes().
 DOMINANT_BY_VARIANT = {"two_stage": ("k_combine_stage1", "stage1"),
                        "mxfp8": ("k_expert_scale_mxfp8", "expert"),
+                       "nvfp4": ("k_expert_scale_nvfp4", "expert"),
                        "routed": ("k_routed_stage1", "stage1")}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_perm_copy
 # launch in the prefill pipeline, from an ncu capture with the L2 left as the
@@ -52,22 +53,22 @@ DOMINANT_TRAFFIC = {"prefill": 142.5e6 + 252.3e6}
 # ------------------------------------------------------------ byte model --
 
 def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_stage=False,
-                      mxfp8=False, routed=False):
+                      mxfp8=False, routed=False, nvfp4=False):
     """Bytes each call must read + write at minimum.
 
     copies: rows packed (sum of part_offsets[s][P]); copies_recv: packed rows
     bound for the receiving partition(s); pairs_recv: permuted pair rows.
     two_stage: the combine pre-adds per (token, partition) slot (copies_recv
     rows written and read back) before the per-token sum.
-    mxfp8: packed and permuted rows are MXFP8 records of H + H/32 bytes, and
-    the stand-in expert that dequantizes them (pair records in, bf16 rows out)
-    is part of the step.
+    mxfp8 / nvfp4: packed and permuted rows are MXFP8 records of H + H/32
+    bytes (NVFP4: H/2 + H/16), and the stand-in expert that dequantizes them
+    (pair records in, bf16 rows out) is part of the step.
     routed: rows carry the token's ids and weights (8 bytes per choice), nothing
     is permuted, the routed expert pre-adds straight from the received rows
     (copies_recv rows in and out) and the home side sums them (stage 2).
     """
     NT = S * T
-    R = H + H // 32 if mxfp8 else 2 * H          # bytes of one moved row
+    R = H + H // 32 if mxfp8 else (H // 2 + H // 16 if nvfp4 else 2 * H)   # bytes of a moved row
     b = {
         "route": NT * E * 4 + NT * k * 8,
         "layout": NT * k * 4 + NT * P * 4 + S * (E + 2 * P + 1) * 4,
@@ -75,7 +76,7 @@ def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_sta
         "permute": copies_recv * R + pairs_recv * R + NT * k * 8,
         "combine": pairs_recv * H * 2 + NT * k * 8 + NT * H * 2,
     }
-    if mxfp8:
+    if mxfp8 or nvfp4:
         b["expert"] = pairs_recv * R + pairs_recv * H * 2
     if two_stage:
         b["combine"] = (pairs_recv * H * 2 + NT * k * 12 + copies_recv * H * 2      # stage 1
@@ -297,6 +298,8 @@ def workload_config(w, l2, variant="contiguous"):
     scope = "route+layout+pack+permute+combine"
     if variant == "routed":
         scope = "route+layout+pack(rows with ids and weights)+routed pre-add+home sum"
+    if variant == "nvfp4":
+        scope = "route+layout+pack(NVFP4 records)+permute+dequantizing stand-in expert+combine"
     if variant == "mxfp8":
         scope = "route+layout+pack(MXFP8 records)+permute+dequantizing stand-in expert+combine"
     return {"workload": f"{w.name}: S={w.S} T={w.T} H={w.H} bf16, E={w.E} top-{w.k}, "
@@ -313,6 +316,7 @@ VARIANTS = {
     "masked": {"layout": "masked"},
     "two_stage": {"combine": "two_stage"},
     "mxfp8": {"quant": "mxfp8"},
+    "nvfp4": {"quant": "nvfp4"},
     "placed": {},          # placement planned from another batch; see plan_for()
     "routed": {"layout": "routed"},
 }
@@ -442,7 +446,8 @@ def run_ours(args, world, rank, local):
             pairs_recv = int((path.pair_row >= 0).sum().item())
         b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv,
                               two_stage=(args.variant == "two_stage"),
-                              mxfp8=(args.variant == "mxfp8"), routed=(args.variant == "routed"))
+                              mxfp8=(args.variant == "mxfp8"), routed=(args.variant == "routed"),
+                              nvfp4=(args.variant == "nvfp4"))
         dom_name, dom_key = DOMINANT_BY_VARIANT.get(args.variant, (DOMINANT, "perm_copy"))
         if placement_info is not None:
             # pairs per partition on the timed batch: contiguous blocks vs the placement
@@ -646,7 +651,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(job_ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if args.variant != "mxfp8" else "bf16/e4m3",
+        "dtype": {"mxfp8": "bf16/e4m3", "nvfp4": "bf16/e2m1"}.get(args.variant, "bf16"),
         "data": "synthetic",
         "config": workload_config(w, "flushed before every timed step: 1 GiB write, then 256 MiB read (clean lines)",
                                   args.variant),
@@ -705,7 +710,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--variant", default="contiguous", choices=sorted(VARIANTS),
                     help="contiguous runs + one-stage combine (default), masked blocks, a "
-                         "two-stage combine, MXFP8 rows, experts placed by load with copies, or "
+                         "two-stage combine, MXFP8 or NVFP4 rows, experts placed by load with copies, or "
                          "routed rows (ids and weights with each row, no permute)")
     ap.add_argument("--spare", type=int, default=4,
                     help="spare copy slots per partition for --variant placed")

@@ -30,7 +30,8 @@ __all__ = [
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
     "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
     "moe_plan_placement", "moe_workspace_bytes_mapped", "moe_dispatch_layout_mapped", "Placement",
-    "moe_dispatch_pack_routed", "moe_routed_expert_stage1", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "moe_dispatch_pack_routed", "moe_routed_expert_stage1", "moe_dispatch_pack_nvfp4",
+    "moe_expert_scale_nvfp4", "nvfp4_record_bytes", "mxfp8_record_bytes", "MoePath", "trace_enable", "trace_disable", "trace_reset",
     "trace_records",
 ]
 
@@ -103,6 +104,10 @@ def load_library() -> ctypes.CDLL:
                                          ctypes.c_int),
             "moe_expert_scale_mxfp8": ([P, P, P, i32, i32, i32, P, P], ctypes.c_int),
             "moe_plan_placement": ([P, i32, i32, i32, P, P, P, P], ctypes.c_int),
+            "moe_dispatch_pack_nvfp4": ([P, i32, i32, i32, i32, ctypes.c_float, P, P, i32, P, P, P,
+                                         P], ctypes.c_int),
+            "moe_expert_scale_nvfp4": ([P, P, P, i32, i32, ctypes.c_float, i32, P, P],
+                                       ctypes.c_int),
             "moe_dispatch_pack_routed": ([P, P, P, i32, i32, i32, i32, i32, P, P, i32, P, P, P, P,
                                           P, P], ctypes.c_int),
             "moe_routed_expert_stage1": ([P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P, P,
@@ -212,6 +217,42 @@ def moe_dispatch_pack(x, token_slot, part_offsets, send, send_src, dev_status=No
 def mxfp8_record_bytes(H: int) -> int:
     """Bytes of one MXFP8 row record: H E4M3 codes, then H/32 E8M0 block scales."""
     return H + H // 32
+
+
+def nvfp4_record_bytes(H: int) -> int:
+    """Bytes of one NVFP4 row record: H/2 bytes of E2M1 codes, then H/16 E4M3 scales."""
+    return H // 2 + H // 16
+
+
+def moe_dispatch_pack_nvfp4(x, token_slot, part_offsets, send_q, send_src, global_scale=1.0,
+                            dev_status=None, stream=None):
+    """x bf16 [S,T,H] -> send_q uint8 [S,cap_send,H/2+H/16] NVFP4 records, send_src [S,cap_send]."""
+    lib = load_library()
+    S, T, H = x.shape
+    P = token_slot.shape[2]
+    cap_send = send_q.shape[1]
+    if send_q.shape[2] != nvfp4_record_bytes(H):
+        raise ValueError(f"send_q rows must be {nvfp4_record_bytes(H)} bytes for H={H}")
+    _check(lib.moe_dispatch_pack_nvfp4(
+        _dev(x, "x", _BF16_TYPES, 3), S, T, H, P, float(global_scale),
+        _dev(token_slot, "token_slot", (torch.int32,), 3),
+        _dev(part_offsets, "part_offsets", (torch.int32,)), cap_send,
+        _dev(send_q, "send_q", (torch.uint8,), 3), _dev(send_src, "send_src", (torch.int32,)),
+        _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_expert_scale_nvfp4(recv_q, expert_offsets, scale, y, global_scale=1.0, stream=None):
+    """Stand-in expert on NVFP4 records: y[r] = bf16(scale[e] * dequant(recv_q[r]))."""
+    lib = load_library()
+    cap_recv, H = y.shape
+    if tuple(recv_q.shape) != (cap_recv, nvfp4_record_bytes(H)):
+        raise ValueError("recv_q must be [cap_recv, H/2 + H/16] uint8")
+    E = scale.shape[0]
+    _check(lib.moe_expert_scale_nvfp4(
+        _dev(recv_q, "recv_q", (torch.uint8,), 2),
+        _dev(expert_offsets, "expert_offsets", (torch.int32,)),
+        _dev(scale, "scale", (torch.float32,)), E, H, float(global_scale), cap_recv,
+        _dev(y, "y", _BF16_TYPES, 2), _stream(stream)))
 
 
 def moe_dispatch_pack_mxfp8(x, token_slot, part_offsets, send_q, send_src, dev_status=None,
@@ -465,14 +506,15 @@ class MoePath:
 
     def __init__(self, S, T, H, E, k, P, recv_part=-1, align=1, cap_send=None, cap_recv=None,
                  device="cuda", layout="contiguous", block_rows=None, combine="single",
-                 quant="none", placement: "Placement | None" = None):
+                 quant="none", placement: "Placement | None" = None, nvfp4_scale: float = 1.0):
         """layout: "contiguous" (expert runs, moe_permute_to_experts), "masked" (one
         block of block_rows rows per expert, moe_permute_to_experts_masked) or "routed"
         (no permute: rows carry their ids and weights, moe_dispatch_pack_routed, and
         moe_routed_expert_stage1 + moe_combine_stage2 replace the expert and combine).
         combine: "single" (moe_combine) or "two_stage" (moe_combine_stage1 + stage2).
-        quant: "none" (bf16 rows) or "mxfp8" (rows sent as MXFP8 records; the
-        receiver's stand-in expert dequantizes them, so every step runs it).
+        quant: "none" (bf16 rows), "mxfp8" or "nvfp4" (rows sent as quantized records;
+        the receiver's stand-in expert dequantizes them, so every step runs it);
+        nvfp4_scale is the NVFP4 per-tensor scale.
         placement: a Placement (moe_plan_placement) -- the layout then maps each
         pair to a physical expert slot and everything after it works on the
         P*Lp physical experts; None keeps expert e in slot e."""
@@ -482,10 +524,14 @@ class MoePath:
             if quant != "none":
                 raise ValueError("the routed layout carries bf16 rows")
             combine = "two_stage"          # the routed expert produces stage 1 itself
-        if quant not in ("none", "mxfp8"):
-            raise ValueError("quant must be none|mxfp8")
+        if quant not in ("none", "mxfp8", "nvfp4"):
+            raise ValueError("quant must be none|mxfp8|nvfp4")
         if quant == "mxfp8" and (H % 512 != 0 or layout != "contiguous"):
             raise ValueError("mxfp8 rows need H % 512 == 0 and the contiguous layout")
+        if quant == "nvfp4" and (H % 256 != 0 or layout != "contiguous"):
+            raise ValueError("nvfp4 rows need H % 256 == 0 and the contiguous layout")
+        self.quantized = quant != "none"
+        self.nvfp4_scale = float(nvfp4_scale)
         if placement is not None and (placement.E != E or placement.P != P):
             raise ValueError("the placement is for another E or P")
         self.S, self.T, self.H, self.E, self.k, self.P = S, T, H, E, k, P
@@ -495,7 +541,7 @@ class MoePath:
         self.recv_part, self.align = recv_part, align
         self.layout, self.combine_mode, self.quant = layout, combine, quant
         # row width as the permute sees it: bf16 slots per row
-        self.row_bytes = mxfp8_record_bytes(H) if quant == "mxfp8" else 2 * H
+        self.row_bytes = {"mxfp8": mxfp8_record_bytes(H), "nvfp4": nvfp4_record_bytes(H)}.get(quant, 2 * H)
         self.Hp = self.row_bytes // 2
         self.cap_send = T * min(k, P) if cap_send is None else cap_send
         Ep = self.Ep
@@ -524,8 +570,8 @@ class MoePath:
         self.part_counts = torch.empty((S, P), **i32)
         self.part_offsets = torch.empty((S, P + 1), **i32)
         self.token_slot = torch.empty((S, T, P), **i32)
-        row_dt = torch.uint8 if quant == "mxfp8" else torch.bfloat16
-        row_w = self.row_bytes if quant == "mxfp8" else H
+        row_dt = torch.uint8 if self.quantized else torch.bfloat16
+        row_w = self.row_bytes if self.quantized else H
         self.send = torch.empty((S, self.cap_send, row_w), dtype=row_dt, device=d)
         self.send_src = torch.empty((S, self.cap_send), **i32)
         self.recv = torch.empty((self.cap_recv, row_w), dtype=row_dt, device=d)
@@ -545,7 +591,7 @@ class MoePath:
             self.send_ids = torch.empty((S, self.cap_send, k), **i32)
             self.send_w = torch.empty((S, self.cap_send, k), dtype=torch.float32, device=d)
         self.y = None
-        if quant == "mxfp8":
+        if self.quantized:
             self.y = torch.empty((self.cap_recv, H), dtype=torch.bfloat16, device=d)
             self.unit_scale = torch.ones((Ep,), dtype=torch.float32, device=d)
 
@@ -605,6 +651,11 @@ class MoePath:
                 ptr(x, "x", _BF16_TYPES), S, T, H, P, vp(self.token_slot.data_ptr()),
                 vp(self.part_offsets.data_ptr()), self.cap_send, vp(self.send.data_ptr()),
                 vp(self.send_src.data_ptr()), stp, st)))
+        elif self.quant == "nvfp4":
+            calls.append((lib.moe_dispatch_pack_nvfp4, (
+                ptr(x, "x", _BF16_TYPES), S, T, H, P, self.nvfp4_scale,
+                vp(self.token_slot.data_ptr()), vp(self.part_offsets.data_ptr()), self.cap_send,
+                vp(self.send.data_ptr()), vp(self.send_src.data_ptr()), stp, st)))
         else:
             calls.append((lib.moe_dispatch_pack, (
                 ptr(x, "x", _BF16_TYPES), S, T, H, P, vp(self.token_slot.data_ptr()),
@@ -627,13 +678,19 @@ class MoePath:
                 vp(self.expert_offsets.data_ptr()), vp(self.pair_row.data_ptr()),
                 vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st)))
         y = self.recv
-        if self.quant == "mxfp8":
+        if self.quantized:
             # the bound call keeps a pointer: hold the per-slot scales on the path
             self._bound_scale = self.unit_scale if scale is None else self.slot_scale(scale)
-            calls.append((lib.moe_expert_scale_mxfp8, (
-                vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()),
-                ptr(self._bound_scale, "scale", (torch.float32,)), Ep, H, self.cap_recv,
-                vp(self.y.data_ptr()), st)))
+            if self.quant == "mxfp8":
+                calls.append((lib.moe_expert_scale_mxfp8, (
+                    vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()),
+                    ptr(self._bound_scale, "scale", (torch.float32,)), Ep, H, self.cap_recv,
+                    vp(self.y.data_ptr()), st)))
+            else:
+                calls.append((lib.moe_expert_scale_nvfp4, (
+                    vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()),
+                    ptr(self._bound_scale, "scale", (torch.float32,)), Ep, H, self.nvfp4_scale,
+                    self.cap_recv, vp(self.y.data_ptr()), st)))
             y = self.y
         if self.combine_mode == "two_stage":
             calls.append((lib.moe_combine_stage1, (
@@ -678,9 +735,13 @@ class MoePath:
                                      self.part_offsets, self.send, self.send_src, self.send_ids,
                                      self.send_w, self.dev_status, stream)
             return
-        if self.quant == "mxfp8":
-            moe_dispatch_pack_mxfp8(x, self.token_slot, self.part_offsets, self.send,
-                                    self.send_src, self.dev_status, stream)
+        if self.quantized:
+            if self.quant == "mxfp8":
+                moe_dispatch_pack_mxfp8(x, self.token_slot, self.part_offsets, self.send,
+                                        self.send_src, self.dev_status, stream)
+            else:
+                moe_dispatch_pack_nvfp4(x, self.token_slot, self.part_offsets, self.send,
+                                        self.send_src, self.nvfp4_scale, self.dev_status, stream)
             moe_permute_to_experts(self.send.view(torch.bfloat16), self.token_slot, self.phys_ids,
                                    self.expert_counts, self.expert_rank, self.Ep, self.recv_part,
                                    self.align, self.recv.view(torch.bfloat16),
@@ -712,9 +773,13 @@ class MoePath:
     def expert(self, scale, stream=None):
         if self.layout != "contiguous":
             raise ValueError("the stand-in expert reads contiguous expert runs")
-        if self.quant == "mxfp8":
+        if self.quantized:
             sc = self.unit_scale if scale is None else self.slot_scale(scale)
-            moe_expert_scale_mxfp8(self.recv, self.expert_offsets, sc, self.y, stream)
+            if self.quant == "mxfp8":
+                moe_expert_scale_mxfp8(self.recv, self.expert_offsets, sc, self.y, stream)
+            else:
+                moe_expert_scale_nvfp4(self.recv, self.expert_offsets, sc, self.y,
+                                       self.nvfp4_scale, stream)
             return self.y
         if self.y is None:
             self.y = torch.empty_like(self.recv)
@@ -723,7 +788,7 @@ class MoePath:
 
     def combine(self, y=None, stream=None):
         if y is None:
-            y = self.y if self.quant == "mxfp8" else self.recv
+            y = self.y if self.quantized else self.recv
         if self.combine_mode == "two_stage":
             moe_combine_stage1(y, self.pair_row, self.topk_w, self.phys_ids, self.token_slot,
                                self.Ep, self.recv_part, self.ret, self.dev_status, stream)
@@ -747,7 +812,7 @@ class MoePath:
         if self.layout == "routed":
             self.routed_combine(scale, stream)
             return self.out
-        y = self.expert(scale, stream) if scale is not None or self.quant == "mxfp8" else None
+        y = self.expert(scale, stream) if scale is not None or self.quantized else None
         self.combine(y, stream)
         return self.out
 
@@ -755,7 +820,7 @@ class MoePath:
         """Kernels one step enqueues: route 1, layout 2 (1 if T <= 256; twice that plus the
         replica map under a placement), pack 1, permute 2 (map + copy), stand-in expert 1
         (always with MXFP8 rows), combine 1 (2 when split into two stages)."""
-        with_expert = with_expert or self.quant == "mxfp8"
+        with_expert = with_expert or self.quantized
         mapped = self.placement is not None
         if self.layout == "routed":
             if self.T == 0:                # the two receive-side calls launch nothing

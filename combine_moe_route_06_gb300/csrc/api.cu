@@ -540,4 +540,47 @@ moe_status_t moe_routed_expert_stage1(const uint16_t *send, const int32_t *send_
                        __func__);
 }
 
+moe_status_t moe_dispatch_pack_nvfp4(const uint16_t *x, int S, int T, int H, int P,
+                                     float global_scale, const int32_t *token_slot,
+                                     const int32_t *part_offsets, int cap_send, uint8_t *send_q,
+                                     int32_t *send_src, uint32_t *dev_status, cudaStream_t stream)
+{
+    moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
+    REQUIRE(global_scale > 0.f && global_scale < 3.0e38f, "%s: global_scale must be positive and finite",
+            __func__);
+    REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(x, NT * H, 16);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(send_q, (int64_t)S * cap_send * (H / 2 + H / 16), 16);
+    REQUIRE_ARR(send_src, (int64_t)S * cap_send, 4);
+    REQUIRE_STATUS(dev_status);
+    return cuda_status(launch_dispatch_pack_nvfp4(x, S, T, H, P, global_scale, token_slot,
+                                                  part_offsets, cap_send, send_q, send_src,
+                                                  dev_status, stream),
+                       __func__);
+}
+
+moe_status_t moe_expert_scale_nvfp4(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                    const float *scale, int E, int H, float global_scale,
+                                    int cap_recv, uint16_t *y, cudaStream_t stream)
+{
+    REQUIRE(E >= 1 && E <= kMaxE, "%s: E=%d must be in [1, %d]", __func__, E, kMaxE);
+    REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
+    REQUIRE(global_scale > 0.f && global_scale < 3.0e38f, "%s: global_scale must be positive and finite",
+            __func__);
+    REQUIRE(cap_recv >= 0, "%s: cap_recv=%d must be >= 0", __func__, cap_recv);
+    REQUIRE_ARR(recv_q, (int64_t)cap_recv * (H / 2 + H / 16), 16);
+    REQUIRE_ARR(expert_offsets, E + 1, 4);
+    REQUIRE_ARR(scale, E, 4);
+    REQUIRE_ARR(y, (int64_t)cap_recv * H, 16);
+    return cuda_status(launch_expert_scale_nvfp4(recv_q, expert_offsets, scale, E, H, global_scale,
+                                                 cap_recv, y, stream),
+                       __func__);
+}
+
 }  // extern "C"

@@ -11,6 +11,7 @@
 // once to bf16 and stream the result out.
 #include <cuda_bf16.h>
 
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -530,6 +531,69 @@ __global__ void __launch_bounds__(256) k_expert_scale_mxfp8(
     }
 }
 
+// Stand-in expert on NVFP4 records (H/2 code bytes, then one E4M3 scale per
+// 16 values):  y = bf16( s_e * e2m1(code) * e4m3(scale) * g ).  The product
+// code * scale is exact in fp32; the two factors g and s_e are applied as one
+// fp32 product, so y may differ from the exactly rounded value by one bf16 unit.
+__global__ void __launch_bounds__(256) k_expert_scale_nvfp4(
+    const uint8_t *__restrict__ recv_q, const int32_t *__restrict__ expert_offsets,
+    const float *__restrict__ scale, int E, int V, float g, int cap_recv, int4 *__restrict__ y)
+{
+    extern __shared__ int off[];  // [E + 1]
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = __ldg(expert_offsets + i);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int rows = off[E] < cap_recv ? off[E] : cap_recv;
+    const int64_t rb = (int64_t)V * 4 + V / 2;
+    const int nseg = (V + 127) / 128;
+    const int64_t ntask = (int64_t)rows * nseg;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
+         task += gwarps) {
+        const int row = (int)(task / nseg);
+        const int gs = (int)(task - (int64_t)row * nseg);
+        int lo = 0, hi = E - 1;  // last e with off[e] <= row
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= row) lo = mid;
+            else hi = mid - 1;
+        }
+        const float f = __fmul_rn(__ldg(scale + lo), g);
+        const uint8_t *rec = recv_q + (int64_t)row * rb;
+        uint32_t c[4];
+        uint8_t sb[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int vi = gs * 128 + u * 32 + lane;
+            c[u] = 0;
+            sb[u] = 0;
+            if (vi < V) {
+                c[u] = __ldg(reinterpret_cast<const uint32_t *>(rec) + vi);
+                sb[u] = __ldg(rec + (int64_t)V * 4 + (vi >> 1));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int vi = gs * 128 + u * 32 + lane;
+            if (vi >= V) continue;
+            const __half_raw shr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sb[u], __NV_E4M3);
+            const float sd = __half2float(*reinterpret_cast<const __half *>(&shr));
+            float a[8];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const __half2_raw hr =
+                    __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(c[u] >> (8 * i)), __NV_E2M1);
+                const float2 q = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                a[2 * i] = __fmul_rn(__fmul_rn(q.x, sd), f);
+                a[2 * i + 1] = __fmul_rn(__fmul_rn(q.y, sd), f);
+            }
+            st_cg(y + (int64_t)row * V + vi, pack_bf16x8(a));
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t *y, int y_rows, const int32_t *pair_row, const float *w,
@@ -670,6 +734,22 @@ cudaError_t launch_routed_stage1(const uint16_t *send, const int32_t *send_ids,
                                          send_w, part_offsets, S, cap_send, span, k, E, E / P, P, V,
                                          recv_part, scale, (int4 *)ret, dev_status));
     }
+    return e;
+}
+
+cudaError_t launch_expert_scale_nvfp4(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                      const float *scale, int E, int H, float g, int cap_recv,
+                                      uint16_t *y, cudaStream_t st)
+{
+    if (cap_recv == 0) return cudaSuccess;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int blocks = di.sm_count * 8;
+    MOE_TRACED_LAUNCH("k_expert_scale_nvfp4", st,
+                      e = launch_pdl(k_expert_scale_nvfp4, dim3(blocks), dim3(256),
+                                     (size_t)(E + 1) * sizeof(int), st, recv_q, expert_offsets,
+                                     scale, E, H / 8, g, cap_recv, (int4 *)y));
     return e;
 }
 

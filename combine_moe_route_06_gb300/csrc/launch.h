@@ -52,6 +52,13 @@ cudaError_t launch_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, i
                                        const int32_t *token_slot, const int32_t *part_offsets,
                                        int cap_send, uint8_t *send_q, int32_t *send_src,
                                        uint32_t *dev_status, cudaStream_t st);
+cudaError_t launch_dispatch_pack_nvfp4(const uint16_t *x, int S, int T, int H, int P, float g,
+                                       const int32_t *token_slot, const int32_t *part_offsets,
+                                       int cap_send, uint8_t *send_q, int32_t *send_src,
+                                       uint32_t *dev_status, cudaStream_t st);
+cudaError_t launch_expert_scale_nvfp4(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                      const float *scale, int E, int H, float g, int cap_recv,
+                                      uint16_t *y, cudaStream_t st);
 cudaError_t launch_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offsets,
                                       const float *scale, int E, int H, int cap_recv, uint16_t *y,
                                       cudaStream_t st);

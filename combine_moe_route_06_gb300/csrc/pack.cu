@@ -9,6 +9,7 @@
 // segment of x once (16-byte vectors, four per lane in flight) and stores it
 // to each of the token's c <= min(k, P) destination rows.  HBM traffic is the
 // minimum: x read once, c copies written.
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -216,6 +217,98 @@ __global__ void __launch_bounds__(kPackThreads) k_pack_mxfp8(
     if (__any_sync(kFull, overflow) && lane == 0) flag_status(dev_status, MOE_ERR_CAPACITY);
 }
 
+// Pack with NVFP4 records (a2a-backends section 7.2: an NVFP4 row is 2,880
+// bytes for 5,120 values, one scale byte per 16).  A record is H/2 bytes of
+// E2M1 codes (element 2i in the low nibble) followed by H/16 E4M3 block
+// scales; with the tensor scale g,
+//   s = e4m3(amax / (6 g)),  code = e2m1_rn_satfinite(v / (s g))   (0 if s = 0)
+// all in fp32 with correctly rounded division.  One warp per (token, 1,024
+// values); lanes 2b, 2b+1 hold one 16-value block for each 16-byte load.
+__global__ void __launch_bounds__(kPackThreads) k_pack_nvfp4(
+    const int4 *__restrict__ x, int S, int T, int V, int P, float g,
+    const int32_t *__restrict__ token_slot, const int32_t *__restrict__ part_offsets,
+    int cap_send, uint8_t *__restrict__ send_q, int32_t *__restrict__ send_src,
+    uint32_t *dev_status)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
+        const int s = (int)(i / cap_send);
+        const int r = (int)(i - (int64_t)s * cap_send);
+        if (r >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) send_src[i] = -1;
+    }
+    const int64_t rb = (int64_t)V * 4 + V / 2;  // record bytes: codes, then scales
+    const float d = __fmul_rn(6.0f, g);
+    const int nseg = (V + kQSegVec - 1) / kQSegVec;
+    const int64_t ntask = (int64_t)S * T * nseg;
+    const int64_t gwarps = gthreads >> 5;
+    bool overflow = false;
+    for (int64_t task = gtid >> 5; task < ntask; task += gwarps) {
+        const int64_t n = task / nseg;
+        const int gseg = (int)(task - n * nseg);
+        const int s = (int)(n / T);
+        int slot = -1;
+        if (lane < P) slot = __ldg(token_slot + n * P + lane);
+        const bool ok = slot >= 0 && slot < cap_send;
+        if (slot >= cap_send) overflow = true;
+        unsigned dmask = __ballot_sync(kFull, ok);
+        if (gseg == 0 && ok) send_src[(int64_t)s * cap_send + slot] = (int32_t)(n - (int64_t)s * T);
+        if (dmask == 0) continue;
+
+        const int v0 = gseg * kQSegVec + lane;
+        uint32_t code[kPackUnroll];
+        uint8_t scale[kPackUnroll];
+#pragma unroll
+        for (int u = 0; u < kPackUnroll; u++) {
+            const int vi = v0 + 32 * u;
+            int4 v = make_int4(0, 0, 0, 0);
+            if (vi < V) v = ld_stream(x + n * V + vi);
+            const uint32_t w4[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+            float f[8];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                f[2 * i] = __uint_as_float(w4[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(__fdiv_rn(amax, d), __NV_SATFINITE,
+                                                                __NV_E4M3);
+            const __half_raw sh = __nv_cvt_fp8_to_halfraw(sb, __NV_E4M3);
+            const float sg = __fmul_rn(__half2float(*reinterpret_cast<const __half *>(&sh)), g);
+            uint32_t c = 0;
+            if (sg != 0.f) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const float2 q = make_float2(__fdiv_rn(f[2 * i], sg), __fdiv_rn(f[2 * i + 1], sg));
+                    c |= (uint32_t)__nv_cvt_float2_to_fp4x2(q, __NV_E2M1, cudaRoundNearest) << (8 * i);
+                }
+            }
+            code[u] = c;
+            scale[u] = (uint8_t)sb;
+        }
+        while (dmask) {
+            const int p = __ffs(dmask) - 1;
+            dmask &= dmask - 1;
+            const int sl = __shfl_sync(kFull, slot, p);
+            uint8_t *rec = send_q + ((int64_t)s * cap_send + sl) * rb;
+#pragma unroll
+            for (int u = 0; u < kPackUnroll; u++) {
+                const int vi = v0 + 32 * u;
+                if (vi < V) {
+                    reinterpret_cast<uint32_t *>(rec)[vi] = code[u];
+                    if ((vi & 1) == 0) rec[(int64_t)V * 4 + (vi >> 1)] = scale[u];
+                }
+            }
+        }
+    }
+    if (__any_sync(kFull, overflow) && lane == 0) flag_status(dev_status, MOE_ERR_CAPACITY);
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
@@ -273,6 +366,30 @@ cudaError_t launch_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, i
     MOE_TRACED_LAUNCH("k_pack_mxfp8", st,
                       e = launch_pdl(k_pack_mxfp8, dim3((unsigned)blocks), dim3(kPackThreads), 0, st,
                                      (const int4 *)x, S, T, V, P, token_slot, part_offsets,
+                                     cap_send, send_q, send_src, dev_status));
+    return e;
+}
+
+cudaError_t launch_dispatch_pack_nvfp4(const uint16_t *x, int S, int T, int H, int P, float g,
+                                       const int32_t *token_slot, const int32_t *part_offsets,
+                                       int cap_send, uint8_t *send_q, int32_t *send_src,
+                                       uint32_t *dev_status, cudaStream_t st)
+{
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int V = H / 8;
+    const int nseg = (V + kQSegVec - 1) / kQSegVec;
+    const int64_t warps = (int64_t)S * T * nseg;
+    const int64_t want = (warps + (kPackThreads / 32) - 1) / (kPackThreads / 32);
+    const int resident = resident_grid((const void *)k_pack_nvfp4, kPackThreads, 0);
+    int64_t blocks = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPackThreads);
+    if (want < blocks) blocks = want;
+    const int64_t tail_blocks = ((int64_t)S * cap_send + kPackThreads - 1) / kPackThreads;
+    if (blocks < 1) blocks = tail_blocks < 1 ? 1 : (tail_blocks < di.sm_count ? tail_blocks : di.sm_count);
+    MOE_TRACED_LAUNCH("k_pack_nvfp4", st,
+                      e = launch_pdl(k_pack_nvfp4, dim3((unsigned)blocks), dim3(kPackThreads), 0, st,
+                                     (const int4 *)x, S, T, V, P, g, token_slot, part_offsets,
                                      cap_send, send_q, send_src, dev_status));
     return e;
 }

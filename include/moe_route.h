@@ -310,6 +310,29 @@ moe_status_t moe_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, int
                                      uint32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Pack with NVFP4 records (a2a-backends section 7.2: FlashInfer's all-to-all
+ * sends NVFP4 rows when the expert kernel takes them; an NVFP4 row of a
+ * DeepSeek-V4.1-Flash token is 2,880 bytes, a one-byte scale for every 16 of
+ * its 5,120 values).  Encoding (the page fixes only the size): NVIDIA's NVFP4
+ * with the per-tensor fp32 scale g = global_scale given by the caller (it is
+ * not part of a row).  Per block of 16 values, in fp32 with correctly
+ * rounded division:
+ *   s = e4m3_rn_satfinite( amax / (6 g) ),  code_i = e2m1_rn_satfinite( v_i / (s g) )
+ * and all codes 0 when s is 0.  A record is H/2 bytes of E2M1 codes (element
+ * 2i in the low nibble), then H/16 bytes of E4M3 scales.
+ *   x       [S][T][H] bf16 in; H a multiple of 256.
+ *   send_q  [S][cap_send][H/2 + H/16] uint8 out, 16-byte aligned; rows no slot
+ *           names are not written.
+ *   token_slot, part_offsets, cap_send, send_src, dev_status: as moe_dispatch_pack.
+ * The records move through moe_permute_to_experts as opaque rows of
+ * (H/2 + H/16)/2 bf16 slots.  Errors: as moe_dispatch_pack; g must be positive.
+ */
+moe_status_t moe_dispatch_pack_nvfp4(const uint16_t *x, int S, int T, int H, int P,
+                                     float global_scale, const int32_t *token_slot,
+                                     const int32_t *part_offsets, int cap_send, uint8_t *send_q,
+                                     int32_t *send_src, uint32_t *dev_status, cudaStream_t stream);
+
+/*
  * Receiver permute into expert-contiguous runs (a2a-backends section 1.5:
  * the contiguous layout, runs optionally padded to a multiple of `align`
  * rows as DeepGEMM wants 128; section 3.3: one row per (token, local
@@ -450,6 +473,17 @@ moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offset
 moe_status_t moe_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert_offsets,
                                     const float *scale, int E, int H, int cap_recv, uint16_t *y,
                                     cudaStream_t stream);
+
+/*
+ * Stand-in expert on NVFP4 records (harness, like moe_expert_scale):
+ *   y[r][h] = bf16( scale[e] * e2m1(code) * e4m3(block scale) * global_scale )
+ * code * block scale is exact in fp32; scale[e] * global_scale is one fp32
+ * product, so y may differ from the exactly rounded value by one bf16 unit.
+ *   recv_q [cap_recv][H/2 + H/16] uint8 (16-byte aligned); y [cap_recv][H] bf16 out.
+ */
+moe_status_t moe_expert_scale_nvfp4(const uint8_t *recv_q, const int32_t *expert_offsets,
+                                    const float *scale, int E, int H, float global_scale,
+                                    int cap_recv, uint16_t *y, cudaStream_t stream);
 
 /*
  * Per-kernel timing (tracing aid; off by default).  While enabled, every
