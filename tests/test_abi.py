@@ -139,3 +139,49 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(m, "_lib", None)
     with pytest.raises(m.MoeLibraryMissing):
         m.load_library()
+
+
+def _rejects(fn, args, needle):
+    assert fn(*args) == m.MOE_ERR_INVALID_ARG, needle
+    assert needle in _msg(lib_ := m.load_library()), (_msg(lib_), needle)
+
+
+def test_next_entry_points_reject(lib):
+    # masked permute: block_rows must not be negative
+    _rejects(lib.moe_permute_to_experts_masked,
+             [FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 2, 16, 4, 256, -1, -1, 128, FAKE, FAKE, FAKE, FAKE,
+              FAKE, ST], "block_rows")
+    # two-stage combine: receiving partition out of range
+    _rejects(lib.moe_combine_stage1,
+             [FAKE, 64, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 16, 4, 256, 4, 64, FAKE, FAKE, ST], "recv_part")
+    _rejects(lib.moe_combine_stage2, [FAKE, FAKE, 1, 8, 4, 256, 7, 64, FAKE, FAKE, ST], "recv_part")
+    # quantized packs: widths the records need, and a positive tensor scale
+    _rejects(lib.moe_dispatch_pack_mxfp8, [FAKE, 1, 8, 96, 4, FAKE, FAKE, 16, FAKE, FAKE, FAKE, ST],
+             "H=96")
+    _rejects(lib.moe_expert_scale_mxfp8, [FAKE, FAKE, FAKE, 16, 160, 8, FAKE, ST], "H=160")
+    _rejects(lib.moe_dispatch_pack_nvfp4,
+             [FAKE, 1, 8, 384, 4, ctypes.c_float(1.0), FAKE, FAKE, 16, FAKE, FAKE, FAKE, ST], "H=384")
+    _rejects(lib.moe_dispatch_pack_nvfp4,
+             [FAKE, 1, 8, 512, 4, ctypes.c_float(0.0), FAKE, FAKE, 16, FAKE, FAKE, FAKE, ST],
+             "global_scale")
+    _rejects(lib.moe_expert_scale_nvfp4,
+             [FAKE, FAKE, FAKE, 16, 512, ctypes.c_float(-2.0), 8, FAKE, ST], "global_scale")
+    # routed payload: k and the receiving partition
+    _rejects(lib.moe_dispatch_pack_routed,
+             [FAKE, FAKE, FAKE, 1, 8, 256, 33, 4, FAKE, FAKE, 16, FAKE, FAKE, FAKE, FAKE, FAKE, ST], "k=33")
+    _rejects(lib.moe_routed_expert_stage1,
+             [FAKE, FAKE, FAKE, FAKE, 1, 8, 16, 2, 16, 4, 256, 9, NULL, FAKE, FAKE, ST], "recv_part")
+    # layout over a placement: slots per partition and the copy count
+    ws = lib.moe_workspace_bytes_mapped(1, 64, 2, 16, 4, 5)
+    assert ws > 0 and lib.moe_workspace_bytes_mapped(1, 64, 2, 16, 4, 3) == 0   # Lp < E/P
+    good = [FAKE, 1, 64, 2, 16, 4, 5, FAKE, FAKE, 18, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws,
+            FAKE, ST]
+    bad = list(good)
+    bad[6] = 3
+    _rejects(lib.moe_dispatch_layout_mapped, bad, "Lp=3")
+    bad = list(good)
+    bad[9] = 40
+    _rejects(lib.moe_dispatch_layout_mapped, bad, "n_copies=40")
+    bad = list(good)
+    bad[17] = ws - 1
+    _rejects(lib.moe_dispatch_layout_mapped, bad, "ws_bytes")
