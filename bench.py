@@ -747,7 +747,9 @@ def run_ours(args, world, rank, local):
                 "host_binding": host_binding,
                 "how": "pinned H2D -> step -> D2H every step; steps pipelined on 3 streams "
                        "with 3 buffer sets; no L2 flush (each step moves ~1 GB)"},
-        "gpu_launches": launches * K,
+        # the timed steps and, between them, the instrumented copies of the step
+        "gpu_launches": 2 * launches * K,
+        "gpu_launches_per_step": launches,
         "launch_mode": "eager" if args.eager else "cuda_graph_replay",
         "host_enqueue_us_per_step": round(host_enqueue_us, 1),
         "clocks": clocks,
