@@ -460,6 +460,9 @@ def run_ours(args, world, rank, local):
         step()
         torch.cuda.synchronize()
         status = int(path.dev_status.item())
+        per_part = path.expert_counts.sum(dim=0).cpu().numpy().reshape(w.P, -1).sum(axis=1)
+        partition_load = {"pairs_max_over_mean": round(float(per_part.max() / max(per_part.mean(), 1e-9)), 4),
+                          "busiest_partition": int(per_part.argmax())}
         copies = int(path.part_offsets[:, -1].sum().item())
         copies_recv = copies if w.recv_part < 0 else int(path.part_counts[:, w.recv_part].sum().item())
         if args.variant == "routed":
@@ -726,6 +729,7 @@ def run_ours(args, world, rank, local):
                         if k_ in b},
         "copies_per_token": round(copies / (w.S * w.T), 4),
         "pairs_recv": pairs_recv,
+        "partition_load": partition_load,
         "dev_status": status,
         "roofline": {"kernel": dom_name, "bound": "hbm",
                      "achieved": round(dom_achieved, 1) if dom_achieved else None,

@@ -8,8 +8,21 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "launch.h"
+
+namespace {
+// One NVTX range per library call (host side: argument checks and enqueue), so a
+// profiler's timeline shows which call launched which kernels.  A push/pop costs
+// a branch when no tool is attached.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+};
+}  // namespace
+#define MOE_CALL_RANGE() CallRange moe_call_range_(__func__)
 
 namespace moe {
 
@@ -166,6 +179,7 @@ size_t moe_workspace_bytes(int S, int T, int k, int E, int P)
 moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k, int32_t *topk_ids,
                             float *topk_w, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, E, 1);
     if (st != MOE_OK) return st;
     REQUIRE((int64_t)S * T * E < ((int64_t)1 << 40), "%s: S*T*E too large", __func__);
@@ -183,6 +197,7 @@ moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, i
                                  void *ws, size_t ws_bytes, uint32_t *dev_status,
                                  cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, E, P);
     if (st != MOE_OK) return st;
     const int64_t NT = (int64_t)S * T;
@@ -207,6 +222,7 @@ moe_status_t moe_dispatch_pack(const uint16_t *x, int S, int T, int H, int P,
                                int cap_send, uint16_t *send, int32_t *send_src,
                                uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
@@ -229,6 +245,7 @@ moe_status_t moe_dispatch_pack_mxfp8(const uint16_t *x, int S, int T, int H, int
                                      int cap_send, uint8_t *send_q, int32_t *send_src,
                                      uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
@@ -255,6 +272,7 @@ moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_s
                                     int32_t *recv_pair, void *ws, size_t ws_bytes,
                                     uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, E, P);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
@@ -293,6 +311,7 @@ moe_status_t moe_permute_to_experts_masked(const uint16_t *send, const int32_t *
                                            int32_t *pair_row, int32_t *recv_pair,
                                            uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, E, P);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
@@ -326,6 +345,7 @@ moe_status_t moe_combine(const uint16_t *y, int y_rows, const int32_t *pair_row,
                          const float *topk_w, int S, int T, int k, int H, uint16_t *out,
                          uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, k, 1);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
@@ -346,6 +366,7 @@ moe_status_t moe_combine_stage1(const uint16_t *y, int y_rows, const int32_t *pa
                                 int H, int recv_part, int cap_send, uint16_t *ret,
                                 uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, E, P);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
@@ -371,6 +392,7 @@ moe_status_t moe_combine_stage2(const uint16_t *ret, const int32_t *token_slot, 
                                 int P, int H, int recv_part, int cap_send, uint16_t *out,
                                 uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
     if (st != MOE_OK) return st;
     REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, %d)", __func__,
@@ -393,6 +415,7 @@ moe_status_t moe_expert_scale(const uint16_t *recv, const int32_t *expert_offset
                               const float *scale, int E, int H, int cap_recv, uint16_t *y,
                               cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     REQUIRE(E >= 1 && E <= kMaxE, "%s: E=%d must be in [1, %d]", __func__, E, kMaxE);
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
     REQUIRE(cap_recv >= 0, "%s: cap_recv=%d must be >= 0", __func__, cap_recv);
@@ -408,6 +431,7 @@ moe_status_t moe_expert_scale_mxfp8(const uint8_t *recv_q, const int32_t *expert
                                     const float *scale, int E, int H, int cap_recv, uint16_t *y,
                                     cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     REQUIRE(E >= 1 && E <= kMaxE, "%s: E=%d must be in [1, %d]", __func__, E, kMaxE);
     REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
     REQUIRE(cap_recv >= 0, "%s: cap_recv=%d must be >= 0", __func__, cap_recv);
@@ -452,6 +476,7 @@ moe_status_t moe_dispatch_layout_mapped(const int32_t *topk_ids, int S, int T, i
                                         size_t ws_bytes, uint32_t *dev_status,
                                         cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, E, P);
     if (st != MOE_OK) return st;
     REQUIRE(Lp >= E / P && (int64_t)P * Lp <= kMaxE,
@@ -488,6 +513,7 @@ moe_status_t moe_dispatch_pack_routed(const uint16_t *x, const int32_t *topk_ids
                                       int32_t *send_ids, float *send_w, uint32_t *dev_status,
                                       cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     REQUIRE(S >= 1 && T >= 0, "%s: S=%d, T=%d", __func__, S, T);
     REQUIRE(k >= 1 && k <= kMaxK, "%s: k=%d must be in [1, %d]", __func__, k, kMaxK);
     REQUIRE(P >= 1 && P <= kMaxP, "%s: P=%d must be in [1, %d]", __func__, P, kMaxP);
@@ -520,6 +546,7 @@ moe_status_t moe_routed_expert_stage1(const uint16_t *send, const int32_t *send_
                                       int recv_part, const float *scale, uint16_t *ret,
                                       uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, k, E, P);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
@@ -545,6 +572,7 @@ moe_status_t moe_dispatch_pack_nvfp4(const uint16_t *x, int S, int T, int H, int
                                      const int32_t *part_offsets, int cap_send, uint8_t *send_q,
                                      int32_t *send_src, uint32_t *dev_status, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     moe_status_t st = check_sizes(__func__, S, T, 1, P, P);
     if (st != MOE_OK) return st;
     REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
@@ -569,6 +597,7 @@ moe_status_t moe_expert_scale_nvfp4(const uint8_t *recv_q, const int32_t *expert
                                     const float *scale, int E, int H, float global_scale,
                                     int cap_recv, uint16_t *y, cudaStream_t stream)
 {
+    MOE_CALL_RANGE();
     REQUIRE(E >= 1 && E <= kMaxE, "%s: E=%d must be in [1, %d]", __func__, E, kMaxE);
     REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256", __func__, H);
     REQUIRE(global_scale > 0.f && global_scale < 3.0e38f, "%s: global_scale must be positive and finite",

@@ -13,6 +13,8 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -58,6 +60,11 @@ extern "C" moe_status_t moe_dispatch_layout_static(const int32_t *topk_ids, int 
                                                    int32_t *part_offsets, int32_t *token_slot,
                                                    uint32_t *dev_status, cudaStream_t stream)
 {
+    // one NVTX range per call, as for the other entry points
+    struct Range {
+        Range() { nvtxRangePushA("moe_dispatch_layout_static"); }
+        ~Range() { nvtxRangePop(); }
+    } range;
     // Sizes first (no CUDA call yet): invalid sizes give moe_workspace_bytes == 0
     // and are reported by moe_dispatch_layout below with its own message.
     const size_t need = moe_workspace_bytes(S, T, k, E, P);
