@@ -460,3 +460,29 @@ def test_trace_inside_cuda_graph():
         m.trace_disable()
     ref = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, None)
     assert close_bf16(bf16_host(path.out), ref["out"])
+
+
+@pytest.mark.parametrize("S,T,H,E,k,P,align", [(2, 300, 8, 1024, 32, 32, 1),
+                                               (3, 257, 24, 64, 8, 4, 128),
+                                               (1, 1, 8, 16, 2, 4, 1),
+                                               (2, 513, 520, 96, 3, 32, 8)])
+def test_path_at_the_limits(S, T, H, E, k, P, align):
+    """The whole path at the ABI's extremes (E = 1024, k = 32, P = 32, the smallest row of
+    8 values, a single token, ragged T over chunks) against the oracle."""
+    w_ = ms.workload("tiny", S=S, T=T, H=H, E=E, k=k, P=P)
+    inp = ms.gen_inputs(w_)
+    path, out = _gpu_path(w_, inp, align=align, scales=inp["scales"])
+    ref = oracle.run_path(inp["x"], inp["logits"], E, k, P, inp["scales"], align=align)
+    assert np.array_equal(host(path.topk_ids), ref["ids"])
+    assert np.array_equal(host(path.token_slot), ref["layout"]["token_slot"])
+    assert np.array_equal(host(path.expert_offsets), ref["permute"]["expert_offsets"])
+    assert np.array_equal(host(path.pair_row), ref["permute"]["pair_row"])
+    rows = int(ref["permute"]["expert_offsets"][-1])
+    assert np.array_equal(bf16_host(path.recv)[:rows], ref["permute"]["recv"][:rows])
+    # the stand-in expert (not a step of the method) rounds x*s in fp32 first: one bf16 unit;
+    # the combine is then held to its tolerance on the expert rows it was given
+    y = bf16_host(path.y)
+    assert close_bf16(y[:rows], ref["y"][:rows], rel=2.0 ** -7, floor=1e-30)
+    want = oracle.combine(y, ref["permute"]["pair_row"], ref["w"].astype(np.float32))
+    assert close_bf16(out, want), worst_rel(out, want)
+    assert int(path.dev_status.item()) == 0
