@@ -43,11 +43,21 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def build_mutant(n: int, path: str) -> str:
+    """Compile the oracle with planted mistake number n (ORC_MUTANT, see moe_oracle.c)
+    into `path`; the test suite uses it to show that its pins reject the mistake."""
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", f"-DORC_MUTANT={int(n)}",
+                    "-o", path, _SRC, "-lm"], check=True)
+    return path
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # MOE_ORACLE_LIB names another build of moe_oracle.c: only the
+            # mutant tests set it, to run the pins against a planted mistake
+            lib = ctypes.CDLL(os.environ.get("MOE_ORACLE_LIB") or build())
             P = ctypes.c_void_p
             i32, i64 = ctypes.c_int32, ctypes.c_int64
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]

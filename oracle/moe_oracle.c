@@ -31,6 +31,15 @@
 #include <stdlib.h>
 #include <string.h>
 
+/*
+ * ORC_MUTANT n (n > 0) plants one deliberate mistake, numbered below; the
+ * test suite builds such mutants to show that its pins reject them.  The
+ * normal build has ORC_MUTANT 0 and none of them.
+ */
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
+
 #define ORC_BIT_INCONSISTENT (1u << 1)
 #define ORC_BIT_CAPACITY     (1u << 2)
 #define ORC_BIT_BAD_ID       (1u << 3)
@@ -69,7 +78,11 @@ uint16_t oracle_bf16_from_double(double v)
     if (qe < -133)
         qe = -133;
     double q = ldexp(1.0, qe);
+#if ORC_MUTANT == 1
+    double r = floor(a / q) * q;     /* mutant 1: truncates instead of rounding */
+#else
     double r = nearbyint(a / q) * q; /* a/q is exact; default mode: ties to even */
+#endif
     if (r >= ldexp(1.0, 128))
         return sign | 0x7F80u;
     float f = (float)r;          /* exact: r has at most 8 significant bits */
@@ -98,7 +111,11 @@ static double binom(int n, int r)
  */
 double oracle_expected_copies(int E, int G, int k)
 {
+#if ORC_MUTANT == 6
+    return (double)G * (1.0 - binom(E - G, k) / binom(E, k));   /* mutant 6 */
+#else
     return (double)G * (1.0 - binom(E - E / G, k) / binom(E, k));
+#endif
 }
 
 /* ------------------------------------------------------- route, [a2a] 1.1 */
@@ -114,7 +131,11 @@ static int cand_cmp(const void *pa, const void *pb)
     const orc_cand *a = (const orc_cand *)pa, *b = (const orc_cand *)pb;
     if (a->v > b->v) return -1;
     if (a->v < b->v) return 1;
+#if ORC_MUTANT == 2
+    return (a->id < b->id) - (a->id > b->id);   /* mutant 2: ties to the higher id */
+#else
     return (a->id > b->id) - (a->id < b->id);
+#endif
 }
 
 /*
@@ -140,7 +161,11 @@ int oracle_route_topk(const float *logits, int64_t N, int E, int k,
         }
         qsort(c, (size_t)E, sizeof(orc_cand), cand_cmp);
         double lmax = (double)c[0].v, denom = 0.0;
+#if ORC_MUTANT == 3
+        for (int j = 0; j < E; j++)                 /* mutant 3: softmax over every logit */
+#else
         for (int j = 0; j < k; j++)
+#endif
             denom += exp((double)c[j].v - lmax);
         for (int j = 0; j < k; j++) {
             ids[n * k + j] = c[j].id;
@@ -206,7 +231,11 @@ int oracle_dispatch_layout(const int32_t *ids, int S, int64_t T, int k, int E, i
                     continue;
                 }
                 expert_counts[s * E + e] += 1;
+#if ORC_MUTANT == 4
+                hit[e % P] = 1;                     /* mutant 4: experts dealt round robin */
+#else
                 hit[e / L] = 1;
+#endif
             }
             for (int p = 0; p < P; p++)
                 part_counts[s * P + p] += hit[p];
@@ -236,10 +265,18 @@ int oracle_dispatch_layout(const int32_t *ids, int S, int64_t T, int k, int E, i
                 int h = 0;
                 for (int j = 0; j < k; j++) {
                     int32_t e = ids[((int64_t)s * T + t) * k + j];
+#if ORC_MUTANT == 4
+                    if (e >= 0 && e < E && e % P == p)
+#else
                     if (e >= 0 && e < E && e / L == p)
+#endif
                         h = 1;
                 }
+#if ORC_MUTANT == 5
+                token_slot[((int64_t)s * T + t) * P + p] = h ? ++next : -1;   /* mutant 5 */
+#else
                 token_slot[((int64_t)s * T + t) * P + p] = h ? next++ : -1;
+#endif
             }
         }
     }
@@ -500,11 +537,19 @@ int oracle_combine(const uint16_t *y, const int32_t *pair_row, const float *w,
     for (int64_t n = 0; n < (int64_t)S * T; n++) {
         for (int h = 0; h < H; h++)
             acc[h] = 0.0;
+#if ORC_MUTANT == 7
+        for (int j = 0; j < k - 1; j++) {          /* mutant 7: the last choice is dropped */
+#else
         for (int j = 0; j < k; j++) {
+#endif
             int32_t r = pair_row[n * k + j];
             if (r < 0)
                 continue;
+#if ORC_MUTANT == 8
+            double wj = 1.0;                        /* mutant 8: weights not applied */
+#else
             double wj = (double)w[n * k + j];
+#endif
             for (int h = 0; h < H; h++)
                 acc[h] += wj * oracle_bf16_to_double(y[(int64_t)r * H + h]);
         }
@@ -562,7 +607,11 @@ int oracle_combine_stage1(const uint16_t *y, const int32_t *pair_row, const floa
                     acc[h] = 0.0;
                 for (int j = 0; j < k; j++) {
                     int32_t e = ids[n * k + j], r = pair_row[n * k + j];
+#if ORC_MUTANT == 13
+                    if (e < 0 || e >= E || r < 0)   /* mutant 13: other partitions' experts too */
+#else
                     if (e < 0 || e >= E || e / L != p || r < 0)
+#endif
                         continue;
                     double wj = (double)w[n * k + j];
                     for (int h = 0; h < H; h++)
@@ -682,7 +731,11 @@ void oracle_quantize_mxfp8_block(const uint16_t *v, uint8_t *codes, uint8_t *sca
     if (amax > 0.0) {
         int ex;
         frexp(amax, &ex);                /* amax in [2^(ex-1), 2^ex) */
+#if ORC_MUTANT == 9
+        se = (ex - 1) - 7;                        /* mutant 9: scale one binade too high */
+#else
         se = (ex - 1) - 8;
+#endif
         if (se < -127)
             se = -127;
         if (se > 127)
@@ -874,7 +927,11 @@ int oracle_plan_placement(const int64_t *load, int E, int P, int R, int32_t *cop
         /* the receiving partition's load with one more copy of `best` */
         const int n1 = ncopy[best] + 1;
         const int64_t new_tgt = part_load[tgt] + oracle_copy_share(load[best], n1, n1 - 1);
+#if ORC_MUTANT == 11
+        if (!(new_tgt <= part_load[g]))           /* mutant 11: keeps a copy that ties */
+#else
         if (!(new_tgt < part_load[g]))
+#endif
             break;
         const int s = tgt * Lp + used[tgt]++;
         slot_expert[s] = best;
@@ -929,7 +986,11 @@ int oracle_map_replicas(const int32_t *ids, int S, int64_t T, int k, int E,
                     phys[i] = E_phys;
                 } else {
                     const int n = copy_offsets[e + 1] - copy_offsets[e];
+#if ORC_MUTANT == 12
+                    phys[i] = copy_slots[copy_offsets[e] + (int)(t % n)];   /* mutant 12 */
+#else
                     phys[i] = copy_slots[copy_offsets[e] + (int)(seen[e] % n)];
+#endif
                     seen[e]++;
                 }
             }
@@ -1048,7 +1109,11 @@ uint8_t oracle_e2m1_from_double(double v)
     int best = 0;
     for (int c = 1; c < 8; c++) {
         const double d = fabs(oracle_e2m1_mag[c] - a), db = fabs(oracle_e2m1_mag[best] - a);
+#if ORC_MUTANT == 10
+        if (d < db || (d == db && (c & 1) == 1))  /* mutant 10: ties to the odd code */
+#else
         if (d < db || (d == db && (c & 1) == 0))
+#endif
             best = c;
     }
     return sign | (uint8_t)best;
@@ -1072,7 +1137,11 @@ void oracle_quantize_nvfp4_block(const uint16_t *v, float g, uint8_t *codes, uin
         if (a > amax)
             amax = a;
     }
+#if ORC_MUTANT == 14
+    const float d = 6.0f;                         /* mutant 14: the tensor scale is ignored */
+#else
     const float d = 6.0f * g;
+#endif
     const float t = amax / d;
     *scale = oracle_e4m3_from_double((double)t);
     const float sg = (float)oracle_e4m3_to_double(*scale) * g;

@@ -789,12 +789,16 @@ def test_map_replicas_identity_and_skips():
 
 
 def test_map_replicas_round_robin_split():
+    # one expert per partition and skewed popularity, so the plan copies hot experts
     rng = np.random.default_rng(12)
-    E, P, R = 16, 4, 2
-    ids = rng.integers(0, E, size=(3, 200, 4)).astype(np.int32)
+    E, P, R = 8, 8, 2
+    pop = (np.arange(E) + 1.0) ** -1.5
+    ids = np.stack([np.stack([rng.choice(E, size=4, replace=False, p=pop / pop.sum())
+                              for _ in range(200)]) for _ in range(3)]).astype(np.int32)
     load = np.bincount(ids[0].ravel(), minlength=E).astype(np.int64)
     plan = oracle.plan_placement(load, P, R)
     co, cs = plan["copy_offsets"], plan["copy_slots"]
+    assert co[-1] > E                                             # copies were made
     phys = oracle.map_replicas(ids, E, co, cs, plan["E_phys"])
     assert np.array_equal(plan["slot_expert"][phys], ids)         # a copy of the right expert
     for s in range(3):
