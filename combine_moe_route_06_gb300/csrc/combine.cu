@@ -414,8 +414,22 @@ __global__ void __launch_bounds__(kCombThreads) k_combine_stage2(
     if (cap_flag) flag_status(dev_status, MOE_ERR_CAPACITY);
 }
 
-// Stand-in expert: one warp per (row, 2 KiB segment); expert of the row by
-// binary search over the run starts.
+// The expert whose run holds `row`: the last e < E with off[e] <= row (off is
+// the ascending run starts, off[0] = 0).  Two warp ballots over at most 32
+// run starts each (E <= 1024) instead of a serial binary search.
+__device__ __forceinline__ int expert_of_row(const int *off, int E, int row, int lane)
+{
+    const int step = (E + 31) >> 5;
+    const int i1 = lane * step;
+    const unsigned b1 = __ballot_sync(kFull, i1 < E && off[i1] <= row);
+    const int base = (31 - __clz(b1)) * step;
+    const int i2 = base + lane;
+    const unsigned b2 = __ballot_sync(kFull, lane < step && i2 < E && off[i2] <= row);
+    return base + (31 - __clz(b2));
+}
+
+// Stand-in expert: one warp per (row, 2 KiB segment); expert of the row from
+// the run starts.
 __global__ void __launch_bounds__(256) k_expert_scale(const int4 *__restrict__ recv,
                                                       const int32_t *__restrict__ expert_offsets,
                                                       const float *__restrict__ scale, int E,
@@ -436,12 +450,7 @@ __global__ void __launch_bounds__(256) k_expert_scale(const int4 *__restrict__ r
          task += gwarps) {
         const int row = (int)(task / nseg);
         const int g = (int)(task - (int64_t)row * nseg);
-        int lo = 0, hi = E - 1;  // last e with off[e] <= row
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (off[mid] <= row) lo = mid;
-            else hi = mid - 1;
-        }
+        const int lo = expert_of_row(off, E, row, lane);
         const float sc = __ldg(scale + lo);
 #pragma unroll
         for (int u = 0; u < 4; u++) {
@@ -485,13 +494,6 @@ __global__ void __launch_bounds__(256) k_expert_scale_mxfp8(
          task += gwarps) {
         const int row = (int)(task / nseg);
         const int g = (int)(task - (int64_t)row * nseg);
-        int lo = 0, hi = E - 1;  // last e with off[e] <= row
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (off[mid] <= row) lo = mid;
-            else hi = mid - 1;
-        }
-        const float sc = __ldg(scale + lo);
         const uint8_t *rec = recv_q + (int64_t)row * rb;
         uint2 c[4];
         int sb[4];
@@ -505,6 +507,8 @@ __global__ void __launch_bounds__(256) k_expert_scale_mxfp8(
                 sb[u] = __ldg(rec + (int64_t)V * 8 + (vi >> 2));
             }
         }
+        // the row's expert, while the loads are in flight
+        const float sc = __ldg(scale + expert_of_row(off, E, row, lane));
 #pragma unroll
         for (int u = 0; u < 4; u++) {
             const int vi = g * 128 + u * 32 + lane;
@@ -554,13 +558,6 @@ __global__ void __launch_bounds__(256) k_expert_scale_nvfp4(
          task += gwarps) {
         const int row = (int)(task / nseg);
         const int gs = (int)(task - (int64_t)row * nseg);
-        int lo = 0, hi = E - 1;  // last e with off[e] <= row
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (off[mid] <= row) lo = mid;
-            else hi = mid - 1;
-        }
-        const float f = __fmul_rn(__ldg(scale + lo), g);
         const uint8_t *rec = recv_q + (int64_t)row * rb;
         uint32_t c[4];
         uint8_t sb[4];
@@ -574,6 +571,8 @@ __global__ void __launch_bounds__(256) k_expert_scale_nvfp4(
                 sb[u] = __ldg(rec + (int64_t)V * 4 + (vi >> 1));
             }
         }
+        // the row's expert, while the loads are in flight
+        const float f = __fmul_rn(__ldg(scale + expert_of_row(off, E, row, lane)), g);
 #pragma unroll
         for (int u = 0; u < 4; u++) {
             const int vi = gs * 128 + u * 32 + lane;
