@@ -13,9 +13,22 @@
  *   moe_combine             weighted sum of expert outputs back in token
  *                           order, fp32 accumulation, bf16 out               (sections 7.1, 7.2)
  *
+ * Further forms of the same round trip, each declared below with its source:
+ *   moe_permute_to_experts_masked   a fixed block per expert plus a count     (sections 4.1, 4.2)
+ *   moe_combine_stage1 / _stage2    pre-add per partition, then a home sum    (section 7.1)
+ *   moe_dispatch_pack_routed,       rows that carry their ids and weights,
+ *   moe_routed_expert_stage1        and the routed expert's per-partition sum (sections 6.1, 7.1)
+ *   moe_dispatch_pack_mxfp8 / _nvfp4  rows quantized once before they are sent (section 7.2)
+ *   moe_plan_placement (host),      experts placed by load with copies of the
+ *   moe_dispatch_layout_mapped      hot ones ("Beyond One GPU", section 6)
+ *   moe_dispatch_layout_static      the layout for callers that cannot allocate
+ *   moe_expert_scale(_mxfp8/_nvfp4) stand-in experts for tests and benchmarks
+ *   moe_trace_*                     optional CUDA-event timing of launches
+ *
  * Expert-parallel ranks are emulated as partitions of buffers in one GPU's
  * memory: partition p holds the L = E/P experts p*L .. p*L+L-1 (contiguous
- * blocks, section 2.1 of the same page).  There is no peer traffic.
+ * blocks, section 2.1 of the same page) unless a placement maps them.  There
+ * is no peer traffic.
  *
  * Conventions for every call
  * --------------------------
@@ -51,6 +64,10 @@
  *   The library only sets bits; the caller clears the word when it wants.
  *   `dev_status` may be NULL, in which case data errors are not reported.
  * - Results are deterministic: the same inputs give the same bytes.
+ * - Calls may be made from several host threads on different streams; the
+ *   only shared state is moe_dispatch_layout_static's built-in scratch (see
+ *   there) and the optional trace.  Every call opens an NVTX range named after
+ *   it, so profiler timelines show which call launched which kernels.
  */
 #ifndef MOE_ROUTE_H
 #define MOE_ROUTE_H
