@@ -827,12 +827,15 @@ class MoePath:
                 return 1 + (2 if mapped else 1) + 1
             layout = 1 if self.T <= 256 else 2
             if mapped:
-                layout = 2 * layout + 1
+                copies = self.placement.copy_slots.size > self.E
+                layout = (2 * layout if copies else layout) + 1
             return 1 + layout + 1 + 1 + 1
         if self.T == 0:
             return 1 + (2 if mapped else 1) + 2 + (1 if with_expert else 0)
         layout = 1 if self.T <= 256 else 2
         if mapped:
-            layout = 2 * layout + 1
+            # the logical pass for the ranks runs only when some expert has copies
+            copies = self.placement.copy_slots.size > self.E
+            layout = (2 * layout if copies else layout) + 1
         comb = 2 if self.combine_mode == "two_stage" else 1
         return 1 + layout + 1 + 2 + comb + (1 if with_expert else 0)

@@ -131,7 +131,8 @@ int plan_placement(const int64_t *load, int E, int P, int R, int32_t *copy_offse
 namespace {
 
 // Physical slot of every pair from the pair's rank among its source's pairs
-// of the same logical expert (computed by the layout over logical ids).
+// of the same logical expert (computed by the layout over logical ids); with
+// rank == nullptr every expert has one slot and the rank is not needed.
 __global__ void __launch_bounds__(256) k_map_replicas(
     const int32_t *__restrict__ ids, const int32_t *__restrict__ rank, int64_t n_pairs, int E,
     int E_phys, const int32_t *__restrict__ copy_offsets, const int32_t *__restrict__ copy_slots,
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(256) k_map_replicas(
         if (e >= E) {
             out = E_phys;                   // the layout over physical ids flags it
         } else if (e >= 0) {
-            const int r = __ldg(rank + i);
+            const int r = rank ? __ldg(rank + i) : 0;
             const int o0 = __ldg(copy_offsets + e), n = __ldg(copy_offsets + e + 1) - o0;
             if (r < 0 || n < 1 || o0 < 0 || o0 + n > n_copies) {
                 bad = true;
@@ -206,10 +207,15 @@ cudaError_t launch_dispatch_layout_mapped(const int32_t *ids, int S, int T, int 
                                           uint32_t *dev_status, cudaStream_t st)
 {
     const MappedWs m = carve(ws, S, T, k, E);
-    // ranks among each source's pairs of each logical expert
-    cudaError_t e = launch_dispatch_layout(ids, S, T, k, E, 1, m.ec1, m.rk1, m.pc1, m.po1, m.ts1,
-                                           m.inner, dev_status, st);
-    if (e != cudaSuccess) return e;
+    // ranks among each source's pairs of each logical expert -- needed only
+    // when some expert has copies (n_copies > E; every expert has at least one)
+    const bool copies = n_copies > E;
+    cudaError_t e = cudaSuccess;
+    if (copies) {
+        e = launch_dispatch_layout(ids, S, T, k, E, 1, m.ec1, m.rk1, m.pc1, m.po1, m.ts1, m.inner,
+                                   dev_status, st);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t n_pairs = (int64_t)S * T * k;
     if (n_pairs > 0) {
         DeviceInfo di;
@@ -218,7 +224,8 @@ cudaError_t launch_dispatch_layout_mapped(const int32_t *ids, int S, int T, int 
         if (blocks > (int64_t)di.sm_count * 8) blocks = (int64_t)di.sm_count * 8;
         MOE_TRACED_LAUNCH("k_map_replicas", st,
                           e = launch_pdl(k_map_replicas, dim3((unsigned)blocks), dim3(256), 0, st,
-                                         ids, (const int32_t *)m.rk1, n_pairs, E, E_phys,
+                                         ids, copies ? (const int32_t *)m.rk1 : nullptr, n_pairs,
+                                         E, E_phys,
                                          copy_offsets, copy_slots, n_copies, phys, dev_status));
         if (e != cudaSuccess) return e;
     }

@@ -289,8 +289,9 @@ moe_status_t moe_plan_placement(const int64_t *load, int E, int P, int R, int32_
  *   the pair becomes -1.
  *   expert_counts [S][P*Lp]; the other outputs as moe_dispatch_layout.
  *   ws: moe_workspace_bytes_mapped(S, T, k, E, P, Lp) bytes, 256-byte aligned.
- * Five kernels: the layout over logical ids (for the ranks r), the map, the
- * layout over physical ids.
+ * n_copies must equal copy_offsets[E].  Five kernels: the layout over logical
+ * ids (for the ranks r), the map, the layout over physical ids; three when
+ * n_copies == E (no expert has copies, so no ranks are needed).
  */
 size_t moe_workspace_bytes_mapped(int S, int T, int k, int E, int P, int Lp);
 moe_status_t moe_dispatch_layout_mapped(const int32_t *topk_ids, int S, int T, int k, int E,
