@@ -14,7 +14,7 @@ import torch
 import combine_moe_route_06_gb300 as m
 import moe_synth as ms
 import oracle
-from gpu_util import DEV, bf16_dev, bf16_host, close_bf16, f32_dev, host, worst_rel
+from gpu_util import bf16_dev, bf16_host, close_bf16, f32_dev, host, worst_rel
 
 pytestmark = pytest.mark.gpu
 

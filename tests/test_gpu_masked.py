@@ -10,7 +10,7 @@ import torch
 import combine_moe_route_06_gb300 as m
 import moe_synth as ms
 import oracle
-from gpu_util import DEV, bf16_dev, bf16_host, close_bf16, f32_dev, host, i32_dev
+from gpu_util import DEV, bf16_dev, bf16_host, close_bf16, host, i32_dev
 
 pytestmark = pytest.mark.gpu
 
