@@ -605,78 +605,40 @@ def run_ours(args, world, rank, local):
         value = bytes_all / (job_ms * 1e-3) / 1e9
 
         # ---------------- end to end: pinned host in, pinned host out --------
-        # Every step copies its logits and x in from pinned host memory and its
-        # output back out.  Steps are pipelined as in a serving loop: two sets
-        # of buffers, H2D on one stream, the step on another, D2H on a third,
-        # ordered by events, so copies of one step overlap the next step.
+        # Through the package's HostPipeline, as a serving loop would run it:
+        # every step copies its logits and x in from pinned host memory and its
+        # output back out; three buffer sets, copies overlapping neighbouring
+        # steps (three streams ordered by events).
         Ke = max(10, min(K, 200))
-        NB = 3                                     # buffer sets in the ring
-        s_in = torch.cuda.Stream(device=dev)
-        s_out = torch.cuda.Stream(device=dev)
-        sets = [(logits, x, path, h_out)]
-        extra_paths = []
-        for _ in range(NB - 1):
-            p_ = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev, **pkw)
-            lg_, x_ = torch.empty_like(logits), torch.empty_like(x)
-            ho_ = torch.empty_like(h_out).pin_memory()
-            with torch.cuda.stream(stream):
-                m.MoePath.run_bound(p_.bind(lg_, x_, stream))   # warm each set once
-            sets.append((lg_, x_, p_, ho_))
-            extra_paths.append(p_)
-        torch.cuda.synchronize()
-        graphs = []
-        if graph is not None:
-            steps = [graph.replay]
-            for lg_, x_, p_, _ in sets[1:]:
-                g_ = torch.cuda.CUDAGraph()
-                cap2 = torch.cuda.Stream(device=dev)
-                with torch.cuda.graph(g_, stream=cap2):
-                    m.MoePath.run_bound(p_.bind(lg_, x_, cap2))
-                graphs.append(g_)
-                steps.append(g_.replay)
-            torch.cuda.synchronize()
-        else:
-            steps = [lambda c=p_.bind(lg_, x_, stream): m.MoePath.run_bound(c)
-                     for lg_, x_, p_, _ in sets]
-        ev_in = [torch.cuda.Event() for _ in range(NB)]
-        ev_comp = [torch.cuda.Event() for _ in range(NB)]
-        ev_out = [torch.cuda.Event() for _ in range(NB)]
+        NB = 3
+        pipe = m.HostPipeline(w.S, w.T, w.H, w.E, w.k, w.P, sets=NB, graphs=not args.eager,
+                              device=dev, recv_part=w.recv_part, **pkw)
+        h_outs = [h_out] + [torch.empty_like(h_out).pin_memory() for _ in range(NB - 1)]
+        for i in range(NB):                        # warm every set once
+            pipe.submit(h_logits, h_x, h_outs[i])
+        pipe.synchronize()
         e_start = torch.cuda.Event(enable_timing=True)
         e_end = torch.cuda.Event(enable_timing=True)
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        e_start.record(s_in)
+        e_start.record(pipe.s_in)
         for i in range(Ke):
-            b_ = i % NB
-            lg, xx, pth, ho = sets[b_]
-            with torch.cuda.stream(s_in):
-                if i >= NB:
-                    s_in.wait_event(ev_comp[b_])   # step i-NB has read this set's inputs
-                lg.copy_(h_logits, non_blocking=True)
-                xx.view(torch.int16).copy_(h_x, non_blocking=True)
-                ev_in[b_].record(s_in)
-            stream.wait_event(ev_in[b_])
-            if i >= NB:
-                stream.wait_event(ev_out[b_])      # step i-NB's output has been read out
-            with torch.cuda.stream(stream):
-                steps[b_]()
-                ev_comp[b_].record(stream)
-            s_out.wait_event(ev_comp[b_])
-            with torch.cuda.stream(s_out):
-                ho.copy_(pth.out.view(torch.int16), non_blocking=True)
-                ev_out[b_].record(s_out)
-        e_end.record(s_out)
+            pipe.submit(h_logits, h_x, h_outs[i % NB])
+        e_end.record(pipe.s_out)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dist, dev)
         e2e_bytes = sum_over_ranks(float(b["step"]) * Ke, dist, dev)
         e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
-        out_ok = all(bool(np.array_equal(ho_.numpy().view(np.uint16),
-                                         p_.out.view(torch.int16).cpu().numpy().view(np.uint16)))
-                     for _, _, p_, ho_ in sets)
-        graphs = None
-        sets = None
-        del extra_paths
+        # every set's last output, as copied out, against the device buffer and the
+        # graph-replay path's output (same inputs, so the same bytes)
+        ref_out = path.out.view(torch.int16).cpu().numpy()
+        out_ok = all(bool(np.array_equal(h_outs[b_].numpy(), ref_out) and
+                          np.array_equal(pipe.paths[(Ke + b_) % NB].out.view(torch.int16).cpu().numpy(),
+                                         ref_out))
+                     for b_ in range(NB))
+        pipe.release()
+        del pipe
 
         graph = None
         torch.cuda.synchronize()
@@ -773,8 +735,8 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": int(h_out.numel() * 2), "steps": Ke,
                 "ms_per_step": round(e2e_ms / Ke, 4), "readback_ok": out_ok,
                 "host_binding": host_binding,
-                "how": "pinned H2D -> step -> D2H every step; steps pipelined on 3 streams "
-                       "with 3 buffer sets; no L2 flush (each step moves ~1 GB)"},
+                "how": "HostPipeline: pinned H2D -> step -> D2H every step on 3 streams with 3 "
+                       "buffer sets; no L2 flush (each step moves ~1 GB)"},
         # the timed steps and, between them, the instrumented copies of the step
         "gpu_launches": 2 * launches * K,
         "gpu_launches_per_step": launches,

@@ -31,7 +31,7 @@ __all__ = [
     "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
     "moe_plan_placement", "moe_workspace_bytes_mapped", "moe_dispatch_layout_mapped", "Placement",
     "moe_dispatch_pack_routed", "moe_routed_expert_stage1", "moe_dispatch_pack_nvfp4",
-    "moe_expert_scale_nvfp4", "nvfp4_record_bytes", "mxfp8_record_bytes", "MoePath", "trace_enable", "trace_disable", "trace_reset",
+    "moe_expert_scale_nvfp4", "nvfp4_record_bytes", "mxfp8_record_bytes", "HostPipeline", "MoePath", "trace_enable", "trace_disable", "trace_reset",
     "trace_records",
 ]
 
@@ -839,3 +839,80 @@ class MoePath:
             layout = (2 * layout if copies else layout) + 1
         comb = 2 if self.combine_mode == "two_stage" else 1
         return 1 + layout + 1 + 2 + comb + (1 if with_expert else 0)
+
+
+class HostPipeline:
+    """Steps fed from and drained to pinned host memory, as a serving loop runs them.
+
+    Each step copies its logits and x in from host buffers, runs the path on
+    one of `sets` buffer sets, and copies the output back to a host buffer.
+    Copies in, steps and copies out use three streams ordered by events, so
+    the copies of one step overlap the steps next to it; a set is reused only
+    after its previous step has read its inputs and its output has been copied
+    out.  With `graphs` the step of every set is captured once as a CUDA graph.
+    """
+
+    def __init__(self, S, T, H, E, k, P, sets=3, graphs=True, device="cuda", **path_kwargs):
+        d = torch.device(device)
+        self.sets = sets
+        self.paths, self.logits, self.x, self.steps = [], [], [], []
+        self.s_in = torch.cuda.Stream(device=d)
+        self.s_step = torch.cuda.Stream(device=d)
+        self.s_out = torch.cuda.Stream(device=d)
+        self._graphs = []
+        for _ in range(sets):
+            p = MoePath(S, T, H, E, k, P, device=d, **path_kwargs)
+            lg = torch.empty((S, T, E), dtype=torch.float32, device=d)
+            xx = torch.empty((S, T, H), dtype=torch.bfloat16, device=d)
+            calls = p.bind(lg, xx, self.s_step)
+            if graphs:
+                g = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream(device=d)
+                with torch.cuda.graph(g, stream=cap):
+                    MoePath.run_bound(p.bind(lg, xx, cap))
+                self._graphs.append(g)
+                self.steps.append(g.replay)
+            else:
+                self.steps.append(lambda c=calls: MoePath.run_bound(c))
+            self.paths.append(p)
+            self.logits.append(lg)
+            self.x.append(xx)
+        self.ev_in = [torch.cuda.Event() for _ in range(sets)]
+        self.ev_step = [torch.cuda.Event() for _ in range(sets)]
+        self.ev_out = [torch.cuda.Event() for _ in range(sets)]
+        self.n = 0
+
+    def submit(self, h_logits, h_x, h_out):
+        """Enqueue one step: h_logits fp32 [S,T,E], h_x bf16 (or int16 bits) [S,T,H] in, and
+        the output's bf16 bits into h_out (int16 [S,T,H]); all pinned host tensors.  Returns
+        the event recorded after the output copy.  h_out must not be reused before that."""
+        b = self.n % self.sets
+        p = self.paths[b]
+        with torch.cuda.stream(self.s_in):
+            if self.n >= self.sets:
+                self.s_in.wait_event(self.ev_step[b])     # the set's last step read its inputs
+            self.logits[b].copy_(h_logits, non_blocking=True)
+            self.x[b].view(torch.int16).copy_(h_x.view(torch.int16), non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+        self.s_step.wait_event(self.ev_in[b])
+        if self.n >= self.sets:
+            self.s_step.wait_event(self.ev_out[b])        # its output has been copied out
+        with torch.cuda.stream(self.s_step):
+            self.steps[b]()
+            self.ev_step[b].record(self.s_step)
+        self.s_out.wait_event(self.ev_step[b])
+        with torch.cuda.stream(self.s_out):
+            h_out.copy_(p.out.view(torch.int16), non_blocking=True)
+            self.ev_out[b].record(self.s_out)
+        self.n += 1
+        return self.ev_out[b]
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_step, self.s_out):
+            s.synchronize()
+
+    def release(self):
+        """Drop the captured graphs (before the buffers they refer to)."""
+        self.synchronize()
+        self._graphs = []
+        self.steps = []
