@@ -145,8 +145,12 @@ moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k,
  *                           #{t' < t : t' needs p}.
  *   ws, ws_bytes  scratch, ws_bytes >= moe_workspace_bytes(S, T, k, E, P).
  *   dev_status    device uint32 status word (bad ids).
- * Counting and ranking are atomic-free (warp ballots and match groups, block
- * scans), so the outputs are the same bytes on every run.
+ * Work is cut into 256-token chunks, one CTA each; with 2 to 16 chunks per
+ * source the chunks of a source form one thread-block cluster and exchange
+ * their counts in distributed shared memory (one launch), with more they go
+ * through `ws` (two launches).  Counting uses order-free integer adds and
+ * ranks follow the fixed (token, slot) order, so the outputs are the same
+ * bytes on every run.
  */
 moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, int E, int P,
                                  int32_t *expert_counts, int32_t *expert_rank,
