@@ -668,9 +668,14 @@ def run_ours(args, world, rank, local):
             m.MoePath.run_bound(calls)
         torch.cuda.synchronize()
         kern = {}
-        for name, ms_ in m.trace_records():
+        kern_recs = m.trace_records()
+        for name, ms_ in kern_recs:
             kern.setdefault(name, []).append(ms_)
         m.trace_disable()
+        # the launch count claimed per step must be what the library launched
+        traced_per_step = len(kern_recs) / Kb
+        if traced_per_step != launches:
+            raise RuntimeError(f"{traced_per_step} kernels traced per step, {launches} expected")
         kernels_us = {name: round(1e3 * statistics.median(v), 2) for name, v in kern.items()}
 
     if rank != 0:
@@ -740,6 +745,7 @@ def run_ours(args, world, rank, local):
         # the timed steps and, between them, the instrumented copies of the step
         "gpu_launches": 2 * launches * K,
         "gpu_launches_per_step": launches,
+        "gpu_launches_per_step_traced": traced_per_step,
         "launch_mode": "eager" if args.eager else "cuda_graph_replay",
         "host_enqueue_us_per_step": round(host_enqueue_us, 1),
         "clocks": clocks,

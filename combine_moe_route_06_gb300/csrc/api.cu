@@ -176,6 +176,14 @@ size_t moe_workspace_bytes(int S, int T, int k, int E, int P)
     return a > b ? a : b;
 }
 
+int moe_dispatch_layout_kernels(int S, int T, int k, int E, int P)
+{
+    if (check_sizes("moe_dispatch_layout_kernels", S, T, k, E, P) != MOE_OK) return -1;
+    int n = 0;
+    if (layout_kernel_count(T, k, E, P, &n) != cudaSuccess) return -1;
+    return n;
+}
+
 moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k, int32_t *topk_ids,
                             float *topk_w, cudaStream_t stream)
 {

@@ -30,6 +30,8 @@ cudaError_t launch_route_topk(const float *logits, int64_t N, int E, int k, int3
                               float *w, cudaStream_t st);
 
 size_t layout_ws_bytes(int S, int T, int E, int P);
+// Kernels launch_dispatch_layout enqueues for these sizes on the current device.
+cudaError_t layout_kernel_count(int T, int k, int E, int P, int *n);
 cudaError_t launch_dispatch_layout(const int32_t *ids, int S, int T, int k, int E, int P,
                                    int32_t *expert_counts, int32_t *expert_rank, int32_t *part_counts,
                                    int32_t *part_offsets, int32_t *token_slot, void *ws,

@@ -663,7 +663,36 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
     return cudaSuccess;
 }
 
+// The cluster form runs when a source has 2 to kMaxCluster chunks, the device
+// schedules clusters of that many CTAs with one CTA per SM, and a chunk's
+// shared memory fits.
+cudaError_t use_cluster_form(int T, int k, int E, int P, bool *out)
+{
+    *out = false;
+    const int C = (int)div_up(T, kChunk);
+    if (C < 2) return cudaSuccess;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    int gmax = 0;
+    size_t max_dyn = 0;
+    if ((e = cluster_size_limit((size_t)di.max_smem_optin / 2 + 1024, &gmax, &max_dyn)) !=
+        cudaSuccess)
+        return e;
+    *out = C <= gmax && cluster_smem(k, E, P) <= max_dyn;
+    return cudaSuccess;
+}
+
 }  // namespace
+
+cudaError_t layout_kernel_count(int T, int k, int E, int P, int *n)
+{
+    bool cluster = false;
+    const cudaError_t e = use_cluster_form(T, k, E, P, &cluster);
+    if (e != cudaSuccess) return e;
+    *n = (T <= kChunk || cluster) ? 1 : 2;
+    return cudaSuccess;
+}
 
 size_t layout_ws_bytes(int S, int T, int E, int P)
 {
@@ -691,13 +720,11 @@ cudaError_t launch_dispatch_layout(const int32_t *ids, int S, int T, int k, int 
     // the block scheduler gives each its own SM instead of stacking them.
     const size_t one_per_sm = (size_t)di.max_smem_optin / 2 + 1024;
 
-    // Cluster form: one cluster per source, one CTA per chunk, when the
-    // device schedules clusters of C CTAs.
-    int gmax = 0;
-    size_t max_dyn = 0;
-    if ((e = cluster_size_limit(one_per_sm, &gmax, &max_dyn)) != cudaSuccess) return e;
-    const size_t smc = cluster_smem(k, E, P);
-    if (C > 1 && C <= gmax && smc <= max_dyn) {
+    // Cluster form: one cluster per source, one CTA per chunk.
+    bool cluster = false;
+    if ((e = use_cluster_form(T, k, E, P, &cluster)) != cudaSuccess) return e;
+    if (cluster) {
+        const size_t smc = cluster_smem(k, E, P);
         const size_t smem = smc > one_per_sm ? smc : one_per_sm;
         MOE_TRACED_LAUNCH("k_layout_cluster", st,
                           e = launch_pdl_cluster(k_layout_cluster, dim3((unsigned)(S * C)),

@@ -112,6 +112,15 @@ const char *moe_last_error_message(void);
 size_t moe_workspace_bytes(int S, int T, int k, int E, int P);
 
 /*
+ * Number of kernels one moe_dispatch_layout call with these sizes enqueues on
+ * the calling thread's current device: 1 (one chunk per source, or one
+ * thread-block cluster per source) or 2 (more chunks per source than a
+ * cluster of that device holds).  For counting launches, e.g. per step of a
+ * captured graph.  Returns -1 for invalid sizes or a failed device query.
+ */
+int moe_dispatch_layout_kernels(int S, int T, int k, int E, int P);
+
+/*
  * Top-k routing (a2a-backends section 1.1: the router gives each token the
  * ids of its chosen experts and one weight per expert).
  *   logits  [S][T][E] float32, finite.
