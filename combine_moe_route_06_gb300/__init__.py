@@ -26,7 +26,7 @@ __all__ = [
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CAPACITY", "MOE_ERR_BAD_EXPERT_ID",
     "MOE_ERR_TIMEOUT", "MOE_ERR_CUDA", "status_bit", "MoeError", "MoeLibraryMissing",
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
-    "moe_dispatch_layout_kernels",
+    "moe_dispatch_layout_kernels", "moe_permute_to_experts_kernels",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
     "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
@@ -90,6 +90,7 @@ def load_library() -> ctypes.CDLL:
             "moe_last_error_message": ([], ctypes.c_char_p),
             "moe_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
             "moe_dispatch_layout_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
+            "moe_permute_to_experts_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
             "moe_route_topk": ([P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
             "moe_dispatch_layout": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P, P],
                                     ctypes.c_int),
@@ -175,6 +176,14 @@ def moe_version() -> int:
 
 def moe_workspace_bytes(S: int, T: int, k: int, E: int, P: int) -> int:
     return int(load_library().moe_workspace_bytes(S, T, k, E, P))
+
+
+def moe_permute_to_experts_kernels(S: int, T: int, k: int, E: int, P: int) -> int:
+    """Kernels one moe_permute_to_experts call enqueues (1: map inside the copy, or 2)."""
+    n = int(load_library().moe_permute_to_experts_kernels(S, T, k, E, P))
+    if n < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"moe_permute_to_experts_kernels({S}, {T}, {k}, {E}, {P})")
+    return n
 
 
 def moe_dispatch_layout_kernels(S: int, T: int, k: int, E: int, P: int) -> int:
@@ -829,8 +838,9 @@ class MoePath:
     def launches_per_step(self, with_expert=False) -> int:
         """Kernels one step enqueues: route 1, layout 1 or 2 (as the library reports for
         the shape; under a placement plus the replica map, and a logical layout first
-        when some expert has copies), pack 1, permute 2 (map + copy), stand-in expert 1
-        (always with quantized rows), combine 1 (2 when split into two stages)."""
+        when some expert has copies), pack 1, permute 1 or 2 (the masked form always
+        2: map + copy), stand-in expert 1 (always with quantized rows), combine 1
+        (2 when split into two stages)."""
         with_expert = with_expert or self.quantized
         mapped = self.placement is not None
         if mapped:
@@ -845,10 +855,14 @@ class MoePath:
             if self.T == 0:                # the two receive-side calls launch nothing
                 return 1 + layout + 1
             return 1 + layout + 1 + 1 + 1
+        if self.layout == "masked":
+            permute = 2 if self.T > 0 else 1      # nothing to copy at T = 0
+        else:
+            permute = moe_permute_to_experts_kernels(self.S, self.T, self.k, self.Ep, self.P)
         if self.T == 0:
-            return 1 + layout + 2 + (1 if with_expert else 0)
+            return 1 + layout + permute + (1 if with_expert else 0)
         comb = 2 if self.combine_mode == "two_stage" else 1
-        return 1 + layout + 1 + 2 + comb + (1 if with_expert else 0)
+        return 1 + layout + 1 + permute + comb + (1 if with_expert else 0)
 
 
 class HostPipeline:

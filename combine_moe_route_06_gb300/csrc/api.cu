@@ -184,6 +184,12 @@ int moe_dispatch_layout_kernels(int S, int T, int k, int E, int P)
     return n;
 }
 
+int moe_permute_to_experts_kernels(int S, int T, int k, int E, int P)
+{
+    if (check_sizes("moe_permute_to_experts_kernels", S, T, k, E, P) != MOE_OK) return -1;
+    return permute_map_fused(S, E) ? 1 : 2;
+}
+
 moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k, int32_t *topk_ids,
                             float *topk_w, cudaStream_t stream)
 {

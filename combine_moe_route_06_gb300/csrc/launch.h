@@ -79,6 +79,8 @@ cudaError_t launch_dispatch_layout_mapped(const int32_t *ids, int S, int T, int 
                                           uint32_t *dev_status, cudaStream_t st);
 
 size_t permute_ws_bytes(int S, int T, int E);
+// Whether launch_permute runs its map step inside the copy kernel (one launch).
+bool permute_map_fused(int S, int E);
 cudaError_t launch_permute(const uint16_t *send, const int32_t *token_slot, const int32_t *ids,
                            const int32_t *expert_counts, const int32_t *expert_rank,
                            int S, int T, int k, int E, int P, int H, int recv_part, int align,

@@ -121,6 +121,14 @@ size_t moe_workspace_bytes(int S, int T, int k, int E, int P);
 int moe_dispatch_layout_kernels(int S, int T, int k, int E, int P);
 
 /*
+ * Number of kernels one moe_permute_to_experts call with these sizes
+ * enqueues: 1 when the map step (run starts, pair rows) runs inside the copy
+ * kernel, which is whenever S*E + 2*E + 1 counts fit in 48 KiB of shared
+ * memory, else 2.  Returns -1 for invalid sizes.
+ */
+int moe_permute_to_experts_kernels(int S, int T, int k, int E, int P);
+
+/*
  * Top-k routing (a2a-backends section 1.1: the router gives each token the
  * ids of its chosen experts and one weight per expert).
  *   logits  [S][T][E] float32, finite.

@@ -202,6 +202,31 @@ def test_permute_multi_source_ragged():
         _check_permute(send, lay["token_slot"], ids, w_.E, rp, al, w_.S * w_.T * w_.k + w_.E * (al - 1))
 
 
+@pytest.mark.parametrize("S,E,recv_part,align,kernels", [
+    (1, 16, -1, 1, ["k_perm_copy"]), (3, 64, 2, 8, ["k_perm_copy"]),
+    (12, 1024, -1, 1, ["k_perm_map", "k_perm_copy"]), (12, 1024, 5, 128, ["k_perm_map", "k_perm_copy"])])
+def test_permute_map_in_copy_or_separate(S, E, recv_part, align, kernels):
+    """The map step runs inside the copy kernel while the counts' prefix sums fit in its shared
+    memory (S*E + 2E + 1 ints <= 48 KiB), else as its own kernel first; both give the oracle's
+    rows, offsets and pair rows, and the library reports the launch count it uses."""
+    w_ = ms.workload("tiny", S=S, T=40, H=64, E=E, k=8, P=8)
+    inp = ms.gen_inputs(w_)
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap_send = w_.T * min(w_.k, w_.P)
+    send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap_send)
+    torch.cuda.synchronize()
+    m.trace_enable("k_perm", 8)
+    try:
+        _check_permute(send, lay["token_slot"], ids, w_.E, recv_part, align,
+                       S * w_.T * w_.k + w_.E * (align - 1))
+        names = [name for name, _ in m.trace_records()]
+    finally:
+        m.trace_disable()
+    assert names == kernels
+    assert m.moe_permute_to_experts_kernels(S, w_.T, w_.k, w_.E, w_.P) == len(kernels)
+
+
 def test_permute_capacity_and_bad_inputs():
     w_, inp, ids, lay, cap_send = _pack_case("tiny")
     ids = ids.copy()
