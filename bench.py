@@ -11,7 +11,8 @@ the device time of the step (CUDA events, L2 flushed before every step).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the CPU oracle (single thread, this host) on the same
-workload and metric.  Under torchrun each rank runs an independent replica on
+workload and metric; the default run also reports the oracle single-threaded
+and on every core (one process per core) as cpu_baseline(_all_cores).  Under torchrun each rank runs an independent replica on
 its own batch (weak scaling, no data-path collective); rank 0 prints.
 """
 from __future__ import annotations
@@ -253,6 +254,61 @@ def time_oracle(w, seconds: float, max_steps: int, min_steps: int = 1):
             break
     b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, *stats)
     return n, el, b
+
+
+def _oracle_worker(name, seconds, barrier, results):
+    """One spawned process of the all-cores oracle timing: its own inputs, then
+    whole steps of the unchanged oracle from the common start until `seconds`."""
+    w = ms.workload(name)
+    inp = ms.gen_inputs(w)
+    oracle_step(inp, w)                      # loads the oracle library
+    barrier.wait(timeout=600)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        stats = oracle_step(inp, w)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    results.put((n, el, stats))
+
+
+def time_oracle_all_cores(w, seconds: float):
+    """The oracle on every core this process may use: one spawned process per
+    core, each running whole steps on its own copy of the workload (the oracle
+    itself stays single-threaded).  Returns (cores, steps, seconds, bytes per
+    step); throughput = steps x bytes / seconds of the longest process.  Raises
+    RuntimeError (after stopping the processes it started) if a process fails
+    or the run overstays its time."""
+    import multiprocessing as mp
+    import queue
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ctx = mp.get_context("spawn")            # fresh interpreters: nothing inherited from CUDA
+    barrier, results = ctx.Barrier(cores), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(w.name, seconds, barrier, results))
+             for _ in range(cores)]
+    for p_ in procs:
+        p_.start()
+    out = []
+    deadline = time.monotonic() + 600 + 4 * seconds
+    try:
+        while len(out) < cores:
+            try:
+                out.append(results.get(timeout=1.0))
+            except queue.Empty:
+                if any(p_.exitcode not in (None, 0) for p_ in procs):
+                    raise RuntimeError("an oracle process failed")
+                if time.monotonic() > deadline:
+                    raise RuntimeError("the all-cores oracle run overstayed its time")
+    finally:
+        for p_ in procs:
+            if p_.is_alive() and len(out) < cores:
+                p_.terminate()
+            p_.join()
+    steps = sum(n for n, _, _ in out)
+    el = max(e for _, e, _ in out)
+    b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, *out[0][2])
+    return cores, steps, el, b
 
 
 def run_reference(args, world, rank):
@@ -688,12 +744,21 @@ def run_ours(args, world, rank, local):
     dom_achieved = (b[dom_key] / (dom_ms * 1e-3) / 1e9) if dom_ms else None
     dc_gbs = b["dispatch_combine"] * len(dc_ms) / (sum(dc_ms) * 1e-3) / 1e9
 
-    cpu = None
+    cpu = cpu_all = None
     if world == 1 and not args.no_cpu_baseline:
         n, el, bb = time_oracle(ms.workload(args.workload), args.cpu_seconds, max_steps=100)
         cpu = {"value": round(bb["step"] * n / el / 1e9, 4), "unit": "GB/s", "cores": 1,
                "kind": "oracle",
                "sample": f"{n} full steps of the {w.name} workload in {el:.1f} s (single thread)"}
+        import platform
+        try:
+            nc, na, ela, ba = time_oracle_all_cores(ms.workload(args.workload), args.cpu_seconds / 2)
+            cpu_all = {"value": round(ba["step"] * na / ela / 1e9, 4), "unit": "GB/s",
+                       "cores": nc, "kind": "oracle", "machine": platform.machine(),
+                       "sample": f"{na} full steps of the {w.name} workload in {ela:.1f} s over "
+                                 f"{nc} processes of the single-threaded oracle, one per core"}
+        except RuntimeError as exc:
+            cpu_all = {"unavailable": str(exc)}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -734,6 +799,7 @@ def run_ours(args, world, rank, local):
                             "run after its own L2 flush between the timed steps (event nodes "
                             "break the programmatic-launch edges, so the timed steps carry none)"},
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         **({"placement": placement_info} if placement_info is not None else {}),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
