@@ -52,6 +52,19 @@ def test_workspace_bytes(lib):
     assert m.moe_workspace_bytes(0, 16, 6, 384, 8) == 0       # S < 1
 
 
+def test_kernel_count_queries(lib):
+    """The permute's form depends only on S*E (the map runs inside the copy while S*E + 2E + 1
+    counts fit in 48 KiB); invalid sizes give -1 for both queries without touching a device."""
+    assert lib.moe_permute_to_experts_kernels(1, 4096, 6, 384, 8) == 1
+    assert lib.moe_permute_to_experts_kernels(8, 4096, 6, 384, 8) == 1
+    assert lib.moe_permute_to_experts_kernels(9, 64, 8, 1024, 8) == 1      # 45,060 bytes: fits
+    assert lib.moe_permute_to_experts_kernels(10, 64, 8, 1024, 8) == 2     # 49,156 bytes: not
+    assert lib.moe_permute_to_experts_kernels(1, 16, 6, 385, 8) == -1     # E % P != 0
+    assert lib.moe_permute_to_experts_kernels(0, 16, 6, 384, 8) == -1     # S < 1
+    assert lib.moe_dispatch_layout_kernels(1, 16, 33, 384, 8) == -1       # k > 32
+    assert lib.moe_dispatch_layout_kernels(1, -1, 6, 384, 8) == -1        # T < 0
+
+
 FAKE = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced: the calls are rejected first
 FAKE_MIS = ctypes.c_void_p((1 << 20) + 2)
 NULL = ctypes.c_void_p(0)
