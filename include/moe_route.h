@@ -24,6 +24,8 @@
  *   moe_dispatch_layout_static      the layout for callers that cannot allocate
  *   moe_expert_scale(_mxfp8/_nvfp4) stand-in experts for tests and benchmarks
  *   moe_trace_*                     optional CUDA-event timing of launches
+ *   moe_dispatch_layout_kernels,    kernels one call enqueues for given sizes
+ *   moe_permute_to_experts_kernels  (for counting launches per step)
  *
  * Expert-parallel ranks are emulated as partitions of buffers in one GPU's
  * memory: partition p holds the L = E/P experts p*L .. p*L+L-1 (contiguous
@@ -400,6 +402,9 @@ moe_status_t moe_dispatch_pack_nvfp4(const uint16_t *x, int S, int T, int H, int
  *   ws, ws_bytes  scratch, ws_bytes >= moe_workspace_bytes(S, T, k, E, P).
  * A routed pair whose slot is -1 (inconsistent inputs) or >= cap_send gets a
  * zero row and flags MOE_ERR_INVALID_ARG or MOE_ERR_CAPACITY respectively.
+ * One kernel both places and copies the rows while the S*E counts fit in its
+ * shared memory (moe_permute_to_experts_kernels), else a placement kernel
+ * runs first; the results are the same.
  */
 moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_slot,
                                     const int32_t *topk_ids, const int32_t *expert_counts,
