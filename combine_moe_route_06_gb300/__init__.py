@@ -886,10 +886,14 @@ class HostPipeline:
         self._graphs = []
         for _ in range(sets):
             p = MoePath(S, T, H, E, k, P, device=d, **path_kwargs)
-            lg = torch.empty((S, T, E), dtype=torch.float32, device=d)
-            xx = torch.empty((S, T, H), dtype=torch.bfloat16, device=d)
+            lg = torch.zeros((S, T, E), dtype=torch.float32, device=d)
+            xx = torch.zeros((S, T, H), dtype=torch.bfloat16, device=d)
             calls = p.bind(lg, xx, self.s_step)
             if graphs:
+                # one eager step first: kernels load and the library's one-time
+                # device queries run outside the capture
+                MoePath.run_bound(calls)
+                torch.cuda.synchronize(d)
                 g = torch.cuda.CUDAGraph()
                 cap = torch.cuda.Stream(device=d)
                 with torch.cuda.graph(g, stream=cap):

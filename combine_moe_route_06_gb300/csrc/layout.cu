@@ -638,7 +638,11 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
             cudaSuccess)
             return e;
+        // Cached only once the occupancy query itself answered: a query that
+        // errors (e.g. refused while a stream is being captured) is asked
+        // again on the next call, which meanwhile takes the two-launch form.
         int g = kMaxCluster;
+        bool answered = false;
         for (; g > 1; g /= 2) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)g);
@@ -652,9 +656,17 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, k_layout_cluster, &cfg) == cudaSuccess && n > 0)
-                break;
-            (void)cudaGetLastError();          // a refused size is not an error here
+            if (cudaOccupancyMaxActiveClusters(&n, k_layout_cluster, &cfg) == cudaSuccess) {
+                answered = true;
+                if (n > 0) break;
+            } else {
+                (void)cudaGetLastError();      // a refused size is not an error here
+            }
+        }
+        if (!answered) {
+            *out = 1;
+            *max_dyn = limit;
+            return cudaSuccess;
         }
         cache[dev] = g;
     }

@@ -169,7 +169,10 @@ moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k,
  * their counts in distributed shared memory (one launch), with more they go
  * through `ws` (two launches).  Counting uses order-free integer adds and
  * ranks follow the fixed (token, slot) order, so the outputs are the same
- * bytes on every run.
+ * bytes on every run.  The first call on a device asks the device once which
+ * cluster sizes it schedules; make it before capturing a stream (a query
+ * refused during a capture is asked again on the next call, and that call
+ * takes the two-launch form).
  */
 moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, int E, int P,
                                  int32_t *expert_counts, int32_t *expert_rank,
