@@ -630,6 +630,20 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         m.trace_disable()
 
+        # ---------------- warm L2 (diagnostic) ------------------------------
+        # The same step back to back without the flush, each step timed by its
+        # own events: what a small step (decode, ~15 MB) costs when its inputs
+        # are still in the 126 MB L2 from the step before.
+        Kw = max(10, min(K, 200))
+        evw = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kw + 3)]
+        with torch.cuda.stream(stream):
+            for i in range(Kw + 3):                # the first 3 refill the L2
+                evw[i][0].record(stream)
+                run_step()
+                evw[i][1].record(stream)
+        torch.cuda.synchronize()
+        warm_us = statistics.median(1e3 * e0.elapsed_time(e1) for e0, e1 in evw[3:])
+
         # ---------------- dispatch + combine alone (diagnostic) ---------------
         # The same calls without the route (its outputs stay in the buffers),
         # as a clean graph (or eager calls), each run after an L2 flush.
@@ -775,6 +789,10 @@ def run_ours(args, world, rank, local):
                              "bytes": b["dispatch_combine"],
                              "how": "layout + pack + permute + combine as their own clean graph "
                                     "(route outputs kept), L2 flushed before each run"},
+        "warm_l2": {"us_median": round(warm_us, 2),
+                    "gbs": round(b["step"] / (warm_us * 1e-6) / 1e9, 2),
+                    "how": "the same step back to back without the L2 flush (inputs and "
+                           "buffers left in L2 by the step before), median of the steps' events"},
         "step_us": {"median": round(1e3 * statistics.median(step_ms), 2),
                     "min": round(1e3 * min(step_ms), 2), "max": round(1e3 * max(step_ms), 2)},
         "stages_us_median": {k_: round(1e3 * statistics.median(v), 2) for k_, v in stage_ms.items()},
