@@ -352,6 +352,33 @@ def run_reference(args, world, rank):
     return 0
 
 
+def stage_summary(stage_ms, b, peak, tokens, copies, pairs):
+    """Per stage of the path: µs (sum of its calls' medians from the per-stage
+    loop), algorithmic GB/s, fraction of the HBM peak and rows/s, rows being
+    what the stage writes: route and layout tokens, pack copies, permute and
+    expert pairs, combine tokens."""
+    def group(name):
+        if name == "route_topk":
+            return "route"
+        for g in ("layout", "pack", "permute", "expert"):
+            if name.startswith(g):
+                return g
+        return "combine"                   # combine, its two stages, the routed pre-add
+    us = {}
+    for name, v in stage_ms.items():
+        g = group(name)
+        us[g] = us.get(g, 0.0) + 1e3 * statistics.median(v)
+    rows = {"route": tokens, "layout": tokens, "pack": copies, "permute": pairs,
+            "expert": pairs, "combine": tokens}
+    out = {}
+    for g, t in us.items():
+        gbs = b[g] / (t * 1e-6) / 1e9 if g in b else None
+        out[g] = {"us": round(t, 2), "gbs": round(gbs, 1) if gbs else None,
+                  "frac_of_hbm_peak": round(gbs / peak, 4) if gbs else None,
+                  "rows_per_s": round(rows[g] / (t * 1e-6), 1)}
+    return out
+
+
 def workload_config(w, l2, variant="contiguous"):
     scope = "route+layout+pack+permute+combine"
     if variant == "routed":
@@ -797,6 +824,7 @@ def run_ours(args, world, rank, local):
                     "min": round(1e3 * min(step_ms), 2), "max": round(1e3 * max(step_ms), 2)},
         "stages_us_median": {k_: round(1e3 * statistics.median(v), 2) for k_, v in stage_ms.items()},
         "stages_note": "separate loop with events between calls (breaks launch overlap)",
+        "stages": stage_summary(stage_ms, b, peak, w.S * w.T, copies, pairs_recv),
         "kernels_us_median": kernels_us,
         "kernels_note": "separate loop with events around every launch (includes launch latency)",
         "stage_bytes": {k_: b[k_] for k_ in ("route", "layout", "pack", "permute", "expert", "combine")
