@@ -634,14 +634,17 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
                                       (int)limit)) != cudaSuccess)
             return e;
         dyn[dev] = limit;
-        if ((e = cudaFuncSetAttribute(k_layout_cluster,
-                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
-            cudaSuccess)
-            return e;
+        // clusters of 16 need the non-portable size; a device that refuses it
+        // gets the portable limit of 8
+        int g = kMaxCluster;
+        if (cudaFuncSetAttribute(k_layout_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) != cudaSuccess) {
+            (void)cudaGetLastError();
+            g = 8;
+        }
         // Cached only once the occupancy query itself answered: a query that
         // errors (e.g. refused while a stream is being captured) is asked
         // again on the next call, which meanwhile takes the two-launch form.
-        int g = kMaxCluster;
         bool answered = false;
         for (; g > 1; g /= 2) {
             cudaLaunchConfig_t cfg = {};
