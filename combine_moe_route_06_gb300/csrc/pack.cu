@@ -190,13 +190,14 @@ __global__ void __launch_bounds__(kPackThreads) k_pack_mxfp8(
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
             const int se = mx_shared_exp(amax);
             const float inv = __uint_as_float((uint32_t)(127 - se) << 23);   // 2^-se, exact
-            uint32_t lo = 0, hi = 0;
+            // two values per conversion (round to nearest even, saturate to
+            // finite); the pair's first value lands in the low byte
+            uint32_t c2[4];
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                lo |= (uint32_t)__nv_cvt_float_to_fp8(f[i] * inv, __NV_SATFINITE, __NV_E4M3) << (8 * i);
-                hi |= (uint32_t)__nv_cvt_float_to_fp8(f[4 + i] * inv, __NV_SATFINITE, __NV_E4M3) << (8 * i);
-            }
-            code[u] = make_uint2(lo, hi);
+            for (int i = 0; i < 4; i++)
+                c2[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(
+                    make_float2(f[2 * i] * inv, f[2 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+            code[u] = make_uint2(c2[0] | (c2[1] << 16), c2[2] | (c2[3] << 16));
             scale[u] = (uint8_t)(se + 127);
         }
         while (dmask) {
