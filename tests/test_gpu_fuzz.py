@@ -1,7 +1,8 @@
 """Seeded random shapes through the whole path on the GPU vs the oracle.
 
-Every case draws S, T, H, E, k, P, align, the receiving partition and the
-path's form (contiguous, masked, two-stage, routed) from a fixed seed, with
+Every case draws S, T (up to 2,500 tokens: up to 10 layout chunks per source,
+so the layout's cluster form too), H, E, k, P, align, the receiving partition
+and the path's form (contiguous, masked, two-stage, routed) from a fixed seed, with
 the logits sometimes quantised so that equal logits (ties) are common.  Index
 outputs and moved rows are compared bit for bit; the output is compared
 within the combine tolerance against the oracle's combine of the same expert
@@ -35,8 +36,8 @@ def _draw(seed):
     E -= E % P
     k = int(rng.integers(1, min(E, 32) + 1))
     S = int(rng.integers(1, 4))
-    T = int(rng.choice([0, 1, 7, 64, 255, 256, 257, 600]))
-    H = 8 * int(rng.integers(1, 160))
+    T = int(rng.choice([0, 1, 7, 64, 255, 256, 257, 600, 1000, 2500]))
+    H = 8 * int(rng.integers(1, 160)) if T <= 600 else 8 * int(rng.integers(1, 40))
     form = str(rng.choice(["contiguous", "contiguous", "masked", "two_stage", "routed"]))
     align = int(rng.choice([1, 1, 2, 128])) if form == "contiguous" else 1
     recv_part = int(rng.integers(-1, P)) if rng.random() < 0.5 else -1
