@@ -737,6 +737,28 @@ def run_ours(args, world, rank, local):
         pipe.release()
         del pipe
 
+        # the link's own rate for the same bytes: plain copies in (inputs) and out
+        # (output) on two streams at once, no kernels
+        d_in = torch.empty(int(h_logits.numel() * 4 + h_x.numel() * 2), dtype=torch.uint8, device=dev)
+        h_in_raw = torch.empty(d_in.numel(), dtype=torch.uint8).pin_memory()
+        d_out = torch.empty(int(h_out.numel() * 2), dtype=torch.uint8, device=dev)
+        h_out_raw = torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory()
+        s_a, s_b = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        l0.record(s_a)
+        s_b.wait_event(l0)
+        for _ in range(Ke):
+            with torch.cuda.stream(s_a):
+                d_in.copy_(h_in_raw, non_blocking=True)
+            with torch.cuda.stream(s_b):
+                h_out_raw.copy_(d_out, non_blocking=True)
+        s_a.wait_stream(s_b)
+        l1.record(s_a)
+        torch.cuda.synchronize()
+        link_us = 1e3 * l0.elapsed_time(l1) / Ke
+        del d_in, h_in_raw, d_out, h_out_raw
+
         graph = None
         torch.cuda.synchronize()
 
@@ -851,9 +873,12 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
                 "d2h_bytes_per_step": int(h_out.numel() * 2), "steps": Ke,
                 "ms_per_step": round(e2e_ms / Ke, 4), "readback_ok": out_ok,
+                "link_us_per_step": round(link_us, 1),
+                "frac_of_link": round(link_us / (1e3 * e2e_ms / Ke), 4),
                 "host_binding": host_binding,
                 "how": "HostPipeline: pinned H2D -> step -> D2H every step on 3 streams with 3 "
-                       "buffer sets; no L2 flush (each step moves ~1 GB)"},
+                       "buffer sets; no L2 flush (each step moves ~1 GB); link_us_per_step: "
+                       "plain copies of the same bytes in and out at once, no kernels"},
         # the timed steps and, between them, the instrumented copies of the step
         "gpu_launches": 2 * launches * K,
         "gpu_launches_per_step": launches,
