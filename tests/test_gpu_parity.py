@@ -12,8 +12,8 @@ import torch
 import combine_moe_route_06_gb300 as m
 import moe_synth as ms
 import oracle
-from gpu_util import (DEV, bf16_dev, bf16_host, close_bf16, f32_dev, host, i32_dev, run_layout,
-                      worst_rel)
+from gpu_util import (DEV, bf16_dev, bf16_host, close_bf16, combine_within_fp32_bound, f32_dev,
+                      host, i32_dev, run_layout, worst_rel)
 
 pytestmark = pytest.mark.gpu
 
@@ -352,6 +352,15 @@ def test_path_full_size(name):
     # the stand-in expert rounds fp32 products; the oracle rounds exact ones: at most 1 ulp apart
     assert close_bf16(y, ref["y"][:rows], rel=2.0 ** -7, floor=1e-30)
     assert close_bf16(out, ref["out"]), worst_rel(out, ref["out"])
+    # the combine's own accuracy on the rows and weights it was given: within the
+    # fp32 accumulation bound plus one bf16 unit of the oracle's exact sum
+    S, T, H, k = w_.S, w_.T, w_.H, w_.k
+    y_all = bf16_host(path.y)
+    pr = host(path.pair_row).reshape(-1, k)
+    wg = host(path.topk_w).reshape(-1, k)
+    want = oracle.combine(y_all, pr.reshape(S, T, k), wg.reshape(S, T, k)).reshape(-1, H)
+    ok, excess = combine_within_fp32_bound(out.reshape(-1, H), want, y_all, pr, wg)
+    assert ok, excess
     assert int(path.dev_status.item()) == 0
 
 
@@ -364,48 +373,71 @@ def test_identity_round_trip(name):
         assert np.array_equal(out, inp["x"])
 
 
-def test_skewed_receiver_full_size():
-    """Skewed workload (8 sources x 4096 tokens, Zipf(1.2), partition 0 receives):
-    all index outputs compared in full; moved rows and the partial combine on a
-    sample of tokens."""
-    w_ = ms.workload("skewed")
-    inp = ms.gen_inputs(w_)
-    path, out = _gpu_path(w_, inp, recv_part=w_.recv_part)
+def _skewed_reference(w_, inp):
+    """Oracle index outputs of the skewed workload.  Indices do not depend on
+    the row width, so the oracle permutes 8-wide stand-in rows; the moved rows
+    are then checked against the source tokens' rows of x."""
     ids, w64 = oracle.route_topk(inp["logits"], w_.k)
-    assert np.array_equal(host(path.topk_ids), ids)
     lay = oracle.dispatch_layout(ids, w_.E, w_.P)
-    assert np.array_equal(host(path.token_slot), lay["token_slot"])
-    assert np.array_equal(host(path.expert_counts), lay["expert_counts"])
-    # indices do not depend on the row width: the oracle permutes 8-wide stand-in rows
     cap_send = w_.T * min(w_.k, w_.P)
     narrow = np.zeros((w_.S, cap_send, 8), np.uint16)
     per = oracle.permute_to_experts(narrow, lay["token_slot"], ids, w_.E, recv_part=w_.recv_part)
+    return ids, w64, lay, per
+
+
+@pytest.mark.parametrize("expert", ["identity", "scale"])
+def test_skewed_receiver_full_size(expert):
+    """Skewed workload (8 sources x 4096 tokens, Zipf(1.2), partition 0 receives),
+    compared in full: every index output; every used receive row bit-exact
+    against its source token's row of x (recv[r] = x[s, t] for the pair
+    recv_pair[r] = (s*T + t)*k + j); every one of the 32,768 partial-combine
+    outputs against the oracle's combine.  With the stand-in expert
+    (y = bf16(recv * s_e)) every expert row is held to one bf16 unit of the
+    oracle's, and the combine to the oracle's combine of the rows it read."""
+    w_ = ms.workload("skewed")
+    inp = ms.gen_inputs(w_)
+    ids, w64, lay, per = _skewed_reference(w_, inp)
+    scales = inp["scales"] if expert == "scale" else None
+    path, out = _gpu_path(w_, inp, recv_part=w_.recv_part, scales=scales)
+    assert np.array_equal(host(path.topk_ids), ids)
+    assert np.max(np.abs(host(path.topk_w) - w64)) <= W_TOL
+    assert np.array_equal(host(path.token_slot), lay["token_slot"])
+    assert np.array_equal(host(path.expert_counts), lay["expert_counts"])
+    assert np.array_equal(host(path.part_offsets), lay["part_offsets"])
     assert np.array_equal(host(path.expert_offsets), per["expert_offsets"])
     assert np.array_equal(host(path.pair_row), per["pair_row"])
     assert np.array_equal(host(path.recv_pair), per["recv_pair"])
-    # rows: sample 512 receive rows and compare with the source token's row
-    rng = np.random.default_rng(0)
+    H, k = w_.H, w_.k
+    x_flat = inp["x"].reshape(-1, H)
     rows_used = int(per["expert_offsets"][-1])
-    sample = rng.choice(rows_used, size=min(512, rows_used), replace=False)
-    recv = bf16_host(path.recv[torch.from_numpy(sample).to(DEV)])
-    q = per["recv_pair"][sample]
-    xs = inp["x"].reshape(-1, w_.H)[q // w_.k]
-    assert np.array_equal(recv, xs)
-    # partial combine of partition 0 for 256 sampled tokens
-    toks = rng.choice(w_.S * w_.T, size=256, replace=False)
-    pr = per["pair_row"].reshape(-1, w_.k)[toks]
-    ww = w64.reshape(-1, w_.k)[toks].astype(np.float32)
-    # the expected rows come from the oracle's recv_pair and the generated x
-    uniq = np.unique(pr[pr >= 0])
-    y = np.zeros((max(len(uniq), 1), w_.H), np.uint16)
-    if len(uniq):
-        y[:len(uniq)] = inp["x"].reshape(-1, w_.H)[per["recv_pair"][uniq] // w_.k]
-    remap = -np.ones(max(rows_used, 1), np.int64)
-    remap[uniq] = np.arange(len(uniq))
-    pr_local = np.where(pr >= 0, remap[np.maximum(pr, 0)], -1).astype(np.int32)
-    ref = oracle.combine(y, pr_local[None], ww[None])[0]
-    got = out.reshape(-1, w_.H)[toks]
-    assert close_bf16(got, ref), worst_rel(got, ref)
+    recv_pair = per["recv_pair"]
+    assert rows_used > 150_000 and np.all(recv_pair[:rows_used] >= 0)
+    # every used receive row (and, with the stand-in expert, every expert row)
+    y_dev = path.recv if scales is None else path.y
+    y_all = np.empty((rows_used, H), np.uint16)
+    eoff = per["expert_offsets"]
+    for r0 in range(0, rows_used, 16384):
+        r1 = min(rows_used, r0 + 16384)
+        src = x_flat[recv_pair[r0:r1] // k]
+        assert np.array_equal(bf16_host(path.recv[r0:r1]), src), (r0, r1)
+        y_all[r0:r1] = bf16_host(y_dev[r0:r1])
+        if scales is not None:
+            # the oracle's stand-in expert on these rows (run starts relative to r0)
+            want_y = oracle.expert_scale(src, np.clip(eoff - r0, 0, r1 - r0), scales)
+            # the kernel rounds the fp32 product, the oracle the exact one: one
+            # bf16 unit apart at most
+            assert close_bf16(y_all[r0:r1], want_y, rel=2.0 ** -7, floor=1e-30), (r0, r1)
+    # every partial-combine output (tokens with no pair in partition 0 give exact 0)
+    pr_all = per["pair_row"].reshape(-1, k)
+    w_all = w64.reshape(-1, k).astype(np.float32)
+    out_all = out.reshape(-1, H)
+    for n0 in range(0, w_.S * w_.T, 4096):
+        n1 = n0 + 4096
+        pr = pr_all[n0:n1]
+        want = oracle.combine(y_all, pr[None], w_all[n0:n1][None])[0]
+        assert close_bf16(out_all[n0:n1], want), (n0, worst_rel(out_all[n0:n1], want))
+        ok, excess = combine_within_fp32_bound(out_all[n0:n1], want, y_all, pr, w_all[n0:n1])
+        assert ok, (n0, excess)
     assert int(path.dev_status.item()) == 0
 
 
