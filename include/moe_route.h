@@ -194,7 +194,12 @@ moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, i
  * MOE_ERR_INVALID_ARG and a message naming the sizes (with E = 384 and P = 8
  * that is past about 680,000 tokens in all).  The first call on a device looks
  * up the array's device address (with that device current) and caches it;
- * make that first call before capturing any stream.  All calls share the one
+ * make that first call before capturing any stream.  The cached address
+ * belongs to the device's primary context: after cudaDeviceReset (or any
+ * other teardown of that context) in the same process, do not call this entry
+ * point again.  Only sizes that take the layout's two-launch form (more
+ * 256-token chunks per source than one thread-block cluster holds, see
+ * moe_dispatch_layout_kernels) read or write the array.  All calls share the one
  * array and it keeps the last call's contents (nothing in it needs to start
  * at zero): calls that can overlap on the GPU -- on different streams, or from
  * different threads -- race on it and must be ordered by the caller.

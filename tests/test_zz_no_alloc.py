@@ -3,11 +3,15 @@
 Some callers have no way to allocate device memory at the moment they call
 the layout (a plugin whose host engine owns all device memory, plain C code
 without an allocator), so this entry point keeps its scratch in an array built
-into the library.  These tests call it through the C ABI and check that it
-gives exactly the bytes that moe_dispatch_layout gives with a caller-provided
-workspace, on two calls in a row with different shapes (the second call reuses
-the array after the first one filled it), and that sizes beyond the built-in
-array are refused.  The file is named to be collected last.
+into the library.  Only the layout's two-launch form uses that scratch: the
+chunk kernel writes every chunk's partition and expert counts into it and the
+fix-up kernel reads them back.  These tests call the entry point through the
+C ABI on two such shapes in a row (the second reads the array after the first
+one filled it with other counts), assert from the launch trace that the
+fix-up kernel ran, and check every output against the CPU oracle and against
+moe_dispatch_layout with a caller-provided workspace; sizes beyond the
+built-in array are refused.  The file sorts last so that, if it fails, a run
+that stops at the first failure has already run every other test.
 """
 import ctypes
 
@@ -43,17 +47,26 @@ def _outputs(S, T, k, E, P):
 
 
 def _static_layout(lib, ids, E, P):
+    """One call of the static entry point; returns its outputs and the names of
+    the kernels it launched (from the library's launch trace)."""
     S, T, k = ids.shape
     o = _outputs(S, T, k, E, P)
     p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    rc = lib.moe_dispatch_layout_static(p(ids), S, T, k, E, P, p(o["expert_counts"]),
-                                        p(o["expert_rank"]), p(o["part_counts"]),
-                                        p(o["part_offsets"]), p(o["token_slot"]),
-                                        p(o["dev_status"]), stream)
-    assert rc == m.MOE_OK, lib.moe_last_error_message().decode()
     torch.cuda.synchronize()
-    return {key: t.cpu().numpy() for key, t in o.items()}
+    m.trace_enable(None, 16)
+    m.trace_reset()
+    try:
+        rc = lib.moe_dispatch_layout_static(p(ids), S, T, k, E, P, p(o["expert_counts"]),
+                                            p(o["expert_rank"]), p(o["part_counts"]),
+                                            p(o["part_offsets"]), p(o["token_slot"]),
+                                            p(o["dev_status"]), stream)
+        assert rc == m.MOE_OK, lib.moe_last_error_message().decode()
+        torch.cuda.synchronize()
+        kernels = [name for name, _ in m.trace_records()]
+    finally:
+        m.trace_disable()
+    return {key: t.cpu().numpy() for key, t in o.items()}, kernels
 
 
 def _workspace_layout(ids, E, P):
@@ -66,18 +79,24 @@ def _workspace_layout(ids, E, P):
     return {key: t.cpu().numpy() for key, t in o.items()}
 
 
-def test_static_layout_matches_workspace_layout_twice(lib):
-    # first call: 8 sources x 4096 tokens (the larger scratch footprint);
-    # second call: one source of 64 tokens, reading what the first left behind
-    for name in ("skewed", "decode"):
-        w = ms.workload(name)
+def test_static_layout_uses_its_scratch_twice(lib):
+    # first call: the large workload (16,384 tokens, 64 chunks in one source,
+    # E = 64); second call: 2 sources x 5,000 tokens (20 chunks each), E = 384,
+    # whose counts overwrite and then read back the same bytes of the array
+    cases = [ms.workload("large"), ms.workload("prefill", S=2, T=5000, index=17)]
+    for w in cases:
+        assert lib.moe_dispatch_layout_kernels(w.S, w.T, w.k, w.E, w.P) == 2, w
         ids_np, _ = oracle.route_topk(ms.gen_logits(w), w.k)
         ids = torch.from_numpy(ids_np).cuda()
-        got = _static_layout(lib, ids, w.E, w.P)
+        got, kernels = _static_layout(lib, ids, w.E, w.P)
+        assert kernels == ["k_layout_local", "k_layout_fix"], (w.name, kernels)
+        ref = oracle.dispatch_layout(ids_np, w.E, w.P)
+        for key in KEYS:
+            assert np.array_equal(got[key], ref[key]), (w.name, key)
+        assert int(got["dev_status"][0]) == ref["status"] == 0
         want = _workspace_layout(ids, w.E, w.P)
         for key in KEYS:
-            assert np.array_equal(got[key], want[key]), (name, key)
-        assert int(got["dev_status"][0]) == int(want["dev_status"][0]) == 0
+            assert np.array_equal(got[key], want[key]), (w.name, key)
 
 
 def test_static_layout_refuses_sizes_beyond_its_scratch(lib):
