@@ -46,11 +46,29 @@ DOMINANT_BY_VARIANT = {"two_stage": ("k_combine_stage1", "stage1"),
                        "mxfp8": ("k_combine", "combine"),
                        "nvfp4": ("k_combine", "combine"),
                        "routed": ("k_routed_stage1", "stage1")}
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_perm_copy
-# launch in the prefill pipeline, from an ncu capture with the L2 left as the
-# previous kernel left it (--cache-control none).  Taken on the current kernel;
-# it must be re-measured whenever k_perm_copy changes.
-DOMINANT_TRAFFIC = {"prefill": 142.5e6 + 252.9e6}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# dominant kernel in the prefill pipeline, from an ncu capture with the L2 left
+# as the previous kernel left it (--cache-control none), with the SHA-256 prefix
+# of the source file the kernel was built from when it was captured (commit
+# 120a03f for k_perm_copy).  The line reports null instead once that file has
+# changed, so a stale capture is never quoted.
+DOMINANT_TRAFFIC = {("k_perm_copy", "prefill"): {"bytes": 142.5e6 + 252.9e6,
+                                                 "source": "combine_moe_route_06_gb300/csrc/permute.cu",
+                                                 "sha16": "9a2fb6e795daf9b3"}}
+
+
+def dominant_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` at `workload` if the capture is current, else None."""
+    import hashlib
+    rec = DOMINANT_TRAFFIC.get((kernel, workload))
+    if rec is None:
+        return None
+    try:
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["bytes"] if sha == rec["sha16"] else None
 
 
 # ------------------------------------------------------------ byte model --
@@ -491,6 +509,68 @@ def bind_to_gpu_numa(torch, local):
         return {"bound": False, "why": str(exc)[:80]}
 
 
+def time_other_workload(m, torch, name, steps, dev, local, flush_l2, peak, variant_kw):
+    """Step time of another workload on the same GPU, with the headline's protocol:
+    the step recorded once into a CUDA graph and replayed, the L2 flushed before
+    every timed step, CUDA events around each step, nvidia-smi clocks sampled
+    meanwhile.  Returns the workload's summary for the JSON line."""
+    w = ms.workload(name)
+    inp = ms.gen_inputs(w)
+    path = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev,
+                     **variant_kw)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    del inp
+    stream = torch.cuda.Stream(device=dev)
+    calls = path.bind(logits, x, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush_l2()
+            m.MoePath.run_bound(calls)
+    torch.cuda.synchronize()
+    path.dev_status.zero_()
+    m.MoePath.run_bound(calls)
+    torch.cuda.synchronize()
+    status = int(path.dev_status.item())
+    copies = int(path.part_offsets[:, -1].sum().item())
+    copies_recv = copies if w.recv_part < 0 else int(path.part_counts[:, w.recv_part].sum().item())
+    pairs_recv = int((path.pair_row >= 0).sum().item())
+    b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv)
+    cap = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        m.MoePath.run_bound(path.bind(logits, x, cap))
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    sampler = ClockSampler(physical_gpu_index(local))
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush_l2()
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    clocks = sampler.stop(t0, t1)
+    graph = None
+    torch.cuda.synchronize()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    tot_s = sum(step_ms) * 1e-3
+    gbs = b["step"] * steps / tot_s / 1e9
+    return {"workload": f"{w.name}: S={w.S} T={w.T} H={w.H} bf16, E={w.E} top-{w.k}, "
+                        f"P={w.P} partitions, recv_part={w.recv_part}",
+            "steps": steps, "step_us_median": round(1e3 * statistics.median(step_ms), 2),
+            "step_us_mean": round(1e3 * statistics.fmean(step_ms), 2),
+            "gbs": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
+            "rows_per_s": round(w.S * w.T * steps / tot_s, 1), "bytes_per_step": b["step"],
+            "copies_per_token": round(copies / (w.S * w.T), 4), "pairs_recv": pairs_recv,
+            "launches_per_step": path.launches_per_step(), "dev_status": status,
+            "clocks": clocks}
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -797,6 +877,17 @@ def run_ours(args, world, rank, local):
             raise RuntimeError(f"{traced_per_step} kernels traced per step, {launches} expected")
         kernels_us = {name: round(1e3 * statistics.median(v), 2) for name, v in kern.items()}
 
+        # ---------------- the other GPU workloads (same protocol, rank 0) --------
+        others = None
+        if rank == 0 and args.other_workloads and args.variant == "contiguous":
+            peak_o, _ = measured_peak()
+            others = {}
+            for name in [n for n in ("decode", "large", "skewed") if n != w.name]:
+                steps_o = {"decode": 500, "large": 200, "skewed": 100}[name]
+                others[name] = time_other_workload(m, torch, name, steps_o, dev, local, flush_l2,
+                                                   peak_o, path_kwargs(args, ms.workload(name)))
+                torch.cuda.empty_cache()
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -859,7 +950,8 @@ def run_ours(args, world, rank, local):
                      "achieved": round(dom_achieved, 1) if dom_achieved else None,
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(dom_achieved / peak, 4) if dom_achieved else None,
-                     "traffic": (DOMINANT_TRAFFIC.get(w.name) if args.variant == "contiguous" else None),
+                     "traffic": (dominant_traffic(dom_name, w.name) if args.variant == "contiguous"
+                                 else None),
                      "bytes_per_launch": b[dom_key],
                      "us_per_launch": round(1e3 * dom_ms, 2) if dom_ms else None,
                      "launches_timed": len(recs),
@@ -886,6 +978,7 @@ def run_ours(args, world, rank, local):
         "launch_mode": "eager" if args.eager else "cuda_graph_replay",
         "host_enqueue_us_per_step": round(host_enqueue_us, 1),
         "clocks": clocks,
+        "other_workloads": others,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
@@ -910,6 +1003,8 @@ def main(argv=None):
                     help="spare copy slots per partition for --variant placed")
     ap.add_argument("--block-rows", type=int, default=0,
                     help="rows per expert block of the masked layout (default S*T)")
+    ap.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
+                    help="skip timing the decode, large and skewed workloads after the headline")
     ap.add_argument("--eager", action="store_true",
                     help="launch the calls from the host every step instead of replaying a CUDA graph")
     ap.add_argument("--profile", action="store_true",
