@@ -111,6 +111,12 @@ def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_sta
     b["dispatch_combine"] = b["layout"] + b["pack"] + b["permute"] + b["combine"] + b.get("expert", 0)
     b["step"] = b["route"] + b["dispatch_combine"]
     b["perm_copy"] = copies_recv * R + pairs_recv * R + NT * k * 8
+    # moe_dispatch: the four calls in one; its pack + permute kernel reads each
+    # receiving send row back right after storing it (an L2 hit), so the bytes it
+    # must move through HBM are the pack's and the permute's less that re-read
+    b["dispatch"] = b["route"] + b["layout"] + b["pack"] + b["permute"]
+    b["pack_permute"] = b["pack"] + b["permute"] - copies_recv * R
+    b["step_hbm_fused"] = b["step"] - copies_recv * R
     return b
 
 
@@ -175,7 +181,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
-    def __init__(self, gpu_index: int, interval_ms: int = 100):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.cmd = ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
                     "--format=csv,noheader,nounits", "-lms", str(interval_ms)]
         self.lines = []
@@ -210,9 +216,14 @@ class ClockSampler:
         self.th.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ts, ln in self.lines:
-            if t0 is not None and not (t0 <= ts <= t1):
-                continue
+        # samples taken while the loop ran; a loop shorter than the sampling
+        # interval takes the samples nearest to it (within 0.25 s) instead
+        lines = [(ts, ln) for ts, ln in self.lines if t0 is None or t0 <= ts <= t1]
+        window = "timed loop"
+        if not lines and t0 is not None:
+            lines = [(ts, ln) for ts, ln in self.lines if t0 - 0.25 <= ts <= t1 + 0.25]
+            window = "within 0.25 s of the timed loop (shorter than the sampling interval)"
+        for ts, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) != len(self.FIELDS):
                 continue
@@ -226,7 +237,7 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
 def physical_gpu_index(local: int) -> int:
@@ -378,6 +389,8 @@ def stage_summary(stage_ms, b, peak, tokens, copies, pairs):
     def group(name):
         if name == "route_topk":
             return "route"
+        if name == "dispatch":
+            return "dispatch"
         for g in ("layout", "pack", "permute", "expert"):
             if name.startswith(g):
                 return g
@@ -387,7 +400,7 @@ def stage_summary(stage_ms, b, peak, tokens, copies, pairs):
         g = group(name)
         us[g] = us.get(g, 0.0) + 1e3 * statistics.median(v)
     rows = {"route": tokens, "layout": tokens, "pack": copies, "permute": pairs,
-            "expert": pairs, "combine": tokens}
+            "expert": pairs, "combine": tokens, "dispatch": pairs}
     out = {}
     for g, t in us.items():
         gbs = b[g] / (t * 1e-6) / 1e9 if g in b else None
@@ -448,6 +461,8 @@ def path_kwargs(args, w):
     times the mean pairs per expert (at least 64 rows, at most every token of
     every source); the JSON line's dev_status shows whether any pair was dropped."""
     kw = dict(VARIANTS[args.variant])
+    if args.dispatch != "auto":
+        kw["dispatch"] = args.dispatch
     if kw.get("layout") == "masked":
         mean = -(-w.S * w.T * w.k // w.E)
         kw["block_rows"] = args.block_rows or min(w.S * w.T, max(64, 4 * mean))
@@ -567,7 +582,8 @@ def time_other_workload(m, torch, name, steps, dev, local, flush_l2, peak, varia
             "gbs": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
             "rows_per_s": round(w.S * w.T * steps / tot_s, 1), "bytes_per_step": b["step"],
             "copies_per_token": round(copies / (w.S * w.T), 4), "pairs_recv": pairs_recv,
-            "launches_per_step": path.launches_per_step(), "dev_status": status,
+            "launches_per_step": path.launches_per_step(), "dispatch_mode": path.dispatch_mode,
+            "dev_status": status,
             "clocks": clocks}
 
 
@@ -645,6 +661,12 @@ def run_ours(args, world, rank, local):
                               mxfp8=(args.variant == "mxfp8"), routed=(args.variant == "routed"),
                               nvfp4=(args.variant == "nvfp4"))
         dom_name, dom_key = DOMINANT_BY_VARIANT.get(args.variant, (DOMINANT, "perm_copy"))
+        if path.dispatch_mode == "fused":
+            # the longest kernel of the fused step: pack + permute in one pass, or
+            # the whole dispatch in one launch for a decode-sized batch
+            dom_name, dom_key = (("k_dispatch_small", "dispatch")
+                                 if m.moe_dispatch_kernels(w.S, w.T, w.k, w.E, w.P) == 1
+                                 else ("k_pack_permute", "pack_permute"))
         if placement_info is not None:
             # pairs per partition on the timed batch: contiguous blocks vs the placement
             ids_h = path.topk_ids.cpu().numpy()
@@ -754,16 +776,19 @@ def run_ours(args, world, rank, local):
         # ---------------- dispatch + combine alone (diagnostic) ---------------
         # The same calls without the route (its outputs stay in the buffers),
         # as a clean graph (or eager calls), each run after an L2 flush.
+        # (With moe_dispatch the route runs inside the dispatch call, so this is the
+        # whole step.)
         Kd = max(10, min(K, 500))
+        dc_start = 1 if path.dispatch_mode == "separate" else 0
         if not args.eager:
             graph_dc = torch.cuda.CUDAGraph()
             cap_dc = torch.cuda.Stream(device=dev)
             with torch.cuda.graph(graph_dc, stream=cap_dc):
-                m.MoePath.run_bound(path.bind(logits, x, cap_dc), start=1)
+                m.MoePath.run_bound(path.bind(logits, x, cap_dc), start=dc_start)
             torch.cuda.synchronize()
             run_dc = graph_dc.replay
         else:
-            run_dc = lambda: m.MoePath.run_bound(calls, start=1)  # noqa: E731
+            run_dc = lambda: m.MoePath.run_bound(calls, start=dc_start)  # noqa: E731
         ev_dc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kd)]
         for i in range(Kd):
             flush_l2()
@@ -927,8 +952,11 @@ def run_ours(args, world, rank, local):
         "dispatch_combine": {"gbs": round(dc_gbs, 2), "us_median": round(1e3 * statistics.median(dc_ms), 2),
                              "frac_of_hbm_peak": round(dc_gbs / peak, 4),
                              "bytes": b["dispatch_combine"],
-                             "how": "layout + pack + permute + combine as their own clean graph "
-                                    "(route outputs kept), L2 flushed before each run"},
+                             "how": ("layout + pack + permute + combine as their own clean graph "
+                                     "(route outputs kept), L2 flushed before each run"
+                                     if dc_start == 1 else
+                                     "the whole step (moe_dispatch routes inside the call), "
+                                     "as its own clean graph, L2 flushed before each run")},
         "warm_l2": {"us_median": round(warm_us, 2),
                     "gbs": round(b["step"] / (warm_us * 1e-6) / 1e9, 2),
                     "how": "the same step back to back without the L2 flush (inputs and "
@@ -976,6 +1004,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches_per_step": launches,
         "gpu_launches_per_step_traced": traced_per_step,
         "launch_mode": "eager" if args.eager else "cuda_graph_replay",
+        "dispatch_mode": path.dispatch_mode,
         "host_enqueue_us_per_step": round(host_enqueue_us, 1),
         "clocks": clocks,
         "other_workloads": others,
@@ -1003,6 +1032,9 @@ def main(argv=None):
                     help="spare copy slots per partition for --variant placed")
     ap.add_argument("--block-rows", type=int, default=0,
                     help="rows per expert block of the masked layout (default S*T)")
+    ap.add_argument("--dispatch", choices=["auto", "fused", "separate"], default="auto",
+                    help="moe_dispatch (route+layout+pack+permute in one call; the default for "
+                         "contiguous bf16 rows) or the four separate calls")
     ap.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
                     help="skip timing the decode, large and skewed workloads after the headline")
     ap.add_argument("--eager", action="store_true",

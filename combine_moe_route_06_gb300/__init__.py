@@ -26,7 +26,8 @@ __all__ = [
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CAPACITY", "MOE_ERR_BAD_EXPERT_ID",
     "MOE_ERR_TIMEOUT", "MOE_ERR_CUDA", "status_bit", "MoeError", "MoeLibraryMissing",
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
-    "moe_dispatch_layout_kernels", "moe_permute_to_experts_kernels",
+    "moe_dispatch_layout_kernels", "moe_permute_to_experts_kernels", "moe_dispatch_kernels",
+    "moe_dispatch",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
     "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
@@ -91,6 +92,9 @@ def load_library() -> ctypes.CDLL:
             "moe_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
             "moe_dispatch_layout_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
             "moe_permute_to_experts_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
+            "moe_dispatch_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
+            "moe_dispatch": ([P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P, P, P,
+                              P, P, P, P, P, P, P, P, P, P, sz, P, P], ctypes.c_int),
             "moe_route_topk": ([P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
             "moe_dispatch_layout": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P, P],
                                     ctypes.c_int),
@@ -408,6 +412,39 @@ def moe_permute_to_experts(send, token_slot, topk_ids, expert_counts, expert_ran
         _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
 
 
+def moe_dispatch(logits, x, E, P, recv_part, align, topk_ids, topk_w, expert_counts, expert_rank,
+                 part_counts, part_offsets, token_slot, send, send_src, recv, expert_offsets,
+                 pair_row, recv_pair, ws, dev_status=None, stream=None):
+    """route + layout + pack + permute in one call (the outputs of the four calls).
+    logits fp32 [S,T,E], x bf16 [S,T,H] in; the rest as the four calls."""
+    lib = load_library()
+    S, T, H = x.shape
+    k = topk_ids.shape[2]
+    cap_send = send.shape[1]
+    cap_recv = recv.shape[0]
+    _check(lib.moe_dispatch(
+        _dev(logits, "logits", (torch.float32,), 3), _dev(x, "x", _BF16_TYPES, 3), S, T, H, E, k,
+        P, recv_part, align, cap_send, cap_recv, _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+        _dev(topk_w, "topk_w", (torch.float32,), 3),
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)),
+        _dev(part_counts, "part_counts", (torch.int32,)),
+        _dev(part_offsets, "part_offsets", (torch.int32,)),
+        _dev(token_slot, "token_slot", (torch.int32,), 3), _dev(send, "send", _BF16_TYPES, 3),
+        _dev(send_src, "send_src", (torch.int32,)), _dev(recv, "recv", _BF16_TYPES, 2),
+        _dev(expert_offsets, "expert_offsets", (torch.int32,)),
+        _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
+        _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_kernels(S, T, k, E, P) -> int:
+    """Kernels one moe_dispatch call with these sizes enqueues on the current device."""
+    n = load_library().moe_dispatch_kernels(S, T, k, E, P)
+    if n < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_dispatch_kernels: invalid sizes")
+    return n
+
+
 def moe_permute_to_experts_masked(send, token_slot, topk_ids, expert_counts, expert_rank, E,
                                   recv_part, block_rows, recv, masked_counts, pair_row, recv_pair,
                                   dev_status=None, stream=None):
@@ -525,7 +562,8 @@ class MoePath:
 
     def __init__(self, S, T, H, E, k, P, recv_part=-1, align=1, cap_send=None, cap_recv=None,
                  device="cuda", layout="contiguous", block_rows=None, combine="single",
-                 quant="none", placement: "Placement | None" = None, nvfp4_scale: float = 1.0):
+                 quant="none", placement: "Placement | None" = None, nvfp4_scale: float = 1.0,
+                 dispatch: str | None = None):
         """layout: "contiguous" (expert runs, moe_permute_to_experts), "masked" (one
         block of block_rows rows per expert, moe_permute_to_experts_masked) or "routed"
         (no permute: rows carry their ids and weights, moe_dispatch_pack_routed, and
@@ -536,7 +574,10 @@ class MoePath:
         nvfp4_scale is the NVFP4 per-tensor scale.
         placement: a Placement (moe_plan_placement) -- the layout then maps each
         pair to a physical expert slot and everything after it works on the
-        P*Lp physical experts; None keeps expert e in slot e."""
+        P*Lp physical experts; None keeps expert e in slot e.
+        dispatch: "fused" (moe_dispatch: route, layout, pack and permute in one call,
+        one launch for a decode-sized batch) or "separate" (the four calls); the
+        default is "fused" where it applies (contiguous bf16 rows, no placement)."""
         if layout not in ("contiguous", "masked", "routed") or combine not in ("single", "two_stage"):
             raise ValueError("layout must be contiguous|masked|routed, combine single|two_stage")
         if layout == "routed":
@@ -549,6 +590,13 @@ class MoePath:
             raise ValueError("mxfp8 rows need H % 512 == 0 and the contiguous layout")
         if quant == "nvfp4" and (H % 256 != 0 or layout != "contiguous"):
             raise ValueError("nvfp4 rows need H % 256 == 0 and the contiguous layout")
+        fusable = layout == "contiguous" and quant == "none" and placement is None
+        if dispatch is None:
+            dispatch = "fused" if fusable else "separate"
+        if dispatch not in ("fused", "separate") or (dispatch == "fused" and not fusable):
+            raise ValueError("dispatch must be fused|separate; fused needs contiguous bf16 rows "
+                             "and no placement")
+        self.dispatch_mode = dispatch
         self.quantized = quant != "none"
         self.nvfp4_scale = float(nvfp4_scale)
         if placement is not None and (placement.E != E or placement.P != P):
@@ -632,6 +680,18 @@ class MoePath:
         stp = vp(self.dev_status.data_ptr())
         Hp, Ep = self.Hp, self.Ep
         ids_p = vp(self.phys_ids.data_ptr())
+        if self.dispatch_mode == "fused":
+            calls = [(lib.moe_dispatch, (
+                ptr(logits, "logits", (torch.float32,)), ptr(x, "x", _BF16_TYPES), S, T, H, E, k, P,
+                self.recv_part, self.align, self.cap_send, self.cap_recv,
+                vp(self.topk_ids.data_ptr()), vp(self.topk_w.data_ptr()),
+                vp(self.expert_counts.data_ptr()), vp(self.expert_rank.data_ptr()),
+                vp(self.part_counts.data_ptr()), vp(self.part_offsets.data_ptr()),
+                vp(self.token_slot.data_ptr()), vp(self.send.data_ptr()),
+                vp(self.send_src.data_ptr()), vp(self.recv.data_ptr()),
+                vp(self.expert_offsets.data_ptr()), vp(self.pair_row.data_ptr()),
+                vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st))]
+            return calls + self._bind_combine(lib, self.recv, stp, st, ids_p)
         calls = [
             (lib.moe_route_topk, (ptr(logits, "logits", (torch.float32,)), S, T, E, k,
                                   vp(self.topk_ids.data_ptr()), vp(self.topk_w.data_ptr()), st)),
@@ -711,20 +771,24 @@ class MoePath:
                     ptr(self._bound_scale, "scale", (torch.float32,)), Ep, H, self.nvfp4_scale,
                     self.cap_recv, vp(self.y.data_ptr()), st)))
             y = self.y
+        return calls + self._bind_combine(lib, y, stp, st, ids_p)
+
+    def _bind_combine(self, lib, y, stp, st, ids_p):
+        """The bound combine call(s) reading expert rows y."""
+        S, T, H, k, P, Ep = self.S, self.T, self.H, self.k, self.P, self.Ep
+        vp = ctypes.c_void_p
         if self.combine_mode == "two_stage":
-            calls.append((lib.moe_combine_stage1, (
-                vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
-                vp(self.topk_w.data_ptr()), ids_p,
-                vp(self.token_slot.data_ptr()), S, T, k, Ep, P, H, self.recv_part, self.cap_send,
-                vp(self.ret.data_ptr()), stp, st)))
-            calls.append((lib.moe_combine_stage2, (
-                vp(self.ret.data_ptr()), vp(self.token_slot.data_ptr()), S, T, P, H,
-                self.recv_part, self.cap_send, vp(self.out.data_ptr()), stp, st)))
-        else:
-            calls.append((lib.moe_combine, (
-                vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
-                vp(self.topk_w.data_ptr()), S, T, k, H, vp(self.out.data_ptr()), stp, st)))
-        return calls
+            return [(lib.moe_combine_stage1, (
+                        vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
+                        vp(self.topk_w.data_ptr()), ids_p,
+                        vp(self.token_slot.data_ptr()), S, T, k, Ep, P, H, self.recv_part,
+                        self.cap_send, vp(self.ret.data_ptr()), stp, st)),
+                    (lib.moe_combine_stage2, (
+                        vp(self.ret.data_ptr()), vp(self.token_slot.data_ptr()), S, T, P, H,
+                        self.recv_part, self.cap_send, vp(self.out.data_ptr()), stp, st))]
+        return [(lib.moe_combine, (
+            vp(y.data_ptr()), self.cap_recv, vp(self.pair_row.data_ptr()),
+            vp(self.topk_w.data_ptr()), S, T, k, H, vp(self.out.data_ptr()), stp, st))]
 
     @staticmethod
     def run_bound(calls, upto: int | None = None, start: int = 0):
@@ -824,10 +888,21 @@ class MoePath:
         moe_combine_stage2(self.ret, self.token_slot, self.out, self.dev_status, stream,
                                recv_part=self.recv_part)
 
+    def dispatch_fused(self, logits, x, stream=None):
+        """route + layout + pack + permute through one moe_dispatch call."""
+        moe_dispatch(logits, x, self.E, self.P, self.recv_part, self.align, self.topk_ids,
+                     self.topk_w, self.expert_counts, self.expert_rank, self.part_counts,
+                     self.part_offsets, self.token_slot, self.send, self.send_src, self.recv,
+                     self.expert_offsets, self.pair_row, self.recv_pair, self.ws,
+                     self.dev_status, stream)
+
     def step(self, logits, x, scale=None, stream=None):
         """route -> layout -> pack -> permute -> [stand-in expert] -> combine; returns out."""
-        self.route(logits, stream)
-        self.dispatch(x, stream)
+        if self.dispatch_mode == "fused":
+            self.dispatch_fused(logits, x, stream)
+        else:
+            self.route(logits, stream)
+            self.dispatch(x, stream)
         if self.layout == "routed":
             self.routed_combine(scale, stream)
             return self.out
@@ -842,6 +917,12 @@ class MoePath:
         2: map + copy), stand-in expert 1 (always with quantized rows), combine 1
         (2 when split into two stages)."""
         with_expert = with_expert or self.quantized
+        if self.dispatch_mode == "fused":
+            comb = 2 if self.combine_mode == "two_stage" else 1
+            if self.T == 0:
+                comb = 0                   # the combine launches nothing for an empty batch
+            return (moe_dispatch_kernels(self.S, self.T, self.k, self.E, self.P) + comb
+                    + (1 if with_expert else 0))
         mapped = self.placement is not None
         if mapped:
             layout = moe_dispatch_layout_kernels(self.S, self.T, self.k, self.Ep, self.P)

@@ -42,6 +42,52 @@ __device__ __forceinline__ int warp_sum(int v)
     return v;
 }
 
+// Whether expert e (of E, L per partition) is held by the receiving set:
+// partition recv_part, or every partition when recv_part < 0.
+__device__ __forceinline__ bool in_recv(int e, int E, int L, int recv_part)
+{
+    return e >= 0 && e < E && (recv_part < 0 || e / L == recv_part);
+}
+
+// Exclusive scan of n <= 1024 values in shared memory by a 256-thread CTA;
+// returns the total.  `a` is overwritten with the exclusive prefix.
+__device__ __forceinline__ int block_exclusive_scan_1024(int *a, int n)
+{
+    __shared__ int wsum[8];
+    __shared__ int total;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    int v[4];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int idx = tid * 4 + i;
+        v[i] = (idx < n) ? a[idx] : 0;
+        local += v[i];
+    }
+    const int inc = warp_inclusive_scan(local);
+    if (lane == 31) wsum[w] = inc;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int i = 0; i < 8; i++) {
+            const int t = wsum[i];
+            wsum[i] = run;
+            run += t;
+        }
+        total = run;
+    }
+    __syncthreads();
+    int run = wsum[w] + inc - local;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int idx = tid * 4 + i;
+        if (idx < n) a[idx] = run;
+        run += v[i];
+    }
+    __syncthreads();
+    return total;
+}
+
 // Set a status bit (MOE_STATUS_BIT(code)) in the caller's word.
 __device__ __forceinline__ void flag_status(uint32_t *dev_status, int code)
 {

@@ -40,50 +40,6 @@ constexpr int kMapThreads = 256;
 constexpr int kMapPairs = 4 * kMapThreads;      // pairs per CTA
 constexpr size_t kFusedMapSmem = 48 * 1024;     // map step inside the copy up to this smem
 
-__device__ __forceinline__ bool in_recv(int e, int E, int L, int recv_part)
-{
-    return e >= 0 && e < E && (recv_part < 0 || e / L == recv_part);
-}
-
-// Exclusive scan of n <= 1024 values in shared memory by a 256-thread CTA;
-// returns the total.  `a` is overwritten with the exclusive prefix.
-__device__ int block_exclusive_scan_1024(int *a, int n)
-{
-    __shared__ int wsum[8];
-    __shared__ int total;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    int v[4];
-    int local = 0;
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int idx = tid * 4 + i;
-        v[i] = (idx < n) ? a[idx] : 0;
-        local += v[i];
-    }
-    const int inc = warp_inclusive_scan(local);
-    if (lane == 31) wsum[w] = inc;
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int i = 0; i < 8; i++) {
-            const int t = wsum[i];
-            wsum[i] = run;
-            run += t;
-        }
-        total = run;
-    }
-    __syncthreads();
-    int run = wsum[w] + inc - local;
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int idx = tid * 4 + i;
-        if (idx < n) a[idx] = run;
-        run += v[i];
-    }
-    __syncthreads();
-    return total;
-}
-
 // grid = S * B CTAs; CTA (s, b) maps pairs [b*kMapPairs, (b+1)*kMapPairs) of source s.
 // Every global load is issued before the first barrier so their latencies overlap.
 __global__ void __launch_bounds__(kMapThreads) k_perm_map(

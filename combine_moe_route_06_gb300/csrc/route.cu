@@ -5,17 +5,11 @@
 // per expert.  Chosen: the k largest logits, in descending order, equal logits
 // resolved to the lower id.  Weights: softmax over the k chosen logits in fp32.
 //
-// One warp per token row.  Lane l holds logits l, l+32, l+64, ... in registers
-// (coalesced 128-byte loads) and tracks its own two best; k rounds of a warp
-// arg-max (value desc, id asc) pick the experts (one redux.sync max over
-// order-preserving keys, one redux.sync min over the tied ids), and the
-// winning lane promotes its second best, rescanning only when that is used up.
-#include <float.h>
-#include <limits.h>
-#include <math.h>
-
+// One warp per token row (route_token_warp in route_warp.cuh: every lane keeps
+// its two best logits, k rounds of a warp arg-max pick the experts).
 #include "common.cuh"
 #include "launch.h"
+#include "route_warp.cuh"
 #include "trace.h"
 
 namespace moe {
@@ -30,91 +24,12 @@ __global__ void __launch_bounds__(256) k_route_topk(const float *__restrict__ lo
     const int lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (n >= N) return;  // uniform per warp
-    const float *row = logits + n * E;
-
-    // order-preserving keys; 0 marks "out of range"
-    unsigned key[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; i++) {
-        const int e = lane + 32 * i;
-        key[i] = (e < E) ? float_key(__ldcs(row + e)) : 0u;
-    }
-
-    // This lane's two best live elements, ordered by (key desc, index asc): a
-    // strict comparison while i ascends keeps the lower index first on ties.
-    // A lane whose best is chosen promotes its second; only a lane chosen a
-    // third time rescans its remaining elements (retired ones are in rmask).
-    unsigned k1 = 0, k2 = 0, rmask = 0;
-    int i1 = 0, i2 = 0;
-    bool have2 = true;
-#pragma unroll
-    for (int i = 0; i < VPL; i++) {
-        const unsigned v = key[i];
-        if (v > k1) {
-            k2 = k1;
-            i2 = i1;
-            k1 = v;
-            i1 = i;
-        } else if (v > k2) {
-            k2 = v;
-            i2 = i;
-        }
-    }
-
-    unsigned my_key = 0;
-    int my_id = -1;
-    for (int r = 0; r < k; r++) {
-        // warp arg-max: largest key, then the lowest id holding it
-        const unsigned mx = __reduce_max_sync(kFull, k1);
-        const unsigned cand = (k1 == mx) ? (unsigned)(lane + 32 * i1) : 0xffffffffu;
-        const unsigned win = __reduce_min_sync(kFull, cand);
-        if (lane == r) {
-            my_key = mx;
-            my_id = (int)win;
-        }
-        bool rescan = false;
-        if ((int)(win & 31u) == lane) {
-            rmask |= 1u << i1;
-            if (have2) {
-                k1 = k2;
-                i1 = i2;
-                have2 = false;
-            } else {
-                rescan = true;
-            }
-        }
-        if (__any_sync(kFull, rescan) && rescan) {
-            k1 = 0;
-            k2 = 0;
-            i1 = 0;
-            i2 = 0;
-#pragma unroll
-            for (int i = 0; i < VPL; i++) {
-                const unsigned v = ((rmask >> i) & 1u) ? 0u : key[i];
-                if (v > k1) {
-                    k2 = k1;
-                    i2 = i1;
-                    k1 = v;
-                    i1 = i;
-                } else if (v > k2) {
-                    k2 = v;
-                    i2 = i;
-                }
-            }
-            have2 = true;
-        }
-    }
-
-    // softmax over the k chosen logits: lane j < k holds choice j
-    const float my_v = key_float(my_key);
-    const float lmax = __shfl_sync(kFull, my_v, 0);
-    const float ex = (lane < k) ? expf(my_v - lmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    int id;
+    float wt;
+    route_token_warp<VPL>(logits + n * E, E, k, id, wt);
     if (lane < k) {
-        ids[n * k + lane] = my_id;
-        w[n * k + lane] = ex / sum;
+        ids[n * k + lane] = id;
+        w[n * k + lane] = wt;
     }
 }
 

@@ -12,6 +12,8 @@
  *   moe_permute_to_experts  receiver side: rows -> expert-contiguous runs    (sections 1.5, 3.3, 5.1)
  *   moe_combine             weighted sum of expert outputs back in token
  *                           order, fp32 accumulation, bf16 out               (sections 7.1, 7.2)
+ *   moe_dispatch            route + layout + pack + permute in one call,
+ *                           one launch for a decode-sized batch              (section 1.4)
  *
  * Further forms of the same round trip, each declared below with its source:
  *   moe_permute_to_experts_masked   a fixed block per expert plus a count     (sections 4.1, 4.2)
@@ -421,6 +423,46 @@ moe_status_t moe_permute_to_experts(const uint16_t *send, const int32_t *token_s
                                     int cap_recv, uint16_t *recv, int32_t *expert_offsets,
                                     int32_t *pair_row, int32_t *recv_pair, void *ws,
                                     size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
+
+/*
+ * The dispatch side in one call: moe_route_topk, moe_dispatch_layout,
+ * moe_dispatch_pack and moe_permute_to_experts on the same arguments, with
+ * the same outputs byte for byte, in fewer launches (a2a-backends section 1.4:
+ * a decode step makes a round trip per MoE layer, so its fixed cost per call
+ * matters; sections 1.1, 1.3, 3.2, 3.3, 5.1 for the steps).
+ *   logits [S][T][E] fp32 in; x [S][T][H] bf16 in.
+ *   topk_ids, topk_w                   out, as moe_route_topk.
+ *   expert_counts, expert_rank, part_counts, part_offsets, token_slot
+ *                                      out, as moe_dispatch_layout.
+ *   send, send_src, cap_send           as moe_dispatch_pack.
+ *   recv, expert_offsets, pair_row, recv_pair, recv_part, align, cap_recv
+ *                                      as moe_permute_to_experts.
+ *   ws, ws_bytes  scratch, ws_bytes >= moe_workspace_bytes(S, T, k, E, P).
+ * Forms (moe_dispatch_kernels reports the launch count):
+ *   - one source of 1..256 tokens: one kernel.  Clusters of 8 CTAs route the
+ *     batch, every CTA lays it out in its own shared memory, then the grid
+ *     moves the rows;
+ *   - otherwise: the routing kernel, the layout's kernel(s), then one kernel
+ *     that packs and permutes in the same pass (or the separate pack and
+ *     permute when the S*E counts do not fit its shared memory, and for T = 0).
+ * In both, the receive rows are read from the send rows of the receiving
+ * partitions right after they are stored (by the same warp), so the bytes
+ * placed in recv are the bytes in send, as in the separate calls.
+ * Errors: those of the four calls.  Routing never produces an id < 0 or >= E.
+ */
+moe_status_t moe_dispatch(const float *logits, const uint16_t *x, int S, int T, int H, int E,
+                          int k, int P, int recv_part, int align, int cap_send, int cap_recv,
+                          int32_t *topk_ids, float *topk_w, int32_t *expert_counts,
+                          int32_t *expert_rank, int32_t *part_counts, int32_t *part_offsets,
+                          int32_t *token_slot, uint16_t *send, int32_t *send_src, uint16_t *recv,
+                          int32_t *expert_offsets, int32_t *pair_row, int32_t *recv_pair,
+                          void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Kernels one moe_dispatch call with these sizes enqueues on the calling
+ * thread's current device (1 for the one-launch form); -1 for invalid sizes.
+ */
+int moe_dispatch_kernels(int S, int T, int k, int E, int P);
 
 /*
  * Masked receive layout (a2a-backends section 4.1: a region per (local expert,

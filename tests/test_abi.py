@@ -198,3 +198,19 @@ def test_next_entry_points_reject(lib):
     bad = list(good)
     bad[17] = ws - 1
     _rejects(lib.moe_dispatch_layout_mapped, bad, "ws_bytes")
+
+
+def test_dispatch_rejects(lib):
+    """moe_dispatch checks the union of the four calls' arguments on the host."""
+    ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
+    good = [FAKE, FAKE, 1, 64, 256, 16, 2, 4, -1, 1, 128, 128] + [FAKE] * 13 + [FAKE, ws, FAKE, ST]
+    for idx, val, needle in ((4, 100, "H=100"), (8, 4, "recv_part"), (9, 0, "align"),
+                             (10, -1, "capacities"), (7, 3, "multiple of P"), (6, 33, "k=33"),
+                             (0, NULL, "`logits`"), (1, ctypes.c_void_p((1 << 20) + 8), "`x`"),
+                             (19, NULL, "`send`"), (21, NULL, "`recv`"), (26, ws - 1, "ws_bytes"),
+                             (25, ctypes.c_void_p((1 << 20) + 16), "`ws`")):
+        bad = list(good)
+        bad[idx] = val
+        _rejects(lib.moe_dispatch, bad, needle)
+    assert lib.moe_dispatch_kernels(1, 16, 6, 385, 8) == -1     # E % P != 0
+    assert lib.moe_dispatch_kernels(1, -1, 6, 384, 8) == -1     # T < 0

@@ -1,0 +1,211 @@
+"""moe_dispatch (route + layout + pack + permute in one call) against the four
+separate calls and the CPU oracle.
+
+Every output buffer starts filled with a sentinel, and the fused call must
+leave every byte of every output exactly as the separate calls leave it
+(written values and untouched sentinels alike), including under capacity
+overflow; where nothing overflows the outputs are also compared with the
+oracle.  The one-launch form (one source of 1..256 tokens) is covered at its
+edges (1, 63, 64, 65, 255, 256 tokens; E from 16 to 1024; k and P up to 32;
+8-value and ragged rows; run alignment; a receiving partition), and the
+launch counts the library reports are checked against the launch trace.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_moe_route_06_gb300 as m
+import moe_synth as ms
+import oracle
+from gpu_util import bf16_dev, bf16_host, f32_dev, host
+
+pytestmark = pytest.mark.gpu
+
+OUT_I32 = ("topk_ids", "expert_counts", "expert_rank", "part_counts", "part_offsets",
+           "token_slot", "send_src", "expert_offsets", "pair_row", "recv_pair")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load_library()
+
+
+def _dispatch(mode, w_, inp, recv_part=-1, align=1, cap_send=None, cap_recv=None, trace=False):
+    """One dispatch through `mode` with sentinel-filled outputs; returns the outputs
+    as host arrays (and the traced kernel names)."""
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, recv_part=recv_part, align=align,
+                     cap_send=cap_send, cap_recv=cap_recv, dispatch=mode)
+    for name in OUT_I32:
+        getattr(path, name).fill_(-7)
+    path.topk_w.fill_(-9.0)
+    path.send.view(torch.int16).fill_(0x5A5A)
+    path.recv.view(torch.int16).fill_(0x3C3C)
+    logits, x = f32_dev(inp["logits"]), bf16_dev(inp["x"])
+    torch.cuda.synchronize()
+    if trace:
+        m.trace_enable(None, 64)
+        m.trace_reset()
+    try:
+        if mode == "fused":
+            path.dispatch_fused(logits, x)
+        else:
+            path.route(logits)
+            path.dispatch(x)
+        torch.cuda.synchronize()
+        kernels = [n for n, _ in m.trace_records()] if trace else None
+    finally:
+        if trace:
+            m.trace_disable()
+    out = {name: host(getattr(path, name)) for name in OUT_I32}
+    out["topk_w"] = host(path.topk_w).view(np.uint32)
+    out["send"] = bf16_host(path.send)
+    out["recv"] = bf16_host(path.recv)
+    out["status"] = int(path.dev_status.item())
+    return out, kernels, path
+
+
+def _same(a, b):
+    for key in a:
+        if key in ("status",):
+            assert a[key] == b[key], (key, a[key], b[key])
+        else:
+            assert np.array_equal(a[key], b[key]), key
+
+
+def _against_oracle(got, w_, inp, recv_part=-1, align=1):
+    ref = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, None, recv_part=recv_part,
+                          align=align)
+    assert np.array_equal(got["topk_ids"], ref["ids"])
+    assert np.max(np.abs(got["topk_w"].view(np.float32) - ref["w"])) <= 2e-6
+    for key in ("expert_counts", "part_counts", "part_offsets", "token_slot"):
+        assert np.array_equal(got[key], ref["layout"][key]), key
+    for key in ("expert_offsets", "pair_row", "recv_pair"):
+        assert np.array_equal(got[key], ref["permute"][key]), key
+    for s in range(w_.S):
+        used = int(ref["layout"]["part_offsets"][s, -1])
+        assert np.array_equal(got["send"][s, :used], ref["send"][s, :used])
+        assert np.array_equal(got["send_src"][s], ref["send_src"][s])
+    rows = int(ref["permute"]["expert_offsets"][-1])
+    assert np.array_equal(got["recv"][:rows], ref["permute"]["recv"][:rows])
+    assert got["status"] == ref["status"] == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])
+def test_fused_equals_separate_and_oracle(name):
+    w_ = ms.workload(name)
+    inp = ms.gen_inputs(w_)
+    fused, kf, path = _dispatch("fused", w_, inp, trace=True)
+    sep, ks, _ = _dispatch("separate", w_, inp, trace=True)
+    _same(fused, sep)
+    _against_oracle(fused, w_, inp)
+    assert len(kf) == m.moe_dispatch_kernels(w_.S, w_.T, w_.k, w_.E, w_.P), kf
+    if w_.S == 1 and w_.T <= 256:
+        assert kf == ["k_dispatch_small"]
+    else:
+        assert kf[-1] == "k_pack_permute" and len(ks) > len(kf), (kf, ks)
+
+
+def test_fused_skewed_receiver_equals_separate():
+    w_ = ms.workload("skewed")
+    inp = ms.gen_inputs(w_)
+    fused, kf, _ = _dispatch("fused", w_, inp, recv_part=w_.recv_part, trace=True)
+    sep, _, _ = _dispatch("separate", w_, inp, recv_part=w_.recv_part)
+    _same(fused, sep)
+    assert kf[-1] == "k_pack_permute"
+    assert fused["status"] == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 255, 256, 257])
+def test_one_launch_edges_in_tokens(T):
+    w_ = ms.workload("decode", T=T, index=100 + T)
+    inp = ms.gen_inputs(w_)
+    fused, kf, _ = _dispatch("fused", w_, inp, trace=True)
+    sep, _, _ = _dispatch("separate", w_, inp)
+    _same(fused, sep)
+    _against_oracle(fused, w_, inp)
+    assert (kf == ["k_dispatch_small"]) == (T <= 256), kf
+
+
+@pytest.mark.parametrize("T,H,E,k,P,align,recv_part", [
+    (100, 8, 16, 2, 4, 1, -1),        # 8-value rows, E < 32 (one logit per lane)
+    (130, 520, 1024, 32, 32, 1, -1),  # the ABI's largest E, k, P; ragged segments
+    (256, 256, 64, 8, 8, 128, -1),    # run alignment: zero padding rows
+    (77, 5120, 384, 6, 8, 1, 3),      # one receiving partition
+    (200, 64, 96, 3, 1, 8, 0),        # a single partition
+    (33, 2048, 992, 7, 32, 4, 5),
+])
+def test_one_launch_shapes(T, H, E, k, P, align, recv_part):
+    w_ = ms.workload("tiny", T=T, H=H, E=E, k=k, P=P, index=7 * T + k)
+    inp = ms.gen_inputs(w_)
+    fused, kf, _ = _dispatch("fused", w_, inp, recv_part=recv_part, align=align, trace=True)
+    sep, _, _ = _dispatch("separate", w_, inp, recv_part=recv_part, align=align)
+    _same(fused, sep)
+    _against_oracle(fused, w_, inp, recv_part=recv_part, align=align)
+    assert kf == ["k_dispatch_small"]
+
+
+@pytest.mark.parametrize("name,T", [("decode", 64), ("decode", 200), ("prefill", 1000)])
+def test_capacity_overflow_matches_separate(name, T):
+    """Caps too small for the batch: rows past them are dropped and flagged the
+    same way (send past cap_send, receive rows past cap_recv)."""
+    w_ = ms.workload(name, T=T, index=300 + T)
+    inp = ms.gen_inputs(w_)
+    for cap_send, cap_recv in ((T, None), (None, T * 2), (T // 2, T)):
+        fused, _, _ = _dispatch("fused", w_, inp, cap_send=cap_send, cap_recv=cap_recv)
+        sep, _, _ = _dispatch("separate", w_, inp, cap_send=cap_send, cap_recv=cap_recv)
+        _same(fused, sep)
+        assert fused["status"] & m.status_bit(m.MOE_ERR_CAPACITY)
+
+
+def test_several_sources_take_the_pack_permute_kernel():
+    w_ = ms.workload("decode", S=3, T=50, index=55)
+    inp = ms.gen_inputs(w_)
+    for recv_part in (-1, 2):
+        fused, kf, _ = _dispatch("fused", w_, inp, recv_part=recv_part, trace=True)
+        sep, _, _ = _dispatch("separate", w_, inp, recv_part=recv_part)
+        _same(fused, sep)
+        _against_oracle(fused, w_, inp, recv_part=recv_part)
+        assert kf[0] == "k_route_topk" and kf[-1] == "k_pack_permute", kf
+
+
+def test_empty_batch():
+    w_ = ms.workload("decode", T=0)
+    inp = ms.gen_inputs(w_)
+    fused, kf, _ = _dispatch("fused", w_, inp, trace=True)
+    sep, _, _ = _dispatch("separate", w_, inp)
+    _same(fused, sep)
+    assert len(kf) == m.moe_dispatch_kernels(1, 0, w_.k, w_.E, w_.P)
+
+
+def test_fused_decode_step_in_a_cuda_graph():
+    """The fused decode step (moe_dispatch + moe_combine) captured once and
+    replayed on new inputs at the same addresses."""
+    w_ = ms.workload("decode")
+    inp = ms.gen_inputs(w_)
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, dispatch="fused")
+    logits, x = f32_dev(inp["logits"]), bf16_dev(inp["x"])
+    s = torch.cuda.Stream()
+    calls = path.bind(logits, x, s)
+    assert [fn.__name__ for fn, _ in calls] == ["moe_dispatch", "moe_combine"]
+    with torch.cuda.stream(s):
+        m.MoePath.run_bound(calls)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        m.MoePath.run_bound(calls)
+    inp2 = ms.gen_inputs(ms.workload("decode", index=9))
+    logits.copy_(f32_dev(inp2["logits"]))
+    x.copy_(bf16_dev(inp2["x"]))
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.run_path(inp2["x"], inp2["logits"], w_.E, w_.k, w_.P, None)
+        assert np.array_equal(host(path.pair_row), ref["permute"]["pair_row"])
+        # identity expert: the combine of a token's own row with weights summing to 1
+        got = ms.f32_from_bf16_bits(bf16_host(path.out)).astype(np.float64)
+        want = ms.f32_from_bf16_bits(ref["out"]).astype(np.float64)
+        assert np.all(np.abs(got - want) <= 1e-2 * np.maximum(np.abs(want), 1e-3))
+    assert int(path.dev_status.item()) == 0

@@ -2,7 +2,8 @@
 
 Every case draws S, T (up to 2,500 tokens: up to 10 layout chunks per source,
 so the layout's cluster form too), H, E, k, P, align, the receiving partition
-and the path's form (contiguous, masked, two-stage, routed) from a fixed seed, with
+and the path's form (contiguous, masked, two-stage, routed; the contiguous
+and two-stage forms through moe_dispatch or the separate calls) from a fixed seed, with
 the logits sometimes quantised so that equal logits (ties) are common.  Index
 outputs and moved rows are compared bit for bit; the output is compared
 within the combine tolerance against the oracle's combine of the same expert
@@ -42,8 +43,10 @@ def _draw(seed):
     align = int(rng.choice([1, 1, 2, 128])) if form == "contiguous" else 1
     recv_part = int(rng.integers(-1, P)) if rng.random() < 0.5 else -1
     ties = rng.random() < 0.3
+    # contiguous and two-stage forms: moe_dispatch (default) or the four separate calls
+    dispatch = "separate" if rng.random() < 0.35 else None
     return dict(S=S, T=T, H=H, E=E, k=k, P=P, form=form, align=align, recv_part=recv_part,
-                ties=ties, seed=seed)
+                ties=ties, seed=seed, dispatch=dispatch)
 
 
 @pytest.mark.parametrize("seed", range(120))
@@ -63,6 +66,8 @@ def test_random_shapes(seed):
         kw = dict(combine="two_stage")
     elif c["form"] == "routed":
         kw = dict(layout="routed")
+    if c["form"] in ("contiguous", "two_stage"):
+        kw["dispatch"] = c["dispatch"]
     path = m.MoePath(S, T, H, E, k, P, recv_part=c["recv_part"], align=c["align"], **kw)
     out = path.step(f32_dev(logits), bf16_dev(inp["x"]))          # identity expert
     torch.cuda.synchronize()

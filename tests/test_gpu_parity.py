@@ -325,19 +325,22 @@ def test_combine_rejects_rows_beyond_y():
 
 # ------------------------------------------------------------- whole path --
 
-def _gpu_path(w_, inp, recv_part=-1, align=1, scales=None):
-    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, recv_part=recv_part, align=align)
+def _gpu_path(w_, inp, recv_part=-1, align=1, scales=None, dispatch=None):
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, recv_part=recv_part, align=align,
+                     dispatch=dispatch)
     out = path.step(f32_dev(inp["logits"]), bf16_dev(inp["x"]),
                     None if scales is None else f32_dev(scales))
     torch.cuda.synchronize()
     return path, bf16_host(out)
 
 
+@pytest.mark.parametrize("dispatch", ["fused", "separate"])
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])
-def test_path_full_size(name):
+def test_path_full_size(name, dispatch):
+    """The whole path, with moe_dispatch or the four separate calls, against the oracle."""
     w_ = ms.workload(name)
     inp = ms.gen_inputs(w_)
-    path, out = _gpu_path(w_, inp, scales=inp["scales"])
+    path, out = _gpu_path(w_, inp, scales=inp["scales"], dispatch=dispatch)
     ref = oracle.run_path(inp["x"], inp["logits"], w_.E, w_.k, w_.P, inp["scales"])
     assert np.array_equal(host(path.topk_ids), ref["ids"])
     assert np.array_equal(host(path.token_slot), ref["layout"]["token_slot"])
@@ -385,20 +388,21 @@ def _skewed_reference(w_, inp):
     return ids, w64, lay, per
 
 
-@pytest.mark.parametrize("expert", ["identity", "scale"])
-def test_skewed_receiver_full_size(expert):
+@pytest.mark.parametrize("expert,dispatch", [("identity", "fused"), ("scale", "separate")])
+def test_skewed_receiver_full_size(expert, dispatch):
     """Skewed workload (8 sources x 4096 tokens, Zipf(1.2), partition 0 receives),
     compared in full: every index output; every used receive row bit-exact
     against its source token's row of x (recv[r] = x[s, t] for the pair
     recv_pair[r] = (s*T + t)*k + j); every one of the 32,768 partial-combine
     outputs against the oracle's combine.  With the stand-in expert
     (y = bf16(recv * s_e)) every expert row is held to one bf16 unit of the
-    oracle's, and the combine to the oracle's combine of the rows it read."""
+    oracle's, and the combine to the oracle's combine of the rows it read.  The
+    identity case runs moe_dispatch, the stand-in expert case the separate calls."""
     w_ = ms.workload("skewed")
     inp = ms.gen_inputs(w_)
     ids, w64, lay, per = _skewed_reference(w_, inp)
     scales = inp["scales"] if expert == "scale" else None
-    path, out = _gpu_path(w_, inp, recv_part=w_.recv_part, scales=scales)
+    path, out = _gpu_path(w_, inp, recv_part=w_.recv_part, scales=scales, dispatch=dispatch)
     assert np.array_equal(host(path.topk_ids), ids)
     assert np.max(np.abs(host(path.topk_w) - w64)) <= W_TOL
     assert np.array_equal(host(path.token_slot), lay["token_slot"])
@@ -494,7 +498,7 @@ def test_trace_inside_cuda_graph():
     """With tracing on during capture, each replay re-records the traced kernel's events."""
     w_ = ms.workload("decode")
     inp = ms.gen_inputs(w_)
-    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P)
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, dispatch="separate")
     logits, x = f32_dev(inp["logits"]), bf16_dev(inp["x"])
     s = torch.cuda.Stream()
     calls = path.bind(logits, x, s)
