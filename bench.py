@@ -117,7 +117,7 @@ def algorithmic_bytes(S, T, H, E, k, P, copies, copies_recv, pairs_recv, two_sta
     # moe_dispatch: the four calls in one; its pack + permute kernel reads each
     # receiving send row back right after storing it (an L2 hit), so the bytes it
     # must move through HBM are the pack's and the permute's less that re-read
-    b["dispatch"] = b["route"] + b["layout"] + b["pack"] + b["permute"]
+    b["dispatch"] = b["route"] + b["layout"] + b["pack"] + b["permute"] - copies_recv * R
     b["pack_permute"] = b["pack"] + b["permute"] - copies_recv * R
     b["step_hbm_fused"] = b["step"] - copies_recv * R
     return b
@@ -922,6 +922,7 @@ def run_ours(args, world, rank, local):
         return 0
 
     peak, peak_src = measured_peak()
+    hbm_step = b["step_hbm_fused"] if path.dispatch_mode == "fused" else b["step"]
     dom_ms = statistics.fmean(recs) if recs else None
     dom_achieved = (b[dom_key] / (dom_ms * 1e-3) / 1e9) if dom_ms else None
     dc_gbs = b["dispatch_combine"] * len(dc_ms) / (sum(dc_ms) * 1e-3) / 1e9
@@ -952,6 +953,11 @@ def run_ours(args, world, rank, local):
                                   args.variant),
         "rows_per_s": round(rows_all / (job_ms * 1e-3), 1),
         "frac_of_hbm_peak": round(value / peak, 4),
+        "hbm_bytes_per_step": hbm_step,
+        "frac_of_hbm_peak_on_hbm_bytes": round(hbm_step * K / (job_ms * 1e-3) / 1e9 / peak, 4),
+        "bytes_note": ("value counts the byte table of the separate calls (the send rows are read "
+                       "by the permute); through moe_dispatch that read-back is an L2 hit, so the "
+                       "step's HBM bytes are hbm_bytes_per_step"),
         "dispatch_combine": {"gbs": round(dc_gbs, 2), "us_median": round(1e3 * statistics.median(dc_ms), 2),
                              "frac_of_hbm_peak": round(dc_gbs / peak, 4),
                              "bytes": b["dispatch_combine"],
