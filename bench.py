@@ -990,6 +990,13 @@ def run_ours(args, world, rank, local):
                      "traffic": (dominant_traffic(dom_name, w.name) if args.variant == "contiguous"
                                  else None),
                      "bytes_per_launch": b[dom_key],
+                     **({"bytes_per_launch_by_call_table": b["pack"] + b["permute"],
+                         "frac_on_call_table": round((b["pack"] + b["permute"]) / (dom_ms * 1e-3) / 1e9
+                                                     / peak, 4) if dom_ms else None,
+                         "bytes_note": "bytes_per_launch = the kernel's HBM bytes (the receiving send "
+                                       "rows are read back from L2); the call table counts that "
+                                       "read-back as the permute's input, as the separate calls do"}
+                        if dom_key == "pack_permute" else {}),
                      "us_per_launch": round(1e3 * dom_ms, 2) if dom_ms else None,
                      "launches_timed": len(recs),
                      "how": "CUDA events around the kernel in an instrumented copy of the step, "
