@@ -53,7 +53,6 @@ constexpr int kSmallMaxT = 256;            // tokens (one thread each in the lay
 constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallCluster = 8;           // CTAs that share one batch's routing
-constexpr int kSmallTokPerWarp = kSmallMaxT / (kSmallCluster * kSmallWarps);
 constexpr int kSmallU = 2;                 // int4 per lane per column segment (1 KiB)
 constexpr int kSmallSegVec = 32 * kSmallU;
 constexpr int kSmallBatch = 4;             // partitions whose rows are read back together
@@ -89,6 +88,7 @@ __device__ __forceinline__ void store_seg(int4 *dst, const int4 *r, int v0, int 
 //   ts    lane p < P: the token's slot in partition p (or -1)
 //   pr    lane j < k: the pair's receive row (or -1); pp its partition
 //   src   the token's row of x; send_s / recv: row bases
+// `loaded`, if given, is the segment already in registers.
 // Stores x's segment to every slot < cap_send, then, B partitions at a time,
 // reads back the send row of each partition holding pairs and stores it to
 // those pairs' rows.  A partition whose slot is missing (< 0, an inconsistent
@@ -97,14 +97,16 @@ template <int U, int B>
 __device__ __forceinline__ void move_token_segment(const int4 *__restrict__ src, int4 *send_s,
                                                    int4 *recv, int V, int v0, int ts, int pr,
                                                    int pp, int P, int cap_send, bool &bad_slot,
-                                                   bool &cap_flag, bool report)
+                                                   bool &cap_flag, bool report,
+                                                   const int4 *loaded = nullptr)
 {
     int4 xr[U];
 #pragma unroll
     for (int u = 0; u < U; u++) {
         const int vi = v0 + 32 * u;
         xr[u] = make_int4(0, 0, 0, 0);
-        if (vi < V) xr[u] = ld_stream(src + vi);
+        if (loaded) xr[u] = loaded[u];
+        else if (vi < V) xr[u] = ld_stream(src + vi);
     }
     const int lane = threadIdx.x & 31;
     unsigned smask = __ballot_sync(kFull, lane < P && ts >= 0 && ts < cap_send);
@@ -156,9 +158,10 @@ __device__ __forceinline__ void move_token_segment(const int4 *__restrict__ src,
 }
 
 // One launch for one source of T <= 256 tokens.  grid = clusters of
-// kSmallCluster CTAs; CTA r of a cluster routes tokens r, r + 8, ... (one warp
-// each) and writes their ids into every CTA of the cluster; the first cluster
-// also stores ids and weights.  Needs E <= 1024 (the block scan), k, P <= 32.
+// kSmallCluster CTAs; warp w of CTA r of a cluster routes tokens r + 8w,
+// r + 8w + 64, ... and writes their ids into every CTA of the cluster; the
+// first cluster also stores ids and weights.  Needs E <= 1024 (the block
+// scan), k, P <= 32.
 template <int VPL>
 __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     const float *__restrict__ logits, const int4 *__restrict__ x, int T, int E, int k, int P,
@@ -197,27 +200,22 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     pdl_wait();
     pdl_trigger();
 
-    // 1. route this CTA's tokens (a warp per token), ids kept in registers
-    int my_id[kSmallTokPerWarp];
-#pragma unroll
-    for (int i = 0; i < kSmallTokPerWarp; i++) {
-        my_id[i] = -1;
-        const int t = r + G * (w + kSmallWarps * i);
-        if (t < T) {
-            float wt;
-            route_token_warp<VPL>(logits + (int64_t)t * E, E, k, my_id[i], wt);
-            if (first_cluster && lane < k) {
-                topk_ids[t * k + lane] = my_id[i];
-                topk_w[t * k + lane] = wt;
-            }
-        }
-    }
     cl_wait();                                  // every CTA of the cluster has started
-#pragma unroll
-    for (int i = 0; i < kSmallTokPerWarp; i++) {
-        const int t = r + G * (w + kSmallWarps * i);
-        if (t < T && lane < k)
-            for (int c = 0; c < G; c++) *cluster.map_shared_rank(ids_s + t * k + lane, c) = my_id[i];
+
+    // 1. route this CTA's tokens (a warp per token) and write each token's ids
+    // into every CTA of the cluster.  (The loop is kept rolled: one copy of the
+    // routing code is fetched, which measured faster than unrolled copies.)
+#pragma unroll 1
+    for (int t = r + G * w; t < T; t += G * kSmallWarps) {
+        int id;
+        float wt;
+        route_token_warp<VPL>(logits + (int64_t)t * E, E, k, id, wt);
+        if (first_cluster && lane < k) {
+            topk_ids[t * k + lane] = id;
+            topk_w[t * k + lane] = wt;
+        }
+        if (lane < k)
+            for (int c = 0; c < G; c++) *cluster.map_shared_rank(ids_s + t * k + lane, c) = id;
     }
     cl_arrive();                                // this CTA's remote writes are done
     cl_wait();                                  // every CTA holds every token's ids
@@ -382,13 +380,33 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
     int4 *__restrict__ recv, int32_t *__restrict__ expert_offsets, int32_t *__restrict__ pair_row,
     int32_t *__restrict__ recv_pair, uint32_t *dev_status)
 {
-    pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t gwarps = gthreads >> 5;
     const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
+    // The first task's x segment is loaded before the grid-dependency wait, so
+    // its HBM latency passes while the layout finishes.  x was complete before
+    // the routing kernel ran: this kernel is launched only once the layout
+    // kernel has passed its own wait (it waits, then lets dependents launch),
+    // and the layout's wait returns only after the routing kernel, which waited
+    // for everything before it, has completed.  Nothing here reads what the
+    // layout writes before pdl_wait().
+    const int64_t rt0 = gtid >> 5;
+    int4 x0[kPPUnroll];
+    if (rt0 < NT * nseg) {
+        const int64_t t0 = NT * nseg - 1 - rt0;
+        const int64_t n0 = t0 / nseg;
+        const int g0 = (int)(t0 - n0 * nseg);
+#pragma unroll
+        for (int u = 0; u < kPPUnroll; u++) {
+            const int vi = g0 * kPPSegVec + lane + 32 * u;
+            x0[u] = make_int4(0, 0, 0, 0);
+            if (vi < V) x0[u] = ld_stream(x + n0 * V + vi);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
     bool cap_flag = false, bad_slot = false, dropped = false, bad_rank = false, bad_id = false;
     bool pack_overflow = false;
 
@@ -464,7 +482,7 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
         }
         move_token_segment<kPPUnroll, kPPBatch>(x + n * V, send + (int64_t)s * cap_send * V, recv, V,
                                       g * kPPSegVec + lane, ts_c, pr, pp, P, cap_send, bad_slot,
-                                      cap_flag, g == 0);
+                                      cap_flag, g == 0, rtask == rt0 ? x0 : nullptr);
     }
 
     // padding rows: warp task (expert, padding row index, segment)
