@@ -50,14 +50,14 @@ DOMINANT_BY_VARIANT = {"two_stage": ("k_combine_stage1", "stage1"),
 # dominant kernel in the prefill pipeline, from an ncu capture with the L2 left
 # as the previous kernel left it (--cache-control none), with the SHA-256 prefix
 # of the source file the kernel was built from when it was captured (commit
-# 120a03f for k_perm_copy, 2abef0a for k_pack_permute).  The line reports null instead once that file has
+# 120a03f for k_perm_copy, 62ef766 for k_pack_permute).  The line reports null instead once that file has
 # changed, so a stale capture is never quoted.
 DOMINANT_TRAFFIC = {("k_perm_copy", "prefill"): {"bytes": 142.5e6 + 252.9e6,
                                                  "source": "combine_moe_route_06_gb300/csrc/permute.cu",
                                                  "sha16": "9a2fb6e795daf9b3"},
-                    ("k_pack_permute", "prefill"): {"bytes": 49.5e6 + 429.6e6,
+                    ("k_pack_permute", "prefill"): {"bytes": 43.8e6 + 429.5e6,
                                                     "source": "combine_moe_route_06_gb300/csrc/dispatch.cu",
-                                                    "sha16": "b1c67cb69b037cc1"}}
+                                                    "sha16": "03bc6a7b59332d98"}}
 
 
 def dominant_traffic(kernel: str, workload: str):
