@@ -15,8 +15,8 @@
 //   one launch (one source of at most 256 tokens, a decode step):
 //     k_dispatch_small.  Thread-block clusters of 8 CTAs; the CTAs of a
 //     cluster route a share of the tokens each and broadcast the ids into
-//     every CTA's shared memory (distributed shared memory, one cluster
-//     barrier).  Every CTA then builds the whole layout of the batch in its
+//     every CTA's shared memory (distributed shared memory, between two
+//     cluster barriers).  Every CTA then builds the whole layout of the batch in its
 //     own shared memory (a 256-token chunk: partition ballots, warp expert
 //     histograms) and the run starts of the receiving experts, so no CTA
 //     waits on another outside its cluster.  Finally the grid's warps move
