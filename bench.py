@@ -701,11 +701,15 @@ def run_ours(args, world, rank, local):
                               nvfp4=(args.variant == "nvfp4"))
         dom_name, dom_key = DOMINANT_BY_VARIANT.get(args.variant, (DOMINANT, "perm_copy"))
         if path.dispatch_mode == "fused":
-            # the longest kernel of the fused step: pack + permute in one pass, or
-            # the whole dispatch in one launch for a decode-sized batch
-            dom_name, dom_key = (("k_dispatch_small", "dispatch")
-                                 if m.moe_dispatch_kernels(w.S, w.T, w.k, w.E, w.P) == 1
-                                 else ("k_pack_permute", "pack_permute"))
+            # the longest kernel of the fused step's own calls: pack + permute in one
+            # pass (quantizing with MXFP8 / NVFP4 rows), or the whole dispatch in one
+            # launch for a decode-sized batch of bf16 rows
+            if path.quantized:
+                dom_name, dom_key = f"k_pack_permute_{path.quant}", "pack_permute"
+            elif m.moe_dispatch_kernels(w.S, w.T, w.k, w.E, w.P) == 1:
+                dom_name, dom_key = "k_dispatch_small", "dispatch"
+            else:
+                dom_name, dom_key = "k_pack_permute", "pack_permute"
         if placement_info is not None:
             # pairs per partition on the timed batch: contiguous blocks vs the placement
             ids_h = path.topk_ids.cpu().numpy()

@@ -27,7 +27,8 @@ __all__ = [
     "MOE_ERR_TIMEOUT", "MOE_ERR_CUDA", "status_bit", "MoeError", "MoeLibraryMissing",
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
     "moe_dispatch_layout_kernels", "moe_permute_to_experts_kernels", "moe_dispatch_kernels",
-    "moe_dispatch",
+    "moe_dispatch", "moe_dispatch_quantized", "moe_dispatch_quantized_kernels", "MOE_FORMAT_MXFP8",
+    "MOE_FORMAT_NVFP4",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
     "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
@@ -43,6 +44,8 @@ MOE_ERR_CAPACITY = 2
 MOE_ERR_BAD_EXPERT_ID = 3
 MOE_ERR_TIMEOUT = 4
 MOE_ERR_CUDA = 5
+MOE_FORMAT_MXFP8 = 1
+MOE_FORMAT_NVFP4 = 2
 
 
 def status_bit(code: int) -> int:
@@ -93,6 +96,10 @@ def load_library() -> ctypes.CDLL:
             "moe_dispatch_layout_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
             "moe_permute_to_experts_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
             "moe_dispatch_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
+            "moe_dispatch_quantized_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
+            "moe_dispatch_quantized": ([P, P, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                        i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                        sz, P, P], ctypes.c_int),
             "moe_dispatch": ([P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P, P, P,
                               P, P, P, P, P, P, P, P, P, P, sz, P, P], ctypes.c_int),
             "moe_route_topk": ([P, i32, i32, i32, i32, P, P, P], ctypes.c_int),
@@ -437,6 +444,40 @@ def moe_dispatch(logits, x, E, P, recv_part, align, topk_ids, topk_w, expert_cou
         _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
 
 
+def moe_dispatch_quantized(logits, x, E, P, fmt, global_scale, recv_part, align, topk_ids, topk_w,
+                           expert_counts, expert_rank, part_counts, part_offsets, token_slot,
+                           send_q, send_src, recv_q, expert_offsets, pair_row, recv_pair, ws,
+                           dev_status=None, stream=None):
+    """moe_dispatch with MXFP8 (fmt 1) or NVFP4 (fmt 2) records: send_q uint8
+    [S,cap_send,rb], recv_q uint8 [cap_recv,rb]; the rest as moe_dispatch."""
+    lib = load_library()
+    S, T, H = x.shape
+    k = topk_ids.shape[2]
+    cap_send = send_q.shape[1]
+    cap_recv = recv_q.shape[0]
+    _check(lib.moe_dispatch_quantized(
+        _dev(logits, "logits", (torch.float32,), 3), _dev(x, "x", _BF16_TYPES, 3), S, T, H, E, k,
+        P, int(fmt), float(global_scale), recv_part, align, cap_send, cap_recv,
+        _dev(topk_ids, "topk_ids", (torch.int32,), 3), _dev(topk_w, "topk_w", (torch.float32,), 3),
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)),
+        _dev(part_counts, "part_counts", (torch.int32,)),
+        _dev(part_offsets, "part_offsets", (torch.int32,)),
+        _dev(token_slot, "token_slot", (torch.int32,), 3), _dev(send_q, "send_q", (torch.uint8,), 3),
+        _dev(send_src, "send_src", (torch.int32,)), _dev(recv_q, "recv_q", (torch.uint8,), 2),
+        _dev(expert_offsets, "expert_offsets", (torch.int32,)),
+        _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
+        _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_quantized_kernels(S, T, k, E, P) -> int:
+    """Kernels one moe_dispatch_quantized call with these sizes enqueues on the current device."""
+    n = load_library().moe_dispatch_quantized_kernels(S, T, k, E, P)
+    if n < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_dispatch_quantized_kernels: invalid sizes")
+    return n
+
+
 def moe_dispatch_kernels(S, T, k, E, P) -> int:
     """Kernels one moe_dispatch call with these sizes enqueues on the current device."""
     n = load_library().moe_dispatch_kernels(S, T, k, E, P)
@@ -575,9 +616,10 @@ class MoePath:
         placement: a Placement (moe_plan_placement) -- the layout then maps each
         pair to a physical expert slot and everything after it works on the
         P*Lp physical experts; None keeps expert e in slot e.
-        dispatch: "fused" (moe_dispatch: route, layout, pack and permute in one call,
-        one launch for a decode-sized batch) or "separate" (the four calls); the
-        default is "fused" where it applies (contiguous bf16 rows, no placement)."""
+        dispatch: "fused" (moe_dispatch, or moe_dispatch_quantized with quantized
+        rows: route, layout, pack and permute in one call, one launch for a
+        decode-sized batch of bf16 rows) or "separate" (the four calls); the
+        default is "fused" where it applies (contiguous layout, no placement)."""
         if layout not in ("contiguous", "masked", "routed") or combine not in ("single", "two_stage"):
             raise ValueError("layout must be contiguous|masked|routed, combine single|two_stage")
         if layout == "routed":
@@ -590,11 +632,11 @@ class MoePath:
             raise ValueError("mxfp8 rows need H % 512 == 0 and the contiguous layout")
         if quant == "nvfp4" and (H % 256 != 0 or layout != "contiguous"):
             raise ValueError("nvfp4 rows need H % 256 == 0 and the contiguous layout")
-        fusable = layout == "contiguous" and quant == "none" and placement is None
+        fusable = layout == "contiguous" and placement is None
         if dispatch is None:
             dispatch = "fused" if fusable else "separate"
         if dispatch not in ("fused", "separate") or (dispatch == "fused" and not fusable):
-            raise ValueError("dispatch must be fused|separate; fused needs contiguous bf16 rows "
+            raise ValueError("dispatch must be fused|separate; fused needs the contiguous layout "
                              "and no placement")
         self.dispatch_mode = dispatch
         self.quantized = quant != "none"
@@ -680,6 +722,20 @@ class MoePath:
         stp = vp(self.dev_status.data_ptr())
         Hp, Ep = self.Hp, self.Ep
         ids_p = vp(self.phys_ids.data_ptr())
+        if self.dispatch_mode == "fused" and self.quantized:
+            fmt = MOE_FORMAT_MXFP8 if self.quant == "mxfp8" else MOE_FORMAT_NVFP4
+            calls = [(lib.moe_dispatch_quantized, (
+                ptr(logits, "logits", (torch.float32,)), ptr(x, "x", _BF16_TYPES), S, T, H, E, k, P,
+                fmt, self.nvfp4_scale if self.quant == "nvfp4" else 1.0, self.recv_part, self.align,
+                self.cap_send, self.cap_recv, vp(self.topk_ids.data_ptr()),
+                vp(self.topk_w.data_ptr()), vp(self.expert_counts.data_ptr()),
+                vp(self.expert_rank.data_ptr()), vp(self.part_counts.data_ptr()),
+                vp(self.part_offsets.data_ptr()), vp(self.token_slot.data_ptr()),
+                vp(self.send.data_ptr()), vp(self.send_src.data_ptr()), vp(self.recv.data_ptr()),
+                vp(self.expert_offsets.data_ptr()), vp(self.pair_row.data_ptr()),
+                vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st))]
+            return calls + self._bind_expert_q(lib, scale, stp, st) + \
+                self._bind_combine(lib, self.y, stp, st, ids_p)
         if self.dispatch_mode == "fused":
             calls = [(lib.moe_dispatch, (
                 ptr(logits, "logits", (torch.float32,)), ptr(x, "x", _BF16_TYPES), S, T, H, E, k, P,
@@ -758,20 +814,23 @@ class MoePath:
                 vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st)))
         y = self.recv
         if self.quantized:
-            # the bound call keeps a pointer: hold the per-slot scales on the path
-            self._bound_scale = self.unit_scale if scale is None else self.slot_scale(scale)
-            if self.quant == "mxfp8":
-                calls.append((lib.moe_expert_scale_mxfp8, (
-                    vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()),
-                    ptr(self._bound_scale, "scale", (torch.float32,)), Ep, H, self.cap_recv,
-                    vp(self.y.data_ptr()), st)))
-            else:
-                calls.append((lib.moe_expert_scale_nvfp4, (
-                    vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()),
-                    ptr(self._bound_scale, "scale", (torch.float32,)), Ep, H, self.nvfp4_scale,
-                    self.cap_recv, vp(self.y.data_ptr()), st)))
+            calls += self._bind_expert_q(lib, scale, stp, st)
             y = self.y
         return calls + self._bind_combine(lib, y, stp, st, ids_p)
+
+    def _bind_expert_q(self, lib, scale, stp, st):
+        """The bound dequantizing stand-in expert (quantized rows: recv records -> y)."""
+        vp = ctypes.c_void_p
+        # the bound call keeps a pointer: hold the per-slot scales on the path
+        self._bound_scale = self.unit_scale if scale is None else self.slot_scale(scale)
+        sc = _dev(self._bound_scale, "scale", (torch.float32,))
+        if self.quant == "mxfp8":
+            return [(lib.moe_expert_scale_mxfp8, (
+                vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()), sc, self.Ep, self.H,
+                self.cap_recv, vp(self.y.data_ptr()), st))]
+        return [(lib.moe_expert_scale_nvfp4, (
+            vp(self.recv.data_ptr()), vp(self.expert_offsets.data_ptr()), sc, self.Ep, self.H,
+            self.nvfp4_scale, self.cap_recv, vp(self.y.data_ptr()), st))]
 
     def _bind_combine(self, lib, y, stp, st, ids_p):
         """The bound combine call(s) reading expert rows y."""
@@ -889,7 +948,18 @@ class MoePath:
                                recv_part=self.recv_part)
 
     def dispatch_fused(self, logits, x, stream=None):
-        """route + layout + pack + permute through one moe_dispatch call."""
+        """route + layout + pack + permute through one moe_dispatch (or, with
+        quantized rows, moe_dispatch_quantized) call."""
+        if self.quantized:
+            moe_dispatch_quantized(logits, x, self.E, self.P,
+                                   MOE_FORMAT_MXFP8 if self.quant == "mxfp8" else MOE_FORMAT_NVFP4,
+                                   self.nvfp4_scale if self.quant == "nvfp4" else 1.0,
+                                   self.recv_part, self.align, self.topk_ids, self.topk_w,
+                                   self.expert_counts, self.expert_rank, self.part_counts,
+                                   self.part_offsets, self.token_slot, self.send, self.send_src,
+                                   self.recv, self.expert_offsets, self.pair_row, self.recv_pair,
+                                   self.ws, self.dev_status, stream)
+            return
         moe_dispatch(logits, x, self.E, self.P, self.recv_part, self.align, self.topk_ids,
                      self.topk_w, self.expert_counts, self.expert_rank, self.part_counts,
                      self.part_offsets, self.token_slot, self.send, self.send_src, self.recv,
@@ -921,7 +991,8 @@ class MoePath:
             comb = 2 if self.combine_mode == "two_stage" else 1
             if self.T == 0:
                 comb = 0                   # the combine launches nothing for an empty batch
-            return (moe_dispatch_kernels(self.S, self.T, self.k, self.E, self.P) + comb
+            count = moe_dispatch_quantized_kernels if self.quantized else moe_dispatch_kernels
+            return (count(self.S, self.T, self.k, self.E, self.P) + comb
                     + (1 if with_expert else 0))
         mapped = self.placement is not None
         if mapped:

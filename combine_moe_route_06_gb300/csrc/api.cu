@@ -372,6 +372,75 @@ moe_status_t moe_dispatch(const float *logits, const uint16_t *x, int S, int T, 
                        __func__);
 }
 
+int moe_dispatch_quantized_kernels(int S, int T, int k, int E, int P)
+{
+    if (check_sizes("moe_dispatch_quantized_kernels", S, T, k, E, P) != MOE_OK) return -1;
+    int n = 0;
+    if (dispatch_quantized_kernel_count(S, T, k, E, P, &n) != cudaSuccess) return -1;
+    return n;
+}
+
+moe_status_t moe_dispatch_quantized(const float *logits, const uint16_t *x, int S, int T, int H,
+                                    int E, int k, int P, int format, float global_scale,
+                                    int recv_part, int align, int cap_send, int cap_recv,
+                                    int32_t *topk_ids, float *topk_w, int32_t *expert_counts,
+                                    int32_t *expert_rank, int32_t *part_counts,
+                                    int32_t *part_offsets, int32_t *token_slot, uint8_t *send_q,
+                                    int32_t *send_src, uint8_t *recv_q, int32_t *expert_offsets,
+                                    int32_t *pair_row, int32_t *recv_pair, void *ws,
+                                    size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream)
+{
+    MOE_CALL_RANGE();
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(format == MOE_FORMAT_MXFP8 || format == MOE_FORMAT_NVFP4,
+            "%s: format=%d must be MOE_FORMAT_MXFP8 (1) or MOE_FORMAT_NVFP4 (2)", __func__, format);
+    if (format == MOE_FORMAT_MXFP8)
+        REQUIRE(H >= 512 && H % 512 == 0, "%s: H=%d must be a positive multiple of 512 for MXFP8",
+                __func__, H);
+    else
+        REQUIRE(H >= 256 && H % 256 == 0, "%s: H=%d must be a positive multiple of 256 for NVFP4",
+                __func__, H);
+    REQUIRE(format != MOE_FORMAT_NVFP4 || (global_scale > 0.f && global_scale < 3.0e38f),
+            "%s: global_scale must be positive and finite", __func__);
+    REQUIRE((int64_t)S * T * E < ((int64_t)1 << 40), "%s: S*T*E too large", __func__);
+    REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, P)", __func__,
+            recv_part);
+    REQUIRE(align >= 1 && align <= 1024, "%s: align=%d must be in [1, 1024]", __func__, align);
+    REQUIRE(cap_send >= 0 && cap_recv >= 0, "%s: capacities must be >= 0", __func__);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    REQUIRE((int64_t)S * T * k + (int64_t)E * (align - 1) < ((int64_t)1 << 31),
+            "%s: S*T*k + E*(align-1) must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    const int64_t rb = format == MOE_FORMAT_MXFP8 ? (int64_t)H + H / 32 : (int64_t)H / 2 + H / 16;
+    REQUIRE_ARR(logits, NT * E, 4);
+    REQUIRE_ARR(x, NT * H, 16);
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(topk_w, NT * k, 4);
+    REQUIRE_ARR(expert_counts, (int64_t)S * E, 4);
+    REQUIRE_ARR(expert_rank, NT * k, 4);
+    REQUIRE_ARR(part_counts, (int64_t)S * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(send_q, (int64_t)S * cap_send * rb, 16);
+    REQUIRE_ARR(send_src, (int64_t)S * cap_send, 4);
+    REQUIRE_ARR(recv_q, (int64_t)cap_recv * rb, 16);
+    REQUIRE_ARR(expert_offsets, E + 1, 4);
+    REQUIRE_ARR(pair_row, NT * k, 4);
+    REQUIRE_ARR(recv_pair, cap_recv, 4);
+    REQUIRE_STATUS(dev_status);
+    const size_t need = moe_workspace_bytes(S, T, k, E, P);
+    REQUIRE_ARR(ws, need, 256);
+    REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
+    return cuda_status(launch_dispatch_quantized(logits, x, S, T, H, E, k, P, format, global_scale,
+                                                 recv_part, align, cap_send, cap_recv, topk_ids,
+                                                 topk_w, expert_counts, expert_rank, part_counts,
+                                                 part_offsets, token_slot, send_q, send_src,
+                                                 recv_q, expert_offsets, pair_row, recv_pair, ws,
+                                                 dev_status, stream),
+                       __func__);
+}
+
 moe_status_t moe_permute_to_experts_masked(const uint16_t *send, const int32_t *token_slot,
                                            const int32_t *topk_ids, const int32_t *expert_counts,
                                            const int32_t *expert_rank, int S, int T, int k,

@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "quant.cuh"
 #include "route_warp.cuh"
 #include "trace.h"
 
@@ -365,6 +366,75 @@ constexpr int kPPSegVec = 32 * kPPUnroll;
 constexpr int kPPThreads = 256;
 constexpr int kPPBatch = 1;                        // one partition's row read back at a time
 
+// Run starts of the receiving experts, built by every CTA in shared memory
+// from the expert counts (as the permute's map step does): off[e] = padded
+// pairs of the receiving experts before e (off[E] = rows used), cnt[e] = pairs
+// of e, sb[s][e] = pairs of e in the sources before s.  CTA 0 also stores
+// expert_offsets.  Every thread of the CTA must call; synchronises the CTA.
+__device__ __forceinline__ void build_run_starts(const int32_t *__restrict__ expert_counts, int S,
+                                                 int E, int L, int recv_part, int align, int *off,
+                                                 int *cnt, int *sb,
+                                                 int32_t *__restrict__ expert_offsets)
+{
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int s2 = 0; s2 < S; s2++) {
+            sb[s2 * E + e] = run;
+            run += __ldg(expert_counts + (int64_t)s2 * E + e);
+        }
+        cnt[e] = run;
+        off[e] = in_recv(e, E, L, recv_part) ? (run + align - 1) / align * align : 0;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan_1024(off, E);
+    if (threadIdx.x == 0) off[E] = total;
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) expert_offsets[e] = off[e];
+}
+
+// Receive row of a pair (expert e, rank r within source s's run of e): run
+// start + pairs of e in earlier sources + rank; -1 if e is not received, the
+// rank is inconsistent with the counts (bad_rank) or the row is past cap_recv
+// (dropped).  An id >= E sets bad_id.
+__device__ __forceinline__ int pair_row_of(int e, int r, int s, int S, int E, int L, int recv_part,
+                                           int cap_recv, const int *off, const int *cnt,
+                                           const int *sb, bool &bad_id, bool &bad_rank,
+                                           bool &dropped)
+{
+    if (e >= E) bad_id = true;
+    if (!in_recv(e, E, L, recv_part)) return -1;
+    const int before = sb[s * E + e];
+    const int own = (s + 1 < S ? sb[(s + 1) * E + e] : cnt[e]) - before;
+    if (r < 0 || r >= own) {
+        bad_rank = true;
+        return -1;
+    }
+    const int row = off[e] + before + r;
+    if (row >= cap_recv) {
+        dropped = true;
+        return -1;
+    }
+    return row;
+}
+
+// recv_pair = -1 for receive rows past the used ones; send_src = -1 for send
+// rows past each source's last copy.  Grid-stride over every thread.
+__device__ __forceinline__ void mark_unused_rows(int used, int cap_recv, int S, int P, int cap_send,
+                                                 const int32_t *__restrict__ part_offsets,
+                                                 int32_t *__restrict__ recv_pair,
+                                                 int32_t *__restrict__ send_src)
+{
+    const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t rr = (int64_t)used + gtid; rr < cap_recv; rr += gthreads) recv_pair[rr] = -1;
+    for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
+        const int s = (int)(i / cap_send);
+        const int rr = (int)(i - (int64_t)s * cap_send);
+        if (rr >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) send_src[i] = -1;
+    }
+}
+
 // Pack and permute in one pass over warp tasks (token, 2 KiB column segment),
 // tokens last to first (the receive rows written last, those of the first
 // tokens, are the ones the combine reads first).  Every CTA first builds the
@@ -423,27 +493,11 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
     };
     if (rtask < ntask) fetch(rtask);
 
-    // run starts: off[e] padded pairs of the receiving experts before e,
-    // cnt[e] pairs of e, sb[s][e] pairs of e in the sources before s
     extern __shared__ int smp[];
     int *off = smp;              // [E + 1]
     int *cnt = off + E + 1;      // [E]
     int *sb = cnt + E;           // [S][E]
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-        for (int s2 = 0; s2 < S; s2++) {
-            sb[s2 * E + e] = run;
-            run += __ldg(expert_counts + (int64_t)s2 * E + e);
-        }
-        cnt[e] = run;
-        off[e] = in_recv(e, E, L, recv_part) ? (run + align - 1) / align * align : 0;
-    }
-    __syncthreads();
-    const int total = block_exclusive_scan_1024(off, E);
-    if (threadIdx.x == 0) off[E] = total;
-    __syncthreads();
-    if (blockIdx.x == 0)
-        for (int e = threadIdx.x; e <= E; e += blockDim.x) expert_offsets[e] = off[e];
+    build_run_starts(expert_counts, S, E, L, recv_part, align, off, cnt, sb, expert_offsets);
 
     for (; rtask < ntask; rtask += gwarps) {
         const int64_t task = ntask - 1 - rtask;
@@ -454,27 +508,14 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
         const int s = (int)(n / T);
         int pr = -1, pp = -1;
         if (lane < k) {
-            const int e = e_c;
-            if (e >= E) bad_id = true;
-            if (in_recv(e, E, L, recv_part)) {
-                const int before = sb[s * E + e];
-                const int own = (s + 1 < S ? sb[(s + 1) * E + e] : cnt[e]) - before;
-                if (r_c < 0 || r_c >= own) {
-                    bad_rank = true;                // rank inconsistent with the counts
-                } else {
-                    pr = off[e] + before + r_c;
-                    if (pr >= cap_recv) {
-                        dropped = true;
-                        pr = -1;
-                    }
-                }
-            }
+            pr = pair_row_of(e_c, r_c, s, S, E, L, recv_part, cap_recv, off, cnt, sb, bad_id,
+                             bad_rank, dropped);
             if (g == 0) {
                 const int64_t q = n * k + lane;
                 pair_row[q] = pr;
                 if (pr >= 0) recv_pair[pr] = (int32_t)q;
             }
-            if (pr >= 0) pp = e / L;
+            if (pr >= 0) pp = e_c / L;
         }
         if (g == 0 && lane < P) {
             if (ts_c >= cap_send) pack_overflow = true;
@@ -505,13 +546,264 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
             if (g == 0 && lane == 0) recv_pair[row] = -1;
         }
     }
-    // receive rows past the used ones; send rows past each source's last copy
-    for (int64_t rr = (int64_t)off[E] + gtid; rr < cap_recv; rr += gthreads) recv_pair[rr] = -1;
-    for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
-        const int s = (int)(i / cap_send);
-        const int rr = (int)(i - (int64_t)s * cap_send);
-        if (rr >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) send_src[i] = -1;
+    mark_unused_rows(off[E], cap_recv, S, P, cap_send, part_offsets, recv_pair, send_src);
+
+    if (cap_flag || dropped || pack_overflow) flag_status(dev_status, MOE_ERR_CAPACITY);
+    if (bad_slot || bad_rank) flag_status(dev_status, MOE_ERR_INVALID_ARG);
+    if (bad_id) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
+}
+
+// ------------------------------------------- pack + permute, quantized --
+
+// 4-byte global accesses that bypass L1 (the read-back of a record piece the
+// same thread has just stored is a real load, served from L2).
+__device__ __forceinline__ void st_cg4(void *p, uint32_t v)
+{
+    asm volatile("st.global.cg.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cg4(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+constexpr int kQFmtMxfp8 = 1;
+constexpr int kQFmtNvfp4 = 2;
+constexpr int kQSegVec = 128;                 // 16-byte x vectors (1,024 values) per segment
+
+// One warp's piece of a record for one 1,024-value segment.  MXFP8: lane l
+// owns values 16l + 512u (u = 0, 1) -> code[u], 16 E4M3 bytes each; lanes 0..7
+// carry the segment's 32 scale bytes as words (lane j: pass j / 4, blocks
+// 4 (j % 4) .. +3).  NVFP4: lane l owns values 32l .. 32l + 31 -> code[0], 16
+// bytes of E2M1 pairs; lanes 0..15 carry the 64 scale bytes as words (lane j:
+// blocks 4j .. 4j + 3).  The record holds codes at value offset / (1 or 2)
+// and the scales after all codes, as the quantized packs lay them out.
+struct QPiece {
+    uint4 code[2];
+    uint32_t sw;
+};
+
+template <int FMT> struct QLayout;
+template <> struct QLayout<kQFmtMxfp8> {
+    static constexpr int kCodePerVec = 8;      // code bytes per 16-byte x vector
+    static constexpr int kVecPerScale = 4;     // x vectors per scale byte
+    static constexpr int kScaleLanes = 8;
+};
+template <> struct QLayout<kQFmtNvfp4> {
+    static constexpr int kCodePerVec = 4;
+    static constexpr int kVecPerScale = 2;
+    static constexpr int kScaleLanes = 16;
+};
+
+// Quantizes the segment starting at vector vb of the token's row (every lane
+// of the warp must call).
+template <int FMT>
+__device__ __forceinline__ QPiece quantize_piece(const int4 *__restrict__ row, int V, int vb,
+                                                 float g, float d)
+{
+    const int lane = threadIdx.x & 31;
+    QPiece q;
+    q.sw = 0u;
+    if (FMT == kQFmtMxfp8) {
+        uint32_t sc[2];
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int vi = vb + 64 * u + 2 * lane;
+            int4 v[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
+            if (vi < V) {
+                v[0] = ld_stream(row + vi);
+                v[1] = ld_stream(row + vi + 1);
+            }
+            mxfp8_quantize16(v, q.code[u], sc[u]);
+        }
+        const int w = lane & 3;
+        uint32_t a = 0u, b = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            a |= __shfl_sync(kFull, sc[0], 8 * w + 2 * i) << (8 * i);
+            b |= __shfl_sync(kFull, sc[1], 8 * w + 2 * i) << (8 * i);
+        }
+        q.sw = (lane < 4) ? a : b;
+    } else {
+        const int vi = vb + 4 * lane;
+        int4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) v[i] = (vi < V) ? ld_stream(row + vi + i) : make_int4(0, 0, 0, 0);
+        uint32_t sp;
+        nvfp4_quantize32(v, g, d, q.code[0], sp);
+        q.code[1] = make_uint4(0u, 0u, 0u, 0u);
+        const int j = lane & 15;
+        q.sw = __shfl_sync(kFull, sp, 2 * j) | (__shfl_sync(kFull, sp, 2 * j + 1) << 16);
     }
+    return q;
+}
+
+// Byte offsets of this lane's code vector(s) and scale word in a record, and
+// whether they lie inside the row.
+template <int FMT>
+__device__ __forceinline__ bool code_at(int V, int vb, int u, int64_t &off)
+{
+    const int lane = threadIdx.x & 31;
+    const int vi = (FMT == kQFmtMxfp8) ? vb + 64 * u + 2 * lane : vb + 4 * lane;
+    off = (int64_t)vi * QLayout<FMT>::kCodePerVec;
+    return vi < V;
+}
+template <int FMT>
+__device__ __forceinline__ bool scale_at(int V, int vb, int64_t &off)
+{
+    using QL = QLayout<FMT>;
+    const int lane = threadIdx.x & 31;
+    if (lane >= QL::kScaleLanes) return false;
+    // first x vector the word's four blocks cover, and the word's place
+    const int v0 = (FMT == kQFmtMxfp8) ? vb + 64 * (lane >> 2) + 16 * (lane & 3) : vb + 8 * lane;
+    off = (int64_t)V * QL::kCodePerVec + v0 / QL::kVecPerScale;
+    return v0 < V;
+}
+
+template <int FMT>
+__device__ __forceinline__ void store_piece(uint8_t *rec, int V, int vb, const QPiece &q)
+{
+    int64_t off;
+#pragma unroll
+    for (int u = 0; u < (FMT == kQFmtMxfp8 ? 2 : 1); u++)
+        if (code_at<FMT>(V, vb, u, off))
+            st_cg(reinterpret_cast<int4 *>(rec + off),
+                  make_int4((int)q.code[u].x, (int)q.code[u].y, (int)q.code[u].z, (int)q.code[u].w));
+    if (scale_at<FMT>(V, vb, off)) st_cg4(rec + off, q.sw);
+}
+
+template <int FMT>
+__device__ __forceinline__ QPiece load_piece(const uint8_t *rec, int V, int vb)
+{
+    QPiece q;
+    q.code[0] = q.code[1] = make_uint4(0u, 0u, 0u, 0u);
+    q.sw = 0u;
+    int64_t off;
+#pragma unroll
+    for (int u = 0; u < (FMT == kQFmtMxfp8 ? 2 : 1); u++)
+        if (code_at<FMT>(V, vb, u, off)) {
+            const int4 c = ld_cg(reinterpret_cast<const int4 *>(rec + off));
+            q.code[u] = make_uint4((uint32_t)c.x, (uint32_t)c.y, (uint32_t)c.z, (uint32_t)c.w);
+        }
+    if (scale_at<FMT>(V, vb, off)) q.sw = ld_cg4(rec + off);
+    return q;
+}
+
+// moe_dispatch's pack + permute pass with quantized rows: as k_pack_permute,
+// but each warp task (token, 1,024-value segment) quantizes the segment once
+// (MXFP8 or NVFP4, quant.cuh) into its record piece (QPiece: codes, and the
+// block scale bytes at the record's tail), stores it to every send slot, reads
+// the piece back from each receiving partition's send record and stores it to
+// that partition's pair records.  Records are rb = V * kCodePerVec +
+// V / kVecPerScale bytes; padding records are zero.  g is the NVFP4 tensor
+// scale.
+template <int FMT>
+__global__ void __launch_bounds__(kPPThreads) k_pack_permute_q(
+    const int4 *__restrict__ x, const int32_t *__restrict__ token_slot,
+    const int32_t *__restrict__ part_offsets, const int32_t *__restrict__ ids,
+    const int32_t *__restrict__ expert_counts, const int32_t *__restrict__ expert_rank, int S,
+    int64_t NT, int k, int E, int L, int P, int T, int V, int recv_part, int align, int cap_send,
+    int cap_recv, float g, uint8_t *__restrict__ send_q, int32_t *__restrict__ send_src,
+    uint8_t *__restrict__ recv_q, int32_t *__restrict__ expert_offsets,
+    int32_t *__restrict__ pair_row, int32_t *__restrict__ recv_pair, uint32_t *dev_status)
+{
+    using QL = QLayout<FMT>;
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t rb = (int64_t)V * QL::kCodePerVec + V / QL::kVecPerScale;
+    const float d = __fmul_rn(6.0f, g);
+    const int nseg = (V + kQSegVec - 1) / kQSegVec;
+    bool cap_flag = false, bad_slot = false, dropped = false, bad_rank = false, bad_id = false;
+    bool pack_overflow = false;
+
+    extern __shared__ int smq[];
+    int *off = smq;              // [E + 1]
+    int *cnt = off + E + 1;      // [E]
+    int *sb = cnt + E;           // [S][E]
+    build_run_starts(expert_counts, S, E, L, recv_part, align, off, cnt, sb, expert_offsets);
+
+    const int64_t ntask = NT * nseg;
+    for (int64_t rtask = gtid >> 5; rtask < ntask; rtask += gwarps) {
+        const int64_t task = ntask - 1 - rtask;       // tokens last to first
+        const int64_t n = task / nseg;
+        const int gs = (int)(task - n * nseg);
+        const int s = (int)(n / T);
+        int ts = -1, pr = -1, pp = -1;
+        if (lane < P) ts = __ldg(token_slot + n * P + lane);
+        if (lane < k) {
+            const int e = __ldg(ids + n * k + lane);
+            pr = pair_row_of(e, __ldg(expert_rank + n * k + lane), s, S, E, L, recv_part, cap_recv,
+                             off, cnt, sb, bad_id, bad_rank, dropped);
+            if (gs == 0) {
+                const int64_t q = n * k + lane;
+                pair_row[q] = pr;
+                if (pr >= 0) recv_pair[pr] = (int32_t)q;
+            }
+            if (pr >= 0) pp = e / L;
+        }
+        if (gs == 0 && lane < P) {
+            if (ts >= cap_send) pack_overflow = true;
+            else if (ts >= 0) send_src[(int64_t)s * cap_send + ts] = (int32_t)(n - (int64_t)s * T);
+        }
+        // quantize the segment once (every lane takes part in the block shuffles)
+        const int vb = gs * kQSegVec;
+        const QPiece q = quantize_piece<FMT>(x + n * V, V, vb, g, d);
+        uint8_t *send_s = send_q + (int64_t)s * cap_send * rb;
+        unsigned smask = __ballot_sync(kFull, lane < P && ts >= 0 && ts < cap_send);
+        while (smask) {
+            const int p = __ffs(smask) - 1;
+            smask &= smask - 1;
+            const int sl = __shfl_sync(kFull, ts, p);
+            store_piece<FMT>(send_s + (int64_t)sl * rb, V, vb, q);
+        }
+        unsigned rmask = __ballot_sync(kFull, pr >= 0);
+        while (rmask) {
+            const int j0 = __ffs(rmask) - 1;
+            const int p0 = __shfl_sync(kFull, pp, j0);
+            const unsigned gmask = __ballot_sync(kFull, pr >= 0 && pp == p0);
+            rmask &= ~gmask;
+            const int sl = __shfl_sync(kFull, ts, p0);
+            const bool ok = sl >= 0 && sl < cap_send;
+            if (!ok && gs == 0 && lane == 0) {
+                if (sl < 0) bad_slot = true;
+                else cap_flag = true;
+            }
+            QPiece r;
+            if (ok) {
+                r = load_piece<FMT>(send_s + (int64_t)sl * rb, V, vb);
+            } else {
+                r.code[0] = r.code[1] = make_uint4(0u, 0u, 0u, 0u);
+                r.sw = 0u;
+            }
+            unsigned dm = gmask;
+            while (dm) {
+                const int j = __ffs(dm) - 1;
+                dm &= dm - 1;
+                const int row = __shfl_sync(kFull, pr, j);
+                store_piece<FMT>(recv_q + (int64_t)row * rb, V, vb, r);
+            }
+        }
+    }
+
+    // padding records: a warp per (expert, padding row), zeroed in 16-byte vectors
+    if (align > 1) {
+        const int rbv = (int)(rb / 16);
+        const int64_t ptask = (int64_t)E * (align - 1);
+        for (int64_t task = gtid >> 5; task < ptask; task += gwarps) {
+            const int e = (int)(task / (align - 1));
+            const int i = (int)(task - (int64_t)e * (align - 1));
+            const int row = off[e] + cnt[e] + i;
+            if (!in_recv(e, E, L, recv_part) || row >= off[e + 1] || row >= cap_recv) continue;
+            int4 *dst = reinterpret_cast<int4 *>(recv_q + (int64_t)row * rb);
+            for (int vi = lane; vi < rbv; vi += 32) st_cg(dst + vi, make_int4(0, 0, 0, 0));
+            if (lane == 0) recv_pair[row] = -1;
+        }
+    }
+    mark_unused_rows(off[E], cap_recv, S, P, cap_send, part_offsets, recv_pair, send_src);
 
     if (cap_flag || dropped || pack_overflow) flag_status(dev_status, MOE_ERR_CAPACITY);
     if (bad_slot || bad_rank) flag_status(dev_status, MOE_ERR_INVALID_ARG);
@@ -670,6 +962,92 @@ cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T
                                      recv_part, align, cap_send, cap_recv, (int4 *)send, send_src,
                                      (int4 *)recv, expert_offsets, pair_row, recv_pair,
                                      dev_status));
+    return e;
+}
+
+cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n)
+{
+    if (T == 0) {                           // layout, pack and permute of an empty batch
+        *n = 3;
+        return cudaSuccess;
+    }
+    int nl = 0;
+    const cudaError_t e = layout_kernel_count(T, k, E, P, &nl);
+    if (e != cudaSuccess) return e;
+    *n = 1 + nl + (permute_map_fused(S, E) ? 1 : 3);
+    return cudaSuccess;
+}
+
+cudaError_t launch_dispatch_quantized(const float *logits, const uint16_t *x, int S, int T, int H,
+                                      int E, int k, int P, int format, float g, int recv_part,
+                                      int align, int cap_send, int cap_recv, int32_t *topk_ids,
+                                      float *topk_w, int32_t *expert_counts, int32_t *expert_rank,
+                                      int32_t *part_counts, int32_t *part_offsets,
+                                      int32_t *token_slot, uint8_t *send_q, int32_t *send_src,
+                                      uint8_t *recv_q, int32_t *expert_offsets, int32_t *pair_row,
+                                      int32_t *recv_pair, void *ws, uint32_t *dev_status,
+                                      cudaStream_t st)
+{
+    cudaError_t e;
+    const int64_t NT = (int64_t)S * T;
+    if ((e = launch_route_topk(logits, NT, E, k, topk_ids, topk_w, st)) != cudaSuccess) return e;
+    if ((e = launch_dispatch_layout(topk_ids, S, T, k, E, P, expert_counts, expert_rank,
+                                    part_counts, part_offsets, token_slot, ws, dev_status, st)) !=
+        cudaSuccess)
+        return e;
+    const int V = H / 8;
+    const int64_t rb = format == kQFmtMxfp8 ? (int64_t)V * 8 + V / 4 : (int64_t)V * 4 + V / 2;
+    if (T == 0 || !permute_map_fused(S, E)) {
+        // empty batch, or run starts too large for one CTA's shared memory:
+        // the separate quantized pack and the permute of records as opaque rows
+        e = format == kQFmtMxfp8
+                ? launch_dispatch_pack_mxfp8(x, S, T, H, P, token_slot, part_offsets, cap_send,
+                                             send_q, send_src, dev_status, st)
+                : launch_dispatch_pack_nvfp4(x, S, T, H, P, g, token_slot, part_offsets, cap_send,
+                                             send_q, send_src, dev_status, st);
+        if (e != cudaSuccess) return e;
+        return launch_permute((const uint16_t *)send_q, token_slot, topk_ids, expert_counts,
+                              expert_rank, S, T, k, E, P, (int)(rb / 2), recv_part, align,
+                              cap_send, cap_recv, (uint16_t *)recv_q, expert_offsets, pair_row,
+                              recv_pair, ws, dev_status, st);
+    }
+    DeviceInfo di;
+    if ((e = device_info(&di)) != cudaSuccess) return e;
+    const int L = E / P;
+    const int nseg = (V + kQSegVec - 1) / kQSegVec;
+    const size_t smem = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
+    const void *fn = format == kQFmtMxfp8 ? (const void *)k_pack_permute_q<kQFmtMxfp8>
+                                          : (const void *)k_pack_permute_q<kQFmtNvfp4>;
+    const int resident = resident_grid(fn, kPPThreads, smem);
+    const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
+    const int64_t warps = NT * nseg + (align > 1 ? (int64_t)E * (align - 1) : 0);
+    int64_t blocks = div_up(warps, kPPThreads / 32);
+    const int64_t tail = div_up((int64_t)cap_recv > (int64_t)S * cap_send ? cap_recv
+                                                                          : (int64_t)S * cap_send,
+                                kPPThreads);
+    const int64_t tail_blocks = tail < di.sm_count ? tail : di.sm_count;
+    if (blocks < tail_blocks) blocks = tail_blocks;
+    if (blocks > wave) blocks = wave;
+    if (blocks < 1) blocks = 1;
+    if (format == kQFmtMxfp8) {
+        MOE_TRACED_LAUNCH("k_pack_permute_mxfp8", st,
+                          e = launch_pdl(k_pack_permute_q<kQFmtMxfp8>, dim3((unsigned)blocks),
+                                         dim3(kPPThreads), smem, st, (const int4 *)x, token_slot,
+                                         (const int32_t *)part_offsets, (const int32_t *)topk_ids,
+                                         (const int32_t *)expert_counts,
+                                         (const int32_t *)expert_rank, S, NT, k, E, L, P, T, V,
+                                         recv_part, align, cap_send, cap_recv, g, send_q, send_src,
+                                         recv_q, expert_offsets, pair_row, recv_pair, dev_status));
+    } else {
+        MOE_TRACED_LAUNCH("k_pack_permute_nvfp4", st,
+                          e = launch_pdl(k_pack_permute_q<kQFmtNvfp4>, dim3((unsigned)blocks),
+                                         dim3(kPPThreads), smem, st, (const int4 *)x, token_slot,
+                                         (const int32_t *)part_offsets, (const int32_t *)topk_ids,
+                                         (const int32_t *)expert_counts,
+                                         (const int32_t *)expert_rank, S, NT, k, E, L, P, T, V,
+                                         recv_part, align, cap_send, cap_recv, g, send_q, send_src,
+                                         recv_q, expert_offsets, pair_row, recv_pair, dev_status));
+    }
     return e;
 }
 

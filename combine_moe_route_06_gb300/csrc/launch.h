@@ -118,6 +118,18 @@ cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T
                             uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
                             int32_t *recv_pair, void *ws, uint32_t *dev_status, cudaStream_t st);
 
+// The dispatch side with quantized rows (format 1: MXFP8 records, 2: NVFP4).
+cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n);
+cudaError_t launch_dispatch_quantized(const float *logits, const uint16_t *x, int S, int T, int H,
+                                      int E, int k, int P, int format, float g, int recv_part,
+                                      int align, int cap_send, int cap_recv, int32_t *topk_ids,
+                                      float *topk_w, int32_t *expert_counts, int32_t *expert_rank,
+                                      int32_t *part_counts, int32_t *part_offsets,
+                                      int32_t *token_slot, uint8_t *send_q, int32_t *send_src,
+                                      uint8_t *recv_q, int32_t *expert_offsets, int32_t *pair_row,
+                                      int32_t *recv_pair, void *ws, uint32_t *dev_status,
+                                      cudaStream_t st);
+
 cudaError_t launch_expert_scale(const uint16_t *recv, const int32_t *expert_offsets,
                                 const float *scale, int E, int H, int cap_recv, uint16_t *y,
                                 cudaStream_t st);

@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "quant.cuh"
 #include "trace.h"
 
 namespace moe {
@@ -122,20 +123,9 @@ __global__ void __launch_bounds__(kPackThreads) k_pack(const int4 *__restrict__ 
 // byte per 32).  A record is H E4M3 codes followed by H/32 E8M0 scales,
 //   X = 2^(floor(log2 max|v|) - 8), code = e4m3_rn_satfinite(v / X).
 // One warp per (token, 1,024-value segment); lanes 4b..4b+3 hold one 32-value
-// block for each of the four 16-byte loads.  The row is quantized once and
-// stored to every destination slot.  Finite inputs give se <= 120, so the
-// 2^-se factor below is a normal float.
+// block for each of the four 16-byte loads (mxfp8_quantize in quant.cuh).  The
+// row is quantized once and stored to every destination slot.
 constexpr int kQSegVec = 32 * kPackUnroll;   // int4 (8 values) per segment
-
-__device__ __forceinline__ int mx_shared_exp(float amax)
-{
-    if (amax == 0.f) return -127;
-    const unsigned bits = __float_as_uint(amax);
-    const int field = (int)((bits >> 23) & 0xFFu);
-    const int e = field ? field - 127 : (31 - __clz((int)(bits & 0x7FFFFFu))) - 149;
-    const int se = e - 8;
-    return se < -127 ? -127 : (se > 127 ? 127 : se);
-}
 
 __global__ void __launch_bounds__(kPackThreads) k_pack_mxfp8(
     const int4 *__restrict__ x, int S, int T, int V, int P, const int32_t *__restrict__ token_slot,
@@ -177,28 +167,7 @@ __global__ void __launch_bounds__(kPackThreads) k_pack_mxfp8(
             const int vi = v0 + 32 * u;
             int4 v = make_int4(0, 0, 0, 0);
             if (vi < V) v = ld_stream(x + n * V + vi);
-            const uint32_t w4[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
-            float f[8];
-            float amax = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                f[2 * i] = __uint_as_float(w4[i] << 16);
-                f[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
-                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-            }
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-            const int se = mx_shared_exp(amax);
-            const float inv = __uint_as_float((uint32_t)(127 - se) << 23);   // 2^-se, exact
-            // two values per conversion (round to nearest even, saturate to
-            // finite); the pair's first value lands in the low byte
-            uint32_t c2[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-                c2[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(
-                    make_float2(f[2 * i] * inv, f[2 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-            code[u] = make_uint2(c2[0] | (c2[1] << 16), c2[2] | (c2[3] << 16));
-            scale[u] = (uint8_t)(se + 127);
+            mxfp8_quantize(v, code[u], scale[u]);
         }
         while (dmask) {
             const int p = __ffs(dmask) - 1;
@@ -267,30 +236,7 @@ __global__ void __launch_bounds__(kPackThreads) k_pack_nvfp4(
             const int vi = v0 + 32 * u;
             int4 v = make_int4(0, 0, 0, 0);
             if (vi < V) v = ld_stream(x + n * V + vi);
-            const uint32_t w4[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
-            float f[8];
-            float amax = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                f[2 * i] = __uint_as_float(w4[i] << 16);
-                f[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
-                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-            }
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-            const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(__fdiv_rn(amax, d), __NV_SATFINITE,
-                                                                __NV_E4M3);
-            const __half_raw sh = __nv_cvt_fp8_to_halfraw(sb, __NV_E4M3);
-            const float sg = __fmul_rn(__half2float(*reinterpret_cast<const __half *>(&sh)), g);
-            uint32_t c = 0;
-            if (sg != 0.f) {
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const float2 q = make_float2(__fdiv_rn(f[2 * i], sg), __fdiv_rn(f[2 * i + 1], sg));
-                    c |= (uint32_t)__nv_cvt_float2_to_fp4x2(q, __NV_E2M1, cudaRoundNearest) << (8 * i);
-                }
-            }
-            code[u] = c;
-            scale[u] = (uint8_t)sb;
+            nvfp4_quantize(v, g, d, code[u], scale[u]);
         }
         while (dmask) {
             const int p = __ffs(dmask) - 1;

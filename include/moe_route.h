@@ -21,6 +21,7 @@
  *   moe_dispatch_pack_routed,       rows that carry their ids and weights,
  *   moe_routed_expert_stage1        and the routed expert's per-partition sum (sections 6.1, 7.1)
  *   moe_dispatch_pack_mxfp8 / _nvfp4  rows quantized once before they are sent (section 7.2)
+ *   moe_dispatch_quantized          moe_dispatch with MXFP8 or NVFP4 records  (section 7.2)
  *   moe_plan_placement (host),      experts placed by load with copies of the
  *   moe_dispatch_layout_mapped      hot ones ("Beyond One GPU", section 6)
  *   moe_dispatch_layout_static      the layout for callers that cannot allocate
@@ -95,6 +96,10 @@ typedef enum {
 } moe_status_t;
 
 #define MOE_STATUS_BIT(code) (1u << (code))
+
+/* Row formats of moe_dispatch_quantized. */
+#define MOE_FORMAT_MXFP8 1
+#define MOE_FORMAT_NVFP4 2
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int moe_version(void);
@@ -463,6 +468,35 @@ moe_status_t moe_dispatch(const float *logits, const uint16_t *x, int S, int T, 
  * thread's current device (1 for the one-launch form); -1 for invalid sizes.
  */
 int moe_dispatch_kernels(int S, int T, int k, int E, int P);
+
+/*
+ * moe_dispatch with the rows sent as quantized records (a2a-backends section
+ * 7.2: tokens are converted before they are sent): the outputs of
+ * moe_route_topk, moe_dispatch_layout, moe_dispatch_pack_mxfp8 (format
+ * MOE_FORMAT_MXFP8, H a multiple of 512) or moe_dispatch_pack_nvfp4 (format
+ * MOE_FORMAT_NVFP4, H a multiple of 256, global_scale its tensor scale g) and
+ * moe_permute_to_experts of the records as opaque rows, byte for byte.
+ *   send_q  [S][cap_send][rb] uint8 out, recv_q [cap_recv][rb] uint8 out, both
+ *           16-byte aligned; rb = H + H/32 (MXFP8) or H/2 + H/16 (NVFP4).
+ *   The other arguments and the errors are those of moe_dispatch (plus a bad
+ *   format, H or global_scale: MOE_ERR_INVALID_ARG).
+ * Kernels: the routing kernel, the layout's kernel(s), then one pass that
+ * quantizes each row segment once, stores the piece to the token's send
+ * records, reads each receiving partition's piece back and stores it to the
+ * pair records (the separate pack and permute for T = 0 or when the S*E
+ * counts do not fit one CTA's shared memory); moe_dispatch_quantized_kernels
+ * reports the count (-1 for invalid sizes).
+ */
+moe_status_t moe_dispatch_quantized(const float *logits, const uint16_t *x, int S, int T, int H,
+                                    int E, int k, int P, int format, float global_scale,
+                                    int recv_part, int align, int cap_send, int cap_recv,
+                                    int32_t *topk_ids, float *topk_w, int32_t *expert_counts,
+                                    int32_t *expert_rank, int32_t *part_counts,
+                                    int32_t *part_offsets, int32_t *token_slot, uint8_t *send_q,
+                                    int32_t *send_src, uint8_t *recv_q, int32_t *expert_offsets,
+                                    int32_t *pair_row, int32_t *recv_pair, void *ws,
+                                    size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
+int moe_dispatch_quantized_kernels(int S, int T, int k, int E, int P);
 
 /*
  * Masked receive layout (a2a-backends section 4.1: a region per (local expert,

@@ -214,3 +214,26 @@ def test_dispatch_rejects(lib):
         _rejects(lib.moe_dispatch, bad, needle)
     assert lib.moe_dispatch_kernels(1, 16, 6, 385, 8) == -1     # E % P != 0
     assert lib.moe_dispatch_kernels(1, -1, 6, 384, 8) == -1     # T < 0
+
+
+def test_dispatch_quantized_rejects(lib):
+    """moe_dispatch_quantized checks its format, the row width the format needs and
+    the NVFP4 tensor scale on the host, besides moe_dispatch's arguments."""
+    ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
+    f = ctypes.c_float
+    good = ([FAKE, FAKE, 1, 64, 512, 16, 2, 4, 1, f(1.0), -1, 1, 128, 128] + [FAKE] * 13
+            + [FAKE, ws, FAKE, ST])
+    for idx, val, needle in ((8, 3, "format"), (4, 256, "multiple of 512"), (7, 3, "multiple of P"),
+                             (10, 4, "recv_part"), (0, NULL, "`logits`"), (21, NULL, "`send_q`"),
+                             (28, ws - 1, "ws_bytes")):
+        bad = list(good)
+        bad[idx] = val
+        _rejects(lib.moe_dispatch_quantized, bad, needle)
+    nv = list(good)
+    nv[8] = 2
+    nv[4] = 384                                         # NVFP4 needs H % 256 == 0
+    _rejects(lib.moe_dispatch_quantized, nv, "multiple of 256")
+    nv[4] = 256
+    nv[9] = f(0.0)
+    _rejects(lib.moe_dispatch_quantized, nv, "global_scale")
+    assert lib.moe_dispatch_quantized_kernels(1, 16, 6, 385, 8) == -1

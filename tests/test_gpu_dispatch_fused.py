@@ -9,6 +9,8 @@ oracle.  The one-launch form (one source of 1..256 tokens) is covered at its
 edges (1, 63, 64, 65, 255, 256 tokens; E from 16 to 1024; k and P up to 32;
 8-value and ragged rows; run alignment; a receiving partition), and the
 launch counts the library reports are checked against the launch trace.
+moe_dispatch_quantized (MXFP8 and NVFP4 records) is held to the separate
+quantized pack and permute the same way, and its records to the oracle's.
 """
 import numpy as np
 import pytest
@@ -209,3 +211,90 @@ def test_fused_decode_step_in_a_cuda_graph():
         want = ms.f32_from_bf16_bits(ref["out"]).astype(np.float64)
         assert np.all(np.abs(got - want) <= 1e-2 * np.maximum(np.abs(want), 1e-3))
     assert int(path.dev_status.item()) == 0
+
+
+# ------------------------------------------------------ quantized records --
+
+def _dispatch_q(mode, quant, w_, inp, g=1.0, recv_part=-1, align=1, cap_send=None,
+                cap_recv=None, trace=False):
+    """One quantized dispatch through `mode` with sentinel-filled outputs."""
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, recv_part=recv_part, align=align,
+                     cap_send=cap_send, cap_recv=cap_recv, quant=quant, nvfp4_scale=g,
+                     dispatch=mode)
+    for name in OUT_I32:
+        getattr(path, name).fill_(-7)
+    path.topk_w.fill_(-9.0)
+    path.send.fill_(0x5A)
+    path.recv.fill_(0x3C)
+    logits, x = f32_dev(inp["logits"]), bf16_dev(inp["x"])
+    torch.cuda.synchronize()
+    if trace:
+        m.trace_enable(None, 64)
+        m.trace_reset()
+    try:
+        if mode == "fused":
+            path.dispatch_fused(logits, x)
+        else:
+            path.route(logits)
+            path.dispatch(x)
+        torch.cuda.synchronize()
+        kernels = [n for n, _ in m.trace_records()] if trace else None
+    finally:
+        if trace:
+            m.trace_disable()
+    out = {name: host(getattr(path, name)) for name in OUT_I32}
+    out["topk_w"] = host(path.topk_w).view(np.uint32)
+    out["send"] = host(path.send)
+    out["recv"] = host(path.recv)
+    out["status"] = int(path.dev_status.item())
+    return out, kernels
+
+
+def _q_oracle(quant, w_, inp, g=1.0, recv_part=-1, align=1):
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    cap_send = w_.T * min(w_.k, w_.P)
+    if quant == "mxfp8":
+        q, src, st = oracle.dispatch_pack_mxfp8(inp["x"], lay["token_slot"], cap_send)
+    else:
+        q, src, st = oracle.dispatch_pack_nvfp4(inp["x"], lay["token_slot"], cap_send, g)
+    per = oracle.permute_to_experts(q.view(np.uint16), lay["token_slot"], ids, w_.E,
+                                    recv_part=recv_part, align=align)
+    return lay, q, src, per
+
+
+@pytest.mark.parametrize("quant,g", [("mxfp8", 1.0), ("nvfp4", 1.0), ("nvfp4", 0.02)])
+@pytest.mark.parametrize("name,over,recv_part,align", [
+    ("decode", {}, -1, 1), ("prefill", {}, -1, 1), ("large", {}, -1, 1),
+    ("tiny", {"S": 2, "T": 300, "H": 512, "E": 64, "k": 8, "P": 8}, 2, 8)])
+def test_quantized_fused_equals_separate_and_oracle(quant, g, name, over, recv_part, align):
+    w_ = ms.workload(name, **over)
+    inp = ms.gen_inputs(w_)
+    fused, kf = _dispatch_q("fused", quant, w_, inp, g, recv_part, align, trace=True)
+    sep, _ = _dispatch_q("separate", quant, w_, inp, g, recv_part, align)
+    _same(fused, sep)
+    assert kf[-1] == f"k_pack_permute_{quant}", kf
+    assert len(kf) == m.moe_dispatch_quantized_kernels(w_.S, w_.T, w_.k, w_.E, w_.P), kf
+    lay, q, src, per = _q_oracle(quant, w_, inp, g, recv_part, align)
+    for key in ("token_slot", "part_offsets", "expert_counts"):
+        assert np.array_equal(fused[key], lay[key]), key
+    for key in ("expert_offsets", "pair_row", "recv_pair"):
+        assert np.array_equal(fused[key], per[key]), key
+    for s in range(w_.S):
+        used = int(lay["part_offsets"][s, -1])
+        assert np.array_equal(fused["send"][s, :used], q[s, :used])
+        assert np.array_equal(fused["send_src"][s], src[s])
+    rows = int(per["expert_offsets"][-1])
+    assert np.array_equal(fused["recv"][:rows], per["recv"].view(np.uint8)[:rows])
+    assert fused["status"] == 0
+
+
+@pytest.mark.parametrize("quant", ["mxfp8", "nvfp4"])
+def test_quantized_capacity_overflow_matches_separate(quant):
+    w_ = ms.workload("prefill", T=600, index=41)
+    inp = ms.gen_inputs(w_)
+    for cap_send, cap_recv in ((600, None), (None, 1200)):
+        fused, _ = _dispatch_q("fused", quant, w_, inp, 1.0, cap_send=cap_send, cap_recv=cap_recv)
+        sep, _ = _dispatch_q("separate", quant, w_, inp, 1.0, cap_send=cap_send, cap_recv=cap_recv)
+        _same(fused, sep)
+        assert fused["status"] & m.status_bit(m.MOE_ERR_CAPACITY)

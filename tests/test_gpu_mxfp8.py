@@ -150,13 +150,15 @@ def _oracle_quant_path(w_, inp, scales, recv_part=-1, align=1):
                 status=st | per["status"])
 
 
+@pytest.mark.parametrize("dispatch", ["fused", "separate"])
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill"])
-def test_mxfp8_path(name):
+def test_mxfp8_path(name, dispatch):
+    """The quantized path through moe_dispatch_quantized or the separate calls."""
     over = {"H": 512} if name == "tiny" else {}
     w_ = ms.workload(name, **over)
     inp = ms.gen_inputs(w_)
     ref = _oracle_quant_path(w_, inp, inp["scales"])
-    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, quant="mxfp8")
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, quant="mxfp8", dispatch=dispatch)
     out = path.step(f32_dev(inp["logits"]), bf16_dev(inp["x"]), f32_dev(inp["scales"]))
     torch.cuda.synchronize()
     assert np.array_equal(host(path.pair_row), ref["permute"]["pair_row"])
@@ -171,18 +173,23 @@ def test_mxfp8_path(name):
     assert int(path.dev_status.item()) == 0 == ref["status"]
 
 
-def test_mxfp8_path_bound_calls_and_identity_scale():
+@pytest.mark.parametrize("dispatch", ["fused", "separate"])
+def test_mxfp8_path_bound_calls_and_identity_scale(dispatch):
     """The pre-marshalled calls give the same bytes as the checked calls; with unit
     scales the output is the combine of the dequantized rows."""
     w_ = ms.workload("decode")
     inp = ms.gen_inputs(w_)
-    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, quant="mxfp8")
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, quant="mxfp8", dispatch=dispatch)
     lg, xx = f32_dev(inp["logits"]), bf16_dev(inp["x"])
     out1 = bf16_host(path.step(lg, xx)).copy()
     calls = path.bind(lg, xx)
-    # route, layout, pack, permute, expert, combine; at T = 64 the layout is one kernel,
-    # and the permute one (its map step runs inside the copy kernel)
-    assert len(calls) == 6 and path.launches_per_step() == 6
+    if dispatch == "separate":
+        # route, layout, pack, permute, expert, combine; at T = 64 the layout is one
+        # kernel, and the permute one (its map step runs inside the copy kernel)
+        assert len(calls) == 6 and path.launches_per_step() == 6
+    else:
+        # moe_dispatch_quantized (route, layout, pack + permute), expert, combine
+        assert len(calls) == 3 and path.launches_per_step() == 5
     path.out.zero_()
     m.MoePath.run_bound(calls)
     torch.cuda.synchronize()

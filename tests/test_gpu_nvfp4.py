@@ -131,12 +131,15 @@ def _oracle_path(w_, inp, scales, g):
                 out=oracle.combine(y, per["pair_row"], wts), status=st | per["status"])
 
 
+@pytest.mark.parametrize("dispatch", ["fused", "separate"])
 @pytest.mark.parametrize("name,g", [("tiny", 1.0), ("decode", 1.0), ("prefill", 0.02)])
-def test_nvfp4_path(name, g):
+def test_nvfp4_path(name, g, dispatch):
+    """The NVFP4 path through moe_dispatch_quantized or the separate calls."""
     w_ = ms.workload(name)
     inp = ms.gen_inputs(w_)
     ref = _oracle_path(w_, inp, inp["scales"], g)
-    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, quant="nvfp4", nvfp4_scale=g)
+    path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, quant="nvfp4", nvfp4_scale=g,
+                     dispatch=dispatch)
     out = path.step(f32_dev(inp["logits"]), bf16_dev(inp["x"]), f32_dev(inp["scales"]))
     torch.cuda.synchronize()
     used = int(ref["layout"]["part_offsets"][0, -1])
@@ -147,4 +150,4 @@ def test_nvfp4_path(name, g):
     assert close_bf16(bf16_host(out), ref["out"]), worst_rel(bf16_host(out), ref["out"])
     assert int(path.dev_status.item()) == 0 == ref["status"]
     calls = path.bind(f32_dev(inp["logits"]), bf16_dev(inp["x"]), scale=f32_dev(inp["scales"]))
-    assert len(calls) == 6
+    assert len(calls) == (6 if dispatch == "separate" else 3)
