@@ -52,14 +52,15 @@ DOMINANT_BY_VARIANT = {"two_stage": ("k_combine_stage1", "stage1"),
 # of the code (comments and whitespace removed, source_code_sha16) of the file
 # the kernel was built from when it was captured (k_perm_copy at commit 120a03f;
 # its file lost two helpers to common.cuh since, the kernel unchanged, and is
-# hashed as it stands now; k_pack_permute at commit 62ef766).  The line reports null instead once that file has
+# hashed as it stands now; k_pack_permute as of the commit that adds
+# moe_dispatch_pack_permute).  The line reports null instead once that file has
 # changed, so a stale capture is never quoted.
 DOMINANT_TRAFFIC = {("k_perm_copy", "prefill"): {"bytes": 142.5e6 + 252.9e6,
                                                  "source": "combine_moe_route_06_gb300/csrc/permute.cu",
                                                  "sha16": "63c0e1b6e21e91ff"},
-                    ("k_pack_permute", "prefill"): {"bytes": 43.8e6 + 429.5e6,
+                    ("k_pack_permute", "prefill"): {"bytes": 42.2e6 + 429.8e6,
                                                     "source": "combine_moe_route_06_gb300/csrc/dispatch.cu",
-                                                    "sha16": "212af651d05194d7"}}
+                                                    "sha16": "197467989d697c9b"}}
 
 
 def source_code_sha16(path: str) -> str:

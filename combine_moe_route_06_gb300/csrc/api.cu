@@ -372,6 +372,58 @@ moe_status_t moe_dispatch(const float *logits, const uint16_t *x, int S, int T, 
                        __func__);
 }
 
+int moe_dispatch_pack_permute_kernels(int S, int T, int k, int E, int P)
+{
+    if (check_sizes("moe_dispatch_pack_permute_kernels", S, T, k, E, P) != MOE_OK) return -1;
+    return pack_permute_kernel_count(S, T, E);
+}
+
+moe_status_t moe_dispatch_pack_permute(const uint16_t *x, const int32_t *token_slot,
+                                       const int32_t *part_offsets, const int32_t *topk_ids,
+                                       const int32_t *expert_counts, const int32_t *expert_rank,
+                                       int S, int T, int k, int E, int P, int H, int recv_part,
+                                       int align, int cap_send, int cap_recv, uint16_t *send,
+                                       int32_t *send_src, uint16_t *recv,
+                                       int32_t *expert_offsets, int32_t *pair_row,
+                                       int32_t *recv_pair, void *ws, size_t ws_bytes,
+                                       uint32_t *dev_status, cudaStream_t stream)
+{
+    MOE_CALL_RANGE();
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, P)", __func__,
+            recv_part);
+    REQUIRE(align >= 1 && align <= 1024, "%s: align=%d must be in [1, 1024]", __func__, align);
+    REQUIRE(cap_send >= 0 && cap_recv >= 0, "%s: capacities must be >= 0", __func__);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    REQUIRE((int64_t)S * T * k + (int64_t)E * (align - 1) < ((int64_t)1 << 31),
+            "%s: S*T*k + E*(align-1) must be < 2^31", __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(x, NT * H, 16);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(expert_counts, (int64_t)S * E, 4);
+    REQUIRE_ARR(expert_rank, NT * k, 4);
+    REQUIRE_ARR(send, (int64_t)S * cap_send * H, 16);
+    REQUIRE_ARR(send_src, (int64_t)S * cap_send, 4);
+    REQUIRE_ARR(recv, (int64_t)cap_recv * H, 16);
+    REQUIRE_ARR(expert_offsets, E + 1, 4);
+    REQUIRE_ARR(pair_row, NT * k, 4);
+    REQUIRE_ARR(recv_pair, cap_recv, 4);
+    REQUIRE_STATUS(dev_status);
+    const size_t need = moe_workspace_bytes(S, T, k, E, P);
+    REQUIRE_ARR(ws, need, 256);
+    REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
+    return cuda_status(launch_pack_permute(x, token_slot, part_offsets, topk_ids, expert_counts,
+                                           expert_rank, S, T, k, E, P, H, recv_part, align,
+                                           cap_send, cap_recv, send, send_src, recv,
+                                           expert_offsets, pair_row, recv_pair, ws, dev_status,
+                                           stream, false),
+                       __func__);
+}
+
 int moe_dispatch_quantized_kernels(int S, int T, int k, int E, int P)
 {
     if (check_sizes("moe_dispatch_quantized_kernels", S, T, k, E, P) != MOE_OK) return -1;

@@ -448,20 +448,23 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
     int64_t NT, int k, int E, int L, int P, int T, int V, int recv_part, int align, int cap_send,
     int cap_recv, int4 *__restrict__ send, int32_t *__restrict__ send_src,
     int4 *__restrict__ recv, int32_t *__restrict__ expert_offsets, int32_t *__restrict__ pair_row,
-    int32_t *__restrict__ recv_pair, uint32_t *dev_status)
+    int32_t *__restrict__ recv_pair, uint32_t *dev_status, bool x_before_wait)
 {
     const int lane = threadIdx.x & 31;
     const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t gwarps = gthreads >> 5;
     const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
-    // The first task's x segment is loaded before the grid-dependency wait, so
-    // its HBM latency passes while the layout finishes.  x was complete before
-    // the routing kernel ran: this kernel is launched only once the layout
-    // kernel has passed its own wait (it waits, then lets dependents launch),
-    // and the layout's wait returns only after the routing kernel, which waited
-    // for everything before it, has completed.  Nothing here reads what the
-    // layout writes before pdl_wait().
+    // With x_before_wait the first task's x segment is loaded before the
+    // grid-dependency wait, so its HBM latency passes while the layout finishes.
+    // moe_dispatch sets it: x was complete before its routing kernel ran, this
+    // kernel is launched only once the layout kernel has passed its own wait (it
+    // waits, then lets dependents launch), and the layout's wait returns only
+    // after the routing kernel, which waited for everything before it, has
+    // completed.  Nothing here reads what the layout writes before pdl_wait().
+    // Called on its own (moe_dispatch_pack_permute) the kernel does not know
+    // what ran before it, so it waits first.
+    if (!x_before_wait) pdl_wait();
     const int64_t rt0 = gtid >> 5;
     int4 x0[kPPUnroll];
     if (rt0 < NT * nseg) {
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
             if (vi < V) x0[u] = ld_stream(x + n0 * V + vi);
         }
     }
-    pdl_wait();
+    if (x_before_wait) pdl_wait();
     pdl_trigger();
     bool cap_flag = false, bad_slot = false, dropped = false, bad_rank = false, bad_id = false;
     bool pack_overflow = false;
@@ -871,6 +874,60 @@ cudaError_t launch_small(const float *logits, const uint16_t *x, int T, int H, i
 
 }  // namespace
 
+int pack_permute_kernel_count(int S, int T, int E)
+{
+    if (T == 0) return 2;                    // the separate pack and permute
+    return permute_map_fused(S, E) ? 1 : 3;  // else pack, map and copy
+}
+
+cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
+                                const int32_t *part_offsets, const int32_t *topk_ids,
+                                const int32_t *expert_counts, const int32_t *expert_rank, int S,
+                                int T, int k, int E, int P, int H, int recv_part, int align,
+                                int cap_send, int cap_recv, uint16_t *send, int32_t *send_src,
+                                uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
+                                int32_t *recv_pair, void *ws, uint32_t *dev_status,
+                                cudaStream_t st, bool x_before_wait)
+{
+    cudaError_t e;
+    if (T == 0 || !permute_map_fused(S, E)) {
+        // empty batch, or run starts too large for one CTA's shared memory:
+        // the separate pack and permute
+        if ((e = launch_dispatch_pack(x, S, T, H, P, token_slot, part_offsets, cap_send, send,
+                                      send_src, dev_status, st)) != cudaSuccess)
+            return e;
+        return launch_permute(send, token_slot, topk_ids, expert_counts, expert_rank, S, T, k, E, P,
+                              H, recv_part, align, cap_send, cap_recv, recv, expert_offsets,
+                              pair_row, recv_pair, ws, dev_status, st);
+    }
+    DeviceInfo di;
+    if ((e = device_info(&di)) != cudaSuccess) return e;
+    const int64_t NT = (int64_t)S * T;
+    const int V = H / 8;
+    const int L = E / P;
+    const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
+    const size_t smem = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
+    const int resident = resident_grid((const void *)k_pack_permute, kPPThreads, smem);
+    const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
+    const int64_t warps = NT * nseg + (align > 1 ? (int64_t)E * (align - 1) * nseg : 0);
+    int64_t blocks = div_up(warps, kPPThreads / 32);
+    const int64_t tail = div_up((int64_t)cap_recv > (int64_t)S * cap_send ? cap_recv
+                                                                          : (int64_t)S * cap_send,
+                                kPPThreads);
+    const int64_t tail_blocks = tail < di.sm_count ? tail : di.sm_count;
+    if (blocks < tail_blocks) blocks = tail_blocks;
+    if (blocks > wave) blocks = wave;
+    if (blocks < 1) blocks = 1;
+    MOE_TRACED_LAUNCH("k_pack_permute", st,
+                      e = launch_pdl(k_pack_permute, dim3((unsigned)blocks), dim3(kPPThreads), smem,
+                                     st, (const int4 *)x, token_slot, part_offsets, topk_ids,
+                                     expert_counts, expert_rank, S, NT, k, E, L, P, T, V,
+                                     recv_part, align, cap_send, cap_recv, (int4 *)send, send_src,
+                                     (int4 *)recv, expert_offsets, pair_row, recv_pair,
+                                     dev_status, x_before_wait));
+    return e;
+}
+
 cudaError_t dispatch_kernel_count(int S, int T, int k, int E, int P, int *n)
 {
     bool small = false;
@@ -880,13 +937,9 @@ cudaError_t dispatch_kernel_count(int S, int T, int k, int E, int P, int *n)
         *n = 1;
         return cudaSuccess;
     }
-    if (T == 0) {                           // layout, pack and permute of an empty batch
-        *n = 3;
-        return cudaSuccess;
-    }
-    int nl = 0;
-    if ((e = layout_kernel_count(T, k, E, P, &nl)) != cudaSuccess) return e;
-    *n = 1 + nl + (permute_map_fused(S, E) ? 1 : 3);
+    int nl = 1;                             // an empty batch: one layout kernel
+    if (T > 0 && (e = layout_kernel_count(T, k, E, P, &nl)) != cudaSuccess) return e;
+    *n = (T > 0 ? 1 : 0) + nl + pack_permute_kernel_count(S, T, E);
     return cudaSuccess;
 }
 
@@ -926,43 +979,10 @@ cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T
                                     part_counts, part_offsets, token_slot, ws, dev_status, st)) !=
         cudaSuccess)
         return e;
-    if (T == 0 || !permute_map_fused(S, E)) {
-        // empty batch, or run starts too large for one CTA's shared memory:
-        // the separate pack and permute
-        if ((e = launch_dispatch_pack(x, S, T, H, P, token_slot, part_offsets, cap_send, send,
-                                      send_src, dev_status, st)) != cudaSuccess)
-            return e;
-        return launch_permute(send, token_slot, topk_ids, expert_counts, expert_rank, S, T, k, E, P,
-                              H, recv_part, align, cap_send, cap_recv, recv, expert_offsets,
-                              pair_row, recv_pair, ws, dev_status, st);
-    }
-    DeviceInfo di;
-    if ((e = device_info(&di)) != cudaSuccess) return e;
-    const int V = H / 8;
-    const int L = E / P;
-    const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
-    const size_t smem = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
-    const int resident = resident_grid((const void *)k_pack_permute, kPPThreads, smem);
-    const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
-    const int64_t warps = NT * nseg + (align > 1 ? (int64_t)E * (align - 1) * nseg : 0);
-    int64_t blocks = div_up(warps, kPPThreads / 32);
-    const int64_t tail = div_up((int64_t)cap_recv > (int64_t)S * cap_send ? cap_recv
-                                                                          : (int64_t)S * cap_send,
-                                kPPThreads);
-    const int64_t tail_blocks = tail < di.sm_count ? tail : di.sm_count;
-    if (blocks < tail_blocks) blocks = tail_blocks;
-    if (blocks > wave) blocks = wave;
-    if (blocks < 1) blocks = 1;
-    MOE_TRACED_LAUNCH("k_pack_permute", st,
-                      e = launch_pdl(k_pack_permute, dim3((unsigned)blocks), dim3(kPPThreads), smem,
-                                     st, (const int4 *)x, (const int32_t *)token_slot,
-                                     (const int32_t *)part_offsets, (const int32_t *)topk_ids,
-                                     (const int32_t *)expert_counts,
-                                     (const int32_t *)expert_rank, S, NT, k, E, L, P, T, V,
-                                     recv_part, align, cap_send, cap_recv, (int4 *)send, send_src,
-                                     (int4 *)recv, expert_offsets, pair_row, recv_pair,
-                                     dev_status));
-    return e;
+    return launch_pack_permute(x, token_slot, part_offsets, topk_ids, expert_counts, expert_rank,
+                               S, T, k, E, P, H, recv_part, align, cap_send, cap_recv, send,
+                               send_src, recv, expert_offsets, pair_row, recv_pair, ws, dev_status,
+                               st, true);
 }
 
 cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n)

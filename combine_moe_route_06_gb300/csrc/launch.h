@@ -118,6 +118,19 @@ cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T
                             uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
                             int32_t *recv_pair, void *ws, uint32_t *dev_status, cudaStream_t st);
 
+// Pack and permute in one pass given a layout (x_before_wait: the launcher
+// guarantees that x was complete before the previous kernel passed its grid
+// dependency wait); the kernels it enqueues.
+int pack_permute_kernel_count(int S, int T, int E);
+cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
+                                const int32_t *part_offsets, const int32_t *topk_ids,
+                                const int32_t *expert_counts, const int32_t *expert_rank, int S,
+                                int T, int k, int E, int P, int H, int recv_part, int align,
+                                int cap_send, int cap_recv, uint16_t *send, int32_t *send_src,
+                                uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
+                                int32_t *recv_pair, void *ws, uint32_t *dev_status,
+                                cudaStream_t st, bool x_before_wait);
+
 // The dispatch side with quantized rows (format 1: MXFP8 records, 2: NVFP4).
 cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n);
 cudaError_t launch_dispatch_quantized(const float *logits, const uint16_t *x, int S, int T, int H,

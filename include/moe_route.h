@@ -14,6 +14,7 @@
  *                           order, fp32 accumulation, bf16 out               (sections 7.1, 7.2)
  *   moe_dispatch            route + layout + pack + permute in one call,
  *                           one launch for a decode-sized batch              (section 1.4)
+ *   moe_dispatch_pack_permute  pack + permute in one pass, any layout        (sections 3.2, 5.1)
  *
  * Further forms of the same round trip, each declared below with its source:
  *   moe_permute_to_experts_masked   a fixed block per expert plus a count     (sections 4.1, 4.2)
@@ -468,6 +469,30 @@ moe_status_t moe_dispatch(const float *logits, const uint16_t *x, int S, int T, 
  * thread's current device (1 for the one-launch form); -1 for invalid sizes.
  */
 int moe_dispatch_kernels(int S, int T, int k, int E, int P);
+
+/*
+ * Pack and permute in one call, for a layout the caller computed (for example
+ * moe_dispatch_layout_mapped over a placement with expert copies): the outputs
+ * of moe_dispatch_pack followed by moe_permute_to_experts with the same
+ * arguments, byte for byte, from one pass over the rows while the S*E counts
+ * fit one CTA's shared memory (each row segment read once from x, stored to
+ * the token's send rows, the receiving partitions' send rows read back right
+ * after and stored to the pair rows); otherwise, and for T = 0, the two
+ * separate calls' kernels.  Arguments and errors as those two calls (x, part_offsets
+ * and send_src from moe_dispatch_pack; the rest from moe_permute_to_experts).
+ * moe_dispatch_pack_permute_kernels reports the kernels it enqueues (-1 for
+ * invalid sizes).
+ */
+moe_status_t moe_dispatch_pack_permute(const uint16_t *x, const int32_t *token_slot,
+                                       const int32_t *part_offsets, const int32_t *topk_ids,
+                                       const int32_t *expert_counts, const int32_t *expert_rank,
+                                       int S, int T, int k, int E, int P, int H, int recv_part,
+                                       int align, int cap_send, int cap_recv, uint16_t *send,
+                                       int32_t *send_src, uint16_t *recv,
+                                       int32_t *expert_offsets, int32_t *pair_row,
+                                       int32_t *recv_pair, void *ws, size_t ws_bytes,
+                                       uint32_t *dev_status, cudaStream_t stream);
+int moe_dispatch_pack_permute_kernels(int S, int T, int k, int E, int P);
 
 /*
  * moe_dispatch with the rows sent as quantized records (a2a-backends section

@@ -237,3 +237,17 @@ def test_dispatch_quantized_rejects(lib):
     nv[9] = f(0.0)
     _rejects(lib.moe_dispatch_quantized, nv, "global_scale")
     assert lib.moe_dispatch_quantized_kernels(1, 16, 6, 385, 8) == -1
+
+
+def test_dispatch_pack_permute_rejects(lib):
+    ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
+    good = [FAKE] * 6 + [1, 64, 2, 16, 4, 256, -1, 1, 128, 128] + [FAKE] * 7 + [ws, FAKE, ST]
+    for idx, val, needle in ((11, 100, "H=100"), (12, 4, "recv_part"), (13, 0, "align"),
+                             (14, -1, "capacities"), (0, NULL, "`x`"), (16, NULL, "`send`"),
+                             (23, ws - 1, "ws_bytes")):
+        bad = list(good)
+        bad[idx] = val
+        _rejects(lib.moe_dispatch_pack_permute, bad, needle)
+    assert lib.moe_dispatch_pack_permute_kernels(1, 16, 6, 385, 8) == -1
+    assert lib.moe_dispatch_pack_permute_kernels(1, 0, 6, 384, 8) == 2
+    assert lib.moe_dispatch_pack_permute_kernels(1, 16, 6, 384, 8) == 1

@@ -10,7 +10,9 @@ edges (1, 63, 64, 65, 255, 256 tokens; E from 16 to 1024; k and P up to 32;
 8-value and ragged rows; run alignment; a receiving partition), and the
 launch counts the library reports are checked against the launch trace.
 moe_dispatch_quantized (MXFP8 and NVFP4 records) is held to the separate
-quantized pack and permute the same way, and its records to the oracle's.
+quantized pack and permute the same way, and its records to the oracle's;
+moe_dispatch_pack_permute (pack + permute for a layout already made) to
+moe_dispatch_pack followed by moe_permute_to_experts.
 """
 import numpy as np
 import pytest
@@ -298,3 +300,57 @@ def test_quantized_capacity_overflow_matches_separate(quant):
         sep, _ = _dispatch_q("separate", quant, w_, inp, 1.0, cap_send=cap_send, cap_recv=cap_recv)
         _same(fused, sep)
         assert fused["status"] & m.status_bit(m.MOE_ERR_CAPACITY)
+
+
+# ------------------------------------------- pack + permute for any layout --
+
+@pytest.mark.parametrize("S,T,H,E,k,P,recv_part,align", [
+    (1, 1000, 5120, 384, 6, 8, -1, 1), (3, 700, 520, 96, 4, 8, 1, 128), (2, 0, 256, 16, 2, 4, -1, 1),
+    (12, 64, 64, 1024, 8, 8, -1, 1)])          # S*E too large for the in-kernel map
+def test_pack_permute_equals_pack_then_permute(S, T, H, E, k, P, recv_part, align):
+    """moe_dispatch_pack_permute on a layout made by moe_dispatch_layout: every
+    output byte as moe_dispatch_pack followed by moe_permute_to_experts."""
+    w_ = ms.workload("tiny", S=S, T=T, H=H, E=E, k=k, P=P, index=S * 1000 + T)
+    inp = ms.gen_inputs(w_)
+    outs = []
+    for mode in ("one_call", "two_calls"):
+        path = m.MoePath(S, T, H, E, k, P, recv_part=recv_part, align=align, dispatch="separate")
+        path.route(f32_dev(inp["logits"]))
+        m.moe_dispatch_layout(path.topk_ids, E, P, path.expert_counts, path.expert_rank,
+                              path.part_counts, path.part_offsets, path.token_slot, path.ws,
+                              path.dev_status)
+        path.send.view(torch.int16).fill_(0x5A5A)
+        path.recv.view(torch.int16).fill_(0x3C3C)
+        for name in ("send_src", "expert_offsets", "pair_row", "recv_pair"):
+            getattr(path, name).fill_(-7)
+        x = bf16_dev(inp["x"])
+        m.trace_enable(None, 16)
+        m.trace_reset()
+        try:
+            if mode == "one_call":
+                m.moe_dispatch_pack_permute(x, path.token_slot, path.part_offsets, path.topk_ids,
+                                            path.expert_counts, path.expert_rank, E, recv_part,
+                                            align, path.send, path.send_src, path.recv,
+                                            path.expert_offsets, path.pair_row, path.recv_pair,
+                                            path.ws, path.dev_status)
+            else:
+                m.moe_dispatch_pack(x, path.token_slot, path.part_offsets, path.send,
+                                    path.send_src, path.dev_status)
+                m.moe_permute_to_experts(path.send, path.token_slot, path.topk_ids,
+                                         path.expert_counts, path.expert_rank, E, recv_part, align,
+                                         path.recv, path.expert_offsets, path.pair_row,
+                                         path.recv_pair, path.ws, path.dev_status)
+            torch.cuda.synchronize()
+            kernels = [n for n, _ in m.trace_records()]
+        finally:
+            m.trace_disable()
+        if mode == "one_call":
+            assert len(kernels) == m.moe_dispatch_pack_permute_kernels(S, T, k, E, P), kernels
+            if T > 0 and S * E <= 8 * 1024:
+                assert kernels == ["k_pack_permute"], kernels
+        outs.append({"send": bf16_host(path.send), "recv": bf16_host(path.recv),
+                     "send_src": host(path.send_src), "expert_offsets": host(path.expert_offsets),
+                     "pair_row": host(path.pair_row), "recv_pair": host(path.recv_pair),
+                     "status": int(path.dev_status.item())})
+    _same(outs[0], outs[1])
+    assert outs[0]["status"] == 0

@@ -141,7 +141,10 @@ def test_mapped_layout_flags_a_slot_outside_the_placement():
                                                ("decode", {}, "two_stage"),
                                                ("tiny", ONE_PER_PART, "single"),
                                                ("tiny", FEW_PER_PART, "two_stage")])
-def test_path_with_placement_equals_path_without(name, over, combine):
+@pytest.mark.parametrize("dispatch", ["fused", "separate"])
+def test_path_with_placement_equals_path_without(name, over, combine, dispatch):
+    """The placed path (mapped layout, then pack + permute in one call or the two
+    separate calls) against the unplaced path and the oracle."""
     w_ = ms.workload(name, **over)
     inp = ms.gen_inputs(w_)
     pl = _plan(w_, 4)
@@ -149,7 +152,8 @@ def test_path_with_placement_equals_path_without(name, over, combine):
         assert pl.copy_offsets[-1] > w_.E            # copies made: the split is exercised
     lg, xx, sc = f32_dev(inp["logits"]), bf16_dev(inp["x"]), f32_dev(inp["scales"])
     plain = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, combine=combine)
-    placed = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, combine=combine, placement=pl)
+    placed = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, combine=combine, placement=pl,
+                       dispatch=dispatch)
     out0 = bf16_host(plain.step(lg, xx, sc)).copy()
     out1 = bf16_host(placed.step(lg, xx, sc)).copy()
     torch.cuda.synchronize()
