@@ -707,7 +707,10 @@ def run_ours(args, world, rank, local):
             # launch for a decode-sized batch of bf16 rows
             if path.quantized:
                 dom_name, dom_key = f"k_pack_permute_{path.quant}", "pack_permute"
-            elif m.moe_dispatch_kernels(w.S, w.T, w.k, w.E, w.P) == 1:
+            elif path.layout == "masked":
+                dom_name, dom_key = "k_pack_permute_masked", "pack_permute"
+            elif (path.placement is None
+                  and m.moe_dispatch_kernels(w.S, w.T, w.k, w.E, w.P) == 1):
                 dom_name, dom_key = "k_dispatch_small", "dispatch"
             else:
                 dom_name, dom_key = "k_pack_permute", "pack_permute"

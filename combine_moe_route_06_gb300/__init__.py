@@ -28,7 +28,8 @@ __all__ = [
     "build", "load_library", "library_path", "moe_version", "moe_workspace_bytes",
     "moe_dispatch_layout_kernels", "moe_permute_to_experts_kernels", "moe_dispatch_kernels",
     "moe_dispatch", "moe_dispatch_quantized", "moe_dispatch_quantized_kernels",
-    "moe_dispatch_pack_permute", "moe_dispatch_pack_permute_kernels", "MOE_FORMAT_MXFP8",
+    "moe_dispatch_pack_permute", "moe_dispatch_pack_permute_kernels",
+    "moe_dispatch_pack_permute_masked", "moe_dispatch_pack_permute_masked_kernels", "MOE_FORMAT_MXFP8",
     "MOE_FORMAT_NVFP4",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
@@ -99,6 +100,11 @@ def load_library() -> ctypes.CDLL:
             "moe_dispatch_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
             "moe_dispatch_quantized_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
             "moe_dispatch_pack_permute_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
+            "moe_dispatch_pack_permute_masked_kernels": ([i32, i32, i32, i32, i32, i32],
+                                                         ctypes.c_int),
+            "moe_dispatch_pack_permute_masked": ([P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                                  i32, i32, i32, P, P, P, P, P, P, P, P],
+                                                 ctypes.c_int),
             "moe_dispatch_pack_permute": ([P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                            i32, i32, P, P, P, P, P, P, P, sz, P, P], ctypes.c_int),
             "moe_dispatch_quantized": ([P, P, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
@@ -505,6 +511,37 @@ def moe_dispatch_pack_permute_kernels(S, T, k, E, P) -> int:
     return n
 
 
+def moe_dispatch_pack_permute_masked(x, token_slot, part_offsets, topk_ids, expert_counts,
+                                     expert_rank, E, recv_part, block_rows, send, send_src, recv,
+                                     masked_counts, pair_row, recv_pair, dev_status=None,
+                                     stream=None):
+    """moe_dispatch_pack + moe_permute_to_experts_masked in one call."""
+    lib = load_library()
+    S, T, H = x.shape
+    P = token_slot.shape[2]
+    k = topk_ids.shape[2]
+    cap_send = send.shape[1]
+    _check(lib.moe_dispatch_pack_permute_masked(
+        _dev(x, "x", _BF16_TYPES, 3), _dev(token_slot, "token_slot", (torch.int32,), 3),
+        _dev(part_offsets, "part_offsets", (torch.int32,)),
+        _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)), S, T, k, E, P, H, recv_part,
+        block_rows, cap_send, _dev(send, "send", _BF16_TYPES, 3),
+        _dev(send_src, "send_src", (torch.int32,)), _dev(recv, "recv", _BF16_TYPES, 2),
+        _dev(masked_counts, "masked_counts", (torch.int32,)),
+        _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
+        _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_pack_permute_masked_kernels(S, T, k, E, P, recv_part) -> int:
+    """Kernels one moe_dispatch_pack_permute_masked call with these sizes enqueues."""
+    n = load_library().moe_dispatch_pack_permute_masked_kernels(S, T, k, E, P, recv_part)
+    if n < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_permute_masked_kernels: invalid sizes")
+    return n
+
+
 def moe_dispatch_quantized_kernels(S, T, k, E, P) -> int:
     """Kernels one moe_dispatch_quantized call with these sizes enqueues on the current device."""
     n = load_library().moe_dispatch_quantized_kernels(S, T, k, E, P)
@@ -670,12 +707,15 @@ class MoePath:
             raise ValueError("nvfp4 rows need H % 256 == 0 and the contiguous layout")
         # moe_dispatch / moe_dispatch_quantized without a placement; with one, the
         # mapped layout and then moe_dispatch_pack_permute (bf16 rows)
-        fusable = layout == "contiguous" and (placement is None or quant == "none")
+        # moe_dispatch / moe_dispatch_quantized without a placement; with one, or with
+        # the masked layout, the layout call and then one pack + permute call (bf16)
+        fusable = ((layout == "contiguous" and (placement is None or quant == "none"))
+                   or (layout == "masked" and quant == "none"))
         if dispatch is None:
             dispatch = "fused" if fusable else "separate"
         if dispatch not in ("fused", "separate") or (dispatch == "fused" and not fusable):
-            raise ValueError("dispatch must be fused|separate; fused needs the contiguous layout "
-                             "(and bf16 rows under a placement)")
+            raise ValueError("dispatch must be fused|separate; fused needs the contiguous or masked "
+                             "layout (and bf16 rows under a placement or in masked blocks)")
         self.dispatch_mode = dispatch
         self.quantized = quant != "none"
         self.nvfp4_scale = float(nvfp4_scale)
@@ -760,7 +800,8 @@ class MoePath:
         stp = vp(self.dev_status.data_ptr())
         Hp, Ep = self.Hp, self.Ep
         ids_p = vp(self.phys_ids.data_ptr())
-        if self.dispatch_mode == "fused" and self.placement is None and self.quantized:
+        one_call = self.placement is None and self.layout == "contiguous"
+        if self.dispatch_mode == "fused" and one_call and self.quantized:
             fmt = MOE_FORMAT_MXFP8 if self.quant == "mxfp8" else MOE_FORMAT_NVFP4
             calls = [(lib.moe_dispatch_quantized, (
                 ptr(logits, "logits", (torch.float32,)), ptr(x, "x", _BF16_TYPES), S, T, H, E, k, P,
@@ -774,7 +815,7 @@ class MoePath:
                 vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st))]
             return calls + self._bind_expert_q(lib, scale, stp, st) + \
                 self._bind_combine(lib, self.y, stp, st, ids_p)
-        if self.dispatch_mode == "fused" and self.placement is None:
+        if self.dispatch_mode == "fused" and one_call:
             calls = [(lib.moe_dispatch, (
                 ptr(logits, "logits", (torch.float32,)), ptr(x, "x", _BF16_TYPES), S, T, H, E, k, P,
                 self.recv_part, self.align, self.cap_send, self.cap_recv,
@@ -801,6 +842,16 @@ class MoePath:
         else:
             calls.append((lib.moe_dispatch_layout, (vp(self.topk_ids.data_ptr()), S, T, k, E, P)
                           + outs))
+        if self.dispatch_mode == "fused" and self.layout == "masked":
+            calls.append((lib.moe_dispatch_pack_permute_masked, (
+                ptr(x, "x", _BF16_TYPES), vp(self.token_slot.data_ptr()),
+                vp(self.part_offsets.data_ptr()), ids_p, vp(self.expert_counts.data_ptr()),
+                vp(self.expert_rank.data_ptr()), S, T, k, Ep, P, H, self.recv_part,
+                self.block_rows, self.cap_send, vp(self.send.data_ptr()),
+                vp(self.send_src.data_ptr()), vp(self.recv.data_ptr()),
+                vp(self.masked_counts.data_ptr()), vp(self.pair_row.data_ptr()),
+                vp(self.recv_pair.data_ptr()), stp, st)))
+            return calls + self._bind_combine(lib, self.recv, stp, st, ids_p)
         if self.dispatch_mode == "fused":
             # under a placement: pack and permute over the physical slots in one pass
             calls.append((lib.moe_dispatch_pack_permute, (
@@ -921,6 +972,13 @@ class MoePath:
             moe_dispatch_layout(self.topk_ids, self.E, self.P, self.expert_counts,
                                 self.expert_rank, self.part_counts, self.part_offsets,
                                 self.token_slot, self.ws, self.dev_status, stream)
+        if self.dispatch_mode == "fused" and self.layout == "masked":
+            moe_dispatch_pack_permute_masked(x, self.token_slot, self.part_offsets, self.phys_ids,
+                                             self.expert_counts, self.expert_rank, self.Ep,
+                                             self.recv_part, self.block_rows, self.send,
+                                             self.send_src, self.recv, self.masked_counts,
+                                             self.pair_row, self.recv_pair, self.dev_status, stream)
+            return
         if self.dispatch_mode == "fused":
             # under a placement: pack and permute over the physical slots in one pass
             moe_dispatch_pack_permute(x, self.token_slot, self.part_offsets, self.phys_ids,
@@ -1025,7 +1083,7 @@ class MoePath:
 
     def step(self, logits, x, scale=None, stream=None):
         """route -> layout -> pack -> permute -> [stand-in expert] -> combine; returns out."""
-        if self.dispatch_mode == "fused" and self.placement is None:
+        if self.dispatch_mode == "fused" and self.placement is None and self.layout == "contiguous":
             self.dispatch_fused(logits, x, stream)
         else:
             self.route(logits, stream)
@@ -1044,7 +1102,7 @@ class MoePath:
         2: map + copy), stand-in expert 1 (always with quantized rows), combine 1
         (2 when split into two stages)."""
         with_expert = with_expert or self.quantized
-        if self.dispatch_mode == "fused" and self.placement is None:
+        if self.dispatch_mode == "fused" and self.placement is None and self.layout == "contiguous":
             comb = 2 if self.combine_mode == "two_stage" else 1
             if self.T == 0:
                 comb = 0                   # the combine launches nothing for an empty batch
@@ -1060,11 +1118,14 @@ class MoePath:
                 layout += moe_dispatch_layout_kernels(self.S, self.T, self.k, self.E, 1)
         else:
             layout = moe_dispatch_layout_kernels(self.S, self.T, self.k, self.E, self.P)
-        if self.dispatch_mode == "fused":        # placement: pack and permute in one call
+        if self.dispatch_mode == "fused":        # the layout call, then pack + permute in one
             comb = (2 if self.combine_mode == "two_stage" else 1) if self.T > 0 else 0
-            return (1 + layout + moe_dispatch_pack_permute_kernels(self.S, self.T, self.k, self.Ep,
-                                                                    self.P)
-                    + comb + (1 if with_expert else 0))
+            if self.layout == "masked":
+                pp = moe_dispatch_pack_permute_masked_kernels(self.S, self.T, self.k, self.Ep,
+                                                              self.P, self.recv_part)
+            else:
+                pp = moe_dispatch_pack_permute_kernels(self.S, self.T, self.k, self.Ep, self.P)
+            return 1 + layout + pp + comb + (1 if with_expert else 0)
         if self.layout == "routed":
             if self.T == 0:                # the two receive-side calls launch nothing
                 return 1 + layout + 1

@@ -556,6 +556,100 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
     if (bad_id) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
 }
 
+// ---------------------------------------- pack + permute, masked layout --
+
+// Pack and the masked receive layout in one pass: as k_pack_permute, but the
+// receiving set's nb experts (e0 .. e0 + nb - 1) own fixed blocks of
+// block_rows rows, a pair's row is its block base + pairs of its expert in
+// earlier sources + its rank (dropped past the block), and every CTA marks a
+// share of the blocks' unused rows; CTA 0 stores the rows in use per block.
+// Shared memory: per block the rows in use, the pairs in all sources, and the
+// pairs in the sources before each s.
+__global__ void __launch_bounds__(kPPThreads) k_pack_permute_masked(
+    const int4 *__restrict__ x, const int32_t *__restrict__ token_slot,
+    const int32_t *__restrict__ part_offsets, const int32_t *__restrict__ ids,
+    const int32_t *__restrict__ expert_counts, const int32_t *__restrict__ expert_rank, int S,
+    int64_t NT, int k, int E, int L, int P, int T, int V, int e0, int nb, int block_rows,
+    int cap_send, int4 *__restrict__ send, int32_t *__restrict__ send_src,
+    int4 *__restrict__ recv, int32_t *__restrict__ masked_counts, int32_t *__restrict__ pair_row,
+    int32_t *__restrict__ recv_pair, uint32_t *dev_status)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t gwarps = gthreads >> 5;
+    const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
+    bool cap_flag = false, bad_slot = false, dropped = false, bad_rank = false, bad_id = false;
+    bool pack_overflow = false;
+
+    extern __shared__ int smm[];
+    int *bcnt = smm;             // [nb] rows of block b in use
+    int *btot = bcnt + nb;       // [nb] pairs of its expert in all sources
+    int *bsb = btot + nb;        // [S][nb] pairs of its expert in the sources before s
+    for (int bb = threadIdx.x; bb < nb; bb += blockDim.x) {
+        int run = 0;
+        for (int s2 = 0; s2 < S; s2++) {
+            bsb[s2 * nb + bb] = run;
+            run += __ldg(expert_counts + (int64_t)s2 * E + e0 + bb);
+        }
+        btot[bb] = run;
+        bcnt[bb] = min(run, block_rows);
+        if (blockIdx.x == 0) masked_counts[bb] = bcnt[bb];
+    }
+    __syncthreads();
+    // unused rows of every block
+    const int64_t rows = (int64_t)nb * block_rows;
+    for (int64_t r = gtid; r < rows; r += gthreads) {
+        const int bb = (int)(r / block_rows);
+        if (r - (int64_t)bb * block_rows >= bcnt[bb]) recv_pair[r] = -1;
+    }
+
+    const int64_t ntask = NT * nseg;
+    for (int64_t rtask = gtid >> 5; rtask < ntask; rtask += gwarps) {
+        const int64_t task = ntask - 1 - rtask;       // tokens last to first
+        const int64_t n = task / nseg;
+        const int g = (int)(task - n * nseg);
+        const int s = (int)(n / T);
+        int ts = -1, pr = -1, pp = -1;
+        if (lane < P) ts = __ldg(token_slot + n * P + lane);
+        if (lane < k) {
+            const int e = __ldg(ids + n * k + lane);
+            if (e >= E) bad_id = true;
+            if (e >= e0 && e < e0 + nb) {
+                const int bb = e - e0, r = __ldg(expert_rank + n * k + lane);
+                const int before = bsb[s * nb + bb];
+                const int own = (s + 1 < S ? bsb[(s + 1) * nb + bb] : btot[bb]) - before;
+                if (r < 0 || r >= own) bad_rank = true;          // rank inconsistent with the counts
+                else if (before + r >= block_rows) dropped = true;
+                else pr = bb * block_rows + before + r;
+            }
+            if (g == 0) {
+                const int64_t q = n * k + lane;
+                pair_row[q] = pr;
+                if (pr >= 0) recv_pair[pr] = (int32_t)q;
+            }
+            if (pr >= 0) pp = e / L;
+        }
+        if (g == 0 && lane < P) {
+            if (ts >= cap_send) pack_overflow = true;
+            else if (ts >= 0) send_src[(int64_t)s * cap_send + ts] = (int32_t)(n - (int64_t)s * T);
+        }
+        move_token_segment<kPPUnroll, kPPBatch>(x + n * V, send + (int64_t)s * cap_send * V, recv, V,
+                                                g * kPPSegVec + lane, ts, pr, pp, P, cap_send,
+                                                bad_slot, cap_flag, g == 0);
+    }
+    for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
+        const int s = (int)(i / cap_send);
+        const int rr = (int)(i - (int64_t)s * cap_send);
+        if (rr >= __ldg(part_offsets + (int64_t)s * (P + 1) + P)) send_src[i] = -1;
+    }
+    if (cap_flag || dropped || pack_overflow) flag_status(dev_status, MOE_ERR_CAPACITY);
+    if (bad_slot || bad_rank) flag_status(dev_status, MOE_ERR_INVALID_ARG);
+    if (bad_id) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
+}
+
 // ------------------------------------------- pack + permute, quantized --
 
 // 4-byte global accesses that bypass L1 (the read-back of a record piece the
@@ -983,6 +1077,64 @@ cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T
                                S, T, k, E, P, H, recv_part, align, cap_send, cap_recv, send,
                                send_src, recv, expert_offsets, pair_row, recv_pair, ws, dev_status,
                                st, true);
+}
+
+namespace {
+inline bool masked_fits(int S, int nb) { return (size_t)(2 + S) * nb * sizeof(int) <= 48 * 1024; }
+}  // namespace
+
+int pack_permute_masked_kernel_count(int S, int T, int E, int P, int recv_part)
+{
+    const int nb = recv_part < 0 ? E : E / P;
+    if (T == 0) return 2;                       // the pack, then the masked map alone
+    return masked_fits(S, nb) ? 1 : 3;          // else pack, map and copy
+}
+
+cudaError_t launch_pack_permute_masked(const uint16_t *x, const int32_t *token_slot,
+                                       const int32_t *part_offsets, const int32_t *topk_ids,
+                                       const int32_t *expert_counts, const int32_t *expert_rank,
+                                       int S, int T, int k, int E, int P, int H, int recv_part,
+                                       int block_rows, int cap_send, uint16_t *send,
+                                       int32_t *send_src, uint16_t *recv, int32_t *masked_counts,
+                                       int32_t *pair_row, int32_t *recv_pair,
+                                       uint32_t *dev_status, cudaStream_t st)
+{
+    cudaError_t e;
+    const int L = E / P;
+    const int nb = recv_part < 0 ? E : L;
+    const int e0 = recv_part < 0 ? 0 : recv_part * L;
+    if (T == 0 || !masked_fits(S, nb)) {
+        if ((e = launch_dispatch_pack(x, S, T, H, P, token_slot, part_offsets, cap_send, send,
+                                      send_src, dev_status, st)) != cudaSuccess)
+            return e;
+        return launch_permute_masked(send, token_slot, topk_ids, expert_counts, expert_rank, S, T, k,
+                                     E, P, H, recv_part, block_rows, cap_send, recv, masked_counts,
+                                     pair_row, recv_pair, dev_status, st);
+    }
+    DeviceInfo di;
+    if ((e = device_info(&di)) != cudaSuccess) return e;
+    const int64_t NT = (int64_t)S * T;
+    const int V = H / 8;
+    const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
+    const size_t smem = (size_t)(2 + S) * nb * sizeof(int);
+    const int resident = resident_grid((const void *)k_pack_permute_masked, kPPThreads, smem);
+    const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
+    int64_t blocks = div_up(NT * nseg, kPPThreads / 32);
+    const int64_t rows = (int64_t)nb * block_rows;
+    const int64_t big = rows > (int64_t)S * cap_send ? rows : (int64_t)S * cap_send;
+    const int64_t tail = div_up(big, kPPThreads);
+    const int64_t tail_blocks = tail < di.sm_count ? tail : di.sm_count;
+    if (blocks < tail_blocks) blocks = tail_blocks;
+    if (blocks > wave) blocks = wave;
+    if (blocks < 1) blocks = 1;
+    MOE_TRACED_LAUNCH("k_pack_permute_masked", st,
+                      e = launch_pdl(k_pack_permute_masked, dim3((unsigned)blocks),
+                                     dim3(kPPThreads), smem, st, (const int4 *)x, token_slot,
+                                     part_offsets, topk_ids, expert_counts, expert_rank, S, NT, k,
+                                     E, L, P, T, V, e0, nb, block_rows, cap_send, (int4 *)send,
+                                     send_src, (int4 *)recv, masked_counts, pair_row, recv_pair,
+                                     dev_status));
+    return e;
 }
 
 cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n)

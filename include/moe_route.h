@@ -15,6 +15,7 @@
  *   moe_dispatch            route + layout + pack + permute in one call,
  *                           one launch for a decode-sized batch              (section 1.4)
  *   moe_dispatch_pack_permute  pack + permute in one pass, any layout        (sections 3.2, 5.1)
+ *   moe_dispatch_pack_permute_masked  the same into the masked layout        (sections 4.1, 4.2)
  *
  * Further forms of the same round trip, each declared below with its source:
  *   moe_permute_to_experts_masked   a fixed block per expert plus a count     (sections 4.1, 4.2)
@@ -493,6 +494,27 @@ moe_status_t moe_dispatch_pack_permute(const uint16_t *x, const int32_t *token_s
                                        int32_t *recv_pair, void *ws, size_t ws_bytes,
                                        uint32_t *dev_status, cudaStream_t stream);
 int moe_dispatch_pack_permute_kernels(int S, int T, int k, int E, int P);
+
+/*
+ * Pack and the masked receive layout in one call: the outputs of
+ * moe_dispatch_pack followed by moe_permute_to_experts_masked with the same
+ * arguments, byte for byte (a2a-backends sections 4.1, 4.2), from one pass
+ * over the rows while the per-block counts of all sources fit one CTA's
+ * shared memory ((2 + S) * blocks ints <= 48 KiB), else (and for T = 0) the
+ * separate calls' kernels; moe_dispatch_pack_permute_masked_kernels reports
+ * the count (-1 for invalid sizes).  Arguments and errors as those two calls.
+ */
+moe_status_t moe_dispatch_pack_permute_masked(const uint16_t *x, const int32_t *token_slot,
+                                              const int32_t *part_offsets,
+                                              const int32_t *topk_ids,
+                                              const int32_t *expert_counts,
+                                              const int32_t *expert_rank, int S, int T, int k,
+                                              int E, int P, int H, int recv_part, int block_rows,
+                                              int cap_send, uint16_t *send, int32_t *send_src,
+                                              uint16_t *recv, int32_t *masked_counts,
+                                              int32_t *pair_row, int32_t *recv_pair,
+                                              uint32_t *dev_status, cudaStream_t stream);
+int moe_dispatch_pack_permute_masked_kernels(int S, int T, int k, int E, int P, int recv_part);
 
 /*
  * moe_dispatch with the rows sent as quantized records (a2a-backends section

@@ -107,3 +107,71 @@ def test_combine_over_masked_equals_combine_over_contiguous():
     assert np.array_equal(bf16_host(out_m), bf16_host(out_c))
     ref = oracle.combine(per["recv"], per["pair_row"], wt.astype(np.float32))
     assert close_bf16(bf16_host(out_m), ref)
+
+
+# ------------------------------------------ pack + masked layout in one call --
+
+def _pack_masked_gpu(x, lay, ids, E, recv_part, block_rows, cap_send):
+    """moe_dispatch_pack_permute_masked on the oracle's layout, outputs canary-filled."""
+    S, T, H = x.shape
+    P = lay["token_slot"].shape[2]
+    k = ids.shape[2]
+    nb = E if recv_part < 0 else E // P
+    send = bf16_dev(np.full((S, cap_send, H), FILL, np.uint16))
+    src = torch.full((S, cap_send), -7, dtype=torch.int32, device=DEV)
+    recv = bf16_dev(np.full((nb * block_rows, H), FILL, np.uint16))
+    counts = torch.full((nb,), -7, dtype=torch.int32, device=DEV)
+    pr = torch.full((S, T, k), -7, dtype=torch.int32, device=DEV)
+    rp = torch.full((nb * block_rows,), -7, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.trace_enable(None, 16)
+    m.trace_reset()
+    try:
+        m.moe_dispatch_pack_permute_masked(
+            bf16_dev(x), i32_dev(lay["token_slot"]), i32_dev(lay["part_offsets"]), i32_dev(ids),
+            i32_dev(lay["expert_counts"]), i32_dev(lay["expert_rank"]), E, recv_part, block_rows,
+            send, src, recv, counts, pr, rp, st)
+        torch.cuda.synchronize()
+        kernels = [n for n, _ in m.trace_records()]
+    finally:
+        m.trace_disable()
+    return {"send": bf16_host(send), "send_src": host(src), "recv": bf16_host(recv),
+            "masked_counts": host(counts), "pair_row": host(pr), "recv_pair": host(rp),
+            "status": int(st.item()), "kernels": kernels}
+
+
+@pytest.mark.parametrize("name,S,recv_part,block_rows", [
+    ("decode", 8, 0, 1024), ("decode", 8, 5, 1024), ("decode", 8, -1, 64), ("decode", 8, 3, 4),
+    ("prefill", None, -1, 128), ("tiny", 3, -1, 40), ("tiny", 3, 1, 200), ("tiny", 3, 2, 7),
+    ("tiny", 12, -1, 16)])
+def test_pack_permute_masked_equals_oracle(name, S, recv_part, block_rows):
+    """Pack + the masked layout in one call against the oracle's pack followed by its
+    masked permute: send rows, send_src, counts, pair rows, recv_pair and every recv row
+    (canary included) bit-exact, and the same status bits."""
+    over = {"E": 1024, "k": 8, "P": 8} if (name == "tiny" and S == 12) else {}
+    w_, inp, ids, wt, lay, send = _case(name, S=S)
+    if over:                                   # blocks of all 1,024 experts from 12 sources
+        w_ = ms.workload("tiny", S=S, **over)
+        inp = ms.gen_inputs(w_)
+        ids, wt = oracle.route_topk(inp["logits"], w_.k)
+        lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+        send, _, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], w_.T * min(w_.k, w_.P))
+    cap_send = w_.T * min(w_.k, w_.P)
+    got = _pack_masked_gpu(inp["x"], lay, ids, w_.E, recv_part, block_rows, cap_send)
+    nb = w_.E if recv_part < 0 else w_.E // w_.P
+    _, src, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap_send)
+    ref = oracle.permute_masked(send, lay["token_slot"], ids, w_.E, recv_part, block_rows,
+                                recv=np.full((nb * block_rows, w_.H), FILL, np.uint16))
+    for s in range(w_.S):
+        used = int(lay["part_offsets"][s, -1])
+        assert np.array_equal(got["send"][s, :used], send[s, :used])
+    assert np.array_equal(got["send_src"], src)
+    for key in ("masked_counts", "pair_row", "recv_pair", "recv"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert got["status"] == ref["status"]
+    if block_rows == 4:
+        assert got["status"] & CAP
+    n_expected = m.moe_dispatch_pack_permute_masked_kernels(w_.S, w_.T, w_.k, w_.E, w_.P, recv_part)
+    assert len(got["kernels"]) == n_expected, got["kernels"]
+    if (2 + w_.S) * nb * 4 <= 48 * 1024:
+        assert got["kernels"] == ["k_pack_permute_masked"]
