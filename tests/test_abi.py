@@ -256,7 +256,7 @@ def test_dispatch_pack_permute_rejects(lib):
 def test_dispatch_pack_permute_masked_rejects(lib):
     good = [FAKE] * 6 + [1, 64, 2, 16, 4, 256, -1, 64, 128] + [FAKE] * 6 + [FAKE, ST]
     for idx, val, needle in ((11, 100, "H=100"), (12, 4, "recv_part"), (13, -1, "block_rows"),
-                             (14, -1, "cap_send"), (0, NULL, "`x`"), (19, NULL, "`masked_counts`")):
+                             (14, -1, "cap_send"), (0, NULL, "`x`"), (18, NULL, "`masked_counts`")):
         bad = list(good)
         bad[idx] = val
         _rejects(lib.moe_dispatch_pack_permute_masked, bad, needle)
