@@ -627,6 +627,91 @@ def time_other_workload(m, torch, name, steps, dev, local, flush_l2, peak, varia
             "clocks": clocks}
 
 
+def time_decode_layers(m, torch, steps, dev, local, peak, variant_kw, layers=40):
+    """Decode as an engine runs it: one CUDA graph holding the round trips of
+    `layers` MoE layers (route ... combine per layer, each layer with its own
+    logits, x and buffers), replayed `steps` times (ishwarj.com a2a post, §1.4:
+    40 round trips per decode step, recorded once and replayed).  The layers'
+    inputs and outputs together are several times the L2, so each layer finds
+    its data in HBM without a flush between replays; the kernels' code stays
+    cached, as it does in a model's graph.  Returns the per-layer figures."""
+    w = ms.workload("decode")
+    lg = ms.gen_logits(w, T=w.T * layers).reshape(layers, w.S, w.T, w.E)
+    xs = ms.gen_x(w, T=w.T * layers).reshape(layers, w.S, w.T, w.H)
+    paths, bound_args = [], []
+    for i in range(layers):
+        p = m.MoePath(w.S, w.T, w.H, w.E, w.k, w.P, recv_part=w.recv_part, device=dev,
+                      **variant_kw)
+        li = torch.from_numpy(np.ascontiguousarray(lg[i])).to(dev)
+        xi = torch.from_numpy(np.ascontiguousarray(xs[i]).view(np.int16)).to(dev).view(torch.bfloat16)
+        paths.append(p)
+        bound_args.append((li, xi))
+    del lg, xs
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for p, (li, xi) in zip(paths, bound_args):
+                m.MoePath.run_bound(p.bind(li, xi, stream))
+    torch.cuda.synchronize()
+    for p in paths:
+        p.dev_status.zero_()
+    copies = pairs_recv = 0
+    for p, (li, xi) in zip(paths, bound_args):
+        m.MoePath.run_bound(p.bind(li, xi, stream))
+    torch.cuda.synchronize()
+    status = max(int(p.dev_status.item()) for p in paths)
+    b_layers = 0
+    for p in paths:
+        c = int(p.part_offsets[:, -1].sum().item())
+        pr = int((p.pair_row >= 0).sum().item())
+        copies += c
+        pairs_recv += pr
+        b_layers += algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, c, c, pr)["step"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cap = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for p, (li, xi) in zip(paths, bound_args):
+            m.MoePath.run_bound(p.bind(li, xi, cap))
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps + 3)]
+    sampler = ClockSampler(physical_gpu_index(local))
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        hold_stream(torch, steps + 3)
+        for i in range(steps + 3):
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    clocks = sampler.stop(t0, t1)
+    graph = None
+    torch.cuda.synchronize()
+    rep_ms = [e0.elapsed_time(e1) for e0, e1 in ev[3:]]
+    tot_s = sum(rep_ms) * 1e-3
+    us_layer = [1e3 * t / layers for t in rep_ms]
+    return {"workload": f"decode: S={w.S} T={w.T} H={w.H} bf16, E={w.E} top-{w.k}, "
+                        f"P={w.P} partitions, {layers} layers in one CUDA graph, "
+                        f"each layer its own inputs and buffers",
+            "layers": layers, "replays": steps,
+            "us_per_layer_mean": round(statistics.fmean(us_layer), 2),
+            "us_per_layer_median": round(statistics.median(us_layer), 2),
+            "graph_us_mean": round(1e3 * statistics.fmean(rep_ms), 2),
+            "gbs": round(b_layers * steps / tot_s / 1e9, 2),
+            "frac_of_hbm_peak": round(b_layers * steps / tot_s / 1e9 / peak, 4),
+            "rows_per_s": round(w.S * w.T * layers * steps / tot_s, 1),
+            "bytes_per_layer_mean": round(b_layers / layers),
+            "data_per_replay_over_l2": round(b_layers / l2, 2),
+            "copies_per_token": round(copies / (w.S * w.T * layers), 4),
+            "launches_per_layer": paths[0].launches_per_step(),
+            "dispatch_mode": paths[0].dispatch_mode, "dev_status": status,
+            "l2_flush": "none: the replay's data is several times the L2",
+            "clocks": clocks}
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -962,6 +1047,10 @@ def run_ours(args, world, rank, local):
                 others[name] = time_other_workload(m, torch, name, steps_o, dev, local, flush_l2,
                                                    peak_o, path_kwargs(args, ms.workload(name)))
                 torch.cuda.empty_cache()
+        if rank == 0 and args.other_workloads and args.variant == "contiguous":
+            others["decode_40_layers"] = time_decode_layers(
+                m, torch, 200, dev, local, peak_o, path_kwargs(args, ms.workload("decode")))
+            torch.cuda.empty_cache()
 
     if rank != 0:
         if dist is not None:

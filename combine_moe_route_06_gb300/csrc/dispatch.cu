@@ -56,7 +56,7 @@ constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallCluster = 8;           // CTAs that share one batch's routing
 constexpr int kSmallU = 2;                 // int4 per lane per column segment (1 KiB)
 constexpr int kSmallSegVec = 32 * kSmallU;
-constexpr int kSmallBatch = 4;             // partitions whose rows are read back together
+constexpr int kSmallBatch = 8;             // partitions whose rows are read back together
 
 // Dynamic shared memory of k_dispatch_small: ids, ranks and slots of the
 // batch, warp expert histograms and lane masks, expert counts, run starts.
@@ -191,6 +191,15 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     __shared__ int wpart[kSmallWarps][kMaxP];
     __shared__ int ptot[kMaxP], poff[kMaxP + 1];
 
+    // Ask L2 for the logits row this warp routes first.  A prefetch returns no
+    // value to the program, so it may run before the grid-dependency wait
+    // whatever the previous kernel writes (L2 is coherent for every SM); when
+    // the logits sit in HBM their fetch overlaps the wait.
+    {
+        const int tr = r + G * w;
+        if (tr < T && lane * 32 < E)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(logits + (int64_t)tr * E + lane * 32));
+    }
     // this CTA has started: the others may write into its shared memory once
     // every CTA has arrived here
     cl_arrive();
@@ -200,6 +209,19 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     }
     pdl_wait();
     pdl_trigger();
+    // this warp's first row task, (token, segment), is fixed by its index: load
+    // its x segment now so the load overlaps the routing and the layout
+    const int nseg0 = (V + kSmallSegVec - 1) / kSmallSegVec;
+    const int task0 = (int)blockIdx.x * kSmallWarps + w;
+    int4 xpre[kSmallU];
+#pragma unroll
+    for (int u = 0; u < kSmallU; u++) {
+        xpre[u] = make_int4(0, 0, 0, 0);
+        if (task0 < T * nseg0) {
+            const int t0 = task0 / nseg0, vi = (task0 - t0 * nseg0) * kSmallSegVec + lane + 32 * u;
+            if (vi < V) xpre[u] = ld_stream(x + (int64_t)t0 * V + vi);
+        }
+    }
 
     cl_wait();                                  // every CTA of the cluster has started
 
@@ -326,7 +348,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
             }
         }
         move_token_segment<kSmallU, kSmallBatch>(x + (int64_t)t * V, send, recv, V, g * kSmallSegVec + lane,
-                                    ts, pr, pp, P, cap_send, bad_slot, cap_flag, g == 0);
+                                    ts, pr, pp, P, cap_send, bad_slot, cap_flag, g == 0,
+                                    task == gw ? xpre : nullptr);
     }
 
     // 4. padding rows of the receiving runs: warp task (expert, row, segment)
