@@ -49,31 +49,34 @@ DOMINANT_BY_VARIANT = {"two_stage": ("k_combine_stage1", "stage1"),
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # dominant kernel in the prefill pipeline, from an ncu capture with the L2 left
 # as the previous kernel left it (--cache-control none), with the SHA-256 prefix
-# of the code (comments and whitespace removed, source_code_sha16) of the file
-# the kernel was built from when it was captured (k_perm_copy at commit 120a03f;
-# its file lost two helpers to common.cuh since, the kernel unchanged, and is
-# hashed as it stands now; k_pack_permute as of the commit that adds
-# moe_dispatch_pack_permute).  The line reports null instead once that file has
-# changed, so a stale capture is never quoted.
+# of the code (comments and whitespace removed, source_code_sha16) of the files
+# the kernel is built from, as they were when it was captured.  The line
+# reports null instead once one of those files has changed, so a stale capture
+# is never quoted.
 DOMINANT_TRAFFIC = {("k_perm_copy", "prefill"): {"bytes": 142.5e6 + 252.9e6,
-                                                 "source": "combine_moe_route_06_gb300/csrc/permute.cu",
+                                                 "sources": ["combine_moe_route_06_gb300/csrc/permute.cu"],
                                                  "sha16": "63c0e1b6e21e91ff"},
-                    ("k_pack_permute", "prefill"): {"bytes": 42.2e6 + 429.8e6,
-                                                    "source": "combine_moe_route_06_gb300/csrc/dispatch.cu",
-                                                    "sha16": "197467989d697c9b"}}
+                    ("k_pack_permute", "prefill"): {"bytes": 42.26e6 + 429.34e6,
+                                                    "sources": ["combine_moe_route_06_gb300/csrc/dispatch.cu",
+                                                                "combine_moe_route_06_gb300/csrc/row_move.cuh"],
+                                                    "sha16": "3dbb5dca141585ae"}}
 
 
-def source_code_sha16(path: str) -> str:
-    """SHA-256 prefix of a C/C++ source with its comments and whitespace removed,
-    so that editing a comment does not mark a capture stale."""
+def source_code_sha16(*paths: str) -> str:
+    """SHA-256 prefix of C/C++ sources (in the order given) with their comments
+    and whitespace removed, so that editing a comment does not mark a capture
+    stale."""
     import hashlib
     import re
-    with open(path) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", " ", text)
-    text = re.sub(r"\s+", " ", text).strip()
-    return hashlib.sha256(text.encode()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = re.sub(r"\s+", " ", text).strip()
+        h.update(text.encode())
+    return h.hexdigest()[:16]
 
 
 def dominant_traffic(kernel: str, workload: str):
@@ -82,7 +85,7 @@ def dominant_traffic(kernel: str, workload: str):
     if rec is None:
         return None
     try:
-        sha = source_code_sha16(os.path.join(ROOT, rec["source"]))
+        sha = source_code_sha16(*[os.path.join(ROOT, p) for p in rec["sources"]])
     except OSError:
         return None
     return rec["bytes"] if sha == rec["sha16"] else None

@@ -1,5 +1,6 @@
-// dispatch.cu -- the whole dispatch side in one call: route -> layout -> pack
-// -> receiver permute (moe_dispatch).
+// dispatch.cu -- the one-pass pack + receiver permute and the whole dispatch
+// side in one call for batches larger than one launch takes (moe_dispatch,
+// moe_dispatch_quantized, moe_dispatch_pack_permute, _masked).
 //
 // a2a-backends page (vincentzed.com/writing/a2a-backends): the router's ids
 // and weights (section 1.1), one copy per partition that holds one of the
@@ -9,378 +10,27 @@
 // moe_route_topk, moe_dispatch_layout, moe_dispatch_pack and
 // moe_permute_to_experts give one after the other.
 //
-// Section 1.4 of the page: a decode step makes ~40 such round trips, so their
-// fixed cost is launches, not bytes.  Two forms:
-//
-//   one launch (one source of at most 256 tokens, a decode step):
-//     k_dispatch_small.  Thread-block clusters of 8 CTAs; the CTAs of a
-//     cluster route a share of the tokens each and broadcast the ids into
-//     every CTA's shared memory (distributed shared memory, between two
-//     cluster barriers).  Every CTA then builds the whole layout of the batch in its
-//     own shared memory (a 256-token chunk: partition ballots, warp expert
-//     histograms) and the run starts of the receiving experts, so no CTA
-//     waits on another outside its cluster.  Finally the grid's warps move
-//     the rows, one (token, 1 KiB column segment) per task.
-//
-//   larger batches: the routing kernel, the layout (moe_dispatch_layout's
-//     kernels), then k_pack_permute: pack and permute in one pass.
-//
-// In both, a row task reads the token's segment of x once, stores it to every
-// send slot of the token, then reads back the segment of the send row of each
-// receiving partition and stores it to that partition's pair rows.  The
-// read-back is the receiver reading the row that just landed in its receive
-// region (the emulated all-to-all: partition p's region of the send buffer);
-// the warp that landed it issues the read, so it is served from L2 and the
-// send rows are not read from HBM a second time.
-#include <cooperative_groups.h>
-
+// moe_dispatch for one source of at most 256 tokens (a decode step) is one
+// launch (dispatch_small.cu).  Larger batches run the routing kernel, the
+// layout (moe_dispatch_layout's kernels), then k_pack_permute: pack and
+// permute in one pass.  A row task reads the token's segment of x once,
+// stores it to every send slot of the token, then reads back the segment of
+// the send row of each receiving partition and stores it to that partition's
+// pair rows (row_move.cuh).  The read-back is the receiver reading the row
+// that just landed in its receive region (the emulated all-to-all: partition
+// p's region of the send buffer); the warp that landed it issues the read, so
+// it is served from L2 and the send rows are not read from HBM a second time.
 #include "common.cuh"
 #include "launch.h"
 #include "quant.cuh"
-#include "route_warp.cuh"
+#include "row_move.cuh"
 #include "trace.h"
-
-namespace cg = cooperative_groups;
 
 namespace moe {
 
 namespace {
 
 inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// ------------------------------------------------------------ one launch --
-
-constexpr int kSmallMaxT = 256;            // tokens (one thread each in the layout step)
-constexpr int kSmallThreads = 256;
-constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kSmallCluster = 8;           // CTAs that share one batch's routing
-constexpr int kSmallU = 2;                 // int4 per lane per column segment (1 KiB)
-constexpr int kSmallSegVec = 32 * kSmallU;
-constexpr int kSmallBatch = 8;             // partitions whose rows are read back together
-
-// Dynamic shared memory of k_dispatch_small: ids, ranks and slots of the
-// batch, warp expert histograms and lane masks, expert counts, run starts.
-inline size_t small_smem(int T, int k, int E, int P)
-{
-    return (size_t)(2 * T * k + T * P + 2 * kSmallWarps * E + E + (E + 1)) * sizeof(int);
-}
-
-__device__ __forceinline__ void cl_arrive()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cl_wait()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Stores the row segment r (U int4 per lane, vector v0 + 32u) at dst.
-template <int U>
-__device__ __forceinline__ void store_seg(int4 *dst, const int4 *r, int v0, int V)
-{
-#pragma unroll
-    for (int u = 0; u < U; u++) {
-        const int vi = v0 + 32 * u;
-        if (vi < V) st_cg(dst + vi, r[u]);
-    }
-}
-
-// The row work of one (token, column segment) task, shared by both forms.
-//   ts    lane p < P: the token's slot in partition p (or -1)
-//   pr    lane j < k: the pair's receive row (or -1); pp its partition
-//   src   the token's row of x; send_s / recv: row bases
-// `loaded`, if given, is the segment already in registers.
-// Stores x's segment to every slot < cap_send, then, B partitions at a time,
-// reads back the send row of each partition holding pairs and stores it to
-// those pairs' rows.  A partition whose slot is missing (< 0, an inconsistent
-// layout) or past cap_send gives its pairs zero rows, as the permute does.
-template <int U, int B>
-__device__ __forceinline__ void move_token_segment(const int4 *__restrict__ src, int4 *send_s,
-                                                   int4 *recv, int V, int v0, int ts, int pr,
-                                                   int pp, int P, int cap_send, bool &bad_slot,
-                                                   bool &cap_flag, bool report,
-                                                   const int4 *loaded = nullptr)
-{
-    int4 xr[U];
-#pragma unroll
-    for (int u = 0; u < U; u++) {
-        const int vi = v0 + 32 * u;
-        xr[u] = make_int4(0, 0, 0, 0);
-        if (loaded) xr[u] = loaded[u];
-        else if (vi < V) xr[u] = ld_stream(src + vi);
-    }
-    const int lane = threadIdx.x & 31;
-    unsigned smask = __ballot_sync(kFull, lane < P && ts >= 0 && ts < cap_send);
-    while (smask) {
-        const int p = __ffs(smask) - 1;
-        smask &= smask - 1;
-        const int sl = __shfl_sync(kFull, ts, p);
-        store_seg<U>(send_s + (int64_t)sl * V, xr, v0, V);
-    }
-    unsigned rmask = __ballot_sync(kFull, pr >= 0);
-    while (rmask) {
-        int4 rb[B][U];
-        unsigned gm[B];
-#pragma unroll
-        for (int b = 0; b < B; b++) {
-            gm[b] = 0u;
-            if (rmask) {
-                const int j0 = __ffs(rmask) - 1;
-                const int p0 = __shfl_sync(kFull, pp, j0);
-                const unsigned gmask = __ballot_sync(kFull, pr >= 0 && pp == p0);
-                rmask &= ~gmask;
-                gm[b] = gmask;
-                const int sl = __shfl_sync(kFull, ts, p0);
-                const bool ok = sl >= 0 && sl < cap_send;
-                if (!ok && report && lane == 0) {
-                    if (sl < 0) bad_slot = true;
-                    else cap_flag = true;
-                }
-                const int4 *row = send_s + (int64_t)(ok ? sl : 0) * V;
-#pragma unroll
-                for (int u = 0; u < U; u++) {
-                    const int vi = v0 + 32 * u;
-                    rb[b][u] = make_int4(0, 0, 0, 0);
-                    if (ok && vi < V) rb[b][u] = ld_stream(row + vi);
-                }
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < B; b++) {
-            unsigned dm = gm[b];
-            while (dm) {
-                const int j = __ffs(dm) - 1;
-                dm &= dm - 1;
-                const int row = __shfl_sync(kFull, pr, j);
-                store_seg<U>(recv + (int64_t)row * V, rb[b], v0, V);
-            }
-        }
-    }
-}
-
-// One launch for one source of T <= 256 tokens.  grid = clusters of
-// kSmallCluster CTAs; warp w of CTA r of a cluster routes tokens r + 8w,
-// r + 8w + 64, ... and writes their ids into every CTA of the cluster; the
-// first cluster also stores ids and weights.  Needs E <= 1024 (the block
-// scan), k, P <= 32.
-template <int VPL>
-__global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
-    const float *__restrict__ logits, const int4 *__restrict__ x, int T, int E, int k, int P,
-    int V, int recv_part, int align, int cap_send, int cap_recv, int32_t *__restrict__ topk_ids,
-    float *__restrict__ topk_w, int32_t *__restrict__ expert_counts,
-    int32_t *__restrict__ expert_rank, int32_t *__restrict__ part_counts,
-    int32_t *__restrict__ part_offsets, int32_t *__restrict__ token_slot, int4 *__restrict__ send,
-    int32_t *__restrict__ send_src, int4 *__restrict__ recv, int32_t *__restrict__ expert_offsets,
-    int32_t *__restrict__ pair_row, int32_t *__restrict__ recv_pair, uint32_t *dev_status)
-{
-    cg::cluster_group cluster = cg::this_cluster();
-    const int G = (int)cluster.num_blocks();
-    const int r = (int)cluster.block_rank();
-    const bool first_cluster = (int)blockIdx.x < G;
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = E / P;
-
-    extern __shared__ __align__(16) int sm[];
-    int *ids_s = sm;                                             // [T][k]
-    int *rank_s = ids_s + T * k;                                 // [T][k]
-    int *slot_s = rank_s + T * k;                                // [T][P]
-    int *whist = slot_s + T * P;                                 // [8][E]
-    unsigned *wmask = (unsigned *)(whist + kSmallWarps * E);     // [8][E]
-    int *cnt = (int *)(wmask + kSmallWarps * E);                 // [E] pairs of expert e
-    int *off = cnt + E;                                          // [E + 1] run starts
-    __shared__ int wpart[kSmallWarps][kMaxP];
-    __shared__ int ptot[kMaxP], poff[kMaxP + 1];
-
-    // Ask L2 for the logits row this warp routes first.  A prefetch returns no
-    // value to the program, so it may run before the grid-dependency wait
-    // whatever the previous kernel writes (L2 is coherent for every SM); when
-    // the logits sit in HBM their fetch overlaps the wait.
-    {
-        const int tr = r + G * w;
-        if (tr < T && lane * 32 < E)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(logits + (int64_t)tr * E + lane * 32));
-    }
-    // this CTA has started: the others may write into its shared memory once
-    // every CTA has arrived here
-    cl_arrive();
-    for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) {
-        whist[i] = 0;
-        wmask[i] = 0u;
-    }
-    pdl_wait();
-    pdl_trigger();
-    // this warp's first row task, (token, segment), is fixed by its index: load
-    // its x segment now so the load overlaps the routing and the layout
-    const int nseg0 = (V + kSmallSegVec - 1) / kSmallSegVec;
-    const int task0 = (int)blockIdx.x * kSmallWarps + w;
-    int4 xpre[kSmallU];
-#pragma unroll
-    for (int u = 0; u < kSmallU; u++) {
-        xpre[u] = make_int4(0, 0, 0, 0);
-        if (task0 < T * nseg0) {
-            const int t0 = task0 / nseg0, vi = (task0 - t0 * nseg0) * kSmallSegVec + lane + 32 * u;
-            if (vi < V) xpre[u] = ld_stream(x + (int64_t)t0 * V + vi);
-        }
-    }
-
-    cl_wait();                                  // every CTA of the cluster has started
-
-    // 1. route this CTA's tokens (a warp per token) and write each token's ids
-    // into every CTA of the cluster.  (The loop is kept rolled: one copy of the
-    // routing code is fetched, which measured faster than unrolled copies.)
-#pragma unroll 1
-    for (int t = r + G * w; t < T; t += G * kSmallWarps) {
-        int id;
-        float wt;
-        route_token_warp<VPL>(logits + (int64_t)t * E, E, k, id, wt);
-        if (first_cluster && lane < k) {
-            topk_ids[t * k + lane] = id;
-            topk_w[t * k + lane] = wt;
-        }
-        if (lane < k)
-            for (int c = 0; c < G; c++) *cluster.map_shared_rank(ids_s + t * k + lane, c) = id;
-    }
-    cl_arrive();                                // this CTA's remote writes are done
-    cl_wait();                                  // every CTA holds every token's ids
-
-    // 2. the layout of the batch, thread per token: partition ballots give
-    // slots, warp histograms and lane masks give ranks (the ids of a token are
-    // distinct experts < E: they come from the routing above)
-    const bool valid_t = (int)threadIdx.x < T;
-    const int *my = ids_s + threadIdx.x * k;
-    unsigned mask = 0;
-    if (valid_t) {
-        for (int j = 0; j < k; j++) {
-            const int e = my[j];
-            mask |= 1u << (e / L);
-            atomicAdd(whist + w * E + e, 1);
-            atomicOr(wmask + w * E + e, 1u << lane);
-        }
-    }
-    for (int p = 0; p < P; p++) {
-        const unsigned b = __ballot_sync(kFull, (mask >> p) & 1u);
-        if (lane == 0) wpart[w][p] = __popc(b);
-    }
-    __syncthreads();
-    if ((int)threadIdx.x < P) {
-        const int p = threadIdx.x;
-        int run = 0;
-#pragma unroll
-        for (int ww = 0; ww < kSmallWarps; ww++) {
-            const int v = wpart[ww][p];
-            wpart[ww][p] = run;
-            run += v;
-        }
-        ptot[p] = run;
-    }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-#pragma unroll
-        for (int ww = 0; ww < kSmallWarps; ww++) {
-            const int v = whist[ww * E + e];
-            whist[ww * E + e] = run;
-            run += v;
-        }
-        cnt[e] = run;
-        off[e] = in_recv(e, E, L, recv_part) ? (run + align - 1) / align * align : 0;
-    }
-    __syncthreads();
-    if (w == 0) {                               // partition offsets: warp scan, P <= 32
-        const int v = (lane < P) ? ptot[lane] : 0;
-        const int inc = warp_inclusive_scan(v);
-        if (lane < P) poff[lane] = inc - v;
-        if (lane == 31) poff[P] = inc;
-    }
-    const int used = block_exclusive_scan_1024(off, E);   // synchronises the CTA
-    if (threadIdx.x == 0) off[E] = used;
-    const unsigned lt = lanemask_lt();
-    for (int p = 0; p < P; p++) {
-        const unsigned b = __ballot_sync(kFull, (mask >> p) & 1u);
-        if (valid_t)
-            slot_s[threadIdx.x * P + p] =
-                ((mask >> p) & 1u) ? poff[p] + wpart[w][p] + __popc(b & lt) : -1;
-    }
-    if (valid_t)
-        for (int j = 0; j < k; j++) {
-            const int e = my[j];
-            rank_s[threadIdx.x * k + j] = whist[w * E + e] + __popc(wmask[w * E + e] & lt);
-        }
-    __syncthreads();
-    if (blockIdx.x == 0) {
-        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-            expert_offsets[e] = off[e];
-            if (e < E) expert_counts[e] = cnt[e];
-        }
-        if ((int)threadIdx.x < P) part_counts[threadIdx.x] = ptot[threadIdx.x];
-        if ((int)threadIdx.x <= P) part_offsets[threadIdx.x] = poff[threadIdx.x];
-    }
-
-    // 3. rows: warp task (token, 1 KiB column segment) over the whole grid
-    const int gw = (int)blockIdx.x * kSmallWarps + w, nw = (int)gridDim.x * kSmallWarps;
-    const int nseg = (V + kSmallSegVec - 1) / kSmallSegVec;
-    bool cap_flag = false, bad_slot = false, dropped = false;
-    for (int task = gw; task < T * nseg; task += nw) {
-        const int t = task / nseg, g = task - (task / nseg) * nseg;
-        int ts = -1, pr = -1, pp = -1, rk = -1;
-        if (lane < P) ts = slot_s[t * P + lane];
-        if (lane < k) {
-            const int e = ids_s[t * k + lane];
-            rk = rank_s[t * k + lane];
-            if (in_recv(e, E, L, recv_part)) {
-                pr = off[e] + rk;
-                if (pr >= cap_recv) {
-                    dropped = true;
-                    pr = -1;
-                }
-            }
-            if (pr >= 0) pp = e / L;
-        }
-        if (g == 0) {
-            if (lane < P) {
-                token_slot[t * P + lane] = ts;
-                if (ts >= cap_send) cap_flag = true;
-                else if (ts >= 0) send_src[ts] = t;
-            }
-            if (lane < k) {
-                expert_rank[t * k + lane] = rk;
-                pair_row[t * k + lane] = pr;
-                if (pr >= 0) recv_pair[pr] = t * k + lane;
-            }
-        }
-        move_token_segment<kSmallU, kSmallBatch>(x + (int64_t)t * V, send, recv, V, g * kSmallSegVec + lane,
-                                    ts, pr, pp, P, cap_send, bad_slot, cap_flag, g == 0,
-                                    task == gw ? xpre : nullptr);
-    }
-
-    // 4. padding rows of the receiving runs: warp task (expert, row, segment)
-    if (align > 1) {
-        const int64_t ptask = (int64_t)E * (align - 1) * nseg;
-        for (int64_t task = gw; task < ptask; task += nw) {
-            const int g = (int)(task % nseg);
-            const int64_t ei = task / nseg;
-            const int e = (int)(ei / (align - 1));
-            const int i = (int)(ei - (int64_t)e * (align - 1));
-            const int row = off[e] + cnt[e] + i;
-            if (!in_recv(e, E, L, recv_part) || row >= off[e + 1] || row >= cap_recv) continue;
-            int4 *dst = recv + (int64_t)row * V;
-            const int v0 = g * kSmallSegVec + lane;
-#pragma unroll
-            for (int u = 0; u < kSmallU; u++) {
-                const int vi = v0 + 32 * u;
-                if (vi < V) st_cg(dst + vi, make_int4(0, 0, 0, 0));
-            }
-            if (g == 0 && lane == 0) recv_pair[row] = -1;
-        }
-    }
-    // 5. unused receive rows and send rows
-    const int gtid = (int)blockIdx.x * kSmallThreads + threadIdx.x;
-    const int gthreads = (int)gridDim.x * kSmallThreads;
-    for (int rr = off[E] + gtid; rr < cap_recv; rr += gthreads) recv_pair[rr] = -1;
-    for (int rr = poff[P] + gtid; rr < cap_send; rr += gthreads) send_src[rr] = -1;
-
-    if (cap_flag || dropped) flag_status(dev_status, MOE_ERR_CAPACITY);
-    if (bad_slot) flag_status(dev_status, MOE_ERR_INVALID_ARG);
-}
 
 // ------------------------------------------------------ pack + permute --
 
@@ -930,65 +580,6 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_q(
     if (bad_id) flag_status(dev_status, MOE_ERR_BAD_EXPERT_ID);
 }
 
-// Static shared memory of k_dispatch_small is about 1.3 KB (warp partition
-// counts, partition totals and offsets, the block scan's sums); the dynamic
-// part must leave this much of the per-CTA limit.
-constexpr size_t kSmallStaticBound = 4096;
-
-// Whether the one-launch form runs for these sizes on the current device:
-// one source of 1..256 tokens whose shared memory fits in one CTA.  (Only
-// cached device attributes are queried, so the answer is the same inside a
-// stream capture.)
-cudaError_t use_small_form(int S, int T, int k, int E, int P, bool *out)
-{
-    *out = false;
-    if (S != 1 || T < 1 || T > kSmallMaxT) return cudaSuccess;
-    DeviceInfo di;
-    cudaError_t e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    *out = small_smem(T, k, E, P) + kSmallStaticBound <= (size_t)di.max_smem_optin;
-    return cudaSuccess;
-}
-
-template <int VPL>
-cudaError_t launch_small(const float *logits, const uint16_t *x, int T, int H, int E, int k,
-                         int P, int recv_part, int align, int cap_send, int cap_recv,
-                         int32_t *topk_ids, float *topk_w, int32_t *expert_counts,
-                         int32_t *expert_rank, int32_t *part_counts, int32_t *part_offsets,
-                         int32_t *token_slot, uint16_t *send, int32_t *send_src, uint16_t *recv,
-                         int32_t *expert_offsets, int32_t *pair_row, int32_t *recv_pair,
-                         uint32_t *dev_status, cudaStream_t st)
-{
-    DeviceInfo di;
-    cudaError_t e = device_info(&di);
-    if (e != cudaSuccess) return e;
-    const size_t smem = small_smem(T, k, E, P);
-    // the 48 KB default covers static and dynamic shared memory together
-    if (smem + kSmallStaticBound > 48 * 1024) {
-        e = cudaFuncSetAttribute(k_dispatch_small<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    // clusters: enough warps for one row task each, at most what fits at once
-    const int V = H / 8;
-    const int nseg = (V + kSmallSegVec - 1) / kSmallSegVec;
-    int64_t ctas = div_up((int64_t)T * nseg, kSmallWarps);
-    const int resident = resident_grid((const void *)k_dispatch_small<VPL>, kSmallThreads, smem);
-    const int64_t cap = (resident > 0 ? resident : di.sm_count) / kSmallCluster * kSmallCluster;
-    ctas = div_up(ctas, kSmallCluster) * kSmallCluster;
-    if (ctas > cap) ctas = cap;
-    if (ctas < kSmallCluster) ctas = kSmallCluster;
-    MOE_TRACED_LAUNCH("k_dispatch_small", st,
-                      e = launch_pdl_cluster(k_dispatch_small<VPL>, dim3((unsigned)ctas),
-                                             dim3(kSmallThreads), smem, kSmallCluster, st, logits,
-                                             (const int4 *)x, T, E, k, P, V, recv_part, align,
-                                             cap_send, cap_recv, topk_ids, topk_w, expert_counts,
-                                             expert_rank, part_counts, part_offsets, token_slot,
-                                             (int4 *)send, send_src, (int4 *)recv, expert_offsets,
-                                             pair_row, recv_pair, dev_status));
-    return e;
-}
-
 }  // namespace
 
 int pack_permute_kernel_count(int S, int T, int E)
@@ -1048,7 +639,7 @@ cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
 cudaError_t dispatch_kernel_count(int S, int T, int k, int E, int P, int *n)
 {
     bool small = false;
-    cudaError_t e = use_small_form(S, T, k, E, P, &small);
+    cudaError_t e = dispatch_small_form(S, T, k, E, P, &small);
     if (e != cudaSuccess) return e;
     if (small) {
         *n = 1;
@@ -1069,27 +660,13 @@ cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T
                             int32_t *recv_pair, void *ws, uint32_t *dev_status, cudaStream_t st)
 {
     bool small = false;
-    cudaError_t e = use_small_form(S, T, k, E, P, &small);
+    cudaError_t e = dispatch_small_form(S, T, k, E, P, &small);
     if (e != cudaSuccess) return e;
-    if (small) {
-        const int vpl = (E + 31) / 32;
-#define MOE_SMALL_CASE(VV)                                                                        \
-    if (vpl <= VV)                                                                                \
-        return launch_small<VV>(logits, x, T, H, E, k, P, recv_part, align, cap_send, cap_recv,   \
-                                topk_ids, topk_w, expert_counts, expert_rank, part_counts,        \
-                                part_offsets, token_slot, send, send_src, recv, expert_offsets,   \
-                                pair_row, recv_pair, dev_status, st);
-        MOE_SMALL_CASE(1)
-        MOE_SMALL_CASE(2)
-        MOE_SMALL_CASE(4)
-        MOE_SMALL_CASE(8)
-        MOE_SMALL_CASE(12)
-        MOE_SMALL_CASE(16)
-        MOE_SMALL_CASE(24)
-        MOE_SMALL_CASE(32)
-#undef MOE_SMALL_CASE
-        return cudaErrorInvalidValue;
-    }
+    if (small)
+        return launch_dispatch_small(logits, x, T, H, E, k, P, recv_part, align, cap_send,
+                                     cap_recv, topk_ids, topk_w, expert_counts, expert_rank,
+                                     part_counts, part_offsets, token_slot, send, send_src, recv,
+                                     expert_offsets, pair_row, recv_pair, dev_status, st);
     const int64_t NT = (int64_t)S * T;
     if ((e = launch_route_topk(logits, NT, E, k, topk_ids, topk_w, st)) != cudaSuccess) return e;
     if ((e = launch_dispatch_layout(topk_ids, S, T, k, E, P, expert_counts, expert_rank,

@@ -108,6 +108,20 @@ cudaError_t launch_combine_stage2(const uint16_t *ret, const int32_t *token_slot
                                   int P, int H, int recv_part, int cap_send, uint16_t *out,
                                   uint32_t *dev_status, cudaStream_t st);
 
+// The dispatch side in one launch for one source of at most 256 tokens
+// (dispatch_small.cu): whether that form runs for these sizes on the current
+// device (cached attributes only, so the answer holds inside a stream
+// capture), and its launch.
+cudaError_t dispatch_small_form(int S, int T, int k, int E, int P, bool *out);
+cudaError_t launch_dispatch_small(const float *logits, const uint16_t *x, int T, int H, int E,
+                                  int k, int P, int recv_part, int align, int cap_send,
+                                  int cap_recv, int32_t *topk_ids, float *topk_w,
+                                  int32_t *expert_counts, int32_t *expert_rank,
+                                  int32_t *part_counts, int32_t *part_offsets,
+                                  int32_t *token_slot, uint16_t *send, int32_t *send_src,
+                                  uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
+                                  int32_t *recv_pair, uint32_t *dev_status, cudaStream_t st);
+
 // The dispatch side in one call (dispatch.cu): route, layout, pack and permute.
 cudaError_t dispatch_kernel_count(int S, int T, int k, int E, int P, int *n);
 cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T, int H, int E,
