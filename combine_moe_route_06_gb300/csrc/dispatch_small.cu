@@ -30,7 +30,7 @@ namespace {
 
 inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-constexpr int kSmallMaxT = 256;            // tokens (one thread each in the layout step)
+constexpr int kSmallMaxT = 256;            // tokens (at most 8 words of token bits per expert)
 constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallCluster = 8;           // CTAs that share one batch's routing
@@ -38,11 +38,13 @@ constexpr int kSmallU = 2;                 // int4 per lane per column segment (
 constexpr int kSmallSegVec = 32 * kSmallU;
 constexpr int kSmallBatch = 8;             // partitions whose rows are read back together
 
-// Dynamic shared memory of k_dispatch_small: ids, ranks and slots of the
-// batch, warp expert histograms and lane masks, expert counts, run starts.
+// Dynamic shared memory of k_dispatch_small: the batch's ids, one bit per
+// (token, expert) and per (token, partition) in words of 32 tokens, expert
+// counts and run starts.
 inline size_t small_smem(int T, int k, int E, int P)
 {
-    return (size_t)(2 * T * k + T * P + 2 * kSmallWarps * E + E + (E + 1)) * sizeof(int);
+    const int nw = (T + 31) / 32;
+    return (size_t)(T * k + nw * (E + P) + E + (E + 1)) * sizeof(int);
 }
 
 __device__ __forceinline__ void cl_arrive()
@@ -57,8 +59,8 @@ __device__ __forceinline__ void cl_wait()
 // One launch for one source of T <= 256 tokens.  grid = clusters of
 // kSmallCluster CTAs; warp w of CTA r of a cluster routes tokens r + 8w,
 // r + 8w + 64, ... and writes their ids into every CTA of the cluster; the
-// first cluster also stores ids and weights.  Needs E <= 1024 (the block
-// scan), k, P <= 32.
+// first cluster also stores ids and weights.  Needs E <= 1024 (four experts
+// per thread in the scan), k, P <= 32.
 template <int VPL>
 __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     const float *__restrict__ logits, const int4 *__restrict__ x, int T, int E, int k, int P,
@@ -76,16 +78,15 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = E / P;
 
+    const int NW = (T + 31) >> 5;                                // words of token bits
     extern __shared__ __align__(16) int sm[];
     int *ids_s = sm;                                             // [T][k]
-    int *rank_s = ids_s + T * k;                                 // [T][k]
-    int *slot_s = rank_s + T * k;                                // [T][P]
-    int *whist = slot_s + T * P;                                 // [8][E]
-    unsigned *wmask = (unsigned *)(whist + kSmallWarps * E);     // [8][E]
-    int *cnt = (int *)(wmask + kSmallWarps * E);                 // [E] pairs of expert e
+    unsigned *ebits = (unsigned *)(ids_s + T * k);               // [NW][E] tokens choosing e
+    unsigned *pbits = ebits + NW * E;                            // [NW][P] tokens sent to p
+    int *cnt = (int *)(pbits + NW * P);                          // [E] pairs of expert e
     int *off = cnt + E;                                          // [E + 1] run starts
-    __shared__ int wpart[kSmallWarps][kMaxP];
     __shared__ int ptot[kMaxP], poff[kMaxP + 1];
+    __shared__ int wsum[kSmallWarps];
 
     // Ask L2 for the logits row this warp routes first.  A prefetch returns no
     // value to the program, so it may run before the grid-dependency wait
@@ -99,10 +100,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     // this CTA has started: the others may write into its shared memory once
     // every CTA has arrived here
     cl_arrive();
-    for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) {
-        whist[i] = 0;
-        wmask[i] = 0u;
-    }
+    for (int i = threadIdx.x; i < NW * (E + P); i += blockDim.x) ebits[i] = 0u;
     pdl_wait();
     pdl_trigger();
     // this warp's first row task, (token, segment), is fixed by its index: load
@@ -139,68 +137,64 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     cl_arrive();                                // this CTA's remote writes are done
     cl_wait();                                  // every CTA holds every token's ids
 
-    // 2. the layout of the batch, thread per token: partition ballots give
-    // slots, warp histograms and lane masks give ranks (the ids of a token are
-    // distinct experts < E: they come from the routing above)
-    const bool valid_t = (int)threadIdx.x < T;
-    const int *my = ids_s + threadIdx.x * k;
-    unsigned mask = 0;
-    if (valid_t) {
-        for (int j = 0; j < k; j++) {
-            const int e = my[j];
-            mask |= 1u << (e / L);
-            atomicAdd(whist + w * E + e, 1);
-            atomicOr(wmask + w * E + e, 1u << lane);
-        }
-    }
-    for (int p = 0; p < P; p++) {
-        const unsigned b = __ballot_sync(kFull, (mask >> p) & 1u);
-        if (lane == 0) wpart[w][p] = __popc(b);
+    // 2. the layout of the batch.  Token t sets bit t of its experts' and its
+    // partitions' words (thread per pair; the ids of a token are distinct
+    // experts < E: they come from the routing above).  An expert's count is the
+    // popcount of its words, a partition's likewise; the rank of a pair, or a
+    // token's slot in a partition, is the popcount of the earlier tokens' bits,
+    // taken below by the warp that moves the token.
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+        const int t = i / k, e = ids_s[i];
+        const unsigned bit = 1u << (t & 31);
+        atomicOr(ebits + (t >> 5) * E + e, bit);
+        atomicOr(pbits + (t >> 5) * P + e / L, bit);
     }
     __syncthreads();
-    if ((int)threadIdx.x < P) {
-        const int p = threadIdx.x;
-        int run = 0;
+    // counts and padded run lengths, thread tid taking experts 4 tid .. 4 tid + 3
+    // (E <= 1024), then their exclusive scan: warp scans, then the warp sums
+    int v[4], local = 0;
 #pragma unroll
-        for (int ww = 0; ww < kSmallWarps; ww++) {
-            const int v = wpart[ww][p];
-            wpart[ww][p] = run;
-            run += v;
+    for (int i = 0; i < 4; i++) {
+        const int e = (int)threadIdx.x * 4 + i;
+        int c = 0;
+        if (e < E) {
+            for (int q = 0; q < NW; q++) c += __popc(ebits[q * E + e]);
+            cnt[e] = c;
         }
-        ptot[p] = run;
+        v[i] = (e < E && in_recv(e, E, L, recv_part)) ? (c + align - 1) / align * align : 0;
+        local += v[i];
     }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-#pragma unroll
-        for (int ww = 0; ww < kSmallWarps; ww++) {
-            const int v = whist[ww * E + e];
-            whist[ww * E + e] = run;
-            run += v;
+    const int inc = warp_inclusive_scan(local);
+    if (lane == 31) wsum[w] = inc;
+    if (w == kSmallWarps - 1) {                 // partition totals and offsets, P <= 32
+        int c = 0;
+        if (lane < P)
+            for (int q = 0; q < NW; q++) c += __popc(pbits[q * P + lane]);
+        const int pinc = warp_inclusive_scan(c);
+        if (lane < P) {
+            ptot[lane] = c;
+            poff[lane] = pinc - c;
         }
-        cnt[e] = run;
-        off[e] = in_recv(e, E, L, recv_part) ? (run + align - 1) / align * align : 0;
+        if (lane == 31) poff[P] = pinc;
     }
     __syncthreads();
-    if (w == 0) {                               // partition offsets: warp scan, P <= 32
-        const int v = (lane < P) ? ptot[lane] : 0;
-        const int inc = warp_inclusive_scan(v);
-        if (lane < P) poff[lane] = inc - v;
-        if (lane == 31) poff[P] = inc;
-    }
-    const int used = block_exclusive_scan_1024(off, E);   // synchronises the CTA
-    if (threadIdx.x == 0) off[E] = used;
-    const unsigned lt = lanemask_lt();
-    for (int p = 0; p < P; p++) {
-        const unsigned b = __ballot_sync(kFull, (mask >> p) & 1u);
-        if (valid_t)
-            slot_s[threadIdx.x * P + p] =
-                ((mask >> p) & 1u) ? poff[p] + wpart[w][p] + __popc(b & lt) : -1;
-    }
-    if (valid_t)
-        for (int j = 0; j < k; j++) {
-            const int e = my[j];
-            rank_s[threadIdx.x * k + j] = whist[w * E + e] + __popc(wmask[w * E + e] & lt);
+    {
+        int base = 0, used = 0;
+#pragma unroll
+        for (int q = 0; q < kSmallWarps; q++) {
+            const int sq = wsum[q];
+            base += (q < w) ? sq : 0;
+            used += sq;
         }
+        int run = base + inc - local;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int e = (int)threadIdx.x * 4 + i;
+            if (e < E) off[e] = run;
+            run += v[i];
+        }
+        if (threadIdx.x == 0) off[E] = used;
+    }
     __syncthreads();
     if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e <= E; e += blockDim.x) {
@@ -218,10 +212,19 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     for (int task = gw; task < T * nseg; task += nw) {
         const int t = task / nseg, g = task - (task / nseg) * nseg;
         int ts = -1, pr = -1, pp = -1, rk = -1;
-        if (lane < P) ts = slot_s[t * P + lane];
+        const int tq = t >> 5;
+        const unsigned tbit = 1u << (t & 31), before = tbit - 1u;
+        if (lane < P) {
+            const unsigned m = pbits[tq * P + lane];
+            if (m & tbit) {
+                ts = poff[lane] + __popc(m & before);
+                for (int q = 0; q < tq; q++) ts += __popc(pbits[q * P + lane]);
+            }
+        }
         if (lane < k) {
             const int e = ids_s[t * k + lane];
-            rk = rank_s[t * k + lane];
+            rk = __popc(ebits[tq * E + e] & before);
+            for (int q = 0; q < tq; q++) rk += __popc(ebits[q * E + e]);
             if (in_recv(e, E, L, recv_part)) {
                 pr = off[e] + rk;
                 if (pr >= cap_recv) {
@@ -278,9 +281,9 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     if (bad_slot) flag_status(dev_status, MOE_ERR_INVALID_ARG);
 }
 
-// Static shared memory of k_dispatch_small is about 1.3 KB (warp partition
-// counts, partition totals and offsets, the block scan's sums); the dynamic
-// part must leave this much of the per-CTA limit.
+// Static shared memory of k_dispatch_small is about 0.3 KB (partition totals
+// and offsets, warp sums of the scan); the dynamic part must leave this much
+// of the per-CTA limit.
 constexpr size_t kSmallStaticBound = 4096;
 
 // Whether the one-launch form runs for these sizes on the current device:
