@@ -51,6 +51,29 @@ __device__ __forceinline__ void cl_arrive()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// An arrival that orders no memory operation (the CTA only announces that it
+// has started).
+__device__ __forceinline__ void cl_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// floor(n / d) for 0 <= n < 2^16, 1 <= d < 2^16, given m = ceil(2^32 / d):
+// n m / 2^32 exceeds n / d by less than n / 2^32 < 2^-16, and the fractional
+// part of n / d is at most 1 - 1/d, so the floor is unchanged.
+__device__ __forceinline__ int div_small(int n, unsigned long long m)
+{
+    return (int)(((unsigned long long)(unsigned)n * m) >> 32);
+}
+inline unsigned long long div_small_magic(int d)
+{
+    return ((1ull << 32) + (unsigned long long)d - 1) / (unsigned long long)d;
+}
+// n / d, by div_small where the launcher passed m (its operands fit), else by division.
+__device__ __forceinline__ int div_by(int n, int d, unsigned long long m)
+{
+    return m ? div_small(n, m) : n / d;
+}
 __device__ __forceinline__ void cl_wait()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -64,7 +87,8 @@ __device__ __forceinline__ void cl_wait()
 template <int VPL>
 __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     const float *__restrict__ logits, const int4 *__restrict__ x, int T, int E, int k, int P,
-    int V, int recv_part, int align, int cap_send, int cap_recv, int32_t *__restrict__ topk_ids,
+    int V, int recv_part, int align, int cap_send, int cap_recv, unsigned long long m_k,
+    unsigned long long m_L, unsigned long long m_seg, int32_t *__restrict__ topk_ids,
     float *__restrict__ topk_w, int32_t *__restrict__ expert_counts,
     int32_t *__restrict__ expert_rank, int32_t *__restrict__ part_counts,
     int32_t *__restrict__ part_offsets, int32_t *__restrict__ token_slot, int4 *__restrict__ send,
@@ -99,7 +123,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     }
     // this CTA has started: the others may write into its shared memory once
     // every CTA has arrived here
-    cl_arrive();
+    cl_arrive_relaxed();
     for (int i = threadIdx.x; i < NW * (E + P); i += blockDim.x) ebits[i] = 0u;
     pdl_wait();
     pdl_trigger();
@@ -112,7 +136,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     for (int u = 0; u < kSmallU; u++) {
         xpre[u] = make_int4(0, 0, 0, 0);
         if (task0 < T * nseg0) {
-            const int t0 = task0 / nseg0, vi = (task0 - t0 * nseg0) * kSmallSegVec + lane + 32 * u;
+            const int t0 = div_by(task0, nseg0, m_seg), vi = (task0 - t0 * nseg0) * kSmallSegVec + lane + 32 * u;
             if (vi < V) xpre[u] = ld_stream(x + (int64_t)t0 * V + vi);
         }
     }
@@ -144,10 +168,10 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     // token's slot in a partition, is the popcount of the earlier tokens' bits,
     // taken below by the warp that moves the token.
     for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
-        const int t = i / k, e = ids_s[i];
+        const int t = div_small(i, m_k), e = ids_s[i];
         const unsigned bit = 1u << (t & 31);
         atomicOr(ebits + (t >> 5) * E + e, bit);
-        atomicOr(pbits + (t >> 5) * P + e / L, bit);
+        atomicOr(pbits + (t >> 5) * P + div_small(e, m_L), bit);
     }
     __syncthreads();
     // counts and padded run lengths, thread tid taking experts 4 tid .. 4 tid + 3
@@ -161,7 +185,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
             for (int q = 0; q < NW; q++) c += __popc(ebits[q * E + e]);
             cnt[e] = c;
         }
-        v[i] = (e < E && in_recv(e, E, L, recv_part)) ? (c + align - 1) / align * align : 0;
+        if (align > 1) c = (c + align - 1) / align * align;
+        v[i] = (e < E && in_recv(e, E, L, recv_part)) ? c : 0;
         local += v[i];
     }
     const int inc = warp_inclusive_scan(local);
@@ -210,7 +235,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     const int nseg = (V + kSmallSegVec - 1) / kSmallSegVec;
     bool cap_flag = false, bad_slot = false, dropped = false;
     for (int task = gw; task < T * nseg; task += nw) {
-        const int t = task / nseg, g = task - (task / nseg) * nseg;
+        const int t = div_by(task, nseg, m_seg), g = task - t * nseg;
         int ts = -1, pr = -1, pp = -1, rk = -1;
         const int tq = t >> 5;
         const unsigned tbit = 1u << (t & 31), before = tbit - 1u;
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
                     pr = -1;
                 }
             }
-            if (pr >= 0) pp = e / L;
+            if (pr >= 0) pp = div_small(e, m_L);
         }
         if (g == 0) {
             if (lane < P) {
@@ -329,11 +354,16 @@ cudaError_t launch_small(const float *logits, const uint16_t *x, int T, int H, i
     ctas = div_up(ctas, kSmallCluster) * kSmallCluster;
     if (ctas > cap) ctas = cap;
     if (ctas < kSmallCluster) ctas = kSmallCluster;
+    // multiply-high divisors: pair index / k (< 2^13), expert / L (< 2^10) always
+    // fit div_small; task / nseg does while T * nseg < 2^16
+    const unsigned long long m_k = div_small_magic(k), m_L = div_small_magic(E / P);
+    const unsigned long long m_seg = (int64_t)T * nseg < 65536 ? div_small_magic(nseg) : 0ull;
     MOE_TRACED_LAUNCH("k_dispatch_small", st,
                       e = launch_pdl_cluster(k_dispatch_small<VPL>, dim3((unsigned)ctas),
                                              dim3(kSmallThreads), smem, kSmallCluster, st, logits,
                                              (const int4 *)x, T, E, k, P, V, recv_part, align,
-                                             cap_send, cap_recv, topk_ids, topk_w, expert_counts,
+                                             cap_send, cap_recv, m_k, m_L, m_seg, topk_ids, topk_w,
+                                             expert_counts,
                                              expert_rank, part_counts, part_offsets, token_slot,
                                              (int4 *)send, send_src, (int4 *)recv, expert_offsets,
                                              pair_row, recv_pair, dev_status));
