@@ -72,9 +72,10 @@ __global__ void __launch_bounds__(kCombThreads) k_combine(const int4 *__restrict
     const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int nseg = (V + kCombSegVec - 1) / kCombSegVec;
     const int64_t ntask = N * nseg;
+    const bool narrow = ntask <= 0xffffffffll;  // task indices fit a 32-bit division
     for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntask;
          task += gwarps) {
-        const int64_t n = task / nseg;
+        const int64_t n = narrow ? (int64_t)((uint32_t)task / (uint32_t)nseg) : task / nseg;
         const int g = (int)(task - n * nseg);
         int pr = -1;
         float wj = 0.f;
