@@ -7,11 +7,12 @@
 // CTAs; the CTAs of a cluster route a share of the tokens each (section 1.1)
 // and broadcast the ids into every CTA's shared memory (distributed shared
 // memory, between two cluster barriers).  Every CTA then builds the whole
-// layout of the batch in its own shared memory (partition ballots give the
-// slots of sections 1.3 and 3.2, warp expert histograms the ranks, a scan the
-// receiving experts' run starts of sections 1.5 and 3.3), so no CTA waits on
-// another outside its cluster.  Finally the grid's warps move the rows, one
-// (token, 1 KiB column segment) per task (row_move.cuh).  The outputs are the
+// layout of the batch in its own shared memory (one bit per token in words
+// per expert and per partition: popcounts give the counts, the slots of
+// sections 1.3 and 3.2 and the ranks; a scan gives the receiving experts' run
+// starts of sections 1.5 and 3.3), so no CTA waits on another outside its
+// cluster.  Finally the grid's warps move the rows, one (token, 1 KiB column
+// segment) per task (row_move.cuh).  The outputs are the
 // bytes moe_route_topk, moe_dispatch_layout, moe_dispatch_pack and
 // moe_permute_to_experts give one after the other.
 #include <cooperative_groups.h>
