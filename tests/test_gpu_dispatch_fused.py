@@ -140,6 +140,11 @@ def test_one_launch_edges_in_tokens(T):
     (77, 5120, 384, 6, 8, 1, 3),      # one receiving partition
     (200, 64, 96, 3, 1, 8, 0),        # a single partition
     (33, 2048, 992, 7, 32, 4, 5),
+    # wide rows: 255 tokens x 256 segments is the largest task index the
+    # multiply-high division takes (65,279 < 2^16); 256 x 256 reaches 2^16 and
+    # takes the plain division
+    (255, 131072, 64, 2, 4, 1, -1),
+    (256, 131072, 64, 2, 4, 1, -1),
 ])
 def test_one_launch_shapes(T, H, E, k, P, align, recv_part):
     w_ = ms.workload("tiny", T=T, H=H, E=E, k=k, P=P, index=7 * T + k)
