@@ -582,6 +582,7 @@ def time_other_workload(m, torch, name, steps, dev, local, flush_l2, peak, varia
     copies = int(path.part_offsets[:, -1].sum().item())
     copies_recv = copies if w.recv_part < 0 else int(path.part_counts[:, w.recv_part].sum().item())
     pairs_recv = int((path.pair_row >= 0).sum().item())
+    per_part = path.expert_counts.sum(dim=0).cpu().numpy().reshape(w.P, -1).sum(axis=1)
     b = algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, copies, copies_recv, pairs_recv)
     cap = torch.cuda.Stream(device=dev)
     graph = torch.cuda.CUDAGraph()
@@ -625,6 +626,8 @@ def time_other_workload(m, torch, name, steps, dev, local, flush_l2, peak, varia
             "gbs": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
             "rows_per_s": round(w.S * w.T * steps / tot_s, 1), "bytes_per_step": b["step"],
             "copies_per_token": round(copies / (w.S * w.T), 4), "pairs_recv": pairs_recv,
+            "partition_load": {"pairs_max_over_mean": round(float(per_part.max() / max(per_part.mean(), 1e-9)), 4),
+                               "busiest_partition": int(per_part.argmax())},
             "launches_per_step": path.launches_per_step(), "dispatch_mode": path.dispatch_mode,
             "dev_status": status,
             "clocks": clocks}
@@ -1045,8 +1048,8 @@ def run_ours(args, world, rank, local):
         if rank == 0 and args.other_workloads and args.variant == "contiguous":
             peak_o, _ = measured_peak()
             others = {}
-            for name in [n for n in ("decode", "large", "skewed") if n != w.name]:
-                steps_o = {"decode": 500, "large": 200, "skewed": 100}[name]
+            for name in [n for n in ("decode", "large", "skewed", "skewed_perm") if n != w.name]:
+                steps_o = {"decode": 500, "large": 200, "skewed": 100, "skewed_perm": 100}[name]
                 others[name] = time_other_workload(m, torch, name, steps_o, dev, local, flush_l2,
                                                    peak_o, path_kwargs(args, ms.workload(name)))
                 torch.cuda.empty_cache()

@@ -22,7 +22,8 @@ import dataclasses
 import numpy as np
 
 __all__ = [
-    "Workload", "WORKLOADS", "workload", "normals", "bf16_bits_from_f32",
+    "Workload", "WORKLOADS", "workload", "normals", "bf16_bits_from_f32", "popularity_rank",
+    "zipf_popularity",
     "f32_from_bf16_bits", "gen_logits", "gen_x", "gen_scales", "gen_inputs",
 ]
 
@@ -30,6 +31,7 @@ _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _SEED_BASE = 0x6D6F6531  # "moe1"
+_SEED_RANK = 0x72616E6B00000000  # "rank": popularity permutations, apart from the other streams
 
 
 def _splitmix64(seed: int, start: int, n: int) -> np.ndarray:
@@ -89,7 +91,8 @@ class Workload:
     E experts, k experts per token, P partitions (emulated expert-parallel
     ranks) holding E/P contiguous experts each.  `zipf_s` > 0 biases expert
     popularity; `recv_part` is the receiving partition of the permute step
-    (-1: all partitions).
+    (-1: all partitions).  With `zipf_perm` the popularity ranks are a seeded
+    permutation of the experts instead of their ids (popularity_rank).
     """
     name: str
     index: int
@@ -101,6 +104,7 @@ class Workload:
     P: int
     zipf_s: float = 0.0
     recv_part: int = -1
+    zipf_perm: bool = False
 
     @property
     def seed_logits(self) -> int:
@@ -109,6 +113,37 @@ class Workload:
     @property
     def seed_x(self) -> int:
         return 2 * (_SEED_BASE + self.index) + 1
+
+    @property
+    def seed_rank(self) -> int:
+        return _SEED_RANK + self.index
+
+
+def popularity_rank(w: Workload) -> np.ndarray:
+    """Popularity rank of each expert (0 = most popular), int64 [E].
+
+    The experts' ids when `zipf_perm` is off; otherwise expert e's rank is its
+    place when E normal draws of stream seed_rank are sorted ascending (stable),
+    a seeded permutation.
+    """
+    if not w.zipf_perm:
+        return np.arange(w.E, dtype=np.int64)
+    order = np.argsort(normals(w.seed_rank, w.E), kind="stable")
+    rank = np.empty(w.E, dtype=np.int64)
+    rank[order] = np.arange(w.E, dtype=np.int64)
+    return rank
+
+
+def zipf_popularity(w: Workload) -> np.ndarray:
+    """p_e proportional to (rank_e + 1)^-zipf_s, summing to 1, float64 [E]."""
+    p = (popularity_rank(w) + 1.0) ** (-w.zipf_s)
+    return p / p.sum()
+
+
+def _busiest_partition(w: Workload) -> Workload:
+    """`w` receiving at the partition whose experts hold the most popularity."""
+    mass = zipf_popularity(w).reshape(w.P, w.E // w.P).sum(axis=1)
+    return dataclasses.replace(w, recv_part=int(np.argmax(mass)))
 
 
 WORKLOADS = {
@@ -122,6 +157,12 @@ WORKLOADS = {
     "skewed": Workload("skewed", 3, S=8, T=4096, H=5120, E=384, k=6, P=8, zipf_s=1.2, recv_part=0),
     # large batch: 16,384 tokens, 2,048-wide, 64 experts top-8 over 8 partitions
     "large": Workload("large", 4, S=1, T=16384, H=2048, E=64, k=8, P=8),
+    # the skewed receiver view with the popularity ranks shuffled over the
+    # experts (a seeded permutation): the hot experts spread over the
+    # partitions; the busiest one receives
+    "skewed_perm": _busiest_partition(
+        Workload("skewed_perm", 5, S=8, T=4096, H=5120, E=384, k=6, P=8, zipf_s=1.2,
+                 zipf_perm=True)),
 }
 
 
@@ -134,16 +175,16 @@ def gen_logits(w: Workload, S: int | None = None, T: int | None = None) -> np.nd
     """Router logits, float32 [S, T, E].
 
     Each logit is N(0, 1).  With zipf_s > 0 the log of a Zipf popularity is
-    added, logit[s,t,e] = z + ln p_e with p_e proportional to (e+1)^-zipf_s, so
-    expert 0 is the most popular and partition 0 the busiest receiver.
+    added, logit[s,t,e] = z + ln p_e with p_e proportional to
+    (rank_e + 1)^-zipf_s: with ranks equal to the ids expert 0 is the most
+    popular and partition 0 the busiest receiver; with permuted ranks
+    (zipf_perm) the hot experts are spread over the partitions.
     """
     S = w.S if S is None else S
     T = w.T if T is None else T
     z = normals(w.seed_logits, S * T * w.E).reshape(S, T, w.E)
     if w.zipf_s > 0:
-        p = (np.arange(1, w.E + 1, dtype=np.float64)) ** (-w.zipf_s)
-        p /= p.sum()
-        z = z + np.log(p)[None, None, :]
+        z = z + np.log(zipf_popularity(w))[None, None, :]
     return z.astype(np.float32)
 
 

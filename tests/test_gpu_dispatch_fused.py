@@ -112,14 +112,24 @@ def test_fused_equals_separate_and_oracle(name):
         assert kf[-1] == "k_pack_permute" and len(ks) > len(kf), (kf, ks)
 
 
-def test_fused_skewed_receiver_equals_separate():
-    w_ = ms.workload("skewed")
+@pytest.mark.parametrize("name", ["skewed", "skewed_perm"])
+def test_fused_skewed_receiver_equals_separate(name):
+    """The receiver view of the skewed workloads (popularity ranks equal to the
+    expert ids, or a seeded permutation of them): every output of the fused
+    call equals the separate calls'; the routing and layout equal the
+    oracle's."""
+    w_ = ms.workload(name)
     inp = ms.gen_inputs(w_)
     fused, kf, _ = _dispatch("fused", w_, inp, recv_part=w_.recv_part, trace=True)
     sep, _, _ = _dispatch("separate", w_, inp, recv_part=w_.recv_part)
     _same(fused, sep)
     assert kf[-1] == "k_pack_permute"
     assert fused["status"] == 0
+    ids, _ = oracle.route_topk(inp["logits"], w_.k)
+    assert np.array_equal(fused["topk_ids"], ids)
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    for key in ("expert_counts", "part_counts", "part_offsets", "token_slot"):
+        assert np.array_equal(fused[key], lay[key]), key
 
 
 @pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 255, 256, 257])
