@@ -149,6 +149,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
 
 
+def host_cpu() -> dict:
+    """The host's architecture, logical CPU count and CPU model as /proc/cpuinfo
+    names it (x86: `model name`; Arm: implementer and part numbers)."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            fields = {}
+            for line in f:
+                if ":" in line:
+                    k_, v_ = line.split(":", 1)
+                    fields.setdefault(k_.strip(), v_.strip())
+        if "model name" in fields:
+            model = fields["model name"]
+        elif "CPU implementer" in fields:
+            model = f"implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    except OSError:
+        pass
+    return {"machine": platform.machine(), "logical_cpus": os.cpu_count(), "model": model}
+
+
 # ------------------------------------------------------ distributed glue --
 
 def dist_env():
@@ -392,6 +413,7 @@ def run_reference(args, world, rank):
         "config": workload_config(w, "none (CPU)"),
         "rows_per_s": round(w.S * w.T * args.steps / tot, 1),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "host": host_cpu(),
                          "sample": f"{args.steps} steps of the {w.name} workload with T={w.T} of "
                                    f"{full.T} tokens per source, single thread"},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -1073,7 +1095,7 @@ def run_ours(args, world, rank, local):
     if world == 1 and not args.no_cpu_baseline:
         n, el, bb = time_oracle(ms.workload(args.workload), args.cpu_seconds, max_steps=100)
         cpu = {"value": round(bb["step"] * n / el / 1e9, 4), "unit": "GB/s", "cores": 1,
-               "kind": "oracle",
+               "kind": "oracle", "host": host_cpu(),
                "sample": f"{n} full steps of the {w.name} workload in {el:.1f} s (single thread)"}
         import platform
         try:
