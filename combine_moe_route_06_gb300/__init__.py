@@ -29,7 +29,8 @@ __all__ = [
     "moe_dispatch_layout_kernels", "moe_permute_to_experts_kernels", "moe_dispatch_kernels",
     "moe_dispatch", "moe_dispatch_quantized", "moe_dispatch_quantized_kernels",
     "moe_dispatch_pack_permute", "moe_dispatch_pack_permute_kernels",
-    "moe_dispatch_pack_permute_masked", "moe_dispatch_pack_permute_masked_kernels", "MOE_FORMAT_MXFP8",
+    "moe_dispatch_pack_permute_masked", "moe_dispatch_pack_permute_masked_kernels",
+    "moe_dispatch_masked", "moe_dispatch_masked_kernels", "MOE_FORMAT_MXFP8",
     "MOE_FORMAT_NVFP4",
     "moe_route_topk", "moe_dispatch_layout", "moe_dispatch_pack", "moe_permute_to_experts",
     "moe_combine", "moe_expert_scale", "moe_permute_to_experts_masked", "moe_combine_stage1",
@@ -102,6 +103,9 @@ def load_library() -> ctypes.CDLL:
             "moe_dispatch_pack_permute_kernels": ([i32, i32, i32, i32, i32], ctypes.c_int),
             "moe_dispatch_pack_permute_masked_kernels": ([i32, i32, i32, i32, i32, i32],
                                                          ctypes.c_int),
+            "moe_dispatch_masked_kernels": ([i32, i32, i32, i32, i32, i32], ctypes.c_int),
+            "moe_dispatch_masked": ([P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P, P, P,
+                                     P, P, P, P, P, P, P, P, P, P, sz, P, P], ctypes.c_int),
             "moe_dispatch_pack_permute_masked": ([P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                                   i32, i32, i32, P, P, P, P, P, P, P, P],
                                                  ctypes.c_int),
@@ -534,6 +538,38 @@ def moe_dispatch_pack_permute_masked(x, token_slot, part_offsets, topk_ids, expe
         _status_ptr(dev_status), _stream(stream)))
 
 
+def moe_dispatch_masked(logits, x, E, P, recv_part, block_rows, topk_ids, topk_w, expert_counts,
+                        expert_rank, part_counts, part_offsets, token_slot, send, send_src, recv,
+                        masked_counts, pair_row, recv_pair, ws, dev_status=None, stream=None):
+    """route + layout + pack + masked permute in one call (the outputs of the four
+    calls).  logits fp32 [S,T,E], x bf16 [S,T,H] in; the rest as the four calls."""
+    lib = load_library()
+    S, T, H = x.shape
+    k = topk_ids.shape[2]
+    cap_send = send.shape[1]
+    _check(lib.moe_dispatch_masked(
+        _dev(logits, "logits", (torch.float32,), 3), _dev(x, "x", _BF16_TYPES, 3), S, T, H, E, k,
+        P, recv_part, block_rows, cap_send, _dev(topk_ids, "topk_ids", (torch.int32,), 3),
+        _dev(topk_w, "topk_w", (torch.float32,), 3),
+        _dev(expert_counts, "expert_counts", (torch.int32,)),
+        _dev(expert_rank, "expert_rank", (torch.int32,)),
+        _dev(part_counts, "part_counts", (torch.int32,)),
+        _dev(part_offsets, "part_offsets", (torch.int32,)),
+        _dev(token_slot, "token_slot", (torch.int32,), 3), _dev(send, "send", _BF16_TYPES, 3),
+        _dev(send_src, "send_src", (torch.int32,)), _dev(recv, "recv", _BF16_TYPES, 2),
+        _dev(masked_counts, "masked_counts", (torch.int32,)),
+        _dev(pair_row, "pair_row", (torch.int32,)), _dev(recv_pair, "recv_pair", (torch.int32,)),
+        _dev(ws, "ws", (torch.uint8,)), ws.numel(), _status_ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_masked_kernels(S, T, k, E, P, recv_part) -> int:
+    """Kernels one moe_dispatch_masked call with these sizes enqueues on the current device."""
+    n = load_library().moe_dispatch_masked_kernels(S, T, k, E, P, recv_part)
+    if n < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_dispatch_masked_kernels: invalid sizes")
+    return n
+
+
 def moe_dispatch_pack_permute_masked_kernels(S, T, k, E, P, recv_part) -> int:
     """Kernels one moe_dispatch_pack_permute_masked call with these sizes enqueues."""
     n = load_library().moe_dispatch_pack_permute_masked_kernels(S, T, k, E, P, recv_part)
@@ -705,10 +741,8 @@ class MoePath:
             raise ValueError("mxfp8 rows need H % 512 == 0 and the contiguous layout")
         if quant == "nvfp4" and (H % 256 != 0 or layout != "contiguous"):
             raise ValueError("nvfp4 rows need H % 256 == 0 and the contiguous layout")
-        # moe_dispatch / moe_dispatch_quantized without a placement; with one, the
-        # mapped layout and then moe_dispatch_pack_permute (bf16 rows)
-        # moe_dispatch / moe_dispatch_quantized without a placement; with one, or with
-        # the masked layout, the layout call and then one pack + permute call (bf16)
+        # moe_dispatch / moe_dispatch_quantized / moe_dispatch_masked without a
+        # placement; with one, the layout call and then one pack + permute call (bf16)
         fusable = ((layout == "contiguous" and (placement is None or quant == "none"))
                    or (layout == "masked" and quant == "none"))
         if dispatch is None:
@@ -801,6 +835,17 @@ class MoePath:
         Hp, Ep = self.Hp, self.Ep
         ids_p = vp(self.phys_ids.data_ptr())
         one_call = self.placement is None and self.layout == "contiguous"
+        if self.dispatch_mode == "fused" and self.placement is None and self.layout == "masked":
+            calls = [(lib.moe_dispatch_masked, (
+                ptr(logits, "logits", (torch.float32,)), ptr(x, "x", _BF16_TYPES), S, T, H, E, k, P,
+                self.recv_part, self.block_rows, self.cap_send, vp(self.topk_ids.data_ptr()),
+                vp(self.topk_w.data_ptr()), vp(self.expert_counts.data_ptr()),
+                vp(self.expert_rank.data_ptr()), vp(self.part_counts.data_ptr()),
+                vp(self.part_offsets.data_ptr()), vp(self.token_slot.data_ptr()),
+                vp(self.send.data_ptr()), vp(self.send_src.data_ptr()), vp(self.recv.data_ptr()),
+                vp(self.masked_counts.data_ptr()), vp(self.pair_row.data_ptr()),
+                vp(self.recv_pair.data_ptr()), vp(self.ws.data_ptr()), self.ws.numel(), stp, st))]
+            return calls + self._bind_combine(lib, self.recv, stp, st, ids_p)
         if self.dispatch_mode == "fused" and one_call and self.quantized:
             fmt = MOE_FORMAT_MXFP8 if self.quant == "mxfp8" else MOE_FORMAT_NVFP4
             calls = [(lib.moe_dispatch_quantized, (
@@ -1063,8 +1108,15 @@ class MoePath:
                                recv_part=self.recv_part)
 
     def dispatch_fused(self, logits, x, stream=None):
-        """route + layout + pack + permute through one moe_dispatch (or, with
-        quantized rows, moe_dispatch_quantized) call."""
+        """route + layout + pack + permute through one moe_dispatch (with quantized
+        rows moe_dispatch_quantized, with the masked layout moe_dispatch_masked) call."""
+        if self.layout == "masked":
+            moe_dispatch_masked(logits, x, self.E, self.P, self.recv_part, self.block_rows,
+                                self.topk_ids, self.topk_w, self.expert_counts, self.expert_rank,
+                                self.part_counts, self.part_offsets, self.token_slot, self.send,
+                                self.send_src, self.recv, self.masked_counts, self.pair_row,
+                                self.recv_pair, self.ws, self.dev_status, stream)
+            return
         if self.quantized:
             moe_dispatch_quantized(logits, x, self.E, self.P,
                                    MOE_FORMAT_MXFP8 if self.quant == "mxfp8" else MOE_FORMAT_NVFP4,
@@ -1083,7 +1135,8 @@ class MoePath:
 
     def step(self, logits, x, scale=None, stream=None):
         """route -> layout -> pack -> permute -> [stand-in expert] -> combine; returns out."""
-        if self.dispatch_mode == "fused" and self.placement is None and self.layout == "contiguous":
+        if (self.dispatch_mode == "fused" and self.placement is None
+                and self.layout in ("contiguous", "masked")):
             self.dispatch_fused(logits, x, stream)
         else:
             self.route(logits, stream)
@@ -1102,6 +1155,10 @@ class MoePath:
         2: map + copy), stand-in expert 1 (always with quantized rows), combine 1
         (2 when split into two stages)."""
         with_expert = with_expert or self.quantized
+        if self.dispatch_mode == "fused" and self.placement is None and self.layout == "masked":
+            comb = (2 if self.combine_mode == "two_stage" else 1) if self.T > 0 else 0
+            return (moe_dispatch_masked_kernels(self.S, self.T, self.k, self.E, self.P,
+                                                self.recv_part) + comb + (1 if with_expert else 0))
         if self.dispatch_mode == "fused" and self.placement is None and self.layout == "contiguous":
             comb = 2 if self.combine_mode == "two_stage" else 1
             if self.T == 0:

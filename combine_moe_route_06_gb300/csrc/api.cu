@@ -476,6 +476,64 @@ moe_status_t moe_dispatch_pack_permute_masked(const uint16_t *x, const int32_t *
                        __func__);
 }
 
+int moe_dispatch_masked_kernels(int S, int T, int k, int E, int P, int recv_part)
+{
+    if (check_sizes("moe_dispatch_masked_kernels", S, T, k, E, P) != MOE_OK) return -1;
+    if (recv_part < -1 || recv_part >= P) return -1;
+    return dispatch_masked_kernel_count(S, T, k, E, P, recv_part);
+}
+
+moe_status_t moe_dispatch_masked(const float *logits, const uint16_t *x, int S, int T, int H,
+                                 int E, int k, int P, int recv_part, int block_rows,
+                                 int cap_send, int32_t *topk_ids, float *topk_w,
+                                 int32_t *expert_counts, int32_t *expert_rank,
+                                 int32_t *part_counts, int32_t *part_offsets,
+                                 int32_t *token_slot, uint16_t *send, int32_t *send_src,
+                                 uint16_t *recv, int32_t *masked_counts, int32_t *pair_row,
+                                 int32_t *recv_pair, void *ws, size_t ws_bytes,
+                                 uint32_t *dev_status, cudaStream_t stream)
+{
+    MOE_CALL_RANGE();
+    moe_status_t st = check_sizes(__func__, S, T, k, E, P);
+    if (st != MOE_OK) return st;
+    REQUIRE((int64_t)S * T * E < ((int64_t)1 << 40), "%s: S*T*E too large", __func__);
+    REQUIRE(H >= 8 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", __func__, H);
+    REQUIRE(recv_part >= -1 && recv_part < P, "%s: recv_part=%d must be in [-1, P)", __func__,
+            recv_part);
+    REQUIRE(block_rows >= 0, "%s: block_rows=%d must be >= 0", __func__, block_rows);
+    REQUIRE(cap_send >= 0, "%s: cap_send=%d must be >= 0", __func__, cap_send);
+    REQUIRE((int64_t)S * cap_send < ((int64_t)1 << 31), "%s: S*cap_send must be < 2^31", __func__);
+    const int64_t nb = recv_part < 0 ? E : E / P;
+    REQUIRE(nb * block_rows < ((int64_t)1 << 31), "%s: blocks*block_rows must be < 2^31",
+            __func__);
+    const int64_t NT = (int64_t)S * T;
+    REQUIRE_ARR(logits, NT * E, 4);
+    REQUIRE_ARR(x, NT * H, 16);
+    REQUIRE_ARR(topk_ids, NT * k, 4);
+    REQUIRE_ARR(topk_w, NT * k, 4);
+    REQUIRE_ARR(expert_counts, (int64_t)S * E, 4);
+    REQUIRE_ARR(expert_rank, NT * k, 4);
+    REQUIRE_ARR(part_counts, (int64_t)S * P, 4);
+    REQUIRE_ARR(part_offsets, (int64_t)S * (P + 1), 4);
+    REQUIRE_ARR(token_slot, NT * P, 4);
+    REQUIRE_ARR(send, (int64_t)S * cap_send * H, 16);
+    REQUIRE_ARR(send_src, (int64_t)S * cap_send, 4);
+    REQUIRE_ARR(recv, nb * block_rows * H, 16);
+    REQUIRE_ARR(masked_counts, nb, 4);
+    REQUIRE_ARR(pair_row, NT * k, 4);
+    REQUIRE_ARR(recv_pair, nb * block_rows, 4);
+    REQUIRE_STATUS(dev_status);
+    const size_t need = moe_workspace_bytes(S, T, k, E, P);
+    REQUIRE_ARR(ws, need, 256);
+    REQUIRE(ws_bytes >= need, "%s: ws_bytes=%zu < required %zu", __func__, ws_bytes, need);
+    return cuda_status(launch_dispatch_masked(logits, x, S, T, H, E, k, P, recv_part, block_rows,
+                                              cap_send, topk_ids, topk_w, expert_counts,
+                                              expert_rank, part_counts, part_offsets, token_slot,
+                                              send, send_src, recv, masked_counts, pair_row,
+                                              recv_pair, ws, dev_status, stream),
+                       __func__);
+}
+
 int moe_dispatch_quantized_kernels(int S, int T, int k, int E, int P)
 {
     if (check_sizes("moe_dispatch_quantized_kernels", S, T, k, E, P) != MOE_OK) return -1;

@@ -666,7 +666,8 @@ cudaError_t launch_dispatch(const float *logits, const uint16_t *x, int S, int T
         return launch_dispatch_small(logits, x, T, H, E, k, P, recv_part, align, cap_send,
                                      cap_recv, topk_ids, topk_w, expert_counts, expert_rank,
                                      part_counts, part_offsets, token_slot, send, send_src, recv,
-                                     expert_offsets, pair_row, recv_pair, dev_status, st);
+                                     expert_offsets, pair_row, recv_pair, dev_status, nullptr, 0,
+                                     st);
     const int64_t NT = (int64_t)S * T;
     if ((e = launch_route_topk(logits, NT, E, k, topk_ids, topk_w, st)) != cudaSuccess) return e;
     if ((e = launch_dispatch_layout(topk_ids, S, T, k, E, P, expert_counts, expert_rank,
@@ -735,6 +736,49 @@ cudaError_t launch_pack_permute_masked(const uint16_t *x, const int32_t *token_s
                                      send_src, (int4 *)recv, masked_counts, pair_row, recv_pair,
                                      dev_status));
     return e;
+}
+
+int dispatch_masked_kernel_count(int S, int T, int k, int E, int P, int recv_part)
+{
+    bool small = false;
+    if (dispatch_small_form(S, T, k, E, P, &small) != cudaSuccess) return -1;
+    if (small) return 1;
+    int nl = 1;                             // an empty batch: one layout kernel
+    if (T > 0 && layout_kernel_count(T, k, E, P, &nl) != cudaSuccess) return -1;
+    return (T > 0 ? 1 : 0) + nl + pack_permute_masked_kernel_count(S, T, E, P, recv_part);
+}
+
+cudaError_t launch_dispatch_masked(const float *logits, const uint16_t *x, int S, int T, int H,
+                                   int E, int k, int P, int recv_part, int block_rows,
+                                   int cap_send, int32_t *topk_ids, float *topk_w,
+                                   int32_t *expert_counts, int32_t *expert_rank,
+                                   int32_t *part_counts, int32_t *part_offsets,
+                                   int32_t *token_slot, uint16_t *send, int32_t *send_src,
+                                   uint16_t *recv, int32_t *masked_counts, int32_t *pair_row,
+                                   int32_t *recv_pair, void *ws, uint32_t *dev_status,
+                                   cudaStream_t st)
+{
+    bool small = false;
+    cudaError_t e = dispatch_small_form(S, T, k, E, P, &small);
+    if (e != cudaSuccess) return e;
+    if (small) {
+        const int nb = recv_part < 0 ? E : E / P;
+        return launch_dispatch_small(logits, x, T, H, E, k, P, recv_part, 1, cap_send,
+                                     nb * block_rows, topk_ids, topk_w, expert_counts,
+                                     expert_rank, part_counts, part_offsets, token_slot, send,
+                                     send_src, recv, nullptr, pair_row, recv_pair, dev_status,
+                                     masked_counts, block_rows, st);
+    }
+    const int64_t NT = (int64_t)S * T;
+    if ((e = launch_route_topk(logits, NT, E, k, topk_ids, topk_w, st)) != cudaSuccess) return e;
+    if ((e = launch_dispatch_layout(topk_ids, S, T, k, E, P, expert_counts, expert_rank,
+                                    part_counts, part_offsets, token_slot, ws, dev_status, st)) !=
+        cudaSuccess)
+        return e;
+    return launch_pack_permute_masked(x, token_slot, part_offsets, topk_ids, expert_counts,
+                                      expert_rank, S, T, k, E, P, H, recv_part, block_rows,
+                                      cap_send, send, send_src, recv, masked_counts, pair_row,
+                                      recv_pair, dev_status, st);
 }
 
 cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n)

@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     int32_t *__restrict__ expert_rank, int32_t *__restrict__ part_counts,
     int32_t *__restrict__ part_offsets, int32_t *__restrict__ token_slot, int4 *__restrict__ send,
     int32_t *__restrict__ send_src, int4 *__restrict__ recv, int32_t *__restrict__ expert_offsets,
-    int32_t *__restrict__ pair_row, int32_t *__restrict__ recv_pair, uint32_t *dev_status)
+    int32_t *__restrict__ pair_row, int32_t *__restrict__ recv_pair, uint32_t *dev_status,
+    int32_t *__restrict__ masked_counts, int block_rows)
 {
     cg::cluster_group cluster = cg::this_cluster();
     const int G = (int)cluster.num_blocks();
@@ -225,11 +226,18 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
         if (threadIdx.x == 0) off[E] = used;
     }
     __syncthreads();
+    // masked receive layout (masked_counts given): expert e0 + b of the receiving
+    // set owns rows b * block_rows .. (b + 1) * block_rows - 1
+    const bool masked = masked_counts != nullptr;
+    const int e0 = recv_part < 0 ? 0 : recv_part * L, nb = recv_part < 0 ? E : L;
     if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-            expert_offsets[e] = off[e];
+            if (!masked) expert_offsets[e] = off[e];
             if (e < E) expert_counts[e] = cnt[e];
         }
+        if (masked)
+            for (int b = threadIdx.x; b < nb; b += blockDim.x)
+                masked_counts[b] = min(cnt[e0 + b], block_rows);
         if ((int)threadIdx.x < P) part_counts[threadIdx.x] = ptot[threadIdx.x];
         if ((int)threadIdx.x <= P) part_offsets[threadIdx.x] = poff[threadIdx.x];
     }
@@ -255,10 +263,15 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
             rk = __popc(ebits[tq * E + e] & before);
             for (int q = 0; q < tq; q++) rk += __popc(ebits[q * E + e]);
             if (in_recv(e, E, L, recv_part)) {
-                pr = off[e] + rk;
-                if (pr >= cap_recv) {
-                    dropped = true;
-                    pr = -1;
+                if (masked) {
+                    if (rk < block_rows) pr = (e - e0) * block_rows + rk;
+                    else dropped = true;
+                } else {
+                    pr = off[e] + rk;
+                    if (pr >= cap_recv) {
+                        dropped = true;
+                        pr = -1;
+                    }
                 }
             }
             if (pr >= 0) pp = div_small(e, m_L);
@@ -281,7 +294,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     }
 
     // 4. padding rows of the receiving runs: warp task (expert, row, segment)
-    if (align > 1) {
+    if (align > 1 && !masked) {
         const int64_t ptask = (int64_t)E * (align - 1) * nseg;
         for (int64_t task = gw; task < ptask; task += nw) {
             const int g = (int)(task % nseg);
@@ -303,7 +316,15 @@ __global__ void __launch_bounds__(kSmallThreads) k_dispatch_small(
     // 5. unused receive rows and send rows
     const int gtid = (int)blockIdx.x * kSmallThreads + threadIdx.x;
     const int gthreads = (int)gridDim.x * kSmallThreads;
-    for (int rr = off[E] + gtid; rr < cap_recv; rr += gthreads) recv_pair[rr] = -1;
+    if (masked) {
+        const int rows = nb * block_rows;
+        for (int rr = gtid; rr < rows; rr += gthreads) {
+            const int b = rr / block_rows;
+            if (rr - b * block_rows >= min(cnt[e0 + b], block_rows)) recv_pair[rr] = -1;
+        }
+    } else {
+        for (int rr = off[E] + gtid; rr < cap_recv; rr += gthreads) recv_pair[rr] = -1;
+    }
     for (int rr = poff[P] + gtid; rr < cap_send; rr += gthreads) send_src[rr] = -1;
 
     if (cap_flag || dropped) flag_status(dev_status, MOE_ERR_CAPACITY);
@@ -337,7 +358,8 @@ cudaError_t launch_small(const float *logits, const uint16_t *x, int T, int H, i
                          int32_t *expert_rank, int32_t *part_counts, int32_t *part_offsets,
                          int32_t *token_slot, uint16_t *send, int32_t *send_src, uint16_t *recv,
                          int32_t *expert_offsets, int32_t *pair_row, int32_t *recv_pair,
-                         uint32_t *dev_status, cudaStream_t st)
+                         uint32_t *dev_status, int32_t *masked_counts, int block_rows,
+                         cudaStream_t st)
 {
     DeviceInfo di;
     cudaError_t e = device_info(&di);
@@ -372,7 +394,8 @@ cudaError_t launch_small(const float *logits, const uint16_t *x, int T, int H, i
                                              expert_counts,
                                              expert_rank, part_counts, part_offsets, token_slot,
                                              (int4 *)send, send_src, (int4 *)recv, expert_offsets,
-                                             pair_row, recv_pair, dev_status));
+                                             pair_row, recv_pair, dev_status, masked_counts,
+                                             block_rows));
     return e;
 }
 
@@ -390,7 +413,8 @@ cudaError_t launch_dispatch_small(const float *logits, const uint16_t *x, int T,
                                   int32_t *part_counts, int32_t *part_offsets,
                                   int32_t *token_slot, uint16_t *send, int32_t *send_src,
                                   uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
-                                  int32_t *recv_pair, uint32_t *dev_status, cudaStream_t st)
+                                  int32_t *recv_pair, uint32_t *dev_status,
+                                  int32_t *masked_counts, int block_rows, cudaStream_t st)
 {
     // logits per lane of the routing warp, rounded up to an instantiated width
     const int vpl = (E + 31) / 32;
@@ -399,7 +423,7 @@ cudaError_t launch_dispatch_small(const float *logits, const uint16_t *x, int T,
         return launch_small<VV>(logits, x, T, H, E, k, P, recv_part, align, cap_send, cap_recv,   \
                                 topk_ids, topk_w, expert_counts, expert_rank, part_counts,        \
                                 part_offsets, token_slot, send, send_src, recv, expert_offsets,   \
-                                pair_row, recv_pair, dev_status, st);
+                                pair_row, recv_pair, dev_status, masked_counts, block_rows, st);
     MOE_SMALL_CASE(1)
     MOE_SMALL_CASE(2)
     MOE_SMALL_CASE(4)

@@ -111,7 +111,9 @@ cudaError_t launch_combine_stage2(const uint16_t *ret, const int32_t *token_slot
 // The dispatch side in one launch for one source of at most 256 tokens
 // (dispatch_small.cu): whether that form runs for these sizes on the current
 // device (cached attributes only, so the answer holds inside a stream
-// capture), and its launch.
+// capture), and its launch.  With masked_counts (non-null) the receive rows
+// take the masked layout (block_rows rows per receiving expert; expert_offsets
+// and align unused), else the contiguous runs.
 cudaError_t dispatch_small_form(int S, int T, int k, int E, int P, bool *out);
 cudaError_t launch_dispatch_small(const float *logits, const uint16_t *x, int T, int H, int E,
                                   int k, int P, int recv_part, int align, int cap_send,
@@ -120,7 +122,22 @@ cudaError_t launch_dispatch_small(const float *logits, const uint16_t *x, int T,
                                   int32_t *part_counts, int32_t *part_offsets,
                                   int32_t *token_slot, uint16_t *send, int32_t *send_src,
                                   uint16_t *recv, int32_t *expert_offsets, int32_t *pair_row,
-                                  int32_t *recv_pair, uint32_t *dev_status, cudaStream_t st);
+                                  int32_t *recv_pair, uint32_t *dev_status,
+                                  int32_t *masked_counts, int block_rows, cudaStream_t st);
+
+// The dispatch side in one call with the masked receive layout (dispatch.cu):
+// one launch for one source of at most 256 tokens, else route, layout and the
+// masked pack + permute.
+int dispatch_masked_kernel_count(int S, int T, int k, int E, int P, int recv_part);
+cudaError_t launch_dispatch_masked(const float *logits, const uint16_t *x, int S, int T, int H,
+                                   int E, int k, int P, int recv_part, int block_rows,
+                                   int cap_send, int32_t *topk_ids, float *topk_w,
+                                   int32_t *expert_counts, int32_t *expert_rank,
+                                   int32_t *part_counts, int32_t *part_offsets,
+                                   int32_t *token_slot, uint16_t *send, int32_t *send_src,
+                                   uint16_t *recv, int32_t *masked_counts, int32_t *pair_row,
+                                   int32_t *recv_pair, void *ws, uint32_t *dev_status,
+                                   cudaStream_t st);
 
 // The dispatch side in one call (dispatch.cu): route, layout, pack and permute.
 cudaError_t dispatch_kernel_count(int S, int T, int k, int E, int P, int *n);

@@ -16,6 +16,8 @@
  *                           one launch for a decode-sized batch              (section 1.4)
  *   moe_dispatch_pack_permute  pack + permute in one pass, any layout        (sections 3.2, 5.1)
  *   moe_dispatch_pack_permute_masked  the same into the masked layout        (sections 4.1, 4.2)
+ *   moe_dispatch_masked     moe_dispatch into the masked layout, one launch
+ *                           for a decode-sized batch                       (sections 1.4, 4.1, 4.2)
  *
  * Further forms of the same round trip, each declared below with its source:
  *   moe_permute_to_experts_masked   a fixed block per expert plus a count     (sections 4.1, 4.2)
@@ -515,6 +517,38 @@ moe_status_t moe_dispatch_pack_permute_masked(const uint16_t *x, const int32_t *
                                               int32_t *pair_row, int32_t *recv_pair,
                                               uint32_t *dev_status, cudaStream_t stream);
 int moe_dispatch_pack_permute_masked_kernels(int S, int T, int k, int E, int P, int recv_part);
+
+/*
+ * The dispatch side in one call with the masked receive layout: the outputs of
+ * moe_route_topk, moe_dispatch_layout, moe_dispatch_pack and
+ * moe_permute_to_experts_masked on the same arguments, byte for byte
+ * (a2a-backends sections 4.1, 4.2: the layout a decode step records in a CUDA
+ * graph, fixed blocks per expert and a count per block; section 1.4 for the
+ * launch count).
+ *   logits [S][T][E] fp32 in; x [S][T][H] bf16 in.
+ *   topk_ids, topk_w                   out, as moe_route_topk.
+ *   expert_counts, expert_rank, part_counts, part_offsets, token_slot
+ *                                      out, as moe_dispatch_layout.
+ *   send, send_src, cap_send           as moe_dispatch_pack.
+ *   recv, masked_counts, pair_row, recv_pair, recv_part, block_rows
+ *                                      as moe_permute_to_experts_masked.
+ *   ws, ws_bytes  scratch, ws_bytes >= moe_workspace_bytes(S, T, k, E, P).
+ * Forms (moe_dispatch_masked_kernels reports the launch count, -1 for invalid
+ * sizes): one source of 1..256 tokens, one kernel (as moe_dispatch's one-launch
+ * form, each pair placed in its expert's block); otherwise the routing kernel,
+ * the layout's kernel(s) and moe_dispatch_pack_permute_masked's kernel(s).
+ * Errors: those of the four calls.  Routing never produces an id < 0 or >= E.
+ */
+moe_status_t moe_dispatch_masked(const float *logits, const uint16_t *x, int S, int T, int H,
+                                 int E, int k, int P, int recv_part, int block_rows,
+                                 int cap_send, int32_t *topk_ids, float *topk_w,
+                                 int32_t *expert_counts, int32_t *expert_rank,
+                                 int32_t *part_counts, int32_t *part_offsets,
+                                 int32_t *token_slot, uint16_t *send, int32_t *send_src,
+                                 uint16_t *recv, int32_t *masked_counts, int32_t *pair_row,
+                                 int32_t *recv_pair, void *ws, size_t ws_bytes,
+                                 uint32_t *dev_status, cudaStream_t stream);
+int moe_dispatch_masked_kernels(int S, int T, int k, int E, int P, int recv_part);
 
 /*
  * moe_dispatch with the rows sent as quantized records (a2a-backends section

@@ -264,3 +264,20 @@ def test_dispatch_pack_permute_masked_rejects(lib):
     assert lib.moe_dispatch_pack_permute_masked_kernels(1, 0, 6, 384, 8, -1) == 2
     assert lib.moe_dispatch_pack_permute_masked_kernels(1, 16, 6, 384, 8, -1) == 1
     assert lib.moe_dispatch_pack_permute_masked_kernels(12, 16, 8, 1024, 8, -1) == 3
+
+
+def test_dispatch_masked_rejects(lib):
+    """moe_dispatch_masked checks moe_dispatch's arguments with the masked layout's
+    block_rows and masked_counts in place of align, cap_recv and expert_offsets."""
+    ws = m.moe_workspace_bytes(1, 64, 2, 16, 4)
+    good = [FAKE, FAKE, 1, 64, 256, 16, 2, 4, -1, 64, 128] + [FAKE] * 13 + [FAKE, ws, FAKE, ST]
+    for idx, val, needle in ((4, 100, "H=100"), (8, 4, "recv_part"), (9, -1, "block_rows"),
+                             (10, -1, "cap_send"), (7, 3, "multiple of P"), (0, NULL, "`logits`"),
+                             (18, NULL, "`send`"), (21, NULL, "`masked_counts`"),
+                             (25, ws - 1, "ws_bytes")):
+        bad = list(good)
+        bad[idx] = val
+        _rejects(lib.moe_dispatch_masked, bad, needle)
+    assert lib.moe_dispatch_masked_kernels(1, 16, 6, 384, 8, 8) == -1      # recv_part
+    assert lib.moe_dispatch_masked_kernels(1, 16, 6, 385, 8, -1) == -1     # E % P != 0
+    assert lib.moe_dispatch_masked_kernels(1, -1, 6, 384, 8, -1) == -1     # T < 0

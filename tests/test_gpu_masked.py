@@ -175,3 +175,105 @@ def test_pack_permute_masked_equals_oracle(name, S, recv_part, block_rows):
     assert len(got["kernels"]) == n_expected, got["kernels"]
     if (2 + w_.S) * nb * 4 <= 48 * 1024:
         assert got["kernels"] == ["k_pack_permute_masked"]
+
+
+# ------------------------- route + layout + pack + masked layout in one call --
+
+def _dispatch_masked_gpu(w_, inp, recv_part, block_rows):
+    """moe_dispatch_masked from the logits, every output canary-filled first."""
+    S, T, H, E, k, P = w_.S, w_.T, w_.H, w_.E, w_.k, w_.P
+    nb = E if recv_part < 0 else E // P
+    cap_send = T * min(k, P)
+    i32 = lambda *shape: torch.full(shape, -7, dtype=torch.int32, device=DEV)  # noqa: E731
+    o = {"topk_ids": i32(S, T, k), "expert_counts": i32(S, E), "expert_rank": i32(S, T, k),
+         "part_counts": i32(S, P), "part_offsets": i32(S, P + 1), "token_slot": i32(S, T, P),
+         "send_src": i32(S, cap_send), "masked_counts": i32(nb), "pair_row": i32(S, T, k),
+         "recv_pair": i32(nb * block_rows)}
+    topk_w = torch.full((S, T, k), -9.0, dtype=torch.float32, device=DEV)
+    send = bf16_dev(np.full((S, cap_send, H), FILL, np.uint16))
+    recv = bf16_dev(np.full((nb * block_rows, H), FILL, np.uint16))
+    ws = torch.empty(max(m.moe_workspace_bytes(S, T, k, E, P), 256), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    logits = torch.from_numpy(np.ascontiguousarray(inp["logits"])).to(DEV)
+    m.trace_enable(None, 16)
+    m.trace_reset()
+    try:
+        m.moe_dispatch_masked(logits, bf16_dev(inp["x"]), E, P, recv_part, block_rows,
+                              o["topk_ids"], topk_w, o["expert_counts"], o["expert_rank"],
+                              o["part_counts"], o["part_offsets"], o["token_slot"], send,
+                              o["send_src"], recv, o["masked_counts"], o["pair_row"],
+                              o["recv_pair"], ws, st)
+        torch.cuda.synchronize()
+        kernels = [n for n, _ in m.trace_records()]
+    finally:
+        m.trace_disable()
+    got = {key: host(v) for key, v in o.items()}
+    got.update({"topk_w": host(topk_w), "send": bf16_host(send), "recv": bf16_host(recv),
+                "status": int(st.item()), "kernels": kernels})
+    return got
+
+
+@pytest.mark.parametrize("name,over,recv_part,block_rows", [
+    ("decode", {}, -1, 64),
+    ("decode", {}, 3, 1024),
+    ("decode", {}, -1, 1),                                  # most pairs dropped
+    ("decode", {"T": 1}, 6, 8),
+    ("decode", {"T": 255}, 5, 16),
+    ("decode", {"T": 256}, -1, 4),
+    ("decode", {"T": 257}, -1, 64),                         # past the one-launch form
+    ("tiny", {"T": 100, "E": 1024, "k": 32, "P": 32}, 7, 8),
+    ("tiny", {"S": 3}, 1, 200),
+    ("prefill", {}, -1, 128),
+])
+def test_dispatch_masked_equals_oracle(name, over, recv_part, block_rows):
+    """moe_dispatch_masked against the oracle's route, layout, pack and masked
+    permute: ids and layout bit-exact, weights within 2e-6, send rows, send_src,
+    counts, pair rows, recv_pair and every recv row (canary included) bit-exact,
+    the same status bits; one kernel for one source of at most 256 tokens."""
+    w_ = ms.workload(name, index=500 + len(over) + block_rows, **over)
+    inp = ms.gen_inputs(w_)
+    got = _dispatch_masked_gpu(w_, inp, recv_part, block_rows)
+    ids, wt = oracle.route_topk(inp["logits"], w_.k)
+    assert np.array_equal(got["topk_ids"], ids)
+    assert np.max(np.abs(got["topk_w"] - wt)) <= 2e-6
+    lay = oracle.dispatch_layout(ids, w_.E, w_.P)
+    for key in ("expert_counts", "expert_rank", "part_counts", "part_offsets", "token_slot"):
+        assert np.array_equal(got[key], lay[key]), key
+    cap_send = w_.T * min(w_.k, w_.P)
+    send, src, _ = oracle.dispatch_pack(inp["x"], lay["token_slot"], cap_send)
+    for s in range(w_.S):
+        used = int(lay["part_offsets"][s, -1])
+        assert np.array_equal(got["send"][s, :used], send[s, :used])
+    assert np.array_equal(got["send_src"], src)
+    nb = w_.E if recv_part < 0 else w_.E // w_.P
+    ref = oracle.permute_masked(send, lay["token_slot"], ids, w_.E, recv_part, block_rows,
+                                recv=np.full((nb * block_rows, w_.H), FILL, np.uint16))
+    for key in ("masked_counts", "pair_row", "recv_pair", "recv"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert got["status"] == ref["status"]
+    n = m.moe_dispatch_masked_kernels(w_.S, w_.T, w_.k, w_.E, w_.P, recv_part)
+    assert len(got["kernels"]) == n, got["kernels"]
+    assert (got["kernels"] == ["k_dispatch_small"]) == (w_.S == 1 and w_.T <= 256), got["kernels"]
+
+
+def test_masked_path_one_call_equals_separate():
+    """MoePath with the masked layout: the fused step (moe_dispatch_masked, then the
+    combine) leaves every output as the separate calls do, in two launches at decode."""
+    w_ = ms.workload("decode", index=77)
+    inp = ms.gen_inputs(w_)
+    outs = {}
+    for mode in ("fused", "separate"):
+        path = m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, layout="masked", block_rows=64,
+                         dispatch=mode)
+        path.recv.view(torch.int16).fill_(FILL)
+        path.recv_pair.fill_(-7)
+        out = path.step(torch.from_numpy(inp["logits"]).to(DEV), bf16_dev(inp["x"]))
+        torch.cuda.synchronize()
+        outs[mode] = {"out": bf16_host(out), "recv": bf16_host(path.recv),
+                      "pair_row": host(path.pair_row), "recv_pair": host(path.recv_pair),
+                      "masked_counts": host(path.masked_counts),
+                      "status": int(path.dev_status.item()),
+                      "launches": path.launches_per_step()}
+    for key in ("out", "recv", "pair_row", "recv_pair", "masked_counts", "status"):
+        assert np.array_equal(outs["fused"][key], outs["separate"][key]), key
+    assert outs["fused"]["launches"] == 2
