@@ -125,6 +125,18 @@ cudaError_t launch_dispatch_small(const float *logits, const uint16_t *x, int T,
                                   int32_t *recv_pair, uint32_t *dev_status,
                                   int32_t *masked_counts, int block_rows, cudaStream_t st);
 
+// The quantized dispatch side in one launch for one source of at most 256
+// tokens (dispatch_small_q.cu; format 1: MXFP8 records, 2: NVFP4, g the NVFP4
+// tensor scale); the form runs where dispatch_small_form says so.
+cudaError_t launch_dispatch_small_q(const float *logits, const uint16_t *x, int T, int H, int E,
+                                    int k, int P, int format, float g, int recv_part, int align,
+                                    int cap_send, int cap_recv, int32_t *topk_ids, float *topk_w,
+                                    int32_t *expert_counts, int32_t *expert_rank,
+                                    int32_t *part_counts, int32_t *part_offsets,
+                                    int32_t *token_slot, uint8_t *send_q, int32_t *send_src,
+                                    uint8_t *recv_q, int32_t *expert_offsets, int32_t *pair_row,
+                                    int32_t *recv_pair, uint32_t *dev_status, cudaStream_t st);
+
 // The dispatch side in one call with the masked receive layout (dispatch.cu):
 // one launch for one source of at most 256 tokens, else route, layout and the
 // masked pack + permute.

@@ -561,12 +561,14 @@ int moe_dispatch_masked_kernels(int S, int T, int k, int E, int P, int recv_part
  *           16-byte aligned; rb = H + H/32 (MXFP8) or H/2 + H/16 (NVFP4).
  *   The other arguments and the errors are those of moe_dispatch (plus a bad
  *   format, H or global_scale: MOE_ERR_INVALID_ARG).
- * Kernels: the routing kernel, the layout's kernel(s), then one pass that
- * quantizes each row segment once, stores the piece to the token's send
- * records, reads each receiving partition's piece back and stores it to the
- * pair records (the separate pack and permute for T = 0 or when the S*E
- * counts do not fit one CTA's shared memory); moe_dispatch_quantized_kernels
- * reports the count (-1 for invalid sizes).
+ * Kernels: for one source of 1..256 tokens one kernel (as moe_dispatch's
+ * one-launch form, each row segment quantized once); otherwise the routing
+ * kernel, the layout's kernel(s), then one pass that quantizes each row
+ * segment once, stores the piece to the token's send records, reads each
+ * receiving partition's piece back and stores it to the pair records (the
+ * separate pack and permute for T = 0 or when the S*E counts do not fit one
+ * CTA's shared memory); moe_dispatch_quantized_kernels reports the count (-1
+ * for invalid sizes).
  */
 moe_status_t moe_dispatch_quantized(const float *logits, const uint16_t *x, int S, int T, int H,
                                     int E, int k, int P, int format, float global_scale,

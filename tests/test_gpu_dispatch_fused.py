@@ -283,14 +283,20 @@ def _q_oracle(quant, w_, inp, g=1.0, recv_part=-1, align=1):
 @pytest.mark.parametrize("quant,g", [("mxfp8", 1.0), ("nvfp4", 1.0), ("nvfp4", 0.02)])
 @pytest.mark.parametrize("name,over,recv_part,align", [
     ("decode", {}, -1, 1), ("prefill", {}, -1, 1), ("large", {}, -1, 1),
-    ("tiny", {"S": 2, "T": 300, "H": 512, "E": 64, "k": 8, "P": 8}, 2, 8)])
+    ("tiny", {"S": 2, "T": 300, "H": 512, "E": 64, "k": 8, "P": 8}, 2, 8),
+    # one launch: one token, the largest batch, ragged segments with run alignment
+    ("decode", {"T": 1}, 4, 1), ("decode", {"T": 256}, -1, 1),
+    ("tiny", {"T": 200, "H": 1536, "E": 64, "k": 8, "P": 8}, 2, 8)])
 def test_quantized_fused_equals_separate_and_oracle(quant, g, name, over, recv_part, align):
-    w_ = ms.workload(name, **over)
+    w_ = ms.workload(name, index=900 + len(over), **over)
     inp = ms.gen_inputs(w_)
     fused, kf = _dispatch_q("fused", quant, w_, inp, g, recv_part, align, trace=True)
     sep, _ = _dispatch_q("separate", quant, w_, inp, g, recv_part, align)
     _same(fused, sep)
-    assert kf[-1] == f"k_pack_permute_{quant}", kf
+    if w_.S == 1 and w_.T <= 256:
+        assert kf == [f"k_dispatch_small_{quant}"], kf
+    else:
+        assert kf[-1] == f"k_pack_permute_{quant}", kf
     assert len(kf) == m.moe_dispatch_quantized_kernels(w_.S, w_.T, w_.k, w_.E, w_.P), kf
     lay, q, src, per = _q_oracle(quant, w_, inp, g, recv_part, align)
     for key in ("token_slot", "part_offsets", "expert_counts"):
@@ -307,10 +313,11 @@ def test_quantized_fused_equals_separate_and_oracle(quant, g, name, over, recv_p
 
 
 @pytest.mark.parametrize("quant", ["mxfp8", "nvfp4"])
-def test_quantized_capacity_overflow_matches_separate(quant):
-    w_ = ms.workload("prefill", T=600, index=41)
+@pytest.mark.parametrize("T", [600, 64])
+def test_quantized_capacity_overflow_matches_separate(quant, T):
+    w_ = ms.workload("prefill", T=T, index=41)
     inp = ms.gen_inputs(w_)
-    for cap_send, cap_recv in ((600, None), (None, 1200)):
+    for cap_send, cap_recv in ((T, None), (None, 2 * T)):
         fused, _ = _dispatch_q("fused", quant, w_, inp, 1.0, cap_send=cap_send, cap_recv=cap_recv)
         sep, _ = _dispatch_q("separate", quant, w_, inp, 1.0, cap_send=cap_send, cap_recv=cap_recv)
         _same(fused, sep)
