@@ -655,7 +655,13 @@ def time_other_workload(m, torch, name, steps, dev, local, flush_l2, peak, varia
             "clocks": clocks}
 
 
-def time_decode_layers(m, torch, steps, dev, local, peak, variant_kw, layers=40):
+# variants whose decode step the 40-layer graph also times (their MoePath options
+# are all in path_kwargs; the placed variant needs a plan, the routed one has no
+# pair rows to count)
+LAYERED_DECODE_VARIANTS = ("contiguous", "masked", "mxfp8", "nvfp4", "two_stage")
+
+
+def time_decode_layers(m, torch, steps, dev, local, peak, variant_kw, layers=40, byte_flags=None):
     """Decode as an engine runs it: one CUDA graph holding the round trips of
     `layers` MoE layers (route ... combine per layer, each layer with its own
     logits, x and buffers), replayed `steps` times (ishwarj.com a2a post, §1.4:
@@ -694,7 +700,8 @@ def time_decode_layers(m, torch, steps, dev, local, peak, variant_kw, layers=40)
         pr = int((p.pair_row >= 0).sum().item())
         copies += c
         pairs_recv += pr
-        b_layers += algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, c, c, pr)["step"]
+        b_layers += algorithmic_bytes(w.S, w.T, w.H, w.E, w.k, w.P, c, c, pr,
+                                      **(byte_flags or {}))["step"]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     cap = torch.cuda.Stream(device=dev)
     graph = torch.cuda.CUDAGraph()
@@ -734,6 +741,8 @@ def time_decode_layers(m, torch, steps, dev, local, peak, variant_kw, layers=40)
             "bytes_per_layer_mean": round(b_layers / layers),
             "data_per_replay_over_l2": round(b_layers / l2, 2),
             "copies_per_token": round(copies / (w.S * w.T * layers), 4),
+            "path_options": {key: val for key, val in variant_kw.items()
+                             if isinstance(val, (str, int, float))},
             "launches_per_layer": paths[0].launches_per_step(),
             "dispatch_mode": paths[0].dispatch_mode, "dev_status": status,
             "l2_flush": "none: the replay's data is several times the L2",
@@ -1075,9 +1084,14 @@ def run_ours(args, world, rank, local):
                 others[name] = time_other_workload(m, torch, name, steps_o, dev, local, flush_l2,
                                                    peak_o, path_kwargs(args, ms.workload(name)))
                 torch.cuda.empty_cache()
-        if rank == 0 and args.other_workloads and args.variant == "contiguous":
+        if rank == 0 and args.other_workloads and args.variant in LAYERED_DECODE_VARIANTS:
+            if others is None:
+                others = {}
             others["decode_40_layers"] = time_decode_layers(
-                m, torch, 200, dev, local, peak_o, path_kwargs(args, ms.workload("decode")))
+                m, torch, 200, dev, local, measured_peak()[0],
+                path_kwargs(args, ms.workload("decode")),
+                byte_flags={"two_stage": args.variant == "two_stage",
+                            "mxfp8": args.variant == "mxfp8", "nvfp4": args.variant == "nvfp4"})
             torch.cuda.empty_cache()
 
     if rank != 0:
