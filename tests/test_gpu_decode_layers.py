@@ -4,7 +4,8 @@ decode step makes ~40 round trips, recorded once and replayed).
 
 Layer l + 1 dispatches the rows layer l's combine wrote (x of layer l + 1 is
 layer l's `out` buffer), every launch chained to the one before it by
-programmatic dependent launch.  The one-launch dispatch asks L2 for its logits
+programmatic dependent launch; the receive rows take the contiguous runs or
+the masked layout (a2a-backends sections 4.1, 4.2).  The one-launch dispatch asks L2 for its logits
 before its grid-dependency wait and loads its first x segment right after the
 wait, so each layer's received rows must be, byte for byte, the previous
 layer's combine output of the same replay: the test rewrites every layer's
@@ -43,13 +44,21 @@ def _inputs(w_, batch):
     return lg, x0
 
 
-def _check_layers(w_, paths, x0_bits, logits):
+def _check_layers(w_, paths, x0_bits, logits, layout):
     x_bits = x0_bits
     for l, p in enumerate(paths):
         ref = oracle.run_path(x_bits, logits[l], w_.E, w_.k, w_.P, None)
         pair_row = host(p.pair_row)
         assert np.array_equal(host(p.topk_ids), ref["ids"]), l
-        assert np.array_equal(pair_row, ref["permute"]["pair_row"]), l
+        if layout == "masked":
+            cap_send = w_.T * min(w_.k, w_.P)
+            mref = oracle.permute_masked(ref["send"], ref["layout"]["token_slot"], ref["ids"],
+                                         w_.E, -1, p.block_rows)
+            assert np.array_equal(pair_row, mref["pair_row"]), l
+            assert np.array_equal(host(p.masked_counts), mref["masked_counts"]), l
+            assert ref["send"].shape[1] == cap_send
+        else:
+            assert np.array_equal(pair_row, ref["permute"]["pair_row"]), l
         assert np.array_equal(host(p.token_slot), ref["layout"]["token_slot"]), l
         # the received rows are the bytes of this layer's x: for l > 0 the
         # previous layer's combine output of this replay
@@ -66,9 +75,11 @@ def _check_layers(w_, paths, x0_bits, logits):
         x_bits = out.reshape(w_.S, w_.T, w_.H)
 
 
-def test_decode_layers_in_one_graph():
+@pytest.mark.parametrize("layout", ["contiguous", "masked"])
+def test_decode_layers_in_one_graph(layout):
     w_ = ms.workload("decode")
-    paths = [m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, dispatch="fused")
+    kw = {"layout": "masked", "block_rows": 64} if layout == "masked" else {}
+    paths = [m.MoePath(w_.S, w_.T, w_.H, w_.E, w_.k, w_.P, dispatch="fused", **kw)
              for _ in range(LAYERS)]
     lg, x0 = _inputs(w_, 11)
     logits = [f32_dev(lg[l]) for l in range(LAYERS)]
@@ -76,13 +87,14 @@ def test_decode_layers_in_one_graph():
     xs = [x_first] + [paths[l - 1].out for l in range(1, LAYERS)]
     s = torch.cuda.Stream()
     calls = [p.bind(logits[l], xs[l], s) for l, p in enumerate(paths)]
+    first = "moe_dispatch_masked" if layout == "masked" else "moe_dispatch"
     for c in calls:
-        assert [fn.__name__ for fn, _ in c] == ["moe_dispatch", "moe_combine"]
+        assert [fn.__name__ for fn, _ in c] == [first, "moe_combine"]
     with torch.cuda.stream(s):
         for c in calls:
             m.MoePath.run_bound(c)
     torch.cuda.synchronize()
-    _check_layers(w_, paths, x0, lg)
+    _check_layers(w_, paths, x0, lg, layout)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for c in calls:
@@ -95,4 +107,4 @@ def test_decode_layers_in_one_graph():
         torch.cuda.synchronize()
         g.replay()
         torch.cuda.synchronize()
-        _check_layers(w_, paths, x0, lg)
+        _check_layers(w_, paths, x0, lg, layout)
