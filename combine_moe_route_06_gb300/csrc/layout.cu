@@ -354,14 +354,16 @@ __global__ void k_layout_empty(int S, int E, int P, int32_t *__restrict__ expert
 // through global memory.
 
 constexpr int kMaxCluster = 16;
+constexpr int kChunkWide = 1024;  // tokens (and threads) per CTA of the wide cluster form
 
-// Dynamic shared memory of k_layout_cluster: ids (16-byte aligned, offset 0),
-// slots, ranks, warp histograms and lane masks, the partition of each expert,
-// this chunk's and the earlier chunks' expert counts.
+// Dynamic shared memory of k_layout_cluster<CHUNK>: ids (16-byte aligned,
+// offset 0), slots, ranks, warp histograms and lane masks, the partition of
+// each expert, this chunk's and the earlier chunks' expert counts.
+template <int CHUNK>
 inline size_t cluster_smem(int k, int E, int P)
 {
-    const size_t ids_pad = ((size_t)kChunk * k + 3) / 4 * 4;
-    return (ids_pad + (size_t)kChunk * ((P | 1) + (k | 1)) + 2 * kChunkWarps * E + 3 * E) *
+    const size_t ids_pad = ((size_t)CHUNK * k + 3) / 4 * 4;
+    return (ids_pad + (size_t)CHUNK * ((P | 1) + (k | 1)) + 2 * (CHUNK / 32) * E + 3 * E) *
            sizeof(int);
 }
 
@@ -377,7 +379,8 @@ __device__ __forceinline__ void cluster_wait()
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kChunk) k_layout_cluster(const int32_t *__restrict__ ids, int T,
+template <int CHUNK>
+__global__ void __launch_bounds__(CHUNK) k_layout_cluster(const int32_t *__restrict__ ids, int T,
                                                            int k, int E, int P, int G,
                                                            int32_t *__restrict__ expert_counts,
                                                            int32_t *__restrict__ expert_rank,
@@ -389,26 +392,26 @@ __global__ void __launch_bounds__(kChunk) k_layout_cluster(const int32_t *__rest
     cg::cluster_group cluster = cg::this_cluster();
     const int j = (int)cluster.block_rank();         // chunk of the source
     const int s = blockIdx.x / G;
-    const int t0 = j * kChunk;
-    const int n = min(kChunk, T - t0);
+    const int t0 = j * CHUNK;
+    const int n = min(CHUNK, T - t0);
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = E / P;
     const int sp = P | 1, sk = k | 1;                // odd row strides: no bank conflicts
 
     extern __shared__ __align__(16) int sm[];
-    int *ids_s = sm;                                                  // [256][k]
-    int *slot_s = ids_s + ((kChunk * k + 3) & ~3);                    // [256][sp]
-    int *rank_s = slot_s + kChunk * sp;                               // [256][sk]
-    int *whist = rank_s + kChunk * sk;                                // [8][E]
-    unsigned *wmask = (unsigned *)(whist + kChunkWarps * E);          // [8][E]
-    int *part_s = (int *)(wmask + kChunkWarps * E);                   // [E]
+    int *ids_s = sm;                                                  // [CHUNK][k]
+    int *slot_s = ids_s + ((CHUNK * k + 3) & ~3);                    // [CHUNK][sp]
+    int *rank_s = slot_s + CHUNK * sp;                               // [CHUNK][sk]
+    int *whist = rank_s + CHUNK * sk;                                // [CHUNK / 32][E]
+    unsigned *wmask = (unsigned *)(whist + (CHUNK / 32) * E);          // [CHUNK / 32][E]
+    int *part_s = (int *)(wmask + (CHUNK / 32) * E);                   // [E]
     int *own_e = part_s + E;     // [E] pairs of expert e in this chunk
     int *ebase = own_e + E;      // [E] pairs of expert e in the earlier chunks (written remotely)
-    __shared__ int wpart[kChunkWarps][kMaxP];
+    __shared__ int wpart[(CHUNK / 32)][kMaxP];
     __shared__ int own_p[kMaxP];  // tokens of this chunk that need partition p
     __shared__ int tot[kMaxP], pre[kMaxP], poff[kMaxP + 1], padd[kMaxP];
 
-    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) {
+    for (int i = threadIdx.x; i < (CHUNK / 32) * E; i += blockDim.x) {
         whist[i] = 0;
         wmask[i] = 0u;
     }
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kChunk) k_layout_cluster(const int32_t *__rest
         const int p = threadIdx.x;
         int run = 0;
 #pragma unroll
-        for (int ww = 0; ww < kChunkWarps; ww++) {
+        for (int ww = 0; ww < (CHUNK / 32); ww++) {
             const int v = wpart[ww][p];
             wpart[ww][p] = run;
             run += v;
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(kChunk) k_layout_cluster(const int32_t *__rest
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
 #pragma unroll
-        for (int ww = 0; ww < kChunkWarps; ww++) {
+        for (int ww = 0; ww < (CHUNK / 32); ww++) {
             const int v = whist[ww * E + e];
             whist[ww * E + e] = run;
             run += v;
@@ -577,9 +580,9 @@ __global__ void __launch_bounds__(kChunk) k_layout_cluster(const int32_t *__rest
     // i % P), kept up to date by steps of blockDim.x instead of a division each
     int32_t *slot_g = token_slot + ((int64_t)s * T + t0) * P;
     {
-        const int dt = kChunk / P, dp = kChunk % P;
+        const int dt = CHUNK / P, dp = CHUNK % P;
         int t = threadIdx.x / P, p = threadIdx.x % P;
-        for (int i = threadIdx.x; i < n * P; i += kChunk) {
+        for (int i = threadIdx.x; i < n * P; i += CHUNK) {
             const int v = slot_s[t * sp + p];
             slot_g[i] = v >= 0 ? v + padd[p] : -1;
             t += dt;
@@ -595,9 +598,9 @@ __global__ void __launch_bounds__(kChunk) k_layout_cluster(const int32_t *__rest
     cluster_wait();
     int32_t *rank_g = expert_rank + ((int64_t)s * T + t0) * k;
     {
-        const int dt = kChunk / k, dj = kChunk % k;
+        const int dt = CHUNK / k, dj = CHUNK % k;
         int t = threadIdx.x / k, jj = threadIdx.x % k;
-        for (int i = threadIdx.x; i < n * k; i += kChunk) {
+        for (int i = threadIdx.x; i < n * k; i += CHUNK) {
             const int r = rank_s[t * sk + jj];
             rank_g[i] = r >= 0 ? r + ebase[ids_s[t * k + jj]] : -1;
             t += dt;
@@ -610,10 +613,11 @@ __global__ void __launch_bounds__(kChunk) k_layout_cluster(const int32_t *__rest
     }
 }
 
-// Largest cluster (16, 8, 4, 2 or 1 CTAs) of k_layout_cluster that the current
-// device can schedule with `smem` bytes of dynamic shared memory per CTA, and
-// the most dynamic shared memory a CTA of it may have (the opt-in limit less
-// the kernel's static shared memory); looked up once per device.
+// Largest cluster (16, 8, 4, 2 or 1 CTAs) of k_layout_cluster<CHUNK> that the
+// current device can schedule with `smem` bytes of dynamic shared memory per
+// CTA, and the most dynamic shared memory a CTA of it may have (the opt-in
+// limit less the kernel's static shared memory); looked up once per device.
+template <int CHUNK>
 cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
 {
     static std::mutex mu;
@@ -628,16 +632,16 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
         DeviceInfo di;
         if ((e = device_info(&di)) != cudaSuccess) return e;
         cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, k_layout_cluster)) != cudaSuccess) return e;
+        if ((e = cudaFuncGetAttributes(&fa, k_layout_cluster<CHUNK>)) != cudaSuccess) return e;
         const size_t limit = (size_t)di.max_smem_optin - fa.sharedSizeBytes;
-        if ((e = cudaFuncSetAttribute(k_layout_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((e = cudaFuncSetAttribute(k_layout_cluster<CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)limit)) != cudaSuccess)
             return e;
         dyn[dev] = limit;
         // clusters of 16 need the non-portable size; a device that refuses it
         // gets the portable limit of 8
         int g = kMaxCluster;
-        if (cudaFuncSetAttribute(k_layout_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed,
+        if (cudaFuncSetAttribute(k_layout_cluster<CHUNK>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                  1) != cudaSuccess) {
             (void)cudaGetLastError();
             g = 8;
@@ -649,7 +653,7 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
         for (; g > 1; g /= 2) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)g);
-            cfg.blockDim = dim3(kChunk);
+            cfg.blockDim = dim3(CHUNK);
             cfg.dynamicSmemBytes = smem;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -659,7 +663,7 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, k_layout_cluster, &cfg) == cudaSuccess) {
+            if (cudaOccupancyMaxActiveClusters(&n, k_layout_cluster<CHUNK>, &cfg) == cudaSuccess) {
                 answered = true;
                 if (n > 0) break;
             } else {
@@ -680,21 +684,28 @@ cudaError_t cluster_size_limit(size_t smem, int *out, size_t *max_dyn)
 
 // The cluster form runs when a source has 2 to kMaxCluster chunks, the device
 // schedules clusters of that many CTAs with one CTA per SM, and a chunk's
-// shared memory fits.
-cudaError_t use_cluster_form(int T, int k, int E, int P, bool *out)
+// shared memory fits.  Chunks are 256 tokens; a source too long for 16 of
+// them takes chunks of 1,024 tokens (and threads) where 16 of those hold it
+// and their shared memory fits.  *chunk is the chunk size, 0 for no cluster.
+cudaError_t use_cluster_form(int T, int k, int E, int P, int *chunk)
 {
-    *out = false;
+    *chunk = 0;
     const int C = (int)div_up(T, kChunk);
     if (C < 2) return cudaSuccess;
     DeviceInfo di;
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
+    const size_t one_per_sm = (size_t)di.max_smem_optin / 2 + 1024;
     int gmax = 0;
     size_t max_dyn = 0;
-    if ((e = cluster_size_limit((size_t)di.max_smem_optin / 2 + 1024, &gmax, &max_dyn)) !=
-        cudaSuccess)
-        return e;
-    *out = C <= gmax && cluster_smem(k, E, P) <= max_dyn;
+    if ((e = cluster_size_limit<kChunk>(one_per_sm, &gmax, &max_dyn)) != cudaSuccess) return e;
+    if (C <= gmax) {
+        if (cluster_smem<kChunk>(k, E, P) <= max_dyn) *chunk = kChunk;
+        return cudaSuccess;
+    }
+    const int Cw = (int)div_up(T, kChunkWide);
+    if ((e = cluster_size_limit<kChunkWide>(one_per_sm, &gmax, &max_dyn)) != cudaSuccess) return e;
+    if (Cw <= gmax && cluster_smem<kChunkWide>(k, E, P) <= max_dyn) *chunk = kChunkWide;
     return cudaSuccess;
 }
 
@@ -702,10 +713,10 @@ cudaError_t use_cluster_form(int T, int k, int E, int P, bool *out)
 
 cudaError_t layout_kernel_count(int T, int k, int E, int P, int *n)
 {
-    bool cluster = false;
-    const cudaError_t e = use_cluster_form(T, k, E, P, &cluster);
+    int chunk = 0;
+    const cudaError_t e = use_cluster_form(T, k, E, P, &chunk);
     if (e != cudaSuccess) return e;
-    *n = (T <= kChunk || cluster) ? 1 : 2;
+    *n = (T <= kChunk || chunk > 0) ? 1 : 2;
     return cudaSuccess;
 }
 
@@ -736,15 +747,27 @@ cudaError_t launch_dispatch_layout(const int32_t *ids, int S, int T, int k, int 
     const size_t one_per_sm = (size_t)di.max_smem_optin / 2 + 1024;
 
     // Cluster form: one cluster per source, one CTA per chunk.
-    bool cluster = false;
-    if ((e = use_cluster_form(T, k, E, P, &cluster)) != cudaSuccess) return e;
-    if (cluster) {
-        const size_t smc = cluster_smem(k, E, P);
+    int chunk = 0;
+    if ((e = use_cluster_form(T, k, E, P, &chunk)) != cudaSuccess) return e;
+    if (chunk == kChunk) {
+        const size_t smc = cluster_smem<kChunk>(k, E, P);
         const size_t smem = smc > one_per_sm ? smc : one_per_sm;
         MOE_TRACED_LAUNCH("k_layout_cluster", st,
-                          e = launch_pdl_cluster(k_layout_cluster, dim3((unsigned)(S * C)),
+                          e = launch_pdl_cluster(k_layout_cluster<kChunk>, dim3((unsigned)(S * C)),
                                                  dim3(kChunk), smem, (unsigned)C, st, ids, T, k, E,
                                                  P, C, expert_counts, expert_rank, part_counts,
+                                                 part_offsets, token_slot, dev_status));
+        return e;
+    }
+    if (chunk == kChunkWide) {
+        const int Cw = (int)div_up(T, kChunkWide);
+        const size_t smc = cluster_smem<kChunkWide>(k, E, P);
+        const size_t smem = smc > one_per_sm ? smc : one_per_sm;
+        MOE_TRACED_LAUNCH("k_layout_cluster", st,
+                          e = launch_pdl_cluster(k_layout_cluster<kChunkWide>,
+                                                 dim3((unsigned)(S * Cw)), dim3(kChunkWide), smem,
+                                                 (unsigned)Cw, st, ids, T, k, E, P, Cw,
+                                                 expert_counts, expert_rank, part_counts,
                                                  part_offsets, token_slot, dev_status));
         return e;
     }

@@ -5,8 +5,9 @@ step) it is one launch of one CTA per source.  With 2 to 16 chunks per source
 (up to 4,096 tokens) it is one launch with a thread-block cluster per source
 and a CTA per chunk: the CTAs lay out their chunks in shared memory, meet at the cluster
 barrier, exchange counts through distributed shared memory and store final
-values.  Longer sources take two launches (chunk-local layout, then a fix-up
-through the workspace).  Both forms must give the oracle's outputs bit for bit
+values.  Sources of up to 16,384 tokens take the same cluster form with chunks
+of 1,024 tokens (and threads) where their shared memory fits.  Longer sources
+take two launches (chunk-local layout, then a fix-up through the workspace).  Both forms must give the oracle's outputs bit for bit
 (a2a-backends section 1.3 and 3.2: slots, counts, offsets; section 1.5: the
 expert ranks the receiver's runs are built from), with ragged tails, repeated
 and invalid ids, and E smaller than the cluster.
@@ -104,8 +105,29 @@ def test_cluster_form_repeats_and_bad_ids():
     _check(ids, 64, 8, "cluster")
 
 
-@pytest.mark.parametrize("S,T,k,E,P", [(1, 4097, 6, 384, 8), (1, 16384, 8, 64, 8),
-                                       (2, 9000, 6, 384, 8), (1, 40000, 32, 64, 32)])
+@pytest.mark.parametrize("S,T,k,E,P", [
+    (1, 4097, 6, 384, 8),        # just past 16 chunks of 256: 5 chunks of 1,024, ragged
+    (1, 16384, 8, 64, 8),        # the large shape: a cluster of 16 wide chunks
+    (2, 9000, 6, 384, 8),        # one cluster per source
+    (1, 12000, 8, 64, 16),       # more partitions
+    (3, 5000, 4, 4, 1),          # fewer experts than CTAs, one partition
+])
+def test_wide_cluster_form(S, T, k, E, P):
+    _check(_ids(S, T, k, E, seed=S * 7 + T), E, P, "cluster")
+
+
+def test_wide_cluster_form_repeats_and_bad_ids():
+    ids = _ids(1, 9000, 8, 64, seed=12, dups=True, bad=True)
+    assert (ids >= 64).any() and (ids < 0).any()
+    _check(ids, 64, 8, "cluster")
+
+
+@pytest.mark.parametrize("S,T,k,E,P", [
+    (1, 16385, 6, 384, 8),       # past 16 chunks of 1,024
+    (2, 20000, 8, 64, 8),
+    (1, 40000, 32, 64, 32),
+    (1, 5000, 32, 1024, 32),     # wide chunks would not fit one CTA's shared memory
+])
 def test_two_launch_form(S, T, k, E, P):
     _check(_ids(S, T, k, E, seed=S * 7 + T), E, P, "two")
 

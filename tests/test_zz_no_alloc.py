@@ -80,10 +80,11 @@ def _workspace_layout(ids, E, P):
 
 
 def test_static_layout_uses_its_scratch_twice(lib):
-    # first call: the large workload (16,384 tokens, 64 chunks in one source,
-    # E = 64); second call: 2 sources x 5,000 tokens (20 chunks each), E = 384,
+    # two shapes longer than one cluster covers (16 chunks of 1,024 tokens):
+    # first the large workload's rows at 20,000 tokens (79 chunks of 256 in one
+    # source, E = 64), then 2 sources x 17,000 tokens (67 chunks each, E = 384),
     # whose counts overwrite and then read back the same bytes of the array
-    cases = [ms.workload("large"), ms.workload("prefill", S=2, T=5000, index=17)]
+    cases = [ms.workload("large", T=20000, index=18), ms.workload("prefill", S=2, T=17000, index=17)]
     for w in cases:
         assert lib.moe_dispatch_layout_kernels(w.S, w.T, w.k, w.E, w.P) == 2, w
         ids_np, _ = oracle.route_topk(ms.gen_logits(w), w.k)
