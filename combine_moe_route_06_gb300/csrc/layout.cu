@@ -19,7 +19,9 @@
 //   - 2 to 16 chunks per source: one thread-block cluster per source
 //     (k_layout_cluster).  The chunks exchange their counts through
 //     distributed shared memory between two cluster barriers and store final
-//     values: one launch, no counts through global memory;
+//     values: one launch, no counts through global memory.  A source of up to
+//     16 chunks of 1,024 tokens takes the same kernel with 1,024-token chunks
+//     (and threads) where their shared memory fits;
 //   - more chunks: k_layout_local stores chunk-local values and the chunk's
 //     counts in the workspace; k_layout_fix sums the earlier chunks' counts
 //     and adds them.

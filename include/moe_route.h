@@ -177,8 +177,10 @@ moe_status_t moe_route_topk(const float *logits, int S, int T, int E, int k,
  *   dev_status    device uint32 status word (bad ids).
  * Work is cut into 256-token chunks, one CTA each; with 2 to 16 chunks per
  * source the chunks of a source form one thread-block cluster and exchange
- * their counts in distributed shared memory (one launch), with more they go
- * through `ws` (two launches).  Counting uses order-free integer adds and
+ * their counts in distributed shared memory (one launch); a longer source of
+ * at most 16 chunks of 1,024 tokens takes the same form with 1,024-token chunks
+ * where their shared memory fits; otherwise the counts go through `ws` (two
+ * launches).  Counting uses order-free integer adds and
  * ranks follow the fixed (token, slot) order, so the outputs are the same
  * bytes on every run.  The first call on a device asks the device once which
  * cluster sizes it schedules; make it before capturing a stream (a query
@@ -209,7 +211,7 @@ moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int S, int T, int k, i
  * belongs to the device's primary context: after cudaDeviceReset (or any
  * other teardown of that context) in the same process, do not call this entry
  * point again.  Only sizes that take the layout's two-launch form (more
- * 256-token chunks per source than one thread-block cluster holds, see
+ * chunks per source than one thread-block cluster holds, see
  * moe_dispatch_layout_kernels) read or write the array.  All calls share the one
  * array and it keeps the last call's contents (nothing in it needs to start
  * at zero): calls that can overlap on the GPU -- on different streams, or from
