@@ -221,6 +221,8 @@ def _dispatch_masked_gpu(w_, inp, recv_part, block_rows):
     ("decode", {"T": 255}, 5, 16),
     ("decode", {"T": 256}, -1, 4),
     ("decode", {"T": 257}, -1, 64),                         # past the one-launch form
+    ("decode", {"T": 0}, -1, 64),                           # an empty batch
+    ("decode", {"T": 0}, 2, 0),
     ("tiny", {"T": 100, "E": 1024, "k": 32, "P": 32}, 7, 8),
     ("tiny", {"S": 3}, 1, 200),
     ("prefill", {}, -1, 128),
@@ -253,7 +255,8 @@ def test_dispatch_masked_equals_oracle(name, over, recv_part, block_rows):
     assert got["status"] == ref["status"]
     n = m.moe_dispatch_masked_kernels(w_.S, w_.T, w_.k, w_.E, w_.P, recv_part)
     assert len(got["kernels"]) == n, got["kernels"]
-    assert (got["kernels"] == ["k_dispatch_small"]) == (w_.S == 1 and w_.T <= 256), got["kernels"]
+    assert (got["kernels"] == ["k_dispatch_small"]) == (w_.S == 1 and 1 <= w_.T <= 256), \
+        got["kernels"]
 
 
 def test_masked_path_one_call_equals_separate():
