@@ -35,13 +35,6 @@ __device__ __forceinline__ int warp_inclusive_scan(int v)
     return v;
 }
 
-__device__ __forceinline__ int warp_sum(int v)
-{
-#pragma unroll
-    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-    return v;
-}
-
 // Whether expert e (of E, L per partition) is held by the receiving set:
 // partition recv_part, or every partition when recv_part < 0.
 __device__ __forceinline__ bool in_recv(int e, int E, int L, int recv_part)
