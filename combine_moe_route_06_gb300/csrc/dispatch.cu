@@ -10,8 +10,10 @@
 // moe_route_topk, moe_dispatch_layout, moe_dispatch_pack and
 // moe_permute_to_experts give one after the other.
 //
-// moe_dispatch for one source of at most 256 tokens (a decode step) is one
-// launch (dispatch_small.cu).  Larger batches run the routing kernel, the
+// moe_dispatch, moe_dispatch_masked and moe_dispatch_quantized for one source
+// of at most 256 tokens (a decode step) are one launch (dispatch_small.cuh,
+// launched from dispatch_small.cu and dispatch_small_q.cu; their launchers
+// below pick that form).  Larger batches run the routing kernel, the
 // layout (moe_dispatch_layout's kernels), then k_pack_permute: pack and
 // permute in one pass.  A row task reads the token's segment of x once,
 // stores it to every send slot of the token, then reads back the segment of
