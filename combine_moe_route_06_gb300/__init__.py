@@ -37,8 +37,8 @@ __all__ = [
     "moe_combine_stage2", "moe_dispatch_pack_mxfp8", "moe_expert_scale_mxfp8",
     "moe_plan_placement", "moe_workspace_bytes_mapped", "moe_dispatch_layout_mapped", "Placement",
     "moe_dispatch_pack_routed", "moe_routed_expert_stage1", "moe_dispatch_pack_nvfp4",
-    "moe_expert_scale_nvfp4", "nvfp4_record_bytes", "mxfp8_record_bytes", "HostPipeline", "MoePath", "trace_enable", "trace_disable", "trace_reset",
-    "trace_records",
+    "moe_expert_scale_nvfp4", "nvfp4_record_bytes", "mxfp8_record_bytes", "HostPipeline",
+    "MoePath", "trace_enable", "trace_disable", "trace_reset", "trace_records",
 ]
 
 MOE_OK = 0
