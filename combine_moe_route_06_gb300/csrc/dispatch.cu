@@ -40,6 +40,24 @@ constexpr int kPPUnroll = 4;                       // int4 per lane per segment 
 constexpr int kPPSegVec = 32 * kPPUnroll;
 constexpr int kPPThreads = 256;
 constexpr int kPPBatch = 1;                        // one partition's row read back at a time
+constexpr int kPPStageMax = 3;                     // tasks per warp whose x is staged early
+constexpr size_t kPPStageBytes = (size_t)(kPPThreads / 32) * kPPSegVec * sizeof(int4);  // per task
+
+// 16-byte asynchronous copy global -> shared (no register staging).  The
+// copying thread sees the bytes after cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(int4 *smem_dst, const int4 *gmem_src)
+{
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 // Run starts of the receiving experts, built by every CTA in shared memory
 // from the expert counts (as the permute's map step does): off[e] = padded
@@ -115,21 +133,31 @@ __device__ __forceinline__ void mark_unused_rows(int used, int cap_recv, int S, 
 // tokens, are the ones the combine reads first).  Every CTA first builds the
 // run starts from the expert counts in shared memory (as the permute's map
 // step does); each warp derives its token's pair rows from the ids and ranks;
-// the warp of segment 0 stores pair_row, recv_pair and send_src.
-__global__ void __launch_bounds__(kPPThreads) k_pack_permute(
+// the warp of segment 0 stores pair_row, recv_pair and send_src.  Inside
+// moe_dispatch each warp loads its first task's x segment into registers and
+// copies the next `stage` tasks' segments into shared memory before the
+// grid-dependency wait, while the layout kernel still runs.
+__global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute(
     const int4 *__restrict__ x, const int32_t *__restrict__ token_slot,
     const int32_t *__restrict__ part_offsets, const int32_t *__restrict__ ids,
     const int32_t *__restrict__ expert_counts, const int32_t *__restrict__ expert_rank, int S,
     int64_t NT, int k, int E, int L, int P, int T, int V, int recv_part, int align, int cap_send,
     int cap_recv, int4 *__restrict__ send, int32_t *__restrict__ send_src,
     int4 *__restrict__ recv, int32_t *__restrict__ expert_offsets, int32_t *__restrict__ pair_row,
-    int32_t *__restrict__ recv_pair, uint32_t *dev_status, bool x_before_wait)
+    int32_t *__restrict__ recv_pair, uint32_t *dev_status, bool x_before_wait, int stage)
 {
     const int lane = threadIdx.x & 31;
     const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t gwarps = gthreads >> 5;
     const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
+    extern __shared__ int smp[];
+    int *off = smp;              // [E + 1]
+    int *cnt = off + E + 1;      // [E]
+    int *sb = cnt + E;           // [S][E]
+    // [warp][stage][kPPUnroll][32 lanes]: x segments of this warp's tasks 1..stage
+    int4 *stg = reinterpret_cast<int4 *>(smp + ((2 * E + 1 + S * E + 3) & ~3)) +
+                (threadIdx.x >> 5) * stage * kPPSegVec;
     // With x_before_wait the first task's x segment is loaded before the
     // grid-dependency wait, so its HBM latency passes while the layout finishes.
     // moe_dispatch sets it: x was complete before its routing kernel ran, this
@@ -153,6 +181,24 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
             if (vi < V) x0[u] = ld_stream(x + n0 * V + vi);
         }
     }
+    // Tasks 1..stage of this warp: their x segments are copied into shared
+    // memory now, so that while the layout finishes HBM reads x instead of
+    // idling and the row phase that follows is left almost only writes.  Each
+    // lane copies the 16-byte pieces it will store itself, so no barrier
+    // orders the copies with their use, only cp_async_wait_all.
+    for (int j = 1; j <= stage; j++) {
+        const int64_t rt = rt0 + (int64_t)j * gwarps;
+        if (rt >= NT * nseg) break;
+        const int64_t t = NT * nseg - 1 - rt;
+        const int64_t n = t / nseg;
+        const int g = (int)(t - n * nseg);
+#pragma unroll
+        for (int u = 0; u < kPPUnroll; u++) {
+            const int vi = g * kPPSegVec + lane + 32 * u;
+            if (vi < V) cp_async16(stg + ((j - 1) * kPPUnroll + u) * 32 + lane, x + n * V + vi);
+        }
+    }
+    cp_async_commit();
     if (x_before_wait) pdl_wait();
     pdl_trigger();
     bool cap_flag = false, bad_slot = false, dropped = false, bad_rank = false, bad_id = false;
@@ -171,13 +217,10 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
     };
     if (rtask < ntask) fetch(rtask);
 
-    extern __shared__ int smp[];
-    int *off = smp;              // [E + 1]
-    int *cnt = off + E + 1;      // [E]
-    int *sb = cnt + E;           // [S][E]
     build_run_starts(expert_counts, S, E, L, recv_part, align, off, cnt, sb, expert_offsets);
+    cp_async_wait_all();
 
-    for (; rtask < ntask; rtask += gwarps) {
+    for (int it = 0; rtask < ntask; rtask += gwarps, it++) {
         const int64_t task = ntask - 1 - rtask;
         const int64_t n = task / nseg;
         const int g = (int)(task - n * nseg);
@@ -199,9 +242,17 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute(
             if (ts_c >= cap_send) pack_overflow = true;
             else if (ts_c >= 0) send_src[(int64_t)s * cap_send + ts_c] = (int32_t)(n - (int64_t)s * T);
         }
+        // x0 (task 0) and the staged segments (tasks 1..stage) pass through one
+        // register array, so the row task sees one array or none
+        int4 xs[kPPUnroll];
+        const bool have = it <= stage;
+#pragma unroll
+        for (int u = 0; u < kPPUnroll; u++)
+            xs[u] = it == 0 ? x0[u] : (have ? stg[((it - 1) * kPPUnroll + u) * 32 + lane]
+                                            : make_int4(0, 0, 0, 0));
         move_token_segment<kPPUnroll, kPPBatch>(x + n * V, send + (int64_t)s * cap_send * V, recv, V,
                                       g * kPPSegVec + lane, ts_c, pr, pp, P, cap_send, bad_slot,
-                                      cap_flag, g == 0, rtask == rt0 ? x0 : nullptr);
+                                      cap_flag, g == 0, have ? xs : nullptr);
     }
 
     // padding rows: warp task (expert, padding row index, segment)
@@ -481,8 +532,34 @@ cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
     const int V = H / 8;
     const int L = E / P;
     const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
-    const size_t smem = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
-    const int resident = resident_grid((const void *)k_pack_permute, kPPThreads, smem);
+    const size_t base = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
+    size_t smem = base;
+    int resident = resident_grid((const void *)k_pack_permute, kPPThreads, base);
+    // Staged x segments, for one source only: as many tasks per warp (at most
+    // kPPStageMax) as fit in the shared memory left beside the CTAs that the
+    // registers allow per SM.  (Measured on GB300, step through moe_dispatch:
+    // 4,096-token prefill 139.8 -> 134.4 us with three tasks, 136.1 with two;
+    // four took 48 KB more shared memory per CTA and made the 16,384-token step
+    // 12 us slower, the combine that follows it under programmatic launch
+    // landing on SMs left with little L1; eight sources of 4,096 tokens were
+    // 3.6 us slower with three tasks, so several sources stage nothing.)
+    int stage = 0;
+    if (x_before_wait && S == 1 && resident > 0) {
+        // the opt-in limit covers static shared memory too (48 bytes here)
+        const size_t max_dyn = (size_t)di.max_smem_optin - 1024;
+        e = cudaFuncSetAttribute(k_pack_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)max_dyn);
+        if (e != cudaSuccess) return e;
+        const size_t base16 = (base + 15) / 16 * 16;
+        for (int m = kPPStageMax; m >= 1 && stage == 0; m--) {
+            const size_t sm = base16 + (size_t)m * kPPStageBytes;
+            if (sm > max_dyn) continue;
+            if (resident_grid((const void *)k_pack_permute, kPPThreads, sm) >= resident) {
+                stage = m;
+                smem = sm;
+            }
+        }
+    }
     const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
     const int64_t warps = NT * nseg + (align > 1 ? (int64_t)E * (align - 1) * nseg : 0);
     int64_t blocks = div_up(warps, kPPThreads / 32);
@@ -499,7 +576,7 @@ cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
                                      expert_counts, expert_rank, S, NT, k, E, L, P, T, V,
                                      recv_part, align, cap_send, cap_recv, (int4 *)send, send_src,
                                      (int4 *)recv, expert_offsets, pair_row, recv_pair,
-                                     dev_status, x_before_wait));
+                                     dev_status, x_before_wait, stage));
     return e;
 }
 
