@@ -472,7 +472,7 @@ moe_status_t moe_dispatch_pack_permute_masked(const uint16_t *x, const int32_t *
                                                   expert_counts, expert_rank, S, T, k, E, P, H,
                                                   recv_part, block_rows, cap_send, send, send_src,
                                                   recv, masked_counts, pair_row, recv_pair,
-                                                  dev_status, stream),
+                                                  dev_status, stream, false),
                        __func__);
 }
 

@@ -59,6 +59,52 @@ __device__ __forceinline__ void cp_async_wait_all()
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// The early x reads of the one-pass kernels (tasks last to first, task rt of
+// warp w = rt0 + j * gwarps at its j-th iteration).  Loads the segment of the
+// warp's first task into x0 and copies those of its next `stage` tasks into
+// stg ([stage][kPPUnroll][32 lanes] int4, this warp's slots).  Each lane copies
+// the 16-byte pieces it will store itself, so no barrier orders the copies
+// with their use, only cp_async_wait_all.  Every lane must call (the copy
+// group is committed even when empty).
+__device__ __forceinline__ void stage_x(const int4 *__restrict__ x, int64_t ntask, int nseg, int V,
+                                        int64_t rt0, int64_t gwarps, int stage,
+                                        int4 (&x0)[kPPUnroll], int4 *stg)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int u = 0; u < kPPUnroll; u++) x0[u] = make_int4(0, 0, 0, 0);
+    for (int j = 0; j <= stage; j++) {
+        const int64_t rt = rt0 + (int64_t)j * gwarps;
+        if (rt >= ntask) break;
+        const int64_t t = ntask - 1 - rt;
+        const int64_t n = t / nseg;
+        const int g = (int)(t - n * nseg);
+#pragma unroll
+        for (int u = 0; u < kPPUnroll; u++) {
+            const int vi = g * kPPSegVec + lane + 32 * u;
+            if (vi >= V) continue;
+            if (j == 0) x0[u] = ld_stream(x + n * V + vi);
+            else cp_async16(stg + ((j - 1) * kPPUnroll + u) * 32 + lane, x + n * V + vi);
+        }
+    }
+    cp_async_commit();
+}
+
+// The x segment of the warp's it-th task if stage_x fetched it (into xs):
+// x0 for the first task, the staged copy for tasks 1..stage.  Call after
+// cp_async_wait_all.
+__device__ __forceinline__ bool staged_x(int it, int stage, const int4 (&x0)[kPPUnroll],
+                                         const int4 *stg, int4 (&xs)[kPPUnroll])
+{
+    const int lane = threadIdx.x & 31;
+    const bool have = it <= stage;
+#pragma unroll
+    for (int u = 0; u < kPPUnroll; u++)
+        xs[u] = it == 0 ? x0[u]
+                        : (have ? stg[((it - 1) * kPPUnroll + u) * 32 + lane] : make_int4(0, 0, 0, 0));
+    return have;
+}
+
 // Run starts of the receiving experts, built by every CTA in shared memory
 // from the expert counts (as the permute's map step does): off[e] = padded
 // pairs of the receiving experts before e (off[E] = rows used), cnt[e] = pairs
@@ -169,36 +215,11 @@ __global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute(
     // what ran before it, so it waits first.
     if (!x_before_wait) pdl_wait();
     const int64_t rt0 = gtid >> 5;
+    // Tasks 1..stage: their x segments are copied into shared memory now, so
+    // that while the layout finishes HBM reads x instead of idling and the row
+    // phase that follows is left almost only writes.
     int4 x0[kPPUnroll];
-    if (rt0 < NT * nseg) {
-        const int64_t t0 = NT * nseg - 1 - rt0;
-        const int64_t n0 = t0 / nseg;
-        const int g0 = (int)(t0 - n0 * nseg);
-#pragma unroll
-        for (int u = 0; u < kPPUnroll; u++) {
-            const int vi = g0 * kPPSegVec + lane + 32 * u;
-            x0[u] = make_int4(0, 0, 0, 0);
-            if (vi < V) x0[u] = ld_stream(x + n0 * V + vi);
-        }
-    }
-    // Tasks 1..stage of this warp: their x segments are copied into shared
-    // memory now, so that while the layout finishes HBM reads x instead of
-    // idling and the row phase that follows is left almost only writes.  Each
-    // lane copies the 16-byte pieces it will store itself, so no barrier
-    // orders the copies with their use, only cp_async_wait_all.
-    for (int j = 1; j <= stage; j++) {
-        const int64_t rt = rt0 + (int64_t)j * gwarps;
-        if (rt >= NT * nseg) break;
-        const int64_t t = NT * nseg - 1 - rt;
-        const int64_t n = t / nseg;
-        const int g = (int)(t - n * nseg);
-#pragma unroll
-        for (int u = 0; u < kPPUnroll; u++) {
-            const int vi = g * kPPSegVec + lane + 32 * u;
-            if (vi < V) cp_async16(stg + ((j - 1) * kPPUnroll + u) * 32 + lane, x + n * V + vi);
-        }
-    }
-    cp_async_commit();
+    stage_x(x, NT * nseg, nseg, V, rt0, gwarps, stage, x0, stg);
     if (x_before_wait) pdl_wait();
     pdl_trigger();
     bool cap_flag = false, bad_slot = false, dropped = false, bad_rank = false, bad_id = false;
@@ -242,14 +263,10 @@ __global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute(
             if (ts_c >= cap_send) pack_overflow = true;
             else if (ts_c >= 0) send_src[(int64_t)s * cap_send + ts_c] = (int32_t)(n - (int64_t)s * T);
         }
-        // x0 (task 0) and the staged segments (tasks 1..stage) pass through one
-        // register array, so the row task sees one array or none
+        // x0 (task 0) and the staged segments pass through one register
+        // array, so the row task sees one array or none
         int4 xs[kPPUnroll];
-        const bool have = it <= stage;
-#pragma unroll
-        for (int u = 0; u < kPPUnroll; u++)
-            xs[u] = it == 0 ? x0[u] : (have ? stg[((it - 1) * kPPUnroll + u) * 32 + lane]
-                                            : make_int4(0, 0, 0, 0));
+        const bool have = staged_x(it, stage, x0, stg, xs);
         move_token_segment<kPPUnroll, kPPBatch>(x + n * V, send + (int64_t)s * cap_send * V, recv, V,
                                       g * kPPSegVec + lane, ts_c, pr, pp, P, cap_send, bad_slot,
                                       cap_flag, g == 0, have ? xs : nullptr);
@@ -291,17 +308,15 @@ __global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute(
 // share of the blocks' unused rows; CTA 0 stores the rows in use per block.
 // Shared memory: per block the rows in use, the pairs in all sources, and the
 // pairs in the sources before each s.
-__global__ void __launch_bounds__(kPPThreads) k_pack_permute_masked(
+__global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute_masked(
     const int4 *__restrict__ x, const int32_t *__restrict__ token_slot,
     const int32_t *__restrict__ part_offsets, const int32_t *__restrict__ ids,
     const int32_t *__restrict__ expert_counts, const int32_t *__restrict__ expert_rank, int S,
     int64_t NT, int k, int E, int L, int P, int T, int V, int e0, int nb, int block_rows,
     int cap_send, int4 *__restrict__ send, int32_t *__restrict__ send_src,
     int4 *__restrict__ recv, int32_t *__restrict__ masked_counts, int32_t *__restrict__ pair_row,
-    int32_t *__restrict__ recv_pair, uint32_t *dev_status)
+    int32_t *__restrict__ recv_pair, uint32_t *dev_status, bool x_before_wait, int stage)
 {
-    pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t gthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -314,6 +329,18 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_masked(
     int *bcnt = smm;             // [nb] rows of block b in use
     int *btot = bcnt + nb;       // [nb] pairs of its expert in all sources
     int *bsb = btot + nb;        // [S][nb] pairs of its expert in the sources before s
+    // [warp][stage][kPPUnroll][32 lanes]: x segments of this warp's tasks 1..stage
+    int4 *stg = reinterpret_cast<int4 *>(smm + ((2 * nb + S * nb + 3) & ~3)) +
+                (threadIdx.x >> 5) * stage * kPPSegVec;
+    // x before the grid-dependency wait only inside moe_dispatch_masked (the
+    // same ordering argument as k_pack_permute); called on its own the kernel
+    // waits first.
+    if (!x_before_wait) pdl_wait();
+    const int64_t rt0 = gtid >> 5;
+    int4 x0[kPPUnroll];
+    stage_x(x, NT * nseg, nseg, V, rt0, gwarps, stage, x0, stg);
+    if (x_before_wait) pdl_wait();
+    pdl_trigger();
     for (int bb = threadIdx.x; bb < nb; bb += blockDim.x) {
         int run = 0;
         for (int s2 = 0; s2 < S; s2++) {
@@ -325,6 +352,7 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_masked(
         if (blockIdx.x == 0) masked_counts[bb] = bcnt[bb];
     }
     __syncthreads();
+    cp_async_wait_all();
     // unused rows of every block
     const int64_t rows = (int64_t)nb * block_rows;
     for (int64_t r = gtid; r < rows; r += gthreads) {
@@ -333,7 +361,8 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_masked(
     }
 
     const int64_t ntask = NT * nseg;
-    for (int64_t rtask = gtid >> 5; rtask < ntask; rtask += gwarps) {
+    int it = 0;
+    for (int64_t rtask = rt0; rtask < ntask; rtask += gwarps, it++) {
         const int64_t task = ntask - 1 - rtask;       // tokens last to first
         const int64_t n = task / nseg;
         const int g = (int)(task - n * nseg);
@@ -362,9 +391,11 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_masked(
             if (ts >= cap_send) pack_overflow = true;
             else if (ts >= 0) send_src[(int64_t)s * cap_send + ts] = (int32_t)(n - (int64_t)s * T);
         }
+        int4 xs[kPPUnroll];
+        const bool have = staged_x(it, stage, x0, stg, xs);
         move_token_segment<kPPUnroll, kPPBatch>(x + n * V, send + (int64_t)s * cap_send * V, recv, V,
                                                 g * kPPSegVec + lane, ts, pr, pp, P, cap_send,
-                                                bad_slot, cap_flag, g == 0);
+                                                bad_slot, cap_flag, g == 0, have ? xs : nullptr);
     }
     for (int64_t i = gtid; i < (int64_t)S * cap_send; i += gthreads) {
         const int s = (int)(i / cap_send);
@@ -506,6 +537,40 @@ int pack_permute_kernel_count(int S, int T, int E)
     return permute_map_fused(S, E) ? 1 : 3;  // else pack, map and copy
 }
 
+namespace {
+
+// Staged tasks per warp for a one-pass kernel whose own shared memory is
+// `base` bytes: as many (at most kPPStageMax) as fit beside the CTAs that its
+// registers allow per SM, none unless `want`.  Sets the kernel's dynamic
+// shared memory limit when it stages.  resident: CTAs of the kernel that fit
+// on the device with `base` bytes (the grid's cap either way).
+template <typename Kern>
+cudaError_t pick_stage(Kern kernel, size_t base, bool want, const DeviceInfo &di, int *stage,
+                       size_t *smem, int *resident)
+{
+    *stage = 0;
+    *smem = base;
+    *resident = resident_grid((const void *)kernel, kPPThreads, base);
+    if (!want || *resident <= 0) return cudaSuccess;
+    // the opt-in limit covers static shared memory too (48 bytes here)
+    const size_t max_dyn = (size_t)di.max_smem_optin - 1024;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn);
+    if (e != cudaSuccess) return e;
+    const size_t base16 = (base + 15) / 16 * 16;
+    for (int m = kPPStageMax; m >= 1; m--) {
+        const size_t sm = base16 + (size_t)m * kPPStageBytes;
+        if (sm <= max_dyn && resident_grid((const void *)kernel, kPPThreads, sm) >= *resident) {
+            *stage = m;
+            *smem = sm;
+            break;
+        }
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
                                 const int32_t *part_offsets, const int32_t *topk_ids,
                                 const int32_t *expert_counts, const int32_t *expert_rank, int S,
@@ -533,33 +598,18 @@ cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
     const int L = E / P;
     const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
     const size_t base = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
+    // Staged x segments, for one source only (measured on GB300, step through
+    // moe_dispatch: 4,096-token prefill 139.8 -> 134.4 us with three tasks per
+    // warp, 136.1 with two; four took 48 KB more shared memory per CTA and made
+    // the 16,384-token step 12 us slower, the combine that follows it under
+    // programmatic launch landing on SMs left with little L1; eight sources of
+    // 4,096 tokens were 3.6 us slower with three tasks, so several sources
+    // stage nothing).
+    int stage = 0, resident = 0;
     size_t smem = base;
-    int resident = resident_grid((const void *)k_pack_permute, kPPThreads, base);
-    // Staged x segments, for one source only: as many tasks per warp (at most
-    // kPPStageMax) as fit in the shared memory left beside the CTAs that the
-    // registers allow per SM.  (Measured on GB300, step through moe_dispatch:
-    // 4,096-token prefill 139.8 -> 134.4 us with three tasks, 136.1 with two;
-    // four took 48 KB more shared memory per CTA and made the 16,384-token step
-    // 12 us slower, the combine that follows it under programmatic launch
-    // landing on SMs left with little L1; eight sources of 4,096 tokens were
-    // 3.6 us slower with three tasks, so several sources stage nothing.)
-    int stage = 0;
-    if (x_before_wait && S == 1 && resident > 0) {
-        // the opt-in limit covers static shared memory too (48 bytes here)
-        const size_t max_dyn = (size_t)di.max_smem_optin - 1024;
-        e = cudaFuncSetAttribute(k_pack_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)max_dyn);
-        if (e != cudaSuccess) return e;
-        const size_t base16 = (base + 15) / 16 * 16;
-        for (int m = kPPStageMax; m >= 1 && stage == 0; m--) {
-            const size_t sm = base16 + (size_t)m * kPPStageBytes;
-            if (sm > max_dyn) continue;
-            if (resident_grid((const void *)k_pack_permute, kPPThreads, sm) >= resident) {
-                stage = m;
-                smem = sm;
-            }
-        }
-    }
+    if ((e = pick_stage(k_pack_permute, base, x_before_wait && S == 1, di, &stage, &smem,
+                        &resident)) != cudaSuccess)
+        return e;
     const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
     const int64_t warps = NT * nseg + (align > 1 ? (int64_t)E * (align - 1) * nseg : 0);
     int64_t blocks = div_up(warps, kPPThreads / 32);
@@ -642,7 +692,7 @@ cudaError_t launch_pack_permute_masked(const uint16_t *x, const int32_t *token_s
                                        int block_rows, int cap_send, uint16_t *send,
                                        int32_t *send_src, uint16_t *recv, int32_t *masked_counts,
                                        int32_t *pair_row, int32_t *recv_pair,
-                                       uint32_t *dev_status, cudaStream_t st)
+                                       uint32_t *dev_status, cudaStream_t st, bool x_before_wait)
 {
     cudaError_t e;
     const int L = E / P;
@@ -661,8 +711,13 @@ cudaError_t launch_pack_permute_masked(const uint16_t *x, const int32_t *token_s
     const int64_t NT = (int64_t)S * T;
     const int V = H / 8;
     const int nseg = (V + kPPSegVec - 1) / kPPSegVec;
-    const size_t smem = (size_t)(2 + S) * nb * sizeof(int);
-    const int resident = resident_grid((const void *)k_pack_permute_masked, kPPThreads, smem);
+    const size_t base = (size_t)(2 + S) * nb * sizeof(int);
+    // staged x segments as in k_pack_permute: one source, x read before the wait
+    int stage = 0, resident = 0;
+    size_t smem = base;
+    if ((e = pick_stage(k_pack_permute_masked, base, x_before_wait && S == 1, di, &stage, &smem,
+                        &resident)) != cudaSuccess)
+        return e;
     const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
     int64_t blocks = div_up(NT * nseg, kPPThreads / 32);
     const int64_t rows = (int64_t)nb * block_rows;
@@ -678,7 +733,7 @@ cudaError_t launch_pack_permute_masked(const uint16_t *x, const int32_t *token_s
                                      part_offsets, topk_ids, expert_counts, expert_rank, S, NT, k,
                                      E, L, P, T, V, e0, nb, block_rows, cap_send, (int4 *)send,
                                      send_src, (int4 *)recv, masked_counts, pair_row, recv_pair,
-                                     dev_status));
+                                     dev_status, x_before_wait, stage));
     return e;
 }
 
@@ -722,7 +777,7 @@ cudaError_t launch_dispatch_masked(const float *logits, const uint16_t *x, int S
     return launch_pack_permute_masked(x, token_slot, part_offsets, topk_ids, expert_counts,
                                       expert_rank, S, T, k, E, P, H, recv_part, block_rows,
                                       cap_send, send, send_src, recv, masked_counts, pair_row,
-                                      recv_pair, dev_status, st);
+                                      recv_pair, dev_status, st, true);
 }
 
 cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n)

@@ -174,7 +174,8 @@ cudaError_t launch_pack_permute(const uint16_t *x, const int32_t *token_slot,
                                 int32_t *recv_pair, void *ws, uint32_t *dev_status,
                                 cudaStream_t st, bool x_before_wait);
 
-// Pack and the masked receive layout in one pass; the kernels it enqueues.
+// Pack and the masked receive layout in one pass (x_before_wait as for
+// launch_pack_permute); the kernels it enqueues.
 int pack_permute_masked_kernel_count(int S, int T, int E, int P, int recv_part);
 cudaError_t launch_pack_permute_masked(const uint16_t *x, const int32_t *token_slot,
                                        const int32_t *part_offsets, const int32_t *topk_ids,
@@ -183,7 +184,7 @@ cudaError_t launch_pack_permute_masked(const uint16_t *x, const int32_t *token_s
                                        int block_rows, int cap_send, uint16_t *send,
                                        int32_t *send_src, uint16_t *recv, int32_t *masked_counts,
                                        int32_t *pair_row, int32_t *recv_pair,
-                                       uint32_t *dev_status, cudaStream_t st);
+                                       uint32_t *dev_status, cudaStream_t st, bool x_before_wait);
 
 // The dispatch side with quantized rows (format 1: MXFP8 records, 2: NVFP4).
 cudaError_t dispatch_quantized_kernel_count(int S, int T, int k, int E, int P, int *n);
