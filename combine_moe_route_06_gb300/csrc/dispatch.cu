@@ -59,13 +59,28 @@ __device__ __forceinline__ void cp_async_wait_all()
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+static_assert(kPPSegVec == kQSegVec, "bf16 and record segments cover the same x vectors");
+
+// x vector of this lane's u-th 16-byte piece of the segment starting at vb:
+// bf16 rows (FMT 0) take vectors lane + 32 u, record pieces their
+// quantizer's order (piece_vec).
+template <int FMT>
+__device__ __forceinline__ int seg_piece(int vb, int u)
+{
+    if constexpr (FMT == 0) return vb + (threadIdx.x & 31) + 32 * u;
+    else return piece_vec<FMT>(vb, u);
+}
+
 // The early x reads of the one-pass kernels (tasks last to first, task rt of
-// warp w = rt0 + j * gwarps at its j-th iteration).  Loads the segment of the
-// warp's first task into x0 and copies those of its next `stage` tasks into
-// stg ([stage][kPPUnroll][32 lanes] int4, this warp's slots).  Each lane copies
-// the 16-byte pieces it will store itself, so no barrier orders the copies
-// with their use, only cp_async_wait_all.  Every lane must call (the copy
-// group is committed even when empty).
+// warp w = rt0 + j * gwarps at its j-th iteration).  With REG0 the segment of
+// the warp's first task goes to registers (x0) and those of its next `stage`
+// tasks to shared memory; without, its first `stage` tasks' segments go to
+// shared memory and x0 stays unused.  stg: this warp's slots, [slot][kPPUnroll]
+// [32 lanes] int4, each lane's pieces in seg_piece<FMT> order.  Each lane
+// copies the 16-byte pieces it will use itself, so no barrier orders the
+// copies with their use, only cp_async_wait_all.  Every lane must call (the
+// copy group is committed even when empty).
+template <int FMT, bool REG0>
 __device__ __forceinline__ void stage_x(const int4 *__restrict__ x, int64_t ntask, int nseg, int V,
                                         int64_t rt0, int64_t gwarps, int stage,
                                         int4 (&x0)[kPPUnroll], int4 *stg)
@@ -73,35 +88,39 @@ __device__ __forceinline__ void stage_x(const int4 *__restrict__ x, int64_t ntas
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int u = 0; u < kPPUnroll; u++) x0[u] = make_int4(0, 0, 0, 0);
-    for (int j = 0; j <= stage; j++) {
+    const int last = REG0 ? stage : stage - 1;
+    for (int j = 0; j <= last; j++) {
         const int64_t rt = rt0 + (int64_t)j * gwarps;
         if (rt >= ntask) break;
         const int64_t t = ntask - 1 - rt;
         const int64_t n = t / nseg;
         const int g = (int)(t - n * nseg);
+        const int slot = REG0 ? j - 1 : j;
 #pragma unroll
         for (int u = 0; u < kPPUnroll; u++) {
-            const int vi = g * kPPSegVec + lane + 32 * u;
+            const int vi = seg_piece<FMT>(g * kPPSegVec, u);
             if (vi >= V) continue;
-            if (j == 0) x0[u] = ld_stream(x + n * V + vi);
-            else cp_async16(stg + ((j - 1) * kPPUnroll + u) * 32 + lane, x + n * V + vi);
+            if (REG0 && j == 0) x0[u] = ld_stream(x + n * V + vi);
+            else cp_async16(stg + (slot * kPPUnroll + u) * 32 + lane, x + n * V + vi);
         }
     }
     cp_async_commit();
 }
 
-// The x segment of the warp's it-th task if stage_x fetched it (into xs):
-// x0 for the first task, the staged copy for tasks 1..stage.  Call after
-// cp_async_wait_all.
+// The x segment of the warp's it-th task if stage_x fetched it (into xs, and
+// true), else false.  Call after cp_async_wait_all.
+template <bool REG0>
 __device__ __forceinline__ bool staged_x(int it, int stage, const int4 (&x0)[kPPUnroll],
                                          const int4 *stg, int4 (&xs)[kPPUnroll])
 {
     const int lane = threadIdx.x & 31;
-    const bool have = it <= stage;
+    const int slot = REG0 ? it - 1 : it;
+    const bool have = REG0 ? it <= stage : it < stage;
 #pragma unroll
     for (int u = 0; u < kPPUnroll; u++)
-        xs[u] = it == 0 ? x0[u]
-                        : (have ? stg[((it - 1) * kPPUnroll + u) * 32 + lane] : make_int4(0, 0, 0, 0));
+        xs[u] = (REG0 && it == 0) ? x0[u]
+                                  : (have ? stg[(slot * kPPUnroll + u) * 32 + lane]
+                                          : make_int4(0, 0, 0, 0));
     return have;
 }
 
@@ -219,7 +238,7 @@ __global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute(
     // that while the layout finishes HBM reads x instead of idling and the row
     // phase that follows is left almost only writes.
     int4 x0[kPPUnroll];
-    stage_x(x, NT * nseg, nseg, V, rt0, gwarps, stage, x0, stg);
+    stage_x<0, true>(x, NT * nseg, nseg, V, rt0, gwarps, stage, x0, stg);
     if (x_before_wait) pdl_wait();
     pdl_trigger();
     bool cap_flag = false, bad_slot = false, dropped = false, bad_rank = false, bad_id = false;
@@ -266,7 +285,7 @@ __global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute(
         // x0 (task 0) and the staged segments pass through one register
         // array, so the row task sees one array or none
         int4 xs[kPPUnroll];
-        const bool have = staged_x(it, stage, x0, stg, xs);
+        const bool have = staged_x<true>(it, stage, x0, stg, xs);
         move_token_segment<kPPUnroll, kPPBatch>(x + n * V, send + (int64_t)s * cap_send * V, recv, V,
                                       g * kPPSegVec + lane, ts_c, pr, pp, P, cap_send, bad_slot,
                                       cap_flag, g == 0, have ? xs : nullptr);
@@ -338,7 +357,7 @@ __global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute_masked(
     if (!x_before_wait) pdl_wait();
     const int64_t rt0 = gtid >> 5;
     int4 x0[kPPUnroll];
-    stage_x(x, NT * nseg, nseg, V, rt0, gwarps, stage, x0, stg);
+    stage_x<0, true>(x, NT * nseg, nseg, V, rt0, gwarps, stage, x0, stg);
     if (x_before_wait) pdl_wait();
     pdl_trigger();
     for (int bb = threadIdx.x; bb < nb; bb += blockDim.x) {
@@ -392,7 +411,7 @@ __global__ void __launch_bounds__(kPPThreads, 3) k_pack_permute_masked(
             else if (ts >= 0) send_src[(int64_t)s * cap_send + ts] = (int32_t)(n - (int64_t)s * T);
         }
         int4 xs[kPPUnroll];
-        const bool have = staged_x(it, stage, x0, stg, xs);
+        const bool have = staged_x<true>(it, stage, x0, stg, xs);
         move_token_segment<kPPUnroll, kPPBatch>(x + n * V, send + (int64_t)s * cap_send * V, recv, V,
                                                 g * kPPSegVec + lane, ts, pr, pp, P, cap_send,
                                                 bad_slot, cap_flag, g == 0, have ? xs : nullptr);
@@ -425,11 +444,10 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_q(
     int64_t NT, int k, int E, int L, int P, int T, int V, int recv_part, int align, int cap_send,
     int cap_recv, float g, uint8_t *__restrict__ send_q, int32_t *__restrict__ send_src,
     uint8_t *__restrict__ recv_q, int32_t *__restrict__ expert_offsets,
-    int32_t *__restrict__ pair_row, int32_t *__restrict__ recv_pair, uint32_t *dev_status)
+    int32_t *__restrict__ pair_row, int32_t *__restrict__ recv_pair, uint32_t *dev_status,
+    int stage)
 {
     using QL = QLayout<FMT>;
-    pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t gwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -443,10 +461,22 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_q(
     int *off = smq;              // [E + 1]
     int *cnt = off + E + 1;      // [E]
     int *sb = cnt + E;           // [S][E]
+    // [warp][stage][4 pieces][32 lanes]: x segments of this warp's tasks 0..stage-1
+    int4 *stg = reinterpret_cast<int4 *>(smq + ((2 * E + 1 + S * E + 3) & ~3)) +
+                (threadIdx.x >> 5) * stage * kPPSegVec;
+    // Only moe_dispatch_quantized launches this kernel, right after the layout:
+    // x is read before the grid-dependency wait as in k_pack_permute.
+    const int64_t rt0 = gtid >> 5;
+    int4 x0[kPPUnroll];
+    stage_x<FMT, false>(x, NT * nseg, nseg, V, rt0, gwarps, stage, x0, stg);
+    pdl_wait();
+    pdl_trigger();
     build_run_starts(expert_counts, S, E, L, recv_part, align, off, cnt, sb, expert_offsets);
+    cp_async_wait_all();
 
     const int64_t ntask = NT * nseg;
-    for (int64_t rtask = gtid >> 5; rtask < ntask; rtask += gwarps) {
+    int it = 0;
+    for (int64_t rtask = rt0; rtask < ntask; rtask += gwarps, it++) {
         const int64_t task = ntask - 1 - rtask;       // tokens last to first
         const int64_t n = task / nseg;
         const int gs = (int)(task - n * nseg);
@@ -470,7 +500,15 @@ __global__ void __launch_bounds__(kPPThreads) k_pack_permute_q(
         }
         // quantize the segment once (every lane takes part in the block shuffles)
         const int vb = gs * kQSegVec;
-        const QPiece q = quantize_piece<FMT>(x + n * V, V, vb, g, d);
+        int4 xs[kPPUnroll];
+        if (!staged_x<false>(it, stage, x0, stg, xs)) {
+#pragma unroll
+            for (int u = 0; u < kPPUnroll; u++) {
+                const int vi = piece_vec<FMT>(vb, u);
+                xs[u] = (vi < V) ? ld_stream(x + n * V + vi) : make_int4(0, 0, 0, 0);
+            }
+        }
+        const QPiece q = quantize_loaded<FMT>(xs, g, d);
         uint8_t *send_s = send_q + (int64_t)s * cap_send * rb;
         unsigned smask = __ballot_sync(kFull, lane < P && ts >= 0 && ts < cap_send);
         while (smask) {
@@ -539,11 +577,18 @@ int pack_permute_kernel_count(int S, int T, int E)
 
 namespace {
 
+// Shared memory per SM the staged kernels may take together (bytes, with the
+// 1 KiB each CTA reserves): the SM's remaining 256 KiB - 164 KiB stay L1 for
+// the kernel that follows under programmatic launch (the combine reads its
+// pair rows and weights through L1; 64 KiB staged per CTA, 212 KiB per SM,
+// made the 16,384-token step 12 us slower).
+constexpr size_t kStageSmemPerSm = (size_t)164 * 1024;
+
 // Staged tasks per warp for a one-pass kernel whose own shared memory is
 // `base` bytes: as many (at most kPPStageMax) as fit beside the CTAs that its
-// registers allow per SM, none unless `want`.  Sets the kernel's dynamic
-// shared memory limit when it stages.  resident: CTAs of the kernel that fit
-// on the device with `base` bytes (the grid's cap either way).
+// registers allow per SM within kStageSmemPerSm, none unless `want`.  Sets the
+// kernel's dynamic shared memory limit when it stages.  resident: CTAs of the
+// kernel that fit on the device with `base` bytes (the grid's cap either way).
 template <typename Kern>
 cudaError_t pick_stage(Kern kernel, size_t base, bool want, const DeviceInfo &di, int *stage,
                        size_t *smem, int *resident)
@@ -552,6 +597,7 @@ cudaError_t pick_stage(Kern kernel, size_t base, bool want, const DeviceInfo &di
     *smem = base;
     *resident = resident_grid((const void *)kernel, kPPThreads, base);
     if (!want || *resident <= 0) return cudaSuccess;
+    const int per_sm = (*resident + di.sm_count - 1) / di.sm_count;
     // the opt-in limit covers static shared memory too (48 bytes here)
     const size_t max_dyn = (size_t)di.max_smem_optin - 1024;
     const cudaError_t e =
@@ -560,6 +606,7 @@ cudaError_t pick_stage(Kern kernel, size_t base, bool want, const DeviceInfo &di
     const size_t base16 = (base + 15) / 16 * 16;
     for (int m = kPPStageMax; m >= 1; m--) {
         const size_t sm = base16 + (size_t)m * kPPStageBytes;
+        if ((size_t)per_sm * (sm + 1024) > kStageSmemPerSm) continue;
         if (sm <= max_dyn && resident_grid((const void *)kernel, kPPThreads, sm) >= *resident) {
             *stage = m;
             *smem = sm;
@@ -845,10 +892,15 @@ cudaError_t launch_dispatch_quantized(const float *logits, const uint16_t *x, in
     if ((e = device_info(&di)) != cudaSuccess) return e;
     const int L = E / P;
     const int nseg = (V + kQSegVec - 1) / kQSegVec;
-    const size_t smem = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
-    const void *fn = format == kQFmtMxfp8 ? (const void *)k_pack_permute_q<kQFmtMxfp8>
-                                          : (const void *)k_pack_permute_q<kQFmtNvfp4>;
-    const int resident = resident_grid(fn, kPPThreads, smem);
+    const size_t base = (size_t)(2 * E + 1 + (int64_t)S * E) * sizeof(int);
+    // staged x segments as in k_pack_permute (one source)
+    int stage = 0, resident = 0;
+    size_t smem = base;
+    e = format == kQFmtMxfp8 ? pick_stage(k_pack_permute_q<kQFmtMxfp8>, base, S == 1, di, &stage,
+                                          &smem, &resident)
+                             : pick_stage(k_pack_permute_q<kQFmtNvfp4>, base, S == 1, di, &stage,
+                                          &smem, &resident);
+    if (e != cudaSuccess) return e;
     const int64_t wave = resident > 0 ? resident : (int64_t)di.sm_count * (2048 / kPPThreads);
     const int64_t warps = NT * nseg + (align > 1 ? (int64_t)E * (align - 1) : 0);
     int64_t blocks = div_up(warps, kPPThreads / 32);
@@ -867,7 +919,8 @@ cudaError_t launch_dispatch_quantized(const float *logits, const uint16_t *x, in
                                          (const int32_t *)expert_counts,
                                          (const int32_t *)expert_rank, S, NT, k, E, L, P, T, V,
                                          recv_part, align, cap_send, cap_recv, g, send_q, send_src,
-                                         recv_q, expert_offsets, pair_row, recv_pair, dev_status));
+                                         recv_q, expert_offsets, pair_row, recv_pair, dev_status,
+                                         stage));
     } else {
         MOE_TRACED_LAUNCH("k_pack_permute_nvfp4", st,
                           e = launch_pdl(k_pack_permute_q<kQFmtNvfp4>, dim3((unsigned)blocks),
@@ -876,7 +929,8 @@ cudaError_t launch_dispatch_quantized(const float *logits, const uint16_t *x, in
                                          (const int32_t *)expert_counts,
                                          (const int32_t *)expert_rank, S, NT, k, E, L, P, T, V,
                                          recv_part, align, cap_send, cap_recv, g, send_q, send_src,
-                                         recv_q, expert_offsets, pair_row, recv_pair, dev_status));
+                                         recv_q, expert_offsets, pair_row, recv_pair, dev_status,
+                                         stage));
     }
     return e;
 }

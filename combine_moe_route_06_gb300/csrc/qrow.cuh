@@ -56,11 +56,20 @@ template <> struct QLayout<kQFmtNvfp4> {
     static constexpr int kScaleLanes = 16;
 };
 
-// Quantizes the segment starting at vector vb of the token's row (every lane
-// of the warp must call).
+// x vector of this lane's i-th 16-byte piece (i < 4) of the segment that
+// starts at vector vb: MXFP8 lanes take two adjacent vectors in each half of
+// the segment, NVFP4 lanes four adjacent vectors.
 template <int FMT>
-__device__ __forceinline__ QPiece quantize_piece(const int4 *__restrict__ row, int V, int vb,
-                                                 float g, float d)
+__device__ __forceinline__ int piece_vec(int vb, int i)
+{
+    const int lane = threadIdx.x & 31;
+    return FMT == kQFmtMxfp8 ? vb + 64 * (i >> 1) + 2 * lane + (i & 1) : vb + 4 * lane + i;
+}
+
+// Quantizes this lane's four pieces v (piece_vec order; zero past the row) of
+// a segment (every lane of the warp must call).
+template <int FMT>
+__device__ __forceinline__ QPiece quantize_loaded(const int4 (&v)[4], float g, float d)
 {
     const int lane = threadIdx.x & 31;
     QPiece q;
@@ -68,15 +77,7 @@ __device__ __forceinline__ QPiece quantize_piece(const int4 *__restrict__ row, i
     if (FMT == kQFmtMxfp8) {
         uint32_t sc[2];
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
-            const int vi = vb + 64 * u + 2 * lane;
-            int4 v[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
-            if (vi < V) {
-                v[0] = ld_stream(row + vi);
-                v[1] = ld_stream(row + vi + 1);
-            }
-            mxfp8_quantize16(v, q.code[u], sc[u]);
-        }
+        for (int u = 0; u < 2; u++) mxfp8_quantize16(v + 2 * u, q.code[u], sc[u]);
         const int w = lane & 3;
         uint32_t a = 0u, b = 0u;
 #pragma unroll
@@ -86,10 +87,6 @@ __device__ __forceinline__ QPiece quantize_piece(const int4 *__restrict__ row, i
         }
         q.sw = (lane < 4) ? a : b;
     } else {
-        const int vi = vb + 4 * lane;
-        int4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) v[i] = (vi < V) ? ld_stream(row + vi + i) : make_int4(0, 0, 0, 0);
         uint32_t sp;
         nvfp4_quantize32(v, g, d, q.code[0], sp);
         q.code[1] = make_uint4(0u, 0u, 0u, 0u);
@@ -97,6 +94,21 @@ __device__ __forceinline__ QPiece quantize_piece(const int4 *__restrict__ row, i
         q.sw = __shfl_sync(kFull, sp, 2 * j) | (__shfl_sync(kFull, sp, 2 * j + 1) << 16);
     }
     return q;
+}
+
+// Quantizes the segment starting at vector vb of the token's row (every lane
+// of the warp must call).
+template <int FMT>
+__device__ __forceinline__ QPiece quantize_piece(const int4 *__restrict__ row, int V, int vb,
+                                                 float g, float d)
+{
+    int4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int vi = piece_vec<FMT>(vb, i);
+        v[i] = (vi < V) ? ld_stream(row + vi) : make_int4(0, 0, 0, 0);
+    }
+    return quantize_loaded<FMT>(v, g, d);
 }
 
 // Byte offsets of this lane's code vector(s) and scale word in a record, and
