@@ -56,10 +56,10 @@ DOMINANT_BY_VARIANT = {"two_stage": ("k_combine_stage1", "stage1"),
 DOMINANT_TRAFFIC = {("k_perm_copy", "prefill"): {"bytes": 142.5e6 + 252.9e6,
                                                  "sources": ["combine_moe_route_06_gb300/csrc/permute.cu"],
                                                  "sha16": "63c0e1b6e21e91ff"},
-                    ("k_pack_permute", "prefill"): {"bytes": 43.53e6 + 430.21e6,
+                    ("k_pack_permute", "prefill"): {"bytes": 43.52e6 + 430.24e6,
                                                     "sources": ["combine_moe_route_06_gb300/csrc/dispatch.cu",
                                                                 "combine_moe_route_06_gb300/csrc/row_move.cuh"],
-                                                    "sha16": "65e063f309e922ca"}}
+                                                    "sha16": "49a45874c40ef65a"}}
 
 
 def source_code_sha16(*paths: str) -> str:
