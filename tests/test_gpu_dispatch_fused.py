@@ -284,6 +284,9 @@ def _q_oracle(quant, w_, inp, g=1.0, recv_part=-1, align=1):
 @pytest.mark.parametrize("name,over,recv_part,align", [
     ("decode", {}, -1, 1), ("prefill", {}, -1, 1), ("large", {}, -1, 1),
     ("tiny", {"S": 2, "T": 300, "H": 512, "E": 64, "k": 8, "P": 8}, 2, 8),
+    # one source past the one-launch form: x staged before the wait, a ragged
+    # last segment (192 vectors = 128 + 64)
+    ("tiny", {"T": 700, "H": 1536, "E": 64, "k": 8, "P": 8}, -1, 1),
     # one launch: one token, the largest batch, ragged segments with run alignment
     ("decode", {"T": 1}, 4, 1), ("decode", {"T": 256}, -1, 1),
     ("tiny", {"T": 200, "H": 1536, "E": 64, "k": 8, "P": 8}, 2, 8)])
