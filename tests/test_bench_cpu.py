@@ -27,3 +27,15 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_dominant_kernel_traffic_record_matches_its_sources():
+    """The DRAM traffic bench.py reports for the prefill step's dominant kernel
+    was captured on the sources as they are now (a change to them without a
+    new capture turns the record off, and this test red)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = bench.DOMINANT_TRAFFIC[("k_pack_permute", "prefill")]
+    assert bench.dominant_traffic("k_pack_permute", "prefill") == rec["bytes"]
+    # the capture sits a little below the kernel's HBM bytes (x partly in L2)
+    assert 0.95 * 479.4e6 < rec["bytes"] <= 479.4e6
